@@ -1,0 +1,309 @@
+/*
+ * spec_verify.h — C ABI of the exact greedy speculative verify step on one GB300.
+ *
+ * What the step computes.  The target model runs ONE batched forward over
+ * M = k+1 rows: row 0 is the carried frontier token, rows 1..k are the draft
+ * proposals.  Each row's argmax is the target's own next-token choice; the
+ * draft is accepted up to the first disagreement, the disagreeing position's
+ * target token becomes the next carried frontier, and the KV rows of the
+ * rejected suffix are rolled back.
+ *   - batched verify of k+1 rows per weight read: Muser book Ch. 33
+ *     ("Speculation: the local win and the distributed verdict") §33.1 and
+ *     Ch. 8 ("The DFlash draft") §8.1;
+ *   - the accept rule: Ch. 33 §33.2 (verify_full_speculative_mt_ordered);
+ *     greedy acceptance is its one-hot (temperature 0) special case, see
+ *     spec_accept below;
+ *   - the carried frontier: Ch. 33 §33.7 (carried-frontier state machine);
+ *   - verify lengths {3, 7, 15} and the 16-row block: Ch. 8 §8.6 item 3;
+ *   - metadata-only KV rewind: Ch. 8 §8.6 item 4 (MetalSpeculativeCheckpoint);
+ *   - k-quant weights consumed directly by the GPU: Ch. 8 §8.5;
+ *   - integer-exact dot products as the anchor: Ch. 32 ("Precision across the
+ *     handoff") §32.4 and §32.7;
+ *   - batch-height-invariant arithmetic: "The Two-Fifteen That Wasn't"
+ *     (sanctum.run), section "The stream that was load-bearing".
+ *
+ * Conventions for every entry point.
+ *   - Device pointers are CUDA global-memory pointers of the current device;
+ *     host pointers are plain process memory.  Nothing here takes ownership of
+ *     a caller pointer: the caller allocates and frees every input, output,
+ *     weight and KV buffer.  The library allocates only the workspace owned by
+ *     a spec_ctx, once, in spec_verify_init, and frees it in
+ *     spec_verify_destroy.  No entry point allocates after init.
+ *   - Work is enqueued on the ctx's stream and is asynchronous unless stated.
+ *     Host-side validation happens before anything is enqueued; a negative
+ *     return code means nothing was enqueued.
+ *   - Device-detected conditions (token out of range, non-finite value, page
+ *     pool exhausted, bad rollback length) are OR-ed into a device status word
+ *     (spec_result.status, or the ctx status word read by spec_last_status)
+ *     and never trap the GPU.
+ *   - All matrices are row-major.  "Q4_K" below means the superblock format
+ *     defined next.
+ *
+ * Q4_K superblock (144 bytes, 256 weights).  A weight matrix W of N output
+ * columns and K inputs (K a multiple of 256) is stored, in the CANONICAL
+ * layout, as N x (K/256) superblocks, column n's superblock b at byte offset
+ * (n*(K/256) + b)*144.  Superblock b of column n holds W[n][256b .. 256b+255]:
+ *   bytes 0..1   d    (IEEE binary16, little endian)
+ *   bytes 2..3   dmin (IEEE binary16, little endian)
+ *   bytes 4..15  a 96-bit little-endian field F: sub-scale sc_j = bits
+ *                [6j, 6j+6) of F and sub-min m_j = bits [48+6j, 48+6j+6),
+ *                j = 0..7 (6-bit unsigned each)
+ *   bytes 16..143  4-bit codes: element e (0..255), j = e/32, r = e%32, lives
+ *                in byte 16 + 16j + (r%16), low nibble if r < 16, else high.
+ * Dequantised weight: w_e = d * sc_j * q_e - dmin * m_j, q_e in 0..15.
+ * The TILED layout produced by spec_weights_repack holds the same bytes
+ * permuted for the tensor-core fragments; every GEMM entry point here takes
+ * the TILED layout.  Its size is identical (N*(K/256)*144 bytes).
+ *
+ * Activation quantisation (per row, per 256-block b): d_a = amax/127 (IEEE
+ * fp32 division), q = clamp(rint(x/d_a), -127, 127) with round-half-even,
+ * d_a = 0 and q = 0 for an all-zero block.  Sub-block sums A_j = sum of the 32
+ * q's of sub-block j.
+ * Integer sums per (row m, column n, superblock b):
+ *   S_j = sum_{i<32} q_w[32j+i] * q_a[256b+32j+i]            (exact)
+ *   ISc = sum_j sc_j * S_j,  IMn = sum_j m_j * A_j            (exact, int32)
+ * Per-superblock value, fp32, each operation rounded to nearest, no fusion:
+ *   v_b = d_a * ((float)d * (float)ISc - (float)dmin * (float)IMn)
+ * Output y[m][n] = sum_b v_b (fp32 accumulation; the summation order is the
+ * kernel's own fixed order and depends on K and N only, never on M).
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stdint.h>
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- host return codes (0 = OK, negative = nothing was enqueued) -------- */
+#define SPEC_OK              0
+#define SPEC_EINVAL         -1  /* geometry or argument out of range            */
+#define SPEC_EVERIFYLEN     -2  /* k not in {3, 7, 15} (Ch. 8 §8.6 item 3)       */
+#define SPEC_ENULL          -3  /* a required pointer is NULL                    */
+#define SPEC_EALIGN         -4  /* a pointer is not 16-byte aligned              */
+#define SPEC_ENOMEM         -5  /* workspace allocation failed (init only)       */
+#define SPEC_ECAPACITY      -6  /* request exceeds the ctx / KV capacity         */
+#define SPEC_ECUDA          -7  /* a CUDA runtime call failed                    */
+#define SPEC_ENODEV         -8  /* no sm_103 device current                      */
+
+/* ---- device status bits (OR-ed; 0 = OK) ------------------------------ */
+#define SPEC_ST_TOKEN_RANGE   0x1  /* a draft token is < 0 or >= vocab           */
+#define SPEC_ST_NONFINITE     0x2  /* NaN/Inf in an activation or a logit       */
+#define SPEC_ST_POOL_EMPTY    0x4  /* not enough free KV pages for the block     */
+#define SPEC_ST_ROLLBACK      0x8  /* rollback length < 0 or > seq_len           */
+#define SPEC_ST_CTX_FULL      0x10 /* seq_len + rows exceeds the page table      */
+
+/* Model geometry and workspace sizing.  H = n_q_heads*head_dim; H and ffn are
+ * multiples of 256; n_q_heads is a multiple of n_kv_heads; head_dim = 128;
+ * page_size = 16; max_rows <= 16 (k_max + 1).  max_ctx bounds the attention
+ * workspace (positions per sequence). */
+typedef struct spec_config {
+    int32_t hidden;       /* H, e.g. 6656                                   */
+    int32_t n_layers;     /* e.g. 52                                        */
+    int32_t n_q_heads;    /* e.g. 52                                        */
+    int32_t n_kv_heads;   /* e.g. 4  (query head h uses kv head h/(nq/nkv)) */
+    int32_t head_dim;     /* 128                                            */
+    int32_t ffn;          /* F, e.g. 17920                                  */
+    int32_t vocab;        /* V, e.g. 131072 (multiple of 16)                */
+    int32_t max_rows;     /* maximum k+1 per step, <= 16                    */
+    int32_t page_size;    /* 16                                             */
+    int32_t max_ctx;      /* maximum sequence length in positions           */
+    float   rms_eps;      /* RMSNorm epsilon, e.g. 1e-6                     */
+} spec_config;
+
+/* Target weights.  Each `const void* const*` is a HOST array of n_layers
+ * DEVICE pointers to TILED Q4_K matrices:
+ *   w_qkv[l]     N = (n_q_heads + 2*n_kv_heads)*head_dim, K = H; output
+ *                columns [0, nq*dh) are Q (head-major), then K, then V.
+ *   w_o[l]       N = H, K = H
+ *   w_gate_up[l] N = 2F, K = H; columns [0, F) gate, [F, 2F) up.
+ *   w_down[l]    N = H, K = F
+ *   w_head       N = V, K = H
+ * Norm gains are device fp32 vectors of length H; a NULL entry means all ones
+ * (norm vectors stay f32: Ch. 8 §8.5). */
+typedef struct spec_weights {
+    const void* const* w_qkv;
+    const void* const* w_o;
+    const void* const* w_gate_up;
+    const void* const* w_down;
+    const float* const* attn_norm;  /* host array of device pointers, or NULL */
+    const float* const* ffn_norm;   /* host array of device pointers, or NULL */
+    const float* final_norm;        /* device pointer or NULL                 */
+    const void* w_head;
+} spec_weights;
+
+/* Paged KV cache (all pointers DEVICE, caller-owned).
+ *   pool        bf16 [num_pages][n_layers][2 (K,V)][n_kv_heads][page_size][head_dim]
+ *   page_table  int32 [max_seq_pages]: logical page p (positions 16p..16p+15)
+ *               -> physical page id, -1 when unmapped
+ *   seq_len     int32 [1]: committed positions
+ *   free_stack  int32 [num_pages] LIFO of free physical page ids
+ *   free_top    int32 [1]: number of ids on free_stack
+ * Committed state = (seq_len, page_table[0 .. ceil(seq_len/16)), free stack).
+ * Bytes of positions >= seq_len are stale and carry no meaning. */
+typedef struct spec_kv {
+    void*    pool;
+    int32_t  num_pages;
+    int32_t  max_seq_pages;
+    int32_t* page_table;
+    int32_t* seq_len;
+    int32_t* free_stack;
+    int32_t* free_top;
+} spec_kv;
+
+/* Step result, DEVICE memory written by the accept kernel at the end of the
+ * step (Ch. 33 §33.2, SpeculativeDecision{accepted, next_token}). */
+typedef struct spec_result {
+    int32_t accepted_len;  /* L in [0, k]                                    */
+    int32_t next_token;    /* argmax of row L: the new carried frontier      */
+    int32_t status;        /* SPEC_ST_* bits; 0 = OK                         */
+    int32_t seq_len;       /* committed KV length after the rollback         */
+} spec_result;
+
+/* Optional debug outputs of a step (all DEVICE, each may be NULL). */
+typedef struct spec_taps {
+    float*   resid;        /* fp32 [n_layers+1][rows][H]: residual stream at the
+                              input of each layer, and after the last layer  */
+    int32_t* argmax;       /* int32 [rows]: per-row argmax (lowest index wins) */
+    float*   logits;       /* fp32 [rows][V]                                 */
+} spec_taps;
+
+typedef struct spec_ctx spec_ctx;
+
+/* Create a context on the current device.  Allocates the workspace sized by
+ * cfg and binds `cuda_stream` (a cudaStream_t; NULL = legacy default stream).
+ * Returns SPEC_OK and *out, or a negative code and *out = NULL. */
+int spec_verify_init(const spec_config* cfg, void* cuda_stream, spec_ctx** out);
+
+/* Release the workspace.  Synchronises the ctx stream first.  NULL is a no-op. */
+void spec_verify_destroy(spec_ctx* ctx);
+
+/* Rebind the stream used by subsequent calls. */
+int spec_set_stream(spec_ctx* ctx, void* cuda_stream);
+
+/* Human-readable text for a return code. */
+const char* spec_strerror(int code);
+
+/* One exact greedy verify step (Ch. 33 §33.2 and §33.7; Ch. 8 §8.6).
+ *   hidden  DEVICE fp32 [k+1][H]: residual-stream rows entering layer 0; row 0
+ *           is the carried frontier, row i (1..k) the draft token draft[i-1].
+ *   draft   DEVICE int32 [k]: proposed tokens.
+ *   k       verify length, one of 3, 7, 15 (else SPEC_EVERIFYLEN before any
+ *           GPU work: Ch. 8 §8.6 item 3); k+1 <= cfg.max_rows.
+ *   res     DEVICE spec_result.
+ * Enqueues: KV page reservation for positions seq_len..seq_len+k, the
+ * 52-block batched forward (K/V rows appended as bf16), final norm, LM head
+ * with fused per-row argmax, and one accept/rollback kernel that writes
+ *   L = min{ i < k : draft[i] != argmax(row i) } (else k),
+ *   next_token = argmax(row L),  seq_len := n_past + L + 1
+ * and returns the pages wholly at or beyond the new seq_len to the free stack.
+ * On a device error nothing is committed: seq_len, the page table and the free
+ * stack are restored to their values before the step and res->status != 0.
+ * No host synchronisation and no allocation happen inside. */
+int spec_verify_step(spec_ctx* ctx, const spec_weights* w, spec_kv* kv,
+                     const float* hidden, const int32_t* draft, int k,
+                     spec_result* res);
+
+/* spec_verify_step plus optional debug taps (taps may be NULL). */
+int spec_verify_step_ex(spec_ctx* ctx, const spec_weights* w, spec_kv* kv,
+                        const float* hidden, const int32_t* draft, int k,
+                        spec_result* res, const spec_taps* taps);
+
+/* The same step from HOST buffers: copies hidden [k+1][H] fp32 and draft [k]
+ * int32 from host memory (pinned for overlap) to the ctx workspace, runs the
+ * step, copies the spec_result back to *res_host, and synchronises the
+ * stream before returning. */
+int spec_verify_step_host(spec_ctx* ctx, const spec_weights* w, spec_kv* kv,
+                          const float* hidden_host, const int32_t* draft_host,
+                          int k, spec_result* res_host);
+
+/* Number of kernels the last spec_verify_step enqueued (for accounting). */
+int spec_last_step_launches(const spec_ctx* ctx);
+
+/* ---- KV cache management (Ch. 8 §8.6 item 4: metadata-only rewind) ------- */
+
+/* Reset a KV cache to empty: seq_len = 0, page_table = -1, free_stack filled
+ * descending (id num_pages-1 at the bottom) so that pops yield ids 0, 1, 2...
+ * Requires num_pages <= 2^30. */
+int spec_kv_reset(spec_ctx* ctx, spec_kv* kv);
+
+/* Map pages for positions [seq_len, seq_len + n) and set seq_len += n.  Used to
+ * lay down a prefilled context; the caller writes those rows' bytes.  Device
+ * errors (pool empty, page table full) leave the state unchanged and set the
+ * ctx status word. */
+int spec_kv_extend(spec_ctx* ctx, spec_kv* kv, int32_t n);
+
+/* Roll the committed length back to new_len (0 <= new_len <= seq_len, checked
+ * on the device; violations set SPEC_ST_ROLLBACK in the ctx status word and
+ * change nothing).  Logical pages p with 16p >= new_len are unmapped and their
+ * ids pushed on the free stack from the highest p down, so re-extending maps
+ * the same ids to the same pages again.  Retained rows are untouched. */
+int spec_kv_rollback(spec_ctx* ctx, spec_kv* kv, int32_t new_len);
+
+/* Read (synchronously) and clear the ctx status word set by the entry points
+ * that have no spec_result.  Returns SPEC_ST_* bits, or a negative code. */
+int spec_last_status(spec_ctx* ctx);
+
+/* ---- building blocks, exposed for parity tests and benchmarks ------------ */
+
+/* One-time weight repack: canonical Q4_K (DEVICE, N x K/256 superblocks) ->
+ * TILED Q4_K (DEVICE, same size).  N % 16 == 0, K % 256 == 0.  src and dst
+ * must not overlap.  Deterministic permutation of bytes, no arithmetic. */
+int spec_weights_repack(spec_ctx* ctx, const void* src_canonical, void* dst_tiled,
+                        int N, int K);
+
+/* Activation quantisation of x (DEVICE fp32 [M][K]) exactly as described at
+ * the top of this file, written in plain layout: q int8 [M][K], d_a fp32
+ * [M][K/256], A int32 [M][K/32].  M <= 16, K % 256 == 0.  Non-finite input
+ * sets SPEC_ST_NONFINITE in the ctx status word. */
+int spec_quantize_q8(spec_ctx* ctx, const float* x, int M, int K,
+                     int8_t* q, float* d_a, int32_t* A);
+
+/* y = W x for M rows: quantise x (DEVICE fp32 [M][K]) per 256-block, run the
+ * skinny Q4_K x Q8 tensor-core GEMM on the TILED weights, write y (DEVICE
+ * fp32 [M][N]).  1 <= M <= 16, N % 16 == 0, K % 256 == 0, N*K within the
+ * workspace built for cfg (largest of the model's matrices).  Row i of y is
+ * bit-identical for every M >= i+1. */
+int spec_gemm_q4k(spec_ctx* ctx, const void* w_tiled, int N, int K,
+                  const float* x, int M, float* y);
+
+/* Same GEMM, also writing the exact integer sums ISc and IMn (DEVICE int32
+ * [M][N][K/256] each) of every (row, column, superblock). */
+int spec_gemm_q4k_sums(spec_ctx* ctx, const void* w_tiled, int N, int K,
+                       const float* x, int M, float* y,
+                       int32_t* isc, int32_t* imn);
+
+/* Final RMSNorm (gain final_norm, NULL = ones) + LM head (TILED Q4_K,
+ * N = cfg.vocab, K = cfg.hidden) + per-row argmax, lowest index on ties.
+ * x DEVICE fp32 [M][H]; idx DEVICE int32 [M]; logits DEVICE fp32 [M][V] or
+ * NULL (the fused path writes no logits).  Non-finite logits set
+ * SPEC_ST_NONFINITE in the ctx status word. */
+int spec_lm_head_argmax(spec_ctx* ctx, const void* w_head_tiled,
+                        const float* final_norm, const float* x, int M,
+                        int32_t* idx, float* logits);
+
+/* Verify attention of one layer: M query rows at positions
+ * seq_len-M .. seq_len-1 (their K/V rows already in the cache) against all
+ * positions 0..p_i of row i.  q DEVICE fp32 [M][n_q_heads][head_dim]; out
+ * DEVICE fp32 [M][n_q_heads*head_dim].  s = q.k/sqrt(head_dim), softmax over
+ * the visible positions, o = sum p v; K and V read as bf16. */
+int spec_attention(spec_ctx* ctx, const spec_kv* kv, int layer,
+                   const float* q, int M, float* out);
+
+/* Greedy accept + rollback alone (the last kernel of a step).
+ *   idx    DEVICE int32 [k+1] per-row argmax of rows 0..k
+ *   draft  DEVICE int32 [k]
+ *   kv     if not NULL: its seq_len holds n_past + k + 1 (block appended) and
+ *          is rolled back to n_past + L + 1.
+ * Writes res (DEVICE).  Accept rule: Ch. 33 §33.2 with one-hot target and
+ * draft distributions: p/q = 1 where draft == argmax (accept with certainty),
+ * p = 0 elsewhere (reject), residual max(p - q, 0) one-hot at the argmax. */
+int spec_accept(spec_ctx* ctx, const int32_t* idx, const int32_t* draft, int k,
+                spec_kv* kv, spec_result* res);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SPEC_VERIFY_H */

@@ -1,0 +1,510 @@
+/*
+ * spec_oracle.c — plain single-threaded CPU oracle of the exact greedy verify
+ * step.  TEST INFRASTRUCTURE ONLY (see spec_oracle.h): nothing in the product
+ * library links or calls it.  Build with -O2 -ffp-contract=off so that every
+ * fp32 product and sum below is rounded on its own, as written.
+ *
+ * Every function is the plain definition, scalar, in serial order.  Precision:
+ *   - integer sums are exact (int32/int64);
+ *   - the per-superblock combination is fp32 with each operation rounded
+ *     (the "fixed fp32 order" reading of the integer-dot anchor, [32] §32.7);
+ *   - sums of many fp32 terms (GEMM outputs over superblocks) accumulate in
+ *     fp64 and are rounded to fp32 once;
+ *   - RMSNorm, attention and SwiGLU are computed in fp64 and stored as fp32;
+ *   - the residual stream is fp32 ([32] chapter intro: F32 residual);
+ *   - K/V rows are stored as bf16, round-to-nearest-even.
+ */
+#include "spec_oracle.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------------ */
+/* number formats                                                            */
+/* ------------------------------------------------------------------------ */
+
+/* IEEE binary16 -> binary32, exact. */
+float orc_half_to_float(uint16_t h) {
+    int sign = (h >> 15) & 1;
+    int exp = (h >> 10) & 0x1f;
+    int man = h & 0x3ff;
+    double v;
+    if (exp == 0) {
+        v = ldexp((double)man, -24);                 /* subnormal: man * 2^-24 */
+    } else if (exp == 31) {
+        v = man ? NAN : INFINITY;
+    } else {
+        v = ldexp((double)(1024 + man), exp - 25);   /* (1 + man/1024) 2^(exp-15) */
+    }
+    return (float)(sign ? -v : v);
+}
+
+float orc_bf16_to_float(uint16_t b) {
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return f;
+}
+
+/* binary32 -> bfloat16, round to nearest, ties to even; NaN stays NaN. */
+uint16_t orc_float_to_bf16(float f) {
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    if ((u & 0x7f800000u) == 0x7f800000u && (u & 0x007fffffu)) return (uint16_t)((u >> 16) | 0x40);
+    uint32_t keep = u >> 16;
+    uint32_t rest = u & 0xffffu;
+    if (rest > 0x8000u || (rest == 0x8000u && (keep & 1u))) keep += 1;
+    return (uint16_t)keep;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Q4_K superblock (canonical byte layout, spec_verify.h)                    */
+/*   bytes 0..1 d, 2..3 dmin (binary16); 4..15 a 96-bit LE field with sc_j at */
+/*   bits 6j..6j+5 and m_j at bits 48+6j..; 16..143 codes, element e of      */
+/*   sub-block j = e/32 in byte 16+16j+(e%32)%16, low nibble if e%32 < 16.   */
+/* ------------------------------------------------------------------------ */
+
+void orc_q4k_scale_min(const uint8_t* sb, int j, int* sc, int* m) {
+    const uint8_t* f = sb + 4;
+    int s = 0, mm = 0;
+    for (int bit = 0; bit < 6; ++bit) {
+        int p = 6 * j + bit;                 /* bit index in the 96-bit field */
+        s |= ((f[p / 8] >> (p % 8)) & 1) << bit;
+        int r = 48 + 6 * j + bit;
+        mm |= ((f[r / 8] >> (r % 8)) & 1) << bit;
+    }
+    *sc = s;
+    *m = mm;
+}
+
+int orc_q4k_code(const uint8_t* sb, int e) {
+    int j = e / 32, r = e % 32;
+    uint8_t byte = sb[16 + 16 * j + (r % 16)];
+    return r < 16 ? (byte & 0x0f) : (byte >> 4);
+}
+
+static uint16_t rd16(const uint8_t* p) { return (uint16_t)(p[0] | (p[1] << 8)); }
+
+/* w_e = d * sc_j * q_e - dmin * m_j, in fp64. */
+void orc_q4k_dequant_f64(const uint8_t* W, int N, int K, double* out) {
+    int nb = K / 256;
+    for (int n = 0; n < N; ++n) {
+        for (int b = 0; b < nb; ++b) {
+            const uint8_t* sb = W + ((size_t)n * nb + b) * 144;
+            double d = orc_half_to_float(rd16(sb));
+            double dmin = orc_half_to_float(rd16(sb + 2));
+            for (int e = 0; e < 256; ++e) {
+                int sc, m;
+                orc_q4k_scale_min(sb, e / 32, &sc, &m);
+                out[(size_t)n * K + 256 * b + e] = d * sc * orc_q4k_code(sb, e) - dmin * m;
+            }
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Q8 activation quantisation, per row and 256-block:                        */
+/*   d_a = amax / 127 (fp32 division); q = clamp(rint(x / d_a), -127, 127)   */
+/*   with round-half-even (the default rounding mode); all-zero block -> 0.  */
+/*   A_j = sum of the 32 codes of sub-block j.                                */
+/* ------------------------------------------------------------------------ */
+int orc_quantize_q8(const float* x, int M, int K, int8_t* q, float* d_a, int32_t* A) {
+    int status = 0;
+    int nb = K / 256;
+    for (int m = 0; m < M; ++m) {
+        for (int b = 0; b < nb; ++b) {
+            const float* xb = x + (size_t)m * K + 256 * b;
+            float amax = 0.0f;
+            for (int e = 0; e < 256; ++e) {
+                if (!isfinite(xb[e])) status |= ORC_ST_NONFINITE;
+                float a = fabsf(xb[e]);
+                if (a > amax) amax = a;
+            }
+            float d = amax / 127.0f;
+            d_a[m * nb + b] = d;
+            for (int e = 0; e < 256; ++e) {
+                int v = 0;
+                if (d != 0.0f && isfinite(xb[e])) {
+                    float r = rintf(xb[e] / d);
+                    if (r > 127.0f) r = 127.0f;
+                    if (r < -127.0f) r = -127.0f;
+                    v = (int)r;
+                }
+                q[(size_t)m * K + 256 * b + e] = (int8_t)v;
+            }
+            for (int j = 0; j < 8; ++j) {
+                int32_t s = 0;
+                for (int i = 0; i < 32; ++i) s += q[(size_t)m * K + 256 * b + 32 * j + i];
+                A[(size_t)m * (K / 32) + 8 * b + j] = s;
+            }
+        }
+    }
+    return status;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Integer-dot GEMM ([32] §32.7 integer-dot anchor):                          */
+/*   S_j = sum_i q_w * q_a (exact), ISc = sum_j sc_j S_j, IMn = sum_j m_j A_j */
+/*   v_b = d_a * (f32(d) * f32(ISc) - f32(dmin) * f32(IMn)), each op rounded  */
+/*   y = sum_b v_b, accumulated in fp64, rounded to fp32 once.               */
+/* ------------------------------------------------------------------------ */
+void orc_gemm_q4k(const uint8_t* W, int N, int K, const int8_t* q, const float* d_a,
+                  const int32_t* A, int M, float* y, int32_t* isc, int32_t* imn, float* vb) {
+    int nb = K / 256;
+    for (int m = 0; m < M; ++m) {
+        for (int n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (int b = 0; b < nb; ++b) {
+                const uint8_t* sb = W + ((size_t)n * nb + b) * 144;
+                const int8_t* qa = q + (size_t)m * K + 256 * b;
+                int32_t ISc = 0, IMn = 0;
+                for (int j = 0; j < 8; ++j) {
+                    int sc, mn;
+                    orc_q4k_scale_min(sb, j, &sc, &mn);
+                    int32_t S = 0;
+                    for (int i = 0; i < 32; ++i) S += orc_q4k_code(sb, 32 * j + i) * qa[32 * j + i];
+                    ISc += sc * S;
+                    IMn += mn * A[(size_t)m * (K / 32) + 8 * b + j];
+                }
+                float d = orc_half_to_float(rd16(sb));
+                float dmin = orc_half_to_float(rd16(sb + 2));
+                float t1 = d * (float)ISc;
+                float t2 = dmin * (float)IMn;
+                float diff = t1 - t2;
+                float v = d_a[m * nb + b] * diff;
+                size_t o = ((size_t)m * N + n) * nb + b;
+                if (isc) isc[o] = ISc;
+                if (imn) imn[o] = IMn;
+                if (vb) vb[o] = v;
+                acc += (double)v;
+            }
+            y[(size_t)m * N + n] = (float)acc;
+        }
+    }
+}
+
+int orc_linear(const uint8_t* W, int N, int K, const float* x, int M, float* y) {
+    int8_t* q = (int8_t*)malloc((size_t)M * K);
+    float* d_a = (float*)malloc(sizeof(float) * (size_t)M * (K / 256));
+    int32_t* A = (int32_t*)malloc(sizeof(int32_t) * (size_t)M * (K / 32));
+    int st = orc_quantize_q8(x, M, K, q, d_a, A);
+    orc_gemm_q4k(W, N, K, q, d_a, A, M, y, NULL, NULL, NULL);
+    free(q);
+    free(d_a);
+    free(A);
+    return st;
+}
+
+void orc_dense_f64(const uint8_t* W, int N, int K, const double* x, int M, double* y) {
+    double* w = (double*)malloc(sizeof(double) * (size_t)N * K);
+    orc_q4k_dequant_f64(W, N, K, w);
+    for (int m = 0; m < M; ++m)
+        for (int n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (int k = 0; k < K; ++k) acc += w[(size_t)n * K + k] * x[(size_t)m * K + k];
+            y[(size_t)m * N + n] = acc;
+        }
+    free(w);
+}
+
+/* ------------------------------------------------------------------------ */
+/* RMSNorm: y = x / sqrt(mean(x^2) + eps) * gamma  (fp64, stored fp32).      */
+/* ------------------------------------------------------------------------ */
+void orc_rmsnorm(const float* x, const float* gamma, int M, int H, float eps, float* y) {
+    for (int m = 0; m < M; ++m) {
+        double ss = 0.0;
+        for (int i = 0; i < H; ++i) ss += (double)x[(size_t)m * H + i] * x[(size_t)m * H + i];
+        double r = 1.0 / sqrt(ss / H + (double)eps);
+        for (int i = 0; i < H; ++i) {
+            double g = gamma ? gamma[i] : 1.0;
+            y[(size_t)m * H + i] = (float)((double)x[(size_t)m * H + i] * r * g);
+        }
+    }
+}
+
+/* SwiGLU: h = silu(g) * u, silu(x) = x / (1 + e^-x)  (fp64, stored fp32). */
+void orc_silu_mul(const float* gate, const float* up, int n, float* h) {
+    for (int i = 0; i < n; ++i) {
+        double g = gate[i];
+        h[i] = (float)(g / (1.0 + exp(-g)) * (double)up[i]);
+    }
+}
+
+/* Per-row argmax, lowest index among equal maxima; gap = top1 - top2. */
+void orc_argmax(const float* logits, int M, int V, int32_t* idx, float* gap) {
+    for (int m = 0; m < M; ++m) {
+        const float* r = logits + (size_t)m * V;
+        int best = 0;
+        for (int v = 1; v < V; ++v)
+            if (r[v] > r[best]) best = v;
+        float second = -INFINITY;
+        for (int v = 0; v < V; ++v)
+            if (v != best && r[v] > second) second = r[v];
+        idx[m] = best;
+        if (gap) gap[m] = r[best] - second;
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Greedy acceptance ([33] §33.2 at temperature 0).  The stochastic rule       */
+/* accepts token t with probability min(p_t/q_t, 1) and on the first reject  */
+/* draws from normalize(max(p - q, 0)); on all-accept it draws from the last  */
+/* row.  With one-hot p (target argmax) and q (draft token):                  */
+/*   draft == argmax -> p/q = 1, accepted with certainty;                     */
+/*   draft != argmax -> p_t = 0, rejected; the residual is one-hot at argmax. */
+/* Hence L = first i < k with draft[i] != idx[i] (else k) and next = idx[L].  */
+/* Geometry guard first: a token outside [0, vocab) rejects the whole call.   */
+/* ------------------------------------------------------------------------ */
+int orc_accept(const int32_t* idx, const int32_t* draft, int k, int vocab,
+               int32_t* accepted, int32_t* next) {
+    for (int i = 0; i < k; ++i)
+        if (draft[i] < 0 || draft[i] >= vocab) return ORC_ST_TOKEN_RANGE;
+    int L = k;
+    for (int i = 0; i < k; ++i)
+        if (draft[i] != idx[i]) { L = i; break; }
+    *accepted = L;
+    *next = idx[L];
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Paged KV metadata ([8] §8.6 item 4: checkpoint = metadata rewind).         */
+/* Free pages form a LIFO stack, initialised descending so that pops yield    */
+/* ids 0, 1, 2, ...; pages are mapped in ascending logical order; a rollback  */
+/* pushes the unmapped ids from the highest logical page down.                */
+/* ------------------------------------------------------------------------ */
+#define ORC_PAGE 16
+
+void orc_kv_reset(orc_kv* kv) {
+    for (int p = 0; p < kv->max_seq_pages; ++p) kv->page_table[p] = -1;
+    for (int i = 0; i < kv->num_pages; ++i) kv->free_stack[i] = kv->num_pages - 1 - i;
+    *kv->free_top = kv->num_pages;
+    *kv->seq_len = 0;
+}
+
+int orc_kv_reserve(orc_kv* kv, int32_t upto) {
+    int32_t pages = (upto + ORC_PAGE - 1) / ORC_PAGE;
+    if (pages > kv->max_seq_pages) return ORC_ST_CTX_FULL;
+    int need = 0;
+    for (int p = 0; p < pages; ++p)
+        if (kv->page_table[p] < 0) ++need;
+    if (need > *kv->free_top) return ORC_ST_POOL_EMPTY;
+    for (int p = 0; p < pages; ++p)
+        if (kv->page_table[p] < 0) {
+            *kv->free_top -= 1;
+            kv->page_table[p] = kv->free_stack[*kv->free_top];
+        }
+    return 0;
+}
+
+int orc_kv_extend(orc_kv* kv, int32_t n) {
+    int st = orc_kv_reserve(kv, *kv->seq_len + n);
+    if (st) return st;
+    *kv->seq_len += n;
+    return 0;
+}
+
+int orc_kv_rollback(orc_kv* kv, int32_t new_len) {
+    int32_t len = *kv->seq_len;
+    if (new_len < 0 || new_len > len) return ORC_ST_ROLLBACK;
+    int32_t hi = (len + ORC_PAGE - 1) / ORC_PAGE;       /* mapped: p < hi      */
+    int32_t lo = (new_len + ORC_PAGE - 1) / ORC_PAGE;   /* kept:   p < lo      */
+    for (int p = hi - 1; p >= lo; --p) {
+        if (kv->page_table[p] >= 0) {
+            kv->free_stack[*kv->free_top] = kv->page_table[p];
+            *kv->free_top += 1;
+            kv->page_table[p] = -1;
+        }
+    }
+    *kv->seq_len = new_len;
+    return 0;
+}
+
+static size_t kv_index(const orc_cfg* c, int page, int layer, int which, int head, int slot) {
+    return ((((size_t)page * c->n_layers + layer) * 2 + which) * c->n_kv_heads + head) *
+               (size_t)c->page_size * c->head_dim + (size_t)slot * c->head_dim;
+}
+
+void orc_kv_write_row(const orc_cfg* c, orc_kv* kv, int layer, int pos,
+                      const float* k_row, const float* v_row) {
+    int page = kv->page_table[pos / c->page_size];
+    int slot = pos % c->page_size;
+    for (int h = 0; h < c->n_kv_heads; ++h)
+        for (int d = 0; d < c->head_dim; ++d) {
+            kv->pool[kv_index(c, page, layer, 0, h, slot) + d] = orc_float_to_bf16(k_row[h * c->head_dim + d]);
+            kv->pool[kv_index(c, page, layer, 1, h, slot) + d] = orc_float_to_bf16(v_row[h * c->head_dim + d]);
+        }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Verify attention: row i sits at position n_past + i and sees positions     */
+/* 0..n_past+i (its own block's earlier rows included).  Query head h reads   */
+/* KV head h / (n_q/n_kv).  s_t = q.k_t / sqrt(head_dim), softmax over the    */
+/* visible t (max subtracted), o = sum_t softmax_t v_t.  K and V are the      */
+/* stored bf16 values.  fp64 throughout, stored fp32.                          */
+/* ------------------------------------------------------------------------ */
+void orc_attention(const orc_cfg* c, const orc_kv* kv, int layer, const float* q,
+                   int M, int n_past, float* out) {
+    int dh = c->head_dim, group = c->n_q_heads / c->n_kv_heads;
+    int max_vis = n_past + M;
+    double* s = (double*)malloc(sizeof(double) * (size_t)max_vis);
+    double scale = 1.0 / sqrt((double)dh);
+    for (int i = 0; i < M; ++i) {
+        int vis = n_past + i + 1;
+        for (int h = 0; h < c->n_q_heads; ++h) {
+            int g = h / group;
+            const float* qh = q + ((size_t)i * c->n_q_heads + h) * dh;
+            double mx = -INFINITY;
+            for (int t = 0; t < vis; ++t) {
+                int page = kv->page_table[t / c->page_size];
+                const uint16_t* kr = kv->pool + kv_index(c, page, layer, 0, g, t % c->page_size);
+                double dot = 0.0;
+                for (int d = 0; d < dh; ++d) dot += (double)qh[d] * orc_bf16_to_float(kr[d]);
+                s[t] = dot * scale;
+                if (s[t] > mx) mx = s[t];
+            }
+            double den = 0.0;
+            for (int t = 0; t < vis; ++t) {
+                s[t] = exp(s[t] - mx);
+                den += s[t];
+            }
+            for (int d = 0; d < dh; ++d) {
+                double o = 0.0;
+                for (int t = 0; t < vis; ++t) {
+                    int page = kv->page_table[t / c->page_size];
+                    const uint16_t* vr = kv->pool + kv_index(c, page, layer, 1, g, t % c->page_size);
+                    o += s[t] * orc_bf16_to_float(vr[d]);
+                }
+                out[((size_t)i * c->n_q_heads + h) * dh + d] = (float)(o / den);
+            }
+        }
+    }
+    free(s);
+}
+
+/* ------------------------------------------------------------------------ */
+/* One transformer block over M rows at positions n_past.. :                  */
+/*   xn = rmsnorm(x, attn_norm); [Q|K|V] = W_qkv q8(xn); K,V -> bf16 cache;   */
+/*   x += W_o q8(attention(Q));                                               */
+/*   xn = rmsnorm(x, ffn_norm); [g|u] = W_gu q8(xn); x += W_down q8(silu(g)u) */
+/* ------------------------------------------------------------------------ */
+int orc_block(const orc_cfg* c, const orc_weights* w, orc_kv* kv, int layer,
+              const float* x_in, int M, int n_past, float* x_out) {
+    int H = c->hidden, dh = c->head_dim, F = c->ffn;
+    int nq = c->n_q_heads * dh, nkv = c->n_kv_heads * dh;
+    int Nqkv = nq + 2 * nkv;
+    int st = 0;
+    float* xn = (float*)malloc(sizeof(float) * (size_t)M * H);
+    float* qkv = (float*)malloc(sizeof(float) * (size_t)M * Nqkv);
+    float* qv = (float*)malloc(sizeof(float) * (size_t)M * nq);
+    float* att = (float*)malloc(sizeof(float) * (size_t)M * nq);
+    float* o = (float*)malloc(sizeof(float) * (size_t)M * H);
+    float* gu = (float*)malloc(sizeof(float) * (size_t)M * 2 * F);
+    float* hh = (float*)malloc(sizeof(float) * (size_t)M * F);
+    float* x = (float*)malloc(sizeof(float) * (size_t)M * H);
+
+    const float* g_attn = (w->attn_norm) ? w->attn_norm[layer] : NULL;
+    const float* g_ffn = (w->ffn_norm) ? w->ffn_norm[layer] : NULL;
+
+    orc_rmsnorm(x_in, g_attn, M, H, c->rms_eps, xn);
+    st |= orc_linear(w->w_qkv[layer], Nqkv, H, xn, M, qkv);
+    for (int i = 0; i < M; ++i) {
+        memcpy(qv + (size_t)i * nq, qkv + (size_t)i * Nqkv, sizeof(float) * nq);
+        orc_kv_write_row(c, kv, layer, n_past + i, qkv + (size_t)i * Nqkv + nq,
+                         qkv + (size_t)i * Nqkv + nq + nkv);
+    }
+    orc_attention(c, kv, layer, qv, M, n_past, att);
+    st |= orc_linear(w->w_o[layer], H, nq, att, M, o);
+    for (size_t i = 0; i < (size_t)M * H; ++i) x[i] = x_in[i] + o[i];
+
+    orc_rmsnorm(x, g_ffn, M, H, c->rms_eps, xn);
+    st |= orc_linear(w->w_gate_up[layer], 2 * F, H, xn, M, gu);
+    for (int i = 0; i < M; ++i)
+        orc_silu_mul(gu + (size_t)i * 2 * F, gu + (size_t)i * 2 * F + F, F, hh + (size_t)i * F);
+    st |= orc_linear(w->w_down[layer], H, F, hh, M, o);
+    for (size_t i = 0; i < (size_t)M * H; ++i) x_out[i] = x[i] + o[i];
+
+    free(xn); free(qkv); free(qv); free(att); free(o); free(gu); free(hh); free(x);
+    return st;
+}
+
+int orc_forward(const orc_cfg* c, const orc_weights* w, orc_kv* kv, const float* hidden,
+                int M, int32_t* idx, float* logits, float* resid) {
+    int H = c->hidden, V = c->vocab;
+    int n_past = *kv->seq_len;
+    int st = orc_kv_reserve(kv, n_past + M);
+    if (st) return st;
+    float* x = (float*)malloc(sizeof(float) * (size_t)M * H);
+    float* y = (float*)malloc(sizeof(float) * (size_t)M * H);
+    float* lg = logits ? logits : (float*)malloc(sizeof(float) * (size_t)M * V);
+    memcpy(x, hidden, sizeof(float) * (size_t)M * H);
+    for (int l = 0; l < c->n_layers; ++l) {
+        if (resid) memcpy(resid + (size_t)l * M * H, x, sizeof(float) * (size_t)M * H);
+        st |= orc_block(c, w, kv, l, x, M, n_past, y);
+        memcpy(x, y, sizeof(float) * (size_t)M * H);
+    }
+    if (resid) memcpy(resid + (size_t)c->n_layers * M * H, x, sizeof(float) * (size_t)M * H);
+    orc_rmsnorm(x, w->final_norm, M, H, c->rms_eps, y);
+    st |= orc_linear(w->w_head, V, H, y, M, lg);
+    for (size_t i = 0; i < (size_t)M * V; ++i)
+        if (!isfinite(lg[i])) st |= ORC_ST_NONFINITE;
+    orc_argmax(lg, M, V, idx, NULL);
+    *kv->seq_len = n_past + M;
+    if (!logits) free(lg);
+    free(x);
+    free(y);
+    return st;
+}
+
+/* The verify step ([33] §33.2, §33.7; [8] §8.6).  Returns -2 for a verify
+ * length outside {3, 7, 15} (rejected before any work, [8] §8.6 item 3).
+ * res = {accepted_len, next_token, status, seq_len}.  On a device-class error
+ * the KV metadata is restored to its state before the step. */
+int orc_verify_step(const orc_cfg* c, const orc_weights* w, orc_kv* kv, const float* hidden,
+                    const int32_t* draft, int k, int32_t* res, int32_t* idx, float* logits,
+                    float* resid) {
+    if (k != 3 && k != 7 && k != 15) return -2;
+    int n_past = *kv->seq_len;
+    res[0] = 0;
+    res[1] = -1;
+    res[3] = n_past;
+    for (int i = 0; i < k; ++i)
+        if (draft[i] < 0 || draft[i] >= c->vocab) {
+            res[2] = ORC_ST_TOKEN_RANGE;
+            return 0;
+        }
+    int st = orc_forward(c, w, kv, hidden, k + 1, idx, logits, resid);
+    if (st & (ORC_ST_POOL_EMPTY | ORC_ST_CTX_FULL)) {
+        res[2] = st;
+        return 0;
+    }
+    int32_t L = 0, next = -1;
+    st |= orc_accept(idx, draft, k, c->vocab, &L, &next);
+    if (st) {
+        orc_kv_rollback(kv, n_past);
+        res[2] = st;
+        return 0;
+    }
+    orc_kv_rollback(kv, n_past + L + 1);
+    res[0] = L;
+    res[1] = next;
+    res[2] = 0;
+    res[3] = *kv->seq_len;
+    return 0;
+}
+
+/* Serial greedy decode ([TF] temp-0 token-fidelity gate): the same k+1 rows,
+ * one forward per row, each appending its KV row before the next.  Row i+1 is
+ * taken as the embedding of draft token i, so tokens[0..L] of a serial run
+ * must equal the accepted drafts plus the next token of the batched step. */
+int orc_serial_greedy(const orc_cfg* c, const orc_weights* w, orc_kv* kv, const float* hidden,
+                      int k, int32_t* tokens) {
+    int st = 0;
+    for (int i = 0; i <= k; ++i) {
+        int32_t t;
+        st |= orc_forward(c, w, kv, hidden + (size_t)i * c->hidden, 1, &t, NULL, NULL);
+        tokens[i] = t;
+    }
+    return st;
+}

@@ -1,0 +1,456 @@
+"""Pins of the CPU oracle against things other than itself (no GPU needed).
+
+Each test fixes the oracle to a closed form, a hand-worked example, an
+invariant, a special case that reduces to a textbook/library routine, or a
+brute-force fp64 computation, so that a dropped term, a wrong sign or index,
+a transposed operand or a wrong rounding mode fails at least one of them.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from speculative_decoding_exact_gb300 import synth
+from tests.q4k_pack import dequant_fields, pack_superblock
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "q4k_handworked.txt")
+
+
+# ---------------------------------------------------------------------------
+# number formats
+# ---------------------------------------------------------------------------
+def test_half_to_float_known_values():
+    assert oracle.half_to_float(0x3C00) == 1.0
+    assert oracle.half_to_float(0xC000) == -2.0
+    assert oracle.half_to_float(0x7BFF) == 65504.0
+    assert oracle.half_to_float(0x0001) == 2.0 ** -24          # smallest subnormal
+    assert oracle.half_to_float(0x0400) == 2.0 ** -14          # smallest normal
+    assert oracle.half_to_float(0x3555) == np.float32(np.float16(1 / 3))
+    assert math.isinf(oracle.half_to_float(0x7C00))
+
+
+def test_half_to_float_matches_numpy_on_all_finite_patterns():
+    bits = np.arange(0, 1 << 16, dtype=np.uint32).astype(np.uint16)
+    ref = bits.view(np.float16).astype(np.float32)
+    for b in range(0, 1 << 16, 97):
+        r = ref[b]
+        if np.isfinite(r):
+            assert oracle.half_to_float(b) == r
+
+
+def test_bf16_round_to_nearest_even():
+    assert oracle.float_to_bf16(1.0) == 0x3F80
+    assert oracle.float_to_bf16(1.0 + 2.0 ** -8) == 0x3F80     # tie -> even (down)
+    assert oracle.float_to_bf16(1.0 + 3 * 2.0 ** -8) == 0x3F82  # tie -> even (up)
+    assert oracle.float_to_bf16(1.0 + 2.0 ** -8 + 2.0 ** -20) == 0x3F81
+    assert oracle.float_to_bf16(-2.5) == 0xC020
+    assert oracle.bf16_to_float(0x3F80) == 1.0
+    x = synth.normal((4096,), 0, 1)
+    ours = np.array([oracle.float_to_bf16(v) for v in x[:512]], dtype=np.uint16)
+    assert np.array_equal(ours, synth.bf16_bits(x[:512]))
+
+
+# ---------------------------------------------------------------------------
+# Q4_K decoding against the independent packer
+# ---------------------------------------------------------------------------
+def test_superblock_fields_roundtrip():
+    rng = np.random.default_rng(7)
+    for _ in range(20):
+        sc = rng.integers(0, 64, 8)
+        m = rng.integers(0, 64, 8)
+        q = rng.integers(0, 16, 256)
+        d, dmin = rng.uniform(1e-3, 1e-2, 2)
+        sb = pack_superblock(d, dmin, sc, m, q)
+        for j in range(8):
+            assert oracle.scale_min(sb, j) == (sc[j], m[j])
+        for e in range(256):
+            assert oracle.code(sb, e) == q[e]
+        w = oracle.dequant_f64(sb, 1, 256)[0]
+        assert np.allclose(w, dequant_fields(d, dmin, sc, m, q), rtol=0, atol=0)
+
+
+def _golden_cases():
+    cases = {}
+    for line in open(GOLDEN):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        kv = dict(tok.split("=", 1) for tok in line.split())
+        cases.setdefault(int(kv.pop("case")), {}).update(kv)
+    return cases
+
+
+def _build_case(c):
+    j_idx = np.arange(8)
+    sc = {"j+1": j_idx + 1, "63-8j": 63 - 8 * j_idx}[c["sc"]]
+    m = {"j": j_idx, "2j+1": 2 * j_idx + 1}[c["m"]]
+    r = np.arange(256) % 32
+    q = {"r%16": r % 16, "(7r+3)%16": (7 * r + 3) % 16}[c["q"]]
+    kind, vals = c["x"].split(":")
+    vals = [float(v) for v in vals.split(",")]
+    x = np.array([vals[e % len(vals)] for e in range(256)], dtype=np.float32)
+    return pack_superblock(float(c["d"]), float(c["dmin"]), sc, m, q), x
+
+
+@pytest.mark.parametrize("case", [1, 2, 3])
+def test_handworked_superblock(case):
+    c = _golden_cases()[case]
+    sb, x = _build_case(c)
+    q, d_a, A, st = oracle.quantize_q8(x[None, :])
+    assert st == 0
+    assert np.all(A[0] == int(c["A"]))
+    y, isc, imn, vb = oracle.gemm_q4k(sb, 1, 256, q, d_a, A, sums=True)
+    assert isc[0, 0, 0] == int(c["ISc"])
+    assert imn[0, 0, 0] == int(c["IMn"])
+    assert vb[0, 0, 0] == np.float32(float(c["v"]))
+    assert y[0, 0] == np.float32(float(c["v"]))
+    if "v_bits" in c:
+        assert int(np.float32(vb[0, 0, 0]).view(np.uint32)) == int(c["v_bits"], 16)
+    if "dense_raw" in c:
+        raw = oracle.dense_f64(sb, 1, 256, x[None, :].astype(np.float64))[0, 0]
+        assert raw == float(c["dense_raw"])
+    # S_j: every sub-block carries the same sum in these cases
+    for j in range(8):
+        s = sum(oracle.code(sb, 32 * j + i) * int(q[0, 32 * j + i]) for i in range(32))
+        assert s == int(c["S"])
+
+
+def test_case2_pins_half_even_rounding():
+    c = _golden_cases()[2]
+    sb, x = _build_case(c)
+    q, d_a, A, _ = oracle.quantize_q8(x[None, :])
+    assert list(q[0, :4]) == [127, 2, 0, 0]
+    y = oracle.gemm_q4k(sb, 1, 256, q, d_a, A)
+    assert y[0, 0] != np.float32(float(c["v_half_away"]))
+
+
+# ---------------------------------------------------------------------------
+# quantiser pins
+# ---------------------------------------------------------------------------
+def test_quantizer_closed_forms():
+    x = synth.normal((3, 1024), 0, 11)
+    x[1, 256:512] = 0.0                                   # all-zero block
+    q, d_a, A, st = oracle.quantize_q8(x)
+    assert st == 0
+    assert d_a[1, 1] == 0.0 and np.all(q[1, 256:512] == 0)
+    for m in range(3):
+        for b in range(4):
+            blk = x[m, 256 * b:256 * b + 256]
+            amax = np.max(np.abs(blk))
+            if amax == 0:
+                continue
+            assert d_a[m, b] == np.float32(amax) / np.float32(127)
+            i = int(np.argmax(np.abs(blk)))
+            assert abs(int(q[m, 256 * b + i])) == 127          # the extreme maps to +-127
+            assert np.all(np.abs(q[m, 256 * b:256 * b + 256]) <= 127)
+    assert np.array_equal(A, q.astype(np.int64).reshape(3, 32, 32).sum(-1))
+    # dequantised error bounded by half a step
+    deq = q.astype(np.float64).reshape(3, 4, 256) * d_a[:, :, None]
+    assert np.all(np.abs(deq - x.reshape(3, 4, 256)) <= d_a[:, :, None] * 0.5 + 1e-12)
+
+
+def test_quantizer_flags_nonfinite():
+    x = np.ones((1, 256), dtype=np.float32)
+    x[0, 5] = np.nan
+    assert oracle.quantize_q8(x)[3] == oracle.ST_NONFINITE
+    x[0, 5] = np.inf
+    assert oracle.quantize_q8(x)[3] == oracle.ST_NONFINITE
+
+
+# ---------------------------------------------------------------------------
+# GEMM against brute-force fp64 (independent dequantisation path)
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("M,N,K", [(1, 1, 256), (3, 5, 512), (4, 17, 1024), (2, 64, 768)])
+def test_gemm_matches_dense_fp64(M, N, K):
+    W = synth.q4k_matrix(N, K, 1, 100 + N)
+    x = synth.normal((M, K), 1, 200 + M)
+    q, d_a, A, _ = oracle.quantize_q8(x)
+    y = oracle.gemm_q4k(W, N, K, q, d_a, A)
+    nb = K // 256
+    xq = (q.astype(np.float64).reshape(M, nb, 256) * d_a[:, :, None].astype(np.float64)).reshape(M, K)
+    ref = oracle.dense_f64(W, N, K, xq)
+    wabs = np.abs(oracle.dequant_f64(W, N, K))
+    scale = np.abs(xq) @ wabs.T                   # sum |w||x|: bound on rounding growth
+    assert np.all(np.abs(y - ref) <= 4 * 2.0 ** -24 * (scale + np.abs(ref)) * nb + 1e-30)
+    # quantisation bound against the raw input
+    raw = oracle.dense_f64(W, N, K, x.astype(np.float64))
+    bound = (wabs * np.repeat(d_a, 256, axis=1)[:, None, :] * 0.5).sum(-1)
+    assert np.all(np.abs(y - raw) <= bound + 1e-3 * np.abs(raw) + 1e-6)
+
+
+def test_gemm_transposition_and_row_independence():
+    N, K = 9, 512
+    W = synth.q4k_matrix(N, K, 2, 1)
+    x = synth.normal((5, K), 2, 2)
+    y = oracle.linear(W, N, K, x)
+    for m in range(5):
+        assert np.array_equal(oracle.linear(W, N, K, x[m:m + 1])[0], y[m])
+    # one-hot activation selects a weight column's k-th entry (times the scale)
+    e = np.zeros((1, K), dtype=np.float32)
+    e[0, 300] = 1.0
+    y1 = oracle.linear(W, N, K, e)[0]
+    w = oracle.dequant_f64(W, N, K)
+    assert np.allclose(y1, w[:, 300] * (np.float32(1) / np.float32(127)) * 127, rtol=1e-6, atol=1e-9)
+
+
+# ---------------------------------------------------------------------------
+# RMSNorm, SwiGLU, argmax
+# ---------------------------------------------------------------------------
+def test_rmsnorm_closed_forms():
+    eps = 1e-6
+    x = np.full((1, 512), 3.0, dtype=np.float32)
+    y = oracle.rmsnorm(x, None, eps)
+    assert np.allclose(y, 3.0 / np.sqrt(9.0 + eps), rtol=1e-7)
+    g = np.linspace(-2, 2, 512).astype(np.float32)
+    x = synth.normal((2, 512), 3, 3)
+    y1 = oracle.rmsnorm(x, None, eps)
+    y2 = oracle.rmsnorm(x, g, eps)
+    assert np.allclose(y2, y1 * g, rtol=2e-7, atol=1e-7)
+    assert np.allclose(np.mean(y1.astype(np.float64) ** 2, axis=1), 1.0, rtol=1e-5)
+    assert np.allclose(oracle.rmsnorm(2 * x, None, eps), y1, rtol=1e-5)  # scale invariance
+
+
+def test_silu_special_values():
+    g = np.array([0.0, 50.0, -50.0, 1.5, -1.5], dtype=np.float32)
+    u = np.ones_like(g)
+    h = oracle.silu_mul(g, u)
+    assert h[0] == 0.0 and abs(h[1] - 50.0) < 1e-6 and abs(h[2]) < 1e-18
+    assert abs((h[3] - h[4]) - 1.5) < 1e-6            # silu(x) - silu(-x) = x
+    assert np.allclose(oracle.silu_mul(g, 2 * u), 2 * h, rtol=1e-7)
+
+
+def test_argmax_lowest_index_and_gap():
+    lg = np.array([[1.0, 3.0, 3.0, 2.0], [5.0, -1.0, 5.0, 4.5]], dtype=np.float32)
+    idx, gap = oracle.argmax(lg)
+    assert list(idx) == [1, 0]
+    assert list(gap) == [0.0, 0.0]
+    idx, gap = oracle.argmax(np.array([[0.0, 2.0, 1.5]], dtype=np.float32))
+    assert idx[0] == 1 and gap[0] == 0.5
+
+
+# ---------------------------------------------------------------------------
+# accept rule: greedy == the pages' stochastic rule with one-hot distributions
+# ---------------------------------------------------------------------------
+def _stochastic_accept(draft, p_rows, q_rows, us):
+    """The accept/reject rule of Ch. 33 §33.2 written from its description:
+    accept token t with prob min(p/q, 1) (1 when q <= 0); on the first reject
+    draw from normalize(max(p - q, 0)) (p itself if that is all zero); after
+    all k accepted draw from the last target row.  Draws use the given
+    uniforms; a one-hot distribution makes every draw deterministic."""
+    def draw(dist):
+        nz = np.flatnonzero(dist > 0)
+        assert len(nz) == 1
+        return int(nz[0])
+    for i, t in enumerate(draft):
+        q, p = q_rows[i][t], p_rows[i][t]
+        acc = 1.0 if q <= 0 else min(p / q, 1.0)
+        if us[i] <= acc:
+            continue
+        res = np.maximum(p_rows[i] - q_rows[i], 0.0)
+        res = p_rows[i] if res.sum() <= 0 else res / res.sum()
+        return i, draw(res)
+    return len(draft), draw(p_rows[-1])
+
+
+@pytest.mark.parametrize("k", [3, 7])
+def test_accept_exhaustive_patterns(k):
+    V = 50
+    rng = np.random.default_rng(k)
+    for pattern in range(1 << k):
+        idx = rng.integers(0, V, k + 1).astype(np.int32)
+        draft = np.array([idx[i] if (pattern >> i) & 1 else (idx[i] + 1 + rng.integers(0, V - 1)) % V
+                          for i in range(k)], dtype=np.int32)
+        L, nxt, st = oracle.accept(idx, draft, V)
+        assert st == 0
+        p_rows = [np.eye(V)[t] for t in idx]
+        q_rows = [np.eye(V)[t] for t in draft]
+        us = 1.0 - rng.random(k)                       # uniforms in (0, 1]
+        assert (L, nxt) == _stochastic_accept(draft, p_rows, q_rows, us)
+
+
+def test_accept_random_k15_and_range_guard():
+    V = 1000
+    rng = np.random.default_rng(3)
+    for _ in range(200):
+        idx = rng.integers(0, V, 16).astype(np.int32)
+        L_t = int(rng.integers(0, 16))
+        draft = synth.plant_draft(idx, L_t, V, 0, int(rng.integers(1 << 30)))
+        L, nxt, st = oracle.accept(idx, draft, V)
+        assert (L, nxt, st) == (L_t, idx[L_t], 0)
+    draft = np.zeros(15, dtype=np.int32)
+    draft[4] = V
+    assert oracle.accept(np.zeros(16, dtype=np.int32), draft, V)[2] == oracle.ST_TOKEN_RANGE
+    draft[4] = -1
+    assert oracle.accept(np.zeros(16, dtype=np.int32), draft, V)[2] == oracle.ST_TOKEN_RANGE
+
+
+# ---------------------------------------------------------------------------
+# paged KV metadata invariants
+# ---------------------------------------------------------------------------
+TINY = oracle.Config(hidden=256, n_layers=1, n_q_heads=2, n_kv_heads=1, head_dim=128, ffn=256,
+                     vocab=64)
+
+
+def _check_conservation(kv):
+    mapped = kv.page_table[kv.page_table >= 0]
+    free = kv.free_stack[: kv.free_top]
+    allids = np.concatenate([mapped, free])
+    assert len(allids) == kv.num_pages and len(set(allids.tolist())) == kv.num_pages
+
+
+def test_kv_reset_pop_order_and_conservation():
+    kv = oracle.KV(TINY, num_pages=10, max_seq_pages=8)
+    assert kv.extend(37) == 0
+    assert kv.seq_len == 37 and list(kv.page_table[:3]) == [0, 1, 2] and kv.page_table[3] == -1
+    _check_conservation(kv)
+
+
+def test_kv_rollback_identity_and_reextend():
+    kv = oracle.KV(TINY, num_pages=10, max_seq_pages=8)
+    kv.extend(20)
+    before = kv.committed()
+    assert kv.rollback(20) == 0
+    after = kv.committed()
+    assert all(np.array_equal(a, b) for a, b in zip(before[1:], after[1:])) and after[0] == 20
+    kv.extend(20)                    # seq_len 40: pages 0..2
+    snap = kv.copy()
+    assert kv.rollback(21) == 0       # keeps pages 0,1 ; frees page 2
+    assert kv.seq_len == 21 and kv.page_table[2] == -1
+    _check_conservation(kv)
+    kv.extend(19)                     # back to 40 -> same physical page as before
+    assert np.array_equal(kv.page_table, snap.page_table)
+    assert np.array_equal(kv.free_stack[: kv.free_top], snap.free_stack[: snap.free_top])
+
+
+def test_kv_rollback_rejects_bad_lengths_and_pool_exhaustion():
+    kv = oracle.KV(TINY, num_pages=3, max_seq_pages=8)
+    kv.extend(10)
+    assert kv.rollback(11) == oracle.ST_ROLLBACK and kv.seq_len == 10
+    assert kv.rollback(-1) == oracle.ST_ROLLBACK
+    snap = kv.committed()
+    assert kv.extend(64) == oracle.ST_POOL_EMPTY          # needs 5 pages, pool holds 3
+    assert all(np.array_equal(a, b) for a, b in zip(snap[1:], kv.committed()[1:]))
+    assert kv.extend(8 * 16 + 1) == oracle.ST_CTX_FULL
+
+
+def test_kv_rollback_pushes_highest_page_first():
+    kv = oracle.KV(TINY, num_pages=10, max_seq_pages=8)
+    kv.extend(64)                                          # pages 0..3
+    kv.rollback(0)
+    # stack top must be the lowest logical page's id so that re-extension reuses it first
+    assert list(kv.free_stack[kv.free_top - 4: kv.free_top]) == [3, 2, 1, 0]
+
+
+# ---------------------------------------------------------------------------
+# attention special cases
+# ---------------------------------------------------------------------------
+def _fill_kv(kv, layer, n, seed):
+    cfg = kv.cfg
+    rows_k = synth.normal((n, cfg.n_kv_heads * cfg.head_dim), seed, 1)
+    rows_v = synth.normal((n, cfg.n_kv_heads * cfg.head_dim), seed, 2)
+    for p in range(n):
+        kv.write_row(layer, p, rows_k[p], rows_v[p])
+    return rows_k, rows_v
+
+
+def test_attention_single_position_returns_value():
+    kv = oracle.KV(TINY, num_pages=4, max_seq_pages=4)
+    kv.extend(1)
+    _, rv = _fill_kv(kv, 0, 1, 5)
+    q = synth.normal((1, 2, 128), 5, 3)
+    out = kv.attention(0, q, n_past=0)
+    vb = np.array([oracle.bf16_to_float(oracle.float_to_bf16(v)) for v in rv[0]], dtype=np.float32)
+    assert np.allclose(out[0, :128], vb, rtol=1e-6) and np.allclose(out[0, 128:], vb, rtol=1e-6)
+
+
+def test_attention_matches_softmax_reference():
+    cfg = oracle.Config(hidden=512, n_layers=1, n_q_heads=4, n_kv_heads=2, head_dim=128, ffn=256,
+                        vocab=64)
+    kv = oracle.KV(cfg, num_pages=8, max_seq_pages=8)
+    n_past, M = 21, 3
+    kv.extend(n_past + M)
+    rk, rv = _fill_kv(kv, 0, n_past + M, 6)
+    q = synth.normal((M, 4, 128), 6, 3)
+    out = kv.attention(0, q, n_past)
+    kb = np.vectorize(oracle.bf16_to_float)(synth.bf16_bits(rk)).reshape(-1, 2, 128)
+    vb = np.vectorize(oracle.bf16_to_float)(synth.bf16_bits(rv)).reshape(-1, 2, 128)
+    for i in range(M):
+        vis = n_past + i + 1
+        for h in range(4):
+            g = h // 2
+            s = kb[:vis, g] @ q[i, h].astype(np.float64) / math.sqrt(128)
+            p = np.exp(s - s.max())
+            ref = (p / p.sum()) @ vb[:vis, g]
+            assert np.allclose(out[i, 128 * h:128 * h + 128], ref, rtol=1e-5, atol=1e-6)
+    # a dominant key reduces attention to a copy of its value
+    q2 = np.zeros((1, 4, 128), dtype=np.float32)
+    q2[0, 0] = 200.0 * kb[5, 0] / np.linalg.norm(kb[5, 0])
+    out2 = kv.attention(0, q2, n_past + M - 1)
+    assert np.allclose(out2[0, :128], vb[5, 0], atol=1e-3)
+
+
+# ---------------------------------------------------------------------------
+# whole-step invariants on a tiny model
+# ---------------------------------------------------------------------------
+def tiny_model(seed=0, n_layers=2, vocab=512):
+    cfg = oracle.Config(hidden=512, n_layers=n_layers, n_q_heads=4, n_kv_heads=2, head_dim=128,
+                        ffn=768, vocab=vocab)
+    H, F, NQ = cfg.hidden, cfg.ffn, cfg.n_qkv
+    w = oracle.Weights(
+        w_qkv=[synth.q4k_matrix(NQ, H, seed, 10 + l) for l in range(n_layers)],
+        w_o=[synth.q4k_matrix(H, H, seed, 20 + l) for l in range(n_layers)],
+        w_gate_up=[synth.q4k_matrix(2 * F, H, seed, 30 + l) for l in range(n_layers)],
+        w_down=[synth.q4k_matrix(H, F, seed, 40 + l) for l in range(n_layers)],
+        w_head=synth.q4k_matrix(vocab, H, seed, 50),
+    )
+    return cfg, w
+
+
+def test_serial_greedy_equals_batched_verify():
+    cfg, w = tiny_model()
+    k = 7
+    hidden = synth.normal((k + 1, cfg.hidden), 0, 60)
+    kv0 = oracle.KV(cfg, num_pages=16, max_seq_pages=16)
+    kv0.extend(19)
+    for layer in range(cfg.n_layers):
+        _fill_kv(kv0, layer, 19, 70 + layer)
+    kv_s = kv0.copy()
+    serial, st = oracle.serial_greedy(cfg, w, kv_s, hidden, k)
+    assert st == 0
+    for L_t in (0, 3, k):
+        kv_b = kv0.copy()
+        draft = synth.plant_draft(serial, L_t, cfg.vocab, 0, 80 + L_t)
+        res, idx, lg, _ = oracle.verify_step(cfg, w, kv_b, hidden, draft)
+        assert list(res) == [L_t, serial[L_t], 0, 19 + L_t + 1]
+        assert np.array_equal(idx, serial)           # batched argmax == serial decode
+        kv_r = kv_s.copy()
+        kv_r.rollback(19 + L_t + 1)
+        a, b = kv_b.committed(), kv_r.committed()
+        assert a[0] == b[0] and all(np.array_equal(x, y) for x, y in zip(a[1:], b[1:]))
+        pages = kv_b.page_table[: (a[0] + 15) // 16]
+        for p_log, p_phys in enumerate(pages):
+            n_rows = min(16, a[0] - 16 * p_log)
+            assert np.array_equal(kv_b.pool[p_phys, :, :, :, :n_rows],
+                                  kv_r.pool[kv_r.page_table[p_log], :, :, :, :n_rows])
+
+
+def test_verify_step_rejects_bad_k_and_restores_on_device_errors():
+    cfg, w = tiny_model(n_layers=1)
+    kv = oracle.KV(cfg, num_pages=8, max_seq_pages=8)
+    kv.extend(5)
+    hidden = synth.normal((6, cfg.hidden), 0, 1)
+    with pytest.raises(ValueError):
+        oracle.verify_step(cfg, w, kv, hidden, np.zeros(5, dtype=np.int32))
+    hidden4 = hidden[:4]
+    snap = kv.committed()
+    bad = np.array([1, cfg.vocab, 2], dtype=np.int32)
+    res, _, _, _ = oracle.verify_step(cfg, w, kv, hidden4, bad)
+    assert res[2] == oracle.ST_TOKEN_RANGE and res[1] == -1
+    assert all(np.array_equal(a, b) for a, b in zip(snap[1:], kv.committed()[1:]))
+    h_nan = hidden4.copy()
+    h_nan[2, 7] = np.nan
+    res, _, _, _ = oracle.verify_step(cfg, w, kv, h_nan, np.array([1, 2, 3], dtype=np.int32))
+    assert res[2] & oracle.ST_NONFINITE and res[3] == 5
+    assert all(np.array_equal(a, b) for a, b in zip(snap[1:], kv.committed()[1:]))

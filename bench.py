@@ -1,0 +1,431 @@
+"""Benchmark of the exact greedy verify step on GB300.
+
+One step = one spec_verify_step (k = 15, 16 rows) of the full synthetic target:
+52 Q4_K blocks at hidden 6656 (QKV 6656->7680, O 6656->6656, gate|up
+6656->2x17920, down 17920->6656), LM head 6656->131072, KV context 2048 bf16,
+argmax, accept and KV rollback — followed by a metadata rollback to the same
+context so every timed step sees the same depth.  Weights (13.75 GB) are far
+larger than L2, so nothing is served from cache between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Prints one JSON line.  --impl reference times the CPU oracle on a bounded
+sample of the same step on the host cores (the oracle is the only reference
+this method has).  With N > 1 (torchrun) each rank runs an independent replica
+(the step has no exchange); the whole-job value sums them and timing is the
+max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verify steps/s and weight GB/s (% of GB300 HBM roofline) at k+1=16 rows"
+CTX = 2048
+K_DRAFT = 15
+ROWS = K_DRAFT + 1
+
+
+def full_cfg():
+    from speculative_decoding_exact_gb300 import runtime, synth
+    return runtime.ModelConfig(**synth.FULL)
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def gemm_algorithmic_bytes(cfg):
+    """Per step: weights N*K*0.5625 + fp32 inputs M*K*4 + fp32 outputs M*N*4 of every GEMM."""
+    tot = 0
+    launches = 0
+    mats = [(N, K) for _, N, K in cfg.matrices()] * cfg.n_layers + [(cfg.vocab, cfg.hidden)]
+    for N, K in mats:
+        tot += N * (K // 256) * 144 + ROWS * K * 4 + ROWS * N * 4
+        launches += 1
+    return tot, launches
+
+
+def kv_read_bytes(cfg, ctx):
+    return cfg.n_layers * 2 * cfg.n_kv_heads * cfg.head_dim * 2 * (ctx + ROWS)
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+class Clocks:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.p = None
+
+    def start(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                       "--format=csv,noheader,nounits", "-lms", "200"],
+                                      stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.p.terminate()
+        try:
+            self.p.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.p.kill()
+        self.f.flush()
+        rows = [r.split(",") for r in open(self.f.name).read().strip().splitlines() if r.strip()]
+        os.unlink(self.f.name)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [x.strip() for x in r]
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except (ValueError, IndexError):
+                continue
+            for nm, v in zip(names, r[5:9]):
+                if v.lower() in ("active", "1", "yes"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle sample (cpu_baseline and --impl reference)
+# ---------------------------------------------------------------------------
+class OracleSample:
+    """A bounded sample of the same step through the oracle on one host core:
+    1/COLF of the columns of each block GEMM of one layer (16 rows, full K),
+    the layer's full attention at context 2048, 1/HEADF of the head columns.
+    Extrapolated: step = 52 * (COLF * t_gemms + t_attn) + HEADF * t_head."""
+    COLF, HEADF = 16, 128
+
+    def __init__(self, cfg):
+        import oracle
+        from speculative_decoding_exact_gb300 import synth
+        self.oracle, self.cfg = oracle, cfg
+        H = cfg.hidden
+        self.mats = []
+        for j, (name, N, K) in enumerate(cfg.matrices()):
+            n = N // self.COLF
+            self.mats.append((synth.q4k_matrix(n, K, 0, 1000 * 0 + j), n, K))
+        self.head = synth.q4k_matrix(cfg.vocab // self.HEADF, H, 0, 999999)
+        self.x_h = synth.normal((ROWS, H), 0, 5)
+        self.x_f = synth.normal((ROWS, cfg.ffn), 0, 6)
+        ocfg = oracle.Config(hidden=H, n_layers=1, n_q_heads=cfg.n_q_heads, n_kv_heads=cfg.n_kv_heads,
+                             head_dim=cfg.head_dim, ffn=cfg.ffn, vocab=cfg.vocab)
+        self.kv = oracle.KV(ocfg, (CTX + ROWS) // 16 + 1, (CTX + ROWS) // 16 + 1)
+        self.kv.extend(CTX + ROWS)
+        nkv = cfg.n_kv_heads * cfg.head_dim
+        kb = synth.bf16_bits(synth.normal((CTX + ROWS, nkv), 0, 7))
+        vb = synth.bf16_bits(synth.normal((CTX + ROWS, nkv), 0, 8))
+        for p in range(CTX + ROWS):
+            pg, sl = self.kv.page_table[p // 16], p % 16
+            self.kv.pool[pg, 0, 0, :, sl] = kb[p].reshape(cfg.n_kv_heads, cfg.head_dim)
+            self.kv.pool[pg, 0, 1, :, sl] = vb[p].reshape(cfg.n_kv_heads, cfg.head_dim)
+        self.q = synth.normal((ROWS, cfg.n_q_heads, cfg.head_dim), 0, 9)
+
+    def run(self):
+        o, t = self.oracle, time.perf_counter
+        t0 = t()
+        xn = o.rmsnorm(self.x_h, None, 1e-6)
+        for W, n, K in self.mats:
+            o.linear(W, n, K, xn if K == self.cfg.hidden else self.x_f)
+        t1 = t()
+        self.kv.attention(0, self.q, CTX)
+        t2 = t()
+        o.linear(self.head, self.cfg.vocab // self.HEADF, self.cfg.hidden, xn)
+        t3 = t()
+        step_s = self.cfg.n_layers * (self.COLF * (t1 - t0) + (t2 - t1)) + self.HEADF * (t3 - t2)
+        return step_s, t3 - t0
+
+    def describe(self):
+        return (f"oracle on 1 host core: one layer's block GEMMs on 1/{self.COLF} of their columns "
+                f"(16 rows, full K), that layer's attention at context {CTX}, 1/{self.HEADF} of the "
+                f"LM-head columns; extrapolated x52 layers, x{self.COLF} columns, x{self.HEADF} head")
+
+
+def cpu_baseline(cfg, min_seconds=10.0):
+    s = OracleSample(cfg)
+    times, spent = [], 0.0
+    while spent < min_seconds:
+        step_s, wall = s.run()
+        times.append(step_s)
+        spent += wall
+    return {"value": 1.0 / statistics.median(times), "unit": "verify steps/s", "cores": 1,
+            "kind": "oracle", "sample": s.describe() + f"; {len(times)} samples"}
+
+
+def run_reference(args, rank, world):
+    cfg = full_cfg()
+    if rank != 0:
+        return
+    s = OracleSample(cfg)
+    for _ in range(args.warmup):
+        s.run()
+    steps = []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        steps.append(s.run()[0])
+    wall = time.perf_counter() - t0
+    v = 1.0 / statistics.mean(steps)
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "verify steps/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1000.0 / v, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "int8xint4 dot, f32 combine", "data": "synthetic",
+            "config": workload_config(cfg),
+            "cpu_baseline": {"value": v, "unit": "verify steps/s", "cores": 1, "kind": "oracle",
+                             "sample": s.describe()},
+            "e2e": {"value": v, "unit": "verify steps/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "sample_wall_s": wall}
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(cfg):
+    return {"workload": f"full synthetic verify pass: 52 Q4_K blocks hidden 6656 + LM head 131072, "
+                        f"k+1=16 rows, KV context {CTX} bf16",
+            "layers": cfg.n_layers, "hidden": cfg.hidden, "ffn": cfg.ffn, "vocab": cfg.vocab,
+            "q_heads": cfg.n_q_heads, "kv_heads": cfg.n_kv_heads, "rows": ROWS, "context": CTX,
+            "weight_bytes": cfg.weight_bytes(),
+            "l2": "inputs larger than L2 (13.75 GB of weights streamed per step)",
+            "parallelism": "replicas"}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+def kernel_source_sha():
+    h = hashlib.sha256()
+    for f in ("gemm.cu", "common.cuh", "internal.h"):
+        h.update(open(os.path.join(ROOT, "speculative_decoding_exact_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic():
+    """Per-launch DRAM bytes of the GEMM kernel from the committed ncu summary,
+    scaled to a full-model step; None if the kernel changed since the capture."""
+    p = os.path.join(ROOT, "profiles", "gemm_q4k_ncu_traffic.txt")
+    if not os.path.exists(p):
+        return None
+    kv = {}
+    for line in open(p):
+        if ":" in line and not line.startswith("#"):
+            a, b = line.split(":", 1)
+            kv[a.strip()] = b.strip()
+    if kv.get("kernel_source_sha") != kernel_source_sha():
+        return None
+    try:
+        return float(kv["traffic_bytes_per_average_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def run_gpu(args, rank, world):
+    import torch
+
+    from speculative_decoding_exact_gb300 import abi, runtime, synth
+    from speculative_decoding_exact_gb300 import build as b
+
+    b.build()
+    local = int(os.environ.get("LOCAL_RANK", 0))
+    torch.cuda.set_device(local)
+    cfg = full_cfg()
+    stream = torch.cuda.Stream()
+    torch.cuda.set_stream(stream)
+    max_ctx = CTX + 64
+    ctx = runtime.Context(cfg, max_ctx=max_ctx, stream=stream)
+    pages = max_ctx // 16
+    t_setup = time.perf_counter()
+    dw = runtime.DeviceWeights(cfg)
+    for l in range(cfg.n_layers):
+        for j, (name, N, K) in enumerate(cfg.matrices()):
+            getattr(dw, name).append(runtime.upload_tiled(ctx, synth.q4k_matrix(N, K, rank, 1000 * l + j),
+                                                          N, K))
+    dw.w_head = runtime.upload_tiled(ctx, synth.q4k_matrix(cfg.vocab, cfg.hidden, rank, 999999),
+                                     cfg.vocab, cfg.hidden)
+    kv = runtime.DeviceKV(cfg, pages, pages)
+    kv.reset(ctx)
+    kv.extend(ctx, CTX)
+    nkv = cfg.n_kv_heads * cfg.head_dim
+    g = torch.Generator(device="cuda").manual_seed(1234 + rank)
+    with torch.cuda.stream(stream):
+        kv.pool.copy_(torch.randn(kv.pool.shape, generator=g, device="cuda").to(torch.bfloat16))
+    hidden = torch.from_numpy(synth.normal((ROWS, cfg.hidden), rank, 5)).cuda()
+    draft = torch.from_numpy(synth.tokens(K_DRAFT, cfg.vocab, rank, 6)).cuda()
+    res = torch.zeros(4, dtype=torch.int32, device="cuda")
+    ws, ks = dw.struct(), kv.struct()
+    torch.cuda.synchronize()
+    setup_s = time.perf_counter() - t_setup
+
+    def step():
+        rc = abi.spec_verify_step(ctx.h, ws, ks, hidden.data_ptr(), draft.data_ptr(), K_DRAFT,
+                                  res.data_ptr())
+        if rc != 0:
+            raise abi.SpecError("spec_verify_step", rc)
+        abi.check("spec_kv_rollback", abi.spec_kv_rollback(ctx.h, ks, CTX))
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    r = res.cpu().numpy()
+    assert r[2] == 0, f"step status {r[2]}"
+    launches = abi.spec_last_step_launches(ctx.h) + 1
+
+    dist = world > 1
+    if dist:
+        import torch.distributed as tdist
+    clocks = Clocks(local)
+    clocks.start()
+    if dist:
+        tdist.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.nvtx.range_push("timed")
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    torch.cuda.nvtx.range_pop()
+    if dist:
+        tdist.barrier()
+    ms = e0.elapsed_time(e1)
+    clk = clocks.stop()
+    if dist:
+        t = torch.tensor([ms], device="cuda")
+        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_per_step = ms / args.steps
+    steps_per_s = 1000.0 / ms_per_step * world
+
+    # GEMM kernel timing: CUDA events around every GEMM launch of the same steps
+    gemm_ms, gemm_launches = profile_gemms(ctx, abi, torch, stream, ws, ks, hidden, draft, res,
+                                           args.steps)
+    gbytes, glaunch = gemm_algorithmic_bytes(cfg)
+    peak, peak_kind = measured_peaks()
+    achieved = gbytes / (gemm_ms * 1e-3) / 1e9 if gemm_ms else None
+    traffic = committed_traffic()
+
+    # end to end through the host-buffer entry point
+    hid_h = torch.from_numpy(synth.normal((ROWS, cfg.hidden), rank, 5)).pin_memory()
+    dr_h = torch.from_numpy(synth.tokens(K_DRAFT, cfg.vocab, rank, 6)).pin_memory()
+    res_h = abi.spec_result()
+    for _ in range(2):
+        abi.check("spec_verify_step_host", abi.spec_verify_step_host(ctx.h, ws, ks, hid_h.data_ptr(),
+                                                                     dr_h.data_ptr(), K_DRAFT, res_h))
+        abi.spec_kv_rollback(ctx.h, ks, CTX)
+    torch.cuda.synchronize()
+    if dist:
+        tdist.barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        abi.check("spec_verify_step_host", abi.spec_verify_step_host(ctx.h, ws, ks, hid_h.data_ptr(),
+                                                                     dr_h.data_ptr(), K_DRAFT, res_h))
+        abi.spec_kv_rollback(ctx.h, ks, CTX)
+    torch.cuda.synchronize()
+    e2e_s = time.perf_counter() - t0
+    if dist:
+        t = torch.tensor([e2e_s], device="cuda")
+        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    e2e = args.steps / e2e_s * world
+
+    if rank != 0:
+        ctx.close()
+        return
+    wb = cfg.weight_bytes()
+    line = {
+        "metric": METRIC, "value": steps_per_s, "unit": "verify steps/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "int8xint4 dot on f16 tensor cores (exact ints), f32 combine", "data": "synthetic",
+        "config": workload_config(cfg),
+        "weight_gbs": wb * steps_per_s / world / 1e9,
+        "weight_frac_of_hbm": {"measured": wb * steps_per_s / world / 1e9 / peak, "peak_gbs": peak,
+                               "spec_8tbs": wb * steps_per_s / world / 1e9 / 8000.0},
+        "total_gbs": (wb + kv_read_bytes(cfg, CTX)) * steps_per_s / world / 1e9,
+        "roofline": {"kernel": "gemm_q4k_kernel (all Q4_K GEMM launches of a step)",
+                     "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": (achieved / peak) if achieved else None, "peak_kind": peak_kind,
+                     "traffic": traffic, "launches_per_step": glaunch,
+                     "avg_launch_us": gemm_ms * 1e3 / glaunch if gemm_ms else None,
+                     "algorithmic_bytes_per_launch": gbytes / glaunch},
+        "cpu_baseline": cpu_baseline(cfg) if world == 1 or rank == 0 else None,
+        "e2e": {"value": e2e, "unit": "verify steps/s",
+                "h2d_bytes_per_step": ROWS * cfg.hidden * 4 + K_DRAFT * 4,
+                "d2h_bytes_per_step": 16},
+        "gpu_launches": launches * args.steps,
+        "clocks": clk,
+        "setup_s": setup_s,
+        "accepted_len_last": int(r[0]),
+    }
+    print(json.dumps(line), flush=True)
+    ctx.close()
+
+
+def profile_gemms(ctx, abi, torch, stream, ws, ks, hidden, draft, res, steps):
+    """Same steps with CUDA events recorded around each GEMM launch on the ctx
+    stream; returns (total GEMM ms per step, GEMM launches per step)."""
+    abi.check("spec_profile_gemms", abi.spec_profile_gemms(ctx.h, 1))
+    tot, n = 0.0, 0
+    for _ in range(steps):
+        abi.check("spec_verify_step", abi.spec_verify_step(ctx.h, ws, ks, hidden.data_ptr(),
+                                                           draft.data_ptr(), K_DRAFT, res.data_ptr()))
+        abi.check("spec_kv_rollback", abi.spec_kv_rollback(ctx.h, ks, CTX))
+        ms, n = abi.spec_profile_read(ctx.h)
+        tot += ms
+    abi.check("spec_profile_gemms", abi.spec_profile_gemms(ctx.h, 0))
+    return tot / steps, n
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as tdist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        tdist.init_process_group("nccl" if args.impl == "ours" else "gloo")
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_gpu(args, rank, world)
+    if world > 1:
+        import torch.distributed as tdist
+        tdist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

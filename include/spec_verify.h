@@ -73,6 +73,12 @@
 #include <stdint.h>
 #include <stddef.h>
 
+#if defined(__GNUC__)
+#define SPEC_API __attribute__((visibility("default")))
+#else
+#define SPEC_API
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -175,16 +181,16 @@ typedef struct spec_ctx spec_ctx;
 /* Create a context on the current device.  Allocates the workspace sized by
  * cfg and binds `cuda_stream` (a cudaStream_t; NULL = legacy default stream).
  * Returns SPEC_OK and *out, or a negative code and *out = NULL. */
-int spec_verify_init(const spec_config* cfg, void* cuda_stream, spec_ctx** out);
+SPEC_API int spec_verify_init(const spec_config* cfg, void* cuda_stream, spec_ctx** out);
 
 /* Release the workspace.  Synchronises the ctx stream first.  NULL is a no-op. */
-void spec_verify_destroy(spec_ctx* ctx);
+SPEC_API void spec_verify_destroy(spec_ctx* ctx);
 
 /* Rebind the stream used by subsequent calls. */
-int spec_set_stream(spec_ctx* ctx, void* cuda_stream);
+SPEC_API int spec_set_stream(spec_ctx* ctx, void* cuda_stream);
 
 /* Human-readable text for a return code. */
-const char* spec_strerror(int code);
+SPEC_API const char* spec_strerror(int code);
 
 /* One exact greedy verify step (Ch. 33 §33.2 and §33.7; Ch. 8 §8.6).
  *   hidden  DEVICE fp32 [k+1][H]: residual-stream rows entering layer 0; row 0
@@ -202,12 +208,12 @@ const char* spec_strerror(int code);
  * On a device error nothing is committed: seq_len, the page table and the free
  * stack are restored to their values before the step and res->status != 0.
  * No host synchronisation and no allocation happen inside. */
-int spec_verify_step(spec_ctx* ctx, const spec_weights* w, spec_kv* kv,
+SPEC_API int spec_verify_step(spec_ctx* ctx, const spec_weights* w, spec_kv* kv,
                      const float* hidden, const int32_t* draft, int k,
                      spec_result* res);
 
 /* spec_verify_step plus optional debug taps (taps may be NULL). */
-int spec_verify_step_ex(spec_ctx* ctx, const spec_weights* w, spec_kv* kv,
+SPEC_API int spec_verify_step_ex(spec_ctx* ctx, const spec_weights* w, spec_kv* kv,
                         const float* hidden, const int32_t* draft, int k,
                         spec_result* res, const spec_taps* taps);
 
@@ -215,50 +221,58 @@ int spec_verify_step_ex(spec_ctx* ctx, const spec_weights* w, spec_kv* kv,
  * int32 from host memory (pinned for overlap) to the ctx workspace, runs the
  * step, copies the spec_result back to *res_host, and synchronises the
  * stream before returning. */
-int spec_verify_step_host(spec_ctx* ctx, const spec_weights* w, spec_kv* kv,
+SPEC_API int spec_verify_step_host(spec_ctx* ctx, const spec_weights* w, spec_kv* kv,
                           const float* hidden_host, const int32_t* draft_host,
                           int k, spec_result* res_host);
 
 /* Number of kernels the last spec_verify_step enqueued (for accounting). */
-int spec_last_step_launches(const spec_ctx* ctx);
+SPEC_API int spec_last_step_launches(const spec_ctx* ctx);
+
+/* Timing of the Q4_K GEMM launches of subsequent steps: with enable != 0 the
+ * step records a CUDA event pair around each GEMM launch on the ctx stream
+ * (events are created here, not in the step).  spec_profile_read synchronises
+ * the stream and returns the summed GEMM time of the last step (ms) and the
+ * number of GEMM launches it made. */
+SPEC_API int spec_profile_gemms(spec_ctx* ctx, int enable);
+SPEC_API int spec_profile_read(spec_ctx* ctx, float* gemm_ms, int* gemm_launches);
 
 /* ---- KV cache management (Ch. 8 §8.6 item 4: metadata-only rewind) ------- */
 
 /* Reset a KV cache to empty: seq_len = 0, page_table = -1, free_stack filled
  * descending (id num_pages-1 at the bottom) so that pops yield ids 0, 1, 2...
  * Requires num_pages <= 2^30. */
-int spec_kv_reset(spec_ctx* ctx, spec_kv* kv);
+SPEC_API int spec_kv_reset(spec_ctx* ctx, spec_kv* kv);
 
 /* Map pages for positions [seq_len, seq_len + n) and set seq_len += n.  Used to
  * lay down a prefilled context; the caller writes those rows' bytes.  Device
  * errors (pool empty, page table full) leave the state unchanged and set the
  * ctx status word. */
-int spec_kv_extend(spec_ctx* ctx, spec_kv* kv, int32_t n);
+SPEC_API int spec_kv_extend(spec_ctx* ctx, spec_kv* kv, int32_t n);
 
 /* Roll the committed length back to new_len (0 <= new_len <= seq_len, checked
  * on the device; violations set SPEC_ST_ROLLBACK in the ctx status word and
  * change nothing).  Logical pages p with 16p >= new_len are unmapped and their
  * ids pushed on the free stack from the highest p down, so re-extending maps
  * the same ids to the same pages again.  Retained rows are untouched. */
-int spec_kv_rollback(spec_ctx* ctx, spec_kv* kv, int32_t new_len);
+SPEC_API int spec_kv_rollback(spec_ctx* ctx, spec_kv* kv, int32_t new_len);
 
 /* Read (synchronously) and clear the ctx status word set by the entry points
  * that have no spec_result.  Returns SPEC_ST_* bits, or a negative code. */
-int spec_last_status(spec_ctx* ctx);
+SPEC_API int spec_last_status(spec_ctx* ctx);
 
 /* ---- building blocks, exposed for parity tests and benchmarks ------------ */
 
 /* One-time weight repack: canonical Q4_K (DEVICE, N x K/256 superblocks) ->
  * TILED Q4_K (DEVICE, same size).  N % 16 == 0, K % 256 == 0.  src and dst
  * must not overlap.  Deterministic permutation of bytes, no arithmetic. */
-int spec_weights_repack(spec_ctx* ctx, const void* src_canonical, void* dst_tiled,
+SPEC_API int spec_weights_repack(spec_ctx* ctx, const void* src_canonical, void* dst_tiled,
                         int N, int K);
 
 /* Activation quantisation of x (DEVICE fp32 [M][K]) exactly as described at
  * the top of this file, written in plain layout: q int8 [M][K], d_a fp32
  * [M][K/256], A int32 [M][K/32].  M <= 16, K % 256 == 0.  Non-finite input
  * sets SPEC_ST_NONFINITE in the ctx status word. */
-int spec_quantize_q8(spec_ctx* ctx, const float* x, int M, int K,
+SPEC_API int spec_quantize_q8(spec_ctx* ctx, const float* x, int M, int K,
                      int8_t* q, float* d_a, int32_t* A);
 
 /* y = W x for M rows: quantise x (DEVICE fp32 [M][K]) per 256-block, run the
@@ -266,12 +280,12 @@ int spec_quantize_q8(spec_ctx* ctx, const float* x, int M, int K,
  * fp32 [M][N]).  1 <= M <= 16, N % 16 == 0, K % 256 == 0, N*K within the
  * workspace built for cfg (largest of the model's matrices).  Row i of y is
  * bit-identical for every M >= i+1. */
-int spec_gemm_q4k(spec_ctx* ctx, const void* w_tiled, int N, int K,
+SPEC_API int spec_gemm_q4k(spec_ctx* ctx, const void* w_tiled, int N, int K,
                   const float* x, int M, float* y);
 
 /* Same GEMM, also writing the exact integer sums ISc and IMn (DEVICE int32
  * [M][N][K/256] each) of every (row, column, superblock). */
-int spec_gemm_q4k_sums(spec_ctx* ctx, const void* w_tiled, int N, int K,
+SPEC_API int spec_gemm_q4k_sums(spec_ctx* ctx, const void* w_tiled, int N, int K,
                        const float* x, int M, float* y,
                        int32_t* isc, int32_t* imn);
 
@@ -280,7 +294,7 @@ int spec_gemm_q4k_sums(spec_ctx* ctx, const void* w_tiled, int N, int K,
  * x DEVICE fp32 [M][H]; idx DEVICE int32 [M]; logits DEVICE fp32 [M][V] or
  * NULL (the fused path writes no logits).  Non-finite logits set
  * SPEC_ST_NONFINITE in the ctx status word. */
-int spec_lm_head_argmax(spec_ctx* ctx, const void* w_head_tiled,
+SPEC_API int spec_lm_head_argmax(spec_ctx* ctx, const void* w_head_tiled,
                         const float* final_norm, const float* x, int M,
                         int32_t* idx, float* logits);
 
@@ -289,7 +303,7 @@ int spec_lm_head_argmax(spec_ctx* ctx, const void* w_head_tiled,
  * positions 0..p_i of row i.  q DEVICE fp32 [M][n_q_heads][head_dim]; out
  * DEVICE fp32 [M][n_q_heads*head_dim].  s = q.k/sqrt(head_dim), softmax over
  * the visible positions, o = sum p v; K and V read as bf16. */
-int spec_attention(spec_ctx* ctx, const spec_kv* kv, int layer,
+SPEC_API int spec_attention(spec_ctx* ctx, const spec_kv* kv, int layer,
                    const float* q, int M, float* out);
 
 /* Greedy accept + rollback alone (the last kernel of a step).
@@ -300,7 +314,7 @@ int spec_attention(spec_ctx* ctx, const spec_kv* kv, int layer,
  * Writes res (DEVICE).  Accept rule: Ch. 33 §33.2 with one-hot target and
  * draft distributions: p/q = 1 where draft == argmax (accept with certainty),
  * p = 0 elsewhere (reject), residual max(p - q, 0) one-hot at the argmax. */
-int spec_accept(spec_ctx* ctx, const int32_t* idx, const int32_t* draft, int k,
+SPEC_API int spec_accept(spec_ctx* ctx, const int32_t* idx, const int32_t* draft, int k,
                 spec_kv* kv, spec_result* res);
 
 #ifdef __cplusplus

@@ -152,23 +152,26 @@ int orc_quantize_q8(const float* x, int M, int K, int8_t* q, float* d_a, int32_t
 void orc_gemm_q4k(const uint8_t* W, int N, int K, const int8_t* q, const float* d_a,
                   const int32_t* A, int M, float* y, int32_t* isc, int32_t* imn, float* vb) {
     int nb = K / 256;
-    for (int m = 0; m < M; ++m) {
-        for (int n = 0; n < N; ++n) {
-            double acc = 0.0;
-            for (int b = 0; b < nb; ++b) {
-                const uint8_t* sb = W + ((size_t)n * nb + b) * 144;
+    double* acc = (double*)malloc(sizeof(double) * (size_t)M);
+    for (int n = 0; n < N; ++n) {
+        for (int m = 0; m < M; ++m) acc[m] = 0.0;
+        for (int b = 0; b < nb; ++b) {
+            /* decode the superblock once: codes, sub-scales, sub-mins, d, dmin */
+            const uint8_t* sb = W + ((size_t)n * nb + b) * 144;
+            int code[256], sc[8], mn[8];
+            for (int j = 0; j < 8; ++j) orc_q4k_scale_min(sb, j, &sc[j], &mn[j]);
+            for (int e = 0; e < 256; ++e) code[e] = orc_q4k_code(sb, e);
+            float d = orc_half_to_float(rd16(sb));
+            float dmin = orc_half_to_float(rd16(sb + 2));
+            for (int m = 0; m < M; ++m) {
                 const int8_t* qa = q + (size_t)m * K + 256 * b;
                 int32_t ISc = 0, IMn = 0;
                 for (int j = 0; j < 8; ++j) {
-                    int sc, mn;
-                    orc_q4k_scale_min(sb, j, &sc, &mn);
                     int32_t S = 0;
-                    for (int i = 0; i < 32; ++i) S += orc_q4k_code(sb, 32 * j + i) * qa[32 * j + i];
-                    ISc += sc * S;
-                    IMn += mn * A[(size_t)m * (K / 32) + 8 * b + j];
+                    for (int i = 0; i < 32; ++i) S += code[32 * j + i] * qa[32 * j + i];
+                    ISc += sc[j] * S;
+                    IMn += mn[j] * A[(size_t)m * (K / 32) + 8 * b + j];
                 }
-                float d = orc_half_to_float(rd16(sb));
-                float dmin = orc_half_to_float(rd16(sb + 2));
                 float t1 = d * (float)ISc;
                 float t2 = dmin * (float)IMn;
                 float diff = t1 - t2;
@@ -177,11 +180,12 @@ void orc_gemm_q4k(const uint8_t* W, int N, int K, const int8_t* q, const float* 
                 if (isc) isc[o] = ISc;
                 if (imn) imn[o] = IMn;
                 if (vb) vb[o] = v;
-                acc += (double)v;
+                acc[m] += (double)v;                 /* superblock order, per (m, n) */
             }
-            y[(size_t)m * N + n] = (float)acc;
         }
+        for (int m = 0; m < M; ++m) y[(size_t)m * N + n] = (float)acc[m];
     }
+    free(acc);
 }
 
 int orc_linear(const uint8_t* W, int N, int K, const float* x, int M, float* y) {

@@ -1,0 +1,584 @@
+// api.cu — the C ABI of include/spec_verify.h: context and workspace, host-side
+// validation (everything is checked before anything is enqueued), and the
+// orchestration of one verify step as a fixed sequence of kernel launches on
+// one stream with programmatic dependent launch between them.
+//
+// Step (Muser book Ch. 33 §33.1-§33.2 and §33.7; Ch. 8 §8.6):
+//   reserve pages for the k+1 block (validates the draft tokens first)
+//   per layer: RMSNorm+Q8 -> QKV GEMM -> split Q / append K,V (bf16) ->
+//              attention partials -> merge+Q8 -> O GEMM -> residual+RMSNorm+Q8
+//              -> gate|up GEMM -> SwiGLU+Q8 -> down GEMM -> residual+RMSNorm+Q8
+//   LM head GEMM -> per-row argmax -> accept + rollback
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include "../../include/spec_verify.h"
+#include "common.cuh"
+#include "internal.h"
+
+using namespace spec;
+
+struct spec_ctx {
+  spec_config cfg;
+  cudaStream_t stream = nullptr;
+  int num_sms = 0;
+  GemmPlan p_qkv, p_o, p_gu, p_down, p_head;
+  AttnPlan attn;
+  size_t act_bytes = 0, pieces_floats = 0;
+  uint8_t* act = nullptr;
+  float* pieces = nullptr;
+  float* resid = nullptr;        // [16][H]
+  uint8_t* qfrag = nullptr;      // attention query fragments, nq * 8 KB
+  float* attn_part = nullptr;
+  float* head_val = nullptr;     // [nparts][16]
+  int32_t* head_idx = nullptr;
+  int head_parts = 0;
+  int32_t* status = nullptr;     // device status word
+  int32_t* step_state = nullptr; // [2]
+  int32_t* idx_buf = nullptr;    // [16]
+  float* hidden_dev = nullptr;   // host-buffer entry point staging
+  int32_t* draft_dev = nullptr;
+  spec_result* res_dev = nullptr;
+  int last_launches = 0;
+  // optional GEMM timing
+  bool profile = false;
+  int prof_n = 0;
+  cudaEvent_t* prof_ev = nullptr;   // 2 per GEMM launch
+  int prof_cap = 0;
+  // recorded steps: a step is replayed as a CUDA graph when every pointer and
+  // size it bakes into its launches is unchanged
+  struct GraphEntry {
+    uint64_t key = 0;
+    cudaGraphExec_t exec = nullptr;
+    int launches = 0;
+    uint64_t used = 0;
+  };
+  GraphEntry graphs[4];
+  uint64_t graph_clock = 0;
+  bool use_graphs = true;
+};
+
+namespace {
+
+constexpr int kAlign = 16;
+
+bool aligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) % kAlign) == 0; }
+
+int cuda_code(cudaError_t e) { return e == cudaSuccess ? SPEC_OK : SPEC_ECUDA; }
+
+#define SPEC_TRY(expr)                         \
+  do {                                         \
+    cudaError_t _e = (expr);                   \
+    if (_e != cudaSuccess) return SPEC_ECUDA;  \
+  } while (0)
+
+size_t pieces_need(const GemmPlan& p) { return (size_t)p.max_slots * 16 * p.N; }
+
+KvView view_of(const spec_ctx* c, const spec_kv* kv) {
+  KvView v;
+  v.pool = static_cast<uint16_t*>(kv->pool);
+  v.page_table = kv->page_table;
+  v.seq_len = kv->seq_len;
+  v.free_stack = kv->free_stack;
+  v.free_top = kv->free_top;
+  v.num_pages = kv->num_pages;
+  v.max_seq_pages = kv->max_seq_pages;
+  v.n_layers = c->cfg.n_layers;
+  v.n_kv = c->cfg.n_kv_heads;
+  v.head_dim = c->cfg.head_dim;
+  v.page_size = c->cfg.page_size;
+  return v;
+}
+
+int check_kv(const spec_kv* kv) {
+  if (!kv || !kv->pool || !kv->page_table || !kv->seq_len || !kv->free_stack || !kv->free_top)
+    return SPEC_ENULL;
+  if (kv->num_pages <= 0 || kv->max_seq_pages <= 0 || kv->num_pages > (1 << 30)) return SPEC_EINVAL;
+  if (!aligned(kv->pool)) return SPEC_EALIGN;
+  return SPEC_OK;
+}
+
+int check_cfg(const spec_config* c) {
+  if (!c) return SPEC_ENULL;
+  if (c->hidden <= 0 || c->hidden % 256 || c->hidden / 256 > 64) return SPEC_EINVAL;
+  if (c->ffn <= 0 || c->ffn % 256) return SPEC_EINVAL;
+  if (c->head_dim != 128 || c->page_size != 16) return SPEC_EINVAL;
+  if (c->n_q_heads <= 0 || c->n_kv_heads <= 0 || c->n_q_heads % c->n_kv_heads) return SPEC_EINVAL;
+  if (c->n_q_heads / c->n_kv_heads > 13) return SPEC_EINVAL;
+  if (c->n_q_heads * c->head_dim != c->hidden) return SPEC_EINVAL;
+  if (c->n_layers <= 0 || c->vocab <= 0 || c->vocab % 16) return SPEC_EINVAL;
+  if (c->max_rows < 1 || c->max_rows > 16) return SPEC_EINVAL;
+  if (c->max_ctx < c->max_rows) return SPEC_EINVAL;
+  if (!(c->rms_eps >= 0.f)) return SPEC_EINVAL;
+  return SPEC_OK;
+}
+
+template <class T>
+int dalloc(T** p, size_t n) {
+  if (n == 0) n = 1;
+  return cudaMalloc(reinterpret_cast<void**>(p), n * sizeof(T)) == cudaSuccess ? SPEC_OK : SPEC_ENOMEM;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* spec_strerror(int code) {
+  switch (code) {
+    case SPEC_OK: return "ok";
+    case SPEC_EINVAL: return "invalid argument or geometry";
+    case SPEC_EVERIFYLEN: return "verify length k must be 3, 7 or 15";
+    case SPEC_ENULL: return "required pointer is NULL";
+    case SPEC_EALIGN: return "pointer not 16-byte aligned";
+    case SPEC_ENOMEM: return "workspace allocation failed";
+    case SPEC_ECAPACITY: return "request exceeds workspace or cache capacity";
+    case SPEC_ECUDA: return "CUDA runtime error";
+    case SPEC_ENODEV: return "no sm_103 device is current";
+    default: return "unknown error";
+  }
+}
+
+int spec_verify_init(const spec_config* cfg, void* cuda_stream, spec_ctx** out) {
+  if (!out) return SPEC_ENULL;
+  *out = nullptr;
+  int rc = check_cfg(cfg);
+  if (rc) return rc;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SPEC_ENODEV;
+  int major = 0, minor = 0, sms = 0;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (major != 10 || minor != 3) return SPEC_ENODEV;
+
+  spec_ctx* c = new (std::nothrow) spec_ctx();
+  if (!c) return SPEC_ENOMEM;
+  c->cfg = *cfg;
+  c->stream = static_cast<cudaStream_t>(cuda_stream);
+  c->num_sms = sms;
+  const int H = cfg->hidden, F = cfg->ffn, V = cfg->vocab;
+  const int nqkv = (cfg->n_q_heads + 2 * cfg->n_kv_heads) * cfg->head_dim;
+  c->p_qkv = make_gemm_plan(nqkv, H, sms);
+  c->p_o = make_gemm_plan(H, H, sms);
+  c->p_gu = make_gemm_plan(2 * F, H, sms);
+  c->p_down = make_gemm_plan(H, F, sms);
+  c->p_head = make_gemm_plan(V, H, sms);
+  c->attn = make_attn_plan(cfg->n_q_heads, cfg->n_kv_heads, cfg->head_dim, cfg->max_ctx);
+  size_t pf = 0;
+  for (const GemmPlan* p : {&c->p_qkv, &c->p_o, &c->p_gu, &c->p_down, &c->p_head})
+    if (pieces_need(*p) > pf) pf = pieces_need(*p);
+  c->pieces_floats = pf;
+  int kmax = H > F ? H : F;
+  if (5 * H > kmax) kmax = 5 * H;   // a draft front projection over 5 concatenated hidden rows
+  c->act_bytes = (size_t)(kmax / 256) * kActSBBytes;
+  c->head_parts = head_argmax_blocks(V);
+  rc = SPEC_OK;
+  rc |= dalloc(&c->act, c->act_bytes);
+  rc |= dalloc(&c->pieces, c->pieces_floats);
+  rc |= dalloc(&c->resid, (size_t)16 * H);
+  rc |= dalloc(&c->qfrag, qfrag_bytes(cfg->n_q_heads));
+  rc |= dalloc(&c->attn_part, attn_partial_floats(c->attn, 16));
+  rc |= dalloc(&c->head_val, (size_t)c->head_parts * 16);
+  rc |= dalloc(&c->head_idx, (size_t)c->head_parts * 16);
+  rc |= dalloc(&c->status, 4);
+  rc |= dalloc(&c->step_state, 4);
+  rc |= dalloc(&c->idx_buf, 16);
+  rc |= dalloc(&c->hidden_dev, (size_t)16 * H);
+  rc |= dalloc(&c->draft_dev, 16);
+  rc |= dalloc(&c->res_dev, 1);
+  if (rc != SPEC_OK) {
+    spec_verify_destroy(c);
+    return SPEC_ENOMEM;
+  }
+  if (gemm_init_attributes() != cudaSuccess) {
+    spec_verify_destroy(c);
+    return SPEC_ECUDA;
+  }
+  if (cudaMemsetAsync(c->status, 0, 16, c->stream) != cudaSuccess ||
+      cudaMemsetAsync(c->act, 0, c->act_bytes, c->stream) != cudaSuccess ||
+      cudaStreamSynchronize(c->stream) != cudaSuccess) {
+    spec_verify_destroy(c);
+    return SPEC_ECUDA;
+  }
+  *out = c;
+  return SPEC_OK;
+}
+
+void spec_verify_destroy(spec_ctx* c) {
+  if (!c) return;
+  cudaStreamSynchronize(c->stream);
+  for (int i = 0; i < c->prof_cap; ++i) cudaEventDestroy(c->prof_ev[i]);
+  free(c->prof_ev);
+  cudaFree(c->act);
+  cudaFree(c->pieces);
+  cudaFree(c->resid);
+  cudaFree(c->qfrag);
+  for (auto& gc : c->graphs)
+    if (gc.exec) cudaGraphExecDestroy(gc.exec);
+  cudaFree(c->attn_part);
+  cudaFree(c->head_val);
+  cudaFree(c->head_idx);
+  cudaFree(c->status);
+  cudaFree(c->step_state);
+  cudaFree(c->idx_buf);
+  cudaFree(c->hidden_dev);
+  cudaFree(c->draft_dev);
+  cudaFree(c->res_dev);
+  delete c;
+}
+
+int spec_set_stream(spec_ctx* c, void* cuda_stream) {
+  if (!c) return SPEC_ENULL;
+  c->stream = static_cast<cudaStream_t>(cuda_stream);
+  return SPEC_OK;
+}
+
+int spec_last_step_launches(const spec_ctx* c) { return c ? c->last_launches : SPEC_ENULL; }
+
+int spec_profile_gemms(spec_ctx* c, int enable) {
+  if (!c) return SPEC_ENULL;
+  if (enable && !c->prof_ev) {
+    const int cap = 2 * (4 * c->cfg.n_layers + 1);
+    c->prof_ev = static_cast<cudaEvent_t*>(calloc(cap, sizeof(cudaEvent_t)));
+    if (!c->prof_ev) return SPEC_ENOMEM;
+    for (int i = 0; i < cap; ++i)
+      if (cudaEventCreate(&c->prof_ev[i]) != cudaSuccess) return SPEC_ECUDA;
+    c->prof_cap = cap;
+  }
+  c->profile = enable != 0;
+  return SPEC_OK;
+}
+
+int spec_profile_read(spec_ctx* c, float* gemm_ms, int* gemm_launches) {
+  if (!c || !gemm_ms || !gemm_launches) return SPEC_ENULL;
+  if (cudaStreamSynchronize(c->stream) != cudaSuccess) return SPEC_ECUDA;
+  float tot = 0.f;
+  for (int i = 0; i < c->prof_n; ++i) {
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, c->prof_ev[2 * i], c->prof_ev[2 * i + 1]) != cudaSuccess)
+      return SPEC_ECUDA;
+    tot += ms;
+  }
+  *gemm_ms = tot;
+  *gemm_launches = c->prof_n;
+  return SPEC_OK;
+}
+
+int spec_last_status(spec_ctx* c) {
+  if (!c) return SPEC_ENULL;
+  int32_t v = 0;
+  if (cudaMemcpyAsync(&v, c->status, 4, cudaMemcpyDeviceToHost, c->stream) != cudaSuccess ||
+      cudaStreamSynchronize(c->stream) != cudaSuccess)
+    return SPEC_ECUDA;
+  if (cudaMemsetAsync(c->status, 0, 4, c->stream) != cudaSuccess) return SPEC_ECUDA;
+  return v;
+}
+
+// ---------------------------------------------------------------------------
+// building blocks
+// ---------------------------------------------------------------------------
+int spec_weights_repack(spec_ctx* c, const void* src, void* dst, int N, int K) {
+  if (!c || !src || !dst) return SPEC_ENULL;
+  if (N <= 0 || K <= 0 || N % 16 || K % 256) return SPEC_EINVAL;
+  const size_t bytes = (size_t)N * (K / 256) * 144;
+  const uint8_t* s = static_cast<const uint8_t*>(src);
+  const uint8_t* d = static_cast<const uint8_t*>(dst);
+  if (!(s + bytes <= d || d + bytes <= s)) return SPEC_EINVAL;
+  if (!aligned(src) || !aligned(dst)) return SPEC_EALIGN;
+  return cuda_code(launch_repack(src, dst, N, K, c->stream));
+}
+
+int spec_quantize_q8(spec_ctx* c, const float* x, int M, int K, int8_t* q, float* d_a, int32_t* A) {
+  if (!c || !x || !q || !d_a || !A) return SPEC_ENULL;
+  if (M < 1 || M > 16 || K <= 0 || K % 256) return SPEC_EINVAL;
+  if ((size_t)(K / 256) * kActSBBytes > c->act_bytes) return SPEC_ECAPACITY;
+  if (!aligned(x)) return SPEC_EALIGN;
+  return cuda_code(launch_quantize(x, M, K, c->act, q, d_a, A, c->status, c->stream, false));
+}
+
+static int gemm_common(spec_ctx* c, const void* w, int N, int K, const float* x, int M, float* y,
+                       int32_t* isc, int32_t* imn) {
+  if (!c || !w || !x || !y) return SPEC_ENULL;
+  if (M < 1 || M > 16 || N <= 0 || K <= 0 || N % 16 || K % 256) return SPEC_EINVAL;
+  if ((size_t)(K / 256) * kActSBBytes > c->act_bytes) return SPEC_ECAPACITY;
+  const GemmPlan p = make_gemm_plan(N, K, c->num_sms);
+  if (pieces_need(p) > c->pieces_floats) return SPEC_ECAPACITY;
+  if (!aligned(w) || !aligned(x)) return SPEC_EALIGN;
+  SPEC_TRY(launch_quantize(x, M, K, c->act, nullptr, nullptr, nullptr, c->status, c->stream, false));
+  SPEC_TRY(launch_gemm(p, w, c->act, c->pieces, isc, imn, M, c->stream, true));
+  SPEC_TRY(launch_sum_pieces(p, c->pieces, y, M, c->stream, true));
+  return SPEC_OK;
+}
+
+int spec_gemm_q4k(spec_ctx* c, const void* w, int N, int K, const float* x, int M, float* y) {
+  return gemm_common(c, w, N, K, x, M, y, nullptr, nullptr);
+}
+
+int spec_gemm_q4k_sums(spec_ctx* c, const void* w, int N, int K, const float* x, int M, float* y,
+                       int32_t* isc, int32_t* imn) {
+  if (!isc || !imn) return SPEC_ENULL;
+  return gemm_common(c, w, N, K, x, M, y, isc, imn);
+}
+
+int spec_lm_head_argmax(spec_ctx* c, const void* w_head, const float* final_norm, const float* x,
+                        int M, int32_t* idx, float* logits) {
+  if (!c || !w_head || !x || !idx) return SPEC_ENULL;
+  if (M < 1 || M > 16) return SPEC_EINVAL;
+  if (!aligned(w_head) || !aligned(x) || (final_norm && !aligned(final_norm))) return SPEC_EALIGN;
+  const spec_config& g = c->cfg;
+  SPEC_TRY(launch_resid_norm_quant(nullptr, nullptr, x, nullptr, final_norm, g.rms_eps, M, g.hidden,
+                                   c->act, nullptr, c->status, c->stream, false));
+  SPEC_TRY(launch_gemm(c->p_head, w_head, c->act, c->pieces, nullptr, nullptr, 0, c->stream, true));
+  SPEC_TRY(launch_head_argmax(c->p_head, c->pieces, M, logits, c->head_val, c->head_idx, c->status,
+                              c->stream, true));
+  SPEC_TRY(launch_argmax_final(c->head_val, c->head_idx, c->head_parts, M, idx, c->stream, true));
+  return SPEC_OK;
+}
+
+int spec_attention(spec_ctx* c, const spec_kv* kv, int layer, const float* q, int M, float* out) {
+  if (!c || !q || !out) return SPEC_ENULL;
+  int rc = check_kv(kv);
+  if (rc) return rc;
+  if (M < 1 || M > 16 || layer < 0 || layer >= c->cfg.n_layers) return SPEC_EINVAL;
+  if (kv->max_seq_pages * c->cfg.page_size > c->attn.max_chunks * c->attn.chunk)
+    return SPEC_ECAPACITY;   // attention workspace must cover every position the cache can hold
+  if (!aligned(q) || !aligned(out)) return SPEC_EALIGN;
+  SPEC_TRY(cudaMemsetAsync(c->status, 0, 4, c->stream));
+  SPEC_TRY(launch_q_to_frag(q, M, c->cfg.n_q_heads, c->qfrag, c->stream, false));
+  SPEC_TRY(launch_attention(c->attn, view_of(c, kv), layer, c->qfrag, M, c->attn_part, out, nullptr,
+                            c->status, c->stream, false));
+  return SPEC_OK;
+}
+
+int spec_accept(spec_ctx* c, const int32_t* idx, const int32_t* draft, int k, spec_kv* kv,
+                spec_result* res) {
+  if (!c || !idx || !draft || !res) return SPEC_ENULL;
+  if (k != 3 && k != 7 && k != 15) return SPEC_EVERIFYLEN;
+  if (kv) {
+    int rc = check_kv(kv);
+    if (rc) return rc;
+  }
+  KvView v;
+  if (kv) v = view_of(c, kv);
+  return cuda_code(launch_accept(idx, nullptr, nullptr, 0, draft, k, c->cfg.vocab, kv ? &v : nullptr,
+                                 nullptr, c->status, reinterpret_cast<int32_t*>(res), nullptr,
+                                 c->stream, false));
+}
+
+int spec_kv_reset(spec_ctx* c, spec_kv* kv) {
+  if (!c) return SPEC_ENULL;
+  int rc = check_kv(kv);
+  if (rc) return rc;
+  return cuda_code(launch_kv_reset(view_of(c, kv), c->stream));
+}
+
+int spec_kv_extend(spec_ctx* c, spec_kv* kv, int32_t n) {
+  if (!c) return SPEC_ENULL;
+  int rc = check_kv(kv);
+  if (rc) return rc;
+  if (n < 0) return SPEC_EINVAL;
+  return cuda_code(launch_kv_reserve(view_of(c, kv), n, 1, nullptr, 0, 0, c->status, nullptr,
+                                     c->stream, false));
+}
+
+int spec_kv_rollback(spec_ctx* c, spec_kv* kv, int32_t new_len) {
+  if (!c) return SPEC_ENULL;
+  int rc = check_kv(kv);
+  if (rc) return rc;
+  if (new_len < 0) return SPEC_EINVAL;
+  return cuda_code(launch_kv_rollback(view_of(c, kv), new_len, c->status, c->stream));
+}
+
+// ---------------------------------------------------------------------------
+// the verify step
+// ---------------------------------------------------------------------------
+static int check_weights(const spec_ctx* c, const spec_weights* w) {
+  if (!w || !w->w_qkv || !w->w_o || !w->w_gate_up || !w->w_down || !w->w_head) return SPEC_ENULL;
+  for (int l = 0; l < c->cfg.n_layers; ++l) {
+    if (!w->w_qkv[l] || !w->w_o[l] || !w->w_gate_up[l] || !w->w_down[l]) return SPEC_ENULL;
+    if (!aligned(w->w_qkv[l]) || !aligned(w->w_o[l]) || !aligned(w->w_gate_up[l]) ||
+        !aligned(w->w_down[l]))
+      return SPEC_EALIGN;
+    if (w->attn_norm && w->attn_norm[l] && !aligned(w->attn_norm[l])) return SPEC_EALIGN;
+    if (w->ffn_norm && w->ffn_norm[l] && !aligned(w->ffn_norm[l])) return SPEC_EALIGN;
+  }
+  if (!aligned(w->w_head) || (w->final_norm && !aligned(w->final_norm))) return SPEC_EALIGN;
+  return SPEC_OK;
+}
+
+static int enqueue_step(spec_ctx* c, const spec_weights* w, spec_kv* kv, const float* hidden,
+                        const int32_t* draft, int k, spec_result* res, const spec_taps* taps) {
+  const int M = k + 1;
+
+  const spec_config& g = c->cfg;
+  const int H = g.hidden, F = g.ffn;
+  cudaStream_t st = c->stream;
+  const KvView kvv = view_of(c, kv);
+  int n = 0;
+  c->prof_n = 0;
+  auto gemm = [&](const GemmPlan& p, const void* wt) -> cudaError_t {
+    const bool prof = c->profile && 2 * c->prof_n + 1 < c->prof_cap;
+    if (prof) {
+      cudaError_t e = cudaEventRecord(c->prof_ev[2 * c->prof_n], st);
+      if (e != cudaSuccess) return e;
+    }
+    cudaError_t e = launch_gemm(p, wt, c->act, c->pieces, nullptr, nullptr, 0, st, !prof);
+    if (e != cudaSuccess) return e;
+    if (prof) {
+      e = cudaEventRecord(c->prof_ev[2 * c->prof_n + 1], st);
+      ++c->prof_n;
+    }
+    return e;
+  };
+  auto attn_gamma = [&](int l) -> const float* { return w->attn_norm ? w->attn_norm[l] : nullptr; };
+  auto ffn_gamma = [&](int l) -> const float* { return w->ffn_norm ? w->ffn_norm[l] : nullptr; };
+  float* tap_resid = taps ? taps->resid : nullptr;
+  const size_t rows_bytes = sizeof(float) * (size_t)M * H;
+
+  SPEC_TRY(launch_kv_reserve(kvv, M, 0, draft, k, g.vocab, c->status, c->step_state, st, true)); ++n;
+  if (tap_resid) SPEC_TRY(cudaMemcpyAsync(tap_resid, hidden, rows_bytes, cudaMemcpyDeviceToDevice, st));
+  SPEC_TRY(launch_resid_norm_quant(nullptr, nullptr, hidden, c->resid, attn_gamma(0), g.rms_eps, M, H,
+                                   c->act, nullptr, c->status, st, true)); ++n;
+  for (int l = 0; l < g.n_layers; ++l) {
+    SPEC_TRY(gemm(c->p_qkv, w->w_qkv[l])); ++n;
+    SPEC_TRY(launch_qkv_post(c->p_qkv, c->pieces, M, g.n_q_heads, g.n_kv_heads, g.head_dim, kvv, l,
+                              c->qfrag, c->status, st, true)); ++n;
+    SPEC_TRY(launch_attention(c->attn, kvv, l, c->qfrag, M, c->attn_part, nullptr, c->act, c->status,
+                              st, true)); n += 2;
+    SPEC_TRY(gemm(c->p_o, w->w_o[l])); ++n;
+    SPEC_TRY(launch_resid_norm_quant(&c->p_o, c->pieces, c->resid, c->resid, ffn_gamma(l), g.rms_eps,
+                                     M, H, c->act, nullptr, c->status, st, true)); ++n;
+    SPEC_TRY(gemm(c->p_gu, w->w_gate_up[l])); ++n;
+    SPEC_TRY(launch_swiglu_quant(c->p_gu, c->pieces, M, F, c->act, c->status, st, true)); ++n;
+    SPEC_TRY(gemm(c->p_down, w->w_down[l])); ++n;
+    const float* next_gamma = (l + 1 < g.n_layers) ? attn_gamma(l + 1) : w->final_norm;
+    SPEC_TRY(launch_resid_norm_quant(&c->p_down, c->pieces, c->resid, c->resid, next_gamma, g.rms_eps,
+                                     M, H, c->act, nullptr, c->status, st, true)); ++n;
+    if (tap_resid)
+      SPEC_TRY(cudaMemcpyAsync(tap_resid + (size_t)(l + 1) * M * H, c->resid, rows_bytes,
+                               cudaMemcpyDeviceToDevice, st));
+  }
+  SPEC_TRY(gemm(c->p_head, w->w_head)); ++n;
+  SPEC_TRY(launch_head_argmax(c->p_head, c->pieces, M, taps ? taps->logits : nullptr, c->head_val,
+                              c->head_idx, c->status, st, true)); ++n;
+  SPEC_TRY(launch_accept(nullptr, c->head_val, c->head_idx, c->head_parts, draft, k, g.vocab, &kvv,
+                         c->step_state, c->status, reinterpret_cast<int32_t*>(res),
+                         taps ? taps->argmax : nullptr, st, true)); ++n;
+  c->last_launches = n;
+  return SPEC_OK;
+}
+
+static uint64_t mix(uint64_t h, uint64_t v) {
+  h ^= v + 0x9e3779b97f4a7c15ull + (h << 6) + (h >> 2);
+  return h;
+}
+
+static uint64_t step_key(const spec_ctx* c, const spec_weights* w, const spec_kv* kv,
+                         const float* hidden, const int32_t* draft, int k, const spec_result* res) {
+  uint64_t h = 0x1234567ull;
+  auto P = [](const void* p) { return (uint64_t)(uintptr_t)p; };
+  h = mix(h, P(hidden));
+  h = mix(h, P(draft));
+  h = mix(h, P(res));
+  h = mix(h, (uint64_t)k);
+  h = mix(h, P(kv->pool));
+  h = mix(h, P(kv->page_table));
+  h = mix(h, P(kv->seq_len));
+  h = mix(h, P(kv->free_stack));
+  h = mix(h, P(kv->free_top));
+  h = mix(h, (uint64_t)kv->num_pages);
+  h = mix(h, (uint64_t)kv->max_seq_pages);
+  for (int l = 0; l < c->cfg.n_layers; ++l) {
+    h = mix(h, P(w->w_qkv[l]));
+    h = mix(h, P(w->w_o[l]));
+    h = mix(h, P(w->w_gate_up[l]));
+    h = mix(h, P(w->w_down[l]));
+    h = mix(h, w->attn_norm ? P(w->attn_norm[l]) : 1);
+    h = mix(h, w->ffn_norm ? P(w->ffn_norm[l]) : 2);
+  }
+  h = mix(h, P(w->final_norm));
+  h = mix(h, P(w->w_head));
+  return h | 1;
+}
+
+int spec_verify_step_ex(spec_ctx* c, const spec_weights* w, spec_kv* kv, const float* hidden,
+                        const int32_t* draft, int k, spec_result* res, const spec_taps* taps) {
+  if (!c || !hidden || !draft || !res) return SPEC_ENULL;
+  if (k != 3 && k != 7 && k != 15) return SPEC_EVERIFYLEN;
+  const int M = k + 1;
+  if (M > c->cfg.max_rows) return SPEC_ECAPACITY;
+  int rc = check_kv(kv);
+  if (rc) return rc;
+  rc = check_weights(c, w);
+  if (rc) return rc;
+  if (!aligned(hidden)) return SPEC_EALIGN;
+  if (kv->max_seq_pages * c->cfg.page_size > c->attn.max_chunks * c->attn.chunk)
+    return SPEC_ECAPACITY;   // attention workspace must cover every position the cache can hold
+
+  // Steps with taps, with GEMM profiling, or on the legacy default stream
+  // (which cannot be captured) are enqueued directly.
+  if (taps || c->profile || !c->use_graphs || c->stream == nullptr)
+    return enqueue_step(c, w, kv, hidden, draft, k, res, taps);
+
+  const uint64_t key = step_key(c, w, kv, hidden, draft, k, res);
+  spec_ctx::GraphEntry* hit = nullptr;
+  for (auto& gc : c->graphs)
+    if (gc.exec && gc.key == key) hit = &gc;
+  if (!hit) {
+    // record the step once: a one-time host-side graph build for this argument set
+    spec_ctx::GraphEntry* victim = &c->graphs[0];
+    for (auto& gc : c->graphs)
+      if (!gc.exec || gc.used < victim->used) victim = &gc;
+    if (victim->exec) {
+      cudaGraphExecDestroy(victim->exec);
+      victim->exec = nullptr;
+    }
+    cudaGraph_t graph = nullptr;
+    SPEC_TRY(cudaStreamBeginCapture(c->stream, cudaStreamCaptureModeThreadLocal));
+    rc = enqueue_step(c, w, kv, hidden, draft, k, res, nullptr);
+    cudaError_t e = cudaStreamEndCapture(c->stream, &graph);
+    if (rc != SPEC_OK) {
+      if (graph) cudaGraphDestroy(graph);
+      return rc;
+    }
+    if (e != cudaSuccess) return SPEC_ECUDA;
+    cudaGraphExec_t exec = nullptr;
+    e = cudaGraphInstantiate(&exec, graph, 0);
+    cudaGraphDestroy(graph);
+    if (e != cudaSuccess) return SPEC_ECUDA;
+    victim->exec = exec;
+    victim->key = key;
+    victim->launches = c->last_launches;
+    hit = victim;
+  }
+  hit->used = ++c->graph_clock;
+  c->last_launches = hit->launches;
+  SPEC_TRY(cudaGraphLaunch(hit->exec, c->stream));
+  return SPEC_OK;
+}
+
+int spec_verify_step(spec_ctx* c, const spec_weights* w, spec_kv* kv, const float* hidden,
+                     const int32_t* draft, int k, spec_result* res) {
+  return spec_verify_step_ex(c, w, kv, hidden, draft, k, res, nullptr);
+}
+
+int spec_verify_step_host(spec_ctx* c, const spec_weights* w, spec_kv* kv, const float* hidden_host,
+                          const int32_t* draft_host, int k, spec_result* res_host) {
+  if (!c || !hidden_host || !draft_host || !res_host) return SPEC_ENULL;
+  if (k != 3 && k != 7 && k != 15) return SPEC_EVERIFYLEN;
+  if (k + 1 > c->cfg.max_rows) return SPEC_ECAPACITY;
+  const size_t hb = sizeof(float) * (size_t)(k + 1) * c->cfg.hidden;
+  SPEC_TRY(cudaMemcpyAsync(c->hidden_dev, hidden_host, hb, cudaMemcpyHostToDevice, c->stream));
+  SPEC_TRY(cudaMemcpyAsync(c->draft_dev, draft_host, sizeof(int32_t) * k, cudaMemcpyHostToDevice,
+                           c->stream));
+  int rc = spec_verify_step(c, w, kv, c->hidden_dev, c->draft_dev, k, c->res_dev);
+  if (rc) return rc;
+  SPEC_TRY(cudaMemcpyAsync(res_host, c->res_dev, sizeof(spec_result), cudaMemcpyDeviceToHost,
+                           c->stream));
+  SPEC_TRY(cudaStreamSynchronize(c->stream));
+  return SPEC_OK;
+}
+
+}  // extern "C"

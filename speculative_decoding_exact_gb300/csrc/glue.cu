@@ -1,0 +1,564 @@
+// glue.cu — the small kernels around the GEMMs of the verify step:
+// activation quantisation into the tensor-core fragment order, residual add +
+// RMSNorm + quantisation (one 8-CTA cluster per row), SwiGLU + quantisation,
+// QKV split with the K/V append into the paged bf16 cache, the LM-head argmax,
+// the greedy accept + KV rollback kernel and the KV metadata kernels.
+//
+// Sources (page titles and sections):
+//   accept rule            Muser book Ch. 33 §33.2 (greedy = one-hot case)
+//   carried frontier       Ch. 33 §33.7
+//   verify lengths, rewind Ch. 8 §8.6 items 3 and 4
+//   F32 residual, one fixed reduction order
+//                          Ch. 32 "Precision across the handoff" (intro, §32.4)
+#include <cooperative_groups.h>
+
+#include "common.cuh"
+#include "internal.h"
+#include "quant.cuh"
+
+namespace cg = cooperative_groups;
+
+namespace spec {
+
+__host__ __device__ __forceinline__ int cta_of_unit2(long long x, long long U, int G) {
+  return (int)(((x + 1) * (long long)G - 1) / U);
+}
+
+// sum of the GEMM pieces of output (row, col), slots in order
+__device__ __forceinline__ float piece_sum(const float* __restrict__ pieces, int N, int nb,
+                                           long long U, int G, int row, int col) {
+  const int gr = (col >> 4) / kTilesPerGroup;
+  const int c0 = cta_of_unit2((long long)gr * nb, U, G);
+  const int ns = cta_of_unit2((long long)gr * nb + nb - 1, U, G) - c0 + 1;
+  // independent loads of at most kMaxSlots slots, added in slot order
+  float v[kMaxSlots];
+#pragma unroll
+  for (int k = 0; k < kMaxSlots; ++k) v[k] = k < ns ? pieces[((size_t)k * 16 + row) * N + col] : 0.f;
+  float s = v[0];
+#pragma unroll
+  for (int k = 1; k < kMaxSlots; ++k)
+    if (k < ns) s += v[k];
+  return s;
+}
+
+template <class T>
+__device__ __forceinline__ void load8(const T* p, float (&v)[8]) {
+  const float4 a = reinterpret_cast<const float4*>(p)[0];
+  const float4 c = reinterpret_cast<const float4*>(p)[1];
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  v[4] = c.x; v[5] = c.y; v[6] = c.z; v[7] = c.w;
+}
+
+// ---- plain quantisation of x[M][K]: grid (ceil(nb/8), 16), 8 warps, warp = block
+__global__ void quantize_kernel(const float* __restrict__ x, int M, int K, uint8_t* act,
+                                int8_t* q_dbg, float* da_dbg, int32_t* A_dbg, int32_t* status) {
+  pdl_wait();
+  pdl_trigger();
+  const int nb = K / 256;
+  const int b = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int row = blockIdx.y;
+  if (b >= nb) return;
+  if (row >= M) {
+    zero_block_warp(row, b, act);
+    return;
+  }
+  float v[8];
+  load8(x + (size_t)row * K + 256 * b + 8 * (threadIdx.x & 31), v);
+  quant_block_warp(v, row, b, K, act, q_dbg, da_dbg, A_dbg, status);
+}
+
+static cudaLaunchConfig_t make_cfg(dim3 grid, dim3 block, size_t smem, cudaStream_t st, bool pdl,
+                                   cudaLaunchAttribute* attrs, int cluster_x = 0) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  int n = 0;
+  if (pdl) {
+    attrs[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (cluster_x > 0) {
+    attrs[n].id = cudaLaunchAttributeClusterDimension;
+    attrs[n].val.clusterDim.x = cluster_x;
+    attrs[n].val.clusterDim.y = 1;
+    attrs[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = attrs;
+  cfg.numAttrs = n;
+  return cfg;
+}
+
+cudaError_t launch_quantize(const float* x, int M, int K, uint8_t* act, int8_t* q_dbg,
+                            float* da_dbg, int32_t* A_dbg, int32_t* status, cudaStream_t st,
+                            bool pdl) {
+  const int nb = K / 256;
+  cudaLaunchAttribute attrs[2];
+  cudaLaunchConfig_t cfg = make_cfg(dim3((nb + 7) / 8, 16), dim3(256), 0, st, pdl, attrs);
+  return cudaLaunchKernelEx(&cfg, quantize_kernel, x, M, K, act, q_dbg, da_dbg, A_dbg, status);
+}
+
+// ---------------------------------------------------------------------------
+// residual + RMSNorm + quantisation.  One cluster of 8 CTAs per row; CTA c of
+// the cluster owns the 256-blocks b = c, c+8, c+16, ... (warp w takes the w-th
+// of them).  The row's sum of squares is reduced lane -> warp (butterfly) ->
+// CTA (warp order) -> cluster (rank order): one fixed order set by H alone.
+// x_out = x_in + sum(pieces) (fp32 add) when pieces are given.
+// ---------------------------------------------------------------------------
+constexpr int kNormCluster = 8;
+
+__global__ void __cluster_dims__(kNormCluster, 1, 1)
+resid_norm_quant_kernel(const float* __restrict__ pieces, int pN, int pnb, long long pU, int pG,
+                        const float* x_in, float* x_out,
+                        const float* __restrict__ gamma, float eps, int M, int H, uint8_t* act,
+                        float* __restrict__ xnorm_out, int32_t* status) {
+  pdl_wait();
+  pdl_trigger();
+  cg::cluster_group cluster = cg::this_cluster();
+  __shared__ float warp_ss[8];
+  __shared__ float cta_ss;
+  const int row = blockIdx.y;
+  const int c = (int)cluster.block_rank();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nb = H / 256;
+  const int b = c + kNormCluster * warp;
+  const bool has = b < nb;
+  float v[8];
+  float ss = 0.f;
+  if (row < M && has) {
+    const int col0 = 256 * b + 8 * lane;
+    load8(x_in + (size_t)row * H + col0, v);
+    if (pieces) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = v[i] + piece_sum(pieces, pN, pnb, pU, pG, row, col0 + i);
+      float4* o = reinterpret_cast<float4*>(x_out + (size_t)row * H + col0);
+      o[0] = make_float4(v[0], v[1], v[2], v[3]);
+      o[1] = make_float4(v[4], v[5], v[6], v[7]);
+    } else if (x_out != x_in && x_out) {
+      float4* o = reinterpret_cast<float4*>(x_out + (size_t)row * H + col0);
+      o[0] = make_float4(v[0], v[1], v[2], v[3]);
+      o[1] = make_float4(v[4], v[5], v[6], v[7]);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) ss += v[i] * v[i];
+  }
+  ss = warp_sum(ss);
+  if (lane == 0) warp_ss[warp] = ss;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float s = 0.f;
+    for (int w = 0; w < 8; ++w) s += warp_ss[w];
+    cta_ss = s;
+  }
+  cluster.sync();
+  float total = 0.f;
+  for (int r = 0; r < kNormCluster; ++r) total += *cluster.map_shared_rank(&cta_ss, r);
+  if (has) {
+    if (row < M) {
+      const float rinv = 1.0f / sqrtf(total / (float)H + eps);
+      const int col0 = 256 * b + 8 * lane;
+      float gm[8];
+      if (gamma) {
+        load8(gamma + col0, gm);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) gm[i] = 1.f;
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = v[i] * rinv * gm[i];
+      if (xnorm_out) {
+        float4* o = reinterpret_cast<float4*>(xnorm_out + (size_t)row * H + col0);
+        o[0] = make_float4(v[0], v[1], v[2], v[3]);
+        o[1] = make_float4(v[4], v[5], v[6], v[7]);
+      }
+      quant_block_warp(v, row, b, H, act, nullptr, nullptr, nullptr, status);
+    } else {
+      zero_block_warp(row, b, act);
+    }
+  }
+  cluster.sync();   // keep this CTA's shared memory alive until all peers read it
+}
+
+cudaError_t launch_resid_norm_quant(const GemmPlan* p, const float* pieces, const float* x_in,
+                                    float* x_out, const float* gamma, float eps, int M, int H,
+                                    uint8_t* act, float* xnorm_out, int32_t* status,
+                                    cudaStream_t st, bool pdl) {
+  cudaLaunchAttribute attrs[2];
+  cudaLaunchConfig_t cfg = make_cfg(dim3(kNormCluster, 16), dim3(256), 0, st, pdl, attrs);
+  const int pN = p ? p->N : 0, pnb = p ? p->nb : 1, pG = p ? p->G : 1;
+  const long long pU = p ? p->U : 1;
+  return cudaLaunchKernelEx(&cfg, resid_norm_quant_kernel, pieces, pN, pnb, pU, pG, x_in, x_out,
+                            gamma, eps, M, H, act, xnorm_out, status);
+}
+
+// ---------------------------------------------------------------------------
+// SwiGLU + quantisation: grid (ceil(nbF/8), 16), warp = one 256-block of h.
+// h = silu(g) * u, silu(g) = g / (1 + exp(-g)), fp32.
+// ---------------------------------------------------------------------------
+__global__ void swiglu_quant_kernel(const float* __restrict__ pieces, int pN, int pnb, long long pU,
+                                    int pG, int M, int F, uint8_t* act, int32_t* status) {
+  pdl_wait();
+  pdl_trigger();
+  const int nb = F / 256;
+  const int b = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int row = blockIdx.y;
+  if (b >= nb) return;
+  if (row >= M) {
+    zero_block_warp(row, b, act);
+    return;
+  }
+  const int col0 = 256 * b + 8 * (threadIdx.x & 31);
+  float v[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float gt = piece_sum(pieces, pN, pnb, pU, pG, row, col0 + i);
+    const float up = piece_sum(pieces, pN, pnb, pU, pG, row, F + col0 + i);
+    const float sl = gt / (1.0f + expf(-gt));
+    v[i] = sl * up;
+  }
+  quant_block_warp(v, row, b, F, act, nullptr, nullptr, nullptr, status);
+}
+
+cudaError_t launch_swiglu_quant(const GemmPlan& p, const float* pieces, int M, int F, uint8_t* act,
+                                int32_t* status, cudaStream_t st, bool pdl) {
+  const int nb = F / 256;
+  cudaLaunchAttribute attrs[2];
+  cudaLaunchConfig_t cfg = make_cfg(dim3((nb + 7) / 8, 16), dim3(256), 0, st, pdl, attrs);
+  return cudaLaunchKernelEx(&cfg, swiglu_quant_kernel, pieces, p.N, p.nb, p.U, p.G, M, F, act,
+                            status);
+}
+
+// ---------------------------------------------------------------------------
+// QKV split: Q -> bf16 hi/lo attention fragments (rows >= M zero); K, V ->
+// bf16 (round to nearest even) into the page of position n_past + row,
+// n_past = seq_len - M (the reserve kernel has already appended the block).
+// Skips the cache when the step is invalid.
+// ---------------------------------------------------------------------------
+__global__ void qkv_post_kernel(const float* __restrict__ pieces, int pN, int pnb, long long pU,
+                                int pG, int M, int nq, int nkv, int dh, KvView kv, int layer,
+                                uint8_t* __restrict__ qfrag, const int32_t* status) {
+  pdl_wait();
+  pdl_trigger();
+  const int row = blockIdx.y;
+  const int col = blockIdx.x * blockDim.x + threadIdx.x;
+  const int qcols = nq * dh;
+  if (col >= pN) return;
+  if (row >= M) {
+    if (col < qcols) write_qfrag(qfrag, row, col / dh, col % dh, 0.f);
+    return;
+  }
+  const float v = piece_sum(pieces, pN, pnb, pU, pG, row, col);
+  if (col < qcols) {
+    write_qfrag(qfrag, row, col / dh, col % dh, v);
+    return;
+  }
+  if (*status & (SPEC_ST_TOKEN_RANGE | SPEC_ST_POOL_EMPTY | SPEC_ST_CTX_FULL)) return;
+  const int c = col - qcols;
+  const int which = c / (nkv * dh);          // 0 = K, 1 = V
+  const int head = (c % (nkv * dh)) / dh, d = c % dh;
+  const int pos = *kv.seq_len - M + row;
+  const int lp = pos / kv.page_size;
+  if (pos < 0 || lp >= kv.max_seq_pages) return;
+  const int page = kv.page_table[lp];
+  if (page < 0 || page >= kv.num_pages) return;
+  const size_t off = ((((size_t)page * kv.n_layers + layer) * 2 + which) * kv.n_kv + head) *
+                         (size_t)kv.page_size * kv.head_dim +
+                     (size_t)(pos % kv.page_size) * kv.head_dim + d;
+  kv.pool[off] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+}
+
+cudaError_t launch_qkv_post(const GemmPlan& p, const float* pieces, int M, int nq, int nkv, int dh,
+                            const KvView& kv, int layer, uint8_t* qfrag, const int32_t* status,
+                            cudaStream_t st, bool pdl) {
+  cudaLaunchAttribute attrs[2];
+  cudaLaunchConfig_t cfg = make_cfg(dim3((p.N + 255) / 256, 16), dim3(256), 0, st, pdl, attrs);
+  return cudaLaunchKernelEx(&cfg, qkv_post_kernel, pieces, p.N, p.nb, p.U, p.G, M, nq, nkv, dh, kv,
+                            layer, qfrag, status);
+}
+
+// ---------------------------------------------------------------------------
+// LM head argmax: CTA c scans columns [c*kArgCols, (c+1)*kArgCols) of every
+// row: logit = sum of the head GEMM pieces; keeps (max, lowest index).
+// ---------------------------------------------------------------------------
+constexpr int kArgCols = 512;
+
+int head_argmax_blocks(int V) { return (V + kArgCols - 1) / kArgCols; }
+
+__device__ __forceinline__ void better(float& bv, int& bi, float v, int i) {
+  // larger value wins; equal values: lower index wins
+  if (v > bv || (v == bv && i < bi)) {
+    bv = v;
+    bi = i;
+  }
+}
+
+// CTA c scans columns [c*kArgCols, (c+1)*kArgCols) of every row; thread t
+// owns columns t, t+256 of each row; per-row (max, lowest index) reduced
+// warp -> CTA in a fixed order.
+__global__ void __launch_bounds__(256)
+head_argmax_kernel(const float* __restrict__ pieces, int pN, int pnb, long long pU, int pG, int M,
+                   float* __restrict__ logits, float* __restrict__ part_val,
+                   int32_t* __restrict__ part_idx, int32_t* status) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ float sv[16][8];
+  __shared__ int si[16][8];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int col_base = blockIdx.x * kArgCols;
+  bool bad = false;
+  for (int row = 0; row < 16; ++row) {
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+    if (row < M) {
+#pragma unroll
+      for (int k = 0; k < kArgCols / 256; ++k) {
+        const int col = col_base + threadIdx.x + 256 * k;
+        if (col < pN) {
+          const float v = piece_sum(pieces, pN, pnb, pU, pG, row, col);
+          if (logits) logits[(size_t)row * pN + col] = v;
+          if (!isfinite(v)) bad = true;
+          better(bv, bi, v, col);
+        }
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      better(bv, bi, ov, oi);
+    }
+    if (lane == 0) {
+      sv[row][warp] = bv;
+      si[row][warp] = bi;
+    }
+  }
+  if (bad) atomicOr(status, SPEC_ST_NONFINITE);
+  __syncthreads();
+  if (threadIdx.x < 16) {
+    const int row = threadIdx.x;
+    float v = sv[row][0];
+    int i = si[row][0];
+    for (int w = 1; w < 8; ++w) better(v, i, sv[row][w], si[row][w]);
+    part_val[(size_t)blockIdx.x * 16 + row] = v;
+    part_idx[(size_t)blockIdx.x * 16 + row] = i;
+  }
+}
+
+cudaError_t launch_head_argmax(const GemmPlan& p, const float* pieces, int M, float* logits,
+                               float* part_val, int32_t* part_idx, int32_t* status, cudaStream_t st,
+                               bool pdl) {
+  cudaLaunchAttribute attrs[2];
+  cudaLaunchConfig_t cfg = make_cfg(dim3(head_argmax_blocks(p.N)), dim3(256), 0, st, pdl, attrs);
+  return cudaLaunchKernelEx(&cfg, head_argmax_kernel, pieces, p.N, p.nb, p.U, p.G, M, logits,
+                            part_val, part_idx, status);
+}
+
+// final reduction of the per-CTA partials: idx[row], lowest index on ties
+__global__ void argmax_final_kernel(const float* __restrict__ part_val,
+                                    const int32_t* __restrict__ part_idx, int nparts, int M,
+                                    int32_t* __restrict__ idx) {
+  pdl_wait();
+  pdl_trigger();
+  const int lane = threadIdx.x;
+  for (int row = 0; row < M; ++row) {
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+    for (int c = lane; c < nparts; c += 32)
+      better(bv, bi, part_val[(size_t)c * 16 + row], part_idx[(size_t)c * 16 + row]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      better(bv, bi, ov, oi);
+    }
+    if (lane == 0) idx[row] = bi;
+  }
+}
+
+cudaError_t launch_argmax_final(const float* part_val, const int32_t* part_idx, int nparts, int M,
+                                int32_t* idx, cudaStream_t st, bool pdl) {
+  cudaLaunchAttribute attrs[2];
+  cudaLaunchConfig_t cfg = make_cfg(dim3(1), dim3(32), 0, st, pdl, attrs);
+  return cudaLaunchKernelEx(&cfg, argmax_final_kernel, part_val, part_idx, nparts, M, idx);
+}
+
+// ---------------------------------------------------------------------------
+// KV metadata (Ch. 8 §8.6 item 4).  Single-thread kernels: a block touches at
+// most ceil(16/16)+1 pages, a rollback at most that many.
+// ---------------------------------------------------------------------------
+__global__ void kv_reset_kernel(KvView kv) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < kv.max_seq_pages) kv.page_table[i] = -1;
+  if (i < kv.num_pages) kv.free_stack[i] = kv.num_pages - 1 - i;
+  if (i == 0) {
+    *kv.free_top = kv.num_pages;
+    *kv.seq_len = 0;
+  }
+}
+
+cudaError_t launch_kv_reset(const KvView& kv, cudaStream_t st) {
+  const int n = kv.max_seq_pages > kv.num_pages ? kv.max_seq_pages : kv.num_pages;
+  kv_reset_kernel<<<(n + 255) / 256, 256, 0, st>>>(kv);
+  return cudaGetLastError();
+}
+
+// step_state: [0] = n_past, [1] = 1 when the block was appended
+__global__ void kv_reserve_kernel(KvView kv, int n, int commit, const int32_t* __restrict__ draft,
+                                  int k, int vocab, int32_t* status, int32_t* step_state) {
+  pdl_wait();
+  pdl_trigger();
+  if (threadIdx.x != 0 || blockIdx.x != 0) return;
+  int st = 0;
+  if (step_state) {
+    step_state[0] = *kv.seq_len;
+    step_state[1] = 0;
+  }
+  if (draft) {
+    for (int i = 0; i < k; ++i)
+      if (draft[i] < 0 || draft[i] >= vocab) st |= SPEC_ST_TOKEN_RANGE;
+  }
+  const int len = *kv.seq_len;
+  const int upto = len + n;
+  const int pages = (upto + kv.page_size - 1) / kv.page_size;
+  if (!st && pages > kv.max_seq_pages) st |= SPEC_ST_CTX_FULL;
+  if (!st) {
+    int need = 0;
+    for (int p = 0; p < pages; ++p)
+      if (kv.page_table[p] < 0) ++need;
+    if (need > *kv.free_top) st |= SPEC_ST_POOL_EMPTY;
+  }
+  if (!st) {
+    for (int p = 0; p < pages; ++p)
+      if (kv.page_table[p] < 0) {
+        const int top = *kv.free_top - 1;
+        kv.page_table[p] = kv.free_stack[top];
+        *kv.free_top = top;
+      }
+    if (commit || step_state) *kv.seq_len = upto;
+    if (step_state) step_state[1] = 1;
+  }
+  if (step_state) {
+    *status = st;           // first kernel of a step: resets the step status
+  } else if (st) {
+    atomicOr(status, st);
+  }
+}
+
+cudaError_t launch_kv_reserve(const KvView& kv, int n, int commit, const int32_t* draft, int k,
+                              int vocab, int32_t* status, int32_t* step_state, cudaStream_t st,
+                              bool pdl) {
+  cudaLaunchAttribute attrs[2];
+  cudaLaunchConfig_t cfg = make_cfg(dim3(1), dim3(32), 0, st, pdl, attrs);
+  return cudaLaunchKernelEx(&cfg, kv_reserve_kernel, kv, n, commit, draft, k, vocab, status,
+                            step_state);
+}
+
+__device__ void kv_rollback_dev(const KvView& kv, int new_len) {
+  const int len = *kv.seq_len;
+  const int hi = (len + kv.page_size - 1) / kv.page_size;
+  const int lo = (new_len + kv.page_size - 1) / kv.page_size;
+  for (int p = hi - 1; p >= lo; --p) {
+    const int id = kv.page_table[p];
+    if (id >= 0 && *kv.free_top < kv.num_pages) {
+      kv.free_stack[*kv.free_top] = id;
+      *kv.free_top += 1;
+      kv.page_table[p] = -1;
+    }
+  }
+  *kv.seq_len = new_len;
+}
+
+__global__ void kv_rollback_kernel(KvView kv, int new_len, int32_t* status) {
+  if (threadIdx.x != 0 || blockIdx.x != 0) return;
+  const int len = *kv.seq_len;
+  if (new_len < 0 || new_len > len) {
+    atomicOr(status, SPEC_ST_ROLLBACK);
+    return;
+  }
+  kv_rollback_dev(kv, new_len);
+}
+
+cudaError_t launch_kv_rollback(const KvView& kv, int new_len, int32_t* status, cudaStream_t st) {
+  kv_rollback_kernel<<<1, 32, 0, st>>>(kv, new_len, status);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Accept + rollback: final argmax reduction over the head partials (or the
+// given idx), L = first i < k with draft[i] != idx[i] (else k), next = idx[L];
+// seq_len := n_past + L + 1 and the pages past it are freed.  On any device
+// error the block is rolled back entirely (seq_len := n_past).
+// res = {accepted_len, next_token, status, seq_len}.
+// ---------------------------------------------------------------------------
+__global__ void accept_kernel(const int32_t* __restrict__ idx_in, const float* __restrict__ part_val,
+                              const int32_t* __restrict__ part_idx, int nparts,
+                              const int32_t* __restrict__ draft, int k, int vocab, KvView kv,
+                              int has_kv, const int32_t* step_state, int32_t* status, int32_t* res,
+                              int32_t* idx_out) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ int idx_s[16];
+  const int lane = threadIdx.x;
+  for (int row = 0; row <= k; ++row) {
+    if (idx_in) {
+      if (lane == 0) idx_s[row] = idx_in[row];
+    } else {
+      float bv = -INFINITY;
+      int bi = 0x7fffffff;
+      for (int c = lane; c < nparts; c += 32) better(bv, bi, part_val[(size_t)c * 16 + row], part_idx[(size_t)c * 16 + row]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        better(bv, bi, ov, oi);
+      }
+      if (lane == 0) idx_s[row] = bi;
+    }
+  }
+  __syncwarp();
+  if (lane != 0) return;
+  int st = step_state ? *status : 0;
+  for (int i = 0; i < k; ++i)
+    if (draft[i] < 0 || draft[i] >= vocab) st |= SPEC_ST_TOKEN_RANGE;
+  for (int row = 0; row <= k; ++row) {
+    if (idx_s[row] < 0 || idx_s[row] >= vocab) st |= SPEC_ST_NONFINITE;
+    if (idx_out) idx_out[row] = idx_s[row];
+  }
+  int L = k;
+  for (int i = 0; i < k; ++i)
+    if (draft[i] != idx_s[i]) {
+      L = i;
+      break;
+    }
+  int next = idx_s[L];
+  const bool appended = step_state ? step_state[1] != 0 : has_kv != 0;
+  const int n_past = step_state ? step_state[0] : (has_kv ? *kv.seq_len - (k + 1) : 0);
+  if (st) {
+    L = 0;
+    next = -1;
+    if (has_kv && appended) kv_rollback_dev(kv, n_past);
+  } else if (has_kv && appended) {
+    kv_rollback_dev(kv, n_past + L + 1);
+  }
+  *status = st;
+  res[0] = L;
+  res[1] = next;
+  res[2] = st;
+  res[3] = has_kv ? *kv.seq_len : 0;
+}
+
+cudaError_t launch_accept(const int32_t* idx, const float* part_val, const int32_t* part_idx,
+                          int nparts, const int32_t* draft, int k, int vocab, const KvView* kv,
+                          const int32_t* step_state, int32_t* status, int32_t* res,
+                          int32_t* idx_out, cudaStream_t st, bool pdl) {
+  cudaLaunchAttribute attrs[2];
+  cudaLaunchConfig_t cfg = make_cfg(dim3(1), dim3(32), 0, st, pdl, attrs);
+  KvView v = kv ? *kv : KvView{};
+  return cudaLaunchKernelEx(&cfg, accept_kernel, idx, part_val, part_idx, nparts, draft, k, vocab, v,
+                            kv ? 1 : 0, step_state, status, res, idx_out);
+}
+
+}  // namespace spec

@@ -1,0 +1,108 @@
+// internal.h — host-side launchers shared between the library's translation
+// units.  Not part of the public ABI (include/spec_verify.h).
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace spec {
+
+// Work plan of one skinny Q4_K GEMM.  Columns are cut into 16-wide tiles and
+// the tiles into groups of kTilesPerGroup; a work unit is (group, superblock).
+// Units are numbered group-major and CTA i of G owns units
+// [floor(i*U/G), floor((i+1)*U/G)).  Every (CTA, group) run writes one fp32
+// partial "piece" of the group's 16 x (16*kTilesPerGroup) outputs into slot
+// (i - first CTA of that group); the consumer adds the slots in order.  The
+// plan depends only on (N, K, number of SMs), never on the row count M.
+struct GemmPlan {
+  int N = 0, K = 0, nb = 0, ntiles = 0, ngroups = 0, G = 0, max_slots = 0;
+  long long U = 0;
+};
+
+constexpr int kGemmWarps = 8;
+constexpr int kGemmTilesPerWarp = 2;
+constexpr int kTilesPerGroup = kGemmWarps * kGemmTilesPerWarp;   // 16 tiles = 256 columns
+constexpr int kGemmStages = 4;
+constexpr int kMaxSlots = 8;      // pieces per group, guaranteed by make_gemm_plan
+
+GemmPlan make_gemm_plan(int N, int K, int num_sms);
+cudaError_t gemm_init_attributes();   // once per process, before any capture
+size_t gemm_smem_bytes();
+// slots of group gr, and the CTA owning a unit (host mirror of the device math)
+int plan_slots_of_group(const GemmPlan& p, int gr);
+
+// ---- launchers (all enqueue on `st`; `pdl` = programmatic dependent launch)
+cudaError_t launch_repack(const void* src, void* dst, int N, int K, cudaStream_t st);
+cudaError_t launch_gemm(const GemmPlan& p, const void* w_tiled, const uint8_t* act, float* pieces,
+                        int32_t* isc, int32_t* imn, int m_sums, cudaStream_t st, bool pdl);
+// y[m][n] = sum of the pieces, m < M
+cudaError_t launch_sum_pieces(const GemmPlan& p, const float* pieces, float* y, int M,
+                              cudaStream_t st, bool pdl);
+
+// act buffer: (K/256) superblocks of kActSBBytes bytes (fragment-ordered f16 codes,
+// min-term slot, d_a) produced from fp32 rows x[M][K]
+cudaError_t launch_quantize(const float* x, int M, int K, uint8_t* act, int8_t* q_dbg,
+                            float* da_dbg, int32_t* A_dbg, int32_t* status, cudaStream_t st,
+                            bool pdl);
+
+// residual add of GEMM pieces (optional), RMSNorm with gain, quantise -> act.
+// x_out = x_in + pieces (x_out may equal x_in, or be NULL without pieces);
+// xnorm_out (optional) receives the normalised rows.
+cudaError_t launch_resid_norm_quant(const GemmPlan* p, const float* pieces, const float* x_in,
+                                    float* x_out, const float* gamma, float eps, int M, int H,
+                                    uint8_t* act, float* xnorm_out, int32_t* status,
+                                    cudaStream_t st, bool pdl);
+
+// h = silu(gate) * up from the gate|up GEMM pieces, quantised -> act (K = F)
+cudaError_t launch_swiglu_quant(const GemmPlan& p, const float* pieces, int M, int F,
+                                uint8_t* act, int32_t* status, cudaStream_t st, bool pdl);
+
+// QKV pieces -> Q attention fragments; K,V rows -> bf16 cache at positions seq_len-M+i
+struct KvView {
+  uint16_t* pool;            // bf16 bits
+  int32_t* page_table;
+  int32_t* seq_len;
+  int32_t* free_stack;
+  int32_t* free_top;
+  int num_pages, max_seq_pages, n_layers, n_kv, head_dim, page_size;
+};
+cudaError_t launch_qkv_post(const GemmPlan& p, const float* pieces, int M, int nq, int nkv,
+                            int dh, const KvView& kv, int layer, uint8_t* qfrag,
+                            const int32_t* status, cudaStream_t st, bool pdl);
+
+// verify attention: partials then merge (+ quantise for the O projection)
+struct AttnPlan {
+  int nq = 0, nkv = 0, dh = 0, max_ctx = 0, chunk = 0, max_chunks = 0;
+};
+AttnPlan make_attn_plan(int nq, int nkv, int dh, int max_ctx);
+size_t attn_partial_floats(const AttnPlan& a, int max_rows);
+// Q fragments (bf16 hi/lo, nq * 8 KB) from fp32 q [M][nq][128]; rows >= M zero
+size_t qfrag_bytes(int nq);
+cudaError_t launch_q_to_frag(const float* q, int M, int nq, uint8_t* qfrag, cudaStream_t st, bool pdl);
+cudaError_t launch_attention(const AttnPlan& a, const KvView& kv, int layer, const uint8_t* qfrag,
+                             int M, float* part, float* out, uint8_t* act, int32_t* status,
+                             cudaStream_t st, bool pdl);
+
+// LM head argmax over the head GEMM pieces: per-(CTA,row) partial (value, index)
+int head_argmax_blocks(int V);
+cudaError_t launch_head_argmax(const GemmPlan& p, const float* pieces, int M, float* logits,
+                               float* part_val, int32_t* part_idx, int32_t* status,
+                               cudaStream_t st, bool pdl);
+cudaError_t launch_argmax_final(const float* part_val, const int32_t* part_idx, int nparts, int M,
+                                int32_t* idx, cudaStream_t st, bool pdl);
+
+// KV metadata kernels
+cudaError_t launch_kv_reset(const KvView& kv, cudaStream_t st);
+// map pages for [seq_len, seq_len + n); commit seq_len += n when `commit`
+// (a step reserves its block; extend commits).  `draft`/`k`/`vocab` (optional)
+// validate the draft tokens first; on any failure nothing changes.
+cudaError_t launch_kv_reserve(const KvView& kv, int n, int commit, const int32_t* draft, int k,
+                              int vocab, int32_t* status, int32_t* step_state, cudaStream_t st,
+                              bool pdl);
+cudaError_t launch_kv_rollback(const KvView& kv, int new_len, int32_t* status, cudaStream_t st);
+// accept + rollback; idx [k+1] from head_argmax final reduce (or given)
+cudaError_t launch_accept(const int32_t* idx, const float* part_val, const int32_t* part_idx,
+                          int nparts, const int32_t* draft, int k, int vocab, const KvView* kv,
+                          const int32_t* step_state, int32_t* status, int32_t* res,
+                          int32_t* idx_out, cudaStream_t st, bool pdl);
+
+}  // namespace spec

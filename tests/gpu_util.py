@@ -1,0 +1,21 @@
+"""Helpers for the GPU parity tests (the CUDA path is called through the C ABI)."""
+import numpy as np
+
+TOL = 1e-3   # max-relative tolerance on fp32 outputs (logits, attention, GEMM y)
+
+
+def rel_err(y: np.ndarray, r: np.ndarray) -> float:
+    """max |y - r| / max(|r|, rms of r's row): the floored max-relative error."""
+    y = np.asarray(y, dtype=np.float64)
+    r = np.asarray(r, dtype=np.float64)
+    r2 = r.reshape(-1, r.shape[-1]) if r.ndim > 1 else r[None, :]
+    y2 = y.reshape(r2.shape)
+    rms = np.sqrt(np.mean(r2 ** 2, axis=1, keepdims=True))
+    den = np.maximum(np.abs(r2), np.maximum(rms, 1e-30))
+    return float(np.max(np.abs(y2 - r2) / den))
+
+
+def assert_close(y, r, tol=TOL, what=""):
+    e = rel_err(y, r)
+    assert e <= tol, f"{what}: floored max-rel error {e:.3e} > {tol}"
+    return e

@@ -289,6 +289,19 @@ SPEC_API int spec_gemm_q4k_sums(spec_ctx* ctx, const void* w_tiled, int N, int K
                        const float* x, int M, float* y,
                        int32_t* isc, int32_t* imn);
 
+/* The same GEMM for callers that must not allocate device memory (no ctx).
+ * The pages have no counterpart; this exists for hosts where calling the CUDA
+ * allocator is not allowed or not safe at the call site.  Scratch (activation
+ * buffer and partial sums) lives in a fixed 8 MiB array that every device
+ * loading the library holds until exit; requests that do not fit return
+ * SPEC_ECAPACITY before anything is enqueued.  All calls on a device share
+ * that array: calls that overlap on the GPU race, calls ordered on one stream
+ * do not.  The first call on a device looks up the array's device address
+ * (make it before capturing any stream).  Enqueued on cuda_stream (a
+ * cudaStream_t, NULL = legacy default stream); y is DEVICE fp32 [M][N]. */
+SPEC_API int spec_gemm_q4k_noalloc(const void* w_tiled, int N, int K, const float* x, int M,
+                                   float* y, void* cuda_stream);
+
 /* Final RMSNorm (gain final_norm, NULL = ones) + LM head (TILED Q4_K,
  * N = cfg.vocab, K = cfg.hidden) + per-row argmax, lowest index on ties.
  * x DEVICE fp32 [M][H]; idx DEVICE int32 [M]; logits DEVICE fp32 [M][V] or

@@ -73,6 +73,7 @@ _SIGS = {
     "spec_accept": (I, [P, P, P, I, C.POINTER(spec_kv), P]),
     "spec_profile_gemms": (I, [P, I]),
     "spec_profile_read": (I, [P, C.POINTER(C.c_float), C.POINTER(C.c_int)]),
+    "spec_gemm_q4k_noalloc": (I, [P, I, I, P, I, P, P]),
 }
 
 _lib = None
@@ -204,3 +205,7 @@ def spec_profile_read(ctx):
     ms, n = C.c_float(), C.c_int()
     check("spec_profile_read", _call("spec_profile_read", ctx, C.byref(ms), C.byref(n)))
     return ms.value, n.value
+
+
+def spec_gemm_q4k_noalloc(w, N, K, x, M, y, stream) -> int:
+    return _call("spec_gemm_q4k_noalloc", P(w), N, K, P(x), M, P(y), P(stream or 0))

@@ -307,7 +307,7 @@ static int gemm_common(spec_ctx* c, const void* w, int N, int K, const float* x,
   if (pieces_need(p) > c->pieces_floats) return SPEC_ECAPACITY;
   if (!aligned(w) || !aligned(x)) return SPEC_EALIGN;
   SPEC_TRY(launch_quantize(x, M, K, c->act, nullptr, nullptr, nullptr, c->status, c->stream, false));
-  SPEC_TRY(launch_gemm(p, w, c->act, c->pieces, isc, imn, M, c->stream, true));
+  SPEC_TRY(launch_gemm(p, w, c->act, c->pieces, isc, imn, M, c->status, c->stream, true));
   SPEC_TRY(launch_sum_pieces(p, c->pieces, y, M, c->stream, true));
   return SPEC_OK;
 }
@@ -330,7 +330,7 @@ int spec_lm_head_argmax(spec_ctx* c, const void* w_head, const float* final_norm
   const spec_config& g = c->cfg;
   SPEC_TRY(launch_resid_norm_quant(nullptr, nullptr, x, nullptr, final_norm, g.rms_eps, M, g.hidden,
                                    c->act, nullptr, c->status, c->stream, false));
-  SPEC_TRY(launch_gemm(c->p_head, w_head, c->act, c->pieces, nullptr, nullptr, 0, c->stream, true));
+  SPEC_TRY(launch_gemm(c->p_head, w_head, c->act, c->pieces, nullptr, nullptr, 0, c->status, c->stream, true));
   SPEC_TRY(launch_head_argmax(c->p_head, c->pieces, M, logits, c->head_val, c->head_idx, c->status,
                               c->stream, true));
   SPEC_TRY(launch_argmax_final(c->head_val, c->head_idx, c->head_parts, M, idx, c->stream, true));
@@ -424,7 +424,7 @@ static int enqueue_step(spec_ctx* c, const spec_weights* w, spec_kv* kv, const f
       cudaError_t e = cudaEventRecord(c->prof_ev[2 * c->prof_n], st);
       if (e != cudaSuccess) return e;
     }
-    cudaError_t e = launch_gemm(p, wt, c->act, c->pieces, nullptr, nullptr, 0, st, !prof);
+    cudaError_t e = launch_gemm(p, wt, c->act, c->pieces, nullptr, nullptr, 0, c->status, st, !prof);
     if (e != cudaSuccess) return e;
     if (prof) {
       e = cudaEventRecord(c->prof_ev[2 * c->prof_n + 1], st);

@@ -5,20 +5,36 @@
 // k-quant weights with k+1 = 16 rows per weight read (Ch. 33 §33.1, Ch. 8 §8.1)
 // and the weights are consumed in their k-quant form (Ch. 8 §8.5).
 //
-// How the integers stay exact on f16 tensor cores:
-//   * a weight code q (0..15) times its 6-bit sub-scale sc is at most 945 and
-//     an activation code is in [-127, 127]: both are exact f16 integers;
-//   * the f16 weight operand sc*q is built as fma(1024+q, sc, -1024*sc): the
-//     LOP3 "magic" 0x6400|q is the f16 number 1024+q, and a fused multiply-add
-//     rounds the exact result sc*q once, i.e. not at all;
-//   * products accumulate in f32; four sub-blocks contribute at most
-//     4*32*945*127 < 2^24, so the two half-superblock accumulators are exact
-//     integers and their f32 sum is the exact ISc rounded once, as (float)ISc;
-//   * the min term IMn = sum_j m_j A_j is one more MMA per superblock with the
-//     activation sums split as A_j = 64*hi_j + lo_j (both exact in f16).
+// How the integers stay exact on the tensor cores (tcgen05.mma):
+//   * a 4-bit weight code q, kept as the byte q (0..15), is the e4m3 number
+//     q * 2^-9: codes 0..7 are the subnormals m * 2^-9 and codes 8..15 the
+//     first normal binade (8 + m) * 2^-9.  Masking the code bytes with
+//     0x0F0F0F0F (and shifting by 4 for the high nibbles) is the whole unpack;
+//   * an 8-bit activation code is split as 16*h + l (both exact e4m3 values),
+//     and the two MMAs A*B_hi and A*B_lo (kind::f8f6f4, K = 32 = one
+//     sub-block) chain into one f32 accumulator: D_j = 2^-9 * S_j exactly,
+//     |S_j| <= 32*15*127 = 60960;
+//   * the sub-block scales are applied in the combine step in f32:
+//     sum_j sc_j D_j over sub-blocks 0-3 and 4-7 separately are exact
+//     (each below 2^24 units of 2^-9), and their sum rounds once, giving
+//     (float)ISc * 2^-9; the factor 2^9 is folded into the superblock scale d
+//     (exact), so d*ISc rounds exactly as in the plain formula;
+//   * the min term IMn = sum_j m_j A_j is one more MMA per superblock
+//     (kind::f16) with the activation sums split as A_j = 64*hi_j + lo_j.
 // The per-superblock combination d_a*(d*ISc - dmin*IMn) uses packed f32x2
 // operations, each rounded on its own (no contraction), and the superblock
 // values accumulate in f32 in superblock order.
+//
+// Work split: one CTA per SM owns 128 weight columns at a time.  Eight
+// unpack warps (two threads per column, sub-blocks 0-3 and 4-7) turn a
+// column's 144-byte superblock into e4m3 code bytes and store them into TMEM
+// lane c (the MMA's A operand, M = 128 rows = columns of W); the 16 activation
+// rows are the MMA's N = 16 columns, read from shared memory (B operand).  Two
+// more warps issue the MMAs (sub-blocks 0-3, and 4-7 plus the min term: one
+// thread issuing all 17 serialises on the issue latency), and one warp issues
+// the bulk copies that stage weights and activations.  A and D are
+// double-buffered in TMEM, so superblock i is unpacked while the MMAs of
+// superblock i-1 run and its results are combined right after.
 //
 // Row i's result depends only on row i's codes and on the fixed (K, N)
 // work plan, so it is identical for every M (batch-height invariance, "The
@@ -31,72 +47,33 @@
 namespace spec {
 
 // ---------------------------------------------------------------------------
-// k-slot permutation.  An m16n8k16 step s (0..15) of superblock b covers 16
-// k-slots; lane quad position t (0..3) owns slots {2t, 2t+1} ("pair A") and
-// {2t+8, 2t+9} ("pair B") of every step.  Slots are mapped to superblock
-// elements so that lane t only ever meets sub-blocks 2t and 2t+1:
-//   pair A, slot 2t+u   -> element 64t + 2s + u        (sub-block 2t)
-//   pair B, slot 2t+8+u -> element 64t + 32 + 2s + u   (sub-block 2t+1)
-// The activation fragments use the same map, so the dot product is unchanged;
-// each lane then needs the sub-scales of 2 sub-blocks instead of 8.
-//
-// Tiled layout of one (tile of 16 columns, superblock) block of 2304 bytes:
-//   [0, 2048)    codes: chunk q (0..3) at 512q; lane L = 4g+t owns 16 bytes at
-//                512q + 16L = words { W(g,A,q), W(g+8,A,q), W(g,B,q), W(g+8,B,q) }.
-//                W(c, P, q) holds, for steps s = 4q+p (p = 0..3), the codes of
-//                column c at the pair-P elements of step s: the even element in
-//                bits 4p..4p+3, the odd one in bits 16+4p..16+4p+3.
-//   [2048, 2112) column c: (d, dmin) binary16 pair at 2048 + 4c
-//   [2112, 2304) column c: the 12-byte 6-bit scale/min field at 2112 + 12c
+// Tiled layout: superblocks are regrouped so that the 128 columns of a tile
+// are contiguous per superblock; bytes inside a superblock are unchanged.
+// Tile T (columns 128T .. 128T+cols(T)-1, cols(T) = min(128, N-128T)),
+// superblock b, column c: byte offset 128*T*nb*144 + (b*cols(T) + c)*144.
 // ---------------------------------------------------------------------------
-
-__device__ __forceinline__ int canon_code(const uint8_t* sb, int e) {
-  int j = e >> 5, r = e & 31;
-  uint8_t byte = sb[16 + 16 * j + (r & 15)];
-  return r < 16 ? (byte & 15) : (byte >> 4);
+__host__ __device__ __forceinline__ size_t tiled_offset(int N, int nb, int col, int b) {
+  const int T = col / kGemmCols, c = col % kGemmCols;
+  const int cols = min(kGemmCols, N - kGemmCols * T);
+  return ((size_t)kGemmCols * T * nb + (size_t)b * cols + c) * kSB;
 }
 
-__global__ void repack_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, int nb,
-                              long long nblocks) {
-  long long blk = blockIdx.x;
-  if (blk >= nblocks) return;
-  int tile = (int)(blk / nb), b = (int)(blk % nb);
-  uint8_t* out = dst + blk * kTileSB;
-  for (int w = threadIdx.x; w < kTileSB / 4; w += blockDim.x) {
-    uint32_t word = 0;
-    if (w < 512) {
-      const int q = w >> 7, L = (w >> 2) & 31, sl = w & 3;
-      const int g = L >> 2, t = L & 3;
-      const int c = g + 8 * (sl & 1);
-      const int pairB = sl >> 1;
-      const uint8_t* sb = src + ((size_t)(tile * 16 + c) * nb + b) * kSB;
-#pragma unroll
-      for (int p = 0; p < 4; ++p) {
-        const int s = 4 * q + p;
-        const int e = 64 * t + 32 * pairB + 2 * s;
-        word |= (uint32_t)canon_code(sb, e) << (4 * p);
-        word |= (uint32_t)canon_code(sb, e + 1) << (16 + 4 * p);
-      }
-    } else if (w < 528) {
-      int c = w - 512;
-      const uint8_t* sb = src + ((size_t)(tile * 16 + c) * nb + b) * kSB;
-      word = sb[0] | (sb[1] << 8) | (sb[2] << 16) | ((uint32_t)sb[3] << 24);
-    } else {
-      int i = w - 528;            // 48 words of scales: column i/3, word i%3
-      int c = i / 3, wi = i % 3;
-      const uint8_t* sb = src + ((size_t)(tile * 16 + c) * nb + b) * kSB + 4 + 4 * wi;
-      word = sb[0] | (sb[1] << 8) | (sb[2] << 16) | ((uint32_t)sb[3] << 24);
-    }
-    reinterpret_cast<uint32_t*>(out)[w] = word;
-  }
+__global__ void repack_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, int N, int nb) {
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;   // 16-byte chunk
+  const long long total = (long long)N * nb * (kSB / 16);
+  if (i >= total) return;
+  const long long sbi = i / (kSB / 16);
+  const int part = (int)(i - sbi * (kSB / 16));
+  const int col = (int)(sbi / nb), b = (int)(sbi % nb);
+  dst[tiled_offset(N, nb, col, b) / 16 + part] = src[i];
 }
 
 cudaError_t launch_repack(const void* src, void* dst, int N, int K, cudaStream_t st) {
-  int nb = K / 256;
-  long long nblocks = (long long)(N / 16) * nb;
-  if (nblocks == 0) return cudaSuccess;
-  repack_kernel<<<(unsigned)nblocks, 192, 0, st>>>(static_cast<const uint8_t*>(src),
-                                                   static_cast<uint8_t*>(dst), nb, nblocks);
+  const int nb = K / 256;
+  const long long total = (long long)N * nb * (kSB / 16);
+  if (total == 0) return cudaSuccess;
+  repack_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(static_cast<const uint4*>(src),
+                                                                  static_cast<uint4*>(dst), N, nb);
   return cudaGetLastError();
 }
 
@@ -107,6 +84,11 @@ __host__ __device__ __forceinline__ int cta_of_unit(long long x, long long U, in
   return (int)(((x + 1) * (long long)G - 1) / U);
 }
 
+int plan_slots_of_group(const GemmPlan& p, int gr) {
+  long long first = (long long)gr * p.nb, last = first + p.nb - 1;
+  return cta_of_unit(last, p.U, p.G) - cta_of_unit(first, p.U, p.G) + 1;
+}
+
 GemmPlan make_gemm_plan(int N, int K, int num_sms) {
   GemmPlan p;
   p.N = N;
@@ -115,7 +97,7 @@ GemmPlan make_gemm_plan(int N, int K, int num_sms) {
   p.ntiles = N / 16;
   p.ngroups = (p.ntiles + kTilesPerGroup - 1) / kTilesPerGroup;
   p.U = (long long)p.ngroups * p.nb;
-  long long G = num_sms;
+  long long G = (long long)num_sms * kGemmCtasPerSm;
   if (G > p.U) G = p.U;
   // at most kMaxSlots CTAs may share a group: each CTA then owns >= nb/6 units
   const long long cap = (6 * p.U) / (p.nb > 0 ? p.nb : 1);
@@ -135,283 +117,343 @@ GemmPlan make_gemm_plan(int N, int K, int num_sms) {
   return p;
 }
 
-int plan_slots_of_group(const GemmPlan& p, int gr) {
-  long long first = (long long)gr * p.nb, last = first + p.nb - 1;
-  return cta_of_unit(last, p.U, p.G) - cta_of_unit(first, p.U, p.G) + 1;
-}
-
-constexpr int kStageWeightBytes = kTilesPerGroup * kTileSB;
-constexpr int kStageBytes = kStageWeightBytes + kActSBBytes;
+constexpr int kStageWeightBytes = kGemmCols * kSB;            // 18432
+constexpr int kStageBytes = kStageWeightBytes + kActSBBytes;   // 27200
+constexpr int kTmemCols = 512;
+// TMEM columns: A buffer b = 0, 1 at 72*b: sub-block j's 32 code bytes in
+// columns 8j .. 8j+7 (four codes per column, lowest k in the low byte), the
+// min-term A' (f16, K = 16) in columns 64 .. 71.  D buffer b = 0, 1 at
+// 144 + 144*b: sub-block j's 16 rows in columns 16j .. 16j+15, the min term in
+// 128 .. 143.
+constexpr int kTmemA = 0, kTmemAStride = 72, kTmemAm = 64, kTmemD0 = 144, kTmemDStride = 144,
+              kTmemDm = 128;
+constexpr int kDBufs = 2;
 
 size_t gemm_smem_bytes() { return (size_t)kGemmStages * kStageBytes; }
 
-// ---------------------------------------------------------------------------
-// the GEMM kernel
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ void mma16816_zc(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                            uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%10,%10,%10,%10};\n"
-      : "=f"(c[0]), "=f"(c[1]), "=f"(c[2]), "=f"(c[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.0f));
+// four code words of one sub-block (16 bytes, element r < 16 in the low nibble
+// of byte r, element 16 + r in its high nibble) -> 8 TMEM columns of e4m3 code
+// bytes in natural order: column t = elements 4t .. 4t+3
+__device__ __forceinline__ void unpack_sub(const uint4& c, uint32_t* r) {
+  const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    r[t] = w[t] & 0x0F0F0F0Fu;
+    r[4 + t] = (w[t] >> 4) & 0x0F0F0F0Fu;
+  }
 }
 
-// f16x2 constants for one (column, sub-block) with 6-bit scale sc:
-//   S = {sc, sc}, O = {-1024 sc, ...} for codes held as 1024+q (mask 0x000F);
-//   S16 = {sc/16, ...}, O16 = {-64 sc, ...} for codes held as 1024+16q (mask 0x00F0).
-// Every value is an exact f16 (sc <= 63), so fma(x, S, O) = sc*q exactly.
-struct ScaleC {
-  uint32_t S, O, S16, O16;
-};
-__device__ __forceinline__ ScaleC scale_consts(uint32_t sc) {
-  ScaleC r;
-  const uint32_t v = sc * 0x00010001u + 0x64006400u;   // {1024+sc, 1024+sc}
-  r.S = hadd2_u32(v, 0xE400E400u);                      // - 1024
-  r.O = hmul2_u32(r.S, 0xE400E400u);                    // * -1024
-  r.S16 = hmul2_u32(r.S, 0x2C002C00u);                  // * 1/16
-  r.O16 = hmul2_u32(r.S, 0xD400D400u);                  // * -64
-  return r;
+__device__ __forceinline__ uint32_t sub_scale(uint32_t f0, uint32_t f1, uint32_t f2, int j) {
+  const int pos = 6 * j;                       // compile-time after unrolling
+  return __funnelshift_r(pos < 32 ? f0 : f1, pos < 32 ? f1 : f2, pos & 31) & 63u;
 }
 
-// codes at bits (0,16) of x -> {sc*q_lo, sc*q_hi}
-__device__ __forceinline__ uint32_t unpack_lo(uint32_t x, const ScaleC& c) {
-  return hfma2_u32(lop3_and_or(x, 0x000F000Fu, 0x64006400u), c.S, c.O);
+SPEC_DEV void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                 "=r"(r[7])
+               : "r"(taddr));
 }
-// codes at bits (4,20) of x -> {sc*q_lo, sc*q_hi}
-__device__ __forceinline__ uint32_t unpack_hi(uint32_t x, const ScaleC& c) {
-  return hfma2_u32(lop3_and_or(x, 0x00F000F0u, 0x64006400u), c.S16, c.O16);
-}
+
+// Roles and hand-offs of one CTA.  Unit i = (group, superblock) number i of
+// this CTA's range; it lives in stage slot s = i % kGemmStages and in TMEM
+// A and D buffers i % 2.  Every wait is bounded in wall time (kWaitNs); a
+// thread that gives up sets SPEC_ST_DEVICE_WAIT and leaves its loop, and the
+// threads that depend on it give up in turn.
+//   producer (warp 8, lane 0): wait empty[s] (unit i-S combined) -> expect the
+//     unit's bytes on full[s] -> bulk-copy its 128 weight superblocks and its
+//     activation block into slot s.
+//   unpack warps 0..7, iteration i: wait full[s] -> unpack unit i into A[i%2]
+//     (free: the MMAs of unit i-2 were seen complete in iteration i-1) ->
+//     arrive a_full[i%2] -> wait mma_done of unit i-1 -> read its D, arrive
+//     d_free -> read its scales from its slot, arrive empty -> combine it.
+//   MMA warps 9, 10 (lane 0), unit i: wait full[s], a_full[i%2] and the
+//     d_free of unit i-2 -> issue the MMAs of sub-blocks 0-3 (warp 9) or 4-7
+//     plus the min term (warp 10) into D[i%2] -> commit to mma_done[i%2] (two
+//     arrivals per phase).
+constexpr uint64_t kWaitNs = 2000000000ull;
 
 template <bool SUMS>
-__global__ void __launch_bounds__(kGemmWarps * 32, 1)
+__global__ void __launch_bounds__(kGemmThreads, 1)
 gemm_q4k_kernel(const uint8_t* __restrict__ wt, const uint8_t* __restrict__ act,
-                float* __restrict__ pieces, int N, int nb, int ntiles, int U, int G,
-                int32_t* __restrict__ isc_out, int32_t* __restrict__ imn_out, int m_sums) {
+                float* __restrict__ pieces, int N, int nb, int U, int G,
+                int32_t* __restrict__ isc_out, int32_t* __restrict__ imn_out, int m_sums,
+                int32_t* status) {
   extern __shared__ __align__(128) uint8_t smem[];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = lane >> 2, t = lane & 3;
+  __shared__ uint32_t tmem_slot;
+  __shared__ __align__(8) uint64_t full[kGemmStages], empty[kGemmStages];
+  __shared__ __align__(8) uint64_t a_full[2], mma_done[kDBufs], d_free[kDBufs];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int lg = warp & 3, hf = (warp >> 2) & 1;    // TMEM lane group; sub-block half / row half
+  const int col_local = 32 * lg + lane;             // weight column inside the tile
   const int u0 = (int)((long long)blockIdx.x * U / G);
   const int u1 = (int)((long long)(blockIdx.x + 1) * U / G);
+  const int nunits = u1 - u0;
 
-  // lane constants: bit positions of (sc_2t, sc_2t+1) and (m_2t, m_2t+1) in the field
-  const int ws = (12 * t) >> 5, sh_s = (12 * t) & 31;
-  const int wm = (48 + 12 * t) >> 5, sh_m = (48 + 12 * t) & 31;
+  if (warp == 0) tmem_alloc(&tmem_slot, kTmemCols);
+  if (tid == 0) {
+    for (int b = 0; b < kGemmStages; ++b) {
+      mbar_init(&full[b], 1);
+      mbar_init(&empty[b], kGemmUnpackThreads);
+    }
+    for (int b = 0; b < 2; ++b) mbar_init(&a_full[b], kGemmUnpackThreads);
+    for (int b = 0; b < kDBufs; ++b) {
+      mbar_init(&mma_done[b], 2);
+      mbar_init(&d_free[b], kGemmUnpackThreads);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
 
-  // copy cursor (unit being issued) and its (group, superblock)
-  int iu = u0, ig = u0 / nb, ib = u0 - (u0 / nb) * nb;
-  auto issue_weights = [&](int slot) {
-    uint8_t* dst = smem + slot * kStageBytes + warp * kGemmTilesPerWarp * kTileSB;
-    const int tile0 = ig * kTilesPerGroup + warp * kGemmTilesPerWarp;
-    const uint8_t* src0 = wt + ((size_t)tile0 * nb + ib) * kTileSB;
-    const uint8_t* src1 = src0 + (size_t)nb * kTileSB;
-    const bool ok0 = tile0 < ntiles, ok1 = tile0 + 1 < ntiles;
-#pragma unroll
-    for (int i = 0; i < 2 * kTileSB / 16 / 32; ++i) {
-      const int c = lane + 32 * i;
-      if (c < kTileSB / 16) {
-        if (ok0) cp_async16(dst + c * 16, src0 + c * 16);
-      } else {
-        if (ok1) cp_async16(dst + c * 16, src1 + (c - kTileSB / 16) * 16);
+  if (warp == 8) {
+    // ------------------------------------------------------------- producer
+    if (lane == 0) {
+      const uint64_t pol_w = l2_policy_evict_first(), pol_a = l2_policy_evict_last();
+      bool ok = true;
+      int issued = 0;
+      int g = u0 / nb, b = u0 - (u0 / nb) * nb;
+      auto weights_of = [&](int gg, int bb, uint32_t& bytes) {
+        const int cols = min(kGemmCols, N - kGemmCols * gg);
+        bytes = (uint32_t)(cols * kSB);
+        return wt + ((size_t)kGemmCols * gg * nb + (size_t)bb * cols) * kSB;
+      };
+      // weights of the first stages do not depend on the previous kernel
+      const int pre = min(nunits, kGemmStages);
+      {
+        int gg = g, bb = b;
+        for (int i = 0; i < pre; ++i) {
+          uint32_t wb;
+          const uint8_t* src = weights_of(gg, bb, wb);
+          mbar_arrive_expect_tx(&full[i], wb + (uint32_t)kActSBBytes);
+          bulk_g2s(smem + i * kStageBytes, src, wb, &full[i], pol_w);
+          if (++bb == nb) { bb = 0; ++gg; }
+        }
       }
+      pdl_wait();
+      pdl_trigger();
+      for (int i = 0; i < nunits; ++i) {
+        const int s = i % kGemmStages;
+        if (i >= kGemmStages) {
+          if (!mbar_wait_ns(&empty[s], ((i / kGemmStages) - 1) & 1, kWaitNs)) {
+            ok = false;
+            break;
+          }
+          uint32_t wb;
+          const uint8_t* src = weights_of(g, b, wb);
+          mbar_arrive_expect_tx(&full[s], wb + (uint32_t)kActSBBytes);
+          bulk_g2s(smem + s * kStageBytes, src, wb, &full[s], pol_w);
+        }
+        bulk_g2s(smem + s * kStageBytes + kStageWeightBytes, act + (size_t)b * kActSBBytes,
+                 (uint32_t)kActSBBytes, &full[s], pol_a);
+        issued = i + 1;
+        if (++b == nb) { b = 0; ++g; }
+      }
+      if (!ok) atomicOr(status, SPEC_ST_DEVICE_WAIT);
+      // no copy may still be writing shared memory when the CTA exits
+      for (int u = max(0, issued - kGemmStages); u < issued; ++u)
+        mbar_wait_ns(&full[u % kGemmStages], (u / kGemmStages) & 1, kWaitNs);
     }
-  };
-  auto issue_act = [&](int slot) {
-    uint8_t* dst = smem + slot * kStageBytes + kStageWeightBytes;
-    const uint8_t* src = act + (size_t)ib * kActSBBytes;
-    for (int c = threadIdx.x; c < kActSBBytes / 16; c += kGemmWarps * 32) cp_async16(dst + c * 16, src + c * 16);
-  };
-  auto advance = [&]() {
-    ++iu;
-    if (++ib == nb) {
-      ib = 0;
-      ++ig;
-    }
-  };
-
-  // Weights do not depend on the previous kernel: stream them first, then wait
-  // for the producer of the activations.
-  {
-    const int su = iu, sg = ig, sb = ib;
-    for (int s = 0; s < kGemmStages - 1; ++s) {
-      if (iu < u1) issue_weights(s);
-      advance();
-    }
-    iu = su;
-    ig = sg;
-    ib = sb;
+  } else if (warp >= 9) {
+    // ------------------------------------------------------------------ MMA
     pdl_wait();
     pdl_trigger();
-    for (int s = 0; s < kGemmStages - 1; ++s) {
-      if (iu < u1) issue_act(s);
-      cp_async_commit();
-      advance();
-    }
-  }
-
-  // output accumulators as packed f32 pairs: [tile][h*2 + column half]
-  unsigned long long yacc[kGemmTilesPerWarp][4];
+    if (lane == 0) {
+      const int hh = warp - 9;
+      // D f32, A and B e4m3 (kind::f8f6f4) or f16 (kind::f16): both format codes 0
+      constexpr uint32_t kIdesc = (1u << 4) | ((16u >> 3) << 17) | ((128u >> 4) << 24);
+      bool ok = true;
+      int last = -1;
+      for (int i = 0; i < nunits; ++i) {
+        const int s = i % kGemmStages;
+        ok = mbar_wait_ns(&full[s], (i / kGemmStages) & 1, kWaitNs) &&
+             mbar_wait_ns(&a_full[i & 1], (i >> 1) & 1, kWaitNs) &&
+             (i < kDBufs || mbar_wait_ns(&d_free[i % kDBufs], ((i - kDBufs) / kDBufs) & 1, kWaitNs));
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t d = tmem + (uint32_t)(kTmemD0 + (i % kDBufs) * kTmemDStride);
+        const uint32_t a = tmem + (uint32_t)(kTmemA + (i & 1) * kTmemAStride);
+        // B blocks: hi of sub-block j at 1024*j, lo at +512 (descriptor units of 16 B)
+        const uint64_t desc0 = smem_desc(smem_u32(smem + s * kStageBytes + kStageWeightBytes), 128, 256);
 #pragma unroll
-  for (int tt = 0; tt < kGemmTilesPerWarp; ++tt)
-#pragma unroll
-    for (int i = 0; i < 4; ++i) yacc[tt][i] = 0ull;
-
-  int cgrp = u0 / nb, cb = u0 - (u0 / nb) * nb;   // compute cursor
-  int slot = 0, islot = kGemmStages - 1;
-  for (int u = u0; u < u1; ++u) {
-    cp_async_wait<kGemmStages - 2>();
-    __syncthreads();
-    if (iu < u1) {
-      issue_weights(islot);
-      issue_act(islot);
-    }
-    cp_async_commit();
-    advance();
-    islot = (islot + 1 == kGemmStages) ? 0 : islot + 1;
-
-    const uint8_t* stg = smem + slot * kStageBytes;
-    const uint8_t* ast = stg + kStageWeightBytes;
-    slot = (slot + 1 == kGemmStages) ? 0 : slot + 1;
-
-    uint4 nib[kGemmTilesPerWarp][4];
-    ScaleC sc[kGemmTilesPerWarp][2][2];     // [tile][column g, g+8][pair A, B]
-    uint32_t mfrag[kGemmTilesPerWarp][2];
-    uint32_t ddw[kGemmTilesPerWarp][2];
-#pragma unroll
-    for (int tt = 0; tt < kGemmTilesPerWarp; ++tt) {
-      const uint8_t* wtile = stg + (warp * kGemmTilesPerWarp + tt) * kTileSB;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) nib[tt][q] = *reinterpret_cast<const uint4*>(wtile + 512 * q + 16 * lane);
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        const uint32_t* f = reinterpret_cast<const uint32_t*>(wtile + 2112 + 12 * (g + 8 * cc));
-        const uint32_t s12 = __funnelshift_r(f[ws], f[ws + 1], sh_s);
-        const uint32_t m12 = __funnelshift_r(f[wm], wm < 2 ? f[wm + 1] : 0u, sh_m);
-        sc[tt][cc][0] = scale_consts(s12 & 63u);
-        sc[tt][cc][1] = scale_consts((s12 >> 6) & 63u);
-        mfrag[tt][cc] = hadd2_u32(((m12 & 63u) | (((m12 >> 6) & 63u) << 16)) + 0x64006400u, 0xE400E400u);
-        ddw[tt][cc] = *reinterpret_cast<const uint32_t*>(wtile + 2048 + 4 * (g + 8 * cc));
-      }
-    }
-
-    float acc[kGemmTilesPerWarp][2][2][4];   // [tile][steps 0-7 | 8-15][row half][4]
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      uint4 xs[kGemmTilesPerWarp];
-#pragma unroll
-      for (int tt = 0; tt < kGemmTilesPerWarp; ++tt)
-        xs[tt] = make_uint4(nib[tt][q].x >> 8, nib[tt][q].y >> 8, nib[tt][q].z >> 8, nib[tt][q].w >> 8);
-#pragma unroll
-      for (int p = 0; p < 4; ++p) {
-        const int s = 4 * q + p;
-        const int half = s >> 3;
-        const uint4 av = *reinterpret_cast<const uint4*>(ast + s * 512 + 16 * lane);
-#pragma unroll
-        for (int tt = 0; tt < kGemmTilesPerWarp; ++tt) {
-          const uint4 x = (p < 2) ? nib[tt][q] : xs[tt];
-          uint32_t a0, a1, a2, a3;
-          if ((p & 1) == 0) {
-            a0 = unpack_lo(x.x, sc[tt][0][0]);
-            a1 = unpack_lo(x.y, sc[tt][1][0]);
-            a2 = unpack_lo(x.z, sc[tt][0][1]);
-            a3 = unpack_lo(x.w, sc[tt][1][1]);
-          } else {
-            a0 = unpack_hi(x.x, sc[tt][0][0]);
-            a1 = unpack_hi(x.y, sc[tt][1][0]);
-            a2 = unpack_hi(x.z, sc[tt][0][1]);
-            a3 = unpack_hi(x.w, sc[tt][1][1]);
-          }
-          if ((s & 7) == 0) {
-            mma16816_zc(acc[tt][half][0], a0, a1, a2, a3, av.x, av.y);
-            mma16816_zc(acc[tt][half][1], a0, a1, a2, a3, av.z, av.w);
-          } else {
-            mma16816(acc[tt][half][0], a0, a1, a2, a3, av.x, av.y);
-            mma16816(acc[tt][half][1], a0, a1, a2, a3, av.z, av.w);
-          }
+        for (int jj = 0; jj < 4; ++jj) {
+          const int j = 4 * hh + jj;
+          mma_f8_ts(d + 16 * j, a + 8 * j, desc0 + 64ull * j, kIdesc, 0);
+          mma_f8_ts(d + 16 * j, a + 8 * j, desc0 + 64ull * j + 32, kIdesc, 1);
         }
+        if (hh == 1) mma_f16_ts(d + kTmemDm, a + kTmemAm, desc0 + 32ull * 16, kIdesc, 0);
+        mma_commit(&mma_done[i % kDBufs]);
+        last = i;
       }
+      if (!ok) atomicOr(status, SPEC_ST_DEVICE_WAIT);
+      // TMEM is released at the end: the MMAs of this thread must have finished
+      if (last >= 0) mbar_wait_ns(&mma_done[last % kDBufs], (last / kDBufs) & 1, kWaitNs);
     }
+  } else {
+    // --------------------------------------------------------------- unpack
+    pdl_wait();
+    pdl_trigger();
+    const uint32_t lane_base = (uint32_t)(32 * lg) << 16;
+    bool ok = true;
+    float y[8];
+#pragma unroll
+    for (int n = 0; n < 8; ++n) y[n] = 0.f;
 
-    // min term, d/dmin/d_a combination, accumulation
-    const uint4 am = *reinterpret_cast<const uint4*>(ast + 16 * 512 + 16 * lane);
-    const float2 da0 = *reinterpret_cast<const float2*>(ast + kActSlots * 512 + 4 * (2 * t));
-    const float2 da1 = *reinterpret_cast<const float2*>(ast + kActSlots * 512 + 4 * (8 + 2 * t));
+    // combine unit u = (group ug, superblock ub): rows 8hf .. 8hf+7 of this column
+    auto combine = [&](int u, int ug, int ub) {
+      const uint32_t dbase =
+          tmem + lane_base + (uint32_t)(kTmemD0 + (u % kDBufs) * kTmemDStride + 8 * hf);
+      uint32_t dj[8][8], rm[8];
 #pragma unroll
-    for (int tt = 0; tt < kGemmTilesPerWarp; ++tt) {
-      float imn[2][4];
-      mma16816_zc(imn[0], mfrag[tt][0], mfrag[tt][1], mfrag[tt][0], mfrag[tt][1], am.x, am.y);
-      mma16816_zc(imn[1], mfrag[tt][0], mfrag[tt][1], mfrag[tt][0], mfrag[tt][1], am.z, am.w);
-      const uint32_t dd0 = ddw[tt][0], dd1 = ddw[tt][1];
-      const float d0 = __half2float(__ushort_as_half((unsigned short)(dd0 & 0xffff)));
-      const float m0f = __half2float(__ushort_as_half((unsigned short)(dd0 >> 16)));
-      const float d1 = __half2float(__ushort_as_half((unsigned short)(dd1 & 0xffff)));
-      const float m1f = __half2float(__ushort_as_half((unsigned short)(dd1 >> 16)));
-      const unsigned long long D0 = f2pack(d0, d0), M0 = f2pack(m0f, m0f);
-      const unsigned long long D1 = f2pack(d1, d1), M1 = f2pack(m1f, m1f);
+      for (int j = 0; j < 8; ++j) tmem_ld8(dbase + 16 * j, dj[j]);
+      tmem_ld8(dbase + kTmemDm, rm);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(&d_free[u % kDBufs]);
+      const int pslot = u % kGemmStages;
+      const uint8_t* stg = smem + pslot * kStageBytes;
+      const int cols = min(kGemmCols, N - kGemmCols * ug);
+      const bool valid = col_local < cols;
+      uint4 hdr = make_uint4(0, 0, 0, 0);
+      if (valid) hdr = *reinterpret_cast<const uint4*>(stg + col_local * kSB);
+      const float4* dap =
+          reinterpret_cast<const float4*>(stg + kStageWeightBytes + kActSlots * 512 + 32 * hf);
+      const float4 da0 = dap[0], da1 = dap[1];
+      mbar_arrive(&empty[pslot]);
+      const float da[8] = {da0.x, da0.y, da0.z, da0.w, da1.x, da1.y, da1.z, da1.w};
+      // d * 2^9 (exact): the D values are 2^-9 * integer sums
+      const float d = __half2float(__ushort_as_half((unsigned short)(hdr.x & 0xffff))) * 512.f;
+      const float dm = __half2float(__ushort_as_half((unsigned short)(hdr.x >> 16)));
+      unsigned long long sc2[8];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const unsigned long long DA = h == 0 ? f2pack(da0.x, da0.y) : f2pack(da1.x, da1.y);
-        // exact ISc (rounded once to f32) from the two exact half sums
-        const unsigned long long isc01 =
-            f2add(f2pack(acc[tt][0][h][0], acc[tt][0][h][1]), f2pack(acc[tt][1][h][0], acc[tt][1][h][1]));
-        const unsigned long long isc23 =
-            f2add(f2pack(acc[tt][0][h][2], acc[tt][0][h][3]), f2pack(acc[tt][1][h][2], acc[tt][1][h][3]));
-        // column g (c0, c1 of the fragment), column g+8 (c2, c3)
-        const unsigned long long v01 =
-            f2mul(DA, f2sub(f2mul(D0, isc01), f2mul(M0, f2pack(imn[h][0], imn[h][1]))));
-        const unsigned long long v23 =
-            f2mul(DA, f2sub(f2mul(D1, isc23), f2mul(M1, f2pack(imn[h][2], imn[h][3]))));
-        yacc[tt][2 * h + 0] = f2add(yacc[tt][2 * h + 0], v01);
-        yacc[tt][2 * h + 1] = f2add(yacc[tt][2 * h + 1], v23);
+      for (int j = 0; j < 8; ++j) {
+        // 6-bit scale as an exact float: 2^23 + sc with the 2^23 subtracted
+        const float f = __uint_as_float(0x4B000000u | sub_scale(hdr.y, hdr.z, hdr.w, j)) - 8388608.f;
+        sc2[j] = f2pack(f, f);
+      }
+      const unsigned long long D2 = f2pack(d, d), M2 = f2pack(dm, dm);
+#pragma unroll
+      for (int n = 0; n < 8; n += 2) {
+        unsigned long long lo = f2mul(sc2[0], f2pack(__uint_as_float(dj[0][n]), __uint_as_float(dj[0][n + 1])));
+        unsigned long long hi = f2mul(sc2[4], f2pack(__uint_as_float(dj[4][n]), __uint_as_float(dj[4][n + 1])));
+#pragma unroll
+        for (int j = 1; j < 4; ++j) {
+          lo = f2fma(sc2[j], f2pack(__uint_as_float(dj[j][n]), __uint_as_float(dj[j][n + 1])), lo);
+          hi = f2fma(sc2[4 + j], f2pack(__uint_as_float(dj[4 + j][n]), __uint_as_float(dj[4 + j][n + 1])), hi);
+        }
+        const unsigned long long isc = f2add(lo, hi);
+        const unsigned long long imn = f2pack(__uint_as_float(rm[n]), __uint_as_float(rm[n + 1]));
+        const unsigned long long v =
+            f2mul(f2pack(da[n], da[n + 1]), f2sub(f2mul(D2, isc), f2mul(M2, imn)));
+        const unsigned long long yy = f2add(f2pack(y[n], y[n + 1]), v);
+        f2unpack(yy, y[n], y[n + 1]);
         if (SUMS) {
-          const int tile = cgrp * kTilesPerGroup + warp * kGemmTilesPerWarp + tt;
-          if (tile < ntiles) {
+          float l0, l1, h0, h1;
+          f2unpack(lo, l0, l1);
+          f2unpack(hi, h0, h1);
+          const int col = kGemmCols * ug + col_local;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int row = 8 * h + 2 * t + (e & 1);
-              const int col = tile * 16 + g + 8 * (e >> 1);
-              if (row < m_sums) {
-                const size_t o = ((size_t)row * N + col) * nb + cb;
-                isc_out[o] = (int)acc[tt][0][h][e] + (int)acc[tt][1][h][e];
-                imn_out[o] = (int)imn[h][e];
-              }
+          for (int e = 0; e < 2; ++e) {
+            const int row = 8 * hf + n + e;
+            if (valid && row < m_sums) {
+              const size_t o = ((size_t)row * N + col) * nb + ub;
+              isc_out[o] = (int)((e ? l1 : l0) * 512.f) + (int)((e ? h1 : h0) * 512.f);
+              imn_out[o] = (int)__uint_as_float(rm[n + e]);
             }
           }
         }
       }
-    }
-
-    // end of this CTA's run over the group: write the piece
-    const bool last_of_group = (cb + 1 == nb);
-    if (u + 1 == u1 || last_of_group) {
-      const int slot_id = (int)blockIdx.x - cta_of_unit((long long)cgrp * nb, U, G);
-      float* base = pieces + (size_t)slot_id * 16 * N;
+      // end of this CTA's run over the group: write the piece
+      if (u0 + u + 1 == u1 || ub + 1 == nb) {
+        const int slot_id = (int)blockIdx.x - cta_of_unit((long long)ug * nb, U, G);
+        if (valid) {
+          const int col = kGemmCols * ug + col_local;
+          float* base = pieces + (size_t)slot_id * 16 * N + (size_t)(8 * hf) * N + col;
 #pragma unroll
-      for (int tt = 0; tt < kGemmTilesPerWarp; ++tt) {
-        const int tile = cgrp * kTilesPerGroup + warp * kGemmTilesPerWarp + tt;
-        if (tile < ntiles) {
-#pragma unroll
-          for (int h = 0; h < 2; ++h)
-#pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
-              float lo, hi;
-              f2unpack(yacc[tt][2 * h + cc], lo, hi);
-              const int row = 8 * h + 2 * t;
-              const int col = tile * 16 + g + 8 * cc;
-              base[(size_t)row * N + col] = lo;
-              base[(size_t)(row + 1) * N + col] = hi;
-            }
+          for (int n = 0; n < 8; ++n) base[(size_t)n * N] = y[n];
         }
 #pragma unroll
-        for (int i = 0; i < 4; ++i) yacc[tt][i] = 0ull;
+        for (int n = 0; n < 8; ++n) y[n] = 0.f;
+      }
+    };
+
+    int pg = 0, pb = 0;                       // group / superblock of unit i-1
+    int cg = u0 / nb, cb = u0 - (u0 / nb) * nb;
+    int done_units = 0;
+    for (int i = 0; i < nunits; ++i) {
+      const int s = i % kGemmStages;
+      // warp-uniform decisions: the TMEM accesses below are warp-collective
+      ok = __all_sync(0xffffffffu, mbar_wait_ns(&full[s], (i / kGemmStages) & 1, kWaitNs));
+      if (!ok) break;
+      const uint8_t* stg = smem + s * kStageBytes;
+      // ---- unpack sub-blocks 4hf .. 4hf+3 of this thread's column into TMEM A[i&1]
+      {
+        const int cols = min(kGemmCols, N - kGemmCols * cg);
+        const bool valid = col_local < cols;
+        const uint4* sbp = reinterpret_cast<const uint4*>(stg + col_local * kSB);
+        const uint32_t abase = tmem + lane_base + (uint32_t)(kTmemA + (i & 1) * kTmemAStride);
+        uint32_t r[32];
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          uint4 c = make_uint4(0, 0, 0, 0);
+          if (valid) c = sbp[1 + 4 * hf + jj];
+          unpack_sub(c, r + 8 * jj);
+        }
+        tmem_st32(abase + (uint32_t)(32 * hf), r);      // sub-blocks 4hf .. 4hf+3
+        if (hf == 0) {
+          // min-term operand: k = j -> m_j, k = 8 + j -> m_j (f16 pairs)
+          uint4 hdr = make_uint4(0, 0, 0, 0);
+          if (valid) hdr = sbp[0];
+          const uint32_t f1 = hdr.z, f2 = hdr.w;
+          uint32_t mp[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int p0 = 48 + 12 * q;           // bits of m_2q, m_2q+1
+            const uint32_t m12 = __funnelshift_r(p0 < 64 ? f1 : f2, p0 < 64 ? f2 : 0u, p0 & 31);
+            mp[q] = hadd2_u32(((m12 & 63u) | (((m12 >> 6) & 63u) << 16)) + 0x64006400u, 0xE400E400u);
+          }
+          tmem_st4(abase + (uint32_t)kTmemAm, mp[0], mp[1], mp[2], mp[3]);
+          tmem_st4(abase + (uint32_t)(kTmemAm + 4), mp[0], mp[1], mp[2], mp[3]);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&a_full[i & 1]);
+
+      // ---- combine the previous superblock while this one runs
+      if (i >= 1) {
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait_ns(&mma_done[(i - 1) % kDBufs], ((i - 1) / kDBufs) & 1, kWaitNs));
+        if (!ok) break;
+        tc_fence_after();
+        combine(i - 1, pg, pb);
+      }
+      done_units = i + 1;
+      pg = cg;
+      pb = cb;
+      if (++cb == nb) {
+        cb = 0;
+        ++cg;
       }
     }
-    if (++cb == nb) {
-      cb = 0;
-      ++cgrp;
+    if (ok && done_units > 0) {
+      const int l = done_units - 1;
+      ok = __all_sync(0xffffffffu, mbar_wait_ns(&mma_done[l % kDBufs], (l / kDBufs) & 1, kWaitNs));
+      if (ok) {
+        tc_fence_after();
+        combine(l, pg, pb);
+      }
     }
+    if (!ok && lane == 0) atomicOr(status, SPEC_ST_DEVICE_WAIT);
   }
-  cp_async_wait<0>();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
 }
 
 static bool g_gemm_attr_set[2] = {false, false};
@@ -427,7 +469,8 @@ cudaError_t gemm_init_attributes() {
 }
 
 cudaError_t launch_gemm(const GemmPlan& p, const void* w_tiled, const uint8_t* act, float* pieces,
-                        int32_t* isc, int32_t* imn, int m_sums, cudaStream_t st, bool pdl) {
+                        int32_t* isc, int32_t* imn, int m_sums, int32_t* status, cudaStream_t st,
+                        bool pdl) {
   const size_t smem = gemm_smem_bytes();
   const bool sums = isc != nullptr;
   auto kern = sums ? gemm_q4k_kernel<true> : gemm_q4k_kernel<false>;
@@ -438,7 +481,7 @@ cudaError_t launch_gemm(const GemmPlan& p, const void* w_tiled, const uint8_t* a
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.G);
-  cfg.blockDim = dim3(kGemmWarps * 32);
+  cfg.blockDim = dim3(kGemmThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
@@ -446,8 +489,8 @@ cudaError_t launch_gemm(const GemmPlan& p, const void* w_tiled, const uint8_t* a
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, kern, static_cast<const uint8_t*>(w_tiled), act, pieces, p.N,
-                            p.nb, p.ntiles, (int)p.U, p.G, isc, imn, m_sums);
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<const uint8_t*>(w_tiled), act, pieces, p.N, p.nb,
+                            (int)p.U, p.G, isc, imn, m_sums, status);
 }
 
 // y[m][n] = sum over the group's slots, in slot order

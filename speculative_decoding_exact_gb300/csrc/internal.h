@@ -18,10 +18,15 @@ struct GemmPlan {
   long long U = 0;
 };
 
-constexpr int kGemmWarps = 8;
-constexpr int kGemmTilesPerWarp = 2;
-constexpr int kTilesPerGroup = kGemmWarps * kGemmTilesPerWarp;   // 16 tiles = 256 columns
-constexpr int kGemmStages = 4;
+// tcgen05 GEMM: one CTA per SM owns 128 weight columns (one per TMEM lane);
+// 8 warps unpack and combine (two threads per column: sub-blocks 0-3 and
+// 4-7), one warp issues the bulk copies, 2 warps issue the tensor-core MMAs.
+constexpr int kGemmUnpackThreads = 256;
+constexpr int kGemmThreads = kGemmUnpackThreads + 96;
+constexpr int kTilesPerGroup = 8;          // 16-column tiles per group = 128 columns
+constexpr int kGemmCols = 16 * kTilesPerGroup;
+constexpr int kGemmStages = 6;
+constexpr int kGemmCtasPerSm = 1;
 constexpr int kMaxSlots = 8;      // pieces per group, guaranteed by make_gemm_plan
 
 GemmPlan make_gemm_plan(int N, int K, int num_sms);
@@ -33,7 +38,8 @@ int plan_slots_of_group(const GemmPlan& p, int gr);
 // ---- launchers (all enqueue on `st`; `pdl` = programmatic dependent launch)
 cudaError_t launch_repack(const void* src, void* dst, int N, int K, cudaStream_t st);
 cudaError_t launch_gemm(const GemmPlan& p, const void* w_tiled, const uint8_t* act, float* pieces,
-                        int32_t* isc, int32_t* imn, int m_sums, cudaStream_t st, bool pdl);
+                        int32_t* isc, int32_t* imn, int m_sums, int32_t* status, cudaStream_t st,
+                        bool pdl);
 // y[m][n] = sum of the pieces, m < M
 cudaError_t launch_sum_pieces(const GemmPlan& p, const float* pieces, float* y, int M,
                               cudaStream_t st, bool pdl);

@@ -95,7 +95,8 @@ extern "C" SPEC_API int spec_gemm_q4k_noalloc(const void* w_tiled, int N, int K,
   if (cudaMemsetAsync(status, 0, sizeof(int32_t), st) != cudaSuccess) return SPEC_ECUDA;
   if (launch_quantize(x, M, K, act, nullptr, nullptr, nullptr, status, st, false) != cudaSuccess)
     return SPEC_ECUDA;
-  if (launch_gemm(p, w_tiled, act, pieces, nullptr, nullptr, 0, st, true) != cudaSuccess) return SPEC_ECUDA;
+  if (launch_gemm(p, w_tiled, act, pieces, nullptr, nullptr, 0, status, st, true) != cudaSuccess)
+    return SPEC_ECUDA;
   if (launch_sum_pieces(p, pieces, y, M, st, true) != cudaSuccess) return SPEC_ECUDA;
   return SPEC_OK;
 }

@@ -25,16 +25,16 @@
 // operations, each rounded on its own (no contraction), and the superblock
 // values accumulate in f32 in superblock order.
 //
-// Work split: one CTA per SM owns 128 weight columns at a time.  Eight
-// unpack warps (two threads per column, sub-blocks 0-3 and 4-7) turn a
-// column's 144-byte superblock into e4m3 code bytes and store them into TMEM
-// lane c (the MMA's A operand, M = 128 rows = columns of W); the 16 activation
-// rows are the MMA's N = 16 columns, read from shared memory (B operand).  Two
-// more warps issue the MMAs (sub-blocks 0-3, and 4-7 plus the min term: one
-// thread issuing all 17 serialises on the issue latency), and one warp issues
-// the bulk copies that stage weights and activations.  A and D are
-// double-buffered in TMEM, so superblock i is unpacked while the MMAs of
-// superblock i-1 run and its results are combined right after.
+// Work split: one CTA per SM owns 128 weight columns at a time.  Four
+// unpack warps (one thread per column) turn a column's 144-byte superblock
+// into e4m3 code bytes and store them into TMEM lane c (the MMA's A operand,
+// M = 128 rows = columns of W); the 16 activation rows are the MMA's N = 16
+// columns, read from shared memory (B operand).  Three warps issue the 17 MMAs
+// of a superblock (one thread issuing all of them serialises on the issue
+// latency), eight warps read the results back and combine them (two threads
+// per column, 8 rows each), and one warp issues the bulk copies that stage
+// weights and activations.  A and D are double-buffered in TMEM: unpacking,
+// MMAs and combining of consecutive superblocks overlap.
 //
 // Row i's result depends only on row i's codes and on the fixed (K, N)
 // work plan, so it is identical for every M (batch-height invariance, "The
@@ -127,7 +127,6 @@ constexpr int kTmemCols = 512;
 // 128 .. 143.
 constexpr int kTmemA = 0, kTmemAStride = 72, kTmemAm = 64, kTmemD0 = 144, kTmemDStride = 144,
               kTmemDm = 128;
-constexpr int kDBufs = 2;
 
 size_t gemm_smem_bytes() { return (size_t)kGemmStages * kStageBytes; }
 
@@ -160,18 +159,20 @@ SPEC_DEV void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
 // A and D buffers i % 2.  Every wait is bounded in wall time (kWaitNs); a
 // thread that gives up sets SPEC_ST_DEVICE_WAIT and leaves its loop, and the
 // threads that depend on it give up in turn.
-//   producer (warp 8, lane 0): wait empty[s] (unit i-S combined) -> expect the
-//     unit's bytes on full[s] -> bulk-copy its 128 weight superblocks and its
-//     activation block into slot s.
-//   unpack warps 0..7, iteration i: wait full[s] -> unpack unit i into A[i%2]
-//     (free: the MMAs of unit i-2 were seen complete in iteration i-1) ->
-//     arrive a_full[i%2] -> wait mma_done of unit i-1 -> read its D, arrive
-//     d_free -> read its scales from its slot, arrive empty -> combine it.
-//   MMA warps 9, 10 (lane 0), unit i: wait full[s], a_full[i%2] and the
-//     d_free of unit i-2 -> issue the MMAs of sub-blocks 0-3 (warp 9) or 4-7
-//     plus the min term (warp 10) into D[i%2] -> commit to mma_done[i%2] (two
-//     arrivals per phase).
+//   producer (warp 12, lane 0): wait empty[s] (unit i-S combined) -> expect
+//     the unit's bytes on full[s] -> bulk-copy its 128 weight superblocks and
+//     its activation block into slot s.
+//   unpack warps 0..3, unit i: wait full[s] and d_free of unit i-2 (its D
+//     read out, hence its MMAs complete: A[i%2] and D[i%2] are free) ->
+//     unpack into A[i%2] -> arrive a_full[i%2].
+//   MMA warps 13..15 (lane 0), unit i: wait a_full[i%2] (which implies the
+//     two waits above) -> issue the MMAs of sub-blocks 3q .. 3q+2 (warp 13+q;
+//     the last one sub-blocks 6, 7 and the min term) into D[i%2] -> commit to
+//     mma_done[i%2] (three arrivals per phase).
+//   combine warps 4..11, unit i: wait mma_done[i%2] -> read D, arrive d_free
+//     -> read the unit's scales from its slot, arrive empty -> combine.
 constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr int kWarpProducer = 12, kWarpMma0 = 13;
 
 template <bool SUMS>
 __global__ void __launch_bounds__(kGemmThreads, 1)
@@ -182,9 +183,9 @@ gemm_q4k_kernel(const uint8_t* __restrict__ wt, const uint8_t* __restrict__ act,
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ uint32_t tmem_slot;
   __shared__ __align__(8) uint64_t full[kGemmStages], empty[kGemmStages];
-  __shared__ __align__(8) uint64_t a_full[2], mma_done[kDBufs], d_free[kDBufs];
+  __shared__ __align__(8) uint64_t a_full[2], mma_done[2], d_free[2];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int lg = warp & 3, hf = (warp >> 2) & 1;    // TMEM lane group; sub-block half / row half
+  const int lg = warp & 3;                          // TMEM lane group of this warp
   const int col_local = 32 * lg + lane;             // weight column inside the tile
   const int u0 = (int)((long long)blockIdx.x * U / G);
   const int u1 = (int)((long long)(blockIdx.x + 1) * U / G);
@@ -194,12 +195,12 @@ gemm_q4k_kernel(const uint8_t* __restrict__ wt, const uint8_t* __restrict__ act,
   if (tid == 0) {
     for (int b = 0; b < kGemmStages; ++b) {
       mbar_init(&full[b], 1);
-      mbar_init(&empty[b], kGemmUnpackThreads);
+      mbar_init(&empty[b], kGemmCombineThreads);
     }
-    for (int b = 0; b < 2; ++b) mbar_init(&a_full[b], kGemmUnpackThreads);
-    for (int b = 0; b < kDBufs; ++b) {
-      mbar_init(&mma_done[b], 2);
-      mbar_init(&d_free[b], kGemmUnpackThreads);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&a_full[b], kGemmUnpackThreads);
+      mbar_init(&mma_done[b], kGemmMmaWarps);
+      mbar_init(&d_free[b], kGemmCombineThreads);
     }
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::);
   }
@@ -208,7 +209,7 @@ gemm_q4k_kernel(const uint8_t* __restrict__ wt, const uint8_t* __restrict__ act,
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
 
-  if (warp == 8) {
+  if (warp == kWarpProducer) {
     // ------------------------------------------------------------- producer
     if (lane == 0) {
       const uint64_t pol_w = l2_policy_evict_first(), pol_a = l2_policy_evict_last();
@@ -256,62 +257,119 @@ gemm_q4k_kernel(const uint8_t* __restrict__ wt, const uint8_t* __restrict__ act,
       for (int u = max(0, issued - kGemmStages); u < issued; ++u)
         mbar_wait_ns(&full[u % kGemmStages], (u / kGemmStages) & 1, kWaitNs);
     }
-  } else if (warp >= 9) {
+  } else if (warp >= kWarpMma0) {
     // ------------------------------------------------------------------ MMA
     pdl_wait();
     pdl_trigger();
     if (lane == 0) {
-      const int hh = warp - 9;
+      const int q = warp - kWarpMma0;
       // D f32, A and B e4m3 (kind::f8f6f4) or f16 (kind::f16): both format codes 0
       constexpr uint32_t kIdesc = (1u << 4) | ((16u >> 3) << 17) | ((128u >> 4) << 24);
       bool ok = true;
       int last = -1;
       for (int i = 0; i < nunits; ++i) {
         const int s = i % kGemmStages;
-        ok = mbar_wait_ns(&full[s], (i / kGemmStages) & 1, kWaitNs) &&
-             mbar_wait_ns(&a_full[i & 1], (i >> 1) & 1, kWaitNs) &&
-             (i < kDBufs || mbar_wait_ns(&d_free[i % kDBufs], ((i - kDBufs) / kDBufs) & 1, kWaitNs));
+        ok = mbar_wait_ns(&a_full[i & 1], (i >> 1) & 1, kWaitNs);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t d = tmem + (uint32_t)(kTmemD0 + (i % kDBufs) * kTmemDStride);
+        const uint32_t d = tmem + (uint32_t)(kTmemD0 + (i & 1) * kTmemDStride);
         const uint32_t a = tmem + (uint32_t)(kTmemA + (i & 1) * kTmemAStride);
         // B blocks: hi of sub-block j at 1024*j, lo at +512 (descriptor units of 16 B)
         const uint64_t desc0 = smem_desc(smem_u32(smem + s * kStageBytes + kStageWeightBytes), 128, 256);
+        // warp 13+q: sub-blocks 3q .. min(3q+2, 7); the last warp also the min term
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          const int j = 4 * hh + jj;
-          mma_f8_ts(d + 16 * j, a + 8 * j, desc0 + 64ull * j, kIdesc, 0);
-          mma_f8_ts(d + 16 * j, a + 8 * j, desc0 + 64ull * j + 32, kIdesc, 1);
+        for (int jj = 0; jj < 3; ++jj) {
+          const int j = 3 * q + jj;
+          if (j < 8) {
+            mma_f8_ts(d + 16 * j, a + 8 * j, desc0 + 64ull * j, kIdesc, 0);
+            mma_f8_ts(d + 16 * j, a + 8 * j, desc0 + 64ull * j + 32, kIdesc, 1);
+          }
         }
-        if (hh == 1) mma_f16_ts(d + kTmemDm, a + kTmemAm, desc0 + 32ull * 16, kIdesc, 0);
-        mma_commit(&mma_done[i % kDBufs]);
+        if (q == kGemmMmaWarps - 1) mma_f16_ts(d + kTmemDm, a + kTmemAm, desc0 + 32ull * 16, kIdesc, 0);
+        mma_commit(&mma_done[i & 1]);
         last = i;
       }
       if (!ok) atomicOr(status, SPEC_ST_DEVICE_WAIT);
       // TMEM is released at the end: the MMAs of this thread must have finished
-      if (last >= 0) mbar_wait_ns(&mma_done[last % kDBufs], (last / kDBufs) & 1, kWaitNs);
+      if (last >= 0) mbar_wait_ns(&mma_done[last & 1], (last >> 1) & 1, kWaitNs);
     }
-  } else {
+  } else if (warp < 4) {
     // --------------------------------------------------------------- unpack
+    const uint32_t lane_base = (uint32_t)(32 * lg) << 16;
+    bool ok = true;
+    int cg = u0 / nb;
+    int cb = u0 - cg * nb;
+    for (int i = 0; i < nunits; ++i) {
+      const int s = i % kGemmStages;
+      // warp-uniform decisions: the TMEM stores below are warp-collective
+      ok = __all_sync(0xffffffffu, mbar_wait_ns(&full[s], (i / kGemmStages) & 1, kWaitNs) &&
+                                       (i < 2 || mbar_wait_ns(&d_free[i & 1], ((i - 2) >> 1) & 1, kWaitNs)));
+      if (!ok) break;
+      tc_fence_after();
+      const uint8_t* stg = smem + s * kStageBytes;
+      const int cols = min(kGemmCols, N - kGemmCols * cg);
+      const bool valid = col_local < cols;
+      const uint4* sbp = reinterpret_cast<const uint4*>(stg + col_local * kSB);
+      const uint32_t abase = tmem + lane_base + (uint32_t)(kTmemA + (i & 1) * kTmemAStride);
+#pragma unroll
+      for (int hv = 0; hv < 2; ++hv) {             // sub-blocks 4hv .. 4hv+3
+        uint32_t r[32];
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          uint4 c = make_uint4(0, 0, 0, 0);
+          if (valid) c = sbp[1 + 4 * hv + jj];
+          unpack_sub(c, r + 8 * jj);
+        }
+        tmem_st32(abase + (uint32_t)(32 * hv), r);
+      }
+      {
+        // min-term operand: k = j -> m_j, k = 8 + j -> m_j (f16 pairs)
+        uint4 hdr = make_uint4(0, 0, 0, 0);
+        if (valid) hdr = sbp[0];
+        const uint32_t f1 = hdr.z, f2 = hdr.w;
+        uint32_t mp[4];
+#pragma unroll
+        for (int qq = 0; qq < 4; ++qq) {
+          const int p0 = 48 + 12 * qq;             // bits of m_2qq, m_2qq+1
+          const uint32_t m12 = __funnelshift_r(p0 < 64 ? f1 : f2, p0 < 64 ? f2 : 0u, p0 & 31);
+          mp[qq] = hadd2_u32(((m12 & 63u) | (((m12 >> 6) & 63u) << 16)) + 0x64006400u, 0xE400E400u);
+        }
+        tmem_st4(abase + (uint32_t)kTmemAm, mp[0], mp[1], mp[2], mp[3]);
+        tmem_st4(abase + (uint32_t)(kTmemAm + 4), mp[0], mp[1], mp[2], mp[3]);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&a_full[i & 1]);
+      if (++cb == nb) {
+        cb = 0;
+        ++cg;
+      }
+    }
+    if (!ok && lane == 0) atomicOr(status, SPEC_ST_DEVICE_WAIT);
+  } else {
+    // -------------------------------------------------------------- combine
     pdl_wait();
     pdl_trigger();
+    const int hf = (warp - 4) >> 2;                 // rows 8hf .. 8hf+7
     const uint32_t lane_base = (uint32_t)(32 * lg) << 16;
     bool ok = true;
     float y[8];
 #pragma unroll
     for (int n = 0; n < 8; ++n) y[n] = 0.f;
-
-    // combine unit u = (group ug, superblock ub): rows 8hf .. 8hf+7 of this column
-    auto combine = [&](int u, int ug, int ub) {
-      const uint32_t dbase =
-          tmem + lane_base + (uint32_t)(kTmemD0 + (u % kDBufs) * kTmemDStride + 8 * hf);
+    int ug = u0 / nb;
+    int ub = u0 - ug * nb;
+    for (int u = 0; u < nunits; ++u) {
+      ok = __all_sync(0xffffffffu, mbar_wait_ns(&mma_done[u & 1], (u >> 1) & 1, kWaitNs));
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t dbase = tmem + lane_base + (uint32_t)(kTmemD0 + (u & 1) * kTmemDStride + 8 * hf);
       uint32_t dj[8][8], rm[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) tmem_ld8(dbase + 16 * j, dj[j]);
       tmem_ld8(dbase + kTmemDm, rm);
       tmem_wait_ld();
       tc_fence_before();
-      mbar_arrive(&d_free[u % kDBufs]);
+      mbar_arrive(&d_free[u & 1]);
       const int pslot = u % kGemmStages;
       const uint8_t* stg = smem + pslot * kStageBytes;
       const int cols = min(kGemmCols, N - kGemmCols * ug);
@@ -334,6 +392,7 @@ gemm_q4k_kernel(const uint8_t* __restrict__ wt, const uint8_t* __restrict__ act,
         sc2[j] = f2pack(f, f);
       }
       const unsigned long long D2 = f2pack(d, d), M2 = f2pack(dm, dm);
+      const int col = kGemmCols * ug + col_local;
 #pragma unroll
       for (int n = 0; n < 8; n += 2) {
         unsigned long long lo = f2mul(sc2[0], f2pack(__uint_as_float(dj[0][n]), __uint_as_float(dj[0][n + 1])));
@@ -353,7 +412,6 @@ gemm_q4k_kernel(const uint8_t* __restrict__ wt, const uint8_t* __restrict__ act,
           float l0, l1, h0, h1;
           f2unpack(lo, l0, l1);
           f2unpack(hi, h0, h1);
-          const int col = kGemmCols * ug + col_local;
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             const int row = 8 * hf + n + e;
@@ -369,7 +427,6 @@ gemm_q4k_kernel(const uint8_t* __restrict__ wt, const uint8_t* __restrict__ act,
       if (u0 + u + 1 == u1 || ub + 1 == nb) {
         const int slot_id = (int)blockIdx.x - cta_of_unit((long long)ug * nb, U, G);
         if (valid) {
-          const int col = kGemmCols * ug + col_local;
           float* base = pieces + (size_t)slot_id * 16 * N + (size_t)(8 * hf) * N + col;
 #pragma unroll
           for (int n = 0; n < 8; ++n) base[(size_t)n * N] = y[n];
@@ -377,73 +434,9 @@ gemm_q4k_kernel(const uint8_t* __restrict__ wt, const uint8_t* __restrict__ act,
 #pragma unroll
         for (int n = 0; n < 8; ++n) y[n] = 0.f;
       }
-    };
-
-    int pg = 0, pb = 0;                       // group / superblock of unit i-1
-    int cg = u0 / nb, cb = u0 - (u0 / nb) * nb;
-    int done_units = 0;
-    for (int i = 0; i < nunits; ++i) {
-      const int s = i % kGemmStages;
-      // warp-uniform decisions: the TMEM accesses below are warp-collective
-      ok = __all_sync(0xffffffffu, mbar_wait_ns(&full[s], (i / kGemmStages) & 1, kWaitNs));
-      if (!ok) break;
-      const uint8_t* stg = smem + s * kStageBytes;
-      // ---- unpack sub-blocks 4hf .. 4hf+3 of this thread's column into TMEM A[i&1]
-      {
-        const int cols = min(kGemmCols, N - kGemmCols * cg);
-        const bool valid = col_local < cols;
-        const uint4* sbp = reinterpret_cast<const uint4*>(stg + col_local * kSB);
-        const uint32_t abase = tmem + lane_base + (uint32_t)(kTmemA + (i & 1) * kTmemAStride);
-        uint32_t r[32];
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          uint4 c = make_uint4(0, 0, 0, 0);
-          if (valid) c = sbp[1 + 4 * hf + jj];
-          unpack_sub(c, r + 8 * jj);
-        }
-        tmem_st32(abase + (uint32_t)(32 * hf), r);      // sub-blocks 4hf .. 4hf+3
-        if (hf == 0) {
-          // min-term operand: k = j -> m_j, k = 8 + j -> m_j (f16 pairs)
-          uint4 hdr = make_uint4(0, 0, 0, 0);
-          if (valid) hdr = sbp[0];
-          const uint32_t f1 = hdr.z, f2 = hdr.w;
-          uint32_t mp[4];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int p0 = 48 + 12 * q;           // bits of m_2q, m_2q+1
-            const uint32_t m12 = __funnelshift_r(p0 < 64 ? f1 : f2, p0 < 64 ? f2 : 0u, p0 & 31);
-            mp[q] = hadd2_u32(((m12 & 63u) | (((m12 >> 6) & 63u) << 16)) + 0x64006400u, 0xE400E400u);
-          }
-          tmem_st4(abase + (uint32_t)kTmemAm, mp[0], mp[1], mp[2], mp[3]);
-          tmem_st4(abase + (uint32_t)(kTmemAm + 4), mp[0], mp[1], mp[2], mp[3]);
-        }
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(&a_full[i & 1]);
-
-      // ---- combine the previous superblock while this one runs
-      if (i >= 1) {
-        ok = __all_sync(0xffffffffu,
-                        mbar_wait_ns(&mma_done[(i - 1) % kDBufs], ((i - 1) / kDBufs) & 1, kWaitNs));
-        if (!ok) break;
-        tc_fence_after();
-        combine(i - 1, pg, pb);
-      }
-      done_units = i + 1;
-      pg = cg;
-      pb = cb;
-      if (++cb == nb) {
-        cb = 0;
-        ++cg;
-      }
-    }
-    if (ok && done_units > 0) {
-      const int l = done_units - 1;
-      ok = __all_sync(0xffffffffu, mbar_wait_ns(&mma_done[l % kDBufs], (l / kDBufs) & 1, kWaitNs));
-      if (ok) {
-        tc_fence_after();
-        combine(l, pg, pb);
+      if (++ub == nb) {
+        ub = 0;
+        ++ug;
       }
     }
     if (!ok && lane == 0) atomicOr(status, SPEC_ST_DEVICE_WAIT);

@@ -18,11 +18,15 @@ struct GemmPlan {
   long long U = 0;
 };
 
-// tcgen05 GEMM: one CTA per SM owns 128 weight columns (one per TMEM lane);
-// 8 warps unpack and combine (two threads per column: sub-blocks 0-3 and
-// 4-7), one warp issues the bulk copies, 2 warps issue the tensor-core MMAs.
-constexpr int kGemmUnpackThreads = 256;
-constexpr int kGemmThreads = kGemmUnpackThreads + 96;
+// tcgen05 GEMM: one CTA per SM owns 128 weight columns (one per TMEM lane):
+// 4 warps unpack the weight codes (one thread per column), 8 warps combine the
+// MMA results (two threads per column, 8 rows each), one warp issues the bulk
+// copies and 3 warps issue the tensor-core MMAs (16 warps: each of the 4
+// schedulers holds 4 warps' registers).
+constexpr int kGemmUnpackThreads = 128;
+constexpr int kGemmCombineThreads = 256;
+constexpr int kGemmMmaWarps = 3;
+constexpr int kGemmThreads = kGemmUnpackThreads + kGemmCombineThreads + 32 + 32 * kGemmMmaWarps;
 constexpr int kTilesPerGroup = 8;          // 16-column tiles per group = 128 columns
 constexpr int kGemmCols = 16 * kTilesPerGroup;
 constexpr int kGemmStages = 6;

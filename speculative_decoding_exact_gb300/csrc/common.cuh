@@ -246,6 +246,13 @@ SPEC_DEV uint64_t l2_policy_evict_last() {
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;\n" : "=l"(p));
   return p;
 }
+// true in exactly one lane of the converged warp (tcgen05 issue from a
+// converged warp keeps the operands in uniform registers)
+SPEC_DEV bool elect_one() {
+  uint32_t p;
+  asm volatile("{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n selp.u32 %0, 1, 0, e;\n}\n" : "=r"(p));
+  return p != 0;
+}
 SPEC_DEV void mbar_arrive(uint64_t* mbar) {
   asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(mbar)) : "memory");
 }

@@ -29,12 +29,14 @@
 // unpack warps (one thread per column) turn a column's 144-byte superblock
 // into e4m3 code bytes and store them into TMEM lane c (the MMA's A operand,
 // M = 128 rows = columns of W); the 16 activation rows are the MMA's N = 16
-// columns, read from shared memory (B operand).  Three warps issue the 17 MMAs
-// of a superblock (one thread issuing all of them serialises on the issue
-// latency), eight warps read the results back and combine them (two threads
-// per column, 8 rows each), and one warp issues the bulk copies that stage
-// weights and activations.  A and D are double-buffered in TMEM: unpacking,
-// MMAs and combining of consecutive superblocks overlap.
+// columns, read from shared memory (B operand).  Three warps share the 17
+// MMAs of a superblock; each runs converged and lets one elected lane issue,
+// which keeps the MMA operands in uniform registers (a lone lane issuing
+// MMAs manages about one per 100 cycles, a converged warp about one per 35).
+// Eight warps read the results back and combine them (two threads per
+// column, 8 rows each), and one warp issues the bulk copies that stage
+// weights and activations.  A is triple-buffered and D double-buffered in
+// TMEM, so unpacking, MMAs and combining of consecutive superblocks overlap.
 //
 // Row i's result depends only on row i's codes and on the fixed (K, N)
 // work plan, so it is identical for every M (batch-height invariance, "The
@@ -120,13 +122,15 @@ GemmPlan make_gemm_plan(int N, int K, int num_sms) {
 constexpr int kStageWeightBytes = kGemmCols * kSB;            // 18432
 constexpr int kStageBytes = kStageWeightBytes + kActSBBytes;   // 27200
 constexpr int kTmemCols = 512;
-// TMEM columns: A buffer b = 0, 1 at 72*b: sub-block j's 32 code bytes in
+// TMEM columns: A buffer b = 0, 1, 2 at 72*b: sub-block j's 32 code bytes in
 // columns 8j .. 8j+7 (four codes per column, lowest k in the low byte), the
 // min-term A' (f16, K = 16) in columns 64 .. 71.  D buffer b = 0, 1 at
-// 144 + 144*b: sub-block j's 16 rows in columns 16j .. 16j+15, the min term in
-// 128 .. 143.
-constexpr int kTmemA = 0, kTmemAStride = 72, kTmemAm = 64, kTmemD0 = 144, kTmemDStride = 144,
+// 224 + 144*b: sub-block j's 16 rows in columns 16j .. 16j+15, the min term
+// in 128 .. 143.
+constexpr int kABufs = 3;
+constexpr int kTmemA = 0, kTmemAStride = 72, kTmemAm = 64, kTmemD0 = 224, kTmemDStride = 144,
               kTmemDm = 128;
+static_assert(kTmemD0 >= kABufs * kTmemAStride && kTmemD0 + 2 * kTmemDStride <= kTmemCols, "TMEM layout");
 
 size_t gemm_smem_bytes() { return (size_t)kGemmStages * kStageBytes; }
 
@@ -155,27 +159,37 @@ SPEC_DEV void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
 }
 
 // Roles and hand-offs of one CTA.  Unit i = (group, superblock) number i of
-// this CTA's range; it lives in stage slot s = i % kGemmStages and in TMEM
-// A and D buffers i % 2.  Every wait is bounded in wall time (kWaitNs); a
+// this CTA's range; it lives in stage slot s = i % kGemmStages, TMEM A buffer
+// i % 3 and D buffer i % 2.  Every wait is bounded in wall time (kWaitNs); a
 // thread that gives up sets SPEC_ST_DEVICE_WAIT and leaves its loop, and the
 // threads that depend on it give up in turn.
-//   producer (warp 12, lane 0): wait empty[s] (unit i-S combined) -> expect
-//     the unit's bytes on full[s] -> bulk-copy its 128 weight superblocks and
-//     its activation block into slot s.
-//   unpack warps 0..3, unit i: wait full[s] and d_free of unit i-2 (its D
-//     read out, hence its MMAs complete: A[i%2] and D[i%2] are free) ->
-//     unpack into A[i%2] -> arrive a_full[i%2].
-//   MMA warps 13..15 (lane 0), unit i: wait a_full[i%2] (which implies the
-//     two waits above) -> issue the MMAs of sub-blocks 3q .. 3q+2 (warp 13+q;
-//     the last one sub-blocks 6, 7 and the min term) into D[i%2] -> commit to
-//     mma_done[i%2] (three arrivals per phase).
-//   combine warps 4..11, unit i: wait mma_done[i%2] -> read D, arrive d_free
-//     -> read the unit's scales from its slot, arrive empty -> combine.
+//   producer warp, lane 0: wait empty[s] (unit i-S combined) -> expect the
+//     unit's bytes on full[s] -> bulk-copy its 128 weight superblocks and its
+//     activation block into slot s.
+//   unpack warps, unit i: wait full[s] and a_free[i%3] (the MMAs of unit i-3
+//     are complete) -> unpack into A[i%3] -> arrive a_full[i%3].
+//   MMA warps, unit i: wait a_full[i%3] and d_free[i%2] (unit i-2 read out)
+//     -> the elected lane issues the warp's share of the MMAs into D[i%2] and
+//     commits to mma_done[i%2] and a_free[i%3] (one arrival per MMA warp).
+//   combine warps, unit i: wait mma_done[i%2] -> read D in two halves, arrive
+//     d_free[i%2] -> read the unit's activation scales, arrive empty[s] ->
+//     combine.
 constexpr uint64_t kWaitNs = 2000000000ull;
-constexpr int kWarpProducer = 12, kWarpMma0 = 13;
+constexpr int kWarpCombine0 = kGemmUnpackWarps;            // 8 combine warps
+constexpr int kWarpProducer = kWarpCombine0 + 8;
+constexpr int kWarpMma0 = kWarpProducer + 1;
+constexpr int kGemmWarps = kWarpMma0 + kGemmMmaWarps;
+static_assert(kGemmWarps * 32 == kGemmThreads, "warp roles");
+// registers: each of the 4 schedulers holds the registers of its warps (16K)
+constexpr int kGemmMaxRegs = kGemmWarps <= 16 ? 128 : 96;
+static_assert(((kGemmWarps + 3) / 4) * 32 * kGemmMaxRegs <= 16384, "register budget");
+
+// MMA share of warp q: sub-blocks mma_j0(q) .. mma_j0(q+1)-1 (two MMAs each);
+// the last warp also issues the min term
+__host__ __device__ constexpr int mma_j0(int q) { return (8 * q + kGemmMmaWarps - 1) / kGemmMmaWarps; }
 
 template <bool SUMS>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+__global__ void __maxnreg__(kGemmMaxRegs)
 gemm_q4k_kernel(const uint8_t* __restrict__ wt, const uint8_t* __restrict__ act,
                 float* __restrict__ pieces, int N, int nb, int U, int G,
                 int32_t* __restrict__ isc_out, int32_t* __restrict__ imn_out, int m_sums,
@@ -183,7 +197,7 @@ gemm_q4k_kernel(const uint8_t* __restrict__ wt, const uint8_t* __restrict__ act,
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ uint32_t tmem_slot;
   __shared__ __align__(8) uint64_t full[kGemmStages], empty[kGemmStages];
-  __shared__ __align__(8) uint64_t a_full[2], mma_done[2], d_free[2];
+  __shared__ __align__(8) uint64_t a_full[kABufs], a_free[kABufs], mma_done[2], d_free[2];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int lg = warp & 3;                          // TMEM lane group of this warp
   const int col_local = 32 * lg + lane;             // weight column inside the tile
@@ -197,8 +211,11 @@ gemm_q4k_kernel(const uint8_t* __restrict__ wt, const uint8_t* __restrict__ act,
       mbar_init(&full[b], 1);
       mbar_init(&empty[b], kGemmCombineThreads);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < kABufs; ++b) {
       mbar_init(&a_full[b], kGemmUnpackThreads);
+      mbar_init(&a_free[b], kGemmMmaWarps);
+    }
+    for (int b = 0; b < 2; ++b) {
       mbar_init(&mma_done[b], kGemmMmaWarps);
       mbar_init(&d_free[b], kGemmCombineThreads);
     }
@@ -261,66 +278,74 @@ gemm_q4k_kernel(const uint8_t* __restrict__ wt, const uint8_t* __restrict__ act,
     // ------------------------------------------------------------------ MMA
     pdl_wait();
     pdl_trigger();
-    if (lane == 0) {
-      const int q = warp - kWarpMma0;
-      // D f32, A and B e4m3 (kind::f8f6f4) or f16 (kind::f16): both format codes 0
-      constexpr uint32_t kIdesc = (1u << 4) | ((16u >> 3) << 17) | ((128u >> 4) << 24);
-      bool ok = true;
-      int last = -1;
-      for (int i = 0; i < nunits; ++i) {
-        const int s = i % kGemmStages;
-        ok = mbar_wait_ns(&a_full[i & 1], (i >> 1) & 1, kWaitNs);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t d = tmem + (uint32_t)(kTmemD0 + (i & 1) * kTmemDStride);
-        const uint32_t a = tmem + (uint32_t)(kTmemA + (i & 1) * kTmemAStride);
-        // B blocks: hi of sub-block j at 1024*j, lo at +512 (descriptor units of 16 B)
-        const uint64_t desc0 = smem_desc(smem_u32(smem + s * kStageBytes + kStageWeightBytes), 128, 256);
-        // warp 13+q: sub-blocks 3q .. min(3q+2, 7); the last warp also the min term
+    // warp-uniform values (the whole warp runs this loop; one lane issues)
+    const int q = __shfl_sync(0xffffffffu, warp - kWarpMma0, 0);
+    const uint32_t tm = __shfl_sync(0xffffffffu, tmem, 0);
+    const uint32_t sbase = __shfl_sync(0xffffffffu, smem_u32(smem), 0);
+    const int j0 = mma_j0(q), j1 = mma_j0(q + 1);
+    // D f32, A and B e4m3 (kind::f8f6f4) or f16 (kind::f16): both format codes 0
+    constexpr uint32_t kIdesc = (1u << 4) | ((16u >> 3) << 17) | ((128u >> 4) << 24);
+    bool ok = true;
+    int last = -1;
+    for (int i = 0; i < nunits; ++i) {
+      const int s = i % kGemmStages, ab = i % kABufs;
+      ok = __all_sync(0xffffffffu,
+                      mbar_wait_ns(&a_full[ab], (i / kABufs) & 1, kWaitNs) &&
+                          (i < 2 || mbar_wait_ns(&d_free[i & 1], ((i - 2) >> 1) & 1, kWaitNs)));
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t d = tm + (uint32_t)(kTmemD0 + (i & 1) * kTmemDStride);
+      const uint32_t a = tm + (uint32_t)(kTmemA + ab * kTmemAStride);
+      // B blocks: hi of sub-block j at 1024*j, lo at +512 (descriptor units of 16 B)
+      const uint64_t desc0 = smem_desc(sbase + (uint32_t)(s * kStageBytes + kStageWeightBytes), 128, 256);
+      if (elect_one()) {
 #pragma unroll
-        for (int jj = 0; jj < 3; ++jj) {
-          const int j = 3 * q + jj;
-          if (j < 8) {
+        for (int jj = 0; jj < (8 + kGemmMmaWarps - 1) / kGemmMmaWarps; ++jj) {
+          const int j = j0 + jj;
+          if (j < j1) {
             mma_f8_ts(d + 16 * j, a + 8 * j, desc0 + 64ull * j, kIdesc, 0);
             mma_f8_ts(d + 16 * j, a + 8 * j, desc0 + 64ull * j + 32, kIdesc, 1);
           }
         }
         if (q == kGemmMmaWarps - 1) mma_f16_ts(d + kTmemDm, a + kTmemAm, desc0 + 32ull * 16, kIdesc, 0);
         mma_commit(&mma_done[i & 1]);
-        last = i;
+        mma_commit(&a_free[ab]);
       }
-      if (!ok) atomicOr(status, SPEC_ST_DEVICE_WAIT);
-      // TMEM is released at the end: the MMAs of this thread must have finished
-      if (last >= 0) mbar_wait_ns(&mma_done[last & 1], (last >> 1) & 1, kWaitNs);
+      __syncwarp();
+      last = i;
     }
-  } else if (warp < 4) {
+    if (!ok && lane == 0) atomicOr(status, SPEC_ST_DEVICE_WAIT);
+    // TMEM is released at the end: the MMAs of this warp must have finished
+    if (last >= 0) mbar_wait_ns(&a_free[last % kABufs], (last / kABufs) & 1, kWaitNs);
+  } else if (warp < kWarpCombine0) {
     // --------------------------------------------------------------- unpack
     const uint32_t lane_base = (uint32_t)(32 * lg) << 16;
     bool ok = true;
     int cg = u0 / nb;
     int cb = u0 - cg * nb;
     for (int i = 0; i < nunits; ++i) {
-      const int s = i % kGemmStages;
+      const int s = i % kGemmStages, ab = i % kABufs;
       // warp-uniform decisions: the TMEM stores below are warp-collective
-      ok = __all_sync(0xffffffffu, mbar_wait_ns(&full[s], (i / kGemmStages) & 1, kWaitNs) &&
-                                       (i < 2 || mbar_wait_ns(&d_free[i & 1], ((i - 2) >> 1) & 1, kWaitNs)));
+      ok = __all_sync(0xffffffffu,
+                      mbar_wait_ns(&full[s], (i / kGemmStages) & 1, kWaitNs) &&
+                          (i < kABufs || mbar_wait_ns(&a_free[ab], ((i - kABufs) / kABufs) & 1, kWaitNs)));
       if (!ok) break;
       tc_fence_after();
       const uint8_t* stg = smem + s * kStageBytes;
       const int cols = min(kGemmCols, N - kGemmCols * cg);
       const bool valid = col_local < cols;
       const uint4* sbp = reinterpret_cast<const uint4*>(stg + col_local * kSB);
-      const uint32_t abase = tmem + lane_base + (uint32_t)(kTmemA + (i & 1) * kTmemAStride);
+      const uint32_t abase = tmem + lane_base + (uint32_t)(kTmemA + ab * kTmemAStride);
 #pragma unroll
-      for (int hv = 0; hv < 2; ++hv) {             // sub-blocks 4hv .. 4hv+3
+      for (int hq = 0; hq < 2; ++hq) {             // sub-blocks 4hq .. 4hq+3 per TMEM store
         uint32_t r[32];
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
           uint4 c = make_uint4(0, 0, 0, 0);
-          if (valid) c = sbp[1 + 4 * hv + jj];
+          if (valid) c = sbp[1 + 4 * hq + jj];
           unpack_sub(c, r + 8 * jj);
         }
-        tmem_st32(abase + (uint32_t)(32 * hv), r);
+        tmem_st32(abase + (uint32_t)(32 * hq), r);
       }
       {
         // min-term operand: k = j -> m_j, k = 8 + j -> m_j (f16 pairs)
@@ -339,7 +364,7 @@ gemm_q4k_kernel(const uint8_t* __restrict__ wt, const uint8_t* __restrict__ act,
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&a_full[i & 1]);
+      mbar_arrive(&a_full[ab]);
       if (++cb == nb) {
         cb = 0;
         ++cg;
@@ -350,7 +375,7 @@ gemm_q4k_kernel(const uint8_t* __restrict__ wt, const uint8_t* __restrict__ act,
     // -------------------------------------------------------------- combine
     pdl_wait();
     pdl_trigger();
-    const int hf = (warp - 4) >> 2;                 // rows 8hf .. 8hf+7
+    const int hf = (warp - kWarpCombine0) >> 2;     // rows 8hf .. 8hf+7
     const uint32_t lane_base = (uint32_t)(32 * lg) << 16;
     bool ok = true;
     float y[8];
@@ -359,23 +384,47 @@ gemm_q4k_kernel(const uint8_t* __restrict__ wt, const uint8_t* __restrict__ act,
     int ug = u0 / nb;
     int ub = u0 - ug * nb;
     for (int u = 0; u < nunits; ++u) {
+      // warp-uniform decision: the TMEM loads below are warp-collective
       ok = __all_sync(0xffffffffu, mbar_wait_ns(&mma_done[u & 1], (u >> 1) & 1, kWaitNs));
       if (!ok) break;
       tc_fence_after();
-      const uint32_t dbase = tmem + lane_base + (uint32_t)(kTmemD0 + (u & 1) * kTmemDStride + 8 * hf);
-      uint32_t dj[8][8], rm[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) tmem_ld8(dbase + 16 * j, dj[j]);
-      tmem_ld8(dbase + kTmemDm, rm);
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(&d_free[u & 1]);
       const int pslot = u % kGemmStages;
       const uint8_t* stg = smem + pslot * kStageBytes;
       const int cols = min(kGemmCols, N - kGemmCols * ug);
       const bool valid = col_local < cols;
+      const int col = kGemmCols * ug + col_local;
+      const uint32_t dbase = tmem + lane_base + (uint32_t)(kTmemD0 + (u & 1) * kTmemDStride + 8 * hf);
+      // the stage was filled before the MMAs of this unit were issued
       uint4 hdr = make_uint4(0, 0, 0, 0);
       if (valid) hdr = *reinterpret_cast<const uint4*>(stg + col_local * kSB);
+      unsigned long long acc[2][4];               // [half][row pair]: sum_j sc_j S_j * 2^-9
+      uint32_t rm[8];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t dj[4][8];
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) tmem_ld8(dbase + 16 * (4 * h + jj), dj[jj]);
+        if (h == 1) {
+          tmem_ld8(dbase + kTmemDm, rm);
+          tmem_wait_ld();
+          tc_fence_before();
+          mbar_arrive(&d_free[u & 1]);
+        } else {
+          tmem_wait_ld();
+        }
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          // 6-bit scale as an exact float: 2^23 + sc with the 2^23 subtracted
+          const float f =
+              __uint_as_float(0x4B000000u | sub_scale(hdr.y, hdr.z, hdr.w, 4 * h + jj)) - 8388608.f;
+          const unsigned long long sc2 = f2pack(f, f);
+#pragma unroll
+          for (int n = 0; n < 8; n += 2) {
+            const unsigned long long sj = f2pack(__uint_as_float(dj[jj][n]), __uint_as_float(dj[jj][n + 1]));
+            acc[h][n >> 1] = jj == 0 ? f2mul(sc2, sj) : f2fma(sc2, sj, acc[h][n >> 1]);
+          }
+        }
+      }
       const float4* dap =
           reinterpret_cast<const float4*>(stg + kStageWeightBytes + kActSlots * 512 + 32 * hf);
       const float4 da0 = dap[0], da1 = dap[1];
@@ -384,25 +433,10 @@ gemm_q4k_kernel(const uint8_t* __restrict__ wt, const uint8_t* __restrict__ act,
       // d * 2^9 (exact): the D values are 2^-9 * integer sums
       const float d = __half2float(__ushort_as_half((unsigned short)(hdr.x & 0xffff))) * 512.f;
       const float dm = __half2float(__ushort_as_half((unsigned short)(hdr.x >> 16)));
-      unsigned long long sc2[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        // 6-bit scale as an exact float: 2^23 + sc with the 2^23 subtracted
-        const float f = __uint_as_float(0x4B000000u | sub_scale(hdr.y, hdr.z, hdr.w, j)) - 8388608.f;
-        sc2[j] = f2pack(f, f);
-      }
       const unsigned long long D2 = f2pack(d, d), M2 = f2pack(dm, dm);
-      const int col = kGemmCols * ug + col_local;
 #pragma unroll
       for (int n = 0; n < 8; n += 2) {
-        unsigned long long lo = f2mul(sc2[0], f2pack(__uint_as_float(dj[0][n]), __uint_as_float(dj[0][n + 1])));
-        unsigned long long hi = f2mul(sc2[4], f2pack(__uint_as_float(dj[4][n]), __uint_as_float(dj[4][n + 1])));
-#pragma unroll
-        for (int j = 1; j < 4; ++j) {
-          lo = f2fma(sc2[j], f2pack(__uint_as_float(dj[j][n]), __uint_as_float(dj[j][n + 1])), lo);
-          hi = f2fma(sc2[4 + j], f2pack(__uint_as_float(dj[4 + j][n]), __uint_as_float(dj[4 + j][n + 1])), hi);
-        }
-        const unsigned long long isc = f2add(lo, hi);
+        const unsigned long long isc = f2add(acc[0][n >> 1], acc[1][n >> 1]);
         const unsigned long long imn = f2pack(__uint_as_float(rm[n]), __uint_as_float(rm[n + 1]));
         const unsigned long long v =
             f2mul(f2pack(da[n], da[n + 1]), f2sub(f2mul(D2, isc), f2mul(M2, imn)));
@@ -410,8 +444,8 @@ gemm_q4k_kernel(const uint8_t* __restrict__ wt, const uint8_t* __restrict__ act,
         f2unpack(yy, y[n], y[n + 1]);
         if (SUMS) {
           float l0, l1, h0, h1;
-          f2unpack(lo, l0, l1);
-          f2unpack(hi, h0, h1);
+          f2unpack(acc[0][n >> 1], l0, l1);
+          f2unpack(acc[1][n >> 1], h0, h1);
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             const int row = 8 * hf + n + e;

@@ -18,12 +18,12 @@ struct GemmPlan {
   long long U = 0;
 };
 
-// tcgen05 GEMM: one CTA per SM owns 128 weight columns (one per TMEM lane):
-// 4 warps unpack the weight codes (one thread per column), 8 warps combine the
-// MMA results (two threads per column, 8 rows each), one warp issues the bulk
-// copies and 3 warps issue the tensor-core MMAs (16 warps: each of the 4
-// schedulers holds 4 warps' registers).
-constexpr int kGemmUnpackThreads = 128;
+// tcgen05 GEMM: one CTA per SM owns 128 weight columns (one per TMEM lane).
+// Warp roles: 4 unpack warps (one thread per column), 8 combine warps (two
+// threads per column, 8 rows each), one warp that issues the bulk copies, and
+// kGemmMmaWarps warps that share the 17 MMAs of a superblock.
+constexpr int kGemmUnpackWarps = 4;
+constexpr int kGemmUnpackThreads = 32 * kGemmUnpackWarps;
 constexpr int kGemmCombineThreads = 256;
 constexpr int kGemmMmaWarps = 3;
 constexpr int kGemmThreads = kGemmUnpackThreads + kGemmCombineThreads + 32 + 32 * kGemmMmaWarps;

@@ -404,13 +404,56 @@ def profile_gemms(ctx, abi, torch, stream, ws, ks, hidden, draft, res, steps):
     return tot / steps, n
 
 
+def run_gemm_shape(args):
+    """Time one Q4_K GEMM shape (16 rows, synthetic weights) through
+    spec_gemm_q4k; a small device footprint, used as the ncu capture target."""
+    import torch
+
+    from speculative_decoding_exact_gb300 import abi, runtime, synth
+    from speculative_decoding_exact_gb300 import build as b
+
+    b.build()
+    N, K = (int(v) for v in args.gemm_shape.lower().split("x"))
+    ctx = runtime.Context(runtime.ModelConfig(**synth.FULL), max_ctx=2112)
+    W = runtime.upload_tiled(ctx, synth.q4k_matrix(N, K, 7, N + K), N, K)
+    x = torch.from_numpy(synth.normal((16, K), 7, 16)).cuda()
+    y = torch.zeros((16, N), dtype=torch.float32, device="cuda")
+
+    def call():
+        abi.check("spec_gemm_q4k", abi.spec_gemm_q4k(ctx.h, W.data_ptr(), N, K, x.data_ptr(), 16,
+                                                     y.data_ptr()))
+
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        call()
+    e1.record()
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1000.0 / args.steps
+    wbytes = N * (K // 256) * 144
+    print(json.dumps({"metric": "q4k gemm weight GB/s (16 rows, quantise + GEMM + piece sum)",
+                      "value": wbytes / us / 1e3, "unit": "GB/s", "us_per_call": us,
+                      "shape": {"N": N, "K": K, "rows": 16}, "weight_bytes": wbytes,
+                      "l2": "weights resident from the previous call when smaller than L2"}))
+    ctx.close()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--gemm-shape", default=None,
+                    help="NxK: time one Q4_K GEMM shape instead of the verify step")
     args = ap.parse_args()
+    if args.gemm_shape:
+        run_gemm_shape(args)
+        return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if world > 1:

@@ -74,8 +74,8 @@ constexpr int kWarpsPerCta = (kMaxGroup + kHeadSplit - 1) / kHeadSplit;
 size_t qfrag_bytes(int nq) { return (size_t)nq * 8 * 2 * 32 * 16; }
 
 __global__ void q_to_frag_kernel(const float* __restrict__ q, int M, int nq, uint8_t* qfrag) {
-  pdl_wait();
   pdl_trigger();
+  pdl_wait();
   const int row = blockIdx.y;
   const int col = blockIdx.x * blockDim.x + threadIdx.x;
   if (col >= nq * 128) return;
@@ -101,8 +101,8 @@ attn_partial_kernel(const uint4* __restrict__ qf, int M, int nq, int nkv, KvView
   __shared__ __align__(128) __nv_bfloat16 Ks[kChunk * kRowPad];
   __shared__ __align__(128) __nv_bfloat16 Vs[kChunk * kRowPad];
 
-  pdl_wait();
   pdl_trigger();
+  pdl_wait();
   const int chunk = blockIdx.x, kvh = blockIdx.y;
   const int group = nq / nkv;
   const int per = (group + kHeadSplit - 1) / kHeadSplit;
@@ -250,8 +250,8 @@ attn_partial_kernel(const uint4* __restrict__ qf, int M, int nq, int nkv, KvView
 __global__ void __launch_bounds__(256)
 attn_merge_kernel(const float* __restrict__ part, int M, int nq, int max_chunks,
                   const int32_t* seq_len, float* __restrict__ out, uint8_t* act, int32_t* status) {
-  pdl_wait();
   pdl_trigger();
+  pdl_wait();
   extern __shared__ float msh[];          // [2][max_chunks] weights, then [2] L
   __shared__ float vals[256];
   __shared__ float hmax[2];

@@ -250,8 +250,8 @@ gemm_q4k_kernel(const uint8_t* __restrict__ wt, const uint8_t* __restrict__ act,
           if (++bb == nb) { bb = 0; ++gg; }
         }
       }
-      pdl_wait();
       pdl_trigger();
+      pdl_wait();
       for (int i = 0; i < nunits; ++i) {
         const int s = i % kGemmStages;
         if (i >= kGemmStages) {
@@ -276,8 +276,8 @@ gemm_q4k_kernel(const uint8_t* __restrict__ wt, const uint8_t* __restrict__ act,
     }
   } else if (warp >= kWarpMma0) {
     // ------------------------------------------------------------------ MMA
-    pdl_wait();
     pdl_trigger();
+    pdl_wait();
     // warp-uniform values (the whole warp runs this loop; one lane issues)
     const int q = __shfl_sync(0xffffffffu, warp - kWarpMma0, 0);
     const uint32_t tm = __shfl_sync(0xffffffffu, tmem, 0);
@@ -373,8 +373,8 @@ gemm_q4k_kernel(const uint8_t* __restrict__ wt, const uint8_t* __restrict__ act,
     if (!ok && lane == 0) atomicOr(status, SPEC_ST_DEVICE_WAIT);
   } else {
     // -------------------------------------------------------------- combine
-    pdl_wait();
     pdl_trigger();
+    pdl_wait();
     const int hf = (warp - kWarpCombine0) >> 2;     // rows 8hf .. 8hf+7
     const uint32_t lane_base = (uint32_t)(32 * lg) << 16;
     bool ok = true;
@@ -523,8 +523,8 @@ cudaError_t launch_gemm(const GemmPlan& p, const void* w_tiled, const uint8_t* a
 // y[m][n] = sum over the group's slots, in slot order
 __global__ void sum_pieces_kernel(const float* __restrict__ pieces, float* __restrict__ y, int N,
                                   int M, int nb, long long U, int G) {
-  pdl_wait();
   pdl_trigger();
+  pdl_wait();
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= (long long)M * N) return;
   const int m = (int)(i / N), n = (int)(i % N);

@@ -20,16 +20,19 @@ namespace cg = cooperative_groups;
 
 namespace spec {
 
-__host__ __device__ __forceinline__ int cta_of_unit2(long long x, long long U, int G) {
-  return (int)(((x + 1) * (long long)G - 1) / U);
+// number of pieces (CTA slots) of the group holding column col.  The GEMM
+// plan splits U units over G CTAs in contiguous ranges: unit x belongs to CTA
+// ((x+1)*G - 1)/U.  U*G stays far below 2^31 for every shape here (the LM
+// head has U = 1024*26, G <= 152), so 32-bit arithmetic is exact.
+__device__ __forceinline__ int piece_slots(int nb, int U, int G, int col) {
+  const int gr = (col >> 4) / kTilesPerGroup;
+  const int x0 = gr * nb, x1 = x0 + nb - 1;
+  return ((x1 + 1) * G - 1) / U - ((x0 + 1) * G - 1) / U + 1;
 }
 
-// sum of the GEMM pieces of output (row, col), slots in order
-__device__ __forceinline__ float piece_sum(const float* __restrict__ pieces, int N, int nb,
-                                           long long U, int G, int row, int col) {
-  const int gr = (col >> 4) / kTilesPerGroup;
-  const int c0 = cta_of_unit2((long long)gr * nb, U, G);
-  const int ns = cta_of_unit2((long long)gr * nb + nb - 1, U, G) - c0 + 1;
+// sum of the ns pieces of output (row, col), slots in order
+__device__ __forceinline__ float piece_sum(const float* __restrict__ pieces, int N, int ns, int row,
+                                           int col) {
   // independent loads of at most kMaxSlots slots, added in slot order
   float v[kMaxSlots];
 #pragma unroll
@@ -39,6 +42,24 @@ __device__ __forceinline__ float piece_sum(const float* __restrict__ pieces, int
   for (int k = 1; k < kMaxSlots; ++k)
     if (k < ns) s += v[k];
   return s;
+}
+
+// the same for 8 consecutive columns col0 .. col0+7 (col0 % 8 == 0, N % 8 == 0:
+// one group, 32-byte aligned rows), each summed in slot order
+__device__ __forceinline__ void piece_sum8(const float* __restrict__ pieces, int N, int ns, int row,
+                                           int col0, float (&out)[8]) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) out[i] = 0.f;
+#pragma unroll
+  for (int k = 0; k < kMaxSlots; ++k) {
+    if (k < ns) {
+      const float4* p = reinterpret_cast<const float4*>(pieces + ((size_t)k * 16 + row) * N + col0);
+      const float4 a = p[0], b = p[1];
+      const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) out[i] = k == 0 ? v[i] : out[i] + v[i];
+    }
+  }
 }
 
 template <class T>
@@ -52,8 +73,8 @@ __device__ __forceinline__ void load8(const T* p, float (&v)[8]) {
 // ---- plain quantisation of x[M][K]: grid (ceil(nb/8), 16), 8 warps, warp = block
 __global__ void quantize_kernel(const float* __restrict__ x, int M, int K, uint8_t* act,
                                 int8_t* q_dbg, float* da_dbg, int32_t* A_dbg, int32_t* status) {
-  pdl_wait();
   pdl_trigger();
+  pdl_wait();
   const int nb = K / 256;
   const int b = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int row = blockIdx.y;
@@ -115,8 +136,8 @@ resid_norm_quant_kernel(const float* __restrict__ pieces, int pN, int pnb, long 
                         const float* x_in, float* x_out,
                         const float* __restrict__ gamma, float eps, int M, int H, uint8_t* act,
                         float* __restrict__ xnorm_out, int32_t* status) {
-  pdl_wait();
   pdl_trigger();
+  pdl_wait();
   cg::cluster_group cluster = cg::this_cluster();
   __shared__ float warp_ss[8];
   __shared__ float cta_ss;
@@ -132,8 +153,10 @@ resid_norm_quant_kernel(const float* __restrict__ pieces, int pN, int pnb, long 
     const int col0 = 256 * b + 8 * lane;
     load8(x_in + (size_t)row * H + col0, v);
     if (pieces) {
+      float ps[8];
+      piece_sum8(pieces, pN, piece_slots(pnb, (int)pU, pG, col0), row, col0, ps);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) v[i] = v[i] + piece_sum(pieces, pN, pnb, pU, pG, row, col0 + i);
+      for (int i = 0; i < 8; ++i) v[i] = v[i] + ps[i];
       float4* o = reinterpret_cast<float4*>(x_out + (size_t)row * H + col0);
       o[0] = make_float4(v[0], v[1], v[2], v[3]);
       o[1] = make_float4(v[4], v[5], v[6], v[7]);
@@ -200,8 +223,8 @@ cudaError_t launch_resid_norm_quant(const GemmPlan* p, const float* pieces, cons
 // ---------------------------------------------------------------------------
 __global__ void swiglu_quant_kernel(const float* __restrict__ pieces, int pN, int pnb, long long pU,
                                     int pG, int M, int F, uint8_t* act, int32_t* status) {
-  pdl_wait();
   pdl_trigger();
+  pdl_wait();
   const int nb = F / 256;
   const int b = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int row = blockIdx.y;
@@ -211,13 +234,13 @@ __global__ void swiglu_quant_kernel(const float* __restrict__ pieces, int pN, in
     return;
   }
   const int col0 = 256 * b + 8 * (threadIdx.x & 31);
-  float v[8];
+  float gt[8], up[8], v[8];
+  piece_sum8(pieces, pN, piece_slots(pnb, (int)pU, pG, col0), row, col0, gt);
+  piece_sum8(pieces, pN, piece_slots(pnb, (int)pU, pG, F + col0), row, F + col0, up);
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const float gt = piece_sum(pieces, pN, pnb, pU, pG, row, col0 + i);
-    const float up = piece_sum(pieces, pN, pnb, pU, pG, row, F + col0 + i);
-    const float sl = gt / (1.0f + expf(-gt));
-    v[i] = sl * up;
+    const float sl = gt[i] / (1.0f + expf(-gt[i]));
+    v[i] = sl * up[i];
   }
   quant_block_warp(v, row, b, F, act, nullptr, nullptr, nullptr, status);
 }
@@ -240,8 +263,8 @@ cudaError_t launch_swiglu_quant(const GemmPlan& p, const float* pieces, int M, i
 __global__ void qkv_post_kernel(const float* __restrict__ pieces, int pN, int pnb, long long pU,
                                 int pG, int M, int nq, int nkv, int dh, KvView kv, int layer,
                                 uint8_t* __restrict__ qfrag, const int32_t* status) {
-  pdl_wait();
   pdl_trigger();
+  pdl_wait();
   const int row = blockIdx.y;
   const int col = blockIdx.x * blockDim.x + threadIdx.x;
   const int qcols = nq * dh;
@@ -250,7 +273,7 @@ __global__ void qkv_post_kernel(const float* __restrict__ pieces, int pN, int pn
     if (col < qcols) write_qfrag(qfrag, row, col / dh, col % dh, 0.f);
     return;
   }
-  const float v = piece_sum(pieces, pN, pnb, pU, pG, row, col);
+  const float v = piece_sum(pieces, pN, piece_slots(pnb, (int)pU, pG, col), row, col);
   if (col < qcols) {
     write_qfrag(qfrag, row, col / dh, col % dh, v);
     return;
@@ -302,12 +325,18 @@ __global__ void __launch_bounds__(256)
 head_argmax_kernel(const float* __restrict__ pieces, int pN, int pnb, long long pU, int pG, int M,
                    float* __restrict__ logits, float* __restrict__ part_val,
                    int32_t* __restrict__ part_idx, int32_t* status) {
-  pdl_wait();
   pdl_trigger();
+  pdl_wait();
   __shared__ float sv[16][8];
   __shared__ int si[16][8];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int col_base = blockIdx.x * kArgCols;
+  int nsl[kArgCols / 256];
+#pragma unroll
+  for (int k = 0; k < kArgCols / 256; ++k) {
+    const int col = col_base + threadIdx.x + 256 * k;
+    nsl[k] = col < pN ? piece_slots(pnb, (int)pU, pG, col) : 1;
+  }
   bool bad = false;
   for (int row = 0; row < 16; ++row) {
     float bv = -INFINITY;
@@ -317,7 +346,7 @@ head_argmax_kernel(const float* __restrict__ pieces, int pN, int pnb, long long 
       for (int k = 0; k < kArgCols / 256; ++k) {
         const int col = col_base + threadIdx.x + 256 * k;
         if (col < pN) {
-          const float v = piece_sum(pieces, pN, pnb, pU, pG, row, col);
+          const float v = piece_sum(pieces, pN, nsl[k], row, col);
           if (logits) logits[(size_t)row * pN + col] = v;
           if (!isfinite(v)) bad = true;
           better(bv, bi, v, col);
@@ -360,8 +389,8 @@ cudaError_t launch_head_argmax(const GemmPlan& p, const float* pieces, int M, fl
 __global__ void argmax_final_kernel(const float* __restrict__ part_val,
                                     const int32_t* __restrict__ part_idx, int nparts, int M,
                                     int32_t* __restrict__ idx) {
-  pdl_wait();
   pdl_trigger();
+  pdl_wait();
   const int lane = threadIdx.x;
   for (int row = 0; row < M; ++row) {
     float bv = -INFINITY;
@@ -408,8 +437,8 @@ cudaError_t launch_kv_reset(const KvView& kv, cudaStream_t st) {
 // step_state: [0] = n_past, [1] = 1 when the block was appended
 __global__ void kv_reserve_kernel(KvView kv, int n, int commit, const int32_t* __restrict__ draft,
                                   int k, int vocab, int32_t* status, int32_t* step_state) {
-  pdl_wait();
   pdl_trigger();
+  pdl_wait();
   if (threadIdx.x != 0 || blockIdx.x != 0) return;
   int st = 0;
   if (step_state) {
@@ -498,8 +527,8 @@ __global__ void accept_kernel(const int32_t* __restrict__ idx_in, const float* _
                               const int32_t* __restrict__ draft, int k, int vocab, KvView kv,
                               int has_kv, const int32_t* step_state, int32_t* status, int32_t* res,
                               int32_t* idx_out) {
-  pdl_wait();
   pdl_trigger();
+  pdl_wait();
   __shared__ int idx_s[16];
   const int lane = threadIdx.x;
   for (int row = 0; row <= k; ++row) {

@@ -70,7 +70,10 @@ def kv_read_bytes(cfg, ctx):
 # clocks sampled during the timed region
 # ---------------------------------------------------------------------------
 class Clocks:
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi sampling every 50 ms; only the samples whose timestamps fall
+    inside the timed window [mark_start, mark_stop] are reported (the nearest
+    ones if the window is shorter than the sampling period)."""
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -78,18 +81,42 @@ class Clocks:
         self.index = index
         self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
         self.p = None
+        self.t0 = self.t1 = None
 
     def start(self):
         try:
             self.p = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
-                                       "--format=csv,noheader,nounits", "-lms", "200"],
+                                       "--format=csv,noheader,nounits", "-lms", "50"],
                                       stdout=self.f, stderr=subprocess.DEVNULL)
         except OSError:
             self.p = None
+            return
+        # wait (up to 10 s) for the first sample so that the window is covered
+        for _ in range(200):
+            if os.path.getsize(self.f.name) > 0:
+                break
+            time.sleep(0.05)
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_stop(self):
+        self.t1 = time.time()
+
+    @staticmethod
+    def _ts(x):
+        import datetime
+        for fmt in ("%Y/%m/%d %H:%M:%S.%f", "%Y/%m/%d %H:%M:%S"):
+            try:
+                return datetime.datetime.strptime(x.strip(), fmt).timestamp()
+            except ValueError:
+                continue
+        return None
 
     def stop(self):
         if self.p is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.1)
         self.p.terminate()
         try:
             self.p.wait(timeout=5)
@@ -98,21 +125,31 @@ class Clocks:
         self.f.flush()
         rows = [r.split(",") for r in open(self.f.name).read().strip().splitlines() if r.strip()]
         os.unlink(self.f.name)
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        samples = []
         for r in rows:
             r = [x.strip() for x in r]
             try:
-                sm.append(float(r[1]))
-                mx.append(float(r[2]))
+                samples.append((self._ts(r[0]), float(r[2]), float(r[3]), r[6:10]))
             except (ValueError, IndexError):
                 continue
-            for nm, v in zip(names, r[5:9]):
+        inside = [x for x in samples
+                  if x[0] is not None and self.t0 is not None and self.t0 <= x[0] <= self.t1]
+        if not inside and samples and self.t0 is not None:
+            mid = 0.5 * (self.t0 + (self.t1 or self.t0))
+            timed = [x for x in samples if x[0] is not None]
+            inside = sorted(timed, key=lambda x: abs(x[0] - mid))[:2] if timed else samples[-2:]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for x in inside:
+            for nm, v in zip(names, x[3]):
                 if v.lower() in ("active", "1", "yes"):
                     reasons.add(nm)
+        sm = [x[1] for x in inside]
+        mx = [x[2] for x in inside]
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(mx) if mx else None,
-                "samples": len(sm), "reasons": sorted(reasons)}
+                "samples": len(sm), "window_s": (self.t1 - self.t0) if self.t0 and self.t1 else None,
+                "reasons": sorted(reasons)}
 
 
 # ---------------------------------------------------------------------------
@@ -290,6 +327,8 @@ def run_gpu(args, rank, world):
             raise abi.SpecError("spec_verify_step", rc)
         abi.check("spec_kv_rollback", abi.spec_kv_rollback(ctx.h, ks, CTX))
 
+    clocks = Clocks(local)
+    clocks.start()
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -300,18 +339,18 @@ def run_gpu(args, rank, world):
     dist = world > 1
     if dist:
         import torch.distributed as tdist
-    clocks = Clocks(local)
-    clocks.start()
     if dist:
         tdist.barrier()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.nvtx.range_push("timed")
+    clocks.mark_start()
     e0.record(stream)
     for _ in range(args.steps):
         step()
     e1.record(stream)
     torch.cuda.synchronize()
+    clocks.mark_stop()
     torch.cuda.nvtx.range_pop()
     if dist:
         tdist.barrier()
@@ -445,7 +484,7 @@ def run_gemm_shape(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--gemm-shape", default=None,

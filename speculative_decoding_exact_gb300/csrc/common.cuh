@@ -199,12 +199,15 @@ SPEC_DEV bool mbar_try(uint64_t* mbar, uint32_t parity) {
   return done != 0;
 }
 // wait for the phase with the given parity, giving up after limit_ns of wall
-// time (the bound holds whatever the hardware does with the suspend hint)
+// time (the bound holds whatever the hardware does with the suspend hint; the
+// clock is read once per 32 tries to keep the loop short)
 SPEC_DEV bool mbar_wait_ns(uint64_t* mbar, uint32_t parity, uint64_t limit_ns) {
   if (mbar_try(mbar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
-    if (mbar_try(mbar, parity)) return true;
+#pragma unroll 1
+    for (int k = 0; k < 32; ++k)
+      if (mbar_try(mbar, parity)) return true;
     if (globaltimer_ns() - t0 > limit_ns) return false;
   }
 }

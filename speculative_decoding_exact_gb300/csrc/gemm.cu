@@ -33,8 +33,8 @@
 // MMAs of a superblock; each runs converged and lets one elected lane issue,
 // which keeps the MMA operands in uniform registers (a lone lane issuing
 // MMAs manages about one per 100 cycles, a converged warp about one per 35).
-// Eight warps read the results back and combine them (two threads per
-// column, 8 rows each), and one warp issues the bulk copies that stage
+// Four warps read the results back and combine them (one thread per column,
+// all 16 rows in two batches of 8), and one warp issues the bulk copies that stage
 // weights and activations.  A is triple-buffered and D double-buffered in
 // TMEM, so unpacking, MMAs and combining of consecutive superblocks overlap.
 //
@@ -171,17 +171,17 @@ SPEC_DEV void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
 //   MMA warps, unit i: wait a_full[i%3] and d_free[i%2] (unit i-2 read out)
 //     -> the elected lane issues the warp's share of the MMAs into D[i%2] and
 //     commits to mma_done[i%2] and a_free[i%3] (one arrival per MMA warp).
-//   combine warps, unit i: wait mma_done[i%2] -> read D in two halves, arrive
-//     d_free[i%2] -> read the unit's activation scales, arrive empty[s] ->
-//     combine.
+//   combine warps, unit i: wait mma_done[i%2] -> start reading D, read the
+//     unit's scales from its slot, arrive empty[s] -> read D (rows 0-7, then
+//     8-15), arrive d_free[i%2] -> combine.
 constexpr uint64_t kWaitNs = 2000000000ull;
-constexpr int kWarpCombine0 = kGemmUnpackWarps;            // 8 combine warps
-constexpr int kWarpProducer = kWarpCombine0 + 8;
+constexpr int kWarpCombine0 = kGemmUnpackWarps;
+constexpr int kWarpProducer = kWarpCombine0 + kGemmCombineThreads / 32;
 constexpr int kWarpMma0 = kWarpProducer + 1;
 constexpr int kGemmWarps = kWarpMma0 + kGemmMmaWarps;
 static_assert(kGemmWarps * 32 == kGemmThreads, "warp roles");
 // registers: each of the 4 schedulers holds the registers of its warps (16K)
-constexpr int kGemmMaxRegs = kGemmWarps <= 16 ? 128 : 96;
+constexpr int kGemmMaxRegs = kGemmWarps <= 12 ? 168 : (kGemmWarps <= 16 ? 128 : 96);
 static_assert(((kGemmWarps + 3) / 4) * 32 * kGemmMaxRegs <= 16384, "register budget");
 
 // MMA share of warp q: sub-blocks mma_j0(q) .. mma_j0(q+1)-1 (two MMAs each);
@@ -375,12 +375,11 @@ gemm_q4k_kernel(const uint8_t* __restrict__ wt, const uint8_t* __restrict__ act,
     // -------------------------------------------------------------- combine
     pdl_trigger();
     pdl_wait();
-    const int hf = (warp - kWarpCombine0) >> 2;     // rows 8hf .. 8hf+7
     const uint32_t lane_base = (uint32_t)(32 * lg) << 16;
     bool ok = true;
-    float y[8];
+    float y[16];
 #pragma unroll
-    for (int n = 0; n < 8; ++n) y[n] = 0.f;
+    for (int n = 0; n < 16; ++n) y[n] = 0.f;
     int ug = u0 / nb;
     int ub = u0 - ug * nb;
     for (int u = 0; u < nunits; ++u) {
@@ -393,66 +392,75 @@ gemm_q4k_kernel(const uint8_t* __restrict__ wt, const uint8_t* __restrict__ act,
       const int cols = min(kGemmCols, N - kGemmCols * ug);
       const bool valid = col_local < cols;
       const int col = kGemmCols * ug + col_local;
-      const uint32_t dbase = tmem + lane_base + (uint32_t)(kTmemD0 + (u & 1) * kTmemDStride + 8 * hf);
-      // the stage was filled before the MMAs of this unit were issued
+      const uint32_t dbase = tmem + lane_base + (uint32_t)(kTmemD0 + (u & 1) * kTmemDStride);
+      // rows 0..7 of every accumulator: start the TMEM loads
+      uint32_t dj[8][8], rm[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) tmem_ld8(dbase + 16 * j, dj[j]);
+      tmem_ld8(dbase + kTmemDm, rm);
+      // the stage was filled before the MMAs of this unit were issued, and the
+      // MMAs are done with it: read the scales and free the slot
       uint4 hdr = make_uint4(0, 0, 0, 0);
       if (valid) hdr = *reinterpret_cast<const uint4*>(stg + col_local * kSB);
-      unsigned long long acc[2][4];               // [half][row pair]: sum_j sc_j S_j * 2^-9
-      uint32_t rm[8];
+      float da[16];
+      {
+        const float4* dap = reinterpret_cast<const float4*>(stg + kStageWeightBytes + kActSlots * 512);
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t dj[4][8];
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) tmem_ld8(dbase + 16 * (4 * h + jj), dj[jj]);
-        if (h == 1) {
-          tmem_ld8(dbase + kTmemDm, rm);
-          tmem_wait_ld();
-          tc_fence_before();
-          mbar_arrive(&d_free[u & 1]);
-        } else {
-          tmem_wait_ld();
-        }
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          // 6-bit scale as an exact float: 2^23 + sc with the 2^23 subtracted
-          const float f =
-              __uint_as_float(0x4B000000u | sub_scale(hdr.y, hdr.z, hdr.w, 4 * h + jj)) - 8388608.f;
-          const unsigned long long sc2 = f2pack(f, f);
-#pragma unroll
-          for (int n = 0; n < 8; n += 2) {
-            const unsigned long long sj = f2pack(__uint_as_float(dj[jj][n]), __uint_as_float(dj[jj][n + 1]));
-            acc[h][n >> 1] = jj == 0 ? f2mul(sc2, sj) : f2fma(sc2, sj, acc[h][n >> 1]);
-          }
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const float4 v4 = dap[q4];
+          da[4 * q4] = v4.x; da[4 * q4 + 1] = v4.y; da[4 * q4 + 2] = v4.z; da[4 * q4 + 3] = v4.w;
         }
       }
-      const float4* dap =
-          reinterpret_cast<const float4*>(stg + kStageWeightBytes + kActSlots * 512 + 32 * hf);
-      const float4 da0 = dap[0], da1 = dap[1];
       mbar_arrive(&empty[pslot]);
-      const float da[8] = {da0.x, da0.y, da0.z, da0.w, da1.x, da1.y, da1.z, da1.w};
+      // 6-bit scales as exact floats: 2^23 + sc with the 2^23 subtracted
+      float scf[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        scf[j] = __uint_as_float(0x4B000000u | sub_scale(hdr.y, hdr.z, hdr.w, j)) - 8388608.f;
       // d * 2^9 (exact): the D values are 2^-9 * integer sums
       const float d = __half2float(__ushort_as_half((unsigned short)(hdr.x & 0xffff))) * 512.f;
       const float dm = __half2float(__ushort_as_half((unsigned short)(hdr.x >> 16)));
       const unsigned long long D2 = f2pack(d, d), M2 = f2pack(dm, dm);
 #pragma unroll
-      for (int n = 0; n < 8; n += 2) {
-        const unsigned long long isc = f2add(acc[0][n >> 1], acc[1][n >> 1]);
-        const unsigned long long imn = f2pack(__uint_as_float(rm[n]), __uint_as_float(rm[n + 1]));
-        const unsigned long long v =
-            f2mul(f2pack(da[n], da[n + 1]), f2sub(f2mul(D2, isc), f2mul(M2, imn)));
-        const unsigned long long yy = f2add(f2pack(y[n], y[n + 1]), v);
-        f2unpack(yy, y[n], y[n + 1]);
-        if (SUMS) {
-          float l0, l1, h0, h1;
-          f2unpack(acc[0][n >> 1], l0, l1);
-          f2unpack(acc[1][n >> 1], h0, h1);
+      for (int rb = 0; rb < 2; ++rb) {             // rows 8rb .. 8rb+7
+        if (rb == 1) {
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int row = 8 * hf + n + e;
-            if (valid && row < m_sums) {
-              const size_t o = ((size_t)row * N + col) * nb + ub;
-              isc_out[o] = (int)((e ? l1 : l0) * 512.f) + (int)((e ? h1 : h0) * 512.f);
-              imn_out[o] = (int)__uint_as_float(rm[n + e]);
+          for (int j = 0; j < 8; ++j) tmem_ld8(dbase + 16 * j + 8, dj[j]);
+          tmem_ld8(dbase + kTmemDm + 8, rm);
+        }
+        tmem_wait_ld();
+        if (rb == 1) {
+          tc_fence_before();
+          mbar_arrive(&d_free[u & 1]);
+        }
+#pragma unroll
+        for (int n = 0; n < 8; n += 2) {
+          unsigned long long lo = 0ull, hi = 0ull;   // sub-blocks 0-3 and 4-7: sum_j sc_j S_j * 2^-9
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const unsigned long long sc2 = f2pack(scf[j], scf[j]);
+            const unsigned long long sj = f2pack(__uint_as_float(dj[j][n]), __uint_as_float(dj[j][n + 1]));
+            if (j < 4) lo = j == 0 ? f2mul(sc2, sj) : f2fma(sc2, sj, lo);
+            else hi = j == 4 ? f2mul(sc2, sj) : f2fma(sc2, sj, hi);
+          }
+          const int r = 8 * rb + n;
+          const unsigned long long isc = f2add(lo, hi);
+          const unsigned long long imn = f2pack(__uint_as_float(rm[n]), __uint_as_float(rm[n + 1]));
+          const unsigned long long v =
+              f2mul(f2pack(da[r], da[r + 1]), f2sub(f2mul(D2, isc), f2mul(M2, imn)));
+          const unsigned long long yy = f2add(f2pack(y[r], y[r + 1]), v);
+          f2unpack(yy, y[r], y[r + 1]);
+          if (SUMS && valid) {
+            float l0, l1, h0, h1;
+            f2unpack(lo, l0, l1);
+            f2unpack(hi, h0, h1);
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              if (r + e < m_sums) {
+                const size_t o = ((size_t)(r + e) * N + col) * nb + ub;
+                isc_out[o] = (int)((e ? l1 : l0) * 512.f) + (int)((e ? h1 : h0) * 512.f);
+                imn_out[o] = (int)__uint_as_float(rm[n + e]);
+              }
             }
           }
         }
@@ -461,12 +469,12 @@ gemm_q4k_kernel(const uint8_t* __restrict__ wt, const uint8_t* __restrict__ act,
       if (u0 + u + 1 == u1 || ub + 1 == nb) {
         const int slot_id = (int)blockIdx.x - cta_of_unit((long long)ug * nb, U, G);
         if (valid) {
-          float* base = pieces + (size_t)slot_id * 16 * N + (size_t)(8 * hf) * N + col;
+          float* base = pieces + (size_t)slot_id * 16 * N + col;
 #pragma unroll
-          for (int n = 0; n < 8; ++n) base[(size_t)n * N] = y[n];
+          for (int n = 0; n < 16; ++n) base[(size_t)n * N] = y[n];
         }
 #pragma unroll
-        for (int n = 0; n < 8; ++n) y[n] = 0.f;
+        for (int n = 0; n < 16; ++n) y[n] = 0.f;
       }
       if (++ub == nb) {
         ub = 0;

@@ -19,12 +19,12 @@ struct GemmPlan {
 };
 
 // tcgen05 GEMM: one CTA per SM owns 128 weight columns (one per TMEM lane).
-// Warp roles: 4 unpack warps (one thread per column), 8 combine warps (two
-// threads per column, 8 rows each), one warp that issues the bulk copies, and
-// kGemmMmaWarps warps that share the 17 MMAs of a superblock.
+// Warp roles: 4 unpack warps and 4 combine warps (one thread per column each),
+// one warp that issues the bulk copies, and kGemmMmaWarps warps that share the
+// 17 MMAs of a superblock.
 constexpr int kGemmUnpackWarps = 4;
 constexpr int kGemmUnpackThreads = 32 * kGemmUnpackWarps;
-constexpr int kGemmCombineThreads = 256;
+constexpr int kGemmCombineThreads = 128;
 constexpr int kGemmMmaWarps = 3;
 constexpr int kGemmThreads = kGemmUnpackThreads + kGemmCombineThreads + 32 + 32 * kGemmMmaWarps;
 constexpr int kTilesPerGroup = 8;          // 16-column tiles per group = 128 columns

@@ -489,7 +489,13 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--gemm-shape", default=None,
                     help="NxK: time one Q4_K GEMM shape instead of the verify step")
+    ap.add_argument("--ctx", type=int, default=2048,
+                    help="KV context of the verify step (the long-context sweep uses 16384, 32768)")
     args = ap.parse_args()
+    global CTX
+    if args.ctx % 16 or args.ctx < 16:
+        ap.error("--ctx must be a positive multiple of 16")
+    CTX = args.ctx
     if args.gemm_shape:
         run_gemm_shape(args)
         return

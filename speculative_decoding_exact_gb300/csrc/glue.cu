@@ -1,6 +1,6 @@
 // glue.cu — the small kernels around the GEMMs of the verify step:
-// activation quantisation into the tensor-core fragment order, residual add +
-// RMSNorm + quantisation (one 8-CTA cluster per row), SwiGLU + quantisation,
+// activation quantisation into the tensor-core operand order, residual add +
+// RMSNorm + quantisation (one CTA per row), SwiGLU + quantisation,
 // QKV split with the K/V append into the paged bf16 cache, the LM-head argmax,
 // the greedy accept + KV rollback kernel and the KV metadata kernels.
 //
@@ -10,13 +10,9 @@
 //   verify lengths, rewind Ch. 8 §8.6 items 3 and 4
 //   F32 residual, one fixed reduction order
 //                          Ch. 32 "Precision across the handoff" (intro, §32.4)
-#include <cooperative_groups.h>
-
 #include "common.cuh"
 #include "internal.h"
 #include "quant.cuh"
-
-namespace cg = cooperative_groups;
 
 namespace spec {
 
@@ -123,65 +119,63 @@ cudaError_t launch_quantize(const float* x, int M, int K, uint8_t* act, int8_t* 
 }
 
 // ---------------------------------------------------------------------------
-// residual + RMSNorm + quantisation.  One cluster of 8 CTAs per row; CTA c of
-// the cluster owns the 256-blocks b = c, c+8, c+16, ... (warp w takes the w-th
-// of them).  The row's sum of squares is reduced lane -> warp (butterfly) ->
-// CTA (warp order) -> cluster (rank order): one fixed order set by H alone.
-// x_out = x_in + sum(pieces) (fp32 add) when pieces are given.
+// residual + RMSNorm + quantisation.  One CTA per row (16 CTAs: rows >= M
+// write zero activation blocks); warp w owns the 256-blocks b = w and
+// b = w + warps (H/256 <= 64).  The row's sum of squares is reduced lane ->
+// warp (butterfly, the warp's blocks in order) -> CTA (warp order): one fixed
+// order set by H alone.  x_out = x_in + sum(pieces) (fp32 add) when pieces
+// are given.
 // ---------------------------------------------------------------------------
-constexpr int kNormCluster = 8;
-
-__global__ void __cluster_dims__(kNormCluster, 1, 1)
+__global__ void __launch_bounds__(1024)
 resid_norm_quant_kernel(const float* __restrict__ pieces, int pN, int pnb, long long pU, int pG,
                         const float* x_in, float* x_out,
                         const float* __restrict__ gamma, float eps, int M, int H, uint8_t* act,
                         float* __restrict__ xnorm_out, int32_t* status) {
   pdl_trigger();
   pdl_wait();
-  cg::cluster_group cluster = cg::this_cluster();
-  __shared__ float warp_ss[8];
-  __shared__ float cta_ss;
-  const int row = blockIdx.y;
-  const int c = (int)cluster.block_rank();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __shared__ float warp_ss[32];
+  __shared__ float row_rinv;
+  const int row = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
   const int nb = H / 256;
-  const int b = c + kNormCluster * warp;
-  const bool has = b < nb;
-  float v[8];
+  float v[2][8];
   float ss = 0.f;
-  if (row < M && has) {
-    const int col0 = 256 * b + 8 * lane;
-    load8(x_in + (size_t)row * H + col0, v);
-    if (pieces) {
-      float ps[8];
-      piece_sum8(pieces, pN, piece_slots(pnb, (int)pU, pG, col0), row, col0, ps);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) v[i] = v[i] + ps[i];
-      float4* o = reinterpret_cast<float4*>(x_out + (size_t)row * H + col0);
-      o[0] = make_float4(v[0], v[1], v[2], v[3]);
-      o[1] = make_float4(v[4], v[5], v[6], v[7]);
-    } else if (x_out != x_in && x_out) {
-      float4* o = reinterpret_cast<float4*>(x_out + (size_t)row * H + col0);
-      o[0] = make_float4(v[0], v[1], v[2], v[3]);
-      o[1] = make_float4(v[4], v[5], v[6], v[7]);
+  for (int t = 0; t < 2; ++t) {
+    const int b = warp + t * nw;
+    if (row < M && b < nb) {
+      const int col0 = 256 * b + 8 * lane;
+      load8(x_in + (size_t)row * H + col0, v[t]);
+      if (pieces) {
+        float ps[8];
+        piece_sum8(pieces, pN, piece_slots(pnb, (int)pU, pG, col0), row, col0, ps);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[t][i] = v[t][i] + ps[i];
+      }
+      if (x_out && (pieces || x_out != x_in)) {
+        float4* o = reinterpret_cast<float4*>(x_out + (size_t)row * H + col0);
+        o[0] = make_float4(v[t][0], v[t][1], v[t][2], v[t][3]);
+        o[1] = make_float4(v[t][4], v[t][5], v[t][6], v[t][7]);
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) ss += v[t][i] * v[t][i];
     }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) ss += v[i] * v[i];
   }
   ss = warp_sum(ss);
   if (lane == 0) warp_ss[warp] = ss;
   __syncthreads();
   if (threadIdx.x == 0) {
-    float s = 0.f;
-    for (int w = 0; w < 8; ++w) s += warp_ss[w];
-    cta_ss = s;
+    float total = 0.f;
+    for (int w = 0; w < nw; ++w) total += warp_ss[w];
+    row_rinv = 1.0f / sqrtf(total / (float)H + eps);
   }
-  cluster.sync();
-  float total = 0.f;
-  for (int r = 0; r < kNormCluster; ++r) total += *cluster.map_shared_rank(&cta_ss, r);
-  if (has) {
+  __syncthreads();
+  const float rinv = row_rinv;
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int b = warp + t * nw;
+    if (b >= nb) continue;
     if (row < M) {
-      const float rinv = 1.0f / sqrtf(total / (float)H + eps);
       const int col0 = 256 * b + 8 * lane;
       float gm[8];
       if (gamma) {
@@ -191,26 +185,28 @@ resid_norm_quant_kernel(const float* __restrict__ pieces, int pN, int pnb, long 
         for (int i = 0; i < 8; ++i) gm[i] = 1.f;
       }
 #pragma unroll
-      for (int i = 0; i < 8; ++i) v[i] = v[i] * rinv * gm[i];
+      for (int i = 0; i < 8; ++i) v[t][i] = v[t][i] * rinv * gm[i];
       if (xnorm_out) {
         float4* o = reinterpret_cast<float4*>(xnorm_out + (size_t)row * H + col0);
-        o[0] = make_float4(v[0], v[1], v[2], v[3]);
-        o[1] = make_float4(v[4], v[5], v[6], v[7]);
+        o[0] = make_float4(v[t][0], v[t][1], v[t][2], v[t][3]);
+        o[1] = make_float4(v[t][4], v[t][5], v[t][6], v[t][7]);
       }
-      quant_block_warp(v, row, b, H, act, nullptr, nullptr, nullptr, status);
+      quant_block_warp(v[t], row, b, H, act, nullptr, nullptr, nullptr, status);
     } else {
       zero_block_warp(row, b, act);
     }
   }
-  cluster.sync();   // keep this CTA's shared memory alive until all peers read it
 }
 
 cudaError_t launch_resid_norm_quant(const GemmPlan* p, const float* pieces, const float* x_in,
                                     float* x_out, const float* gamma, float eps, int M, int H,
                                     uint8_t* act, float* xnorm_out, int32_t* status,
                                     cudaStream_t st, bool pdl) {
+  const int nb = H / 256;
+  const int warps = nb < 32 ? nb : 32;
+  if (nb > 2 * warps) return cudaErrorInvalidValue;
   cudaLaunchAttribute attrs[2];
-  cudaLaunchConfig_t cfg = make_cfg(dim3(kNormCluster, 16), dim3(256), 0, st, pdl, attrs);
+  cudaLaunchConfig_t cfg = make_cfg(dim3(16), dim3(32 * warps), 0, st, pdl, attrs);
   const int pN = p ? p->N : 0, pnb = p ? p->nb : 1, pG = p ? p->G : 1;
   const long long pU = p ? p->U : 1;
   return cudaLaunchKernelEx(&cfg, resid_norm_quant_kernel, pieces, pN, pnb, pU, pG, x_in, x_out,

@@ -327,6 +327,37 @@ def test_attention_parity(small_ctx, n_past, M):
     assert_close(out.cpu().numpy(), ref, what="attention")
 
 
+@pytest.fixture(scope="module")
+def long_ctx():
+    import __graft_entry__
+    __graft_entry__.build()
+    c = runtime.Context(SMALL, max_ctx=16448)
+    yield c
+    c.close()
+
+
+def test_attention_parity_long_context(long_ctx):
+    # long-context verify (16k keys, the block straddling a page boundary):
+    # 257 64-key chunks per row, merged in chunk order
+    cfg = SMALL
+    n_past, M = 16384 + 7, 16
+    pages = (n_past + M + 15) // 16 + 1
+    kv = make_kv(cfg, num_pages=pages, max_seq_pages=pages)
+    kv.reset(long_ctx)
+    kv.extend(long_ctx, n_past + M)
+    okv = oracle.KV(_ocfg(cfg), pages, pages)
+    okv.extend(n_past + M)
+    fill_kv_both(long_ctx, cfg, kv, okv, 1, n_past + M, 90)
+    q = synth.normal((M, cfg.n_q_heads, 128), 91, M) * 4.0
+    qd = dev(q)
+    out = torch.zeros((M, cfg.hidden), dtype=torch.float32, device="cuda")
+    abi.check("spec_attention", abi.spec_attention(long_ctx.h, kv.struct(), 1, qd.data_ptr(), M,
+                                                   out.data_ptr()))
+    sync()
+    ref = okv.attention(1, q, n_past)
+    assert_close(out.cpu().numpy(), ref, what="attention at 16k context")
+
+
 def test_attention_batch_height_invariance(small_ctx):
     cfg = SMALL
     n_past, M = 45, 16

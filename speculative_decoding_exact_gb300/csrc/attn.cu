@@ -313,7 +313,7 @@ attn_merge_kernel(const float* __restrict__ part, int M, int nq, int max_chunks,
                   const int32_t* seq_len, float* __restrict__ out, uint8_t* act, int32_t* status) {
   pdl_trigger();
   pdl_wait();
-  extern __shared__ float msh[];          // [2][max_chunks] weights
+  extern __shared__ float msh[];          // [2][max_chunks] weights, then [2][max_chunks] sums
   __shared__ float vals[256];
   __shared__ float lsum[2];
   const int b = blockIdx.x, row = blockIdx.y;
@@ -328,11 +328,14 @@ attn_merge_kernel(const float* __restrict__ part, int M, int nq, int max_chunks,
     const float* st = part + (((size_t)(2 * b + hh)) * 16 + row) * 130;
     // lane takes the chunks lane, lane + 32, ...: maxima first (kept in
     // shared memory), then the weights and the weighted sums
+    // (max, sum) of chunk c are adjacent: one 8-byte load per chunk
     float m = -INFINITY;
+    float* lsh = msh + 2 * max_chunks;      // the chunk sums, [2][max_chunks]
     for (int c = lane; c < nchunks; c += 32) {
-      const float mc = st[c * cstride + 128];
-      msh[hh * max_chunks + c] = mc;
-      m = fmaxf(m, mc);
+      const float2 ml = *reinterpret_cast<const float2*>(st + c * cstride + 128);
+      msh[hh * max_chunks + c] = ml.x;
+      lsh[hh * max_chunks + c] = ml.y;
+      m = fmaxf(m, ml.x);
     }
     m = warp_max(m);
     float L = 0.f;
@@ -340,7 +343,7 @@ attn_merge_kernel(const float* __restrict__ part, int M, int nq, int max_chunks,
       const float mc = msh[hh * max_chunks + c];
       const float w = (mc == -INFINITY) ? 0.f : expf(mc - m);
       msh[hh * max_chunks + c] = w;
-      L += w * st[c * cstride + 129];
+      L += w * lsh[hh * max_chunks + c];
     }
     L = warp_sum(L);
     if (lane == 0) lsum[hh] = L;
@@ -352,13 +355,12 @@ attn_merge_kernel(const float* __restrict__ part, int M, int nq, int max_chunks,
   const float* w = msh + hh * max_chunks;
   float o = 0.f;
   int c = 0;
-  for (; c + 4 <= nchunks; c += 4) {
-    const float o0 = pp[(c + 0) * cstride], o1 = pp[(c + 1) * cstride];
-    const float o2 = pp[(c + 2) * cstride], o3 = pp[(c + 3) * cstride];
-    o += w[c + 0] * o0;
-    o += w[c + 1] * o1;
-    o += w[c + 2] * o2;
-    o += w[c + 3] * o3;
+  for (; c + 8 <= nchunks; c += 8) {        // 8 loads in flight, then the sums in chunk order
+    float oc[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) oc[k] = pp[(c + k) * cstride];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) o += w[c + k] * oc[k];
   }
   for (; c < nchunks; ++c) o += w[c] * pp[c * cstride];
   const float res = valid ? o / lsum[hh] : 0.f;
@@ -405,7 +407,7 @@ cudaError_t launch_attention(const AttnPlan& a, const KvView& kv, int layer, con
   cudaLaunchConfig_t cfg2 = {};
   cfg2.gridDim = dim3(a.nq * 128 / 256, 16);
   cfg2.blockDim = dim3(256);
-  cfg2.dynamicSmemBytes = sizeof(float) * (2 * (size_t)a.max_chunks + 2);
+  cfg2.dynamicSmemBytes = sizeof(float) * (4 * (size_t)a.max_chunks + 2);
   cfg2.stream = st;
   cfg2.attrs = attr;
   cfg2.numAttrs = pdl ? 1 : 0;

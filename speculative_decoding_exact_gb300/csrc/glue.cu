@@ -131,13 +131,25 @@ resid_norm_quant_kernel(const float* __restrict__ pieces, int pN, int pnb, long 
                         const float* x_in, float* x_out,
                         const float* __restrict__ gamma, float eps, int M, int H, uint8_t* act,
                         float* __restrict__ xnorm_out, int32_t* status) {
-  pdl_trigger();
-  pdl_wait();
   __shared__ float warp_ss[32];
   __shared__ float row_rinv;
   const int row = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
   const int nb = H / 256;
+  // gamma does not depend on the previous kernel: fetch it before waiting
+  float gm[2][8];
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int b = warp + t * nw;
+    if (gamma && b < nb) {
+      load8(gamma + 256 * b + 8 * lane, gm[t]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) gm[t][i] = 1.f;
+    }
+  }
+  pdl_trigger();
+  pdl_wait();
   float v[2][8];
   float ss = 0.f;
 #pragma unroll
@@ -177,15 +189,8 @@ resid_norm_quant_kernel(const float* __restrict__ pieces, int pN, int pnb, long 
     if (b >= nb) continue;
     if (row < M) {
       const int col0 = 256 * b + 8 * lane;
-      float gm[8];
-      if (gamma) {
-        load8(gamma + col0, gm);
-      } else {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) gm[i] = 1.f;
-      }
-#pragma unroll
-      for (int i = 0; i < 8; ++i) v[t][i] = v[t][i] * rinv * gm[i];
+      for (int i = 0; i < 8; ++i) v[t][i] = v[t][i] * rinv * gm[t][i];
       if (xnorm_out) {
         float4* o = reinterpret_cast<float4*>(xnorm_out + (size_t)row * H + col0);
         o[0] = make_float4(v[t][0], v[t][1], v[t][2], v[t][3]);

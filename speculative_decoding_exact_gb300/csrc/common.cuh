@@ -116,6 +116,23 @@ SPEC_DEV float warp_max(float v) {
   return v;
 }
 
+// Thread-block cluster: this CTA's rank, a store into a peer CTA's shared
+// memory, and the cluster-wide barrier (release on arrive, acquire on wait).
+SPEC_DEV uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
+  return r;
+}
+SPEC_DEV void st_cluster_f32(const float* local, uint32_t rank, float v) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+  asm volatile("st.shared::cluster.f32 [%0], %1;\n" ::"r"(remote), "f"(v) : "memory");
+}
+SPEC_DEV void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+
 // Programmatic dependent launch: let the next kernel in the stream start its
 // independent prologue (weight prefetch) early, and wait for the previous
 // kernel's results before touching them.

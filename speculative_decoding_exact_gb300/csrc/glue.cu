@@ -119,28 +119,32 @@ cudaError_t launch_quantize(const float* x, int M, int K, uint8_t* act, int8_t* 
 }
 
 // ---------------------------------------------------------------------------
-// residual + RMSNorm + quantisation.  One CTA per row (16 CTAs: rows >= M
-// write zero activation blocks); warp w owns the 256-blocks b = w and
-// b = w + warps (H/256 <= 64).  The row's sum of squares is reduced lane ->
-// warp (butterfly, the warp's blocks in order) -> CTA (warp order): one fixed
-// order set by H alone.  x_out = x_in + sum(pieces) (fp32 add) when pieces
-// are given.
+// residual + RMSNorm + quantisation.  A cluster of kNormSplit CTAs per row
+// (16 rows: rows >= M write zero activation blocks); warp w of cluster rank c
+// owns the 256-blocks b = c + kNormSplit*w and b = c + kNormSplit*(w + warps)
+// (H/256 <= 64).  The row's sum of squares is reduced lane -> warp
+// (butterfly, the warp's blocks in order); every warp sum is pushed into the
+// shared memory of every CTA of the cluster, and after one cluster barrier
+// each warp adds the kNormSplit*warps sums in a butterfly: one fixed order set
+// by H alone.  x_out = x_in + sum(pieces) (fp32 add) when pieces are given.
 // ---------------------------------------------------------------------------
+constexpr int kNormSplit = 4;
+
 __global__ void __launch_bounds__(1024)
 resid_norm_quant_kernel(const float* __restrict__ pieces, int pN, int pnb, long long pU, int pG,
                         const float* x_in, float* x_out,
                         const float* __restrict__ gamma, float eps, int M, int H, uint8_t* act,
                         float* __restrict__ xnorm_out, int32_t* status) {
-  __shared__ float warp_ss[32];
-  __shared__ float row_rinv;
-  const int row = blockIdx.x;
+  __shared__ float part_ss[64];
+  const int row = blockIdx.y;
+  const int c = kNormSplit > 1 ? (int)cluster_rank() : 0;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
   const int nb = H / 256;
   // gamma does not depend on the previous kernel: fetch it before waiting
   float gm[2][8];
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
-    const int b = warp + t * nw;
+    const int b = c + kNormSplit * (warp + t * nw);
     if (gamma && b < nb) {
       load8(gamma + 256 * b + 8 * lane, gm[t]);
     } else {
@@ -154,7 +158,7 @@ resid_norm_quant_kernel(const float* __restrict__ pieces, int pN, int pnb, long 
   float ss = 0.f;
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
-    const int b = warp + t * nw;
+    const int b = c + kNormSplit * (warp + t * nw);
     if (row < M && b < nb) {
       const int col0 = 256 * b + 8 * lane;
       load8(x_in + (size_t)row * H + col0, v[t]);
@@ -164,28 +168,40 @@ resid_norm_quant_kernel(const float* __restrict__ pieces, int pN, int pnb, long 
 #pragma unroll
         for (int i = 0; i < 8; ++i) v[t][i] = v[t][i] + ps[i];
       }
-      if (x_out && (pieces || x_out != x_in)) {
-        float4* o = reinterpret_cast<float4*>(x_out + (size_t)row * H + col0);
-        o[0] = make_float4(v[t][0], v[t][1], v[t][2], v[t][3]);
-        o[1] = make_float4(v[t][4], v[t][5], v[t][6], v[t][7]);
-      }
 #pragma unroll
       for (int i = 0; i < 8; ++i) ss += v[t][i] * v[t][i];
     }
   }
   ss = warp_sum(ss);
-  if (lane == 0) warp_ss[warp] = ss;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float total = 0.f;
-    for (int w = 0; w < nw; ++w) total += warp_ss[w];
-    row_rinv = 1.0f / sqrtf(total / (float)H + eps);
+  // warp sum -> slot c*nw + warp of every CTA of the cluster
+  if (lane < kNormSplit) {
+    if (kNormSplit > 1) {
+      st_cluster_f32(&part_ss[c * nw + warp], (uint32_t)lane, ss);
+    } else {
+      part_ss[warp] = ss;
+    }
   }
-  __syncthreads();
-  const float rinv = row_rinv;
+  // the residual stores go out while the partial sums travel
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
-    const int b = warp + t * nw;
+    const int b = c + kNormSplit * (warp + t * nw);
+    if (row < M && b < nb && x_out && (pieces || x_out != x_in)) {
+      float4* o = reinterpret_cast<float4*>(x_out + (size_t)row * H + 256 * b + 8 * lane);
+      o[0] = make_float4(v[t][0], v[t][1], v[t][2], v[t][3]);
+      o[1] = make_float4(v[t][4], v[t][5], v[t][6], v[t][7]);
+    }
+  }
+  if (kNormSplit > 1) {
+    cluster_sync_all();
+  } else {
+    __syncthreads();
+  }
+  const int np = kNormSplit * nw;
+  const float total = warp_sum((lane < np ? part_ss[lane] : 0.f) + (lane + 32 < np ? part_ss[lane + 32] : 0.f));
+  const float rinv = 1.0f / sqrtf(total / (float)H + eps);
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int b = c + kNormSplit * (warp + t * nw);
     if (b >= nb) continue;
     if (row < M) {
       const int col0 = 256 * b + 8 * lane;
@@ -208,10 +224,12 @@ cudaError_t launch_resid_norm_quant(const GemmPlan* p, const float* pieces, cons
                                     uint8_t* act, float* xnorm_out, int32_t* status,
                                     cudaStream_t st, bool pdl) {
   const int nb = H / 256;
-  const int warps = nb < 32 ? nb : 32;
-  if (nb > 2 * warps) return cudaErrorInvalidValue;
+  const int per = (nb + kNormSplit - 1) / kNormSplit;       // blocks per CTA
+  const int warps = per < 32 ? per : 32;
+  if (per > 2 * warps || kNormSplit * warps > 64) return cudaErrorInvalidValue;
   cudaLaunchAttribute attrs[2];
-  cudaLaunchConfig_t cfg = make_cfg(dim3(16), dim3(32 * warps), 0, st, pdl, attrs);
+  cudaLaunchConfig_t cfg = make_cfg(dim3(kNormSplit, 16), dim3(32 * warps), 0, st, pdl, attrs,
+                                    kNormSplit > 1 ? kNormSplit : 0);
   const int pN = p ? p->N : 0, pnb = p ? p->nb : 1, pG = p ? p->G : 1;
   const long long pU = p ? p->U : 1;
   return cudaLaunchKernelEx(&cfg, resid_norm_quant_kernel, pieces, pN, pnb, pU, pG, x_in, x_out,

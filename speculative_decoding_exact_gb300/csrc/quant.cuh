@@ -30,71 +30,91 @@ SPEC_DEV int act_off(int n, int s, int k) {
 SPEC_DEV int act_off8(int n, int j, int part, int k) {
   return 1024 * j + 512 * part + (n >> 3) * 256 + (k >> 4) * 128 + (n & 7) * 16 + (k & 15);
 }
-// e4m3 bits of an integer v with |v| <= 240 and at most 4 significant bits
-// (sign, 4-bit exponent with bias 7, 3-bit mantissa), read off its fp32 bits
-SPEC_DEV uint32_t e4m3_of_int(int v) {
-  if (v == 0) return 0u;
-  const uint32_t b = __float_as_uint((float)v);
-  const uint32_t e = ((b >> 23) & 255u) - 127u + 7u;
-  return ((b >> 24) & 0x80u) | (e << 3) | ((b >> 20) & 7u);
+// e4m3 bytes of two exact e4m3 values: lo in bits 0-7, hi in bits 8-15
+SPEC_DEV uint32_t e4m3x2(float lo, float hi) {
+  unsigned short r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
 }
 
 // Quantisation of one 256-block of one row, executed by one warp.  Lane l owns
 // elements 8l..8l+7 (sub-block l/4).
+//
+// q = rint(x/d_a) needs the IEEE quotient only where it decides the integer.
+// With r = RN(1/d_a) and y = RN(x*r), |y - x/d_a| <= 2^-23 |x/d_a| and
+// |RN(x/d_a) - x/d_a| <= 2^-24 |x/d_a|; for |x/d_a| <= 128 the two differ by
+// less than 2^-15.  So when y lies more than 2^-12 away from every
+// half-integer, rint(y) = rint(RN(x/d_a)); a lane with an element closer than
+// that (or a block with a non-finite element, or d_a outside
+// [2^-125, FLT_MAX]) takes the IEEE division for all its elements.  Codes,
+// their 16h + l split and the sub-block sums are carried as exact floats.
 __device__ __forceinline__ void quant_block_warp(const float (&v)[8], int row, int b, int K, uint8_t* act,
                                                  int8_t* q_dbg, float* da_dbg, int32_t* A_dbg,
                                                  int32_t* status) {
   const int lane = threadIdx.x & 31;
   float amax = 0.f;
-  bool bad = false;
+  bool ok = true;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    bad |= !isfinite(v[i]);
+    ok = ok && fabsf(v[i]) <= 3.40282347e38f;          // false for inf and NaN
     amax = fmaxf(amax, fabsf(v[i]));
   }
+  if (!ok) atomicOr(status, SPEC_ST_NONFINITE);
+  const bool all_ok = __all_sync(0xffffffffu, ok);
   amax = warp_max(amax);
-  if (bad) atomicOr(status, SPEC_ST_NONFINITE);
   const float d = amax / 127.0f;
-  int q[8];
+  const bool exact = !all_ok || !(d == 0.f || (d >= 0x1p-125f && d <= 3.40282347e38f));
+  const float r = (exact || d == 0.f) ? 0.f : __frcp_rn(d);
+  float q[8];
+  bool near = exact;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    int c = 0;
-    if (d != 0.f && isfinite(v[i])) {
-      float r = rintf(v[i] / d);
-      r = fminf(fmaxf(r, -127.f), 127.f);
-      c = (int)r;
-    }
-    q[i] = c;
+    const float y = v[i] * r;
+    q[i] = rintf(y);
+    near = near || fabsf(fabsf(y - q[i]) - 0.5f) < 0x1p-12f;
   }
-  int part = 0;
+  if (near) {
 #pragma unroll
-  for (int i = 0; i < 8; ++i) part += q[i];
+    for (int i = 0; i < 8; ++i) q[i] = (d != 0.f && fabsf(v[i]) <= 3.40282347e38f) ? rintf(v[i] / d) : 0.f;
+  }
+  float part = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    q[i] = fminf(fmaxf(q[i], -127.f), 127.f) + 0.f;     // + 0 turns -0 into +0
+    part += q[i];
+  }
   part += __shfl_xor_sync(0xffffffffu, part, 1);
   part += __shfl_xor_sync(0xffffffffu, part, 2);   // A_j for j = lane/4 (all 4 lanes of the quad)
 
   uint8_t* sb = act + (size_t)b * kActSBBytes;
-  // codes: elements 8*lane + i = code k = 8*(lane%4) + i of sub-block lane/4
+  // codes: elements 8*lane + i = code k = 8*(lane%4) + i of sub-block lane/4;
+  // q = 16h + l with h = floor(q/16)
   const int j = lane >> 2, q4 = lane & 3;
-  uint32_t hw[2] = {0u, 0u}, lw[2] = {0u, 0u};
+  float hv[8], lv[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const int l = q[i] & 15, h = q[i] >> 4;     // q = 16h + l (arithmetic shift: floor)
-    hw[i >> 2] |= e4m3_of_int(16 * h) << (8 * (i & 3));
-    lw[i >> 2] |= e4m3_of_int(l) << (8 * (i & 3));
+    hv[i] = 16.f * floorf(q[i] * 0.0625f);
+    lv[i] = q[i] - hv[i];
+  }
+  uint32_t hw[2], lw[2];
+#pragma unroll
+  for (int w = 0; w < 2; ++w) {
+    hw[w] = e4m3x2(hv[4 * w], hv[4 * w + 1]) | (e4m3x2(hv[4 * w + 2], hv[4 * w + 3]) << 16);
+    lw[w] = e4m3x2(lv[4 * w], lv[4 * w + 1]) | (e4m3x2(lv[4 * w + 2], lv[4 * w + 3]) << 16);
   }
   *reinterpret_cast<uint2*>(sb + act_off8(row, j, 0, 8 * q4)) = make_uint2(hw[0], hw[1]);
   *reinterpret_cast<uint2*>(sb + act_off8(row, j, 1, 8 * q4)) = make_uint2(lw[0], lw[1]);
   // min-term block: lane 4j writes 64*hi_j and lo_j of sub-block j
   if (q4 == 0) {
-    const int hh = part >> 6, ll = part & 63;
-    *reinterpret_cast<unsigned short*>(sb + act_off(row, 16, j)) = __half_as_ushort(__int2half_rn(64 * hh));
-    *reinterpret_cast<unsigned short*>(sb + act_off(row, 16, 8 + j)) = __half_as_ushort(__int2half_rn(ll));
+    const float hh = 64.f * floorf(part * 0.015625f), ll = part - hh;
+    *reinterpret_cast<unsigned short*>(sb + act_off(row, 16, j)) = __half_as_ushort(__float2half_rn(hh));
+    *reinterpret_cast<unsigned short*>(sb + act_off(row, 16, 8 + j)) = __half_as_ushort(__float2half_rn(ll));
   }
   if (lane == 0) reinterpret_cast<float*>(sb + kActSlots * 512)[row] = d;
   if (q_dbg) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) q_dbg[(size_t)row * K + 256 * b + 8 * lane + i] = (int8_t)q[i];
-    if ((lane & 3) == 0) A_dbg[(size_t)row * (K / 32) + 8 * b + (lane >> 2)] = part;
+    for (int i = 0; i < 8; ++i) q_dbg[(size_t)row * K + 256 * b + 8 * lane + i] = (int8_t)(int)q[i];
+    if ((lane & 3) == 0) A_dbg[(size_t)row * (K / 32) + 8 * b + (lane >> 2)] = (int)part;
     if (lane == 0) da_dbg[(size_t)row * (K / 256) + b] = d;
   }
 }

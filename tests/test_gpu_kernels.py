@@ -61,6 +61,38 @@ def test_quantize_bit_exact(ctx, M, K):
     assert np.array_equal(A.cpu().numpy(), oA)
 
 
+def test_quantize_ties_bit_exact(ctx):
+    # quotients x/d_a on or within an ulp of a half-integer: the codes follow
+    # the IEEE quotient with round-half-even (d_a = 1 blocks give exact ties)
+    rng = np.random.default_rng(17)
+    M, K = 4, 2048
+    x = np.zeros((M, K), dtype=np.float32)
+    for m in range(M):
+        for b in range(K // 256):
+            amax = np.float32(127.0) if (m + b) % 2 == 0 else np.float32(rng.uniform(0.05, 40.0))
+            d = np.float32(amax / np.float32(127.0))
+            n = rng.integers(-127, 127, 256).astype(np.float32)
+            blk = ((n + np.float32(0.5)) * d).astype(np.float32)
+            step = rng.integers(-1, 2, 256)
+            blk = np.where(step > 0, np.nextafter(blk, np.float32(np.inf)),
+                           np.where(step < 0, np.nextafter(blk, np.float32(-np.inf)), blk)).astype(np.float32)
+            blk = np.clip(blk, -amax, amax)
+            blk[0] = amax
+            x[m, 256 * b:256 * (b + 1)] = blk
+    q = torch.zeros((M, K), dtype=torch.int8, device="cuda")
+    da = torch.zeros((M, K // 256), dtype=torch.float32, device="cuda")
+    A = torch.zeros((M, K // 32), dtype=torch.int32, device="cuda")
+    xd = dev(x)
+    abi.check("spec_quantize_q8", abi.spec_quantize_q8(ctx.h, xd.data_ptr(), M, K, q.data_ptr(),
+                                                       da.data_ptr(), A.data_ptr()))
+    sync()
+    oq, oda, oA, st = oracle.quantize_q8(x)
+    assert st == 0
+    assert np.array_equal(da.cpu().numpy().view(np.uint32), oda.view(np.uint32))
+    assert np.array_equal(q.cpu().numpy(), oq)
+    assert np.array_equal(A.cpu().numpy(), oA)
+
+
 def test_quantize_flags_nonfinite(ctx):
     x = synth.normal((2, 512), 0, 5)
     x[1, 300] = np.nan

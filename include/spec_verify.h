@@ -100,7 +100,7 @@ extern "C" {
 #define SPEC_ST_POOL_EMPTY    0x4  /* not enough free KV pages for the block     */
 #define SPEC_ST_ROLLBACK      0x8  /* rollback length < 0 or > seq_len           */
 #define SPEC_ST_CTX_FULL      0x10 /* seq_len + rows exceeds the page table      */
-#define SPEC_ST_DEVICE_WAIT   0x20 /* a bounded wait for the tensor core gave up  */
+#define SPEC_ST_DEVICE_WAIT   0x20 /* a bounded device wait (tensor core, bulk copy) gave up */
 
 /* Model geometry and workspace sizing.  H = n_q_heads*head_dim; H and ffn are
  * multiples of 256; n_q_heads is a multiple of n_kv_heads; head_dim = 128;

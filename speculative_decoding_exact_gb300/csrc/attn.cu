@@ -21,6 +21,8 @@
 // Precision: K and V are exact bf16; q and p are split into bf16 hi + lo parts
 // (two MMAs each) so the products carry ~16 significant bits; accumulation is
 // fp32.
+#include <cuda.h>
+
 #include "common.cuh"
 #include "internal.h"
 #include "quant.cuh"
@@ -28,7 +30,6 @@
 namespace spec {
 
 constexpr int kChunk = 64;
-constexpr int kRowPad = 136;         // bf16 per padded K/V row in shared memory (272 B)
 constexpr int kMaxGroup = 13;        // max query heads per kv head
 
 constexpr int kTargetChunks = 48;    // chunks per context at most (about)
@@ -45,7 +46,56 @@ AttnPlan make_attn_plan(int nq, int nkv, int dh, int max_ctx) {
   a.max_chunks = (max_ctx + a.chunk - 1) / a.chunk;
   return a;
 }
-size_t attn_smem_bytes() { return (size_t)2 * 2 * kChunk * kRowPad * sizeof(__nv_bfloat16); }
+// Shared memory of the partial kernel: a double buffer of K and V sub-chunks,
+// each [d half (2)][64 keys][128 bytes] with the 16-byte chunks of a row
+// permuted by the 128-byte swizzle of the tensor copies (chunk j of row r at
+// j ^ (r % 8)), then the chunk's page ids (16 keys per page).  1 KB of slack
+// aligns the buffers to the 1 KB swizzle period.
+constexpr int kHalfBytes = kChunk * 128;              // one d half of a K or V sub-chunk
+constexpr int kKvBufBytes = 2 * 2 * kHalfBytes;       // K and V of one buffer
+constexpr size_t kKvSmemBytes = 1024 + 2 * (size_t)kKvBufBytes;
+size_t attn_smem_bytes(int chunk) { return kKvSmemBytes + sizeof(int) * (size_t)(chunk / 16); }
+
+// byte offset of 16-byte chunk j (0..7) of row r in a swizzled [rows][128 B] half
+SPEC_DEV uint32_t swz(int r, int j) { return (uint32_t)(r * 128 + ((j ^ (r & 7)) << 4)); }
+
+// 2-D tensor copy global -> shared: box at (x, y) of the map, completion on mbar
+SPEC_DEV void tma_load_2d(void* dst_smem, const CUtensorMap* map, int x, int y, uint64_t* mbar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];\n" ::"r"(
+          smem_u32(dst_smem)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(mbar))
+      : "memory");
+}
+
+// The KV pool [num_pages][n_layers][K, V][n_kv][16 positions][128] bf16 seen as
+// one 2-D tensor of 256-byte rows (row = ((page*n_layers + layer)*2 + kv)*n_kv
+// + head, times 16, plus the position in the page); boxes of 16 rows x 64
+// values (one d half of one page), 128-byte swizzle.
+static cudaError_t make_kv_tmap(const KvView& kv, CUtensorMap* map) {
+  using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+  static EncodeFn encode = nullptr;
+  if (!encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess) return e;
+    if (q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
+    encode = reinterpret_cast<EncodeFn>(fn);
+  }
+  const unsigned long long rows = (unsigned long long)kv.num_pages * kv.n_layers * 2 * kv.n_kv * 16;
+  if (rows == 0 || rows >= (1ull << 31)) return cudaErrorInvalidValue;   // y coordinates are int32
+  const cuuint64_t dims[2] = {128, rows};
+  const cuuint64_t strides[1] = {256};
+  const cuuint32_t box[2] = {64, 16};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kv.pool, dims, strides, box, estr,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
 
 size_t attn_partial_floats(const AttnPlan& a, int max_rows) {
   (void)max_rows;
@@ -67,11 +117,18 @@ SPEC_DEV uint32_t pack_bf16(float lo, float hi) {
   return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(lo)) |
          ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(hi)) << 16);
 }
-// split x into bf16 hi + bf16 lo (x - hi), packed pairs
+// split x into bf16 hi + bf16 lo (x - hi), packed pairs (x0 in the low half)
 SPEC_DEV void split2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
-  const __nv_bfloat16 h0 = __float2bfloat16_rn(x0), h1 = __float2bfloat16_rn(x1);
-  hi = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
-  lo = pack_bf16(x0 - __bfloat162float(h0), x1 - __bfloat162float(h1));
+  const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+  const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - __low2float(h), x1 - __high2float(h));
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+// 2^x (PTX ex2.approx: relative error about 2^-22; 2^-inf = 0)
+SPEC_DEV float exp2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
 }
 
 // dh is fixed to 128 (8 k-steps of 16 for q.k, 16 n-tiles of 8 for p.v).
@@ -122,10 +179,14 @@ SPEC_DEV uint4 ldg_frag(const uint4* p) {
 template <bool MULTI>
 __global__ void __launch_bounds__(warps_per_cta(MULTI) * 32, 2)
 attn_partial_kernel(const uint4* __restrict__ qf, int M, int nq, int nkv, int chunk_keys, KvView kv,
-                    int layer, float* __restrict__ part, const int32_t* status) {
+                    const __grid_constant__ CUtensorMap kvmap, int layer, float* __restrict__ part,
+                    int32_t* status) {
   constexpr int kHeadSplit = head_split(MULTI);
-  // [buffer][K, V][64 keys][padded 136 bf16]
-  extern __shared__ __align__(128) __nv_bfloat16 kvs[];
+  extern __shared__ __align__(128) uint8_t dsm[];
+  uint8_t* kvs = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm) + 1023) & ~(uintptr_t)1023);
+  int* pg = reinterpret_cast<int*>(dsm + kKvSmemBytes);
+  __shared__ __align__(8) uint64_t kvbar[2];     // K/V of buffer b landed (bulk copies)
+  __shared__ int copy_ok;
 
   pdl_trigger();
   pdl_wait();
@@ -134,41 +195,81 @@ attn_partial_kernel(const uint4* __restrict__ qf, int M, int nq, int nkv, int ch
   const int per = (group + kHeadSplit - 1) / kHeadSplit;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
-  if (*status & (SPEC_ST_TOKEN_RANGE | SPEC_ST_POOL_EMPTY | SPEC_ST_CTX_FULL)) return;
-  const int len = *kv.seq_len;             // block appended: n_past + M
-  const int n_past = len - M;
   const int key0 = chunk * chunk_keys;
+  // status, length and the chunk's page ids in one round of loads
+  const int32_t st = *status;
+  const int len = *kv.seq_len;             // block appended: n_past + M
+  for (int i = threadIdx.x; i < chunk_keys / 16; i += blockDim.x) {
+    const int lp = key0 / 16 + i;
+    pg[i] = lp < kv.max_seq_pages ? kv.page_table[lp] : -1;
+  }
+  if (threadIdx.x == 0) {
+    mbar_init(&kvbar[0], 1);
+    mbar_init(&kvbar[1], 1);
+    fence_mbarrier_init();
+  }
+  __syncthreads();
+  if (st & (SPEC_ST_TOKEN_RANGE | SPEC_ST_POOL_EMPTY | SPEC_ST_CTX_FULL)) return;
+  const int n_past = len - M;
   if (key0 >= len) return;
   // sub-chunks with keys (exactly one when the chunk is one sub-chunk long)
   const int nsub = MULTI ? min(chunk_keys, len - key0 + kChunk - 1) / kChunk : 1;
 
-  // ---- K, V sub-chunk sc -> shared buffer sc % 2 (rows beyond len are zero)
+  // ---- K, V sub-chunk sc -> shared buffer sc % 2: lanes 0..15 of warp 0 each
+  // copy one d half of the K or V rows of one page (16 keys) with a tensor
+  // copy; lane 0 arms the buffer's barrier with the bytes of the pages copied.
+  // Pages past len or with an out-of-range id are not copied; their rows, and
+  // the rows at or past len in a copied page, are zeroed once the copies have
+  // landed (fix_sub).
+  auto page_of = [&](int pos0) -> int {
+    const int page = pos0 < len ? pg[(pos0 - key0) >> 4] : -1;
+    return (page >= 0 && page < kv.num_pages) ? page : -1;
+  };
   auto load_sub = [&](int sc) {
-    __nv_bfloat16* buf = kvs + (size_t)(sc & 1) * 2 * kChunk * kRowPad;
+    if (warp != 0) return;
+    uint8_t* buf = kvs + (size_t)(sc & 1) * kKvBufBytes;
+    uint64_t* bar = &kvbar[sc & 1];
     const int ks0 = key0 + sc * kChunk;
-    for (int i = threadIdx.x; i < 2 * kChunk * 16; i += blockDim.x) {
-      const int which = i / (kChunk * 16), r = (i / 16) % kChunk, c16 = i % 16;
-      __nv_bfloat16* dst = buf + which * kChunk * kRowPad + r * kRowPad + c16 * 8;
-      const int pos = ks0 + r;
-      const int lp = pos / kv.page_size;
-      const int page = (pos < len && lp < kv.max_seq_pages) ? kv.page_table[lp] : -1;
-      if (page >= 0 && page < kv.num_pages) {
-        const size_t off = ((((size_t)page * kv.n_layers + layer) * 2 + which) * kv.n_kv + kvh) *
-                               (size_t)kv.page_size * kv.head_dim +
-                           (size_t)(pos % kv.page_size) * kv.head_dim + c16 * 8;
-        cp_async16(dst, kv.pool + off);
-      } else {
-        *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
-      }
+    const int pp = (lane >> 2) & 3, which = (lane >> 1) & 1, half = lane & 1;
+    const int page = page_of(ks0 + 16 * pp);
+    const bool go = lane < 16 && page >= 0;
+    const uint32_t ops = __popc(__ballot_sync(0xffffffffu, go));
+    if (lane == 0) mbar_arrive_expect_tx(bar, ops * 2048u);
+    if (go) {
+      const int y = (((page * kv.n_layers + layer) * 2 + which) * kv.n_kv + kvh) * 16;
+      tma_load_2d(buf + which * 2 * kHalfBytes + half * kHalfBytes + pp * 2048, &kvmap, 64 * half, y, bar);
     }
-    cp_async_commit();
+  };
+  // rows of sub-chunk sc that must read as zero: keys at or past len, keys of a
+  // page with an out-of-range id (CTA-uniform)
+  auto sub_needs_fix = [&](int sc) -> bool {
+    const int ks0 = key0 + sc * kChunk;
+    if (ks0 + kChunk > len) return true;
+#pragma unroll
+    for (int pp = 0; pp < kChunk / 16; ++pp)
+      if (page_of(ks0 + 16 * pp) < 0) return true;
+    return false;
+  };
+  auto fix_sub = [&](int sc) {
+    uint8_t* buf = kvs + (size_t)(sc & 1) * kKvBufBytes;
+    const int ks0 = key0 + sc * kChunk;
+    for (int i = threadIdx.x; i < kChunk * 4; i += blockDim.x) {     // (row, K/V, half)
+      const int r = i >> 2, which = (i >> 1) & 1, half = i & 1;
+      const int pos = ks0 + r;
+      if (pos < len && page_of(ks0 + 16 * (r >> 4)) >= 0) continue;
+      uint4* row = reinterpret_cast<uint4*>(buf + which * 2 * kHalfBytes + half * kHalfBytes + r * 128);
+#pragma unroll
+      for (int c16 = 0; c16 < 8; ++c16) row[c16] = make_uint4(0, 0, 0, 0);
+    }
+    fence_proxy_async();      // ordered before the tensor copies that later refill the buffer
   };
 
   const int hl = blockIdx.z * per + warp;          // head within the kv group
   const bool active = warp < per && hl < group;
   const int head = kvh * group + (active ? hl : 0);
   const uint4* Qf = qf + (size_t)head * 8 * 2 * 32;   // [8 ksteps][hi, lo][32 lanes]
-  const float scale = 1.0f / sqrtf(128.0f);
+  // scores in base-2 units: u = (q.k / sqrt(128)) * log2(e), p = 2^(u - max)
+  const float c2 = 1.4426950408889634f / sqrtf(128.0f);
 
   // running per-row state (rows g and g+8): max, sum, unnormalised o
   float mrun[2] = {-INFINITY, -INFINITY}, lrun[2] = {0.f, 0.f};
@@ -180,15 +281,24 @@ attn_partial_kernel(const uint4* __restrict__ qf, int M, int nq, int nkv, int ch
 
   load_sub(0);
   for (int sc = 0; sc < nsub; ++sc) {
-    if (sc + 1 < nsub) {
-      load_sub(sc + 1);
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
-    }
+    if (sc + 1 < nsub) load_sub(sc + 1);
+    // one thread waits (bounded) for the buffer; the CTA barrier passes the
+    // result and the landed rows to all threads
+    if (threadIdx.x == 0) copy_ok = mbar_wait_ns(&kvbar[sc & 1], (sc >> 1) & 1, 2000000000ull) ? 1 : 0;
     __syncthreads();
-    const __nv_bfloat16* Ks = kvs + (size_t)(sc & 1) * 2 * kChunk * kRowPad;
-    const __nv_bfloat16* Vs = Ks + kChunk * kRowPad;
+    if (!copy_ok) {
+      if (threadIdx.x == 0) {          // flag it; let the other buffer's copies land (bounded)
+        atomicOr(status, SPEC_ST_DEVICE_WAIT);
+        if (sc + 1 < nsub) mbar_wait_ns(&kvbar[(sc + 1) & 1], ((sc + 1) >> 1) & 1, 2000000000ull);
+      }
+      return;
+    }
+    if (sub_needs_fix(sc)) {
+      fix_sub(sc);
+      __syncthreads();
+    }
+    const uint8_t* Ks = kvs + (size_t)(sc & 1) * kKvBufBytes;
+    const uint8_t* Vs = Ks + 2 * kHalfBytes;
     const int ks0 = key0 + sc * kChunk;
     if (active) {
       // ---- scores S = q.k for 64 keys: 8 n-tiles x 4
@@ -206,9 +316,8 @@ attn_partial_kernel(const uint4* __restrict__ qf, int M, int nq, int nkv, int ch
 #pragma unroll
         for (int nt = 0; nt < 8; ++nt) {
           uint32_t b0, b1, b2, b3;
-          const int krow = 8 * nt + (lane & 7);
-          const int kcol = 32 * kp + 8 * (lane >> 3);
-          ldsm_x4(b0, b1, b2, b3, Ks + krow * kRowPad + kcol);
+          const int krow = 8 * nt + (lane & 7);   // d = 32 kp + 8 (lane / 8): half kp / 2
+          ldsm_x4(b0, b1, b2, b3, Ks + (kp >> 1) * kHalfBytes + swz(krow, 4 * (kp & 1) + (lane >> 3)));
           mma16816_bf16(s[nt], qh0.x, qh0.y, qh0.z, qh0.w, b0, b1);
           mma16816_bf16(s[nt], ql0.x, ql0.y, ql0.z, ql0.w, b0, b1);
           mma16816_bf16(s[nt], qh1.x, qh1.y, qh1.z, qh1.w, b2, b3);
@@ -216,35 +325,49 @@ attn_partial_kernel(const uint4* __restrict__ qf, int M, int nq, int nkv, int ch
         }
       }
 
-      // ---- mask, running max, p = exp(s - max), rescale of the running state
+      // ---- mask, running max, p = 2^(u - max), rescale of the running state.
+      // A sub-chunk whose keys all precede the block is visible to every row.
+      const bool full = ks0 + kChunk - 1 <= n_past;
       float mx[2] = {-INFINITY, -INFINITY};
+      if (full) {
 #pragma unroll
-      for (int nt = 0; nt < 8; ++nt)
+        for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int row = g + 8 * (e >> 1);
-          const int key = ks0 + 8 * nt + 2 * t + (e & 1);
-          const bool vis = row < M && key <= n_past + row;
-          const float v = vis ? s[nt][e] * scale : -INFINITY;
-          s[nt][e] = v;
-          mx[e >> 1] = fmaxf(mx[e >> 1], v);
-        }
-      float alpha[2];
+          for (int e = 0; e < 4; ++e) {
+            s[nt][e] *= c2;
+            mx[e >> 1] = fmaxf(mx[e >> 1], s[nt][e]);
+          }
+      } else {
+        // key ks0 + 8nt + 2t + (e&1) is visible to row g + 8(e>>1) < M when
+        // 8nt + (e&1) <= n_past + row - ks0 - 2t
+        int lim[2];
+#pragma unroll
+        for (int r = 0; r < 2; ++r) lim[r] = (g + 8 * r < M) ? n_past + g + 8 * r - ks0 - 2 * t : -1;
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float v = (8 * nt + (e & 1) <= lim[e >> 1]) ? s[nt][e] * c2 : -INFINITY;
+            s[nt][e] = v;
+            mx[e >> 1] = fmaxf(mx[e >> 1], v);
+          }
+      }
+      float alpha[2], mbase[2];
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
         mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
         mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
         const float mnew = fmaxf(mrun[r], mx[r]);
-        alpha[r] = (mrun[r] == -INFINITY) ? 0.f : expf(mrun[r] - mnew);
+        alpha[r] = (mrun[r] == -INFINITY) ? 0.f : exp2_approx(mrun[r] - mnew);
         mrun[r] = mnew;
+        mbase[r] = mnew == -INFINITY ? 0.f : mnew;    // a row with no visible key yet: p = 2^-inf = 0
       }
       float sum[2] = {0.f, 0.f};
 #pragma unroll
       for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const float m = mrun[e >> 1];
-          const float p = (s[nt][e] == -INFINITY) ? 0.f : expf(s[nt][e] - m);
+          const float p = exp2_approx(s[nt][e] - mbase[e >> 1]);
           s[nt][e] = p;
           sum[e >> 1] += p;
         }
@@ -254,10 +377,12 @@ attn_partial_kernel(const uint4* __restrict__ qf, int M, int nq, int nkv, int ch
         sum[r] += __shfl_xor_sync(0xffffffffu, sum[r], 2);
         lrun[r] = lrun[r] * alpha[r] + sum[r];
       }
+      if (sc > 0) {
 #pragma unroll
-      for (int nd = 0; nd < 16; ++nd)
+        for (int nd = 0; nd < 16; ++nd)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) o[nd][e] *= alpha[e >> 1];
+          for (int e = 0; e < 4; ++e) o[nd][e] *= alpha[e >> 1];
+      }
 
       // ---- o += p.v : 16 n-tiles of 8 dims
 #pragma unroll
@@ -270,9 +395,8 @@ attn_partial_kernel(const uint4* __restrict__ qf, int M, int nq, int nkv, int ch
 #pragma unroll
         for (int np = 0; np < 8; ++np) {          // pairs of dim tiles
           uint32_t b0, b1, b2, b3;
-          const int vrow = 16 * kk + (lane & 7) + 8 * ((lane >> 3) & 1);
-          const int vcol = 16 * np + 8 * (lane >> 4);
-          ldsm_x4_t(b0, b1, b2, b3, Vs + vrow * kRowPad + vcol);
+          const int vrow = 16 * kk + (lane & 7) + 8 * ((lane >> 3) & 1);   // d = 16 np + 8 (lane / 16)
+          ldsm_x4_t(b0, b1, b2, b3, Vs + (np >> 2) * kHalfBytes + swz(vrow, 2 * (np & 3) + (lane >> 4)));
           mma16816_bf16(o[2 * np], ph[0], ph[1], ph[2], ph[3], b0, b1);
           mma16816_bf16(o[2 * np], pl[0], pl[1], pl[2], pl[3], b0, b1);
           mma16816_bf16(o[2 * np + 1], ph[0], ph[1], ph[2], ph[3], b2, b3);
@@ -280,11 +404,11 @@ attn_partial_kernel(const uint4* __restrict__ qf, int M, int nq, int nkv, int ch
         }
       }
     }
-    __syncthreads();            // the next prefetch overwrites this buffer
+    if (sc + 1 < nsub) __syncthreads();     // the next prefetch overwrites this buffer
   }
   if (!active) return;
 
-  // ---- partials: [chunk][head][row][128 o | max | sum]
+  // ---- partials: [chunk][head][row][128 o | max (base-2 units) | sum]
   const int stride = 130;
 #pragma unroll
   for (int r = 0; r < 2; ++r) {
@@ -303,7 +427,8 @@ attn_partial_kernel(const uint4* __restrict__ qf, int M, int nq, int nkv, int ch
 
 // merge: grid (nq*128/256 blocks, 16 rows), 256 threads = 2 heads x 128 dims.
 // For row i the chunks 0 .. (n_past+i)/C are combined:
-//   M = max_c m_c;  w_c = exp(m_c - M);  L = sum_c w_c l_c;  o = sum_c w_c o_c;
+//   M = max_c m_c;  w_c = 2^(m_c - M) (maxima in base-2 units);  L = sum_c w_c l_c;
+//   o = sum_c w_c o_c;
 // out = o / L.  Warp hh (one per head) computes M, the weights and L with
 // warp shuffles in a fixed butterfly order; o is summed in chunk order.  The
 // chunk count depends on the row's position only, so the result is the same
@@ -341,7 +466,7 @@ attn_merge_kernel(const float* __restrict__ part, int M, int nq, int max_chunks,
     float L = 0.f;
     for (int c = lane; c < nchunks; c += 32) {
       const float mc = msh[hh * max_chunks + c];
-      const float w = (mc == -INFINITY) ? 0.f : expf(mc - m);
+      const float w = (mc == -INFINITY) ? 0.f : exp2f(mc - m);
       msh[hh * max_chunks + c] = w;
       L += w * lsh[hh * max_chunks + c];
     }
@@ -386,23 +511,26 @@ cudaError_t launch_attention(const AttnPlan& a, const KvView& kv, int layer, con
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
+  alignas(64) CUtensorMap kvmap;
+  cudaError_t em = make_kv_tmap(kv, &kvmap);
+  if (em != cudaSuccess) return em;
   const bool multi = a.chunk > kChunk;
   auto kern = multi ? attn_partial_kernel<true> : attn_partial_kernel<false>;
-  static bool smem_attr[2] = {false, false};
-  if (!smem_attr[multi]) {
-    cudaError_t ea = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          (int)attn_smem_bytes());
+  const size_t smem = attn_smem_bytes(a.chunk);
+  static size_t smem_attr[2] = {0, 0};
+  if (smem_attr[multi] < smem) {
+    cudaError_t ea = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (ea != cudaSuccess) return ea;
-    smem_attr[multi] = true;
+    smem_attr[multi] = smem;
   }
   cfg.gridDim = dim3(a.max_chunks, a.nkv, head_split(multi));
   cfg.blockDim = dim3(32 * warps_per_cta(multi));
-  cfg.dynamicSmemBytes = attn_smem_bytes();
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
   cudaError_t e = cudaLaunchKernelEx(&cfg, kern, reinterpret_cast<const uint4*>(qfrag),
-                                     M, a.nq, a.nkv, a.chunk, kv, layer, part, (const int32_t*)status);
+                                     M, a.nq, a.nkv, a.chunk, kv, kvmap, layer, part, status);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg2 = {};
   cfg2.gridDim = dim3(a.nq * 128 / 256, 16);

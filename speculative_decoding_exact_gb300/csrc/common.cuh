@@ -256,6 +256,14 @@ SPEC_DEV void bulk_g2s(void* dst_smem, const void* src, uint32_t bytes, uint64_t
       "l"(src), "r"(bytes), "r"(smem_u32(mbar)), "l"(policy)
       : "memory");
 }
+// the same without an L2 cache hint
+SPEC_DEV void bulk_g2s(void* dst_smem, const void* src, uint32_t bytes, uint64_t* mbar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+                   smem_u32(dst_smem)),
+               "l"(src), "r"(bytes), "r"(smem_u32(mbar))
+               : "memory");
+}
+SPEC_DEV void fence_mbarrier_init() { asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory"); }
 SPEC_DEV uint64_t l2_policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(p));

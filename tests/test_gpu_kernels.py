@@ -155,6 +155,26 @@ def test_gemm_full_width_sampled(ctx, N):
     assert_close(y[:, cols], oy, what="y sampled")
 
 
+@pytest.mark.parametrize("M", [2, 5, 13, 16])
+def test_gemm_fc_front_projection_sampled(ctx, M):
+    """Draft front projection shape (5 concatenated hidden rows: K = 33280,
+    N = 6656) at M = accepted + 1 rows and at M = 16: exact integer sums and
+    fp32 outputs on a sample of columns (an exact sub-problem of the oracle)."""
+    N, K = 6656, 33280
+    W = synth.q4k_matrix(N, K, 8, M)
+    x = synth.normal((M, K), 8, 17 + M)
+    Wt = runtime.upload_tiled(ctx, W, N, K)
+    y, isc, imn = run_gemm(ctx, Wt, N, K, x, sums=True)
+    rng = np.random.default_rng(M)
+    cols = np.sort(np.concatenate([rng.choice(N, 96, replace=False), [0, 127, 128, N - 1]]))
+    Wsub = W.reshape(N, -1)[cols].reshape(-1)
+    q, da, A, _ = oracle.quantize_q8(x)
+    oy, oisc, oimn, _ = oracle.gemm_q4k(Wsub, len(cols), K, q, da, A, sums=True)
+    assert np.array_equal(isc[:, cols], oisc), "ISc differs"
+    assert np.array_equal(imn[:, cols], oimn), "IMn differs"
+    assert_close(y[:, cols], oy, what="y sampled")
+
+
 def test_gemm_batch_height_invariance(ctx):
     N, K = 4096, 6656
     W = synth.q4k_matrix(N, K, 6, 1)

@@ -30,7 +30,7 @@ struct spec_ctx {
   uint8_t* act = nullptr;
   float* pieces = nullptr;
   float* resid = nullptr;        // [16][H]
-  uint8_t* qfrag = nullptr;      // attention query fragments, nq * 8 KB
+  uint8_t* qtile = nullptr;      // attention query tiles, 64 KB per (kv head, tile)
   float* attn_part = nullptr;
   float* head_val = nullptr;     // [nparts][16]
   int32_t* head_idx = nullptr;
@@ -178,7 +178,7 @@ int spec_verify_init(const spec_config* cfg, void* cuda_stream, spec_ctx** out) 
   rc |= dalloc(&c->act, c->act_bytes);
   rc |= dalloc(&c->pieces, c->pieces_floats);
   rc |= dalloc(&c->resid, (size_t)16 * H);
-  rc |= dalloc(&c->qfrag, qfrag_bytes(cfg->n_q_heads));
+  rc |= dalloc(&c->qtile, qtile_bytes(c->attn));
   rc |= dalloc(&c->attn_part, attn_partial_floats(c->attn, 16));
   rc |= dalloc(&c->head_val, (size_t)c->head_parts * 16);
   rc |= dalloc(&c->head_idx, (size_t)c->head_parts * 16);
@@ -198,6 +198,7 @@ int spec_verify_init(const spec_config* cfg, void* cuda_stream, spec_ctx** out) 
   }
   if (cudaMemsetAsync(c->status, 0, 16, c->stream) != cudaSuccess ||
       cudaMemsetAsync(c->act, 0, c->act_bytes, c->stream) != cudaSuccess ||
+      cudaMemsetAsync(c->qtile, 0, qtile_bytes(c->attn), c->stream) != cudaSuccess ||
       cudaStreamSynchronize(c->stream) != cudaSuccess) {
     spec_verify_destroy(c);
     return SPEC_ECUDA;
@@ -214,7 +215,7 @@ void spec_verify_destroy(spec_ctx* c) {
   cudaFree(c->act);
   cudaFree(c->pieces);
   cudaFree(c->resid);
-  cudaFree(c->qfrag);
+  cudaFree(c->qtile);
   for (auto& gc : c->graphs)
     if (gc.exec) cudaGraphExecDestroy(gc.exec);
   cudaFree(c->attn_part);
@@ -346,8 +347,8 @@ int spec_attention(spec_ctx* c, const spec_kv* kv, int layer, const float* q, in
     return SPEC_ECAPACITY;   // attention workspace must cover every position the cache can hold
   if (!aligned(q) || !aligned(out)) return SPEC_EALIGN;
   SPEC_TRY(cudaMemsetAsync(c->status, 0, 4, c->stream));
-  SPEC_TRY(launch_q_to_frag(q, M, c->cfg.n_q_heads, c->qfrag, c->stream, false));
-  SPEC_TRY(launch_attention(c->attn, view_of(c, kv), layer, c->qfrag, M, c->attn_part, out, nullptr,
+  SPEC_TRY(launch_q_to_tile(q, M, c->attn, c->qtile, c->stream, false));
+  SPEC_TRY(launch_attention(c->attn, view_of(c, kv), layer, c->qtile, M, c->attn_part, out, nullptr,
                             c->status, c->stream, false));
   return SPEC_OK;
 }
@@ -444,8 +445,8 @@ static int enqueue_step(spec_ctx* c, const spec_weights* w, spec_kv* kv, const f
   for (int l = 0; l < g.n_layers; ++l) {
     SPEC_TRY(gemm(c->p_qkv, w->w_qkv[l])); ++n;
     SPEC_TRY(launch_qkv_post(c->p_qkv, c->pieces, M, g.n_q_heads, g.n_kv_heads, g.head_dim, kvv, l,
-                              c->qfrag, c->status, st, true)); ++n;
-    SPEC_TRY(launch_attention(c->attn, kvv, l, c->qfrag, M, c->attn_part, nullptr, c->act, c->status,
+                              c->qtile, c->attn.tiles, c->status, st, true)); ++n;
+    SPEC_TRY(launch_attention(c->attn, kvv, l, c->qtile, M, c->attn_part, nullptr, c->act, c->status,
                               st, true)); n += 2;
     SPEC_TRY(gemm(c->p_o, w->w_o[l])); ++n;
     SPEC_TRY(launch_resid_norm_quant(&c->p_o, c->pieces, c->resid, c->resid, ffn_gamma(l), g.rms_eps,

@@ -5,18 +5,19 @@
 // Ch. 33 §33.7).  Query head h reads KV head h / (n_q/n_kv).
 // s = q.k / sqrt(head_dim), softmax over the visible positions, o = sum p v.
 //
-// Decomposition (flash-decoding): CTA (chunk c, kv head, head half) takes the
-// keys [c*C, (c+1)*C) for its query heads of that kv head (one warp per head,
-// the 16 rows of the block are the MMA's 16 rows), walking them in 64-key
-// sub-chunks with a running (max, sum, unnormalised o) per row (online
-// softmax), and writes those partials.  C is 64 times the number of
-// sub-chunks per chunk, set from max_ctx alone so that a long context still
-// uses at most about 48 chunks (the partials would otherwise outgrow the KV
-// they summarise).  A merge kernel combines the chunks in chunk order,
-// normalises, and quantises the rows for the output projection.  Chunk and
-// sub-chunk boundaries are fixed by max_ctx and masked keys contribute exact
-// zeros, so row i's result is the same for every M (batch-height invariance:
-// "The Two-Fifteen That Wasn't").
+// Decomposition (flash-decoding): CTA (chunk c, kv head, tile) takes the keys
+// [c*C, (c+1)*C) for up to 8 query heads of that kv head.  The 8 heads x 16
+// block rows are the 128 rows of tcgen05 MMAs:
+//   S[128 x 64 keys]   = Q[128 x 128 d] . K^T      (A, B in shared memory)
+//   O[128 x 128 d]    += P[128 x 64 keys] . V      (A = P in TMEM, B = V)
+// walking the chunk in 64-key sub-chunks with a running (max, sum) per row
+// and O accumulated in TMEM (online softmax), and writes the partials.  C is
+// 64 times the sub-chunks per chunk, set from max_ctx alone so that one
+// launch is one wave of at most kCtaBudget CTAs.  A merge kernel combines the
+// chunks in chunk order, normalises, and quantises the rows for the output
+// projection.  Chunk and sub-chunk boundaries are fixed by max_ctx and masked
+// keys contribute exact zeros, so row i's result is the same for every M
+// (batch-height invariance: "The Two-Fifteen That Wasn't").
 //
 // Precision: K and V are exact bf16; q and p are split into bf16 hi + lo parts
 // (two MMAs each) so the products carry ~16 significant bits; accumulation is
@@ -29,10 +30,11 @@
 
 namespace spec {
 
-constexpr int kChunk = 64;
-constexpr int kMaxGroup = 13;        // max query heads per kv head
-
-constexpr int kTargetChunks = 48;    // chunks per context at most (about)
+constexpr int kChunk = 64;                 // keys per sub-chunk (4 pages of 16)
+constexpr int kCtaBudget = 148;            // CTAs of one partial launch at most
+constexpr int kHeadsPerTile = 8;           // 8 heads x 16 rows = 128 MMA rows
+constexpr int kKvBufs = 3;                 // K/V sub-chunk ring
+constexpr int kPartStride = 130;           // floats per partial row: o[128], max, sum
 
 AttnPlan make_attn_plan(int nq, int nkv, int dh, int max_ctx) {
   AttnPlan a;
@@ -40,24 +42,51 @@ AttnPlan make_attn_plan(int nq, int nkv, int dh, int max_ctx) {
   a.nkv = nkv;
   a.dh = dh;
   a.max_ctx = max_ctx;
-  const int subs64 = (max_ctx + kChunk - 1) / kChunk;
-  const int subs = (subs64 + kTargetChunks - 1) / kTargetChunks;   // 64-key sub-chunks per chunk
-  a.chunk = kChunk * (subs > 0 ? subs : 1);
+  a.group = nkv > 0 ? nq / nkv : 0;
+  a.tiles = (a.group + kHeadsPerTile - 1) / kHeadsPerTile;
+  const int per_chunk = nkv * (a.tiles > 0 ? a.tiles : 1);
+  const int budget = kCtaBudget / per_chunk > 0 ? kCtaBudget / per_chunk : 1;
+  const int subs64 = max_ctx > 0 ? (max_ctx + kChunk - 1) / kChunk : 1;
+  const int subs = (subs64 + budget - 1) / budget;            // 64-key sub-chunks per chunk
+  a.chunk = kChunk * subs;
   a.max_chunks = (max_ctx + a.chunk - 1) / a.chunk;
+  if (a.max_chunks < 1) a.max_chunks = 1;
   return a;
 }
-// Shared memory of the partial kernel: a double buffer of K and V sub-chunks,
-// each [d half (2)][64 keys][128 bytes] with the 16-byte chunks of a row
-// permuted by the 128-byte swizzle of the tensor copies (chunk j of row r at
-// j ^ (r % 8)), then the chunk's page ids (16 keys per page).  1 KB of slack
-// aligns the buffers to the 1 KB swizzle period.
-constexpr int kHalfBytes = kChunk * 128;              // one d half of a K or V sub-chunk
-constexpr int kKvBufBytes = 2 * 2 * kHalfBytes;       // K and V of one buffer
-constexpr size_t kKvSmemBytes = 1024 + 2 * (size_t)kKvBufBytes;
-size_t attn_smem_bytes(int chunk) { return kKvSmemBytes + sizeof(int) * (size_t)(chunk / 16); }
 
-// byte offset of 16-byte chunk j (0..7) of row r in a swizzled [rows][128 B] half
-SPEC_DEV uint32_t swz(int r, int j) { return (uint32_t)(r * 128 + ((j ^ (r & 7)) << 4)); }
+// Shared memory of the partial kernel (1 KB aligned; the 128-byte swizzle
+// repeats every 1 KB): the Q tile (hi, lo; each [d half][128 rows][128 B]),
+// a ring of kKvBufs K/V sub-chunks (K then V, each [d half][64 keys][128 B]),
+// then the chunk's page ids.  In every [rows][128 B] block the 16-byte chunk j
+// of row r sits at j ^ (r % 8).  The partials of the tile are staged over the
+// Q tile and the first ring slot once every MMA has completed.
+constexpr int kHalfBytes = kChunk * 128;                       // 8 KB
+constexpr int kKvBufBytes = 4 * kHalfBytes;                    // 32 KB
+constexpr int kQHalfBytes = 128 * 128;                         // 16 KB
+constexpr int kQTileBytes = 4 * kQHalfBytes;                   // 64 KB
+constexpr size_t kSmemFixed = 1024 + kQTileBytes + (size_t)kKvBufs * kKvBufBytes;
+static_assert(128 * kPartStride * 4 <= kQTileBytes + kKvBufBytes, "partials staging");
+size_t attn_smem_bytes(int chunk) { return kSmemFixed + sizeof(int) * (size_t)(chunk / 16); }
+
+// TMEM columns: S (two buffers of 64), P hi (32) and lo (32), O (128)
+constexpr uint32_t kTmS = 0, kTmP = 128, kTmO = 256;
+constexpr int kTmCols = 512;
+
+// warps: 0-7 own the tile rows, two threads per row (warp w: rows 32(w%4)..,
+// S columns 32(w/4).., O columns 64(w/4)..) for the softmax, the O rescale and
+// the partials; 8 issues the MMAs, 9 issues the copies
+constexpr int kRowWarps = 8;
+constexpr int kRowThreads = 32 * kRowWarps;
+constexpr int kAttnWarps = kRowWarps + 2;
+constexpr int kWarpMma = kRowWarps, kWarpCopy = kRowWarps + 1;
+constexpr uint64_t kAttnWaitNs = 2000000000ull;
+
+size_t qtile_bytes(const AttnPlan& a) { return (size_t)a.nkv * a.tiles * kQTileBytes; }
+
+size_t attn_partial_floats(const AttnPlan& a, int max_rows) {
+  (void)max_rows;
+  return (size_t)a.max_chunks * a.nq * 16 * kPartStride;
+}
 
 // 2-D tensor copy global -> shared: box at (x, y) of the map, completion on mbar
 SPEC_DEV void tma_load_2d(void* dst_smem, const CUtensorMap* map, int x, int y, uint64_t* mbar) {
@@ -97,333 +126,418 @@ static cudaError_t make_kv_tmap(const KvView& kv, CUtensorMap* map) {
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-size_t attn_partial_floats(const AttnPlan& a, int max_rows) {
-  (void)max_rows;
-  return (size_t)a.max_chunks * a.nq * 16 * (a.dh + 2);
-}
-
-SPEC_DEV void ldsm_x4(uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3, const void* p) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(smem_u32(p)));
-}
-SPEC_DEV void ldsm_x4_t(uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3, const void* p) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(smem_u32(p)));
-}
-
-SPEC_DEV uint32_t pack_bf16(float lo, float hi) {
-  return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(lo)) |
-         ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(hi)) << 16);
-}
-// split x into bf16 hi + bf16 lo (x - hi), packed pairs (x0 in the low half)
-SPEC_DEV void split2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
-  const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
-  const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - __low2float(h), x1 - __high2float(h));
-  hi = *reinterpret_cast<const uint32_t*>(&h);
-  lo = *reinterpret_cast<const uint32_t*>(&l);
-}
 // 2^x (PTX ex2.approx: relative error about 2^-22; 2^-inf = 0)
 SPEC_DEV float exp2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
   return y;
 }
-
-// dh is fixed to 128 (8 k-steps of 16 for q.k, 16 n-tiles of 8 for p.v).
-// grid (chunk, kv head, head part): the query heads of a kv head are split
-// over HS CTAs (the K/V chunk is read HS times, all but once from L2).  One
-// 64-key sub-chunk per chunk (short contexts): HS = 2, 7 warps.  Several
-// sub-chunks: HS = 3, at most 5 warps, so that two CTAs per SM fit the
-// registers of the running softmax state.
-__host__ __device__ constexpr int head_split(bool multi) { return multi ? 3 : 2; }
-__host__ __device__ constexpr int warps_per_cta(bool multi) {
-  return (kMaxGroup + head_split(multi) - 1) / head_split(multi);
+// split x into bf16 hi + bf16 lo, packed pairs (x0 in the low half): hi is x
+// with the low 16 bits dropped (exact), lo = x - hi (exact in fp32, below
+// 2^-7 |x|) rounded to bf16, so hi + lo carries about 16 significant bits
+SPEC_DEV void split2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  const uint32_t b0 = __float_as_uint(x0), b1 = __float_as_uint(x1);
+  hi = __byte_perm(b0, b1, 0x7632);
+  const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - __uint_as_float(b0 & 0xFFFF0000u),
+                                                 x1 - __uint_as_float(b1 & 0xFFFF0000u));
+  lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+SPEC_DEV void tmem_st16(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n" ::"r"(
+          taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]));
+}
+SPEC_DEV void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+// shared-memory descriptor of a 128-byte-swizzled operand: lbo and sbo in bytes
+SPEC_DEV uint64_t desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return smem_desc(saddr, lbo, sbo) | ((uint64_t)2 << 61);
+}
+// D[tmem] (+)= A[smem] * B[smem]^T, kind::f16, issued by one thread
+SPEC_DEV void mma_f16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
+}
+// bulk copy shared -> global (bulk group of this thread)
+SPEC_DEV void bulk_s2g(void* dst, const void* src_smem, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n" ::"l"(dst),
+               "r"(smem_u32(src_smem)), "r"(bytes)
+               : "memory");
+  asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
+  asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");
 }
 
-size_t qfrag_bytes(int nq) { return (size_t)nq * 8 * 2 * 32 * 16; }
-
-__global__ void q_to_frag_kernel(const float* __restrict__ q, int M, int nq, uint8_t* qfrag) {
+// ---- Q tiles from fp32 q [M][nq][128] (rows >= M zero), the standalone path
+__global__ void q_to_tile_kernel(const float* __restrict__ q, int M, int nq, int group, int tiles,
+                                 uint8_t* qtile) {
   pdl_trigger();
   pdl_wait();
   const int row = blockIdx.y;
   const int col = blockIdx.x * blockDim.x + threadIdx.x;
   if (col >= nq * 128) return;
-  write_qfrag(qfrag, row, col >> 7, col & 127, row < M ? q[(size_t)row * nq * 128 + col] : 0.f);
+  write_qtile(qtile, row, col >> 7, col & 127, row < M ? q[(size_t)row * nq * 128 + col] : 0.f, group,
+              tiles);
 }
 
-cudaError_t launch_q_to_frag(const float* q, int M, int nq, uint8_t* qfrag, cudaStream_t st, bool pdl) {
+cudaError_t launch_q_to_tile(const float* q, int M, const AttnPlan& a, uint8_t* qtile, cudaStream_t st,
+                             bool pdl) {
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((nq * 128 + 255) / 256, 16);
+  cfg.gridDim = dim3((a.nq * 128 + 255) / 256, 16);
   cfg.blockDim = dim3(256);
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, q_to_frag_kernel, q, M, nq, qfrag);
+  return cudaLaunchKernelEx(&cfg, q_to_tile_kernel, q, M, a.nq, a.group, a.tiles, qtile);
 }
 
-// a Q-fragment load the compiler re-issues per use (kept out of the registers
-// across the key loop: the fragments are L1/L2 hits)
-SPEC_DEV uint4 ldg_frag(const uint4* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];\n"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
-
-template <bool MULTI>
-__global__ void __launch_bounds__(warps_per_cta(MULTI) * 32, 2)
-attn_partial_kernel(const uint4* __restrict__ qf, int M, int nq, int nkv, int chunk_keys, KvView kv,
-                    const __grid_constant__ CUtensorMap kvmap, int layer, float* __restrict__ part,
-                    int32_t* status) {
-  constexpr int kHeadSplit = head_split(MULTI);
+// ---------------------------------------------------------------------------
+// partials: grid (chunk, kv head, tile), kAttnWarps warps.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kAttnWarps * 32, 1)
+attn_partial_kernel(const uint8_t* __restrict__ qtile, int M, int nq, int nkv, int group, int tiles,
+                    int chunk_keys, KvView kv, const __grid_constant__ CUtensorMap kvmap, int layer,
+                    float* __restrict__ part, int32_t* status) {
   extern __shared__ __align__(128) uint8_t dsm[];
-  uint8_t* kvs = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm) + 1023) & ~(uintptr_t)1023);
-  int* pg = reinterpret_cast<int*>(dsm + kKvSmemBytes);
-  __shared__ __align__(8) uint64_t kvbar[2];     // K/V of buffer b landed (bulk copies)
-  __shared__ int copy_ok;
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm) + 1023) & ~(uintptr_t)1023);
+  uint8_t* qs = sm;                                    // Q tile: hi [0, 32K), lo [32K, 64K)
+  uint8_t* kvb = sm + kQTileBytes;                     // ring slot b at kvb + b * kKvBufBytes
+  int* pg = reinterpret_cast<int*>(dsm + kSmemFixed);
+  __shared__ uint32_t tmem_slot;
+  __shared__ __align__(8) uint64_t q_full, k_full[kKvBufs], v_full[kKvBufs], kv_free[kKvBufs], s_full[2],
+      s_free[2], p_full, pv_done;
 
+  __shared__ float rowmax[2][2][128];       // [sub-chunk parity][column half][row]
+  __shared__ float lpart[2][128];           // [column half][row]
+  __shared__ int proceed;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int chunk = blockIdx.x, kvh = blockIdx.y, tile = blockIdx.z;
+  const int key0 = chunk * chunk_keys;
+  // barriers and TMEM do not depend on the previous kernel
+  if (warp == 0) tmem_alloc(&tmem_slot, kTmCols);
+  if (tid == 0) {
+    mbar_init(&q_full, 1);
+    for (int b = 0; b < kKvBufs; ++b) {
+      mbar_init(&k_full[b], 1);
+      mbar_init(&v_full[b], 1);
+      mbar_init(&kv_free[b], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&s_full[b], 1);
+      mbar_init(&s_free[b], kRowThreads);
+    }
+    mbar_init(&p_full, kRowThreads);
+    mbar_init(&pv_done, 1);
+    fence_mbarrier_init();
+  }
+  if (warp == kWarpCopy && lane == 0)
+    asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&kvmap)) : "memory");
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
   pdl_trigger();
   pdl_wait();
-  const int chunk = blockIdx.x, kvh = blockIdx.y;
-  const int group = nq / nkv;
-  const int per = (group + kHeadSplit - 1) / kHeadSplit;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = lane >> 2, t = lane & 3;
-  const int key0 = chunk * chunk_keys;
-  // status, length and the chunk's page ids in one round of loads
+  // the Q tile goes out first; status, length and the chunk's page ids in
+  // one round of loads meanwhile
+  if (warp == kWarpCopy && lane == 0) {
+    mbar_arrive_expect_tx(&q_full, (uint32_t)kQTileBytes);
+    bulk_g2s(qs, qtile + (size_t)(kvh * tiles + tile) * kQTileBytes, (uint32_t)kQTileBytes, &q_full);
+  }
   const int32_t st = *status;
   const int len = *kv.seq_len;             // block appended: n_past + M
-  for (int i = threadIdx.x; i < chunk_keys / 16; i += blockDim.x) {
+  for (int i = tid; i < chunk_keys / 16; i += blockDim.x) {
     const int lp = key0 / 16 + i;
     pg[i] = lp < kv.max_seq_pages ? kv.page_table[lp] : -1;
   }
-  if (threadIdx.x == 0) {
-    mbar_init(&kvbar[0], 1);
-    mbar_init(&kvbar[1], 1);
-    fence_mbarrier_init();
-  }
+  if (tid == 0) proceed = !(st & (SPEC_ST_TOKEN_RANGE | SPEC_ST_POOL_EMPTY | SPEC_ST_CTX_FULL)) && key0 < len;
   __syncthreads();
-  if (st & (SPEC_ST_TOKEN_RANGE | SPEC_ST_POOL_EMPTY | SPEC_ST_CTX_FULL)) return;
   const int n_past = len - M;
-  if (key0 >= len) return;
-  // sub-chunks with keys (exactly one when the chunk is one sub-chunk long)
-  const int nsub = MULTI ? min(chunk_keys, len - key0 + kChunk - 1) / kChunk : 1;
+  // sub-chunks with keys (0 when the CTA has nothing to do)
+  const int nsub = proceed ? min(chunk_keys, len - key0 + kChunk - 1) / kChunk : 0;
 
-  // ---- K, V sub-chunk sc -> shared buffer sc % 2: lanes 0..15 of warp 0 each
-  // copy one d half of the K or V rows of one page (16 keys) with a tensor
-  // copy; lane 0 arms the buffer's barrier with the bytes of the pages copied.
-  // Pages past len or with an out-of-range id are not copied; their rows, and
-  // the rows at or past len in a copied page, are zeroed once the copies have
-  // landed (fix_sub).
+  // page id of the page holding pos0 (a multiple of 16), -1 past len or out of range
   auto page_of = [&](int pos0) -> int {
     const int page = pos0 < len ? pg[(pos0 - key0) >> 4] : -1;
     return (page >= 0 && page < kv.num_pages) ? page : -1;
   };
-  auto load_sub = [&](int sc) {
-    if (warp != 0) return;
-    uint8_t* buf = kvs + (size_t)(sc & 1) * kKvBufBytes;
-    uint64_t* bar = &kvbar[sc & 1];
-    const int ks0 = key0 + sc * kChunk;
-    const int pp = (lane >> 2) & 3, which = (lane >> 1) & 1, half = lane & 1;
-    const int page = page_of(ks0 + 16 * pp);
-    const bool go = lane < 16 && page >= 0;
-    const uint32_t ops = __popc(__ballot_sync(0xffffffffu, go));
-    if (lane == 0) mbar_arrive_expect_tx(bar, ops * 2048u);
-    if (go) {
-      const int y = (((page * kv.n_layers + layer) * 2 + which) * kv.n_kv + kvh) * 16;
-      tma_load_2d(buf + which * 2 * kHalfBytes + half * kHalfBytes + pp * 2048, &kvmap, 64 * half, y, bar);
-    }
-  };
-  // rows of sub-chunk sc that must read as zero: keys at or past len, keys of a
-  // page with an out-of-range id (CTA-uniform)
-  auto sub_needs_fix = [&](int sc) -> bool {
-    const int ks0 = key0 + sc * kChunk;
-    if (ks0 + kChunk > len) return true;
-#pragma unroll
-    for (int pp = 0; pp < kChunk / 16; ++pp)
-      if (page_of(ks0 + 16 * pp) < 0) return true;
-    return false;
-  };
-  auto fix_sub = [&](int sc) {
-    uint8_t* buf = kvs + (size_t)(sc & 1) * kKvBufBytes;
-    const int ks0 = key0 + sc * kChunk;
-    for (int i = threadIdx.x; i < kChunk * 4; i += blockDim.x) {     // (row, K/V, half)
-      const int r = i >> 2, which = (i >> 1) & 1, half = i & 1;
-      const int pos = ks0 + r;
-      if (pos < len && page_of(ks0 + 16 * (r >> 4)) >= 0) continue;
-      uint4* row = reinterpret_cast<uint4*>(buf + which * 2 * kHalfBytes + half * kHalfBytes + r * 128);
-#pragma unroll
-      for (int c16 = 0; c16 < 8; ++c16) row[c16] = make_uint4(0, 0, 0, 0);
-    }
-    fence_proxy_async();      // ordered before the tensor copies that later refill the buffer
-  };
 
-  const int hl = blockIdx.z * per + warp;          // head within the kv group
-  const bool active = warp < per && hl < group;
-  const int head = kvh * group + (active ? hl : 0);
-  const uint4* Qf = qf + (size_t)head * 8 * 2 * 32;   // [8 ksteps][hi, lo][32 lanes]
-  // scores in base-2 units: u = (q.k / sqrt(128)) * log2(e), p = 2^(u - max)
-  const float c2 = 1.4426950408889634f / sqrtf(128.0f);
-
-  // running per-row state (rows g and g+8): max, sum, unnormalised o
-  float mrun[2] = {-INFINITY, -INFINITY}, lrun[2] = {0.f, 0.f};
-  float o[16][4];
-#pragma unroll
-  for (int nd = 0; nd < 16; ++nd)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) o[nd][e] = 0.f;
-
-  load_sub(0);
-  for (int sc = 0; sc < nsub; ++sc) {
-    if (sc + 1 < nsub) load_sub(sc + 1);
-    // one thread waits (bounded) for the buffer; the CTA barrier passes the
-    // result and the landed rows to all threads
-    if (threadIdx.x == 0) copy_ok = mbar_wait_ns(&kvbar[sc & 1], (sc >> 1) & 1, 2000000000ull) ? 1 : 0;
-    __syncthreads();
-    if (!copy_ok) {
-      if (threadIdx.x == 0) {          // flag it; let the other buffer's copies land (bounded)
-        atomicOr(status, SPEC_ST_DEVICE_WAIT);
-        if (sc + 1 < nsub) mbar_wait_ns(&kvbar[(sc + 1) & 1], ((sc + 1) >> 1) & 1, 2000000000ull);
+  if (warp == kWarpCopy) {
+    // ------------------------------------------------------------ copies
+    bool ok = true;
+    int issued = 0;
+    for (int sc = 0; sc < nsub; ++sc) {
+      const int b = sc % kKvBufs;
+      if (sc >= kKvBufs)
+        ok = __all_sync(0xffffffffu, mbar_wait_ns(&kv_free[b], ((sc / kKvBufs) - 1) & 1, kAttnWaitNs));
+      if (!ok) break;
+      // lanes 0..15: K (lanes 0-7) or V, page (lane/2)%4, d half; K first
+      uint8_t* buf = kvb + (size_t)b * kKvBufBytes;
+      const int ks0 = key0 + sc * kChunk;
+      const int which = (lane >> 3) & 1, pp = (lane >> 1) & 3, half = lane & 1;
+      const int page = page_of(ks0 + 16 * pp);
+      const bool go = lane < 16 && page >= 0;
+      const uint32_t kops = __popc(__ballot_sync(0xffffffffu, go && which == 0));
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&k_full[b], kops * 2048u);
+        mbar_arrive_expect_tx(&v_full[b], kops * 2048u);   // a page's K and V come together
       }
-      return;
-    }
-    if (sub_needs_fix(sc)) {
-      fix_sub(sc);
-      __syncthreads();
-    }
-    const uint8_t* Ks = kvs + (size_t)(sc & 1) * kKvBufBytes;
-    const uint8_t* Vs = Ks + 2 * kHalfBytes;
-    const int ks0 = key0 + sc * kChunk;
-    if (active) {
-      // ---- scores S = q.k for 64 keys: 8 n-tiles x 4
-      float s[8][4];
-#pragma unroll
-      for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) s[nt][e] = 0.f;
-#pragma unroll
-      for (int kp = 0; kp < 4; ++kp) {          // pairs of k-steps
-        const uint4 qh0 = ldg_frag(Qf + ((2 * kp) * 2 + 0) * 32 + lane);
-        const uint4 ql0 = ldg_frag(Qf + ((2 * kp) * 2 + 1) * 32 + lane);
-        const uint4 qh1 = ldg_frag(Qf + ((2 * kp + 1) * 2 + 0) * 32 + lane);
-        const uint4 ql1 = ldg_frag(Qf + ((2 * kp + 1) * 2 + 1) * 32 + lane);
-#pragma unroll
-        for (int nt = 0; nt < 8; ++nt) {
-          uint32_t b0, b1, b2, b3;
-          const int krow = 8 * nt + (lane & 7);   // d = 32 kp + 8 (lane / 8): half kp / 2
-          ldsm_x4(b0, b1, b2, b3, Ks + (kp >> 1) * kHalfBytes + swz(krow, 4 * (kp & 1) + (lane >> 3)));
-          mma16816_bf16(s[nt], qh0.x, qh0.y, qh0.z, qh0.w, b0, b1);
-          mma16816_bf16(s[nt], ql0.x, ql0.y, ql0.z, ql0.w, b0, b1);
-          mma16816_bf16(s[nt], qh1.x, qh1.y, qh1.z, qh1.w, b2, b3);
-          mma16816_bf16(s[nt], ql1.x, ql1.y, ql1.z, ql1.w, b2, b3);
-        }
+      if (go) {
+        const int y = (((page * kv.n_layers + layer) * 2 + which) * kv.n_kv + kvh) * 16;
+        tma_load_2d(buf + which * 2 * kHalfBytes + half * kHalfBytes + pp * 2048, &kvmap, 64 * half, y,
+                    which == 0 ? &k_full[b] : &v_full[b]);
       }
-
-      // ---- mask, running max, p = 2^(u - max), rescale of the running state.
-      // A sub-chunk whose keys all precede the block is visible to every row.
-      const bool full = ks0 + kChunk - 1 <= n_past;
-      float mx[2] = {-INFINITY, -INFINITY};
-      if (full) {
+      issued = sc + 1;
+    }
+    if (!ok && lane == 0) atomicOr(status, SPEC_ST_DEVICE_WAIT);
+    // no copy may still be writing shared memory when the CTA exits
+    if (lane == 0) {
+      mbar_wait_ns(&q_full, 0, kAttnWaitNs);
+      for (int u = max(0, issued - kKvBufs); u < issued; ++u) {
+        mbar_wait_ns(&k_full[u % kKvBufs], (u / kKvBufs) & 1, kAttnWaitNs);
+        mbar_wait_ns(&v_full[u % kKvBufs], (u / kKvBufs) & 1, kAttnWaitNs);
+      }
+    }
+  } else if (warp == kWarpMma) {
+    // ------------------------------------------------------------ MMA issue
+    // D f32 (bit 4), A and B bf16 (bits 7, 10), N >> 3 at 17, M >> 4 at 24;
+    // P.V reads V (the B operand) MN-major (bit 16)
+    constexpr uint32_t kIdQK = (1u << 4) | (1u << 7) | (1u << 10) | ((64u >> 3) << 17) | ((128u >> 4) << 24);
+    constexpr uint32_t kIdPV =
+        (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
+    const uint32_t tm = __shfl_sync(0xffffffffu, tmem, 0);
+    const uint32_t qa = __shfl_sync(0xffffffffu, smem_u32(qs), 0);
+    const uint32_t kva = __shfl_sync(0xffffffffu, smem_u32(kvb), 0);
+    bool ok = __all_sync(0xffffffffu, mbar_wait_ns(&q_full, 0, kAttnWaitNs));
+    int last_pv = -1, last_qk = -1;
+    // S[sc % 2] = Q . K(sc)^T: 8 d steps of 16, hi and lo parts of Q
+    auto issue_qk = [&](int sc) -> bool {
+      const int b = sc % kKvBufs, sb = sc & 1;
+      bool w = mbar_wait_ns(&k_full[b], (sc / kKvBufs) & 1, kAttnWaitNs);
+      if (sc >= 2) w = w && mbar_wait_ns(&s_free[sb], ((sc >> 1) - 1) & 1, kAttnWaitNs);
+      if (!__all_sync(0xffffffffu, w)) return false;
+      tc_fence_after();
+      if (elect_one()) {
+        const uint32_t kaddr = kva + (uint32_t)(b * kKvBufBytes);
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
+        for (int ks = 0; ks < 8; ++ks)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            s[nt][e] *= c2;
-            mx[e >> 1] = fmaxf(mx[e >> 1], s[nt][e]);
+          for (int part = 0; part < 2; ++part) {
+            const uint64_t da = desc_sw128(qa + part * 2 * kQHalfBytes + (ks >> 2) * kQHalfBytes + (ks & 3) * 32, 16, 1024);
+            const uint64_t db = desc_sw128(kaddr + (ks >> 2) * kHalfBytes + (ks & 3) * 32, 16, 1024);
+            mma_f16_ss(tm + kTmS + 64u * sb, da, db, kIdQK, (ks | part) != 0);
           }
+        mma_commit(&s_full[sb]);
+      }
+      __syncwarp();
+      last_qk = sc;
+      return true;
+    };
+    if (ok && nsub > 0) ok = issue_qk(0);
+    for (int sc = 0; ok && sc < nsub; ++sc) {
+      if (sc + 1 < nsub && !(ok = issue_qk(sc + 1))) break;
+      // O (+)= P . V(sc): 4 key steps of 16, hi and lo parts of P
+      ok = __all_sync(0xffffffffu, mbar_wait_ns(&p_full, sc & 1, kAttnWaitNs) &&
+                                       mbar_wait_ns(&v_full[sc % kKvBufs], (sc / kKvBufs) & 1, kAttnWaitNs));
+      if (!ok) break;
+      tc_fence_after();
+      if (elect_one()) {
+        const uint32_t vaddr = kva + (uint32_t)((sc % kKvBufs) * kKvBufBytes + 2 * kHalfBytes);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+          for (int part = 0; part < 2; ++part) {
+            // V is MN-major: lbo = 8 KB between d halves, sbo = 1 KB between 8-key groups
+            const uint64_t db = desc_sw128(vaddr + kk * 2048, kHalfBytes, 1024);
+            mma_f16_ts(tm + kTmO, tm + kTmP + 32u * part + 8u * kk, db, kIdPV,
+                       (sc | kk | part) != 0);
+          }
+        mma_commit(&pv_done);
+        mma_commit(&kv_free[sc % kKvBufs]);
+      }
+      __syncwarp();
+      last_pv = sc;
+    }
+    if (!ok && lane == 0) atomicOr(status, SPEC_ST_DEVICE_WAIT);
+    // TMEM is released at the end: every MMA issued here must have finished
+    if (last_pv >= 0) mbar_wait_ns(&pv_done, last_pv & 1, kAttnWaitNs);
+    if (last_qk > last_pv) mbar_wait_ns(&s_full[last_qk & 1], (last_qk >> 1) & 1, kAttnWaitNs);
+  } else {
+    // ------------------------------------------------------------ tile rows
+    const int r = 32 * (warp & 3) + lane;               // tile row = TMEM lane
+    const int h = warp >> 2;                            // S columns 32h.., O columns 64h..
+    const int hl = tile * kHeadsPerTile + (r >> 4);     // head within the kv group
+    const int row = r & 15;                             // block row
+    const bool live = hl < group && row < M;
+    const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+    const float c2 = 1.4426950408889634f / sqrtf(128.0f);   // log2(e) / sqrt(d)
+    float mref = -INFINITY, lsum = 0.f;
+    bool ok = true;
+    // Every row thread passes the same named barriers in the same order: a
+    // failed wait is carried to the next barrier (bar.red.and), where all
+    // 256 threads leave together.
+    for (int sc = 0; sc < nsub; ++sc) {
+      const int sb = sc & 1, b = sc % kKvBufs;
+      const int ks0 = key0 + sc * kChunk;
+      const bool got = ok && __all_sync(0xffffffffu, mbar_wait_ns(&s_full[sb], (sc >> 1) & 1, kAttnWaitNs));
+      float s[32];
+      if (got) {
+        tc_fence_after();
+        uint32_t u[32];
+        tmem_ld32(tmem + lane_base + kTmS + 64u * sb + 32u * h, u);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 32; ++c) s[c] = __uint_as_float(u[c]);
+        tc_fence_before();
+        mbar_arrive(&s_free[sb]);
       } else {
-        // key ks0 + 8nt + 2t + (e&1) is visible to row g + 8(e>>1) < M when
-        // 8nt + (e&1) <= n_past + row - ks0 - 2t
-        int lim[2];
 #pragma unroll
-        for (int r = 0; r < 2; ++r) lim[r] = (g + 8 * r < M) ? n_past + g + 8 * r - ks0 - 2 * t : -1;
-#pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float v = (8 * nt + (e & 1) <= lim[e >> 1]) ? s[nt][e] * c2 : -INFINITY;
-            s[nt][e] = v;
-            mx[e >> 1] = fmaxf(mx[e >> 1], v);
-          }
+        for (int c = 0; c < 32; ++c) s[c] = 0.f;
       }
-      float alpha[2], mbase[2];
+      // pages of this sub-chunk: a key of a page past len or with an
+      // out-of-range id is masked (and its V row zeroed below)
+      bool pok[4];
 #pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
-        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
-        const float mnew = fmaxf(mrun[r], mx[r]);
-        alpha[r] = (mrun[r] == -INFINITY) ? 0.f : exp2_approx(mrun[r] - mnew);
-        mrun[r] = mnew;
-        mbase[r] = mnew == -INFINITY ? 0.f : mnew;    // a row with no visible key yet: p = 2^-inf = 0
-      }
-      float sum[2] = {0.f, 0.f};
+      for (int pp = 0; pp < 4; ++pp) pok[pp] = page_of(ks0 + 16 * pp) >= 0;
+      const bool allpages = pok[0] && pok[1] && pok[2] && pok[3];
+      const bool full = ks0 + kChunk - 1 <= n_past && allpages;
+      // scores in base-2 units, masked -> -inf; key ks0 + c visible to row
+      // when c <= n_past + row - ks0
+      float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      if (full && live) {
 #pragma unroll
-      for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float p = exp2_approx(s[nt][e] - mbase[e >> 1]);
-          s[nt][e] = p;
-          sum[e >> 1] += p;
+        for (int c = 0; c < 32; ++c) {
+          s[c] *= c2;
+          mx4[c & 3] = fmaxf(mx4[c & 3], s[c]);
         }
+      } else {
+        const int lim = live ? n_past + row - ks0 : -1;
 #pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        sum[r] += __shfl_xor_sync(0xffffffffu, sum[r], 1);
-        sum[r] += __shfl_xor_sync(0xffffffffu, sum[r], 2);
-        lrun[r] = lrun[r] * alpha[r] + sum[r];
+        for (int c = 0; c < 32; ++c) {
+          const int key = 32 * h + c;
+          const bool vis = key <= lim && pok[key >> 4];
+          s[c] = vis ? s[c] * c2 : -INFINITY;
+          mx4[c & 3] = fmaxf(mx4[c & 3], s[c]);
+        }
       }
+      // row max over both column halves (exchanged through shared memory)
+      rowmax[sb][h][r] = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+      ok = named_bar_and(1, kRowThreads, got);
+      if (!ok) break;                                   // all row threads together
+      const float mx = fmaxf(rowmax[sb][0][r], rowmax[sb][1][r]);
+      // the reference max moves only when a score exceeds it by more than 8
+      // (p <= 2^8): O is rescaled rarely.  Both threads of a row take the
+      // same decision.
+      float alpha = 1.f;
+      if (mx > mref + 8.f) {
+        alpha = mref == -INFINITY ? 0.f : exp2_approx(mref - mx);
+        mref = mx;
+        lsum *= alpha;
+      }
+      const float base = mref == -INFINITY ? 0.f : mref;
+      uint32_t ph[16], pl[16];
+      float ps4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const float p0 = exp2_approx(s[2 * c] - base), p1 = exp2_approx(s[2 * c + 1] - base);
+        ps4[c & 3] += p0 + p1;
+        split2(p0, p1, ph[c], pl[c]);
+      }
+      lsum += (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
+      // P(sc) may be written, and O rescaled, once P.V(sc-1) has finished
       if (sc > 0) {
+        ok = __all_sync(0xffffffffu, mbar_wait_ns(&pv_done, (sc - 1) & 1, kAttnWaitNs));
+        if (!ok) continue;                              // carried to the next barrier
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+          for (int q = 0; q < 2; ++q) {
+            uint32_t o[32];
+            const uint32_t oa = tmem + lane_base + kTmO + 64u * h + 32u * q;
+            tmem_ld32(oa, o);
+            tmem_wait_ld();
 #pragma unroll
-        for (int nd = 0; nd < 16; ++nd)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) o[nd][e] *= alpha[e >> 1];
+            for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+            tmem_st32(oa, o);
+          }
+        }
       }
-
-      // ---- o += p.v : 16 n-tiles of 8 dims
+      // V rows of keys that must read as zero (past len, bad page id), once
+      // the V copies of this buffer have landed
+      if (ks0 + kChunk > len || !allpages) {
+        if (!__all_sync(0xffffffffu, mbar_wait_ns(&v_full[b], (sc / kKvBufs) & 1, kAttnWaitNs))) {
+          ok = false;
+          continue;                                     // carried to the next barrier
+        }
+        uint8_t* vb = kvb + (size_t)b * kKvBufBytes + 2 * kHalfBytes;
+#pragma unroll 1
+        for (int i = 128 * h + r; i < kChunk * 16; i += kRowThreads) {   // (key, d half, 16-byte chunk)
+          const int c = i >> 4, half = (i >> 3) & 1, ch = i & 7;
+          if (ks0 + c < len && pok[c >> 4]) continue;
+          *reinterpret_cast<uint4*>(vb + half * kHalfBytes + c * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async();
+      }
+      tmem_st16(tmem + lane_base + kTmP + 16u * h, ph);
+      tmem_st16(tmem + lane_base + kTmP + 32u + 16u * h, pl);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&p_full);
+    }
+    if (!ok && r == 0 && h == 0) atomicOr(status, SPEC_ST_DEVICE_WAIT);
+    // ---- partials of the tile: [chunk][head][row][o 128 | max (base 2) | sum]
+    const int nrows = min(kHeadsPerTile, group - tile * kHeadsPerTile) * 16;
+    const bool done = ok && nsub > 0 && __all_sync(0xffffffffu, mbar_wait_ns(&pv_done, (nsub - 1) & 1, kAttnWaitNs));
+    lpart[h][r] = lsum;
+    if (done) {
+      tc_fence_after();
+      float* stage = reinterpret_cast<float*>(sm) + (size_t)r * kPartStride + 64 * h;
+#pragma unroll 1
+      for (int q = 0; q < 2; ++q) {
+        uint32_t o[32];
+        tmem_ld32(tmem + lane_base + kTmO + 64u * h + 32u * q, o);
+        tmem_wait_ld();
+        if (r < nrows) {
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {           // 16 keys per k-step
-        uint32_t ph[4], pl[4];
-        split2(s[2 * kk][0], s[2 * kk][1], ph[0], pl[0]);
-        split2(s[2 * kk][2], s[2 * kk][3], ph[1], pl[1]);
-        split2(s[2 * kk + 1][0], s[2 * kk + 1][1], ph[2], pl[2]);
-        split2(s[2 * kk + 1][2], s[2 * kk + 1][3], ph[3], pl[3]);
-#pragma unroll
-        for (int np = 0; np < 8; ++np) {          // pairs of dim tiles
-          uint32_t b0, b1, b2, b3;
-          const int vrow = 16 * kk + (lane & 7) + 8 * ((lane >> 3) & 1);   // d = 16 np + 8 (lane / 16)
-          ldsm_x4_t(b0, b1, b2, b3, Vs + (np >> 2) * kHalfBytes + swz(vrow, 2 * (np & 3) + (lane >> 4)));
-          mma16816_bf16(o[2 * np], ph[0], ph[1], ph[2], ph[3], b0, b1);
-          mma16816_bf16(o[2 * np], pl[0], pl[1], pl[2], pl[3], b0, b1);
-          mma16816_bf16(o[2 * np + 1], ph[0], ph[1], ph[2], ph[3], b2, b3);
-          mma16816_bf16(o[2 * np + 1], pl[0], pl[1], pl[2], pl[3], b2, b3);
+          for (int c = 0; c < 32; c += 2)
+            *reinterpret_cast<float2*>(stage + 32 * q + c) =
+                make_float2(__uint_as_float(o[c]), __uint_as_float(o[c + 1]));
         }
       }
     }
-    if (sc + 1 < nsub) __syncthreads();     // the next prefetch overwrites this buffer
-  }
-  if (!active) return;
-
-  // ---- partials: [chunk][head][row][128 o | max (base-2 units) | sum]
-  const int stride = 130;
-#pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    const int row = g + 8 * r;
-    float* base = part + (((size_t)chunk * nq + head) * 16 + row) * stride;
-#pragma unroll
-    for (int nd = 0; nd < 16; ++nd)
-      *reinterpret_cast<float2*>(base + 8 * nd + 2 * t) = make_float2(o[nd][2 * r], o[nd][2 * r + 1]);
-    if (t == 0) {
-      base[128] = mrun[r];
-      base[129] = lrun[r];
+    // every row's sum = its two column halves, in that order
+    const bool all_done = named_bar_and(1, kRowThreads, done);
+    if (all_done && h == 0 && r < nrows)
+      *reinterpret_cast<float2*>(reinterpret_cast<float*>(sm) + (size_t)r * kPartStride + 128) =
+          make_float2(mref, lpart[0][r] + lpart[1][r]);
+    fence_proxy_async();
+    if (named_bar_and(1, kRowThreads, all_done) && r == 0 && h == 0) {
+      float* dst = part + (((size_t)chunk * nq + (size_t)kvh * group + tile * kHeadsPerTile) * 16) * kPartStride;
+      bulk_s2g(dst, sm, (uint32_t)(nrows * kPartStride * 4));
     }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmCols);
   }
 }
-
 
 // merge: grid (nq*128/256 blocks, 16 rows), 256 threads = 2 heads x 128 dims.
 // For row i the chunks 0 .. (n_past+i)/C are combined:
@@ -504,33 +618,32 @@ attn_merge_kernel(const float* __restrict__ part, int M, int nq, int max_chunks,
   }
 }
 
-cudaError_t launch_attention(const AttnPlan& a, const KvView& kv, int layer, const uint8_t* qfrag,
+cudaError_t launch_attention(const AttnPlan& a, const KvView& kv, int layer, const uint8_t* qtile,
                              int M, float* part, float* out, uint8_t* act, int32_t* status,
                              cudaStream_t st, bool pdl) {
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cudaLaunchConfig_t cfg = {};
   alignas(64) CUtensorMap kvmap;
   cudaError_t em = make_kv_tmap(kv, &kvmap);
   if (em != cudaSuccess) return em;
-  const bool multi = a.chunk > kChunk;
-  auto kern = multi ? attn_partial_kernel<true> : attn_partial_kernel<false>;
   const size_t smem = attn_smem_bytes(a.chunk);
-  static size_t smem_attr[2] = {0, 0};
-  if (smem_attr[multi] < smem) {
-    cudaError_t ea = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  static size_t smem_attr = 0;
+  if (smem_attr < smem) {
+    cudaError_t ea = cudaFuncSetAttribute(attn_partial_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          (int)smem);
     if (ea != cudaSuccess) return ea;
-    smem_attr[multi] = smem;
+    smem_attr = smem;
   }
-  cfg.gridDim = dim3(a.max_chunks, a.nkv, head_split(multi));
-  cfg.blockDim = dim3(32 * warps_per_cta(multi));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.max_chunks, a.nkv, a.tiles);
+  cfg.blockDim = dim3(32 * kAttnWarps);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, reinterpret_cast<const uint4*>(qfrag),
-                                     M, a.nq, a.nkv, a.chunk, kv, kvmap, layer, part, status);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, attn_partial_kernel, qtile, M, a.nq, a.nkv, a.group, a.tiles,
+                                     a.chunk, kv, kvmap, layer, part, status);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg2 = {};
   cfg2.gridDim = dim3(a.nq * 128 / 256, 16);

@@ -305,19 +305,21 @@ SPEC_DEV uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
   return d;
 }
 
-// Query fragments for the attention MMAs: per head, 8 k-steps of 16 dims, a
-// bf16 hi part and a bf16 lo part (x - hi), 32 lanes x 16 bytes in the
-// m16n8k16 A-fragment order (row = query row of the block).
-SPEC_DEV void write_qfrag(uint8_t* qf, int row, int head, int d, float v) {
-  const int kk = d >> 4, within = d & 15;
-  const int t = (within & 7) >> 1, u = within & 1;
-  const int reg = (row >> 3) + ((within >> 3) << 1);
-  const int lane = 4 * (row & 7) + t;
+// Query tiles of the attention MMAs: per (kv head, tile of 8 query heads) a
+// 64 KB block: the bf16 hi parts, then the lo parts (x - hi), each as two d
+// halves of [128 rows][128 B], row = 16 * (head % 8) + block row, with the
+// 16-byte chunk j of row r at j ^ (r % 8) (the 128-byte swizzle of the MMA
+// operand).
+SPEC_DEV void write_qtile(uint8_t* qt, int row, int head, int d, float v, int group, int tiles) {
+  const int kvh = head / group, hl = head - kvh * group;
+  const int r = ((hl & 7) << 4) + row;
+  const int half = d >> 6, j = (d & 63) >> 3, e = d & 7;
+  const size_t base = (size_t)(kvh * tiles + (hl >> 3)) * 65536 + (size_t)half * 16384 + (size_t)r * 128 +
+                      (size_t)((j ^ (r & 7)) << 4) + 2 * e;
   const __nv_bfloat16 hi = __float2bfloat16_rn(v);
   const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
-  const size_t base = ((size_t)(head * 8 + kk) * 2) * 32 * 16 + (size_t)lane * 16 + reg * 4 + u * 2;
-  *reinterpret_cast<unsigned short*>(qf + base) = __bfloat16_as_ushort(hi);
-  *reinterpret_cast<unsigned short*>(qf + base + 32 * 16) = __bfloat16_as_ushort(lo);
+  *reinterpret_cast<unsigned short*>(qt + base) = __bfloat16_as_ushort(hi);
+  *reinterpret_cast<unsigned short*>(qt + base + 32768) = __bfloat16_as_ushort(lo);
 }
 
 }  // namespace spec

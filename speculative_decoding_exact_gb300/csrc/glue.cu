@@ -279,22 +279,43 @@ cudaError_t launch_swiglu_quant(const GemmPlan& p, const float* pieces, int M, i
 // n_past = seq_len - M (the reserve kernel has already appended the block).
 // Skips the cache when the step is invalid.
 // ---------------------------------------------------------------------------
+constexpr int kQkvThreads = 256;     // columns per CTA; one more warp prefetches the KV
+
 __global__ void qkv_post_kernel(const float* __restrict__ pieces, int pN, int pnb, long long pU,
                                 int pG, int M, int nq, int nkv, int dh, KvView kv, int layer,
-                                uint8_t* __restrict__ qfrag, const int32_t* status) {
+                                uint8_t* __restrict__ qtile, int tiles, const int32_t* status) {
   pdl_trigger();
   pdl_wait();
+  // The attention that follows reads this layer's K and V of every page up to
+  // the length: one 32 KB slab per page ([K, V][n_kv][16][128] bf16).  An
+  // extra warp sends them to L2 now, while HBM has nothing else to do: lane l
+  // of CTA c takes page c + l * (number of CTAs), spreading the copies over
+  // the SMs' copy engines; its loads run alongside the other warps' loads.
+  if (threadIdx.x >= kQkvThreads) {
+    const int ncta = gridDim.x * gridDim.y;
+    const int gi = blockIdx.y * gridDim.x + blockIdx.x + (threadIdx.x - kQkvThreads) * ncta;
+    const int lp = gi < kv.max_seq_pages ? gi : kv.max_seq_pages - 1;
+    const int page = kv.page_table[lp];
+    const int npg = (*kv.seq_len + kv.page_size - 1) / kv.page_size;
+    const uint32_t slab = (uint32_t)(2 * kv.n_kv * kv.page_size * kv.head_dim * 2);
+    if (gi < npg && gi < kv.max_seq_pages && page >= 0 && page < kv.num_pages)
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(
+                       kv.pool + ((size_t)page * kv.n_layers + layer) * (slab / 2)),
+                   "r"(slab)
+                   : "memory");
+    return;
+  }
   const int row = blockIdx.y;
-  const int col = blockIdx.x * blockDim.x + threadIdx.x;
+  const int col = blockIdx.x * kQkvThreads + threadIdx.x;
   const int qcols = nq * dh;
   if (col >= pN) return;
   if (row >= M) {
-    if (col < qcols) write_qfrag(qfrag, row, col / dh, col % dh, 0.f);
+    if (col < qcols) write_qtile(qtile, row, col / dh, col % dh, 0.f, nq / nkv, tiles);
     return;
   }
   const float v = piece_sum(pieces, pN, piece_slots(pnb, (int)pU, pG, col), row, col);
   if (col < qcols) {
-    write_qfrag(qfrag, row, col / dh, col % dh, v);
+    write_qtile(qtile, row, col / dh, col % dh, v, nq / nkv, tiles);
     return;
   }
   if (*status & (SPEC_ST_TOKEN_RANGE | SPEC_ST_POOL_EMPTY | SPEC_ST_CTX_FULL)) return;
@@ -313,12 +334,13 @@ __global__ void qkv_post_kernel(const float* __restrict__ pieces, int pN, int pn
 }
 
 cudaError_t launch_qkv_post(const GemmPlan& p, const float* pieces, int M, int nq, int nkv, int dh,
-                            const KvView& kv, int layer, uint8_t* qfrag, const int32_t* status,
-                            cudaStream_t st, bool pdl) {
+                            const KvView& kv, int layer, uint8_t* qtile, int tiles,
+                            const int32_t* status, cudaStream_t st, bool pdl) {
   cudaLaunchAttribute attrs[2];
-  cudaLaunchConfig_t cfg = make_cfg(dim3((p.N + 255) / 256, 16), dim3(256), 0, st, pdl, attrs);
+  cudaLaunchConfig_t cfg = make_cfg(dim3((p.N + kQkvThreads - 1) / kQkvThreads, 16), dim3(kQkvThreads + 32), 0,
+                                    st, pdl, attrs);
   return cudaLaunchKernelEx(&cfg, qkv_post_kernel, pieces, p.N, p.nb, p.U, p.G, M, nq, nkv, dh, kv,
-                            layer, qfrag, status);
+                            layer, qtile, tiles, status);
 }
 
 // ---------------------------------------------------------------------------

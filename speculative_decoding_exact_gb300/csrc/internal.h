@@ -76,19 +76,23 @@ struct KvView {
   int num_pages, max_seq_pages, n_layers, n_kv, head_dim, page_size;
 };
 cudaError_t launch_qkv_post(const GemmPlan& p, const float* pieces, int M, int nq, int nkv,
-                            int dh, const KvView& kv, int layer, uint8_t* qfrag,
+                            int dh, const KvView& kv, int layer, uint8_t* qtile, int tiles,
                             const int32_t* status, cudaStream_t st, bool pdl);
 
 // verify attention: partials then merge (+ quantise for the O projection)
 struct AttnPlan {
   int nq = 0, nkv = 0, dh = 0, max_ctx = 0, chunk = 0, max_chunks = 0;
+  int group = 0, tiles = 0;     // query heads per kv head; 128-row MMA tiles per kv head
 };
 AttnPlan make_attn_plan(int nq, int nkv, int dh, int max_ctx);
 size_t attn_partial_floats(const AttnPlan& a, int max_rows);
-// Q fragments (bf16 hi/lo, nq * 8 KB) from fp32 q [M][nq][128]; rows >= M zero
-size_t qfrag_bytes(int nq);
-cudaError_t launch_q_to_frag(const float* q, int M, int nq, uint8_t* qfrag, cudaStream_t st, bool pdl);
-cudaError_t launch_attention(const AttnPlan& a, const KvView& kv, int layer, const uint8_t* qfrag,
+// Q tiles (bf16 hi/lo, 64 KB per (kv head, tile); layout at write_qtile) from
+// fp32 q [M][nq][128]; rows >= M zero.  Rows of heads past the group are never
+// written: the buffer is zeroed once at init.
+size_t qtile_bytes(const AttnPlan& a);
+cudaError_t launch_q_to_tile(const float* q, int M, const AttnPlan& a, uint8_t* qtile, cudaStream_t st,
+                             bool pdl);
+cudaError_t launch_attention(const AttnPlan& a, const KvView& kv, int layer, const uint8_t* qtile,
                              int M, float* part, float* out, uint8_t* act, int32_t* status,
                              cudaStream_t st, bool pdl);
 

@@ -546,62 +546,69 @@ attn_partial_kernel(const uint8_t* __restrict__ qtile, int M, int nq, int nkv, i
 // out = o / L.  Warp hh (one per head) computes M, the weights and L with
 // warp shuffles in a fixed butterfly order; o is summed in chunk order.  The
 // chunk count depends on the row's position only, so the result is the same
-// for every M.
+// for every M.  The o values of the first kMergeBatch chunks, the (max, sum)
+// pairs, the status and the length are all loaded in one round: the o loads
+// do not depend on the weights, and chunks past the row's count are loaded
+// but not used.
+constexpr int kMergeBatch = 24;
+
 __global__ void __launch_bounds__(256)
 attn_merge_kernel(const float* __restrict__ part, int M, int nq, int max_chunks, int chunk_keys,
                   const int32_t* seq_len, float* __restrict__ out, uint8_t* act, int32_t* status) {
   pdl_trigger();
   pdl_wait();
-  extern __shared__ float msh[];          // [2][max_chunks] weights, then [2][max_chunks] sums
+  extern __shared__ float msh[];          // [2][max_chunks] weights
   __shared__ float vals[256];
   __shared__ float lsum[2];
   const int b = blockIdx.x, row = blockIdx.y;
   const int H = nq * 128;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const size_t cstride = (size_t)nq * 16 * kPartStride;
+  const int hh = threadIdx.x >> 7, d = threadIdx.x & 127;
+  const float* pp = part + (((size_t)(2 * b + hh)) * 16 + row) * kPartStride + d;
+  float oc[kMergeBatch];
+#pragma unroll
+  for (int k = 0; k < kMergeBatch; ++k) oc[k] = k < max_chunks ? pp[k * cstride] : 0.f;
+  float2 ml[2];                            // warps 0, 1: (max, sum) of chunks lane, lane + 32
+  if (warp < 2) {
+    const float* st = part + (((size_t)(2 * b + warp)) * 16 + row) * kPartStride + 128;
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      const int c = lane + 32 * t;
+      ml[t] = c < max_chunks ? *reinterpret_cast<const float2*>(st + c * cstride) : make_float2(0.f, 0.f);
+    }
+  }
   const bool valid = row < M && !(*status & (SPEC_ST_TOKEN_RANGE | SPEC_ST_POOL_EMPTY | SPEC_ST_CTX_FULL));
   const int n_past = *seq_len - M;
-  const int nchunks = valid ? (n_past + row) / chunk_keys + 1 : 0;
-  const size_t cstride = (size_t)nq * 16 * 130;
+  const int nchunks = valid ? min((n_past + row) / chunk_keys + 1, max_chunks) : 0;
   if (warp < 2) {
-    const int hh = warp;
-    const float* st = part + (((size_t)(2 * b + hh)) * 16 + row) * 130;
-    // lane takes the chunks lane, lane + 32, ...: maxima first (kept in
-    // shared memory), then the weights and the weighted sums
-    // (max, sum) of chunk c are adjacent: one 8-byte load per chunk
+    const float* st = part + (((size_t)(2 * b + warp)) * 16 + row) * kPartStride + 128;
+    auto ml_of = [&](int c, int t) -> float2 {
+      return t == 0 ? ml[0] : (t == 1 ? ml[1] : *reinterpret_cast<const float2*>(st + c * cstride));
+    };
     float m = -INFINITY;
-    float* lsh = msh + 2 * max_chunks;      // the chunk sums, [2][max_chunks]
-    for (int c = lane; c < nchunks; c += 32) {
-      const float2 ml = *reinterpret_cast<const float2*>(st + c * cstride + 128);
-      msh[hh * max_chunks + c] = ml.x;
-      lsh[hh * max_chunks + c] = ml.y;
-      m = fmaxf(m, ml.x);
-    }
+#pragma unroll 1
+    for (int c = lane, t = 0; c < nchunks; c += 32, ++t) m = fmaxf(m, ml_of(c, t).x);
     m = warp_max(m);
     float L = 0.f;
-    for (int c = lane; c < nchunks; c += 32) {
-      const float mc = msh[hh * max_chunks + c];
-      const float w = (mc == -INFINITY) ? 0.f : exp2f(mc - m);
-      msh[hh * max_chunks + c] = w;
-      L += w * lsh[hh * max_chunks + c];
+#pragma unroll 1
+    for (int c = lane, t = 0; c < nchunks; c += 32, ++t) {
+      const float2 v = ml_of(c, t);
+      const float w = (v.x == -INFINITY) ? 0.f : exp2f(v.x - m);
+      msh[warp * max_chunks + c] = w;
+      L += w * v.y;
     }
     L = warp_sum(L);
-    if (lane == 0) lsum[hh] = L;
+    if (lane == 0) lsum[warp] = L;
   }
   __syncthreads();
   // weighted sum of the unnormalised outputs, in chunk order
-  const int hh = threadIdx.x >> 7, d = threadIdx.x & 127;
-  const float* pp = part + (((size_t)(2 * b + hh)) * 16 + row) * 130 + d;
   const float* w = msh + hh * max_chunks;
   float o = 0.f;
-  int c = 0;
-  for (; c + 8 <= nchunks; c += 8) {        // 8 loads in flight, then the sums in chunk order
-    float oc[8];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) oc[k] = pp[(c + k) * cstride];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) o += w[c + k] * oc[k];
-  }
-  for (; c < nchunks; ++c) o += w[c] * pp[c * cstride];
+  for (int k = 0; k < kMergeBatch; ++k)
+    if (k < nchunks) o += w[k] * oc[k];
+  for (int c = kMergeBatch; c < nchunks; ++c) o += w[c] * pp[c * cstride];
   const float res = valid ? o / lsum[hh] : 0.f;
   vals[threadIdx.x] = res;
   if (out && row < M) out[(size_t)row * H + 256 * b + threadIdx.x] = res;
@@ -648,7 +655,7 @@ cudaError_t launch_attention(const AttnPlan& a, const KvView& kv, int layer, con
   cudaLaunchConfig_t cfg2 = {};
   cfg2.gridDim = dim3(a.nq * 128 / 256, 16);
   cfg2.blockDim = dim3(256);
-  cfg2.dynamicSmemBytes = sizeof(float) * (4 * (size_t)a.max_chunks + 2);
+  cfg2.dynamicSmemBytes = sizeof(float) * 2 * (size_t)a.max_chunks;
   cfg2.stream = st;
   cfg2.attrs = attr;
   cfg2.numAttrs = pdl ? 1 : 0;

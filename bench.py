@@ -481,6 +481,60 @@ def run_gemm_shape(args):
     ctx.close()
 
 
+def run_attention(args):
+    """Time the verify attention alone: 16 rows, the full model's 52 query / 4 KV
+    heads of 128, KV context --ctx (the block of 16 rows appended after it),
+    through spec_attention on a one-layer paged KV pool.  The L2 is flushed
+    with a 256 MB write before every call (one layer's KV at 2k is 4.2 MB), and
+    each call is timed alone with CUDA events.  A small device footprint, used
+    as the ncu capture target of the attention kernels."""
+    import torch
+
+    from speculative_decoding_exact_gb300 import abi, runtime, synth
+    from speculative_decoding_exact_gb300 import build as b
+
+    b.build()
+    cfg = runtime.ModelConfig(**dict(synth.FULL, n_layers=1))
+    max_ctx = CTX + 64
+    ctx = runtime.Context(cfg, max_ctx=max_ctx)
+    pages = max_ctx // cfg.page_size
+    kv = runtime.DeviceKV(cfg, pages, pages)
+    kv.reset(ctx)
+    kv.extend(ctx, CTX + 16)
+    g = torch.Generator(device="cuda").manual_seed(5)
+    kv.pool.copy_(torch.randn(kv.pool.shape, generator=g, device="cuda").to(torch.bfloat16))
+    q = torch.from_numpy(synth.normal((16, cfg.n_q_heads * cfg.head_dim), 5, 1)).cuda()
+    out = torch.zeros((16, cfg.n_q_heads * cfg.head_dim), dtype=torch.float32, device="cuda")
+    flush = torch.empty(256 * 2**20 // 4, dtype=torch.float32, device="cuda")
+    kvs = kv.struct()
+
+    def call():
+        abi.check("spec_attention", abi.spec_attention(ctx.h, kvs, 0, q.data_ptr(), 16, out.data_ptr()))
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        call()
+    torch.cuda.synchronize()
+    total = 0.0
+    for _ in range(args.steps):
+        flush.zero_()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        call()
+        e1.record()
+        torch.cuda.synchronize()
+        total += e0.elapsed_time(e1)
+    us = total * 1000.0 / args.steps
+    kv_bytes = (CTX + 16) * cfg.n_kv_heads * 2 * cfg.head_dim * 2
+    print(json.dumps({"metric": "verify attention KV GB/s (16 rows, q tiles + partials + merge)",
+                      "value": kv_bytes / us / 1e3, "unit": "GB/s", "us_per_call": us,
+                      "config": {"ctx": CTX, "rows": 16, "n_q_heads": cfg.n_q_heads,
+                                 "n_kv_heads": cfg.n_kv_heads, "head_dim": cfg.head_dim},
+                      "kv_bytes": kv_bytes, "l2": "flushed (256 MB write) before every call"}))
+    ctx.close()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -489,6 +543,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--gemm-shape", default=None,
                     help="NxK: time one Q4_K GEMM shape instead of the verify step")
+    ap.add_argument("--attn", action="store_true",
+                    help="time the verify attention alone at context --ctx instead of the verify step")
     ap.add_argument("--ctx", type=int, default=2048,
                     help="KV context of the verify step (the long-context sweep uses 16384, 32768)")
     args = ap.parse_args()
@@ -498,6 +554,9 @@ def main():
     CTX = args.ctx
     if args.gemm_shape:
         run_gemm_shape(args)
+        return
+    if args.attn:
+        run_attention(args)
         return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

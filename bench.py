@@ -403,7 +403,7 @@ def run_gpu(args, rank, world):
         "metric": METRIC, "value": steps_per_s, "unit": "verify steps/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "int8xint4 dot on f16 tensor cores (exact ints), f32 combine", "data": "synthetic",
+        "dtype": "int8xuint4 dot (exact integers on e4m3 tcgen05 MMAs), f32 combine, bf16 KV", "data": "synthetic",
         "config": workload_config(cfg),
         "weight_gbs": wb * steps_per_s / world / 1e9,
         "weight_frac_of_hbm": {"measured": wb * steps_per_s / world / 1e9 / peak, "peak_gbs": peak,

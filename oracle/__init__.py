@@ -74,6 +74,13 @@ def lib():
         _lib.orc_float_to_bf16.restype = C.c_uint16
         _lib.orc_float_to_bf16.argtypes = [C.c_float]
         _lib.orc_rmsnorm.argtypes = [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_float, C.c_void_p]
+        _lib.orc_mt_next.restype = C.c_uint32
+        _lib.orc_mt_next.argtypes = [C.c_void_p]
+        _lib.orc_mt_seed.argtypes = [C.c_void_p, C.c_uint32]
+        _lib.orc_uniform_f32.restype = C.c_float
+        _lib.orc_uniform_f32.argtypes = [C.c_void_p]
+        _lib.orc_sample_accept.argtypes = [C.c_void_p, C.c_void_p, C.c_void_p, C.c_int, C.c_int,
+                                           C.c_void_p, C.c_void_p, C.c_void_p]
     return _lib
 
 
@@ -190,6 +197,52 @@ def accept(idx: np.ndarray, draft: np.ndarray, vocab: int):
     L, nxt = C.c_int32(), C.c_int32()
     st = lib().orc_accept(_p(idx), _p(draft), len(draft), int(vocab), C.byref(L), C.byref(nxt))
     return int(L.value), int(nxt.value), int(st)
+
+
+# ---------------------------------------------------------------------------
+# stochastic exact acceptance ([33] §33.2) and its MT19937 stream
+# ---------------------------------------------------------------------------
+MT_WORDS = 625        # 624 state words + the index of the next word
+
+
+def mt_seed(seed: int) -> np.ndarray:
+    st = np.zeros(MT_WORDS, dtype=np.uint32)
+    lib().orc_mt_seed(_p(st), int(seed) & 0xFFFFFFFF)
+    return st
+
+
+def mt_next(st: np.ndarray, n: int) -> np.ndarray:
+    """n raw 32-bit draws; st (a 625-word state) is advanced in place."""
+    out = np.empty(n, dtype=np.uint32)
+    for i in range(n):
+        out[i] = lib().orc_mt_next(_p(st))
+    return out
+
+
+def uniform_f32(st: np.ndarray) -> float:
+    return float(lib().orc_uniform_f32(_p(st)))
+
+
+def softmax_row(logits: np.ndarray) -> np.ndarray:
+    logits = np.ascontiguousarray(logits, dtype=np.float32)
+    p = np.empty_like(logits)
+    lib().orc_softmax_row(_p(logits), logits.shape[0], _p(p))
+    return p
+
+
+def sample_accept(logits: np.ndarray, q: np.ndarray, draft: np.ndarray, st: np.ndarray):
+    """(accepted, next, status, margin); st (625 words) is advanced in place.
+    logits fp32 [k+1][V], q fp32 [k][V], draft int32 [k]."""
+    logits = np.ascontiguousarray(logits, dtype=np.float32)
+    q = np.ascontiguousarray(q, dtype=np.float32)
+    draft = np.ascontiguousarray(draft, dtype=np.int32)
+    k = len(draft)
+    V = logits.shape[1]
+    assert logits.shape == (k + 1, V) and q.shape == (k, V) and st.dtype == np.uint32
+    res = np.zeros(2, dtype=np.int32)
+    margin = C.c_double(0.0)
+    rc = lib().orc_sample_accept(_p(logits), _p(q), _p(draft), k, V, _p(st), _p(res), C.byref(margin))
+    return int(res[0]), int(res[1]), int(rc), float(margin.value)
 
 
 # ---------------------------------------------------------------------------

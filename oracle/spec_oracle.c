@@ -273,6 +273,143 @@ int orc_accept(const int32_t* idx, const int32_t* draft, int k, int vocab,
 }
 
 /* ------------------------------------------------------------------------ */
+/* Stochastic exact acceptance ([33] §33.2, the general rule of which the     */
+/* greedy accept above is the one-hot case).                                 */
+/* ------------------------------------------------------------------------ */
+
+/* MT19937, from its published definition (Matsumoto & Nishimura 1998):
+ * degree n = 624, middle word m = 397, twist matrix a = 0x9908B0DF, tempering
+ * (u, s, b, t, c, l) = (11, 7, 0x9D2C5680, 15, 0xEFC60000, 18), seeding
+ * multiplier 1812433253.  The state is 625 words: the 624 state words and
+ * the index of the next word to temper (624 = twist first). */
+#define ORC_MT_N 624
+#define ORC_MT_M 397
+
+void orc_mt_seed(uint32_t* st, uint32_t seed) {
+    st[0] = seed;
+    for (uint32_t i = 1; i < ORC_MT_N; ++i)
+        st[i] = 1812433253u * (st[i - 1] ^ (st[i - 1] >> 30)) + i;
+    st[ORC_MT_N] = ORC_MT_N;
+}
+
+static void orc_mt_twist(uint32_t* st) {
+    for (int i = 0; i < ORC_MT_N; ++i) {
+        uint32_t x = (st[i] & 0x80000000u) | (st[(i + 1) % ORC_MT_N] & 0x7fffffffu);
+        uint32_t xa = x >> 1;
+        if (x & 1u) xa ^= 0x9908B0DFu;
+        st[i] = st[(i + ORC_MT_M) % ORC_MT_N] ^ xa;
+    }
+    st[ORC_MT_N] = 0;
+}
+
+uint32_t orc_mt_next(uint32_t* st) {
+    if (st[ORC_MT_N] >= ORC_MT_N) orc_mt_twist(st);
+    uint32_t y = st[st[ORC_MT_N]++];
+    y ^= y >> 11;
+    y ^= (y << 7) & 0x9D2C5680u;
+    y ^= (y << 15) & 0xEFC60000u;
+    y ^= y >> 18;
+    return y;
+}
+
+/* uniform in [0, 1): the top 24 bits of one draw, times 2^-24 (exact in
+ * binary32).  The pages name uniform_f32 without its conversion; this is the
+ * plainest one that uses every bit a binary32 in [0, 1) can hold. */
+float orc_uniform_f32(uint32_t* st) { return (float)(orc_mt_next(st) >> 8) * 0x1p-24f; }
+
+/* softmax of one logit row: p_x = exp(l_x - max) / sum, computed in fp64 and
+ * rounded to fp32 once (temperature 1) */
+void orc_softmax_row(const float* l, int V, float* p) {
+    double m = -INFINITY;
+    for (int x = 0; x < V; ++x)
+        if (l[x] > m) m = l[x];
+    double s = 0.0;
+    for (int x = 0; x < V; ++x) s += exp((double)l[x] - m);
+    for (int x = 0; x < V; ++x) p[x] = (float)(exp((double)l[x] - m) / s);
+}
+
+/* Draw one token from the distribution r over [0, V): one uniform u, then the
+ * tokens in index order with a running fp32 sum c; the first token with
+ * u < c.  If rounding leaves c <= u at the end, the last token with r > 0.
+ * (The pages walk a precomputed token order; index order is this reading.)
+ * *margin receives the distance of u from the nearest running-sum boundary
+ * around the chosen token. */
+static int32_t orc_sample_row(const float* r, int V, uint32_t* mt, double* margin) {
+    const float u = orc_uniform_f32(mt);
+    float c = 0.f, prev = 0.f;
+    int32_t last = -1;
+    for (int x = 0; x < V; ++x) {
+        if (r[x] > 0.f) last = x;
+        prev = c;
+        c += r[x];
+        if (u < c) {
+            double d0 = (double)u - prev, d1 = (double)c - u;
+            *margin = d0 < d1 ? d0 : d1;
+            return x;
+        }
+    }
+    *margin = (double)u - c;
+    return last;
+}
+
+/* The accept rule of [33] §33.2 over k drafts:
+ *   for i < k: x = draft[i], p = p_i(x), q = q_i(x),
+ *       a = 1 if q <= 0 else min(p / q, 1); one uniform u;
+ *       u <= a: accept and go on; otherwise stop: the next token is drawn from
+ *       max(p_i - q_i, 0) / total (from p_i itself when total <= 0);
+ *   all accepted: the next token is drawn from p_k.
+ * logits fp32 [k+1][V] (p = softmax, temperature 1); q fp32 [k][V] (the draft's
+ * distributions); mt the 625-word MT19937 state, advanced by the draws.
+ * res = {accepted, next}; *margin = the smallest distance of a uniform from
+ * the threshold it was compared with (for tests that skip knife-edge draws).
+ * Returns ORC_ST_TOKEN_RANGE for a draft token outside [0, V). */
+int orc_sample_accept(const float* logits, const float* q, const int32_t* draft, int k, int V,
+                      uint32_t* mt, int32_t* res, double* margin) {
+    for (int i = 0; i < k; ++i)
+        if (draft[i] < 0 || draft[i] >= V) return ORC_ST_TOKEN_RANGE;
+    float* p = (float*)malloc(sizeof(float) * (size_t)V);
+    float* r = (float*)malloc(sizeof(float) * (size_t)V);
+    double mg = INFINITY, m1;
+    int L = k;
+    for (int i = 0; i < k; ++i) {
+        orc_softmax_row(logits + (size_t)i * V, V, p);
+        const float qx = q[(size_t)i * V + draft[i]];
+        const float px = p[draft[i]];
+        const float a = qx <= 0.f ? 1.f : fminf(px / qx, 1.f);
+        const float u = orc_uniform_f32(mt);
+        if (fabs((double)u - a) < mg) mg = fabs((double)u - a);
+        if (u <= a) continue;
+        L = i;
+        break;
+    }
+    int32_t next;
+    if (L < k) {
+        const float* qi = q + (size_t)L * V;
+        float total = 0.f;
+        for (int x = 0; x < V; ++x) {
+            r[x] = fmaxf(p[x] - qi[x], 0.f);
+            total += r[x];
+        }
+        if (total <= 0.f) {
+            memcpy(r, p, sizeof(float) * (size_t)V);
+        } else {
+            for (int x = 0; x < V; ++x) r[x] = r[x] / total;
+        }
+        next = orc_sample_row(r, V, mt, &m1);
+    } else {
+        orc_softmax_row(logits + (size_t)k * V, V, p);
+        next = orc_sample_row(p, V, mt, &m1);
+    }
+    if (m1 < mg) mg = m1;
+    free(p);
+    free(r);
+    res[0] = L;
+    res[1] = next;
+    if (margin) *margin = mg;
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Paged KV metadata ([8] §8.6 item 4: checkpoint = metadata rewind).         */
 /* Free pages form a LIFO stack, initialised descending so that pops yield    */
 /* ids 0, 1, 2, ...; pages are mapped in ascending logical order; a rollback  */

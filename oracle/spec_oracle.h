@@ -97,6 +97,13 @@ void orc_attention(const orc_cfg* c, const orc_kv* kv, int layer, const float* q
 /* one transformer block on M rows at positions n_past.. (K/V appended) */
 int orc_block(const orc_cfg* c, const orc_weights* w, orc_kv* kv, int layer,
               const float* x_in, int M, int n_past, float* x_out);
+/* stochastic exact acceptance ([33] §33.2): MT19937 state of 625 words */
+void     orc_mt_seed(uint32_t* st, uint32_t seed);
+uint32_t orc_mt_next(uint32_t* st);
+float    orc_uniform_f32(uint32_t* st);
+void     orc_softmax_row(const float* l, int V, float* p);
+int      orc_sample_accept(const float* logits, const float* q, const int32_t* draft, int k, int V,
+                           uint32_t* mt, int32_t* res, double* margin);
 /* forward of M rows at positions seq_len..: reserves pages, appends K/V, sets
  * seq_len += M; writes argmax idx [M], logits [M][V] (nullable) and the
  * residual taps [(n_layers+1)][M][H] (nullable) */

@@ -454,3 +454,97 @@ def test_verify_step_rejects_bad_k_and_restores_on_device_errors():
     res, _, _, _ = oracle.verify_step(cfg, w, kv, h_nan, np.array([1, 2, 3], dtype=np.int32))
     assert res[2] & oracle.ST_NONFINITE and res[3] == 5
     assert all(np.array_equal(a, b) for a, b in zip(snap[1:], kv.committed()[1:]))
+
+
+# ---------------------------------------------------------------------------
+# stochastic exact acceptance ([33] §33.2) and its MT19937 stream
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("seed", [5489, 0, 1, 123456789, 0xFFFFFFFF])
+def test_mt19937_matches_numpy_legacy_seeding(seed):
+    # numpy's MT19937 with the classic integer seeding is an independent
+    # implementation of the same published generator; 2000 draws span 4 twists
+    st = oracle.mt_seed(seed)
+    bg = np.random.MT19937(0)
+    bg._legacy_seeding(seed)
+    assert np.array_equal(oracle.mt_next(st, 2000), bg.random_raw(2000).astype(np.uint32))
+
+
+def test_mt19937_published_10000th_output():
+    # the 10000th draw of the generator seeded with 5489 is 4123659995
+    # (the value library specifications use to pin MT19937)
+    assert int(oracle.mt_next(oracle.mt_seed(5489), 10000)[-1]) == 4123659995
+
+
+def test_uniform_f32_is_top_24_bits():
+    st = oracle.mt_seed(77)
+    raw = oracle.mt_next(oracle.mt_seed(77), 50)
+    u = np.array([oracle.uniform_f32(st) for _ in range(50)], dtype=np.float32)
+    assert np.array_equal(u, ((raw >> 8).astype(np.float64) * 2.0**-24).astype(np.float32))
+    assert np.all((u >= 0) & (u < 1))
+
+
+def _one_hot_logits(idx, V):
+    lg = np.full((len(idx), V), -1.0e4, dtype=np.float32)
+    lg[np.arange(len(idx)), idx] = 0.0            # exp(-1e4) = 0: p is one-hot exactly
+    return lg
+
+
+@pytest.mark.parametrize("k", [3, 7, 15])
+def test_sample_accept_reduces_to_greedy_for_one_hot(k):
+    # p one-hot at the target argmax, q one-hot at the draft: p/q = 1 on a
+    # match and 0 on a mismatch, and the residual is one-hot at the argmax
+    rng = np.random.default_rng(k)
+    V = 64
+    for trial in range(40):
+        idx = rng.integers(0, V, k + 1).astype(np.int32)
+        L_t = int(rng.integers(0, k + 1))
+        draft = idx[:k].copy()
+        if L_t < k:
+            draft[L_t] = (idx[L_t] + 1 + int(rng.integers(0, V - 1))) % V
+        q = np.zeros((k, V), dtype=np.float32)
+        q[np.arange(k), draft] = 1.0
+        st = oracle.mt_seed(1000 + trial)
+        L, nxt, rc, margin = oracle.sample_accept(_one_hot_logits(idx, V), q, draft, st)
+        gL, gnext, grc = oracle.accept(idx, draft, V)
+        assert rc == 0 and grc == 0
+        if margin > 0:                             # u == 0 would accept a p = 0 draft (rule: u <= a)
+            assert (L, nxt) == (gL, gnext) == (L_t, idx[L_t])
+
+
+def test_sample_accept_guards_token_range():
+    V, k = 32, 3
+    lg = np.zeros((k + 1, V), dtype=np.float32)
+    q = np.full((k, V), 1.0 / V, dtype=np.float32)
+    st = oracle.mt_seed(3)
+    before = st.copy()
+    _, _, rc, _ = oracle.sample_accept(lg, q, np.array([1, V, 2], dtype=np.int32), st)
+    assert rc == oracle.ST_TOKEN_RANGE
+    assert np.array_equal(st, before)              # no draw before the guard
+
+
+def test_sample_accept_first_token_follows_the_target():
+    # the rule's invariant: whatever q is, the first emitted token (the draft
+    # if accepted, else the residual draw) is distributed as p_0
+    rng = np.random.default_rng(11)
+    V, N = 12, 24000
+    lg0 = rng.normal(0, 1.5, V).astype(np.float32)
+    p0 = oracle.softmax_row(lg0)
+    q0 = rng.dirichlet(np.ones(V) * 0.7).astype(np.float32)
+    logits = np.stack([lg0, rng.normal(0, 1, V).astype(np.float32)])
+    st = oracle.mt_seed(2024)
+    cq = np.cumsum(q0.astype(np.float64))
+    counts = np.zeros(V)
+    acc = 0
+    for _ in range(N):
+        x0 = int(min(np.searchsorted(cq, rng.random() * cq[-1], side="right"), V - 1))
+        L, nxt, rc, _ = oracle.sample_accept(logits, q0[None, :], np.array([x0], dtype=np.int32), st)
+        assert rc == 0
+        counts[x0 if L == 1 else nxt] += 1
+        acc += L
+    expect = N * p0.astype(np.float64)
+    chi2 = float(np.sum((counts - expect) ** 2 / expect))
+    # 11 degrees of freedom: P(chi2 > 35) < 3e-4
+    assert chi2 < 35.0, (chi2, counts, expect)
+    # acceptance probability is sum_x min(p_x, q_x)
+    a = float(np.minimum(p0, q0).sum())
+    assert abs(acc / N - a) < 5 * math.sqrt(a * (1 - a) / N)

@@ -331,6 +331,48 @@ SPEC_API int spec_attention(spec_ctx* ctx, const spec_kv* kv, int layer,
 SPEC_API int spec_accept(spec_ctx* ctx, const int32_t* idx, const int32_t* draft, int k,
                 spec_kv* kv, spec_result* res);
 
+/* ---- Stochastic exact acceptance (Ch. 33 §33.2; the rule of which
+ * spec_accept is the one-hot case).
+ *
+ * For i < k: x = draft[i], p = p_i(x), q = q_i(x), a = 1 if q <= 0 else
+ * min(p/q, 1); one uniform u; u <= a accepts and goes on.  On the first
+ * rejection the next token is drawn from max(p_i - q_i, 0) renormalised (from
+ * p_i itself when that is all zero); when all k are accepted, from p_k.
+ * p_i = softmax of the target logits of row i (temperature 1).
+ *
+ * Uniforms come from a caller-owned MT19937 stream (Matsumoto & Nishimura
+ * 1998), one per attempted draft, then one for the final draw, in that
+ * order; uniform = (draw >> 8) * 2^-24.  A draw walks the tokens in index
+ * order and returns the first whose running sum of the renormalised weights
+ * exceeds u (the last token of positive weight if rounding leaves none).
+ * On a device error (a draft token outside [0, V), non-finite logits) no
+ * uniform is drawn; the result is as in spec_verify_step. */
+#define SPEC_MT_WORDS 625   /* 624 state words + the index of the next word */
+
+/* Seed an MT19937 state in HOST memory (state_host: SPEC_MT_WORDS words);
+ * the caller copies it to the device once and keeps it there. */
+SPEC_API int spec_mt_seed(uint32_t* state_host, uint32_t seed);
+
+/* The decision alone, from logits that are already computed.
+ *   logits DEVICE fp32 [k+1][V]   target logits of rows 0..k
+ *   q      DEVICE fp32 [k][V]     the draft's distribution at positions 0..k-1
+ *   draft  DEVICE int32 [k], 1 <= k <= 15
+ *   mt     DEVICE uint32 [SPEC_MT_WORDS], advanced by the draws
+ *   kv     as in spec_accept (NULL: no rollback)
+ * Writes res (DEVICE); next_token is the drawn token. */
+SPEC_API int spec_sample_accept(spec_ctx* ctx, const float* logits, const float* q,
+                                const int32_t* draft, int k, uint32_t* mt, spec_kv* kv,
+                                spec_result* res);
+
+/* The verify step with the sampled decision: as spec_verify_step_ex, with
+ * q (DEVICE fp32 [k][V]) and mt (DEVICE, SPEC_MT_WORDS words) as above.  The
+ * step keeps the M rows' logits in its workspace (8 MB at V = 131072);
+ * taps->logits and taps->argmax are filled when given. */
+SPEC_API int spec_verify_step_sampled(spec_ctx* ctx, const spec_weights* w, spec_kv* kv,
+                                      const float* hidden, const int32_t* draft, const float* q,
+                                      int k, uint32_t* mt, spec_result* res,
+                                      const spec_taps* taps);
+
 #ifdef __cplusplus
 }
 #endif

@@ -74,7 +74,13 @@ _SIGS = {
     "spec_profile_gemms": (I, [P, I]),
     "spec_profile_read": (I, [P, C.POINTER(C.c_float), C.POINTER(C.c_int)]),
     "spec_gemm_q4k_noalloc": (I, [P, I, I, P, I, P, P]),
+    "spec_mt_seed": (I, [P, C.c_uint32]),
+    "spec_sample_accept": (I, [P, P, P, P, I, P, C.POINTER(spec_kv), P]),
+    "spec_verify_step_sampled": (I, [P, C.POINTER(spec_weights), C.POINTER(spec_kv), P, P, P, I, P, P,
+                                     C.POINTER(spec_taps)]),
 }
+
+MT_WORDS = 625
 
 _lib = None
 
@@ -190,6 +196,20 @@ def spec_lm_head_argmax(ctx, w_head, final_norm, x, M, idx, logits) -> int:
 
 def spec_attention(ctx, kv, layer, q, M, out) -> int:
     return _call("spec_attention", ctx, C.byref(kv), layer, P(q), M, P(out))
+
+
+def spec_mt_seed(state_host, seed: int) -> int:
+    return _call("spec_mt_seed", P(state_host), int(seed) & 0xFFFFFFFF)
+
+
+def spec_sample_accept(ctx, logits, q, draft, k, mt, kv: spec_kv | None, res) -> int:
+    return _call("spec_sample_accept", ctx, P(logits), P(q), P(draft), k, P(mt),
+                 C.byref(kv) if kv is not None else None, P(res))
+
+
+def spec_verify_step_sampled(ctx, w, kv, hidden, draft, q, k, mt, res, taps: spec_taps | None) -> int:
+    return _call("spec_verify_step_sampled", ctx, C.byref(w), C.byref(kv), P(hidden), P(draft), P(q), k,
+                 P(mt), P(res), C.byref(taps) if taps is not None else None)
 
 
 def spec_accept(ctx, idx, draft, k, kv: spec_kv | None, res) -> int:

@@ -36,6 +36,8 @@ struct spec_ctx {
   int32_t* head_idx = nullptr;
   int head_parts = 0;
   int32_t* status = nullptr;     // device status word
+  float* logits_ws = nullptr;    // [16][V] target logits of a sampled step
+  float2* sstats = nullptr;      // [16] row max and sum of exp of a sampled step
   int32_t* step_state = nullptr; // [2]
   int32_t* idx_buf = nullptr;    // [16]
   float* hidden_dev = nullptr;   // host-buffer entry point staging
@@ -183,6 +185,8 @@ int spec_verify_init(const spec_config* cfg, void* cuda_stream, spec_ctx** out) 
   rc |= dalloc(&c->head_val, (size_t)c->head_parts * 16);
   rc |= dalloc(&c->head_idx, (size_t)c->head_parts * 16);
   rc |= dalloc(&c->status, 4);
+  rc |= dalloc(&c->logits_ws, (size_t)16 * V);
+  rc |= dalloc(&c->sstats, 16);
   rc |= dalloc(&c->step_state, 4);
   rc |= dalloc(&c->idx_buf, 16);
   rc |= dalloc(&c->hidden_dev, (size_t)16 * H);
@@ -216,6 +220,8 @@ void spec_verify_destroy(spec_ctx* c) {
   cudaFree(c->pieces);
   cudaFree(c->resid);
   cudaFree(c->qtile);
+  cudaFree(c->logits_ws);
+  cudaFree(c->sstats);
   for (auto& gc : c->graphs)
     if (gc.exec) cudaGraphExecDestroy(gc.exec);
   cudaFree(c->attn_part);
@@ -409,8 +415,15 @@ static int check_weights(const spec_ctx* c, const spec_weights* w) {
   return SPEC_OK;
 }
 
+// the draft's distributions and the MT19937 state of a sampled step
+struct SampleArgs {
+  const float* q;
+  uint32_t* mt;
+};
+
 static int enqueue_step(spec_ctx* c, const spec_weights* w, spec_kv* kv, const float* hidden,
-                        const int32_t* draft, int k, spec_result* res, const spec_taps* taps) {
+                        const int32_t* draft, int k, spec_result* res, const spec_taps* taps,
+                        const SampleArgs* sa) {
   const int M = k + 1;
 
   const spec_config& g = c->cfg;
@@ -462,11 +475,28 @@ static int enqueue_step(spec_ctx* c, const spec_weights* w, spec_kv* kv, const f
                                cudaMemcpyDeviceToDevice, st));
   }
   SPEC_TRY(gemm(c->p_head, w->w_head)); ++n;
-  SPEC_TRY(launch_head_argmax(c->p_head, c->pieces, M, taps ? taps->logits : nullptr, c->head_val,
-                              c->head_idx, c->status, st, true)); ++n;
-  SPEC_TRY(launch_accept(nullptr, c->head_val, c->head_idx, c->head_parts, draft, k, g.vocab, &kvv,
-                         c->step_state, c->status, reinterpret_cast<int32_t*>(res),
-                         taps ? taps->argmax : nullptr, st, true)); ++n;
+  if (sa) {
+    // sampled acceptance: the logits of every row, their normalizers, then
+    // the decisions on the caller's MT19937 stream
+    SPEC_TRY(launch_head_argmax(c->p_head, c->pieces, M, c->logits_ws, c->head_val, c->head_idx,
+                                c->status, st, true)); ++n;
+    if (taps && taps->argmax) {
+      SPEC_TRY(launch_argmax_final(c->head_val, c->head_idx, c->head_parts, M, taps->argmax, st, true));
+      ++n;
+    }
+    if (taps && taps->logits)
+      SPEC_TRY(cudaMemcpyAsync(taps->logits, c->logits_ws, sizeof(float) * (size_t)M * g.vocab,
+                               cudaMemcpyDeviceToDevice, st));
+    SPEC_TRY(launch_sample_accept(c->logits_ws, sa->q, draft, k, g.vocab, c->sstats, sa->mt, &kvv,
+                                  c->step_state, c->status, reinterpret_cast<int32_t*>(res), st, true));
+    n += 2;
+  } else {
+    SPEC_TRY(launch_head_argmax(c->p_head, c->pieces, M, taps ? taps->logits : nullptr, c->head_val,
+                                c->head_idx, c->status, st, true)); ++n;
+    SPEC_TRY(launch_accept(nullptr, c->head_val, c->head_idx, c->head_parts, draft, k, g.vocab, &kvv,
+                           c->step_state, c->status, reinterpret_cast<int32_t*>(res),
+                           taps ? taps->argmax : nullptr, st, true)); ++n;
+  }
   c->last_launches = n;
   return SPEC_OK;
 }
@@ -477,9 +507,12 @@ static uint64_t mix(uint64_t h, uint64_t v) {
 }
 
 static uint64_t step_key(const spec_ctx* c, const spec_weights* w, const spec_kv* kv,
-                         const float* hidden, const int32_t* draft, int k, const spec_result* res) {
+                         const float* hidden, const int32_t* draft, int k, const spec_result* res,
+                         const SampleArgs* sa) {
   uint64_t h = 0x1234567ull;
   auto P = [](const void* p) { return (uint64_t)(uintptr_t)p; };
+  h = mix(h, sa ? 0x5a ^ P(sa->q) : 0x9e);
+  h = mix(h, sa ? P(sa->mt) : 0);
   h = mix(h, P(hidden));
   h = mix(h, P(draft));
   h = mix(h, P(res));
@@ -504,8 +537,9 @@ static uint64_t step_key(const spec_ctx* c, const spec_weights* w, const spec_kv
   return h | 1;
 }
 
-int spec_verify_step_ex(spec_ctx* c, const spec_weights* w, spec_kv* kv, const float* hidden,
-                        const int32_t* draft, int k, spec_result* res, const spec_taps* taps) {
+static int run_step(spec_ctx* c, const spec_weights* w, spec_kv* kv, const float* hidden,
+                    const int32_t* draft, int k, spec_result* res, const spec_taps* taps,
+                    const SampleArgs* sa) {
   if (!c || !hidden || !draft || !res) return SPEC_ENULL;
   if (k != 3 && k != 7 && k != 15) return SPEC_EVERIFYLEN;
   const int M = k + 1;
@@ -521,9 +555,9 @@ int spec_verify_step_ex(spec_ctx* c, const spec_weights* w, spec_kv* kv, const f
   // Steps with taps, with GEMM profiling, or on the legacy default stream
   // (which cannot be captured) are enqueued directly.
   if (taps || c->profile || !c->use_graphs || c->stream == nullptr)
-    return enqueue_step(c, w, kv, hidden, draft, k, res, taps);
+    return enqueue_step(c, w, kv, hidden, draft, k, res, taps, sa);
 
-  const uint64_t key = step_key(c, w, kv, hidden, draft, k, res);
+  const uint64_t key = step_key(c, w, kv, hidden, draft, k, res, sa);
   spec_ctx::GraphEntry* hit = nullptr;
   for (auto& gc : c->graphs)
     if (gc.exec && gc.key == key) hit = &gc;
@@ -538,7 +572,7 @@ int spec_verify_step_ex(spec_ctx* c, const spec_weights* w, spec_kv* kv, const f
     }
     cudaGraph_t graph = nullptr;
     SPEC_TRY(cudaStreamBeginCapture(c->stream, cudaStreamCaptureModeThreadLocal));
-    rc = enqueue_step(c, w, kv, hidden, draft, k, res, nullptr);
+    rc = enqueue_step(c, w, kv, hidden, draft, k, res, nullptr, sa);
     cudaError_t e = cudaStreamEndCapture(c->stream, &graph);
     if (rc != SPEC_OK) {
       if (graph) cudaGraphDestroy(graph);
@@ -560,9 +594,50 @@ int spec_verify_step_ex(spec_ctx* c, const spec_weights* w, spec_kv* kv, const f
   return SPEC_OK;
 }
 
+int spec_verify_step_ex(spec_ctx* c, const spec_weights* w, spec_kv* kv, const float* hidden,
+                        const int32_t* draft, int k, spec_result* res, const spec_taps* taps) {
+  return run_step(c, w, kv, hidden, draft, k, res, taps, nullptr);
+}
+
 int spec_verify_step(spec_ctx* c, const spec_weights* w, spec_kv* kv, const float* hidden,
                      const int32_t* draft, int k, spec_result* res) {
-  return spec_verify_step_ex(c, w, kv, hidden, draft, k, res, nullptr);
+  return run_step(c, w, kv, hidden, draft, k, res, nullptr, nullptr);
+}
+
+int spec_verify_step_sampled(spec_ctx* c, const spec_weights* w, spec_kv* kv, const float* hidden,
+                             const int32_t* draft, const float* q, int k, uint32_t* mt,
+                             spec_result* res, const spec_taps* taps) {
+  if (!q || !mt) return SPEC_ENULL;
+  if (!aligned(q) || !aligned(mt)) return SPEC_EALIGN;
+  const SampleArgs sa{q, mt};
+  return run_step(c, w, kv, hidden, draft, k, res, taps, &sa);
+}
+
+// MT19937 seeding (Matsumoto & Nishimura 1998): word 0 = seed, word i =
+// 1812433253 * (w[i-1] ^ (w[i-1] >> 30)) + i; word 624 = 624 (regenerate first)
+int spec_mt_seed(uint32_t* state_host, uint32_t seed) {
+  if (!state_host) return SPEC_ENULL;
+  state_host[0] = seed;
+  for (uint32_t i = 1; i < 624; ++i)
+    state_host[i] = 1812433253u * (state_host[i - 1] ^ (state_host[i - 1] >> 30)) + i;
+  state_host[624] = 624;
+  return SPEC_OK;
+}
+
+int spec_sample_accept(spec_ctx* c, const float* logits, const float* q, const int32_t* draft, int k,
+                       uint32_t* mt, spec_kv* kv, spec_result* res) {
+  if (!c || !logits || !q || !draft || !mt || !res) return SPEC_ENULL;
+  if (k < 1 || k > 15) return SPEC_EVERIFYLEN;
+  if (!aligned(logits) || !aligned(q) || !aligned(mt)) return SPEC_EALIGN;
+  if (kv) {
+    int rc = check_kv(kv);
+    if (rc) return rc;
+  }
+  KvView v;
+  if (kv) v = view_of(c, kv);
+  return cuda_code(launch_sample_accept(logits, q, draft, k, c->cfg.vocab, c->sstats, mt, kv ? &v : nullptr,
+                                        nullptr, c->status, reinterpret_cast<int32_t*>(res), c->stream,
+                                        false));
 }
 
 int spec_verify_step_host(spec_ctx* c, const spec_weights* w, spec_kv* kv, const float* hidden_host,

@@ -13,6 +13,7 @@
 #include "common.cuh"
 #include "internal.h"
 #include "quant.cuh"
+#include "kvmeta.cuh"
 
 namespace spec {
 
@@ -524,21 +525,6 @@ cudaError_t launch_kv_reserve(const KvView& kv, int n, int commit, const int32_t
   cudaLaunchConfig_t cfg = make_cfg(dim3(1), dim3(32), 0, st, pdl, attrs);
   return cudaLaunchKernelEx(&cfg, kv_reserve_kernel, kv, n, commit, draft, k, vocab, status,
                             step_state);
-}
-
-__device__ void kv_rollback_dev(const KvView& kv, int new_len) {
-  const int len = *kv.seq_len;
-  const int hi = (len + kv.page_size - 1) / kv.page_size;
-  const int lo = (new_len + kv.page_size - 1) / kv.page_size;
-  for (int p = hi - 1; p >= lo; --p) {
-    const int id = kv.page_table[p];
-    if (id >= 0 && *kv.free_top < kv.num_pages) {
-      kv.free_stack[*kv.free_top] = id;
-      *kv.free_top += 1;
-      kv.page_table[p] = -1;
-    }
-  }
-  *kv.seq_len = new_len;
 }
 
 __global__ void kv_rollback_kernel(KvView kv, int new_len, int32_t* status) {

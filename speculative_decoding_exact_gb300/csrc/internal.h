@@ -96,6 +96,14 @@ cudaError_t launch_attention(const AttnPlan& a, const KvView& kv, int layer, con
                              int M, float* part, float* out, uint8_t* act, int32_t* status,
                              cudaStream_t st, bool pdl);
 
+// stochastic exact acceptance: row normalizers (stats fp32x2 [k+1]: max and
+// sum of exp) then the decisions, the final draw and the rollback; mt is the
+// 625-word MT19937 state (DEVICE), advanced by the draws
+cudaError_t launch_sample_accept(const float* logits, const float* q, const int32_t* draft, int k,
+                                 int V, float2* stats, uint32_t* mt, const KvView* kv,
+                                 const int32_t* step_state, int32_t* status, int32_t* res,
+                                 cudaStream_t st, bool pdl);
+
 // LM head argmax over the head GEMM pieces: per-(CTA,row) partial (value, index)
 int head_argmax_blocks(int V);
 cudaError_t launch_head_argmax(const GemmPlan& p, const float* pieces, int M, float* logits,

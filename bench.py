@@ -283,10 +283,15 @@ def committed_traffic():
         return None
 
 
-def run_gpu(args, rank, world):
+def setup_model(rank):
+    """The full synthetic model on this rank's GPU: random Q4_K weights of the
+    52-block architecture + head, a paged KV filled to CTX with random bf16,
+    16 hidden rows and 15 draft tokens.  Returns a namespace of the pieces."""
+    import types
+
     import torch
 
-    from speculative_decoding_exact_gb300 import abi, runtime, synth
+    from speculative_decoding_exact_gb300 import runtime, synth
     from speculative_decoding_exact_gb300 import build as b
 
     b.build()
@@ -309,16 +314,28 @@ def run_gpu(args, rank, world):
     kv = runtime.DeviceKV(cfg, pages, pages)
     kv.reset(ctx)
     kv.extend(ctx, CTX)
-    nkv = cfg.n_kv_heads * cfg.head_dim
     g = torch.Generator(device="cuda").manual_seed(1234 + rank)
     with torch.cuda.stream(stream):
         kv.pool.copy_(torch.randn(kv.pool.shape, generator=g, device="cuda").to(torch.bfloat16))
     hidden = torch.from_numpy(synth.normal((ROWS, cfg.hidden), rank, 5)).cuda()
     draft = torch.from_numpy(synth.tokens(K_DRAFT, cfg.vocab, rank, 6)).cuda()
     res = torch.zeros(4, dtype=torch.int32, device="cuda")
-    ws, ks = dw.struct(), kv.struct()
     torch.cuda.synchronize()
-    setup_s = time.perf_counter() - t_setup
+    return types.SimpleNamespace(cfg=cfg, ctx=ctx, stream=stream, dw=dw, kv=kv, hidden=hidden, draft=draft,
+                                 res=res, ws=dw.struct(), ks=kv.struct(), local=local,
+                                 setup_s=time.perf_counter() - t_setup)
+
+
+def run_gpu(args, rank, world):
+    import torch
+
+    from speculative_decoding_exact_gb300 import abi, runtime, synth
+    from speculative_decoding_exact_gb300 import build as b
+
+    mdl = setup_model(rank)
+    cfg, ctx, stream, local = mdl.cfg, mdl.ctx, mdl.stream, mdl.local
+    hidden, draft, res, ws, ks = mdl.hidden, mdl.draft, mdl.res, mdl.ws, mdl.ks
+    setup_s = mdl.setup_s
 
     def step():
         rc = abi.spec_verify_step(ctx.h, ws, ks, hidden.data_ptr(), draft.data_ptr(), K_DRAFT,
@@ -481,6 +498,151 @@ def run_gemm_shape(args):
     ctx.close()
 
 
+def _time_steps(torch, stream, step, warmup, steps):
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def run_sampled(args):
+    """The verify step with the sampled decision (Ch. 33 §33.2) on the full
+    model at context --ctx: q = the draft's distributions (softmax of random
+    logits, 15 x V, on the device), the MT19937 state on the device.  One JSON
+    line with steps/s next to the greedy step's, timed the same way."""
+    import torch
+
+    from speculative_decoding_exact_gb300 import abi
+
+    mdl = setup_model(0)
+    cfg, ctx, stream = mdl.cfg, mdl.ctx, mdl.stream
+    g = torch.Generator(device="cuda").manual_seed(77)
+    q = torch.softmax(torch.randn((K_DRAFT, cfg.vocab), generator=g, device="cuda") * 3.0, dim=1).contiguous()
+    st = np.zeros(abi.MT_WORDS, dtype=np.uint32)
+    abi.check("spec_mt_seed", abi.spec_mt_seed(st.ctypes.data, 5489))
+    mt = torch.from_numpy(st.view(np.int32).copy()).cuda()
+    hist = torch.zeros((args.steps, 4), dtype=torch.int32, device="cuda")
+    it = [0]
+
+    def sampled():
+        abi.check("spec_verify_step_sampled",
+                  abi.spec_verify_step_sampled(ctx.h, mdl.ws, mdl.ks, mdl.hidden.data_ptr(), mdl.draft.data_ptr(),
+                                               q.data_ptr(), K_DRAFT, mt.data_ptr(), mdl.res.data_ptr(), None))
+        hist[it[0] % args.steps].copy_(mdl.res)
+        it[0] += 1
+        abi.check("spec_kv_rollback", abi.spec_kv_rollback(ctx.h, mdl.ks, CTX))
+
+    def greedy():
+        abi.check("spec_verify_step", abi.spec_verify_step(ctx.h, mdl.ws, mdl.ks, mdl.hidden.data_ptr(),
+                                                           mdl.draft.data_ptr(), K_DRAFT, mdl.res.data_ptr()))
+        abi.check("spec_kv_rollback", abi.spec_kv_rollback(ctx.h, mdl.ks, CTX))
+
+    ms_s = _time_steps(torch, stream, sampled, args.warmup, args.steps)
+    h = hist.cpu().numpy()
+    assert np.all(h[:, 2] == 0), "sampled step status"
+    ms_g = _time_steps(torch, stream, greedy, args.warmup, args.steps)
+    print(json.dumps({"metric": "verify steps/s, sampled acceptance (Ch. 33 section 33.2)",
+                      "value": 1000.0 / ms_s, "unit": "verify steps/s", "ms_per_step": ms_s,
+                      "greedy_steps_per_s": 1000.0 / ms_g, "sampled_overhead_us": (ms_s - ms_g) * 1e3,
+                      "mean_accepted": float(h[:, 0].mean()), "steps": args.steps, "warmup": args.warmup,
+                      "config": dict(workload_config(cfg), draft_q="softmax(3 N(0,1)) per position",
+                                     rng="MT19937 seed 5489 on the device")}), flush=True)
+    ctx.close()
+
+
+def run_accept_profile(args):
+    """Verify steps at context --ctx with drafts planted so that the accepted
+    length L follows a target mean (each position accepted with probability
+    a, a solved from E[min(Geom, 15)] = mean), plus an all-accepted run; one
+    JSON line per profile with steps/s and accepted tokens/s = steps/s x
+    mean(L + 1), next to the draft front projection (Q4_K 33,280 -> 6,656)
+    timed at M = round(mean L) + 1 and M = 16."""
+    import torch
+
+    from speculative_decoding_exact_gb300 import abi, runtime, synth
+
+    mdl = setup_model(0)
+    cfg, ctx, stream = mdl.cfg, mdl.ctx, mdl.stream
+    V = cfg.vocab
+    # the target argmax of every row (the same every step: fixed rows, rolled-back KV)
+    am = torch.zeros(ROWS, dtype=torch.int32, device="cuda")
+    taps = abi.spec_taps(None, am.data_ptr(), None)
+    abi.check("spec_verify_step_ex", abi.spec_verify_step_ex(ctx.h, mdl.ws, mdl.ks, mdl.hidden.data_ptr(),
+                                                             mdl.draft.data_ptr(), K_DRAFT, mdl.res.data_ptr(),
+                                                             taps))
+    abi.check("spec_kv_rollback", abi.spec_kv_rollback(ctx.h, mdl.ks, CTX))
+    torch.cuda.synchronize()
+    idx = am.cpu().numpy()
+
+    def alpha_for(mean):
+        lo, hi = 0.0, 1.0
+        for _ in range(60):
+            a = 0.5 * (lo + hi)
+            e = sum(a ** i for i in range(1, K_DRAFT + 1))
+            lo, hi = (a, hi) if e < mean else (lo, a)
+        return 0.5 * (lo + hi)
+
+    fc_N, fc_K = cfg.hidden, 5 * cfg.hidden
+    Wfc = runtime.upload_tiled(ctx, synth.q4k_matrix(fc_N, fc_K, 3, 4242), fc_N, fc_K)
+    xfc = torch.from_numpy(synth.normal((16, fc_K), 3, 17)).cuda()
+    yfc = torch.zeros((16, fc_N), dtype=torch.float32, device="cuda")
+
+    def fc_us(M):
+        def call():
+            abi.check("spec_gemm_q4k", abi.spec_gemm_q4k(ctx.h, Wfc.data_ptr(), fc_N, fc_K, xfc.data_ptr(), M,
+                                                         yfc.data_ptr()))
+        return _time_steps(torch, stream, call, 3, 20) * 1e3
+
+    rng = np.random.default_rng(5)
+    for mean in (1.0, 4.0, 12.0, float(K_DRAFT)):
+        a = alpha_for(mean) if mean < K_DRAFT else 1.0
+        Ls = np.zeros(args.steps, dtype=np.int32)
+        drafts = np.zeros((args.steps, K_DRAFT), dtype=np.int32)
+        for t in range(args.steps):
+            L = 0
+            while L < K_DRAFT and rng.random() < a:
+                L += 1
+            Ls[t] = L
+            d = rng.integers(0, V, K_DRAFT).astype(np.int32)
+            d[:L] = idx[:L]
+            if L < K_DRAFT:
+                d[L] = (idx[L] + 1) % V
+            drafts[t] = d
+        dd = torch.from_numpy(drafts).cuda()
+        hist = torch.zeros((args.steps, 4), dtype=torch.int32, device="cuda")
+        it = [0]
+
+        def step():
+            t = it[0] % args.steps
+            mdl.draft.copy_(dd[t])
+            abi.check("spec_verify_step", abi.spec_verify_step(ctx.h, mdl.ws, mdl.ks, mdl.hidden.data_ptr(),
+                                                               mdl.draft.data_ptr(), K_DRAFT, mdl.res.data_ptr()))
+            hist[t].copy_(mdl.res)
+            it[0] += 1
+            abi.check("spec_kv_rollback", abi.spec_kv_rollback(ctx.h, mdl.ks, CTX))
+
+        it[0] = 0
+        ms = _time_steps(torch, stream, step, 0, args.steps)
+        h = hist.cpu().numpy()
+        assert np.all(h[:, 2] == 0) and np.array_equal(h[:, 0], Ls), "planted accepted lengths"
+        sps = 1000.0 / ms
+        m_acc = float(h[:, 0].mean())
+        print(json.dumps({"metric": "accepted tokens/s at k+1=16 rows (verify steps/s x mean(L+1))",
+                          "value": sps * (m_acc + 1.0), "unit": "tokens/s", "steps_per_s": sps,
+                          "target_mean_accepted": mean, "mean_accepted": m_acc, "steps": args.steps,
+                          "fc_front_projection_us": {"M": int(round(m_acc)) + 1,
+                                                     "us": fc_us(int(round(m_acc)) + 1), "M16_us": fc_us(16)},
+                          "config": dict(workload_config(cfg), acceptance=f"per-position {a:.4f}")}),
+              flush=True)
+    ctx.close()
+
+
 def run_attention(args):
     """Time the verify attention alone: 16 rows, the full model's 52 query / 4 KV
     heads of 128, KV context --ctx (the block of 16 rows appended after it),
@@ -543,6 +705,10 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--gemm-shape", default=None,
                     help="NxK: time one Q4_K GEMM shape instead of the verify step")
+    ap.add_argument("--sampled", action="store_true",
+                    help="time the verify step with the sampled decision (Ch. 33 section 33.2)")
+    ap.add_argument("--accept-profile", action="store_true",
+                    help="steps with planted drafts at mean accepted lengths 1, 4, 12, 15: accepted tokens/s")
     ap.add_argument("--attn", action="store_true",
                     help="time the verify attention alone at context --ctx instead of the verify step")
     ap.add_argument("--ctx", type=int, default=2048,
@@ -557,6 +723,12 @@ def main():
         return
     if args.attn:
         run_attention(args)
+        return
+    if args.sampled:
+        run_sampled(args)
+        return
+    if args.accept_profile:
+        run_accept_profile(args)
         return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -328,27 +328,30 @@ void orc_softmax_row(const float* l, int V, float* p) {
     for (int x = 0; x < V; ++x) p[x] = (float)(exp((double)l[x] - m) / s);
 }
 
-/* Draw one token from the distribution r over [0, V): one uniform u, then the
- * tokens in index order with a running fp32 sum c; the first token with
- * u < c.  If rounding leaves c <= u at the end, the last token with r > 0.
+/* Draw one token from the weights w over [0, V) (w >= 0, total = their sum):
+ * one uniform u, then the tokens in index order with a running fp32 sum c of
+ * the weights; the first token with u * total < c.  This is the walk over the
+ * renormalised weights w / total with the division taken out of every term.
+ * If rounding leaves c <= u * total at the end, the last token with w > 0.
  * (The pages walk a precomputed token order; index order is this reading.)
- * *margin receives the distance of u from the nearest running-sum boundary
- * around the chosen token. */
-static int32_t orc_sample_row(const float* r, int V, uint32_t* mt, double* margin) {
+ * *margin receives the distance, in units of total, of u * total from the
+ * nearest running-sum boundary around the chosen token. */
+static int32_t orc_sample_row(const float* w, int V, float total, uint32_t* mt, double* margin) {
     const float u = orc_uniform_f32(mt);
+    const float t = u * total;
     float c = 0.f, prev = 0.f;
     int32_t last = -1;
     for (int x = 0; x < V; ++x) {
-        if (r[x] > 0.f) last = x;
+        if (w[x] > 0.f) last = x;
         prev = c;
-        c += r[x];
-        if (u < c) {
-            double d0 = (double)u - prev, d1 = (double)c - u;
-            *margin = d0 < d1 ? d0 : d1;
+        c += w[x];
+        if (t < c) {
+            double d0 = (double)t - prev, d1 = (double)c - t;
+            *margin = (d0 < d1 ? d0 : d1) / total;
             return x;
         }
     }
-    *margin = (double)u - c;
+    *margin = ((double)t - c) / total;
     return last;
 }
 
@@ -356,8 +359,8 @@ static int32_t orc_sample_row(const float* r, int V, uint32_t* mt, double* margi
  *   for i < k: x = draft[i], p = p_i(x), q = q_i(x),
  *       a = 1 if q <= 0 else min(p / q, 1); one uniform u;
  *       u <= a: accept and go on; otherwise stop: the next token is drawn from
- *       max(p_i - q_i, 0) / total (from p_i itself when total <= 0);
- *   all accepted: the next token is drawn from p_k.
+ *       the weights max(p_i - q_i, 0) (from p_i itself when they sum to 0);
+ *   all accepted: the next token is drawn from the weights p_k.
  * logits fp32 [k+1][V] (p = softmax, temperature 1); q fp32 [k][V] (the draft's
  * distributions); mt the 625-word MT19937 state, advanced by the draws.
  * res = {accepted, next}; *margin = the smallest distance of a uniform from
@@ -392,13 +395,15 @@ int orc_sample_accept(const float* logits, const float* q, const int32_t* draft,
         }
         if (total <= 0.f) {
             memcpy(r, p, sizeof(float) * (size_t)V);
-        } else {
-            for (int x = 0; x < V; ++x) r[x] = r[x] / total;
+            total = 0.f;
+            for (int x = 0; x < V; ++x) total += p[x];
         }
-        next = orc_sample_row(r, V, mt, &m1);
+        next = orc_sample_row(r, V, total, mt, &m1);
     } else {
         orc_softmax_row(logits + (size_t)k * V, V, p);
-        next = orc_sample_row(p, V, mt, &m1);
+        float total = 0.f;
+        for (int x = 0; x < V; ++x) total += p[x];
+        next = orc_sample_row(p, V, total, mt, &m1);
     }
     if (m1 < mg) mg = m1;
     free(p);

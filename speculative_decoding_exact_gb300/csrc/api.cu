@@ -38,6 +38,7 @@ struct spec_ctx {
   int32_t* status = nullptr;     // device status word
   float* logits_ws = nullptr;    // [16][V] target logits of a sampled step
   float2* sstats = nullptr;      // [16] row max and sum of exp of a sampled step
+  uint8_t* sscratch = nullptr;   // decision scratch of a sampled step
   int32_t* step_state = nullptr; // [2]
   int32_t* idx_buf = nullptr;    // [16]
   float* hidden_dev = nullptr;   // host-buffer entry point staging
@@ -187,6 +188,7 @@ int spec_verify_init(const spec_config* cfg, void* cuda_stream, spec_ctx** out) 
   rc |= dalloc(&c->status, 4);
   rc |= dalloc(&c->logits_ws, (size_t)16 * V);
   rc |= dalloc(&c->sstats, 16);
+  rc |= dalloc(&c->sscratch, sample_scratch_bytes());
   rc |= dalloc(&c->step_state, 4);
   rc |= dalloc(&c->idx_buf, 16);
   rc |= dalloc(&c->hidden_dev, (size_t)16 * H);
@@ -222,6 +224,7 @@ void spec_verify_destroy(spec_ctx* c) {
   cudaFree(c->qtile);
   cudaFree(c->logits_ws);
   cudaFree(c->sstats);
+  cudaFree(c->sscratch);
   for (auto& gc : c->graphs)
     if (gc.exec) cudaGraphExecDestroy(gc.exec);
   cudaFree(c->attn_part);
@@ -487,9 +490,9 @@ static int enqueue_step(spec_ctx* c, const spec_weights* w, spec_kv* kv, const f
     if (taps && taps->logits)
       SPEC_TRY(cudaMemcpyAsync(taps->logits, c->logits_ws, sizeof(float) * (size_t)M * g.vocab,
                                cudaMemcpyDeviceToDevice, st));
-    SPEC_TRY(launch_sample_accept(c->logits_ws, sa->q, draft, k, g.vocab, c->sstats, sa->mt, &kvv,
-                                  c->step_state, c->status, reinterpret_cast<int32_t*>(res), st, true));
-    n += 2;
+    SPEC_TRY(launch_sample_accept(c->logits_ws, sa->q, draft, k, g.vocab, c->sstats, c->sscratch, sa->mt,
+                                  &kvv, c->step_state, c->status, reinterpret_cast<int32_t*>(res), st, true));
+    n += 4;
   } else {
     SPEC_TRY(launch_head_argmax(c->p_head, c->pieces, M, taps ? taps->logits : nullptr, c->head_val,
                                 c->head_idx, c->status, st, true)); ++n;
@@ -635,9 +638,9 @@ int spec_sample_accept(spec_ctx* c, const float* logits, const float* q, const i
   }
   KvView v;
   if (kv) v = view_of(c, kv);
-  return cuda_code(launch_sample_accept(logits, q, draft, k, c->cfg.vocab, c->sstats, mt, kv ? &v : nullptr,
-                                        nullptr, c->status, reinterpret_cast<int32_t*>(res), c->stream,
-                                        false));
+  return cuda_code(launch_sample_accept(logits, q, draft, k, c->cfg.vocab, c->sstats, c->sscratch, mt,
+                                        kv ? &v : nullptr, nullptr, c->status,
+                                        reinterpret_cast<int32_t*>(res), c->stream, false));
 }
 
 int spec_verify_step_host(spec_ctx* c, const spec_weights* w, spec_kv* kv, const float* hidden_host,

@@ -99,8 +99,9 @@ cudaError_t launch_attention(const AttnPlan& a, const KvView& kv, int layer, con
 // stochastic exact acceptance: row normalizers (stats fp32x2 [k+1]: max and
 // sum of exp) then the decisions, the final draw and the rollback; mt is the
 // 625-word MT19937 state (DEVICE), advanced by the draws
+size_t sample_scratch_bytes();
 cudaError_t launch_sample_accept(const float* logits, const float* q, const int32_t* draft, int k,
-                                 int V, float2* stats, uint32_t* mt, const KvView* kv,
+                                 int V, float2* stats, uint8_t* scratch, uint32_t* mt, const KvView* kv,
                                  const int32_t* step_state, int32_t* status, int32_t* res,
                                  cudaStream_t st, bool pdl);
 

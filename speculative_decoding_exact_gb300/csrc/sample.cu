@@ -3,15 +3,21 @@
 //
 //   for i < k: x = draft[i], p = p_i(x), q = q_i(x), a = 1 if q <= 0 else
 //       min(p / q, 1), one uniform u; u <= a accepts and goes on; otherwise
-//       stop: the next token is drawn from max(p_i - q_i, 0) / total (from p_i
-//       itself when total <= 0);
-//   all accepted: the next token is drawn from p_k.
+//       stop: the next token is drawn from the weights max(p_i - q_i, 0)
+//       (from p_i itself when they sum to 0);
+//   all accepted: the next token is drawn from the weights p_k.
 // p_i = softmax of the target logits of row i (temperature 1); q_i = the
 // draft's distribution at position i.  Every uniform comes from a caller-owned
 // MT19937 stream (Matsumoto & Nishimura 1998), one per attempted draft and one
 // for the final draw, in that order; uniform = top 24 bits x 2^-24.  A draw
-// walks the tokens in index order and returns the first whose running sum
-// exceeds u (the last token of positive weight if rounding leaves none).
+// walks the tokens in index order and returns the first whose running sum of
+// weights exceeds u x (their total), i.e. the walk over the renormalised
+// weights with the division taken out of every term (the last token of
+// positive weight if rounding leaves none).
+//
+// Kernels: row normalizers (one CTA per row), the decisions and the final
+// uniform (one CTA), per-tile sums of the drawn row (one CTA per
+// kSampleThreads tokens, coalesced), the draw and the rollback (one CTA).
 #include "common.cuh"
 #include "internal.h"
 #include "kvmeta.cuh"
@@ -85,11 +91,11 @@ softmax_stats_kernel(const float* __restrict__ logits, int V, float2* __restrict
   }
 }
 
-// ---- block-wide exclusive scan of one float per thread (fixed order: warp
-// Kogge-Stone, then the warp totals by warp 0); returns the exclusive prefix,
-// *total = the sum of all.
-SPEC_DEV float block_exclusive_scan(float v, float* sh, float* total) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+// ---- block-wide inclusive scan of one float per thread in a fixed order
+// (warp Kogge-Stone, then the warp totals scanned by warp 0 and added);
+// *total = the last thread's inclusive value.  sh: 64 floats of shared memory.
+SPEC_DEV float block_inclusive_scan(float v, float* sh, float* total) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
   float inc = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -99,7 +105,7 @@ SPEC_DEV float block_exclusive_scan(float v, float* sh, float* total) {
   if (lane == 31) sh[warp] = inc;
   __syncthreads();
   if (warp == 0) {
-    float w = sh[lane];
+    float w = lane < nw ? sh[lane] : 0.f;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const float t = __shfl_up_sync(0xffffffffu, w, o);
@@ -108,26 +114,43 @@ SPEC_DEV float block_exclusive_scan(float v, float* sh, float* total) {
     sh[32 + lane] = w;                       // inclusive prefix of the warp totals
   }
   __syncthreads();
-  const float before = warp > 0 ? sh[32 + warp - 1] : 0.f;
-  *total = sh[32 + 31];
-  const float r = before + (inc - v);
+  const float r = warp > 0 ? sh[32 + warp - 1] + inc : inc;
+  __syncthreads();
+  if (threadIdx.x == blockDim.x - 1) sh[0] = r;
+  __syncthreads();
+  *total = sh[0];
   __syncthreads();                           // sh may be reused by the caller
   return r;
 }
 
-// ---- decisions, the final draw and the rollback: one CTA, kSampleThreads.
-// Thread t owns the tokens [t*C, (t+1)*C) of a row, C = ceil(V / threads).
+// Scratch of one decision (device): L, the final uniform, the status, then
+// per tile of kSampleThreads tokens the sums and the last positive index of
+// the weights w (the residual or p_k) and of p.
+struct SampleScratch {
+  int L;
+  float u;
+  int status;
+  int pad;
+};
+constexpr int kMaxTiles = 1024;              // V <= 1024 * kSampleThreads
+size_t sample_scratch_bytes() { return sizeof(SampleScratch) + 4 * sizeof(float) * kMaxTiles; }
+
+// weight of token x of the drawn row: max(p - q, 0) for a rejection, p else
+SPEC_DEV float sample_weight(const float* lr, const float* qr, float2 ms, int x, int V, bool resid, bool use_p) {
+  if (x >= V) return 0.f;
+  const float p = expf(lr[x] - ms.x) / ms.y;
+  return (resid && !use_p) ? fmaxf(p - qr[x], 0.f) : p;
+}
+
+// ---- decisions and the final uniform: one CTA (the MT state is staged in
+// shared memory by all threads; thread 0 draws)
 __global__ void __launch_bounds__(kSampleThreads)
-sample_accept_kernel(const float* __restrict__ logits, const float* __restrict__ q,
-                     const int32_t* __restrict__ draft, int k, int V,
-                     const float2* __restrict__ stats, uint32_t* mt, KvView kv, int has_kv,
-                     const int32_t* step_state, int32_t* status, int32_t* res) {
+sample_decide_kernel(const float* __restrict__ logits, const float* __restrict__ q,
+                     const int32_t* __restrict__ draft, int k, int V, const float2* __restrict__ stats,
+                     uint32_t* mt, const int32_t* step_state, const int32_t* status, SampleScratch* sc) {
   pdl_trigger();
   pdl_wait();
   __shared__ uint32_t st[kMtN + 1];
-  __shared__ float sh[64];
-  __shared__ int sL, sst, best;
-  __shared__ float su;
   const int tid = threadIdx.x;
   for (int i = tid; i <= kMtN; i += kSampleThreads) st[i] = mt[i];
   __syncthreads();
@@ -140,6 +163,7 @@ sample_accept_kernel(const float* __restrict__ logits, const float* __restrict__
       if (!(ms.y > 0.f) || !isfinite(ms.x) || !isfinite(ms.y)) s |= SPEC_ST_NONFINITE;
     }
     int L = k;
+    float u = 0.f;
     if (!s) {
       for (int i = 0; i < k; ++i) {
         const int x = draft[i];
@@ -151,103 +175,143 @@ sample_accept_kernel(const float* __restrict__ logits, const float* __restrict__
         L = i;
         break;
       }
+      u = mt_uniform(st);                    // the final draw
     }
-    sL = L;
-    sst = s;
-    best = 0x7fffffff;
+    sc->L = L;
+    sc->u = u;
+    sc->status = s;
   }
-  __syncthreads();
-  const int L = sL;
-  int next = -1;
-  if (!sst) {
-    // weights of the row drawn from: the residual of row L, or p_k
-    const int row = L;
-    const bool resid = L < k;
-    const float2 ms = stats[row];
-    const float* lr = logits + (size_t)row * V;
-    const float* qr = resid ? q + (size_t)row * V : nullptr;
-    const int C = (V + kSampleThreads - 1) / kSampleThreads;
-    const int x0 = min(tid * C, V), x1 = min(x0 + C, V);
-    bool use_p = !resid;
-    float part = 0.f;
-    for (int x = x0; x < x1; ++x) {
-      const float p = expf(lr[x] - ms.x) / ms.y;
-      part += use_p ? p : fmaxf(p - qr[x], 0.f);
-    }
-    float total;
-    block_exclusive_scan(part, sh, &total);
-    if (resid && !(total > 0.f)) {          // residual all zero: draw from p_L itself
-      use_p = true;
-      part = 0.f;
-      for (int x = x0; x < x1; ++x) part += expf(lr[x] - ms.x) / ms.y;
-      block_exclusive_scan(part, sh, &total);
-    }
-    // normalised weights r = w / total; their running sum in index order:
-    // chunk sums scanned across threads, then each chunk walked in order
-    float rpart = 0.f;
-    for (int x = x0; x < x1; ++x) {
-      const float p = expf(lr[x] - ms.x) / ms.y;
-      rpart += (use_p ? p : fmaxf(p - qr[x], 0.f)) / total;
-    }
-    float rtot;
-    const float before = block_exclusive_scan(rpart, sh, &rtot);
-    if (tid == 0) su = mt_uniform(st);
-    __syncthreads();
-    const float u = su;
-    float c = 0.f;
-    int last = -1, hit = 0x7fffffff;
-    for (int x = x0; x < x1; ++x) {
-      const float p = expf(lr[x] - ms.x) / ms.y;
-      const float r = (use_p ? p : fmaxf(p - qr[x], 0.f)) / total;
-      if (r > 0.f) last = x;
-      c += r;
-      if (u < before + c) {
-        hit = x;
-        break;
-      }
-    }
-    if (hit != 0x7fffffff) atomicMin(&best, hit);
-    __syncthreads();
-    const int found = best;
-    __syncthreads();
-    if (found == 0x7fffffff) {
-      // rounding left no crossing: the last token of positive weight (no
-      // thread stopped early, so every thread saw its whole chunk)
-      if (tid == 0) best = -1;
-      __syncthreads();
-      if (last >= 0) atomicMax(&best, last);
-      __syncthreads();
-      next = best;
-    } else {
-      next = found;
-    }
-  }
-  // the MT state and the result
   __syncthreads();
   for (int i = tid; i <= kMtN; i += kSampleThreads) mt[i] = st[i];
+}
+
+// ---- per tile of kSampleThreads tokens of the drawn row (coalesced): the sum
+// of the weights w and of p (the block scan's last value) and the last
+// positive index of each
+__global__ void __launch_bounds__(kSampleThreads)
+sample_tiles_kernel(const float* __restrict__ logits, const float* __restrict__ q, int k, int V,
+                    const float2* __restrict__ stats, SampleScratch* sc) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ float sh[64];
+  __shared__ int lw, lp;
+  if (sc->status) return;
+  const int L = sc->L, j = blockIdx.x, tid = threadIdx.x;
+  const bool resid = L < k;
+  const int x = j * kSampleThreads + tid;
+  const float* lr = logits + (size_t)L * V;
+  const float* qr = resid ? q + (size_t)L * V : nullptr;
+  const float2 ms = stats[L];
+  const float w = sample_weight(lr, qr, ms, x, V, resid, false);
+  const float p = sample_weight(lr, qr, ms, x, V, resid, true);
+  if (tid == 0) {
+    lw = -1;
+    lp = -1;
+  }
+  float tw, tp;
+  block_inclusive_scan(w, sh, &tw);
+  block_inclusive_scan(p, sh, &tp);
+  if (w > 0.f) atomicMax(&lw, x);
+  if (p > 0.f) atomicMax(&lp, x);
+  __syncthreads();
+  if (tid == 0) {
+    float* t = reinterpret_cast<float*>(sc + 1);
+    t[j] = tw;
+    t[kMaxTiles + j] = tp;
+    reinterpret_cast<int*>(t)[2 * kMaxTiles + j] = lw;
+    reinterpret_cast<int*>(t)[3 * kMaxTiles + j] = lp;
+  }
+}
+
+// ---- the draw and the rollback: one CTA.  With prefix_j the inclusive scan
+// of the tile sums up to tile j-1, the running sum at token x of tile j is
+// prefix_j + (the tile's inclusive scan at x); the drawn token is the first
+// with u * total < that sum, found in the first tile with
+// u * total < prefix_j + tile_j (the same expression as its last token).
+__global__ void __launch_bounds__(kSampleThreads)
+sample_finish_kernel(const float* __restrict__ logits, const float* __restrict__ q, int k, int V,
+                     const float2* __restrict__ stats, const SampleScratch* sc, KvView kv, int has_kv,
+                     const int32_t* step_state, int32_t* status, int32_t* res) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ float sh[64];
+  __shared__ int hit_tile, hit_x, last;
+  __shared__ float prefix_hit;
+  const int tid = threadIdx.x;
+  const int s = sc->status;
+  int next = -1;
+  const int L = sc->L;
+  if (!s) {
+    const bool resid = L < k;
+    const int ntiles = (V + kSampleThreads - 1) / kSampleThreads;
+    const float* t = reinterpret_cast<const float*>(sc + 1);
+    const int* ti = reinterpret_cast<const int*>(t);
+    float tot;
+    float inc = block_inclusive_scan(tid < ntiles ? t[tid] : 0.f, sh, &tot);
+    const bool use_p = resid && !(tot > 0.f);     // residual all zero: draw from p_L itself
+    if (use_p) inc = block_inclusive_scan(tid < ntiles ? t[kMaxTiles + tid] : 0.f, sh, &tot);
+    const float mine = tid < ntiles ? (use_p ? t[kMaxTiles + tid] : t[tid]) : 0.f;
+    if (tid == 0) {
+      hit_tile = 0x7fffffff;
+      hit_x = 0x7fffffff;
+      last = -1;
+    }
+    __syncthreads();
+    // inclusive value of the previous tile (prefix_j), from the neighbour
+    __shared__ float incl[kMaxTiles];
+    if (tid < ntiles) incl[tid] = inc;
+    __syncthreads();
+    const float prefix = tid > 0 && tid < ntiles ? incl[tid - 1] : 0.f;
+    const float T = sc->u * tot;
+    if (tid < ntiles && T < prefix + mine) atomicMin(&hit_tile, tid);
+    if (tid < ntiles) {
+      const int lt = use_p ? ti[3 * kMaxTiles + tid] : ti[2 * kMaxTiles + tid];
+      if (lt >= 0) atomicMax(&last, lt);
+    }
+    __syncthreads();
+    const int j = hit_tile;
+    if (j != 0x7fffffff) {
+      if (tid == 0) prefix_hit = j > 0 ? incl[j - 1] : 0.f;
+      __syncthreads();
+      const float* lr = logits + (size_t)L * V;
+      const float* qr = resid ? q + (size_t)L * V : nullptr;
+      const int x = j * kSampleThreads + tid;
+      const float w = sample_weight(lr, qr, stats[L], x, V, resid, use_p);
+      float tt;
+      const float c = prefix_hit + block_inclusive_scan(w, sh, &tt);
+      if (x < V && T < c) atomicMin(&hit_x, x);
+      __syncthreads();
+      // a ragged last tile can miss by an ulp: its scan over the valid tokens
+      // need not repeat the tile sum bit for bit
+      next = hit_x != 0x7fffffff ? hit_x : last;
+    } else {
+      next = last;                           // rounding left no crossing
+    }
+  }
   if (tid != 0) return;
-  int s = sst;
+  int st = s;
   int Lr = L;
   const bool appended = step_state ? step_state[1] != 0 : has_kv != 0;
   const int n_past = step_state ? step_state[0] : (has_kv ? *kv.seq_len - (k + 1) : 0);
-  if (s) {
+  if (st) {
     Lr = 0;
     next = -1;
     if (has_kv && appended) kv_rollback_dev(kv, n_past);
   } else if (has_kv && appended) {
     kv_rollback_dev(kv, n_past + Lr + 1);
   }
-  *status = s;
+  *status = st;
   res[0] = Lr;
   res[1] = next;
-  res[2] = s;
+  res[2] = st;
   res[3] = has_kv ? *kv.seq_len : 0;
 }
 
 cudaError_t launch_sample_accept(const float* logits, const float* q, const int32_t* draft, int k,
-                                 int V, float2* stats, uint32_t* mt, const KvView* kv,
+                                 int V, float2* stats, uint8_t* scratch, uint32_t* mt, const KvView* kv,
                                  const int32_t* step_state, int32_t* status, int32_t* res,
                                  cudaStream_t st, bool pdl) {
+  if ((V + kSampleThreads - 1) / kSampleThreads > kMaxTiles) return cudaErrorInvalidValue;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -257,12 +321,20 @@ cudaError_t launch_sample_accept(const float* logits, const float* q, const int3
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
+  SampleScratch* sc = reinterpret_cast<SampleScratch*>(scratch);
   cudaError_t e = cudaLaunchKernelEx(&cfg, softmax_stats_kernel, logits, V, stats);
   if (e != cudaSuccess) return e;
   cfg.gridDim = dim3(1);
+  e = cudaLaunchKernelEx(&cfg, sample_decide_kernel, logits, q, draft, k, V, (const float2*)stats, mt,
+                         step_state, (const int32_t*)status, sc);
+  if (e != cudaSuccess) return e;
+  cfg.gridDim = dim3((V + kSampleThreads - 1) / kSampleThreads);
+  e = cudaLaunchKernelEx(&cfg, sample_tiles_kernel, logits, q, k, V, (const float2*)stats, sc);
+  if (e != cudaSuccess) return e;
+  cfg.gridDim = dim3(1);
   KvView v = kv ? *kv : KvView{};
-  return cudaLaunchKernelEx(&cfg, sample_accept_kernel, logits, q, draft, k, V, (const float2*)stats, mt, v,
-                            kv ? 1 : 0, step_state, status, res);
+  return cudaLaunchKernelEx(&cfg, sample_finish_kernel, logits, q, k, V, (const float2*)stats,
+                            (const SampleScratch*)sc, v, kv ? 1 : 0, step_state, status, res);
 }
 
 }  // namespace spec

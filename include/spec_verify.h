@@ -331,6 +331,19 @@ SPEC_API int spec_attention(spec_ctx* ctx, const spec_kv* kv, int layer,
 SPEC_API int spec_accept(spec_ctx* ctx, const int32_t* idx, const int32_t* draft, int k,
                 spec_kv* kv, spec_result* res);
 
+/* ---- Hidden-state capture for a draft's front projection (Ch. 8: the
+ * draft is fed the target's hidden states from five pinned target layers,
+ * concatenated, through fc: 5 x 6,656 = 33,280 -> 6,656).
+ *
+ * From the next step on, the residual stream after block layer_ids[j] (the
+ * block's output, fp32) of each of the M rows is written to
+ * rows[m][j*H .. j*H + H), row stride n*H: the layout spec_gemm_q4k takes as
+ * its input x for K = n*H.  n <= 8 distinct ids in [0, n_layers); n = 0 turns
+ * the capture off.  rows: DEVICE fp32 [16][n*H], 16-byte aligned, owned by the
+ * caller and kept alive while the capture is on.  The capture is part of the
+ * residual kernel that produces the block output: no extra launch. */
+SPEC_API int spec_set_capture(spec_ctx* ctx, const int32_t* layer_ids_host, int n, float* rows);
+
 /* ---- Stochastic exact acceptance (Ch. 33 §33.2; the rule of which
  * spec_accept is the one-hot case).
  *

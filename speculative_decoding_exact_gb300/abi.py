@@ -75,6 +75,7 @@ _SIGS = {
     "spec_profile_read": (I, [P, C.POINTER(C.c_float), C.POINTER(C.c_int)]),
     "spec_gemm_q4k_noalloc": (I, [P, I, I, P, I, P, P]),
     "spec_mt_seed": (I, [P, C.c_uint32]),
+    "spec_set_capture": (I, [P, P, I, P]),
     "spec_sample_accept": (I, [P, P, P, P, I, P, C.POINTER(spec_kv), P]),
     "spec_verify_step_sampled": (I, [P, C.POINTER(spec_weights), C.POINTER(spec_kv), P, P, P, I, P, P,
                                      C.POINTER(spec_taps)]),
@@ -196,6 +197,10 @@ def spec_lm_head_argmax(ctx, w_head, final_norm, x, M, idx, logits) -> int:
 
 def spec_attention(ctx, kv, layer, q, M, out) -> int:
     return _call("spec_attention", ctx, C.byref(kv), layer, P(q), M, P(out))
+
+
+def spec_set_capture(ctx, layer_ids_host, n, rows) -> int:
+    return _call("spec_set_capture", ctx, P(layer_ids_host), n, P(rows))
 
 
 def spec_mt_seed(state_host, seed: int) -> int:

@@ -39,6 +39,10 @@ struct spec_ctx {
   float* logits_ws = nullptr;    // [16][V] target logits of a sampled step
   float2* sstats = nullptr;      // [16] row max and sum of exp of a sampled step
   uint8_t* sscratch = nullptr;   // decision scratch of a sampled step
+  // hidden-state capture: block outputs of cap_ids[j] -> cap_rows[m][j*H ..]
+  int cap_n = 0;
+  int cap_ids[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  float* cap_rows = nullptr;
   int32_t* step_state = nullptr; // [2]
   int32_t* idx_buf = nullptr;    // [16]
   float* hidden_dev = nullptr;   // host-buffer entry point staging
@@ -471,8 +475,11 @@ static int enqueue_step(spec_ctx* c, const spec_weights* w, spec_kv* kv, const f
     SPEC_TRY(launch_swiglu_quant(c->p_gu, c->pieces, M, F, c->act, c->status, st, true)); ++n;
     SPEC_TRY(gemm(c->p_down, w->w_down[l])); ++n;
     const float* next_gamma = (l + 1 < g.n_layers) ? attn_gamma(l + 1) : w->final_norm;
+    float* cap = nullptr;
+    for (int j = 0; j < c->cap_n; ++j)
+      if (c->cap_ids[j] == l) cap = c->cap_rows + (size_t)j * H;
     SPEC_TRY(launch_resid_norm_quant(&c->p_down, c->pieces, c->resid, c->resid, next_gamma, g.rms_eps,
-                                     M, H, c->act, nullptr, c->status, st, true)); ++n;
+                                     M, H, c->act, nullptr, c->status, st, true, cap, c->cap_n * H)); ++n;
     if (tap_resid)
       SPEC_TRY(cudaMemcpyAsync(tap_resid + (size_t)(l + 1) * M * H, c->resid, rows_bytes,
                                cudaMemcpyDeviceToDevice, st));
@@ -516,6 +523,8 @@ static uint64_t step_key(const spec_ctx* c, const spec_weights* w, const spec_kv
   auto P = [](const void* p) { return (uint64_t)(uintptr_t)p; };
   h = mix(h, sa ? 0x5a ^ P(sa->q) : 0x9e);
   h = mix(h, sa ? P(sa->mt) : 0);
+  h = mix(h, P(c->cap_rows));
+  for (int j = 0; j < c->cap_n; ++j) h = mix(h, 0x100 + (uint64_t)c->cap_ids[j]);
   h = mix(h, P(hidden));
   h = mix(h, P(draft));
   h = mix(h, P(res));
@@ -614,6 +623,22 @@ int spec_verify_step_sampled(spec_ctx* c, const spec_weights* w, spec_kv* kv, co
   if (!aligned(q) || !aligned(mt)) return SPEC_EALIGN;
   const SampleArgs sa{q, mt};
   return run_step(c, w, kv, hidden, draft, k, res, taps, &sa);
+}
+
+int spec_set_capture(spec_ctx* c, const int32_t* layer_ids, int n, float* rows) {
+  if (!c) return SPEC_ENULL;
+  if (n < 0 || n > 8) return SPEC_EINVAL;
+  if (n > 0 && (!layer_ids || !rows)) return SPEC_ENULL;
+  if (n > 0 && !aligned(rows)) return SPEC_EALIGN;
+  for (int j = 0; j < n; ++j) {
+    if (layer_ids[j] < 0 || layer_ids[j] >= c->cfg.n_layers) return SPEC_EINVAL;
+    for (int i = 0; i < j; ++i)
+      if (layer_ids[i] == layer_ids[j]) return SPEC_EINVAL;
+  }
+  c->cap_n = n;
+  for (int j = 0; j < n; ++j) c->cap_ids[j] = layer_ids[j];
+  c->cap_rows = n > 0 ? rows : nullptr;
+  return SPEC_OK;
 }
 
 // MT19937 seeding (Matsumoto & Nishimura 1998): word 0 = seed, word i =

@@ -127,7 +127,8 @@ cudaError_t launch_quantize(const float* x, int M, int K, uint8_t* act, int8_t* 
 // (butterfly, the warp's blocks in order); every warp sum is pushed into the
 // shared memory of every CTA of the cluster, and after one cluster barrier
 // each warp adds the kNormSplit*warps sums in a butterfly: one fixed order set
-// by H alone.  x_out = x_in + sum(pieces) (fp32 add) when pieces are given.
+// by H alone.  x_out = x_in + sum(pieces) (fp32 add) when pieces are given;
+// cap (optional) receives the same rows with row stride cap_ld.
 // ---------------------------------------------------------------------------
 constexpr int kNormSplit = 4;
 
@@ -135,7 +136,8 @@ __global__ void __launch_bounds__(1024)
 resid_norm_quant_kernel(const float* __restrict__ pieces, int pN, int pnb, long long pU, int pG,
                         const float* x_in, float* x_out,
                         const float* __restrict__ gamma, float eps, int M, int H, uint8_t* act,
-                        float* __restrict__ xnorm_out, int32_t* status) {
+                        float* __restrict__ xnorm_out, float* __restrict__ cap, int cap_ld,
+                        int32_t* status) {
   __shared__ float part_ss[64];
   const int row = blockIdx.y;
   const int c = kNormSplit > 1 ? (int)cluster_rank() : 0;
@@ -191,6 +193,11 @@ resid_norm_quant_kernel(const float* __restrict__ pieces, int pN, int pnb, long 
       o[0] = make_float4(v[t][0], v[t][1], v[t][2], v[t][3]);
       o[1] = make_float4(v[t][4], v[t][5], v[t][6], v[t][7]);
     }
+    if (row < M && b < nb && cap) {           // hidden-state capture (row stride cap_ld)
+      float4* o = reinterpret_cast<float4*>(cap + (size_t)row * cap_ld + 256 * b + 8 * lane);
+      o[0] = make_float4(v[t][0], v[t][1], v[t][2], v[t][3]);
+      o[1] = make_float4(v[t][4], v[t][5], v[t][6], v[t][7]);
+    }
   }
   if (kNormSplit > 1) {
     cluster_sync_all();
@@ -223,7 +230,7 @@ resid_norm_quant_kernel(const float* __restrict__ pieces, int pN, int pnb, long 
 cudaError_t launch_resid_norm_quant(const GemmPlan* p, const float* pieces, const float* x_in,
                                     float* x_out, const float* gamma, float eps, int M, int H,
                                     uint8_t* act, float* xnorm_out, int32_t* status,
-                                    cudaStream_t st, bool pdl) {
+                                    cudaStream_t st, bool pdl, float* cap, int cap_ld) {
   const int nb = H / 256;
   const int per = (nb + kNormSplit - 1) / kNormSplit;       // blocks per CTA
   const int warps = per < 32 ? per : 32;
@@ -234,7 +241,7 @@ cudaError_t launch_resid_norm_quant(const GemmPlan* p, const float* pieces, cons
   const int pN = p ? p->N : 0, pnb = p ? p->nb : 1, pG = p ? p->G : 1;
   const long long pU = p ? p->U : 1;
   return cudaLaunchKernelEx(&cfg, resid_norm_quant_kernel, pieces, pN, pnb, pU, pG, x_in, x_out,
-                            gamma, eps, M, H, act, xnorm_out, status);
+                            gamma, eps, M, H, act, xnorm_out, cap, cap_ld, status);
 }
 
 // ---------------------------------------------------------------------------

@@ -60,7 +60,7 @@ cudaError_t launch_quantize(const float* x, int M, int K, uint8_t* act, int8_t* 
 cudaError_t launch_resid_norm_quant(const GemmPlan* p, const float* pieces, const float* x_in,
                                     float* x_out, const float* gamma, float eps, int M, int H,
                                     uint8_t* act, float* xnorm_out, int32_t* status,
-                                    cudaStream_t st, bool pdl);
+                                    cudaStream_t st, bool pdl, float* cap = nullptr, int cap_ld = 0);
 
 // h = silu(gate) * up from the gate|up GEMM pieces, quantised -> act (K = F)
 cudaError_t launch_swiglu_quant(const GemmPlan& p, const float* pieces, int M, int F,

@@ -414,6 +414,47 @@ def verify_step(cfg: Config, w: Weights, kv: KV, hidden: np.ndarray, draft: np.n
     return res, idx, lg, rs
 
 
+ST_BAD_TREE = 0x40
+
+
+def tree_masks(tokens: np.ndarray, parent: np.ndarray, vocab: int):
+    """(ancestor-or-self masks uint32 [n], status) of a token tree."""
+    tokens = np.ascontiguousarray(tokens, dtype=np.int32)
+    parent = np.ascontiguousarray(parent, dtype=np.int32)
+    mask = np.zeros(len(parent), dtype=np.uint32)
+    st = lib().orc_tree_masks(_p(tokens), _p(parent), len(parent), int(vocab), _p(mask))
+    return mask, int(st)
+
+
+def tree_accept(idx: np.ndarray, tokens: np.ndarray, parent: np.ndarray):
+    """(L, next, path[0..L]) of the greedy rule on a token tree."""
+    idx = np.ascontiguousarray(idx, dtype=np.int32)
+    tokens = np.ascontiguousarray(tokens, dtype=np.int32)
+    parent = np.ascontiguousarray(parent, dtype=np.int32)
+    L, nxt = C.c_int32(), C.c_int32()
+    path = np.zeros(16, dtype=np.int32)
+    lib().orc_tree_accept(_p(idx), _p(tokens), _p(parent), len(parent), C.byref(L), C.byref(nxt), _p(path))
+    return int(L.value), int(nxt.value), path[: L.value + 1].copy()
+
+
+def verify_tree(cfg: Config, w: Weights, kv: KV, hidden: np.ndarray, tokens: np.ndarray,
+                parent: np.ndarray, logits: bool = True):
+    """Returns (res = [accepted, next, status, seq_len], path, idx, logits) of the
+    tree verify step; node 0 = the carried frontier, parent[i] < i."""
+    hidden = np.ascontiguousarray(hidden, dtype=np.float32)
+    tokens = np.ascontiguousarray(tokens, dtype=np.int32)
+    parent = np.ascontiguousarray(parent, dtype=np.int32)
+    n = len(parent)
+    res = np.zeros(4, dtype=np.int32)
+    path = np.full(16, -1, dtype=np.int32)
+    idx = np.full(n, -1, dtype=np.int32)
+    lg = np.empty((n, cfg.vocab), dtype=np.float32) if logits else None
+    c, cw, ck = cfg.c(), w.c(), kv.c()
+    lib().orc_verify_tree(C.byref(c), C.byref(cw), C.byref(ck), _p(hidden), _p(tokens), _p(parent), n,
+                          _p(res), _p(path), _p(idx), _p(lg))
+    return res, path[: res[0] + 1].copy(), idx, lg
+
+
 def serial_greedy(cfg: Config, w: Weights, kv: KV, hidden: np.ndarray, k: int):
     hidden = np.ascontiguousarray(hidden, dtype=np.float32)
     tokens = np.empty(k + 1, dtype=np.int32)

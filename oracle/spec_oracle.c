@@ -490,43 +490,58 @@ void orc_kv_write_row(const orc_cfg* c, orc_kv* kv, int layer, int pos,
 /* visible t (max subtracted), o = sum_t softmax_t v_t.  K and V are the      */
 /* stored bf16 values.  fp64 throughout, stored fp32.                          */
 /* ------------------------------------------------------------------------ */
-void orc_attention(const orc_cfg* c, const orc_kv* kv, int layer, const float* q,
-                   int M, int n_past, float* out) {
+/* Row i sees the positions 0..n_past-1 and the block rows j with bit j of
+ * mask[i] set (mask NULL: the causal block, j <= i).  A token tree's mask is
+ * a node's ancestors and itself. */
+void orc_attention_tree(const orc_cfg* c, const orc_kv* kv, int layer, const float* q,
+                        int M, int n_past, const uint32_t* mask, float* out) {
     int dh = c->head_dim, group = c->n_q_heads / c->n_kv_heads;
     int max_vis = n_past + M;
     double* s = (double*)malloc(sizeof(double) * (size_t)max_vis);
+    int* vt = (int*)malloc(sizeof(int) * (size_t)max_vis);
     double scale = 1.0 / sqrt((double)dh);
     for (int i = 0; i < M; ++i) {
-        int vis = n_past + i + 1;
+        int nv = 0;                                   /* the visible positions, in order */
+        for (int t = 0; t < n_past; ++t) vt[nv++] = t;
+        for (int j = 0; j < M; ++j)
+            if (mask ? ((mask[i] >> j) & 1u) : (j <= i)) vt[nv++] = n_past + j;
         for (int h = 0; h < c->n_q_heads; ++h) {
             int g = h / group;
             const float* qh = q + ((size_t)i * c->n_q_heads + h) * dh;
             double mx = -INFINITY;
-            for (int t = 0; t < vis; ++t) {
+            for (int e = 0; e < nv; ++e) {
+                int t = vt[e];
                 int page = kv->page_table[t / c->page_size];
                 const uint16_t* kr = kv->pool + kv_index(c, page, layer, 0, g, t % c->page_size);
                 double dot = 0.0;
                 for (int d = 0; d < dh; ++d) dot += (double)qh[d] * orc_bf16_to_float(kr[d]);
-                s[t] = dot * scale;
-                if (s[t] > mx) mx = s[t];
+                s[e] = dot * scale;
+                if (s[e] > mx) mx = s[e];
             }
             double den = 0.0;
-            for (int t = 0; t < vis; ++t) {
-                s[t] = exp(s[t] - mx);
-                den += s[t];
+            for (int e = 0; e < nv; ++e) {
+                s[e] = exp(s[e] - mx);
+                den += s[e];
             }
             for (int d = 0; d < dh; ++d) {
                 double o = 0.0;
-                for (int t = 0; t < vis; ++t) {
+                for (int e = 0; e < nv; ++e) {
+                    int t = vt[e];
                     int page = kv->page_table[t / c->page_size];
                     const uint16_t* vr = kv->pool + kv_index(c, page, layer, 1, g, t % c->page_size);
-                    o += s[t] * orc_bf16_to_float(vr[d]);
+                    o += s[e] * orc_bf16_to_float(vr[d]);
                 }
                 out[((size_t)i * c->n_q_heads + h) * dh + d] = (float)(o / den);
             }
         }
     }
     free(s);
+    free(vt);
+}
+
+void orc_attention(const orc_cfg* c, const orc_kv* kv, int layer, const float* q,
+                   int M, int n_past, float* out) {
+    orc_attention_tree(c, kv, layer, q, M, n_past, NULL, out);
 }
 
 /* ------------------------------------------------------------------------ */
@@ -535,8 +550,8 @@ void orc_attention(const orc_cfg* c, const orc_kv* kv, int layer, const float* q
 /*   x += W_o q8(attention(Q));                                               */
 /*   xn = rmsnorm(x, ffn_norm); [g|u] = W_gu q8(xn); x += W_down q8(silu(g)u) */
 /* ------------------------------------------------------------------------ */
-int orc_block(const orc_cfg* c, const orc_weights* w, orc_kv* kv, int layer,
-              const float* x_in, int M, int n_past, float* x_out) {
+static int orc_block_tree(const orc_cfg* c, const orc_weights* w, orc_kv* kv, int layer,
+                          const float* x_in, int M, int n_past, const uint32_t* mask, float* x_out) {
     int H = c->hidden, dh = c->head_dim, F = c->ffn;
     int nq = c->n_q_heads * dh, nkv = c->n_kv_heads * dh;
     int Nqkv = nq + 2 * nkv;
@@ -560,7 +575,7 @@ int orc_block(const orc_cfg* c, const orc_weights* w, orc_kv* kv, int layer,
         orc_kv_write_row(c, kv, layer, n_past + i, qkv + (size_t)i * Nqkv + nq,
                          qkv + (size_t)i * Nqkv + nq + nkv);
     }
-    orc_attention(c, kv, layer, qv, M, n_past, att);
+    orc_attention_tree(c, kv, layer, qv, M, n_past, mask, att);
     st |= orc_linear(w->w_o[layer], H, nq, att, M, o);
     for (size_t i = 0; i < (size_t)M * H; ++i) x[i] = x_in[i] + o[i];
 
@@ -575,8 +590,13 @@ int orc_block(const orc_cfg* c, const orc_weights* w, orc_kv* kv, int layer,
     return st;
 }
 
-int orc_forward(const orc_cfg* c, const orc_weights* w, orc_kv* kv, const float* hidden,
-                int M, int32_t* idx, float* logits, float* resid) {
+int orc_block(const orc_cfg* c, const orc_weights* w, orc_kv* kv, int layer,
+              const float* x_in, int M, int n_past, float* x_out) {
+    return orc_block_tree(c, w, kv, layer, x_in, M, n_past, NULL, x_out);
+}
+
+static int orc_forward_tree(const orc_cfg* c, const orc_weights* w, orc_kv* kv, const float* hidden,
+                            int M, const uint32_t* mask, int32_t* idx, float* logits, float* resid) {
     int H = c->hidden, V = c->vocab;
     int n_past = *kv->seq_len;
     int st = orc_kv_reserve(kv, n_past + M);
@@ -587,7 +607,7 @@ int orc_forward(const orc_cfg* c, const orc_weights* w, orc_kv* kv, const float*
     memcpy(x, hidden, sizeof(float) * (size_t)M * H);
     for (int l = 0; l < c->n_layers; ++l) {
         if (resid) memcpy(resid + (size_t)l * M * H, x, sizeof(float) * (size_t)M * H);
-        st |= orc_block(c, w, kv, l, x, M, n_past, y);
+        st |= orc_block_tree(c, w, kv, l, x, M, n_past, mask, y);
         memcpy(x, y, sizeof(float) * (size_t)M * H);
     }
     if (resid) memcpy(resid + (size_t)c->n_layers * M * H, x, sizeof(float) * (size_t)M * H);
@@ -601,6 +621,11 @@ int orc_forward(const orc_cfg* c, const orc_weights* w, orc_kv* kv, const float*
     free(x);
     free(y);
     return st;
+}
+
+int orc_forward(const orc_cfg* c, const orc_weights* w, orc_kv* kv, const float* hidden,
+                int M, int32_t* idx, float* logits, float* resid) {
+    return orc_forward_tree(c, w, kv, hidden, M, NULL, idx, logits, resid);
 }
 
 /* The verify step ([33] §33.2, §33.7; [8] §8.6).  Returns -2 for a verify
@@ -632,6 +657,112 @@ int orc_verify_step(const orc_cfg* c, const orc_weights* w, orc_kv* kv, const fl
         res[2] = st;
         return 0;
     }
+    orc_kv_rollback(kv, n_past + L + 1);
+    res[0] = L;
+    res[1] = next;
+    res[2] = 0;
+    res[3] = *kv->seq_len;
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Token-tree verification ([33] §33.7: a tree spends the batch on covering  */
+/* near-miss branches).  Node 0 is the carried frontier; node i >= 1 holds    */
+/* the draft token tokens[i], proposed as the continuation of parent[i] <     */
+/* i.  Node i's row sees the context and its ancestors and itself.           */
+/* ------------------------------------------------------------------------ */
+
+/* ancestor-or-self masks; ORC_ST_BAD_TREE for a parent list that is not a
+ * tree in topological order, ORC_ST_TOKEN_RANGE for a token outside [0, V) */
+int orc_tree_masks(const int32_t* tokens, const int32_t* parent, int n, int vocab, uint32_t* mask) {
+    if (n < 1 || n > 16 || parent[0] != -1) return ORC_ST_BAD_TREE;
+    mask[0] = 1u;
+    for (int i = 1; i < n; ++i) {
+        if (parent[i] < 0 || parent[i] >= i) return ORC_ST_BAD_TREE;
+        if (tokens[i] < 0 || tokens[i] >= vocab) return ORC_ST_TOKEN_RANGE;
+        mask[i] = mask[parent[i]] | (1u << i);
+    }
+    return 0;
+}
+
+/* The greedy rule on a tree: the root is accepted; node i is accepted when
+ * its parent is and tokens[i] equals the parent's argmax.  The deepest
+ * accepted node (the lowest index among equals) ends the path root -> a;
+ * L = depth(a) drafts accepted, next = idx[a].  path[0..L] = the nodes. */
+void orc_tree_accept(const int32_t* idx, const int32_t* tokens, const int32_t* parent, int n,
+                     int32_t* L, int32_t* next, int32_t* path) {
+    int acc[16], depth[16];
+    int best = 0;
+    acc[0] = 1;
+    depth[0] = 0;
+    for (int i = 1; i < n; ++i) {
+        acc[i] = acc[parent[i]] && tokens[i] == idx[parent[i]];
+        depth[i] = depth[parent[i]] + 1;
+        if (acc[i] && depth[i] > depth[best]) best = i;
+    }
+    *L = depth[best];
+    *next = idx[best];
+    int a = best;
+    for (int d = depth[best]; d >= 0; --d) {
+        path[d] = a;
+        a = d > 0 ? parent[a] : a;
+    }
+}
+
+/* move the K/V rows of block slots path[d] to slots d (d = 1..L), every layer */
+void orc_kv_compact(const orc_cfg* c, orc_kv* kv, int n_past, const int32_t* path, int L) {
+    size_t row = (size_t)c->head_dim;
+    uint16_t* tmp = (uint16_t*)malloc(sizeof(uint16_t) * row * 16);
+    for (int l = 0; l < c->n_layers; ++l)
+        for (int which = 0; which < 2; ++which)
+            for (int g = 0; g < c->n_kv_heads; ++g) {
+                for (int d = 1; d <= L; ++d) {              /* read all sources first */
+                    int t = n_past + path[d];
+                    int page = kv->page_table[t / c->page_size];
+                    memcpy(tmp + (size_t)d * row, kv->pool + kv_index(c, page, l, which, g, t % c->page_size),
+                           sizeof(uint16_t) * row);
+                }
+                for (int d = 1; d <= L; ++d) {
+                    int t = n_past + d;
+                    int page = kv->page_table[t / c->page_size];
+                    memcpy(kv->pool + kv_index(c, page, l, which, g, t % c->page_size), tmp + (size_t)d * row,
+                           sizeof(uint16_t) * row);
+                }
+            }
+    free(tmp);
+}
+
+/* The tree verify step: res = {accepted_len, next_token, status, seq_len},
+ * path[0..L] the accepted nodes.  The forward runs the n node rows with the
+ * tree mask; the accepted path's K/V rows end at positions n_past .. n_past+L
+ * and the KV is rolled back to n_past + L + 1.  A bad tree or token range is
+ * reported before any work. */
+int orc_verify_tree(const orc_cfg* c, const orc_weights* w, orc_kv* kv, const float* hidden,
+                    const int32_t* tokens, const int32_t* parent, int n, int32_t* res, int32_t* path,
+                    int32_t* idx, float* logits) {
+    uint32_t mask[16];
+    int n_past = *kv->seq_len;
+    res[0] = 0;
+    res[1] = -1;
+    res[3] = n_past;
+    int st = orc_tree_masks(tokens, parent, n, c->vocab, mask);
+    if (st) {
+        res[2] = st;
+        return 0;
+    }
+    st = orc_forward_tree(c, w, kv, hidden, n, mask, idx, logits, NULL);
+    if (st & (ORC_ST_POOL_EMPTY | ORC_ST_CTX_FULL)) {
+        res[2] = st;
+        return 0;
+    }
+    if (st) {
+        orc_kv_rollback(kv, n_past);
+        res[2] = st;
+        return 0;
+    }
+    int32_t L, next;
+    orc_tree_accept(idx, tokens, parent, n, &L, &next, path);
+    orc_kv_compact(c, kv, n_past, path, L);
     orc_kv_rollback(kv, n_past + L + 1);
     res[0] = L;
     res[1] = next;

@@ -97,6 +97,18 @@ void orc_attention(const orc_cfg* c, const orc_kv* kv, int layer, const float* q
 /* one transformer block on M rows at positions n_past.. (K/V appended) */
 int orc_block(const orc_cfg* c, const orc_weights* w, orc_kv* kv, int layer,
               const float* x_in, int M, int n_past, float* x_out);
+/* token trees ([33] §33.7): node 0 = the carried frontier, parent[i] < i */
+#define ORC_ST_BAD_TREE 0x40
+void orc_attention_tree(const orc_cfg* c, const orc_kv* kv, int layer, const float* q,
+                        int M, int n_past, const uint32_t* mask, float* out);
+int  orc_tree_masks(const int32_t* tokens, const int32_t* parent, int n, int vocab, uint32_t* mask);
+void orc_tree_accept(const int32_t* idx, const int32_t* tokens, const int32_t* parent, int n,
+                     int32_t* L, int32_t* next, int32_t* path);
+void orc_kv_compact(const orc_cfg* c, orc_kv* kv, int n_past, const int32_t* path, int L);
+int  orc_verify_tree(const orc_cfg* c, const orc_weights* w, orc_kv* kv, const float* hidden,
+                     const int32_t* tokens, const int32_t* parent, int n, int32_t* res, int32_t* path,
+                     int32_t* idx, float* logits);
+
 /* stochastic exact acceptance ([33] §33.2): MT19937 state of 625 words */
 void     orc_mt_seed(uint32_t* st, uint32_t seed);
 uint32_t orc_mt_next(uint32_t* st);

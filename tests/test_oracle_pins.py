@@ -548,3 +548,125 @@ def test_sample_accept_first_token_follows_the_target():
     # acceptance probability is sum_x min(p_x, q_x)
     a = float(np.minimum(p0, q0).sum())
     assert abs(acc / N - a) < 5 * math.sqrt(a * (1 - a) / N)
+
+
+# ---------------------------------------------------------------------------
+# token trees ([33] §33.7): node 0 = the carried frontier, parent[i] < i
+# ---------------------------------------------------------------------------
+def _committed_equal(kv_a, kv_b):
+    a, b = kv_a.committed(), kv_b.committed()
+    assert a[0] == b[0]
+    for p_log in range((a[0] + 15) // 16):
+        n_rows = min(16, a[0] - 16 * p_log)
+        assert np.array_equal(kv_a.pool[kv_a.page_table[p_log], :, :, :, :n_rows],
+                              kv_b.pool[kv_b.page_table[p_log], :, :, :, :n_rows])
+
+
+def test_tree_masks_are_ancestor_sets_and_reject_bad_trees():
+    rng = np.random.default_rng(4)
+    for _ in range(50):
+        n = int(rng.integers(1, 17))
+        parent = np.array([-1] + [int(rng.integers(0, i)) for i in range(1, n)], dtype=np.int32)
+        tokens = rng.integers(0, 100, n).astype(np.int32)
+        mask, st = oracle.tree_masks(tokens, parent, 100)
+        assert st == 0
+        for i in range(n):
+            anc, a = {i}, i
+            while parent[a] >= 0:
+                a = int(parent[a])
+                anc.add(a)
+            assert {j for j in range(n) if (int(mask[i]) >> j) & 1} == anc
+    ok_tok = np.zeros(3, dtype=np.int32)
+    assert oracle.tree_masks(ok_tok, np.array([0, 0, 1], dtype=np.int32), 100)[1] == oracle.ST_BAD_TREE
+    assert oracle.tree_masks(ok_tok, np.array([-1, 1, 0], dtype=np.int32), 100)[1] == oracle.ST_BAD_TREE
+    assert oracle.tree_masks(np.array([0, 100, 1], dtype=np.int32), np.array([-1, 0, 0], dtype=np.int32),
+                             100)[1] == oracle.ST_TOKEN_RANGE
+
+
+def test_tree_accept_is_the_longest_matching_root_path():
+    # independent formulation: every root path whose tokens follow the argmax
+    # chain; the longest wins, the lowest end node among equals
+    rng = np.random.default_rng(6)
+    V = 5                                           # small vocabulary: many matches and ties
+    for _ in range(300):
+        n = int(rng.integers(1, 17))
+        parent = np.array([-1] + [int(rng.integers(0, i)) for i in range(1, n)], dtype=np.int32)
+        tokens = rng.integers(0, V, n).astype(np.int32)
+        idx = rng.integers(0, V, n).astype(np.int32)
+        best = (0, 0)                               # (-depth, node)
+        for end in range(n):
+            path, a = [end], end
+            while parent[a] >= 0:
+                a = int(parent[a])
+                path.append(a)
+            path.reverse()
+            if all(tokens[path[d]] == idx[path[d - 1]] for d in range(1, len(path))):
+                best = min(best, (-(len(path) - 1), end))
+        L, nxt, path = oracle.tree_accept(idx, tokens, parent)
+        assert L == -best[0] and path[-1] == best[1] and nxt == idx[best[1]]
+        assert path[0] == 0 and all(parent[path[d]] == path[d - 1] for d in range(1, L + 1))
+
+
+def test_chain_tree_is_the_linear_verify():
+    cfg, w = tiny_model()
+    k = 7
+    hidden = synth.normal((k + 1, cfg.hidden), 0, 60)
+    kv0 = oracle.KV(cfg, num_pages=16, max_seq_pages=16)
+    kv0.extend(19)
+    for layer in range(cfg.n_layers):
+        _fill_kv(kv0, layer, 19, 70 + layer)
+    serial, _ = oracle.serial_greedy(cfg, w, kv0.copy(), hidden, k)
+    for L_t in (0, 4, k):
+        draft = synth.plant_draft(serial, L_t, cfg.vocab, 0, 80 + L_t)
+        kv_l, kv_t = kv0.copy(), kv0.copy()
+        res_l, idx_l, lg_l, _ = oracle.verify_step(cfg, w, kv_l, hidden, draft)
+        parent = np.arange(-1, k, dtype=np.int32)
+        tokens = np.concatenate([[0], draft]).astype(np.int32)
+        res_t, path, idx_t, lg_t = oracle.verify_tree(cfg, w, kv_t, hidden, tokens, parent)
+        assert list(res_t) == list(res_l) and np.array_equal(path, np.arange(L_t + 1))
+        assert np.array_equal(idx_t, idx_l) and np.array_equal(lg_t.view(np.uint32), lg_l.view(np.uint32))
+        _committed_equal(kv_t, kv_l)
+
+
+def test_tree_with_decoys_equals_serial_greedy():
+    # the true branch carries the serial decode's rows and tokens; decoy
+    # branches (wrong tokens, other rows) hang off it.  The tree step accepts
+    # exactly the true branch, and the compacted KV equals the serial decode's.
+    cfg, w = tiny_model(seed=2)
+    k = 6
+    rng = np.random.default_rng(12)
+    hidden = synth.normal((k + 1, cfg.hidden), 2, 61)
+    kv0 = oracle.KV(cfg, num_pages=16, max_seq_pages=16)
+    kv0.extend(23)
+    for layer in range(cfg.n_layers):
+        _fill_kv(kv0, layer, 23, 90 + layer)
+    kv_s = kv0.copy()
+    serial, st = oracle.serial_greedy(cfg, w, kv_s, hidden, k)
+    assert st == 0
+    for L_t in (0, 2, k):
+        # nodes: true chain 0..L_t' (rows hidden[0..]), with decoys interleaved
+        rows, tokens, parent, true_node = [hidden[0]], [0], [-1], [0]
+        depth = 0
+        while depth < k:
+            for _ in range(int(rng.integers(1, 3))):      # decoy children of the current true node
+                rows.append(synth.normal((cfg.hidden,), 2, 1000 + len(rows)))
+                tokens.append((serial[depth] + 1 + int(rng.integers(0, cfg.vocab - 1))) % cfg.vocab)
+                parent.append(true_node[-1])
+            # the true child: right token up to depth L_t, a wrong one after
+            rows.append(hidden[depth + 1])
+            tokens.append(serial[depth] if depth < L_t else (serial[depth] + 7) % cfg.vocab)
+            parent.append(true_node[-1])
+            true_node.append(len(rows) - 1)
+            depth += 1
+            if len(rows) >= 14:
+                break
+        n = len(rows)
+        kv_t = kv0.copy()
+        res, path, idx, _ = oracle.verify_tree(cfg, w, kv_t, np.stack(rows).astype(np.float32),
+                                               np.array(tokens, dtype=np.int32), np.array(parent, dtype=np.int32))
+        Lx = min(L_t, len(true_node) - 1)
+        assert res[2] == 0 and res[0] == Lx and res[1] == serial[Lx], (res, Lx, serial)
+        assert np.array_equal(path, np.array(true_node[:Lx + 1]))
+        kv_r = kv_s.copy()
+        kv_r.rollback(23 + Lx + 1)
+        _committed_equal(kv_t, kv_r)

@@ -101,6 +101,7 @@ extern "C" {
 #define SPEC_ST_ROLLBACK      0x8  /* rollback length < 0 or > seq_len           */
 #define SPEC_ST_CTX_FULL      0x10 /* seq_len + rows exceeds the page table      */
 #define SPEC_ST_DEVICE_WAIT   0x20 /* a bounded device wait (tensor core, bulk copy) gave up */
+#define SPEC_ST_BAD_TREE      0x40 /* a token tree's parent list is not a tree in topological order */
 
 /* Model geometry and workspace sizing.  H = n_q_heads*head_dim; H and ffn are
  * multiples of 256; n_q_heads is a multiple of n_kv_heads; head_dim = 128;
@@ -330,6 +331,27 @@ SPEC_API int spec_attention(spec_ctx* ctx, const spec_kv* kv, int layer,
  * p = 0 elsewhere (reject), residual max(p - q, 0) one-hot at the argmax. */
 SPEC_API int spec_accept(spec_ctx* ctx, const int32_t* idx, const int32_t* draft, int k,
                 spec_kv* kv, spec_result* res);
+
+/* ---- Token-tree verification (Ch. 33 §33.7: a tree spends the verify batch
+ * on covering near-miss branches), up to 16 nodes.
+ *
+ * Node 0 is the carried frontier; node i >= 1 holds the draft token
+ * tokens[i], proposed as the continuation of node parent[i] < i (parent[0] =
+ * -1; tokens[0] is not read).  Node i's row is hidden[i]; it sees the
+ * context and its ancestors and itself.  The root is accepted; node i is
+ * accepted when its parent is and tokens[i] equals the parent's argmax.  The
+ * deepest accepted node a (the lowest index among equals) ends the path root
+ * -> a: accepted_len = depth(a), next_token = argmax of a.  The path's K/V
+ * rows move to positions n_past .. n_past + depth(a), and the KV is rolled
+ * back to n_past + depth(a) + 1.
+ *   hidden   DEVICE fp32 [n][H]; tokens, parent DEVICE int32 [n]; 1 <= n <= 16
+ *   path_out DEVICE int32 [16] or NULL: the path's nodes, then -1
+ *   taps     as in spec_verify_step_ex (argmax = per node)
+ * A parent list that is not a tree in topological order sets
+ * SPEC_ST_BAD_TREE before any work; the KV is left as it was. */
+SPEC_API int spec_verify_tree(spec_ctx* ctx, const spec_weights* w, spec_kv* kv, const float* hidden,
+                              const int32_t* tokens, const int32_t* parent, int n, spec_result* res,
+                              int32_t* path_out, const spec_taps* taps);
 
 /* ---- Hidden-state capture for a draft's front projection (Ch. 8: the
  * draft is fed the target's hidden states from five pinned target layers,

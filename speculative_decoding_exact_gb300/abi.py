@@ -17,6 +17,7 @@ HEADER = os.path.join(os.path.dirname(HERE), "include", "spec_verify.h")
 SPEC_OK, SPEC_EINVAL, SPEC_EVERIFYLEN, SPEC_ENULL, SPEC_EALIGN = 0, -1, -2, -3, -4
 SPEC_ENOMEM, SPEC_ECAPACITY, SPEC_ECUDA, SPEC_ENODEV = -5, -6, -7, -8
 ST_TOKEN_RANGE, ST_NONFINITE, ST_POOL_EMPTY, ST_ROLLBACK, ST_CTX_FULL = 1, 2, 4, 8, 16
+ST_DEVICE_WAIT, ST_BAD_TREE = 0x20, 0x40
 
 
 class spec_config(C.Structure):
@@ -76,6 +77,8 @@ _SIGS = {
     "spec_gemm_q4k_noalloc": (I, [P, I, I, P, I, P, P]),
     "spec_mt_seed": (I, [P, C.c_uint32]),
     "spec_set_capture": (I, [P, P, I, P]),
+    "spec_verify_tree": (I, [P, C.POINTER(spec_weights), C.POINTER(spec_kv), P, P, P, I, P, P,
+                             C.POINTER(spec_taps)]),
     "spec_sample_accept": (I, [P, P, P, P, I, P, C.POINTER(spec_kv), P]),
     "spec_verify_step_sampled": (I, [P, C.POINTER(spec_weights), C.POINTER(spec_kv), P, P, P, I, P, P,
                                      C.POINTER(spec_taps)]),
@@ -197,6 +200,11 @@ def spec_lm_head_argmax(ctx, w_head, final_norm, x, M, idx, logits) -> int:
 
 def spec_attention(ctx, kv, layer, q, M, out) -> int:
     return _call("spec_attention", ctx, C.byref(kv), layer, P(q), M, P(out))
+
+
+def spec_verify_tree(ctx, w, kv, hidden, tokens, parent, n, res, path_out, taps: spec_taps | None) -> int:
+    return _call("spec_verify_tree", ctx, C.byref(w), C.byref(kv), P(hidden), P(tokens), P(parent), n, P(res),
+                 P(path_out), C.byref(taps) if taps is not None else None)
 
 
 def spec_set_capture(ctx, layer_ids_host, n, rows) -> int:

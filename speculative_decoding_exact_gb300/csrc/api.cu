@@ -39,6 +39,8 @@ struct spec_ctx {
   float* logits_ws = nullptr;    // [16][V] target logits of a sampled step
   float2* sstats = nullptr;      // [16] row max and sum of exp of a sampled step
   uint8_t* sscratch = nullptr;   // decision scratch of a sampled step
+  uint32_t* tree_mask = nullptr; // [16] ancestor masks of a token-tree step
+  uint8_t* tscratch = nullptr;   // decision scratch of a token-tree step
   // hidden-state capture: block outputs of cap_ids[j] -> cap_rows[m][j*H ..]
   int cap_n = 0;
   int cap_ids[8] = {0, 0, 0, 0, 0, 0, 0, 0};
@@ -193,6 +195,8 @@ int spec_verify_init(const spec_config* cfg, void* cuda_stream, spec_ctx** out) 
   rc |= dalloc(&c->logits_ws, (size_t)16 * V);
   rc |= dalloc(&c->sstats, 16);
   rc |= dalloc(&c->sscratch, sample_scratch_bytes());
+  rc |= dalloc(&c->tree_mask, 16);
+  rc |= dalloc(&c->tscratch, tree_scratch_bytes());
   rc |= dalloc(&c->step_state, 4);
   rc |= dalloc(&c->idx_buf, 16);
   rc |= dalloc(&c->hidden_dev, (size_t)16 * H);
@@ -229,6 +233,8 @@ void spec_verify_destroy(spec_ctx* c) {
   cudaFree(c->logits_ws);
   cudaFree(c->sstats);
   cudaFree(c->sscratch);
+  cudaFree(c->tree_mask);
+  cudaFree(c->tscratch);
   for (auto& gc : c->graphs)
     if (gc.exec) cudaGraphExecDestroy(gc.exec);
   cudaFree(c->attn_part);
@@ -427,10 +433,17 @@ struct SampleArgs {
   const float* q;
   uint32_t* mt;
 };
+// a token tree: node tokens (tokens[0], the carried frontier's, is unused),
+// parents, and where to write the accepted path
+struct TreeArgs {
+  const int32_t* tokens;
+  const int32_t* parent;
+  int32_t* path_out;
+};
 
 static int enqueue_step(spec_ctx* c, const spec_weights* w, spec_kv* kv, const float* hidden,
                         const int32_t* draft, int k, spec_result* res, const spec_taps* taps,
-                        const SampleArgs* sa) {
+                        const SampleArgs* sa, const TreeArgs* ta = nullptr) {
   const int M = k + 1;
 
   const spec_config& g = c->cfg;
@@ -458,7 +471,9 @@ static int enqueue_step(spec_ctx* c, const spec_weights* w, spec_kv* kv, const f
   float* tap_resid = taps ? taps->resid : nullptr;
   const size_t rows_bytes = sizeof(float) * (size_t)M * H;
 
-  SPEC_TRY(launch_kv_reserve(kvv, M, 0, draft, k, g.vocab, c->status, c->step_state, st, true)); ++n;
+  const uint32_t* tmask = ta ? c->tree_mask : nullptr;
+  SPEC_TRY(launch_kv_reserve(kvv, M, 0, ta ? ta->tokens + 1 : draft, k, g.vocab, c->status, c->step_state, st,
+                             true, ta ? ta->parent : nullptr, ta ? c->tree_mask : nullptr)); ++n;
   if (tap_resid) SPEC_TRY(cudaMemcpyAsync(tap_resid, hidden, rows_bytes, cudaMemcpyDeviceToDevice, st));
   SPEC_TRY(launch_resid_norm_quant(nullptr, nullptr, hidden, c->resid, attn_gamma(0), g.rms_eps, M, H,
                                    c->act, nullptr, c->status, st, true)); ++n;
@@ -467,7 +482,7 @@ static int enqueue_step(spec_ctx* c, const spec_weights* w, spec_kv* kv, const f
     SPEC_TRY(launch_qkv_post(c->p_qkv, c->pieces, M, g.n_q_heads, g.n_kv_heads, g.head_dim, kvv, l,
                               c->qtile, c->attn.tiles, c->status, st, true)); ++n;
     SPEC_TRY(launch_attention(c->attn, kvv, l, c->qtile, M, c->attn_part, nullptr, c->act, c->status,
-                              st, true)); n += 2;
+                              st, true, tmask)); n += 2;
     SPEC_TRY(gemm(c->p_o, w->w_o[l])); ++n;
     SPEC_TRY(launch_resid_norm_quant(&c->p_o, c->pieces, c->resid, c->resid, ffn_gamma(l), g.rms_eps,
                                      M, H, c->act, nullptr, c->status, st, true)); ++n;
@@ -485,7 +500,15 @@ static int enqueue_step(spec_ctx* c, const spec_weights* w, spec_kv* kv, const f
                                cudaMemcpyDeviceToDevice, st));
   }
   SPEC_TRY(gemm(c->p_head, w->w_head)); ++n;
-  if (sa) {
+  if (ta) {
+    // token tree: the argmax of every node, the accepted path, its K/V moves
+    SPEC_TRY(launch_head_argmax(c->p_head, c->pieces, M, taps ? taps->logits : nullptr, c->head_val,
+                                c->head_idx, c->status, st, true)); ++n;
+    SPEC_TRY(launch_tree_accept(c->head_val, c->head_idx, c->head_parts, ta->tokens, ta->parent, M, g.vocab,
+                                kvv, c->step_state, c->tscratch, c->status, reinterpret_cast<int32_t*>(res),
+                                ta->path_out, taps ? taps->argmax : nullptr, st, true));
+    n += 3;
+  } else if (sa) {
     // sampled acceptance: the logits of every row, their normalizers, then
     // the decisions on the caller's MT19937 stream
     SPEC_TRY(launch_head_argmax(c->p_head, c->pieces, M, c->logits_ws, c->head_val, c->head_idx,
@@ -518,12 +541,15 @@ static uint64_t mix(uint64_t h, uint64_t v) {
 
 static uint64_t step_key(const spec_ctx* c, const spec_weights* w, const spec_kv* kv,
                          const float* hidden, const int32_t* draft, int k, const spec_result* res,
-                         const SampleArgs* sa) {
+                         const SampleArgs* sa, const TreeArgs* ta) {
   uint64_t h = 0x1234567ull;
   auto P = [](const void* p) { return (uint64_t)(uintptr_t)p; };
   h = mix(h, sa ? 0x5a ^ P(sa->q) : 0x9e);
   h = mix(h, sa ? P(sa->mt) : 0);
   h = mix(h, P(c->cap_rows));
+  h = mix(h, ta ? 0x7e ^ P(ta->tokens) : 0x31);
+  h = mix(h, ta ? P(ta->parent) : 0);
+  h = mix(h, ta ? P(ta->path_out) : 0);
   for (int j = 0; j < c->cap_n; ++j) h = mix(h, 0x100 + (uint64_t)c->cap_ids[j]);
   h = mix(h, P(hidden));
   h = mix(h, P(draft));
@@ -551,9 +577,9 @@ static uint64_t step_key(const spec_ctx* c, const spec_weights* w, const spec_kv
 
 static int run_step(spec_ctx* c, const spec_weights* w, spec_kv* kv, const float* hidden,
                     const int32_t* draft, int k, spec_result* res, const spec_taps* taps,
-                    const SampleArgs* sa) {
+                    const SampleArgs* sa, const TreeArgs* ta = nullptr) {
   if (!c || !hidden || !draft || !res) return SPEC_ENULL;
-  if (k != 3 && k != 7 && k != 15) return SPEC_EVERIFYLEN;
+  if (ta ? (k < 0 || k > 15) : (k != 3 && k != 7 && k != 15)) return SPEC_EVERIFYLEN;
   const int M = k + 1;
   if (M > c->cfg.max_rows) return SPEC_ECAPACITY;
   int rc = check_kv(kv);
@@ -567,9 +593,9 @@ static int run_step(spec_ctx* c, const spec_weights* w, spec_kv* kv, const float
   // Steps with taps, with GEMM profiling, or on the legacy default stream
   // (which cannot be captured) are enqueued directly.
   if (taps || c->profile || !c->use_graphs || c->stream == nullptr)
-    return enqueue_step(c, w, kv, hidden, draft, k, res, taps, sa);
+    return enqueue_step(c, w, kv, hidden, draft, k, res, taps, sa, ta);
 
-  const uint64_t key = step_key(c, w, kv, hidden, draft, k, res, sa);
+  const uint64_t key = step_key(c, w, kv, hidden, draft, k, res, sa, ta);
   spec_ctx::GraphEntry* hit = nullptr;
   for (auto& gc : c->graphs)
     if (gc.exec && gc.key == key) hit = &gc;
@@ -584,7 +610,7 @@ static int run_step(spec_ctx* c, const spec_weights* w, spec_kv* kv, const float
     }
     cudaGraph_t graph = nullptr;
     SPEC_TRY(cudaStreamBeginCapture(c->stream, cudaStreamCaptureModeThreadLocal));
-    rc = enqueue_step(c, w, kv, hidden, draft, k, res, nullptr, sa);
+    rc = enqueue_step(c, w, kv, hidden, draft, k, res, nullptr, sa, ta);
     cudaError_t e = cudaStreamEndCapture(c->stream, &graph);
     if (rc != SPEC_OK) {
       if (graph) cudaGraphDestroy(graph);
@@ -614,6 +640,15 @@ int spec_verify_step_ex(spec_ctx* c, const spec_weights* w, spec_kv* kv, const f
 int spec_verify_step(spec_ctx* c, const spec_weights* w, spec_kv* kv, const float* hidden,
                      const int32_t* draft, int k, spec_result* res) {
   return run_step(c, w, kv, hidden, draft, k, res, nullptr, nullptr);
+}
+
+int spec_verify_tree(spec_ctx* c, const spec_weights* w, spec_kv* kv, const float* hidden,
+                     const int32_t* tokens, const int32_t* parent, int n, spec_result* res,
+                     int32_t* path_out, const spec_taps* taps) {
+  if (!tokens || !parent) return SPEC_ENULL;
+  if (n < 1 || n > 16) return SPEC_EVERIFYLEN;
+  const TreeArgs ta{tokens, parent, path_out};
+  return run_step(c, w, kv, hidden, tokens, n - 1, res, taps, nullptr, &ta);
 }
 
 int spec_verify_step_sampled(spec_ctx* c, const spec_weights* w, spec_kv* kv, const float* hidden,

@@ -211,7 +211,7 @@ cudaError_t launch_q_to_tile(const float* q, int M, const AttnPlan& a, uint8_t* 
 __global__ void __launch_bounds__(kAttnWarps * 32, 1)
 attn_partial_kernel(const uint8_t* __restrict__ qtile, int M, int nq, int nkv, int group, int tiles,
                     int chunk_keys, KvView kv, const __grid_constant__ CUtensorMap kvmap, int layer,
-                    float* __restrict__ part, int32_t* status) {
+                    const uint32_t* __restrict__ tree_mask, float* __restrict__ part, int32_t* status) {
   extern __shared__ __align__(128) uint8_t dsm[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm) + 1023) & ~(uintptr_t)1023);
   uint8_t* qs = sm;                                    // Q tile: hi [0, 32K), lo [32K, 64K)
@@ -265,7 +265,7 @@ attn_partial_kernel(const uint8_t* __restrict__ qtile, int M, int nq, int nkv, i
     const int lp = key0 / 16 + i;
     pg[i] = lp < kv.max_seq_pages ? kv.page_table[lp] : -1;
   }
-  if (tid == 0) proceed = !(st & (SPEC_ST_TOKEN_RANGE | SPEC_ST_POOL_EMPTY | SPEC_ST_CTX_FULL)) && key0 < len;
+  if (tid == 0) proceed = !(st & kStepAbort) && key0 < len;
   __syncthreads();
   const int n_past = len - M;
   // sub-chunks with keys (0 when the CTA has nothing to do)
@@ -384,6 +384,9 @@ attn_partial_kernel(const uint8_t* __restrict__ qtile, int M, int nq, int nkv, i
     const int hl = tile * kHeadsPerTile + (r >> 4);     // head within the kv group
     const int row = r & 15;                             // block row
     const bool live = hl < group && row < M;
+    // the block keys this row sees, bit j = block row j: its ancestors and
+    // itself in a token tree, rows 0..row (causal) otherwise
+    const uint32_t tm = !live ? 0u : (tree_mask ? tree_mask[row] : (2u << row) - 1u);
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
     const float c2 = 1.4426950408889634f / sqrtf(128.0f);   // log2(e) / sqrt(d)
     float mref = -INFINITY, lsum = 0.f;
@@ -426,11 +429,14 @@ attn_partial_kernel(const uint8_t* __restrict__ qtile, int M, int nq, int nkv, i
           mx4[c & 3] = fmaxf(mx4[c & 3], s[c]);
         }
       } else {
-        const int lim = live ? n_past + row - ks0 : -1;
+        // key ks0 + key is visible when it precedes the block (and the row is
+        // live), or when it is block row rel = ks0 + key - n_past with bit rel
+        // of tm set
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
           const int key = 32 * h + c;
-          const bool vis = key <= lim && pok[key >> 4];
+          const int rel = ks0 + key - n_past;
+          const bool vis = pok[key >> 4] && (rel < 0 ? live : (rel < 32 && ((tm >> rel) & 1u)));
           s[c] = vis ? s[c] * c2 : -INFINITY;
           mx4[c & 3] = fmaxf(mx4[c & 3], s[c]);
         }
@@ -578,7 +584,7 @@ attn_merge_kernel(const float* __restrict__ part, int M, int nq, int max_chunks,
       ml[t] = c < max_chunks ? *reinterpret_cast<const float2*>(st + c * cstride) : make_float2(0.f, 0.f);
     }
   }
-  const bool valid = row < M && !(*status & (SPEC_ST_TOKEN_RANGE | SPEC_ST_POOL_EMPTY | SPEC_ST_CTX_FULL));
+  const bool valid = row < M && !(*status & kStepAbort);
   const int n_past = *seq_len - M;
   const int nchunks = valid ? min((n_past + row) / chunk_keys + 1, max_chunks) : 0;
   if (warp < 2) {
@@ -627,7 +633,7 @@ attn_merge_kernel(const float* __restrict__ part, int M, int nq, int max_chunks,
 
 cudaError_t launch_attention(const AttnPlan& a, const KvView& kv, int layer, const uint8_t* qtile,
                              int M, float* part, float* out, uint8_t* act, int32_t* status,
-                             cudaStream_t st, bool pdl) {
+                             cudaStream_t st, bool pdl, const uint32_t* tree_mask) {
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -650,7 +656,7 @@ cudaError_t launch_attention(const AttnPlan& a, const KvView& kv, int layer, con
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
   cudaError_t e = cudaLaunchKernelEx(&cfg, attn_partial_kernel, qtile, M, a.nq, a.nkv, a.group, a.tiles,
-                                     a.chunk, kv, kvmap, layer, part, status);
+                                     a.chunk, kv, kvmap, layer, tree_mask, part, status);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg2 = {};
   cfg2.gridDim = dim3(a.nq * 128 / 256, 16);

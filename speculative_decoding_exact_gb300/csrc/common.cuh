@@ -133,6 +133,10 @@ SPEC_DEV void cluster_sync_all() {
   asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
 }
 
+// status bits after which a step does no work on the block (nothing was
+// reserved in the KV)
+constexpr int32_t kStepAbort = SPEC_ST_TOKEN_RANGE | SPEC_ST_POOL_EMPTY | SPEC_ST_CTX_FULL | SPEC_ST_BAD_TREE;
+
 // Programmatic dependent launch: let the next kernel in the stream start its
 // independent prologue (weight prefetch) early, and wait for the previous
 // kernel's results before touching them.

@@ -326,7 +326,7 @@ __global__ void qkv_post_kernel(const float* __restrict__ pieces, int pN, int pn
     write_qtile(qtile, row, col / dh, col % dh, v, nq / nkv, tiles);
     return;
   }
-  if (*status & (SPEC_ST_TOKEN_RANGE | SPEC_ST_POOL_EMPTY | SPEC_ST_CTX_FULL)) return;
+  if (*status & kStepAbort) return;
   const int c = col - qcols;
   const int which = c / (nkv * dh);          // 0 = K, 1 = V
   const int head = (c % (nkv * dh)) / dh, d = c % dh;
@@ -485,7 +485,8 @@ cudaError_t launch_kv_reset(const KvView& kv, cudaStream_t st) {
 
 // step_state: [0] = n_past, [1] = 1 when the block was appended
 __global__ void kv_reserve_kernel(KvView kv, int n, int commit, const int32_t* __restrict__ draft,
-                                  int k, int vocab, int32_t* status, int32_t* step_state) {
+                                  int k, int vocab, int32_t* status, int32_t* step_state,
+                                  const int32_t* __restrict__ parent, uint32_t* tree_mask) {
   pdl_trigger();
   pdl_wait();
   if (threadIdx.x != 0 || blockIdx.x != 0) return;
@@ -493,6 +494,22 @@ __global__ void kv_reserve_kernel(KvView kv, int n, int commit, const int32_t* _
   if (step_state) {
     step_state[0] = *kv.seq_len;
     step_state[1] = 0;
+  }
+  if (parent) {
+    // a token tree of n nodes: parent[0] = -1, 0 <= parent[i] < i; the mask
+    // of node i = its ancestors and itself (Ch. 33 §33.7)
+    uint32_t m[16];
+    if (n < 1 || n > 16 || parent[0] != -1) st |= SPEC_ST_BAD_TREE;
+    m[0] = 1u;
+    for (int i = 1; i < n && !st; ++i) {
+      if (parent[i] < 0 || parent[i] >= i) {
+        st |= SPEC_ST_BAD_TREE;
+        break;
+      }
+      m[i] = m[parent[i]] | (1u << i);
+    }
+    if (!st)
+      for (int i = 0; i < n; ++i) tree_mask[i] = m[i];
   }
   if (draft) {
     for (int i = 0; i < k; ++i)
@@ -527,11 +544,11 @@ __global__ void kv_reserve_kernel(KvView kv, int n, int commit, const int32_t* _
 
 cudaError_t launch_kv_reserve(const KvView& kv, int n, int commit, const int32_t* draft, int k,
                               int vocab, int32_t* status, int32_t* step_state, cudaStream_t st,
-                              bool pdl) {
+                              bool pdl, const int32_t* parent, uint32_t* tree_mask) {
   cudaLaunchAttribute attrs[2];
   cudaLaunchConfig_t cfg = make_cfg(dim3(1), dim3(32), 0, st, pdl, attrs);
   return cudaLaunchKernelEx(&cfg, kv_reserve_kernel, kv, n, commit, draft, k, vocab, status,
-                            step_state);
+                            step_state, parent, tree_mask);
 }
 
 __global__ void kv_rollback_kernel(KvView kv, int new_len, int32_t* status) {

@@ -92,9 +92,11 @@ size_t attn_partial_floats(const AttnPlan& a, int max_rows);
 size_t qtile_bytes(const AttnPlan& a);
 cudaError_t launch_q_to_tile(const float* q, int M, const AttnPlan& a, uint8_t* qtile, cudaStream_t st,
                              bool pdl);
+// tree_mask (DEVICE uint32 [M], optional): the block rows row i sees (bit j =
+// block row j); NULL = causal
 cudaError_t launch_attention(const AttnPlan& a, const KvView& kv, int layer, const uint8_t* qtile,
                              int M, float* part, float* out, uint8_t* act, int32_t* status,
-                             cudaStream_t st, bool pdl);
+                             cudaStream_t st, bool pdl, const uint32_t* tree_mask = nullptr);
 
 // stochastic exact acceptance: row normalizers (stats fp32x2 [k+1]: max and
 // sum of exp) then the decisions, the final draw and the rollback; mt is the
@@ -104,6 +106,16 @@ cudaError_t launch_sample_accept(const float* logits, const float* q, const int3
                                  int V, float2* stats, uint8_t* scratch, uint32_t* mt, const KvView* kv,
                                  const int32_t* step_state, int32_t* status, int32_t* res,
                                  cudaStream_t st, bool pdl);
+
+// token-tree decision: argmax of the n rows from the head partials, the
+// accepted path, the K/V moves of the path and the rollback; path_out (DEVICE
+// int32 [16], optional) = the path's nodes, -1 after it
+size_t tree_scratch_bytes();
+cudaError_t launch_tree_accept(const float* part_val, const int32_t* part_idx, int nparts,
+                               const int32_t* tokens, const int32_t* parent, int n, int vocab,
+                               const KvView& kv, const int32_t* step_state, uint8_t* scratch,
+                               int32_t* status, int32_t* res, int32_t* path_out, int32_t* idx_out,
+                               cudaStream_t st, bool pdl);
 
 // LM head argmax over the head GEMM pieces: per-(CTA,row) partial (value, index)
 int head_argmax_blocks(int V);
@@ -120,7 +132,8 @@ cudaError_t launch_kv_reset(const KvView& kv, cudaStream_t st);
 // validate the draft tokens first; on any failure nothing changes.
 cudaError_t launch_kv_reserve(const KvView& kv, int n, int commit, const int32_t* draft, int k,
                               int vocab, int32_t* status, int32_t* step_state, cudaStream_t st,
-                              bool pdl);
+                              bool pdl, const int32_t* parent = nullptr,
+                              uint32_t* tree_mask = nullptr);
 cudaError_t launch_kv_rollback(const KvView& kv, int new_len, int32_t* status, cudaStream_t st);
 // accept + rollback; idx [k+1] from head_argmax final reduce (or given)
 cudaError_t launch_accept(const int32_t* idx, const float* part_val, const int32_t* part_idx,

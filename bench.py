@@ -643,6 +643,47 @@ def run_accept_profile(args):
     ctx.close()
 
 
+def run_tree(args):
+    """Token-tree verify steps (Ch. 33 section 33.7) on the full model at
+    context --ctx: a random tree of --tree nodes (node 0 = the carried
+    frontier, parent[i] uniform in [0, i), random tokens, random rows), timed
+    like the linear step, which is timed beside it."""
+    import torch
+
+    from speculative_decoding_exact_gb300 import abi, synth
+
+    mdl = setup_model(0)
+    cfg, ctx, stream = mdl.cfg, mdl.ctx, mdl.stream
+    n = args.tree
+    rng = np.random.default_rng(3)
+    parent = torch.from_numpy(np.array([-1] + [int(rng.integers(0, i)) for i in range(1, n)],
+                                       dtype=np.int32)).cuda()
+    tokens = torch.from_numpy(rng.integers(0, cfg.vocab, n).astype(np.int32)).cuda()
+    rows = torch.from_numpy(synth.normal((n, cfg.hidden), 0, 55)).cuda()
+    path = torch.zeros(16, dtype=torch.int32, device="cuda")
+
+    def tree():
+        abi.check("spec_verify_tree", abi.spec_verify_tree(ctx.h, mdl.ws, mdl.ks, rows.data_ptr(), tokens.data_ptr(),
+                                                           parent.data_ptr(), n, mdl.res.data_ptr(),
+                                                           path.data_ptr(), None))
+        abi.check("spec_kv_rollback", abi.spec_kv_rollback(ctx.h, mdl.ks, CTX))
+
+    def linear():
+        abi.check("spec_verify_step", abi.spec_verify_step(ctx.h, mdl.ws, mdl.ks, mdl.hidden.data_ptr(),
+                                                           mdl.draft.data_ptr(), K_DRAFT, mdl.res.data_ptr()))
+        abi.check("spec_kv_rollback", abi.spec_kv_rollback(ctx.h, mdl.ks, CTX))
+
+    ms_t = _time_steps(torch, stream, tree, args.warmup, args.steps)
+    r = mdl.res.cpu().numpy()
+    assert r[2] == 0, f"tree step status {r[2]}"
+    ms_l = _time_steps(torch, stream, linear, args.warmup, args.steps)
+    print(json.dumps({"metric": f"token-tree verify steps/s ({n} nodes)", "value": 1000.0 / ms_t,
+                      "unit": "verify steps/s", "ms_per_step": ms_t, "linear_16_rows_steps_per_s": 1000.0 / ms_l,
+                      "steps": args.steps, "warmup": args.warmup,
+                      "config": dict(workload_config(cfg), tree="random parents, random tokens")}), flush=True)
+    ctx.close()
+
+
 def run_attention(args):
     """Time the verify attention alone: 16 rows, the full model's 52 query / 4 KV
     heads of 128, KV context --ctx (the block of 16 rows appended after it),
@@ -709,6 +750,8 @@ def main():
                     help="time the verify step with the sampled decision (Ch. 33 section 33.2)")
     ap.add_argument("--accept-profile", action="store_true",
                     help="steps with planted drafts at mean accepted lengths 1, 4, 12, 15: accepted tokens/s")
+    ap.add_argument("--tree", type=int, default=0,
+                    help="time token-tree verify steps with a random tree of this many nodes (1..16)")
     ap.add_argument("--attn", action="store_true",
                     help="time the verify attention alone at context --ctx instead of the verify step")
     ap.add_argument("--ctx", type=int, default=2048,
@@ -726,6 +769,9 @@ def main():
         return
     if args.sampled:
         run_sampled(args)
+        return
+    if args.tree:
+        run_tree(args)
         return
     if args.accept_profile:
         run_accept_profile(args)

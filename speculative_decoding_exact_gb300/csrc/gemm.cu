@@ -119,6 +119,7 @@ GemmPlan make_gemm_plan(int N, int K, int num_sms) {
   return p;
 }
 
+constexpr int kGemmPreStages = 3;   // stages whose weights are fetched before the dependency wait
 constexpr int kStageWeightBytes = kGemmCols * kSB;            // 18432
 constexpr int kStageBytes = kStageWeightBytes + kActSBBytes;   // 27200
 constexpr int kTmemCols = 512;
@@ -238,8 +239,13 @@ gemm_q4k_kernel(const uint8_t* __restrict__ wt, const uint8_t* __restrict__ act,
         bytes = (uint32_t)(cols * kSB);
         return wt + ((size_t)kGemmCols * gg * nb + (size_t)bb * cols) * kSB;
       };
-      // weights of the first stages do not depend on the previous kernel
-      const int pre = min(nunits, kGemmStages);
+      // Weights of the first stages do not depend on the previous kernel and
+      // are fetched before the wait.  Only kGemmPreStages of the 6: this
+      // prefetch runs while the previous (latency-bound) kernel reads its
+      // inputs from L2, and 152 CTAs x 6 stages of 18 KB queued in front of
+      // those reads slowed them; on the 2k verify step 0/2/3/4/5/6 stages
+      // gave 205.3/210.5/212.8/211.3/209.1/206.9 steps/s.
+      const int pre = min(nunits, kGemmPreStages);
       {
         int gg = g, bb = b;
         for (int i = 0; i < pre; ++i) {
@@ -254,11 +260,11 @@ gemm_q4k_kernel(const uint8_t* __restrict__ wt, const uint8_t* __restrict__ act,
       pdl_wait();
       for (int i = 0; i < nunits; ++i) {
         const int s = i % kGemmStages;
-        if (i >= kGemmStages) {
-          if (!mbar_wait_ns(&empty[s], ((i / kGemmStages) - 1) & 1, kWaitNs)) {
-            ok = false;
-            break;
-          }
+        if (i >= kGemmStages && !mbar_wait_ns(&empty[s], ((i / kGemmStages) - 1) & 1, kWaitNs)) {
+          ok = false;
+          break;
+        }
+        if (i >= pre) {
           uint32_t wb;
           const uint8_t* src = weights_of(g, b, wb);
           mbar_arrive_expect_tx(&full[s], wb + (uint32_t)kActSBBytes);

@@ -119,7 +119,6 @@ GemmPlan make_gemm_plan(int N, int K, int num_sms) {
   return p;
 }
 
-constexpr int kGemmPreStages = 3;   // stages whose weights are fetched before the dependency wait
 constexpr int kStageWeightBytes = kGemmCols * kSB;            // 18432
 constexpr int kStageBytes = kStageWeightBytes + kActSBBytes;   // 27200
 constexpr int kTmemCols = 512;
@@ -194,7 +193,7 @@ __global__ void __maxnreg__(kGemmMaxRegs)
 gemm_q4k_kernel(const uint8_t* __restrict__ wt, const uint8_t* __restrict__ act,
                 float* __restrict__ pieces, int N, int nb, int U, int G,
                 int32_t* __restrict__ isc_out, int32_t* __restrict__ imn_out, int m_sums,
-                int32_t* status) {
+                int pre_stages, int32_t* status) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ uint32_t tmem_slot;
   __shared__ __align__(8) uint64_t full[kGemmStages], empty[kGemmStages];
@@ -239,13 +238,12 @@ gemm_q4k_kernel(const uint8_t* __restrict__ wt, const uint8_t* __restrict__ act,
         bytes = (uint32_t)(cols * kSB);
         return wt + ((size_t)kGemmCols * gg * nb + (size_t)bb * cols) * kSB;
       };
-      // Weights of the first stages do not depend on the previous kernel and
-      // are fetched before the wait.  Only kGemmPreStages of the 6: this
-      // prefetch runs while the previous (latency-bound) kernel reads its
-      // inputs from L2, and 152 CTAs x 6 stages of 18 KB queued in front of
-      // those reads slowed them; on the 2k verify step 0/2/3/4/5/6 stages
-      // gave 205.3/210.5/212.8/211.3/209.1/206.9 steps/s.
-      const int pre = min(nunits, kGemmPreStages);
+      // Weights of the first pre_stages stages do not depend on the previous
+      // kernel and are fetched before the wait.  Not all 6: this prefetch runs
+      // while the previous (latency-bound) kernel reads its inputs from L2,
+      // and 152 CTAs x 6 stages of 18 KB queued in front of those reads slowed
+      // them (the plan sets the depth per GEMM).
+      const int pre = min(nunits, min(max(pre_stages, 0), kGemmStages));
       {
         int gg = g, bb = b;
         for (int i = 0; i < pre; ++i) {
@@ -531,7 +529,7 @@ cudaError_t launch_gemm(const GemmPlan& p, const void* w_tiled, const uint8_t* a
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kern, static_cast<const uint8_t*>(w_tiled), act, pieces, p.N, p.nb,
-                            (int)p.U, p.G, isc, imn, m_sums, status);
+                            (int)p.U, p.G, isc, imn, m_sums, p.pre_stages, status);
 }
 
 // y[m][n] = sum over the group's slots, in slot order

@@ -16,6 +16,7 @@ namespace spec {
 struct GemmPlan {
   int N = 0, K = 0, nb = 0, ntiles = 0, ngroups = 0, G = 0, max_slots = 0;
   long long U = 0;
+  int pre_stages = 3;   // stages whose weights are fetched before the dependency wait (<= 6)
 };
 
 // tcgen05 GEMM: one CTA per SM owns 128 weight columns (one per TMEM lane).

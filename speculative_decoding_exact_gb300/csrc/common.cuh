@@ -16,62 +16,17 @@
 namespace spec {
 
 constexpr int kSB = 144;            // bytes per Q4_K superblock
-constexpr int kTileSB = 16 * kSB;   // bytes per tiled (16 columns x 1 superblock) block
 constexpr int kActSlots = 17;       // 16 k-steps + 1 min-term slot per superblock
 constexpr int kActSBBytes = kActSlots * 512 + 64;   // + 16 fp32 d_a
-constexpr int kPage = 16;
 
-// ---- tensor core: D += A(16x16 f16, row) * B(16x8 f16, col), f32 accumulate
-SPEC_DEV void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                       uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};\n"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// bf16 variant (attention)
-SPEC_DEV void mma16816_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                            uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};\n"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// ---- async copies
+// ---- shared-memory addresses
 SPEC_DEV uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
-SPEC_DEV void cp_async16(void* smem, const void* gmem) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(smem)), "l"(gmem));
-}
-SPEC_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
-template <int N>
-SPEC_DEV void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N)); }
-
-// ---- bit tricks
-// (a & b) | c
-SPEC_DEV uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t c) {
-  uint32_t d;
-  asm("lop3.b32 %0, %1, %2, %3, 0xEA;\n" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-  return d;
-}
-SPEC_DEV uint32_t hfma2_u32(uint32_t a, uint32_t b, uint32_t c) {
-  uint32_t d;
-  asm("fma.rn.f16x2 %0, %1, %2, %3;\n" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-  return d;
-}
+// ---- packed f16 arithmetic
 SPEC_DEV uint32_t hadd2_u32(uint32_t a, uint32_t b) {
   uint32_t d;
   asm("add.rn.f16x2 %0, %1, %2;\n" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
-SPEC_DEV uint32_t hmul2_u32(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("mul.rn.f16x2 %0, %1, %2;\n" : "=r"(d) : "r"(a), "r"(b));
   return d;
 }
 
@@ -173,13 +128,6 @@ SPEC_DEV void tmem_st4(uint32_t taddr, uint32_t a, uint32_t b, uint32_t c, uint3
   asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(taddr), "r"(a), "r"(b),
                "r"(c), "r"(d));
 }
-SPEC_DEV void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-}
 // D[tmem] (+)= A[tmem] * B[smem]^T, kind::f16 (f16 inputs, f32 accumulate), issued by one thread
 SPEC_DEV void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc, uint32_t accumulate) {
   asm volatile(
@@ -231,19 +179,6 @@ SPEC_DEV bool mbar_wait_ns(uint64_t* mbar, uint32_t parity, uint64_t limit_ns) {
       if (mbar_try(mbar, parity)) return true;
     if (globaltimer_ns() - t0 > limit_ns) return false;
   }
-}
-// bounded wait by iteration count (no suspend hint); false if it gave up
-SPEC_DEV bool mbar_wait(uint64_t* mbar, uint32_t parity, int limit) {
-  uint32_t done = 0;
-  for (int it = 0; it < limit && !done; ++it) {
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        " selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(done)
-        : "r"(smem_u32(mbar)), "r"(parity)
-        : "memory");
-  }
-  return done != 0;
 }
 // arrive once and add tx_bytes to the bytes the current phase waits for
 SPEC_DEV void mbar_arrive_expect_tx(uint64_t* mbar, uint32_t tx_bytes) {

@@ -368,7 +368,8 @@ __device__ __forceinline__ void better(float& bv, int& bi, float v, int i) {
 }
 
 // CTA c scans columns [c*kArgCols, (c+1)*kArgCols) of every row; thread t
-// owns columns t, t+256 of each row; per-row (max, lowest index) reduced
+// owns columns t + 256k (k < kArgCols/256) of every row, all rows loaded in
+// one round; per-row (max, lowest index) reduced
 // warp -> CTA in a fixed order.
 __global__ void __launch_bounds__(256)
 head_argmax_kernel(const float* __restrict__ pieces, int pN, int pnb, long long pU, int pG, int M,
@@ -386,16 +387,42 @@ head_argmax_kernel(const float* __restrict__ pieces, int pN, int pnb, long long 
     const int col = col_base + threadIdx.x + 256 * k;
     nsl[k] = col < pN ? piece_slots(pnb, (int)pU, pG, col) : 1;
   }
+  // the logits of both columns for every row: slot 0 of all rows in one
+  // round of loads, then the further slots, each added in slot order
+  constexpr int kC = kArgCols / 256;
+  float lv[kC][16];
+#pragma unroll
+  for (int k = 0; k < kC; ++k) {
+    const int col = col_base + threadIdx.x + 256 * k;
+#pragma unroll
+    for (int row = 0; row < 16; ++row)
+      lv[k][row] = (col < pN && row < M) ? pieces[(size_t)row * pN + col] : 0.f;
+  }
+  int nsmax = 1;
+#pragma unroll
+  for (int k = 0; k < kC; ++k) nsmax = max(nsmax, nsl[k]);
+  for (int sl = 1; sl < nsmax; ++sl) {
+#pragma unroll
+    for (int k = 0; k < kC; ++k) {
+      const int col = col_base + threadIdx.x + 256 * k;
+      if (col < pN && sl < nsl[k]) {
+#pragma unroll
+        for (int row = 0; row < 16; ++row)
+          if (row < M) lv[k][row] += pieces[((size_t)sl * 16 + row) * pN + col];
+      }
+    }
+  }
   bool bad = false;
+#pragma unroll
   for (int row = 0; row < 16; ++row) {
     float bv = -INFINITY;
     int bi = 0x7fffffff;
     if (row < M) {
 #pragma unroll
-      for (int k = 0; k < kArgCols / 256; ++k) {
+      for (int k = 0; k < kC; ++k) {
         const int col = col_base + threadIdx.x + 256 * k;
         if (col < pN) {
-          const float v = piece_sum(pieces, pN, nsl[k], row, col);
+          const float v = lv[k][row];
           if (logits) logits[(size_t)row * pN + col] = v;
           if (!isfinite(v)) bad = true;
           better(bv, bi, v, col);
@@ -440,32 +467,31 @@ __global__ void argmax_final_kernel(const float* __restrict__ part_val,
                                     int32_t* __restrict__ idx) {
   pdl_trigger();
   pdl_wait();
-  const int lane = threadIdx.x;
-  for (int row = 0; row < M; ++row) {
-    float bv = -INFINITY;
-    int bi = 0x7fffffff;
-    for (int c = lane; c < nparts; c += 32)
-      better(bv, bi, part_val[(size_t)c * 16 + row], part_idx[(size_t)c * 16 + row]);
+  const int row = threadIdx.x >> 5, lane = threadIdx.x & 31;   // one warp per row
+  if (row >= M) return;
+  float bv = -INFINITY;
+  int bi = 0x7fffffff;
+  for (int c = lane; c < nparts; c += 32)
+    better(bv, bi, part_val[(size_t)c * 16 + row], part_idx[(size_t)c * 16 + row]);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      better(bv, bi, ov, oi);
-    }
-    if (lane == 0) idx[row] = bi;
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+    better(bv, bi, ov, oi);
   }
+  if (lane == 0) idx[row] = bi;
 }
 
 cudaError_t launch_argmax_final(const float* part_val, const int32_t* part_idx, int nparts, int M,
                                 int32_t* idx, cudaStream_t st, bool pdl) {
   cudaLaunchAttribute attrs[2];
-  cudaLaunchConfig_t cfg = make_cfg(dim3(1), dim3(32), 0, st, pdl, attrs);
+  cudaLaunchConfig_t cfg = make_cfg(dim3(1), dim3(32 * 16), 0, st, pdl, attrs);
   return cudaLaunchKernelEx(&cfg, argmax_final_kernel, part_val, part_idx, nparts, M, idx);
 }
 
 // ---------------------------------------------------------------------------
-// KV metadata (Ch. 8 §8.6 item 4).  Single-thread kernels: a block touches at
-// most ceil(16/16)+1 pages, a rollback at most that many.
+// KV metadata (Ch. 8 §8.6 item 4).  The reserve scans the page table with a
+// warp; a rollback touches at most ceil(16/16)+1 pages and runs on one thread.
 // ---------------------------------------------------------------------------
 __global__ void kv_reset_kernel(KvView kv) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
@@ -489,52 +515,66 @@ __global__ void kv_reserve_kernel(KvView kv, int n, int commit, const int32_t* _
                                   const int32_t* __restrict__ parent, uint32_t* tree_mask) {
   pdl_trigger();
   pdl_wait();
-  if (threadIdx.x != 0 || blockIdx.x != 0) return;
-  int st = 0;
-  if (step_state) {
-    step_state[0] = *kv.seq_len;
-    step_state[1] = 0;
-  }
-  if (parent) {
-    // a token tree of n nodes: parent[0] = -1, 0 <= parent[i] < i; the mask
-    // of node i = its ancestors and itself (Ch. 33 §33.7)
-    uint32_t m[16];
-    if (n < 1 || n > 16 || parent[0] != -1) st |= SPEC_ST_BAD_TREE;
-    m[0] = 1u;
-    for (int i = 1; i < n && !st; ++i) {
-      if (parent[i] < 0 || parent[i] >= i) {
-        st |= SPEC_ST_BAD_TREE;
-        break;
-      }
-      m[i] = m[parent[i]] | (1u << i);
-    }
-    if (!st)
-      for (int i = 0; i < n; ++i) tree_mask[i] = m[i];
-  }
-  if (draft) {
-    for (int i = 0; i < k; ++i)
-      if (draft[i] < 0 || draft[i] >= vocab) st |= SPEC_ST_TOKEN_RANGE;
-  }
+  if (blockIdx.x != 0) return;
+  const int lane = threadIdx.x;              // one warp
   const int len = *kv.seq_len;
+  int st = 0;
+  if (lane == 0) {
+    if (step_state) {
+      step_state[0] = len;
+      step_state[1] = 0;
+    }
+    if (parent) {
+      // a token tree of n nodes: parent[0] = -1, 0 <= parent[i] < i; the mask
+      // of node i = its ancestors and itself (Ch. 33 §33.7)
+      uint32_t m[16];
+      if (n < 1 || n > 16 || parent[0] != -1) st |= SPEC_ST_BAD_TREE;
+      m[0] = 1u;
+      for (int i = 1; i < n && !st; ++i) {
+        if (parent[i] < 0 || parent[i] >= i) {
+          st |= SPEC_ST_BAD_TREE;
+          break;
+        }
+        m[i] = m[parent[i]] | (1u << i);
+      }
+      if (!st)
+        for (int i = 0; i < n; ++i) tree_mask[i] = m[i];
+    }
+    if (draft) {
+      for (int i = 0; i < k; ++i)
+        if (draft[i] < 0 || draft[i] >= vocab) st |= SPEC_ST_TOKEN_RANGE;
+    }
+  }
+  st = __shfl_sync(0xffffffffu, st, 0);
   const int upto = len + n;
   const int pages = (upto + kv.page_size - 1) / kv.page_size;
   if (!st && pages > kv.max_seq_pages) st |= SPEC_ST_CTX_FULL;
+  // the unmapped pages below `pages`, counted by the warp; the r-th of them in
+  // page order gets free_stack[top - 1 - r] (the pops of a serial walk)
+  int need = 0;
+  if (!st)
+    for (int base = 0; base < pages; base += 32) {
+      const int p = base + lane;
+      need += __popc(__ballot_sync(0xffffffffu, p < pages && kv.page_table[p] < 0));
+    }
+  const int top = *kv.free_top;
+  if (!st && need > top) st |= SPEC_ST_POOL_EMPTY;
   if (!st) {
-    int need = 0;
-    for (int p = 0; p < pages; ++p)
-      if (kv.page_table[p] < 0) ++need;
-    if (need > *kv.free_top) st |= SPEC_ST_POOL_EMPTY;
+    int before = 0;
+    for (int base = 0; base < pages; base += 32) {
+      const int p = base + lane;
+      const bool hole = p < pages && kv.page_table[p] < 0;
+      const uint32_t holes = __ballot_sync(0xffffffffu, hole);
+      if (hole) kv.page_table[p] = kv.free_stack[top - 1 - before - __popc(holes & ((1u << lane) - 1u))];
+      before += __popc(holes);
+    }
+    if (lane == 0) {
+      *kv.free_top = top - need;
+      if (commit || step_state) *kv.seq_len = upto;
+      if (step_state) step_state[1] = 1;
+    }
   }
-  if (!st) {
-    for (int p = 0; p < pages; ++p)
-      if (kv.page_table[p] < 0) {
-        const int top = *kv.free_top - 1;
-        kv.page_table[p] = kv.free_stack[top];
-        *kv.free_top = top;
-      }
-    if (commit || step_state) *kv.seq_len = upto;
-    if (step_state) step_state[1] = 1;
-  }
+  if (lane != 0) return;
   if (step_state) {
     *status = st;           // first kernel of a step: resets the step status
   } else if (st) {
@@ -581,8 +621,8 @@ __global__ void accept_kernel(const int32_t* __restrict__ idx_in, const float* _
   pdl_trigger();
   pdl_wait();
   __shared__ int idx_s[16];
-  const int lane = threadIdx.x;
-  for (int row = 0; row <= k; ++row) {
+  const int row = threadIdx.x >> 5, lane = threadIdx.x & 31;   // one warp per row
+  if (row <= k) {
     if (idx_in) {
       if (lane == 0) idx_s[row] = idx_in[row];
     } else {
@@ -598,8 +638,8 @@ __global__ void accept_kernel(const int32_t* __restrict__ idx_in, const float* _
       if (lane == 0) idx_s[row] = bi;
     }
   }
-  __syncwarp();
-  if (lane != 0) return;
+  __syncthreads();
+  if (threadIdx.x != 0) return;
   int st = step_state ? *status : 0;
   for (int i = 0; i < k; ++i)
     if (draft[i] < 0 || draft[i] >= vocab) st |= SPEC_ST_TOKEN_RANGE;
@@ -635,7 +675,7 @@ cudaError_t launch_accept(const int32_t* idx, const float* part_val, const int32
                           const int32_t* step_state, int32_t* status, int32_t* res,
                           int32_t* idx_out, cudaStream_t st, bool pdl) {
   cudaLaunchAttribute attrs[2];
-  cudaLaunchConfig_t cfg = make_cfg(dim3(1), dim3(32), 0, st, pdl, attrs);
+  cudaLaunchConfig_t cfg = make_cfg(dim3(1), dim3(32 * 16), 0, st, pdl, attrs);
   KvView v = kv ? *kv : KvView{};
   return cudaLaunchKernelEx(&cfg, accept_kernel, idx, part_val, part_idx, nparts, draft, k, vocab, v,
                             kv ? 1 : 0, step_state, status, res, idx_out);

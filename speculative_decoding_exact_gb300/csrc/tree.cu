@@ -37,8 +37,8 @@ __global__ void tree_decide_kernel(const float* __restrict__ part_val, const int
   pdl_trigger();
   pdl_wait();
   __shared__ int idx_s[16];
-  const int lane = threadIdx.x;
-  for (int row = 0; row < n; ++row) {
+  const int row = threadIdx.x >> 5, lane = threadIdx.x & 31;   // one warp per node
+  if (row < n) {
     float bv = -INFINITY;
     int bi = 0x7fffffff;
     for (int c = lane; c < nparts; c += 32)
@@ -51,8 +51,8 @@ __global__ void tree_decide_kernel(const float* __restrict__ part_val, const int
     }
     if (lane == 0) idx_s[row] = bi;
   }
-  __syncwarp();
-  if (lane != 0) return;
+  __syncthreads();
+  if (threadIdx.x != 0) return;
   int st = *status;
   for (int row = 0; row < n; ++row) {
     if (idx_s[row] < 0 || idx_s[row] >= vocab) st |= SPEC_ST_NONFINITE;
@@ -146,7 +146,7 @@ cudaError_t launch_tree_accept(const float* part_val, const int32_t* part_idx, i
   cfg.numAttrs = pdl ? 1 : 0;
   TreeScratch* sc = reinterpret_cast<TreeScratch*>(scratch);
   cfg.gridDim = dim3(1);
-  cfg.blockDim = dim3(32);
+  cfg.blockDim = dim3(32 * 16);
   cudaError_t e = cudaLaunchKernelEx(&cfg, tree_decide_kernel, part_val, part_idx, nparts, tokens, parent, n,
                                      vocab, (const int32_t*)status, sc, idx_out);
   if (e != cudaSuccess) return e;

@@ -492,7 +492,7 @@ static int enqueue_step(spec_ctx* c, const spec_weights* w, spec_kv* kv, const f
   for (int l = 0; l < g.n_layers; ++l) {
     SPEC_TRY(gemm(c->p_qkv, w->w_qkv[l])); ++n;
     SPEC_TRY(launch_qkv_post(c->p_qkv, c->pieces, M, g.n_q_heads, g.n_kv_heads, g.head_dim, kvv, l,
-                              c->qtile, c->attn.tiles, c->status, st, true)); ++n;
+                              c->qtile, c->attn.tiles, c->status, st, true, c->attn.early)); ++n;
     SPEC_TRY(launch_attention(c->attn, kvv, l, c->qtile, M, c->attn_part, nullptr, c->act, c->status,
                               st, true, tmask)); n += 2;
     SPEC_TRY(gemm(c->p_o, w->w_o[l])); ++n;

@@ -291,9 +291,14 @@ constexpr int kQkvThreads = 256;     // columns per CTA; one more warp prefetche
 
 __global__ void qkv_post_kernel(const float* __restrict__ pieces, int pN, int pnb, long long pU,
                                 int pG, int M, int nq, int nkv, int dh, KvView kv, int layer,
-                                uint8_t* __restrict__ qtile, int tiles, const int32_t* status) {
-  pdl_trigger();
+                                uint8_t* __restrict__ qtile, int tiles, const int32_t* status,
+                                int late_trigger) {
+  // With late_trigger the attention that follows reads the KV metadata before
+  // its own wait: signalling it only after this wait means that every kernel
+  // before this one has completed when it starts.
+  if (!late_trigger) pdl_trigger();
   pdl_wait();
+  if (late_trigger) pdl_trigger();
   // The attention that follows reads this layer's K and V of every page up to
   // the length: one 32 KB slab per page ([K, V][n_kv][16][128] bf16).  An
   // extra warp sends them to L2 now, while HBM has nothing else to do: lane l
@@ -343,12 +348,12 @@ __global__ void qkv_post_kernel(const float* __restrict__ pieces, int pN, int pn
 
 cudaError_t launch_qkv_post(const GemmPlan& p, const float* pieces, int M, int nq, int nkv, int dh,
                             const KvView& kv, int layer, uint8_t* qtile, int tiles,
-                            const int32_t* status, cudaStream_t st, bool pdl) {
+                            const int32_t* status, cudaStream_t st, bool pdl, bool late_trigger) {
   cudaLaunchAttribute attrs[2];
   cudaLaunchConfig_t cfg = make_cfg(dim3((p.N + kQkvThreads - 1) / kQkvThreads, 16), dim3(kQkvThreads + 32), 0,
                                     st, pdl, attrs);
   return cudaLaunchKernelEx(&cfg, qkv_post_kernel, pieces, p.N, p.nb, p.U, p.G, M, nq, nkv, dh, kv,
-                            layer, qtile, tiles, status);
+                            layer, qtile, tiles, status, (int)late_trigger);
 }
 
 // ---------------------------------------------------------------------------

@@ -78,12 +78,16 @@ struct KvView {
 };
 cudaError_t launch_qkv_post(const GemmPlan& p, const float* pieces, int M, int nq, int nkv,
                             int dh, const KvView& kv, int layer, uint8_t* qtile, int tiles,
-                            const int32_t* status, cudaStream_t st, bool pdl);
+                            const int32_t* status, cudaStream_t st, bool pdl, bool late_trigger);
 
 // verify attention: partials then merge (+ quantise for the O projection)
 struct AttnPlan {
   int nq = 0, nkv = 0, dh = 0, max_ctx = 0, chunk = 0, max_chunks = 0;
   int group = 0, tiles = 0;     // query heads per kv head; 128-row MMA tiles per kv head
+  // the chunk fits the K/V ring: the partial kernel reads the KV metadata and
+  // copies the chunk's rows of earlier steps before its dependency wait, and
+  // the QKV kernel before it signals only after its own wait
+  bool early = false;
 };
 AttnPlan make_attn_plan(int nq, int nkv, int dh, int max_ctx);
 size_t attn_partial_floats(const AttnPlan& a, int max_rows);

@@ -114,6 +114,38 @@ def test_step_matches_oracle_and_is_teacher_forced_per_layer(model):
         assert_close(taps["resid"][l + 1], x_out, what=f"layer {l} output")
 
 
+def test_step_long_context_plan_matches_oracle(model):
+    """The same step under a long-context work plan (max_ctx 8192: chunks of
+    256 keys, more than the K/V ring holds, so the attention reads the KV
+    metadata after its dependency wait) matches the oracle as the short plan
+    does."""
+    _, ow, dw = model
+    cfg, ocfg = SMALL, ocfg_of(SMALL)
+    k = 15
+    hidden = synth.normal((k + 1, cfg.hidden), 3, 510)
+    okv0 = fresh_kv(model[0])[1]
+    oidx, olog, _, st = oracle.forward(ocfg, ow, okv0.copy(), hidden, logits=True)
+    assert st == 0
+    _, gap = oracle.argmax(olog)
+    ctx_long = runtime.Context(SMALL, max_ctx=8192)
+    try:
+        for L_t in (3, 15):
+            dkv, okv = fresh_kv(ctx_long)
+            draft = synth.plant_draft(oidx, L_t, cfg.vocab, 3, 800 + L_t)
+            ores, oidx2, olog2, _ = oracle.verify_step(ocfg, ow, okv, hidden, draft)
+            res, taps = gpu_step(ctx_long, dw, dkv, hidden, draft)
+            assert_close(taps["logits"], olog2, what="logits (long plan)")
+            clear = gap > 1e-2
+            assert np.array_equal(taps["argmax"][clear], oidx2[clear])
+            if np.all(clear):
+                assert list(res) == list(ores), (list(res), list(ores))
+            s = dkv.state()
+            oc = okv.committed()
+            assert s[0] == oc[0] and np.array_equal(s[1], oc[1])
+    finally:
+        ctx_long.close()
+
+
 def test_step_batch_height_invariance(model):
     """Rows 0..3 of a k=15 step and of a k=3 step over the same first rows give
     bit-identical logits ("The Two-Fifteen That Wasn't": exact speculation needs

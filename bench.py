@@ -51,6 +51,24 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
+def max_over_ranks(x, world, device):
+    """The max of x over the ranks of the job (x itself at world 1): the job's
+    time is its slowest rank's."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as tdist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_steps_per_s(ms_max, steps, world):
+    """Whole-job verify steps/s: every rank runs `steps` steps of its own
+    replica within the slowest rank's `ms_max` milliseconds."""
+    return steps * world * 1000.0 / ms_max
+
+
 def gemm_algorithmic_bytes(cfg):
     """Per step: weights N*K*0.5625 + fp32 inputs M*K*4 + fp32 outputs M*N*4 of every GEMM."""
     tot = 0
@@ -373,12 +391,9 @@ def run_gpu(args, rank, world):
         tdist.barrier()
     ms = e0.elapsed_time(e1)
     clk = clocks.stop()
-    if dist:
-        t = torch.tensor([ms], device="cuda")
-        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, world, "cuda")
     ms_per_step = ms / args.steps
-    steps_per_s = 1000.0 / ms_per_step * world
+    steps_per_s = job_steps_per_s(ms, args.steps, world)
 
     # GEMM kernel timing: CUDA events around every GEMM launch of the same steps
     gemm_ms, gemm_launches = profile_gemms(ctx, abi, torch, stream, ws, ks, hidden, draft, res,
@@ -405,12 +420,8 @@ def run_gpu(args, rank, world):
                                                                      dr_h.data_ptr(), K_DRAFT, res_h))
         abi.spec_kv_rollback(ctx.h, ks, CTX)
     torch.cuda.synchronize()
-    e2e_s = time.perf_counter() - t0
-    if dist:
-        t = torch.tensor([e2e_s], device="cuda")
-        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
-        e2e_s = float(t.item())
-    e2e = args.steps / e2e_s * world
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world, "cuda")
+    e2e = job_steps_per_s(e2e_s * 1000.0, args.steps, world)
 
     if rank != 0:
         ctx.close()
@@ -781,7 +792,8 @@ def main():
     if world > 1:
         import torch
         import torch.distributed as tdist
-        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        if args.impl == "ours":
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
         tdist.init_process_group("nccl" if args.impl == "ours" else "gloo")
     if args.impl == "reference":
         run_reference(args, rank, world)

@@ -146,6 +146,33 @@ def test_step_long_context_plan_matches_oracle(model):
         ctx_long.close()
 
 
+@pytest.mark.parametrize("n_past", [0, 120, 250])
+def test_step_block_positions_match_oracle(model, n_past):
+    """The block at other depths of the short plan (64-key chunks): at the
+    start of the cache (no earlier rows to copy before the dependency wait),
+    straddling the chunk boundary at 128, and deep in the cache."""
+    ctx, ow, dw = model
+    cfg, ocfg = SMALL, ocfg_of(SMALL)
+    k = 15
+    hidden = synth.normal((k + 1, cfg.hidden), 3, 520 + n_past)
+    okv0 = fresh_kv(ctx, n_past)[1]
+    oidx, olog, _, st = oracle.forward(ocfg, ow, okv0.copy(), hidden, logits=True)
+    assert st == 0
+    _, gap = oracle.argmax(olog)
+    dkv, okv = fresh_kv(ctx, n_past)
+    draft = synth.plant_draft(oidx, 9, cfg.vocab, 3, 830 + n_past)
+    ores, oidx2, olog2, _ = oracle.verify_step(ocfg, ow, okv, hidden, draft)
+    res, taps = gpu_step(ctx, dw, dkv, hidden, draft)
+    assert_close(taps["logits"], olog2, what=f"logits at n_past {n_past}")
+    clear = gap > 1e-2
+    assert np.array_equal(taps["argmax"][clear], oidx2[clear])
+    if np.all(clear):
+        assert list(res) == list(ores), (list(res), list(ores))
+    s = dkv.state()
+    oc = okv.committed()
+    assert s[0] == oc[0] and np.array_equal(s[1], oc[1])
+
+
 def test_step_batch_height_invariance(model):
     """Rows 0..3 of a k=15 step and of a k=3 step over the same first rows give
     bit-identical logits ("The Two-Fifteen That Wasn't": exact speculation needs

@@ -15,7 +15,7 @@
 // weights with the division taken out of every term (the last token of
 // positive weight if rounding leaves none).
 //
-// Kernels: row normalizers (one CTA per row), the decisions and the final
+// Kernels: row normalizers (8 CTAs per row), the decisions and the final
 // uniform (one CTA), per-tile sums of the drawn row (one CTA per
 // kSampleThreads tokens, coalesced), the draw and the rollback (one CTA).
 #include "common.cuh"
@@ -48,10 +48,13 @@ SPEC_DEV uint32_t mt_draw(uint32_t* st) {
 }
 SPEC_DEV float mt_uniform(uint32_t* st) { return (float)(mt_draw(st) >> 8) * 0x1p-24f; }
 
-// ---- row normalizers: grid (rows), kSampleThreads threads; per row the max
-// m and s = sum exp(l - m) of the logits, thread-strided online pairs combined
-// lane -> warp (butterfly) -> CTA (warp order).  A row with a non-finite logit
-// gets (NaN, NaN), which the decision kernel reports as SPEC_ST_NONFINITE.
+// ---- row normalizers: grid (kStatParts, rows), kSampleThreads threads.  CTA
+// (part, row) takes the logits [part*Vp, min(V, (part+1)*Vp)), Vp =
+// ceil(V / kStatParts): their max m (one pass), then s = sum exp(l - m) (a
+// second pass over the same 64 KB, served from L1), each reduced lane -> warp
+// (butterfly) -> CTA (warp order).  A part with a non-finite logit gets (NaN,
+// NaN); an empty part (-inf, 0).  The decision kernel merges a row's parts
+// in part order.
 SPEC_DEV void ms_merge(float& m, float& s, float m2, float s2) {
   const float mn = fmaxf(m, m2);
   if (mn == -INFINITY) return;
@@ -59,35 +62,41 @@ SPEC_DEV void ms_merge(float& m, float& s, float m2, float s2) {
   m = mn;
 }
 
+constexpr int kStatParts = 8;
+
 __global__ void __launch_bounds__(kSampleThreads)
-softmax_stats_kernel(const float* __restrict__ logits, int V, float2* __restrict__ stats) {
+softmax_stats_kernel(const float* __restrict__ logits, int V, float2* __restrict__ pstats) {
   pdl_trigger();
   pdl_wait();
-  __shared__ float wm[32], ws[32];
-  const int row = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __shared__ float red[32];
+  const int part = blockIdx.x, row = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int Vp = (V + kStatParts - 1) / kStatParts;
+  const int x0 = part * Vp, x1 = min(V, x0 + Vp);
   const float* l = logits + (size_t)row * V;
-  float m = -INFINITY, s = 0.f;
-  bool bad = false;                        // NaN or inf anywhere in the row
-  for (int x = threadIdx.x; x < V; x += kSampleThreads) {
+  float m = -INFINITY;
+  bool bad = false;                        // NaN or inf anywhere in the part
+  for (int x = x0 + threadIdx.x; x < x1; x += kSampleThreads) {
     const float v = l[x];
     bad = bad || !(fabsf(v) <= 3.40282347e38f);
-    ms_merge(m, s, v, 1.f);
+    m = fmaxf(m, v);
   }
   bad = __syncthreads_or(bad);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float m2 = __shfl_xor_sync(0xffffffffu, m, o), s2 = __shfl_xor_sync(0xffffffffu, s, o);
-    ms_merge(m, s, m2, s2);
-  }
-  if (lane == 0) {
-    wm[warp] = m;
-    ws[warp] = s;
-  }
+  m = warp_max(m);
+  if (lane == 0) red[warp] = m;
+  __syncthreads();
+  m = red[0];
+  for (int w = 1; w < kSampleThreads / 32; ++w) m = fmaxf(m, red[w]);
+  __syncthreads();                         // red is reused below
+  float s = 0.f;
+  if (m != -INFINITY)
+    for (int x = x0 + threadIdx.x; x < x1; x += kSampleThreads) s += expf(l[x] - m);
+  s = warp_sum(s);
+  if (lane == 0) red[warp] = s;
   __syncthreads();
   if (threadIdx.x == 0) {
-    float M = wm[0], S = ws[0];
-    for (int w = 1; w < kSampleThreads / 32; ++w) ms_merge(M, S, wm[w], ws[w]);
-    stats[row] = bad ? make_float2(NAN, NAN) : make_float2(M, S);
+    float S = red[0];
+    for (int w = 1; w < kSampleThreads / 32; ++w) S += red[w];
+    pstats[row * kStatParts + part] = bad ? make_float2(NAN, NAN) : make_float2(m, S);
   }
 }
 
@@ -133,7 +142,9 @@ struct SampleScratch {
   int pad;
 };
 constexpr int kMaxTiles = 1024;              // V <= 1024 * kSampleThreads
-size_t sample_scratch_bytes() { return sizeof(SampleScratch) + 4 * sizeof(float) * kMaxTiles; }
+// then the row normalizers' parts: float2 [16 rows][kStatParts]
+constexpr size_t kPstatsOffset = sizeof(SampleScratch) + 4 * sizeof(float) * kMaxTiles;
+size_t sample_scratch_bytes() { return kPstatsOffset + sizeof(float2) * 16 * kStatParts; }
 
 // weight of token x of the drawn row: max(p - q, 0) for a rejection, p else
 SPEC_DEV float sample_weight(const float* lr, const float* qr, float2 ms, int x, int V, bool resid, bool use_p) {
@@ -146,20 +157,36 @@ SPEC_DEV float sample_weight(const float* lr, const float* qr, float2 ms, int x,
 // shared memory by all threads; thread 0 draws)
 __global__ void __launch_bounds__(kSampleThreads)
 sample_decide_kernel(const float* __restrict__ logits, const float* __restrict__ q,
-                     const int32_t* __restrict__ draft, int k, int V, const float2* __restrict__ stats,
-                     uint32_t* mt, const int32_t* step_state, const int32_t* status, SampleScratch* sc) {
+                     const int32_t* __restrict__ draft, int k, int V,
+                     uint32_t* mt, const int32_t* step_state, const int32_t* status, SampleScratch* sc,
+                     const float2* __restrict__ pstats, float2* __restrict__ stats_out) {
   pdl_trigger();
   pdl_wait();
   __shared__ uint32_t st[kMtN + 1];
+  __shared__ float2 rs[16];
   const int tid = threadIdx.x;
   for (int i = tid; i <= kMtN; i += kSampleThreads) st[i] = mt[i];
+  // thread r merges row r's normalizer parts in part order (any NaN part
+  // makes the row NaN); the tile and finish kernels read the result
+  if (tid <= k) {
+    float M = -INFINITY, S = 0.f;
+    bool nan = false;
+    for (int p = 0; p < kStatParts; ++p) {
+      const float2 v = pstats[tid * kStatParts + p];
+      if (isnan(v.x) || isnan(v.y)) nan = true;
+      else ms_merge(M, S, v.x, v.y);
+    }
+    const float2 r = nan ? make_float2(NAN, NAN) : make_float2(M, S);
+    rs[tid] = r;
+    stats_out[tid] = r;
+  }
   __syncthreads();
   if (tid == 0) {
     int s = step_state ? *status : 0;
     for (int i = 0; i < k; ++i)
       if (draft[i] < 0 || draft[i] >= V) s |= SPEC_ST_TOKEN_RANGE;
     for (int row = 0; row <= k; ++row) {
-      const float2 ms = stats[row];
+      const float2 ms = rs[row];
       if (!(ms.y > 0.f) || !isfinite(ms.x) || !isfinite(ms.y)) s |= SPEC_ST_NONFINITE;
     }
     int L = k;
@@ -167,7 +194,7 @@ sample_decide_kernel(const float* __restrict__ logits, const float* __restrict__
     if (!s) {
       for (int i = 0; i < k; ++i) {
         const int x = draft[i];
-        const float2 ms = stats[i];
+        const float2 ms = rs[i];
         const float p = expf(logits[(size_t)i * V + x] - ms.x) / ms.y;
         const float qx = q[(size_t)i * V + x];
         const float a = qx <= 0.f ? 1.f : fminf(p / qx, 1.f);
@@ -316,17 +343,18 @@ cudaError_t launch_sample_accept(const float* logits, const float* q, const int3
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(k + 1);
+  cfg.gridDim = dim3(kStatParts, k + 1);
   cfg.blockDim = dim3(kSampleThreads);
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
   SampleScratch* sc = reinterpret_cast<SampleScratch*>(scratch);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, softmax_stats_kernel, logits, V, stats);
+  float2* pstats = reinterpret_cast<float2*>(scratch + kPstatsOffset);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, softmax_stats_kernel, logits, V, pstats);
   if (e != cudaSuccess) return e;
   cfg.gridDim = dim3(1);
-  e = cudaLaunchKernelEx(&cfg, sample_decide_kernel, logits, q, draft, k, V, (const float2*)stats, mt,
-                         step_state, (const int32_t*)status, sc);
+  e = cudaLaunchKernelEx(&cfg, sample_decide_kernel, logits, q, draft, k, V, mt, step_state,
+                         (const int32_t*)status, sc, (const float2*)pstats, stats);
   if (e != cudaSuccess) return e;
   cfg.gridDim = dim3((V + kSampleThreads - 1) / kSampleThreads);
   e = cudaLaunchKernelEx(&cfg, sample_tiles_kernel, logits, q, k, V, (const float2*)stats, sc);

@@ -79,6 +79,8 @@ def lib():
         _lib.orc_mt_seed.argtypes = [C.c_void_p, C.c_uint32]
         _lib.orc_uniform_f32.restype = C.c_float
         _lib.orc_uniform_f32.argtypes = [C.c_void_p]
+        _lib.orc_sample_ordered.restype = C.c_int32
+        _lib.orc_sample_ordered.argtypes = [C.c_void_p, C.c_int, C.c_void_p, C.c_void_p]
         _lib.orc_sample_accept.argtypes = [C.c_void_p, C.c_void_p, C.c_void_p, C.c_int, C.c_int,
                                            C.c_void_p, C.c_void_p, C.c_void_p]
     return _lib
@@ -228,6 +230,16 @@ def softmax_row(logits: np.ndarray) -> np.ndarray:
     p = np.empty_like(logits)
     lib().orc_softmax_row(_p(logits), logits.shape[0], _p(p))
     return p
+
+
+def sample_ordered(w: np.ndarray, st: np.ndarray):
+    """One draw from the distribution w (fp32 [V]): (token, margin); st (625
+    words) is advanced in place."""
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    assert st.dtype == np.uint32
+    margin = C.c_double(0.0)
+    tok = lib().orc_sample_ordered(_p(w), w.shape[0], _p(st), C.byref(margin))
+    return int(tok), float(margin.value)
 
 
 def sample_accept(logits: np.ndarray, q: np.ndarray, draft: np.ndarray, st: np.ndarray):

@@ -328,44 +328,48 @@ void orc_softmax_row(const float* l, int V, float* p) {
     for (int x = 0; x < V; ++x) p[x] = (float)(exp((double)l[x] - m) / s);
 }
 
-/* Draw one token from the weights w over [0, V) (w >= 0, total = their sum):
- * one uniform u, then the tokens in index order with a running fp32 sum c of
- * the weights; the first token with u * total < c.  This is the walk over the
- * renormalised weights w / total with the division taken out of every term.
- * If rounding leaves c <= u * total at the end, the last token with w > 0.
- * (The pages walk a precomputed token order; index order is this reading.)
- * *margin receives the distance, in units of total, of u * total from the
- * nearest running-sum boundary around the chosen token. */
-static int32_t orc_sample_row(const float* w, int V, float total, uint32_t* mt, double* margin) {
+/* The draw of [33] §33.2 (sample_distribution_mt_ordered is named there, not
+ * printed): one uniform u, then the tokens of the row's order with a running
+ * fp32 sum c of their probabilities w; the first token with u < c.  The order
+ * is index order (the reading of "a precomputed token order"), restricted to
+ * the tokens with w > 0 as the listing filters it; a token of weight 0 adds
+ * nothing to c and can never be the first with u < c, so the walk below skips
+ * nothing explicitly.  If rounding leaves c <= u after the last token, the
+ * last token of the order (the last with w > 0).
+ * *margin receives the distance of u from the nearest running-sum boundary
+ * around the chosen token. */
+int32_t orc_sample_ordered(const float* w, int V, uint32_t* mt, double* margin) {
     const float u = orc_uniform_f32(mt);
-    const float t = u * total;
     float c = 0.f, prev = 0.f;
     int32_t last = -1;
     for (int x = 0; x < V; ++x) {
-        if (w[x] > 0.f) last = x;
+        if (!(w[x] > 0.f)) continue;
+        last = x;
         prev = c;
         c += w[x];
-        if (t < c) {
-            double d0 = (double)t - prev, d1 = (double)c - t;
-            *margin = (d0 < d1 ? d0 : d1) / total;
+        if (u < c) {
+            double d0 = (double)u - prev, d1 = (double)c - u;
+            *margin = d0 < d1 ? d0 : d1;
             return x;
         }
     }
-    *margin = ((double)t - c) / total;
+    *margin = (double)u - c;
     return last;
 }
 
-/* The accept rule of [33] §33.2 over k drafts:
+/* The accept rule of [33] §33.2 over k drafts, step by step as printed:
  *   for i < k: x = draft[i], p = p_i(x), q = q_i(x),
  *       a = 1 if q <= 0 else min(p / q, 1); one uniform u;
- *       u <= a: accept and go on; otherwise stop: the next token is drawn from
- *       the weights max(p_i - q_i, 0) (from p_i itself when they sum to 0);
- *   all accepted: the next token is drawn from the weights p_k.
+ *       u <= a: accept and go on; otherwise stop and build the residual
+ *       r = max(p_i - q_i, 0) (fp32, token by token), total = its fp32 sum in
+ *       token order; total <= 0: r = p_i; else every r_x /= total (fp32
+ *       division); the next token is drawn from r (orc_sample_ordered);
+ *   all accepted: the next token is drawn from p_k.
  * logits fp32 [k+1][V] (p = softmax, temperature 1); q fp32 [k][V] (the draft's
  * distributions); mt the 625-word MT19937 state, advanced by the draws.
  * res = {accepted, next}; *margin = the smallest distance of a uniform from
  * the threshold it was compared with (for tests that skip knife-edge draws).
- * Returns ORC_ST_TOKEN_RANGE for a draft token outside [0, V). */
+ * Returns ORC_ST_TOKEN_RANGE for a draft token outside [0, V), before any draw. */
 int orc_sample_accept(const float* logits, const float* q, const int32_t* draft, int k, int V,
                       uint32_t* mt, int32_t* res, double* margin) {
     for (int i = 0; i < k; ++i)
@@ -395,15 +399,13 @@ int orc_sample_accept(const float* logits, const float* q, const int32_t* draft,
         }
         if (total <= 0.f) {
             memcpy(r, p, sizeof(float) * (size_t)V);
-            total = 0.f;
-            for (int x = 0; x < V; ++x) total += p[x];
+        } else {
+            for (int x = 0; x < V; ++x) r[x] /= total;
         }
-        next = orc_sample_row(r, V, total, mt, &m1);
+        next = orc_sample_ordered(r, V, mt, &m1);
     } else {
         orc_softmax_row(logits + (size_t)k * V, V, p);
-        float total = 0.f;
-        for (int x = 0; x < V; ++x) total += p[x];
-        next = orc_sample_row(p, V, total, mt, &m1);
+        next = orc_sample_ordered(p, V, mt, &m1);
     }
     if (m1 < mg) mg = m1;
     free(p);

@@ -114,6 +114,11 @@ void     orc_mt_seed(uint32_t* st, uint32_t seed);
 uint32_t orc_mt_next(uint32_t* st);
 float    orc_uniform_f32(uint32_t* st);
 void     orc_softmax_row(const float* l, int V, float* p);
+/* one draw from the weights w [V] (a distribution): the first token in index
+ * order whose running fp32 sum exceeds one uniform u (the last token of
+ * positive weight if none does); *margin = distance of u from the nearest
+ * running-sum boundary around the chosen token */
+int32_t  orc_sample_ordered(const float* w, int V, uint32_t* mt, double* margin);
 int      orc_sample_accept(const float* logits, const float* q, const int32_t* draft, int k, int V,
                            uint32_t* mt, int32_t* res, double* margin);
 /* forward of M rows at positions seq_len..: reserves pages, appends K/V, sets

@@ -522,13 +522,132 @@ def test_sample_accept_guards_token_range():
     assert np.array_equal(st, before)              # no draw before the guard
 
 
+def _np_uniforms(seed, n):
+    """n uniforms of [33] §33.2's stream from numpy's MT19937 (an implementation
+    independent of the oracle's), converted as uniform_f32: top 24 bits x 2^-24"""
+    bg = np.random.MT19937(0)
+    bg._legacy_seeding(seed)
+    return (bg.random_raw(n).astype(np.uint64) >> np.uint64(8)).astype(np.float64) * 2.0 ** -24
+
+
+def test_softmax_closed_forms():
+    # logits ln(w) give p = w / sum(w); fp32 logits carry a relative error of
+    # ~6e-8 into p
+    for w in ([1.0, 3.0], [1.0, 2.0, 3.0, 4.0], [5.0, 1.0, 1.0, 1.0, 2.0]):
+        w = np.array(w)
+        p = oracle.softmax_row(np.log(w).astype(np.float32))
+        assert np.allclose(p, w / w.sum(), rtol=3e-7, atol=0), (p, w / w.sum())
+    # equal logits: exactly 1/V (a power of two), for any common offset
+    for c in (0.0, -3.5, 1000.0, -1000.0):
+        p = oracle.softmax_row(np.full(1024, c, dtype=np.float32))
+        assert np.all(p == np.float32(1.0 / 1024))
+
+
+def test_softmax_is_shift_invariant_without_overflow():
+    # integer logits c + (0, 1, 2, 3) are exact in fp32 for the offsets below;
+    # p_i = e^i / (1 + e + e^2 + e^3) whatever c is.  Without subtracting the
+    # max first, exp overflows (or underflows to 0/0) at these offsets.
+    want = np.exp(np.arange(4.0)) / np.exp(np.arange(4.0)).sum()
+    for c in (0.0, 88.0, 200.0, 1000.0, 3.0e4, -3.0e4, 1.0e6):
+        p = oracle.softmax_row((np.arange(4.0) + c).astype(np.float32))
+        assert np.all(np.isfinite(p))
+        assert np.allclose(p, want, rtol=2e-7, atol=0), (c, p, want)
+
+
+def test_softmax_is_temperature_one():
+    # doubling the logits squares the weights: p(2 ln w) = w^2 / sum(w^2);
+    # a temperature other than 1 would map 2 ln w elsewhere
+    w = np.array([1.0, 2.0, 3.0, 4.0])
+    p1 = oracle.softmax_row((np.log(w)).astype(np.float32))
+    p2 = oracle.softmax_row((2 * np.log(w)).astype(np.float32))
+    assert np.allclose(p2, w ** 2 / (w ** 2).sum(), rtol=5e-7)
+    assert not np.allclose(p1, p2, rtol=1e-2)
+    # two logits: p_1 = 1 / (1 + exp(l_0 - l_1)), the logistic function
+    for d in (-20.0, -3.0, -0.5, 0.0, 0.25, 4.0, 30.0):
+        p = oracle.softmax_row(np.array([0.0, d], dtype=np.float32))
+        assert abs(p[1] - 1.0 / (1.0 + math.exp(-d))) <= 1e-7 * max(1.0, 1.0 / (1.0 + math.exp(-d)))
+
+
+def test_softmax_ratios_and_normalisation():
+    # softmax is the unique vector with p_i / p_j = exp(l_i - l_j) and sum 1
+    rng = np.random.default_rng(5)
+    for V in (7, 300, 4096):
+        lg = rng.normal(0, 4, V).astype(np.float32)
+        p = oracle.softmax_row(lg).astype(np.float64)
+        assert abs(p.sum() - 1.0) < V * 1e-7
+        j = int(np.argmax(lg))
+        ratio = p / p[j]
+        want = np.exp(lg.astype(np.float64) - float(lg[j]))
+        keep = want > 1e-30
+        assert np.allclose(ratio[keep], want[keep], rtol=3e-7)
+        # and an independent fp64 softmax with an explicit max shift
+        e = np.exp(lg.astype(np.float64) - lg.astype(np.float64).max())
+        assert np.allclose(p, e / e.sum(), rtol=1e-7, atol=1e-45)
+
+
+def test_ordered_draw_walks_the_running_sum():
+    # the uniforms of seed 5489 from numpy's MT19937; the draw returns the
+    # first token whose running sum exceeds u, never a token of weight 0
+    u = _np_uniforms(5489, 6)
+    st = oracle.mt_seed(5489)
+    tok, _ = oracle.sample_ordered(np.full(10, 0.1, dtype=np.float32), st)
+    assert tok == int(u[0] * 10)
+    tok, _ = oracle.sample_ordered(np.array([0.0, 0.5, 0.0, 0.5], dtype=np.float32), st)
+    assert tok == (1 if u[1] < 0.5 else 3)
+    w = np.array([0.0, 0.25, 0.0, 0.0, 0.75, 0.0], dtype=np.float32)
+    for i in range(2, 6):
+        tok, margin = oracle.sample_ordered(w, st)
+        assert tok == (1 if u[i] < 0.25 else 4) and margin == pytest.approx(
+            min(abs(u[i] - 0.25), u[i] if u[i] < 0.25 else 1.0 - u[i]), abs=1e-7)
+    # a sum that rounding leaves below u: the last token of positive weight
+    st = oracle.mt_seed(5489)
+    tok, _ = oracle.sample_ordered(np.array([0.0, 1e-9, 0.0], dtype=np.float32), st)
+    assert tok == 1
+
+
+def test_reject_draws_from_the_renormalised_residual():
+    # p = (1, 1, 2) / 4, draft token 0 with q = one-hot at 0: accept with
+    # probability min(p_0 / q_0, 1) = 1/4; on rejection the residual
+    # max(p - q, 0) = (0, 1/4, 1/2) renormalises to (0, 1/3, 2/3).
+    # Decisions are recomputed here from numpy's MT19937 stream.
+    lg = np.log(np.array([[1.0, 1.0, 2.0], [1.0, 1.0, 1.0]])).astype(np.float32)
+    q = np.array([[1.0, 0.0, 0.0]], dtype=np.float32)
+    draft = np.array([0], dtype=np.int32)
+    for seed in range(200):
+        u = _np_uniforms(seed, 2)
+        L, nxt, rc, margin = oracle.sample_accept(lg, q, draft, oracle.mt_seed(seed))
+        assert rc == 0
+        if margin < 1e-6:
+            continue
+        if u[0] <= 0.25:
+            assert L == 1 and 0 <= nxt < 3                  # accepted: next drawn from p_1
+            assert nxt == int(u[1] * 3)
+        else:
+            assert L == 0 and nxt == (1 if u[1] < 1.0 / 3.0 else 2)
+    # total <= 0: p_0 == q_0 exactly leaves no residual, and the draw uses p_0
+    lg2 = np.zeros((2, 4), dtype=np.float32)
+    q2 = np.full((1, 4), 0.25, dtype=np.float32)
+    q2[0, 3] = 0.0
+    q2[0, 0] = 0.5                                  # p_0 = 1/4 each: residual (0, 0, 0, 1/4)
+    for seed in range(50):
+        u = _np_uniforms(seed, 2)
+        L, nxt, rc, margin = oracle.sample_accept(lg2, q2, np.array([0], dtype=np.int32),
+                                                  oracle.mt_seed(seed))
+        if margin < 1e-6:
+            continue
+        if u[0] > 0.5:                              # a = min(0.25 / 0.5, 1) = 0.5
+            assert (L, nxt) == (0, 3)               # the residual is one-hot at token 3
+
+
 def test_sample_accept_first_token_follows_the_target():
     # the rule's invariant: whatever q is, the first emitted token (the draft
-    # if accepted, else the residual draw) is distributed as p_0
+    # if accepted, else the residual draw) is distributed as p_0.  p_0 is
+    # fixed in closed form by logits ln(w): p_0 = w / sum(w).
     rng = np.random.default_rng(11)
     V, N = 12, 24000
-    lg0 = rng.normal(0, 1.5, V).astype(np.float32)
-    p0 = oracle.softmax_row(lg0)
+    w = np.arange(1, V + 1, dtype=np.float64) ** 1.5
+    p0 = w / w.sum()
+    lg0 = np.log(w).astype(np.float32)
     q0 = rng.dirichlet(np.ones(V) * 0.7).astype(np.float32)
     logits = np.stack([lg0, rng.normal(0, 1, V).astype(np.float32)])
     st = oracle.mt_seed(2024)
@@ -541,7 +660,7 @@ def test_sample_accept_first_token_follows_the_target():
         assert rc == 0
         counts[x0 if L == 1 else nxt] += 1
         acc += L
-    expect = N * p0.astype(np.float64)
+    expect = N * p0
     chi2 = float(np.sum((counts - expect) ** 2 / expect))
     # 11 degrees of freedom: P(chi2 > 35) < 3e-4
     assert chi2 < 35.0, (chi2, counts, expect)

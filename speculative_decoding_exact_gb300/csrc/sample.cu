@@ -9,15 +9,20 @@
 // p_i = softmax of the target logits of row i (temperature 1); q_i = the
 // draft's distribution at position i.  Every uniform comes from a caller-owned
 // MT19937 stream (Matsumoto & Nishimura 1998), one per attempted draft and one
-// for the final draw, in that order; uniform = top 24 bits x 2^-24.  A draw
-// walks the tokens in index order and returns the first whose running sum of
-// weights exceeds u x (their total), i.e. the walk over the renormalised
-// weights with the division taken out of every term (the last token of
-// positive weight if rounding leaves none).
+// for the final draw, in that order; uniform = top 24 bits x 2^-24.  As the
+// listing of §33.2 does, a rejection's residual r = max(p_i - q_i, 0) is
+// summed (total) and every entry divided by total, unless total <= 0, when
+// the draw uses p_i itself.  A draw walks the tokens in index order and
+// returns the first whose running sum of the draw weights exceeds u (the last
+// token of positive weight if rounding leaves none).  The device sums in a
+// fixed tree order, not token by token, so totals may differ from a serial
+// sum by rounding.
 //
 // Kernels: row normalizers (8 CTAs per row), the decisions and the final
-// uniform (one CTA), per-tile sums of the drawn row (one CTA per
-// kSampleThreads tokens, coalesced), the draw and the rollback (one CTA).
+// uniform (one CTA), per-tile sums of the drawn row's raw weights (one CTA
+// per kSampleThreads tokens, coalesced), per-tile sums of its draw weights
+// (the same tiles, after the total is known), the draw and the rollback (one
+// CTA).
 #include "common.cuh"
 #include "internal.h"
 #include "kvmeta.cuh"
@@ -134,7 +139,8 @@ SPEC_DEV float block_inclusive_scan(float v, float* sh, float* total) {
 
 // Scratch of one decision (device): L, the final uniform, the status, then
 // per tile of kSampleThreads tokens the sums and the last positive index of
-// the weights w (the residual or p_k) and of p.
+// the raw weights w (the residual or p_k) and of p, and the sums of the draw
+// weights (w / total, or p).
 struct SampleScratch {
   int L;
   float u;
@@ -143,7 +149,7 @@ struct SampleScratch {
 };
 constexpr int kMaxTiles = 1024;              // V <= 1024 * kSampleThreads
 // then the row normalizers' parts: float2 [16 rows][kStatParts]
-constexpr size_t kPstatsOffset = sizeof(SampleScratch) + 4 * sizeof(float) * kMaxTiles;
+constexpr size_t kPstatsOffset = sizeof(SampleScratch) + 5 * sizeof(float) * kMaxTiles;
 size_t sample_scratch_bytes() { return kPstatsOffset + sizeof(float2) * 16 * kStatParts; }
 
 // weight of token x of the drawn row: max(p - q, 0) for a rejection, p else
@@ -250,11 +256,51 @@ sample_tiles_kernel(const float* __restrict__ logits, const float* __restrict__ 
   }
 }
 
+// total of the raw weights: the block scan of the raw tile sums (thread t
+// holds tile t), the same expression in every kernel that needs it
+SPEC_DEV float raw_total(const float* t, int ntiles, float* sh) {
+  float tot;
+  block_inclusive_scan(threadIdx.x < ntiles ? t[threadIdx.x] : 0.f, sh, &tot);
+  return tot;
+}
+
+// weight of token x in the draw: the residual divided by its total, or p
+// (the residual summed to <= 0, or all drafts were accepted)
+SPEC_DEV float draw_weight(const float* lr, const float* qr, float2 ms, int x, int V, bool resid,
+                           bool use_p, float tot) {
+  if (x >= V) return 0.f;
+  const float p = expf(lr[x] - ms.x) / ms.y;
+  return (resid && !use_p) ? __fdiv_rn(fmaxf(p - qr[x], 0.f), tot) : p;
+}
+
+// ---- per tile of kSampleThreads tokens of the drawn row: the sum of the
+// draw weights (the block scan's last value), after the total is known
+__global__ void __launch_bounds__(kSampleThreads)
+sample_norm_tiles_kernel(const float* __restrict__ logits, const float* __restrict__ q, int k, int V,
+                         const float2* __restrict__ stats, SampleScratch* sc) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ float sh[64];
+  if (sc->status) return;
+  const int L = sc->L, j = blockIdx.x, tid = threadIdx.x;
+  const bool resid = L < k;
+  const int ntiles = (V + kSampleThreads - 1) / kSampleThreads;
+  float* t = reinterpret_cast<float*>(sc + 1);
+  const float tot = raw_total(t, ntiles, sh);
+  const bool use_p = resid && !(tot > 0.f);
+  const float* lr = logits + (size_t)L * V;
+  const float* qr = resid ? q + (size_t)L * V : nullptr;
+  const float v = draw_weight(lr, qr, stats[L], j * kSampleThreads + tid, V, resid, use_p, tot);
+  float tv;
+  block_inclusive_scan(v, sh, &tv);
+  if (tid == 0) t[4 * kMaxTiles + j] = tv;
+}
+
 // ---- the draw and the rollback: one CTA.  With prefix_j the inclusive scan
-// of the tile sums up to tile j-1, the running sum at token x of tile j is
-// prefix_j + (the tile's inclusive scan at x); the drawn token is the first
-// with u * total < that sum, found in the first tile with
-// u * total < prefix_j + tile_j (the same expression as its last token).
+// of the draw-weight tile sums up to tile j-1, the running sum at token x of
+// tile j is prefix_j + (the tile's inclusive scan at x); the drawn token is
+// the first with u < that sum, found in the first tile with
+// u < prefix_j + tile_j (the same expression as its last token).
 __global__ void __launch_bounds__(kSampleThreads)
 sample_finish_kernel(const float* __restrict__ logits, const float* __restrict__ q, int k, int V,
                      const float2* __restrict__ stats, const SampleScratch* sc, KvView kv, int has_kv,
@@ -264,6 +310,7 @@ sample_finish_kernel(const float* __restrict__ logits, const float* __restrict__
   __shared__ float sh[64];
   __shared__ int hit_tile, hit_x, last;
   __shared__ float prefix_hit;
+  __shared__ float incl[kMaxTiles];
   const int tid = threadIdx.x;
   const int s = sc->status;
   int next = -1;
@@ -273,26 +320,24 @@ sample_finish_kernel(const float* __restrict__ logits, const float* __restrict__
     const int ntiles = (V + kSampleThreads - 1) / kSampleThreads;
     const float* t = reinterpret_cast<const float*>(sc + 1);
     const int* ti = reinterpret_cast<const int*>(t);
-    float tot;
-    float inc = block_inclusive_scan(tid < ntiles ? t[tid] : 0.f, sh, &tot);
+    const float tot = raw_total(t, ntiles, sh);
     const bool use_p = resid && !(tot > 0.f);     // residual all zero: draw from p_L itself
-    if (use_p) inc = block_inclusive_scan(tid < ntiles ? t[kMaxTiles + tid] : 0.f, sh, &tot);
-    const float mine = tid < ntiles ? (use_p ? t[kMaxTiles + tid] : t[tid]) : 0.f;
+    const float mine = tid < ntiles ? t[4 * kMaxTiles + tid] : 0.f;
+    float all;
+    const float inc = block_inclusive_scan(mine, sh, &all);
     if (tid == 0) {
       hit_tile = 0x7fffffff;
       hit_x = 0x7fffffff;
       last = -1;
     }
-    __syncthreads();
     // inclusive value of the previous tile (prefix_j), from the neighbour
-    __shared__ float incl[kMaxTiles];
     if (tid < ntiles) incl[tid] = inc;
     __syncthreads();
     const float prefix = tid > 0 && tid < ntiles ? incl[tid - 1] : 0.f;
-    const float T = sc->u * tot;
-    if (tid < ntiles && T < prefix + mine) atomicMin(&hit_tile, tid);
+    const float u = sc->u;
+    if (tid < ntiles && u < prefix + mine) atomicMin(&hit_tile, tid);
     if (tid < ntiles) {
-      const int lt = use_p ? ti[3 * kMaxTiles + tid] : ti[2 * kMaxTiles + tid];
+      const int lt = (resid && !use_p) ? ti[2 * kMaxTiles + tid] : ti[3 * kMaxTiles + tid];
       if (lt >= 0) atomicMax(&last, lt);
     }
     __syncthreads();
@@ -303,10 +348,10 @@ sample_finish_kernel(const float* __restrict__ logits, const float* __restrict__
       const float* lr = logits + (size_t)L * V;
       const float* qr = resid ? q + (size_t)L * V : nullptr;
       const int x = j * kSampleThreads + tid;
-      const float w = sample_weight(lr, qr, stats[L], x, V, resid, use_p);
+      const float v = draw_weight(lr, qr, stats[L], x, V, resid, use_p, tot);
       float tt;
-      const float c = prefix_hit + block_inclusive_scan(w, sh, &tt);
-      if (x < V && T < c) atomicMin(&hit_x, x);
+      const float c = prefix_hit + block_inclusive_scan(v, sh, &tt);
+      if (x < V && v > 0.f && u < c) atomicMin(&hit_x, x);
       __syncthreads();
       // a ragged last tile can miss by an ulp: its scan over the valid tokens
       // need not repeat the tile sum bit for bit
@@ -358,6 +403,8 @@ cudaError_t launch_sample_accept(const float* logits, const float* q, const int3
   if (e != cudaSuccess) return e;
   cfg.gridDim = dim3((V + kSampleThreads - 1) / kSampleThreads);
   e = cudaLaunchKernelEx(&cfg, sample_tiles_kernel, logits, q, k, V, (const float2*)stats, sc);
+  if (e != cudaSuccess) return e;
+  e = cudaLaunchKernelEx(&cfg, sample_norm_tiles_kernel, logits, q, k, V, (const float2*)stats, sc);
   if (e != cudaSuccess) return e;
   cfg.gridDim = dim3(1);
   KvView v = kv ? *kv : KvView{};

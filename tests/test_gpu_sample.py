@@ -5,9 +5,10 @@ Bit-exact: the MT19937 state after every call (the device draws exactly the
 oracle's uniforms, regenerations included).  Decisions (accepted length, drawn
 token): equal to the oracle's on the same logits, q, drafts and stream
 whenever no uniform lies within 1e-5 of the threshold it is compared with
-(the two sides compute p with different exp implementations and sums);
-skipped draws are counted and must stay rare.  Distribution: the first
-emitted token follows the target's p_0 (chi-square).
+(the two sides compute p with different exp implementations, and the
+residual's total in different summation orders); every test counts the
+trials it skips and bounds that count.  Distribution: the first emitted token
+follows the target's p_0 (chi-square against p_0 in closed form).
 """
 import math
 
@@ -101,21 +102,27 @@ def test_sample_accept_matches_oracle(small_ctx, k):
             skipped += 1
             continue
         assert (res[0], res[1]) == (L, nxt), (t, res, L, nxt, margin)
+    print(f"k={k}: {skipped} of {trials} trials skipped (a uniform within {MARGIN} of its threshold)")
     assert skipped <= 2, f"{skipped} of {trials} trials had a uniform within {MARGIN} of its threshold"
 
 
 def test_sample_accept_full_vocab(full_ctx):
     ctx, V, k = full_ctx, FULL.vocab, 15
     rng = np.random.default_rng(5)
-    for t in range(6):
+    skipped, trials = 0, 8
+    for t in range(trials):
         ost, dst = mt_device(900 + t)
         logits, q, draft = random_case(rng, k, V, scale=4.0)
         res = gpu_sample(ctx, logits, q, draft, dst)
         L, nxt, rc, margin = oracle.sample_accept(logits, q, draft, ost)
         assert rc == 0 and res[2] == 0
         assert np.array_equal(dst.cpu().numpy().view(np.uint32), ost)
-        if margin > MARGIN:
-            assert (res[0], res[1]) == (L, nxt), (t, res, L, nxt)
+        if margin <= MARGIN:
+            skipped += 1
+            continue
+        assert (res[0], res[1]) == (L, nxt), (t, res, L, nxt)
+    print(f"full vocabulary: {skipped} of {trials} trials skipped (a uniform within {MARGIN} of its threshold)")
+    assert skipped <= 1
 
 
 def test_sample_accept_one_hot_is_greedy(small_ctx):
@@ -134,8 +141,9 @@ def test_sample_accept_one_hot_is_greedy(small_ctx):
         ost, dst = mt_device(40 + t)
         res = gpu_sample(ctx, logits, q, draft, dst)
         _, _, _, margin = oracle.sample_accept(logits, q, draft, ost)
-        if margin > 0:
-            assert (res[0], res[1]) == (L_t, idx[L_t])
+        # margin 0: a uniform of exactly 0 accepts a draft of p = 0 (u <= a)
+        assert margin > 0, "a uniform of exactly 0 in this stream; pick another seed"
+        assert (res[0], res[1]) == (L_t, idx[L_t])
 
 
 def test_sample_accept_device_errors_draw_nothing(small_ctx):
@@ -153,14 +161,16 @@ def test_sample_accept_device_errors_draw_nothing(small_ctx):
 
 
 def test_sample_accept_first_token_follows_target(small_ctx):
-    # 16 live tokens (the others have p = 0 exactly); draft x0 ~ q0 per trial
+    # 16 live tokens (the others have p = 0 exactly) with logits ln(w): p_0 =
+    # w / sum(w) in closed form; draft x0 ~ q0 per trial
     ctx, V = small_ctx, SMALL.vocab
     rng = np.random.default_rng(21)
     live = np.sort(rng.choice(V, 16, replace=False))
+    w = np.arange(1, 17, dtype=np.float64)
     logits = np.full((2, V), -1.0e4, dtype=np.float32)
-    logits[0, live] = rng.normal(0, 1.2, 16).astype(np.float32)
+    logits[0, live] = np.log(w).astype(np.float32)
     logits[1, live] = rng.normal(0, 1.2, 16).astype(np.float32)
-    p0 = oracle.softmax_row(logits[0])[live].astype(np.float64)
+    p0 = w / w.sum()
     q = np.zeros((1, V), dtype=np.float32)
     q[0, live] = rng.dirichlet(np.ones(16)).astype(np.float32)
     cq = np.cumsum(q[0, live].astype(np.float64))
@@ -201,6 +211,7 @@ def test_sampled_step_matches_oracle_on_its_logits():
         ow, dw = build_model(ctx, cfg, seed=3)
         k, n_past = 15, 71
         rng = np.random.default_rng(8)
+        skipped = 0
         for t in range(3):
             dkv = runtime.DeviceKV(cfg, 24, 24)
             dkv.reset(ctx)
@@ -235,9 +246,13 @@ def test_sampled_step_matches_oracle_on_its_logits():
             L, nxt, rc, margin = oracle.sample_accept(logits, q, draft, ost)
             assert rc == 0 and r[2] == 0
             assert np.array_equal(dst.cpu().numpy().view(np.uint32), ost)
-            if margin > MARGIN:
+            if margin <= MARGIN:
+                skipped += 1
+            else:
                 assert (r[0], r[1]) == (L, nxt)
             # the KV keeps the frontier and the accepted drafts
             assert r[3] == n_past + r[0] + 1 == dkv.state()[0]
+        print(f"sampled step: {skipped} of 3 decisions skipped (a uniform within {MARGIN} of its threshold)")
+        assert skipped <= 1
     finally:
         ctx.close()

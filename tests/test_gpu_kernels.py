@@ -14,7 +14,7 @@ torch = pytest.importorskip("torch")
 
 import oracle  # noqa: E402
 from speculative_decoding_exact_gb300 import abi, runtime, synth  # noqa: E402
-from tests.gpu_util import assert_close  # noqa: E402
+from tests.gpu_util import require_clear_rows, assert_close  # noqa: E402
 
 SMALL = runtime.ModelConfig(hidden=3328, n_layers=2, n_q_heads=26, n_kv_heads=2, head_dim=128,
                             ffn=8960, vocab=4096)
@@ -139,6 +139,66 @@ def test_gemm_integer_sums_bit_exact(ctx, M, N, K):
     assert_close(y, oy, what="y")
 
 
+def _extreme_superblocks(rng, n):
+    """n canonical superblocks drawn from three extreme patterns: every code 15
+    with sc = m = 63 (the largest sums), codes alternating 0/15 with sc
+    alternating 63/0 per sub-block, and random codes in {0, 15} with random
+    sc, m in {0, 63}.  d and dmin vary over [1e-3, 1e-2)."""
+    from tests.q4k_pack import pack_superblock
+    out = np.empty((n, 144), dtype=np.uint8)
+    for i in range(n):
+        kind = i % 3
+        d, dmin = float(rng.uniform(1e-3, 1e-2)), float(rng.uniform(1e-3, 1e-2))
+        if kind == 0:
+            sc, m, codes = [63] * 8, [63] * 8, [15] * 256
+        elif kind == 1:
+            sc, m, codes = [63, 0] * 4, [63] * 8, [15 * (e % 2) for e in range(256)]
+        else:
+            sc = list(63 * rng.integers(0, 2, 8))
+            m = list(63 * rng.integers(0, 2, 8))
+            codes = list(15 * rng.integers(0, 2, 256))
+        out[i] = pack_superblock(d, dmin, sc, m, codes)
+    return out
+
+
+def _extreme_rows(rng, K):
+    """16 activation rows whose codes are all +-127 (or 0): constant +1, constant
+    -1, sign alternating per element, per sub-block and per superblock, and
+    random signs (some rows with zeros); any amax gives codes +-127 here."""
+    e = np.arange(K)
+    rows = [np.ones(K), -np.ones(K), np.where(e % 2, -1.0, 1.0), np.where((e // 32) % 2, -1.0, 1.0),
+            np.where((e // 256) % 2, -1.0, 1.0) * 3.5]
+    while len(rows) < 16:
+        r = rng.choice([-1.0, 1.0], K)
+        if len(rows) % 3 == 0:
+            r = r * rng.integers(0, 2, K)           # codes in {-127, 0, 127}
+            r[::256] = 1.0                          # keep every block's amax at 1
+        rows.append(r * float(rng.uniform(0.01, 100.0)))
+    return np.stack(rows).astype(np.float32)
+
+
+@pytest.mark.parametrize("K", [256, 17920])
+def test_gemm_integer_sums_exact_at_extreme_magnitudes(ctx, K):
+    """The tensor-core path keeps S_j, ISc and IMn exact at their largest
+    magnitudes (|S_j| = 32*15*127 = 60960, |ISc| up to 8*63*60960, IMn up
+    to 8*63*32*127): codes 15, scales and mins 63, activation codes +-127, and
+    alternating-sign extremes, over one superblock and over 70."""
+    rng = np.random.default_rng(K)
+    N, nb = 256, K // 256
+    W = _extreme_superblocks(rng, N * nb).reshape(-1)
+    x = _extreme_rows(rng, K)
+    Wt = runtime.upload_tiled(ctx, W, N, K)
+    y, isc, imn = run_gemm(ctx, Wt, N, K, x, sums=True)
+    q, da, A, st = oracle.quantize_q8(x)
+    assert st == 0 and np.all(np.isin(q, [-127, 0, 127]))
+    oy, oisc, oimn, _ = oracle.gemm_q4k(W, N, K, q, da, A, sums=True)
+    assert int(np.max(np.abs(oisc))) == 8 * 63 * 60960      # the extremes are reached
+    assert int(np.max(np.abs(oimn))) == 8 * 63 * 32 * 127
+    assert np.array_equal(isc, oisc), "ISc differs"
+    assert np.array_equal(imn, oimn), "IMn differs"
+    assert_close(y, oy, what="y")
+
+
 @pytest.mark.parametrize("N", [6656, 26624])
 def test_gemm_full_width_sampled(ctx, N):
     """Projection sweep shapes (K=6656, M=16): all outputs on the GPU, a sample of
@@ -192,11 +252,13 @@ def test_gemm_batch_height_invariance(ctx):
 # ---------------------------------------------------------------------------
 # LM head + argmax
 # ---------------------------------------------------------------------------
-@pytest.mark.parametrize("M", [4, 16])
-def test_lm_head_argmax(small_ctx, M):
+@pytest.mark.parametrize("M,centred", [(4, False), (16, False), (16, True)])
+def test_lm_head_argmax(small_ctx, M, centred):
+    """centred: zero-mean weights (dmin = 7.5 d), so the rows' argmaxes differ
+    and the cross-CTA reduction decides among many columns."""
     ctx = small_ctx
     V, H = SMALL.vocab, SMALL.hidden
-    W = synth.q4k_matrix(V, H, 7, M)
+    W = synth.q4k_matrix(V, H, 7, M, dmin_over_d=7.5 if centred else None)
     x = synth.normal((M, H), 7, 3) * 3.0
     gamma = (1.0 + 0.1 * synth.normal((H,), 7, 4)).astype(np.float32)
     Wt = runtime.upload_tiled(ctx, W, V, H)
@@ -212,8 +274,10 @@ def test_lm_head_argmax(small_ctx, M):
     oidx, gap = oracle.argmax(olg)
     assert_close(lg.cpu().numpy(), olg, what="logits")
     gi = idx.cpu().numpy()
-    ok = gap > 1e-2
-    assert np.array_equal(gi[ok], oidx[ok]), "argmax differs on rows with a clear top-2 gap"
+    require_clear_rows(gap, f"head rows (M={M}, centred={centred})")
+    assert np.array_equal(gi, oidx), "argmax differs from the oracle"
+    if centred:
+        assert len(set(oidx.tolist())) >= M // 2, "centred weights should spread the argmax"
     # the fused argmax equals the argmax of the kernel's own logits (lowest index on ties)
     assert np.array_equal(gi, np.argmax(lg.cpu().numpy(), axis=1))
 

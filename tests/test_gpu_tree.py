@@ -3,7 +3,8 @@ through spec_verify_tree.
 
 Bit-exact: a chain tree equals the linear verify step (result, argmax, logits,
 KV metadata and rows); the tree step's result, accepted path and committed KV
-metadata equal the oracle's when every node's top-2 gap is clear (> 1e-2);
+metadata equal the oracle's (every node's top-2 gap must be clear, > 1e-2:
+the tests count the nodes below it and require none);
 the path's K/V rows after the moves equal the oracle's to one bf16 ulp.
 Tolerance: logits.
 """
@@ -16,7 +17,7 @@ torch = pytest.importorskip("torch")
 
 import oracle  # noqa: E402
 from speculative_decoding_exact_gb300 import abi, runtime, synth  # noqa: E402
-from tests.gpu_util import assert_close  # noqa: E402
+from tests.gpu_util import assert_close, require_clear_rows  # noqa: E402
 from tests.model_util import build_model, fill_context, ocfg_of  # noqa: E402
 
 SMALL = runtime.ModelConfig(hidden=3328, n_layers=2, n_q_heads=26, n_kv_heads=2, head_dim=128,
@@ -140,12 +141,11 @@ def test_tree_step_matches_oracle(model, seed):
     assert res[2] == 0
     assert_close(lg, olg, what="logits")
     _, gap = oracle.argmax(olg)
-    clear = gap > 1e-2
-    assert np.array_equal(am[clear], oidx[clear])
-    if np.all(clear):
-        assert list(res) == list(ores)
-        assert np.array_equal(path[: res[0] + 1], opath) and np.all(path[res[0] + 1:] == -1)
-        kv_rows_equal(dkv, okv, int(ores[3]))
+    require_clear_rows(gap, f"tree {seed} nodes")
+    assert np.array_equal(am, oidx)
+    assert list(res) == list(ores)
+    assert np.array_equal(path[: res[0] + 1], opath) and np.all(path[res[0] + 1:] == -1)
+    kv_rows_equal(dkv, okv, int(ores[3]))
 
 
 def test_tree_graph_replay_and_bad_tree(model):

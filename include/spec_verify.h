@@ -304,6 +304,15 @@ SPEC_API int spec_gemm_q4k_sums(spec_ctx* ctx, const void* w_tiled, int N, int K
 SPEC_API int spec_gemm_q4k_noalloc(const void* w_tiled, int N, int K, const float* x, int M,
                                    float* y, void* cuda_stream);
 
+/* Device status of the last spec_gemm_q4k_noalloc call on the current device:
+ * synchronises cuda_stream (the stream that call was enqueued on), then reads
+ * the status word at the start of the fixed array without allocating.
+ * Returns SPEC_ST_* bits (0 = OK; SPEC_ST_NONFINITE: a non-finite activation;
+ * SPEC_ST_DEVICE_WAIT: a bounded device wait gave up and y is incomplete), or
+ * a negative code.  Every call clears the word first, so it describes only the
+ * latest call; calls that overlap on the GPU share it. */
+SPEC_API int spec_gemm_q4k_noalloc_status(void* cuda_stream);
+
 /* Final RMSNorm (gain final_norm, NULL = ones) + LM head (TILED Q4_K,
  * N = cfg.vocab, K = cfg.hidden) + per-row argmax, lowest index on ties.
  * x DEVICE fp32 [M][H]; idx DEVICE int32 [M]; logits DEVICE fp32 [M][V] or

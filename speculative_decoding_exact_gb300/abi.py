@@ -75,6 +75,7 @@ _SIGS = {
     "spec_profile_gemms": (I, [P, I]),
     "spec_profile_read": (I, [P, C.POINTER(C.c_float), C.POINTER(C.c_int)]),
     "spec_gemm_q4k_noalloc": (I, [P, I, I, P, I, P, P]),
+    "spec_gemm_q4k_noalloc_status": (I, [P]),
     "spec_mt_seed": (I, [P, C.c_uint32]),
     "spec_set_capture": (I, [P, P, I, P]),
     "spec_verify_tree": (I, [P, C.POINTER(spec_weights), C.POINTER(spec_kv), P, P, P, I, P, P,
@@ -242,3 +243,7 @@ def spec_profile_read(ctx):
 
 def spec_gemm_q4k_noalloc(w, N, K, x, M, y, stream) -> int:
     return _call("spec_gemm_q4k_noalloc", P(w), N, K, P(x), M, P(y), P(stream or 0))
+
+
+def spec_gemm_q4k_noalloc_status(stream) -> int:
+    return _call("spec_gemm_q4k_noalloc_status", P(stream or 0))

@@ -495,16 +495,14 @@ gemm_q4k_kernel(const uint8_t* __restrict__ wt, const uint8_t* __restrict__ act,
   }
 }
 
-static bool g_gemm_attr_set[2] = {false, false};
-
+// The kernel's dynamic shared memory exceeds the default limit; the limit is
+// a per-device attribute, raised on every device that runs the GEMM (by
+// spec_verify_init for a ctx, and on a device's first allocation-free call).
 cudaError_t gemm_init_attributes() {
   const int smem = (int)gemm_smem_bytes();
   cudaError_t e = cudaFuncSetAttribute(gemm_q4k_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(gemm_q4k_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
-  g_gemm_attr_set[0] = g_gemm_attr_set[1] = true;
-  return cudaSuccess;
+  return cudaFuncSetAttribute(gemm_q4k_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
 }
 
 cudaError_t launch_gemm(const GemmPlan& p, const void* w_tiled, const uint8_t* act, float* pieces,
@@ -513,11 +511,6 @@ cudaError_t launch_gemm(const GemmPlan& p, const void* w_tiled, const uint8_t* a
   const size_t smem = gemm_smem_bytes();
   const bool sums = isc != nullptr;
   auto kern = sums ? gemm_q4k_kernel<true> : gemm_q4k_kernel<false>;
-  if (!g_gemm_attr_set[sums]) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    g_gemm_attr_set[sums] = true;
-  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.G);
   cfg.blockDim = dim3(kGemmThreads);

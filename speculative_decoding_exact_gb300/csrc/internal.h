@@ -35,7 +35,7 @@ constexpr int kGemmCtasPerSm = 1;
 constexpr int kMaxSlots = 8;      // pieces per group, guaranteed by make_gemm_plan
 
 GemmPlan make_gemm_plan(int N, int K, int num_sms);
-cudaError_t gemm_init_attributes();   // once per process, before any capture
+cudaError_t gemm_init_attributes();   // once per device, before any launch or capture
 size_t gemm_smem_bytes();
 // slots of group gr, and the CTA owning a unit (host mirror of the device math)
 int plan_slots_of_group(const GemmPlan& p, int gr);

@@ -19,8 +19,13 @@
 //     overlaps on the GPU (different streams, no ordering between them) race
 //     and corrupt each other's results; calls ordered on one stream are safe;
 //   * the first call on a device looks up the array's device address with
-//     cudaGetSymbolAddress while that device is current; make that first call
-//     before capturing any stream into a CUDA graph.
+//     cudaGetSymbolAddress while that device is current, and raises the GEMM
+//     kernel's shared-memory limit on that device; make that first call before
+//     capturing any stream into a CUDA graph;
+//   * device-detected conditions (a non-finite activation, a bounded device
+//     wait that gave up, after which y is incomplete) are OR-ed into a status
+//     word at the start of the array, cleared by every call;
+//     spec_gemm_q4k_noalloc_status reads it back without allocating.
 #include <mutex>
 
 #include "../../include/spec_verify.h"
@@ -58,6 +63,8 @@ int device_slot(DeviceSlot** out) {
     void* p = nullptr;
     // the host-side symbol is only a stand-in: the kernels need the device address
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return SPEC_ECUDA;
+    // the shared-memory limit is a per-device attribute
+    if (spec::gemm_init_attributes() != cudaSuccess) return SPEC_ECUDA;
     s.scratch = static_cast<unsigned char*>(p);
     s.num_sms = sms;
     s.ready = true;
@@ -99,4 +106,14 @@ extern "C" SPEC_API int spec_gemm_q4k_noalloc(const void* w_tiled, int N, int K,
     return SPEC_ECUDA;
   if (launch_sum_pieces(p, pieces, y, M, st, true) != cudaSuccess) return SPEC_ECUDA;
   return SPEC_OK;
+}
+
+extern "C" SPEC_API int spec_gemm_q4k_noalloc_status(void* cuda_stream) {
+  DeviceSlot* slot = nullptr;
+  int rc = device_slot(&slot);
+  if (rc) return rc;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess) return SPEC_ECUDA;
+  int32_t word = 0;
+  if (cudaMemcpy(&word, slot->scratch, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return SPEC_ECUDA;
+  return word;
 }

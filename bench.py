@@ -282,22 +282,27 @@ def kernel_source_sha():
     return h.hexdigest()[:16]
 
 
-def committed_traffic():
-    """Per-launch DRAM bytes of the GEMM kernel from the committed ncu summary,
-    scaled to a full-model step; None if the kernel changed since the capture."""
+def committed_traffic(cfg):
+    """DRAM bytes (read + write) per GEMM launch of a step, averaged over the
+    step's launches, from the committed per-shape ncu captures; None if the
+    kernel changed since the capture or a shape of the step was not captured."""
     p = os.path.join(ROOT, "profiles", "gemm_q4k_ncu_traffic.txt")
     if not os.path.exists(p):
         return None
-    kv = {}
+    sha, shapes = None, {}
     for line in open(p):
-        if ":" in line and not line.startswith("#"):
-            a, b = line.split(":", 1)
-            kv[a.strip()] = b.strip()
-    if kv.get("kernel_source_sha") != kernel_source_sha():
+        if line.startswith("kernel_source_sha:"):
+            sha = line.split(":", 1)[1].strip()
+        elif line.startswith("shape "):
+            name, rest = line[len("shape "):].split(":", 1)
+            f = rest.split()
+            shapes[name.strip()] = int(f[0]) + int(f[1])
+    if sha != kernel_source_sha():
         return None
+    mats = [(N, K) for _, N, K in cfg.matrices()] * cfg.n_layers + [(cfg.vocab, cfg.hidden)]
     try:
-        return float(kv["traffic_bytes_per_average_launch"])
-    except (KeyError, ValueError):
+        return sum(shapes[f"{N}x{K}"] for N, K in mats) / len(mats)
+    except KeyError:
         return None
 
 
@@ -401,7 +406,7 @@ def run_gpu(args, rank, world):
     gbytes, glaunch = gemm_algorithmic_bytes(cfg)
     peak, peak_kind = measured_peaks()
     achieved = gbytes / (gemm_ms * 1e-3) / 1e9 if gemm_ms else None
-    traffic = committed_traffic()
+    traffic = committed_traffic(cfg)
 
     # end to end through the host-buffer entry point
     hid_h = torch.from_numpy(synth.normal((ROWS, cfg.hidden), rank, 5)).pin_memory()
@@ -654,6 +659,403 @@ def run_accept_profile(args):
     ctx.close()
 
 
+def run_sweep(args):
+    """Projection sweep: Q4_K 6656->6656 and 6656->26624 at M in {1, 2, 4, 8,
+    16} rows through spec_gemm_q4k (quantise + GEMM + ordered piece sum), a
+    bandwidth test of the skinny dequant-GEMM.  The weights rotate over >= 2 GB
+    of distinct device copies (82 of the small matrix, 21 of the large), so no
+    call finds its weights in the 129 MB L2.  One JSON line per (shape, M):
+    weight GB/s, us per call, fraction of the measured copy bandwidth."""
+    import torch
+
+    from speculative_decoding_exact_gb300 import abi, runtime, synth
+    from speculative_decoding_exact_gb300 import build as b
+
+    b.build()
+    stream = torch.cuda.Stream()
+    torch.cuda.set_stream(stream)
+    ctx = runtime.Context(runtime.ModelConfig(**synth.FULL), max_ctx=2112, stream=stream)
+    peak, peak_kind = measured_peaks()
+    K = 6656
+    for N in (6656, 26624):
+        wbytes = N * (K // 256) * 144
+        ncopies = max(2, -(-2 * 10**9 // wbytes))
+        W0 = runtime.upload_tiled(ctx, synth.q4k_matrix(N, K, 7, N), N, K)
+        copies = [W0] + [W0.clone() for _ in range(ncopies - 1)]
+        x = torch.from_numpy(synth.normal((16, K), 7, 16)).cuda()
+        y = torch.zeros((16, N), dtype=torch.float32, device="cuda")
+        torch.cuda.synchronize()
+        for M in (1, 2, 4, 8, 16):
+            it = [0]
+
+            def call():
+                W = copies[it[0] % ncopies]
+                it[0] += 1
+                abi.check("spec_gemm_q4k", abi.spec_gemm_q4k(ctx.h, W.data_ptr(), N, K, x.data_ptr(), M,
+                                                             y.data_ptr()))
+
+            calls = max(args.steps, 2 * ncopies)
+            ms = _time_steps(torch, stream, call, max(args.warmup, 3), calls)
+            us = ms * 1e3
+            alg = wbytes + M * K * 4 + M * N * 4
+            gbs = wbytes / us / 1e3
+            print(json.dumps({"metric": "Q4_K projection weight GB/s (quantise + GEMM + piece sum)",
+                              "value": gbs, "unit": "GB/s", "us_per_call": us,
+                              "algorithmic_gbs": alg / us / 1e3,
+                              "roofline": {"bound": "hbm", "achieved": alg / us / 1e3, "peak": peak,
+                                           "unit": "GB/s", "frac": alg / us / 1e3 / peak,
+                                           "peak_kind": peak_kind},
+                              "frac_of_8tbs": gbs / 8000.0,
+                              "shape": {"N": N, "K": K, "rows": M}, "weight_bytes": wbytes,
+                              "calls": calls, "warmup": max(args.warmup, 3),
+                              "config": {"workload": f"projection sweep {K}->{N}, {M} rows",
+                                         "l2": f"weights rotated over {ncopies} device copies "
+                                               f"({ncopies * wbytes / 1e9:.2f} GB) so L2 serves no repeat"}}),
+                  flush=True)
+        del copies, W0
+        torch.cuda.empty_cache()
+    ctx.close()
+
+
+def run_head_accept(args):
+    """LM head + accept: final RMSNorm, the Q4_K head 6656 -> 131072 with its
+    fused per-row argmax over 16 rows (spec_lm_head_argmax), then the accept
+    kernel with the KV rollback (spec_accept) on a paged bf16 KV of 52 layers x
+    4 heads x 128 at n_past = 2055 (the block straddles a page).  Drafts are
+    planted so that the accepted lengths are uniform in 0..15 over >= 64
+    trials; the device result of every trial is checked against the planted
+    length.  One trial = KV block reserve (spec_kv_extend by 16) + head/argmax
+    + accept/rollback + rollback to n_past."""
+    import torch
+
+    from speculative_decoding_exact_gb300 import abi, runtime, synth
+    from speculative_decoding_exact_gb300 import build as b
+
+    b.build()
+    cfg = full_cfg()
+    stream = torch.cuda.Stream()
+    torch.cuda.set_stream(stream)
+    n_past, max_ctx = 2055, 2112
+    ctx = runtime.Context(cfg, max_ctx=max_ctx, stream=stream)
+    H, V = cfg.hidden, cfg.vocab
+    Wh = runtime.upload_tiled(ctx, synth.q4k_matrix(V, H, 0, 999999), V, H)
+    gamma = torch.ones(H, dtype=torch.float32, device="cuda")
+    x = torch.from_numpy(synth.normal((ROWS, H), 0, 11)).cuda()
+    pages = max_ctx // 16
+    kv = runtime.DeviceKV(cfg, pages, pages)
+    kv.reset(ctx)
+    kv.extend(ctx, n_past)
+    ks = kv.struct()
+    idx = torch.zeros(ROWS, dtype=torch.int32, device="cuda")
+    abi.check("spec_lm_head_argmax", abi.spec_lm_head_argmax(ctx.h, Wh.data_ptr(), gamma.data_ptr(), x.data_ptr(),
+                                                             ROWS, idx.data_ptr(), None))
+    torch.cuda.synchronize()
+    target = idx.cpu().numpy()
+    trials = max(64, args.steps)
+    rng = np.random.default_rng(2055)
+    Ls = rng.integers(0, K_DRAFT + 1, trials).astype(np.int32)
+    drafts = torch.from_numpy(np.stack([synth.plant_draft(target, int(L), V, 0, 4000 + t)
+                                        for t, L in enumerate(Ls)])).cuda()
+    hist = torch.zeros((trials, 4), dtype=torch.int32, device="cuda")
+    res = torch.zeros(4, dtype=torch.int32, device="cuda")
+    it = [0]
+
+    def trial():
+        t = it[0] % trials
+        it[0] += 1
+        abi.check("spec_kv_extend", abi.spec_kv_extend(ctx.h, ks, ROWS))
+        abi.check("spec_lm_head_argmax", abi.spec_lm_head_argmax(ctx.h, Wh.data_ptr(), gamma.data_ptr(),
+                                                                 x.data_ptr(), ROWS, idx.data_ptr(), None))
+        abi.check("spec_accept", abi.spec_accept(ctx.h, idx.data_ptr(), drafts[t].data_ptr(), K_DRAFT, ks,
+                                                 res.data_ptr()))
+        hist[t].copy_(res)
+        abi.check("spec_kv_rollback", abi.spec_kv_rollback(ctx.h, ks, n_past))
+
+    it[0] = 0
+    ms = _time_steps(torch, stream, trial, 0, trials)
+    h = hist.cpu().numpy()
+    assert np.all(h[:, 2] == 0) and np.array_equal(h[:, 0], Ls), "planted accepted lengths"
+    assert np.array_equal(h[:, 3], n_past + Ls + 1), "rolled-back lengths"
+    assert abi.spec_last_status(ctx.h) == 0
+    peak, peak_kind = measured_peaks()
+    wbytes = V * (H // 256) * 144
+    print(json.dumps({"metric": "LM head + argmax + accept/rollback per second (16 rows, V = 131072)",
+                      "value": 1000.0 / ms, "unit": "head+accept/s", "ms_per_trial": ms,
+                      "head_weight_gbs": wbytes / (ms * 1e-3) / 1e9,
+                      "head_frac_of_measured_hbm": wbytes / (ms * 1e-3) / 1e9 / peak, "peak_kind": peak_kind,
+                      "trials": trials, "accepted_hist": np.bincount(Ls, minlength=K_DRAFT + 1).tolist(),
+                      "config": {"workload": "Q4_K head 6656->131072 + argmax + accept + KV rollback, "
+                                             "16 rows, n_past 2055, paged bf16 KV 52 x 4 x 128, page 16",
+                                 "l2": "head weights (491 MB) larger than L2"}}), flush=True)
+    ctx.close()
+
+
+def run_ctx_sweep(args):
+    """The 52-block verify pass with the KV context swept over 2,048 / 16,384 /
+    32,768 and planted acceptance profiles of mean accepted length 1, 4 and 12
+    (each position accepted with probability a, E[min(Geom, 15)] = mean),
+    with the DFlash-style front projection (Q4_K 33,280 -> 6,656) timed at
+    M = round(mean L) + 1 and M = 16.  One JSON line per (context, mean):
+    steps/s and accepted tokens/s = steps/s x mean(L + 1)."""
+    import torch
+
+    from speculative_decoding_exact_gb300 import abi, runtime, synth
+
+    mdl = setup_model(0)
+    cfg, stream = mdl.cfg, mdl.stream
+    V = cfg.vocab
+    mdl.ctx.close()
+    fc_N, fc_K = cfg.hidden, 5 * cfg.hidden
+    for ctx_len in (2048, 16384, 32768):
+        max_ctx = ctx_len + 64
+        ctx = runtime.Context(cfg, max_ctx=max_ctx, stream=stream)
+        pages = max_ctx // 16
+        kv = runtime.DeviceKV(cfg, pages, pages)
+        kv.reset(ctx)
+        kv.extend(ctx, ctx_len)
+        g = torch.Generator(device="cuda").manual_seed(1234 + ctx_len)
+        with torch.cuda.stream(stream):
+            for l in range(cfg.n_layers):
+                kv.pool[:, l].copy_(torch.randn(kv.pool[:, l].shape, generator=g, device="cuda")
+                                    .to(torch.bfloat16))
+        ks = kv.struct()
+        ws = mdl.dw.struct()
+        if ctx_len == 2048:
+            Wfc = runtime.upload_tiled(ctx, synth.q4k_matrix(fc_N, fc_K, 3, 4242), fc_N, fc_K)
+            xfc = torch.from_numpy(synth.normal((16, fc_K), 3, 17)).cuda()
+            yfc = torch.zeros((16, fc_N), dtype=torch.float32, device="cuda")
+        am = torch.zeros(ROWS, dtype=torch.int32, device="cuda")
+        abi.check("spec_verify_step_ex", abi.spec_verify_step_ex(ctx.h, ws, ks, mdl.hidden.data_ptr(),
+                                                                 mdl.draft.data_ptr(), K_DRAFT, mdl.res.data_ptr(),
+                                                                 abi.spec_taps(None, am.data_ptr(), None)))
+        abi.check("spec_kv_rollback", abi.spec_kv_rollback(ctx.h, ks, ctx_len))
+        torch.cuda.synchronize()
+        idx = am.cpu().numpy()
+
+        def fc_us(M):
+            def call():
+                abi.check("spec_gemm_q4k", abi.spec_gemm_q4k(ctx.h, Wfc.data_ptr(), fc_N, fc_K, xfc.data_ptr(),
+                                                             M, yfc.data_ptr()))
+            return _time_steps(torch, stream, call, 3, 20) * 1e3
+
+        rng = np.random.default_rng(ctx_len)
+        for mean in (1.0, 4.0, 12.0):
+            a = _alpha_for_mean(mean)
+            Ls = np.zeros(args.steps, dtype=np.int32)
+            drafts = np.zeros((args.steps, K_DRAFT), dtype=np.int32)
+            for t in range(args.steps):
+                L = 0
+                while L < K_DRAFT and rng.random() < a:
+                    L += 1
+                Ls[t] = L
+                d = rng.integers(0, V, K_DRAFT).astype(np.int32)
+                d[:L] = idx[:L]
+                if L < K_DRAFT:
+                    d[L] = (idx[L] + 1) % V
+                drafts[t] = d
+            dd = torch.from_numpy(drafts).cuda()
+            hist = torch.zeros((args.steps, 4), dtype=torch.int32, device="cuda")
+            it = [0]
+
+            def step():
+                t = it[0] % args.steps
+                it[0] += 1
+                abi.check("spec_verify_step", abi.spec_verify_step(ctx.h, ws, ks, mdl.hidden.data_ptr(),
+                                                                   dd[t].data_ptr(), K_DRAFT, mdl.res.data_ptr()))
+                hist[t].copy_(mdl.res)
+                abi.check("spec_kv_rollback", abi.spec_kv_rollback(ctx.h, ks, ctx_len))
+
+            for _ in range(max(args.warmup, 3)):
+                step()
+            it[0] = 0
+            ms = _time_steps(torch, stream, step, 0, args.steps)
+            h = hist.cpu().numpy()
+            assert np.all(h[:, 2] == 0) and np.array_equal(h[:, 0], Ls), "planted accepted lengths"
+            sps = 1000.0 / ms
+            m_acc = float(h[:, 0].mean())
+            wb = cfg.weight_bytes()
+            print(json.dumps({"metric": "accepted tokens/s at k+1=16 rows (verify steps/s x mean(L+1))",
+                              "value": sps * (m_acc + 1.0), "unit": "tokens/s", "steps_per_s": sps,
+                              "ms_per_step": ms, "context": ctx_len, "target_mean_accepted": mean,
+                              "mean_accepted": m_acc, "steps": args.steps,
+                              "weight_gbs": wb * sps / 1e9,
+                              "total_gbs": (wb + kv_read_bytes(cfg, ctx_len)) * sps / 1e9,
+                              "fc_front_projection_us": {"M": int(round(m_acc)) + 1,
+                                                         "us": fc_us(int(round(m_acc)) + 1), "M16_us": fc_us(16)},
+                              "config": dict(workload_config(cfg), context=ctx_len,
+                                             acceptance=f"per-position {a:.4f}")}), flush=True)
+        del kv
+        ctx.close()
+        torch.cuda.empty_cache()
+
+
+def run_overlap(args):
+    """Split submit (Ch. 33 §33.2 / Figure 33.1) on the full model at context
+    --ctx: the step captures the block outputs of layers 1, 13, 25, 37, 49
+    (the draft's five hidden rows) and records an event after block 49; a
+    second stream with its own spec_ctx waits on it and runs the draft's
+    front projection (Q4_K 33,280 -> 6,656, 16 rows) while the step's last
+    blocks and LM head run.  Reports, in ms: the step alone (recorded graph),
+    the step with the split event (enqueued launch by launch), the projection
+    alone, the two one after the other on one stream, and overlapped."""
+    import torch
+
+    from speculative_decoding_exact_gb300 import abi, runtime, synth
+
+    mdl = setup_model(0)
+    cfg, ctx, sa = mdl.cfg, mdl.ctx, mdl.stream
+    H = cfg.hidden
+    ids = np.array([1, 13, 25, 37, 49], dtype=np.int32)
+    cap = torch.zeros((16, 5 * H), dtype=torch.float32, device="cuda")
+    abi.check("spec_set_capture", abi.spec_set_capture(ctx.h, ids.ctypes.data, 5, cap.data_ptr()))
+    sb = torch.cuda.Stream()
+    ctx_b = runtime.Context(cfg, max_ctx=CTX + 64, stream=sb)
+    fc_N, fc_K = H, 5 * H
+    Wfc = runtime.upload_tiled(ctx_b, synth.q4k_matrix(fc_N, fc_K, 3, 4242), fc_N, fc_K)
+    yfc = torch.zeros((16, fc_N), dtype=torch.float32, device="cuda")
+    torch.cuda.synchronize()
+
+    def step():
+        abi.check("spec_verify_step", abi.spec_verify_step(ctx.h, mdl.ws, mdl.ks, mdl.hidden.data_ptr(),
+                                                           mdl.draft.data_ptr(), K_DRAFT, mdl.res.data_ptr()))
+        abi.check("spec_kv_rollback", abi.spec_kv_rollback(ctx.h, mdl.ks, CTX))
+
+    def fc(c):
+        abi.check("spec_gemm_q4k", abi.spec_gemm_q4k(c.h, Wfc.data_ptr(), fc_N, fc_K, cap.data_ptr(), 16,
+                                                     yfc.data_ptr()))
+
+    ms_step = _time_steps(torch, sa, step, args.warmup, args.steps)
+    ms_fc = _time_steps(torch, sb, lambda: fc(ctx_b), args.warmup, args.steps)
+
+    def serial():
+        step()
+        # the projection on the step's stream: a spec_ctx of the same stream
+        fc(ctx_serial)
+
+    ctx_serial = runtime.Context(cfg, max_ctx=CTX + 64, stream=sa)
+    ms_serial = _time_steps(torch, sa, serial, args.warmup, args.steps)
+    ctx_serial.close()
+
+    ev = torch.cuda.Event()
+    ev.record(sa)
+    torch.cuda.synchronize()
+    abi.check("spec_set_split", abi.spec_set_split(ctx.h, 49, ev.cuda_event))
+    ms_step_split = _time_steps(torch, sa, step, args.warmup, args.steps)
+    done_b = torch.cuda.Event()
+
+    def overlapped():
+        step()
+        sb.wait_event(ev)
+        fc(ctx_b)
+        done_b.record(sb)
+        sa.wait_event(done_b)                        # the round ends when both are done
+
+    ms_overlap = _time_steps(torch, sa, overlapped, args.warmup, args.steps)
+    abi.check("spec_set_split", abi.spec_set_split(ctx.h, -1, None))
+    abi.check("spec_set_capture", abi.spec_set_capture(ctx.h, None, 0, None))
+    print(json.dumps({"metric": "verify step + draft front projection, split submit (ms per round)",
+                      "value": ms_overlap, "unit": "ms", "higher_is_better": False,
+                      "step_ms": ms_step, "step_with_split_event_ms": ms_step_split, "fc_ms": ms_fc,
+                      "serial_ms": ms_serial, "overlapped_ms": ms_overlap,
+                      "saved_vs_serial_ms": ms_serial - ms_overlap, "steps": args.steps, "warmup": args.warmup,
+                      "config": dict(workload_config(cfg), capture_layers=ids.tolist(), split_after=49,
+                                     fc="Q4_K 33280->6656, 16 rows, own spec_ctx on a second stream")}),
+          flush=True)
+    ctx_b.close()
+    ctx.close()
+
+
+def run_draft(args):
+    """A DFlash-shaped draft forward (Ch. 8 §8.2) with random Q4_K weights,
+    timed beside the verify step: the front projection fc 33,280 -> 6,656 over
+    16 rows of five concatenated target hidden states, five blocks at hidden
+    6,656 (52 query heads, FFN 17,920), attention over a context of 2,112 rows
+    (the 64-row sink plus the 2,048-row window of Ch. 8 §8.3) and the 16-row
+    block, then the target's own LM head and the per-row argmax (the draft
+    borrows the target's head, Ch. 8 §8.2).  The pages' draft has 8 KV heads
+    of 128; the attention kernels take a whole number of query heads per KV
+    head and 52 is not a multiple of 8, so the draft blocks here have the
+    target's 4 KV heads.  Everything runs through the library's own kernels:
+    spec_gemm_q4k for fc, then a 5-layer verify step for the blocks, head and
+    argmax.  Reports ms per draft forward, per verify step, and per cycle."""
+    import torch
+
+    from speculative_decoding_exact_gb300 import abi, runtime, synth
+
+    mdl = setup_model(0)
+    cfg, ctx, stream = mdl.cfg, mdl.ctx, mdl.stream
+    H = cfg.hidden
+    dcfg = runtime.ModelConfig(**dict(synth.FULL, n_layers=5))
+    dctx_len = 64 + 2048
+    dmax = dctx_len + 64
+    dctx = runtime.Context(dcfg, max_ctx=dmax, stream=stream)
+    dw = runtime.DeviceWeights(dcfg)
+    for l in range(dcfg.n_layers):
+        for j, (name, N, K) in enumerate(dcfg.matrices()):
+            getattr(dw, name).append(runtime.upload_tiled(dctx, synth.q4k_matrix(N, K, 9, 5000 + 10 * l + j), N, K))
+    dw.w_head = mdl.dw.w_head                     # the target's LM head
+    fc_N, fc_K = H, 5 * H
+    Wfc = runtime.upload_tiled(dctx, synth.q4k_matrix(fc_N, fc_K, 9, 5999), fc_N, fc_K)
+    pages = dmax // 16
+    dkv = runtime.DeviceKV(dcfg, pages, pages)
+    dkv.reset(dctx)
+    dkv.extend(dctx, dctx_len)
+    g = torch.Generator(device="cuda").manual_seed(99)
+    with torch.cuda.stream(stream):
+        dkv.pool.copy_(torch.randn(dkv.pool.shape, generator=g, device="cuda").to(torch.bfloat16))
+    cap = torch.from_numpy(synth.normal((16, fc_K), 9, 6000)).cuda()
+    hid = torch.zeros((16, H), dtype=torch.float32, device="cuda")
+    dtok = torch.from_numpy(synth.tokens(K_DRAFT, cfg.vocab, 9, 6001)).cuda()
+    dres = torch.zeros(4, dtype=torch.int32, device="cuda")
+    prop = torch.zeros(16, dtype=torch.int32, device="cuda")
+    dws, dks = dw.struct(), dkv.struct()
+    taps = abi.spec_taps(None, prop.data_ptr(), None)
+    torch.cuda.synchronize()
+
+    def draft():
+        abi.check("spec_gemm_q4k", abi.spec_gemm_q4k(dctx.h, Wfc.data_ptr(), fc_N, fc_K, cap.data_ptr(), 16,
+                                                     hid.data_ptr()))
+        abi.check("spec_verify_step_ex", abi.spec_verify_step_ex(dctx.h, dws, dks, hid.data_ptr(), dtok.data_ptr(),
+                                                                 K_DRAFT, dres.data_ptr(), taps))
+        abi.check("spec_kv_rollback", abi.spec_kv_rollback(dctx.h, dks, dctx_len))
+
+    def verify():
+        abi.check("spec_verify_step", abi.spec_verify_step(ctx.h, mdl.ws, mdl.ks, mdl.hidden.data_ptr(),
+                                                           mdl.draft.data_ptr(), K_DRAFT, mdl.res.data_ptr()))
+        abi.check("spec_kv_rollback", abi.spec_kv_rollback(ctx.h, mdl.ks, CTX))
+
+    def cycle():
+        draft()
+        verify()
+
+    ms_d = _time_steps(torch, stream, draft, args.warmup, args.steps)
+    assert int(dres[2].item()) == 0
+    ms_v = _time_steps(torch, stream, verify, args.warmup, args.steps)
+    ms_c = _time_steps(torch, stream, cycle, args.warmup, args.steps)
+    dbytes = dcfg.weight_bytes() + fc_N * (fc_K // 256) * 144
+    print(json.dumps({"metric": "DFlash-shaped draft forward (fc + 5 blocks + target LM head + argmax), ms",
+                      "value": ms_d, "unit": "ms", "higher_is_better": False,
+                      "draft_ms": ms_d, "verify_ms": ms_v, "cycle_ms": ms_c,
+                      "draft_weight_bytes": dbytes, "draft_weight_gbs": dbytes / (ms_d * 1e-3) / 1e9,
+                      "steps": args.steps, "warmup": args.warmup,
+                      "config": {"workload": "draft: fc Q4_K 33280->6656, 5 blocks hidden 6656 (52 q / 4 kv heads, "
+                                             "FFN 17920), context 64 sink + 2048 window, target LM head 131072, "
+                                             "16 rows; verify: the full 52-block step at context "
+                                             f"{CTX}", "draft_weights": "random Q4_K"}}), flush=True)
+    dctx.close()
+    ctx.close()
+
+
+def _alpha_for_mean(mean):
+    """Per-position acceptance a with E[min(Geom(a), 15)] = sum_{i=1..15} a^i = mean."""
+    lo, hi = 0.0, 1.0
+    for _ in range(60):
+        a = 0.5 * (lo + hi)
+        e = sum(a ** i for i in range(1, K_DRAFT + 1))
+        lo, hi = (a, hi) if e < mean else (lo, a)
+    return 0.5 * (lo + hi)
+
+
 def run_tree(args):
     """Token-tree verify steps (Ch. 33 section 33.7) on the full model at
     context --ctx: a random tree of --tree nodes (node 0 = the carried
@@ -765,6 +1167,16 @@ def main():
                     help="time token-tree verify steps with a random tree of this many nodes (1..16)")
     ap.add_argument("--attn", action="store_true",
                     help="time the verify attention alone at context --ctx instead of the verify step")
+    ap.add_argument("--sweep", action="store_true",
+                    help="projection sweep 6656->6656 and 6656->26624 at M = 1..16, weights rotated over 2 GB")
+    ap.add_argument("--head-accept", action="store_true",
+                    help="LM head 6656->131072 + argmax + accept/rollback at n_past 2055, L ~ U{0..15}")
+    ap.add_argument("--ctx-sweep", action="store_true",
+                    help="verify steps at context 2k/16k/32k x mean accepted length 1/4/12, with the fc timing")
+    ap.add_argument("--draft", action="store_true",
+                    help="time a DFlash-shaped draft forward (fc + 5 blocks + LM head) beside the verify step")
+    ap.add_argument("--overlap", action="store_true",
+                    help="split submit: the draft front projection on a second stream overlaps the step's suffix")
     ap.add_argument("--ctx", type=int, default=2048,
                     help="KV context of the verify step (the long-context sweep uses 16384, 32768)")
     args = ap.parse_args()
@@ -774,6 +1186,21 @@ def main():
     CTX = args.ctx
     if args.gemm_shape:
         run_gemm_shape(args)
+        return
+    if args.sweep:
+        run_sweep(args)
+        return
+    if args.head_accept:
+        run_head_accept(args)
+        return
+    if args.ctx_sweep:
+        run_ctx_sweep(args)
+        return
+    if args.overlap:
+        run_overlap(args)
+        return
+    if args.draft:
+        run_draft(args)
         return
     if args.attn:
         run_attention(args)

@@ -375,6 +375,26 @@ SPEC_API int spec_verify_tree(spec_ctx* ctx, const spec_weights* w, spec_kv* kv,
  * residual kernel that produces the block output: no extra launch. */
 SPEC_API int spec_set_capture(spec_ctx* ctx, const int32_t* layer_ids_host, int n, float* rows);
 
+/* ---- Split submit (Ch. 33 §33.2, the Mirror-SD route of the paragraph
+ * before Figure 33.1, and Figure 33.1): the target's graph is split at a
+ * capture layer; the prefix through that layer runs first, and the draft's
+ * work overlaps the target's remaining layers and LM head.
+ *
+ * From the next step on, every verify step (linear, tree or sampled) records
+ * cuda_event (a cudaEvent_t created by the caller on this ctx's device) on
+ * the ctx stream as soon as the output of block `layer` is written,
+ * including its hidden-state capture rows (spec_set_capture).  A second
+ * stream that waits on the event (cudaStreamWaitEvent) may read those rows
+ * while the step's suffix runs, e.g. to run the draft's front projection.
+ * The work on that stream must not use this ctx's workspace: give it a
+ * spec_ctx of its own, or use spec_gemm_q4k_noalloc.  The step's result is
+ * unchanged; its end is observed as before (the ctx stream).  A step that
+ * is replayed as a recorded graph carries the event as an external event
+ * record node, so a wait issued after the step was enqueued still refers to
+ * that step's record.  layer = -1 turns the split off (cuda_event is
+ * ignored); the event must stay valid while the split is on. */
+SPEC_API int spec_set_split(spec_ctx* ctx, int layer, void* cuda_event);
+
 /* ---- Stochastic exact acceptance (Ch. 33 §33.2; the rule of which
  * spec_accept is the one-hot case).
  *

@@ -78,6 +78,7 @@ _SIGS = {
     "spec_gemm_q4k_noalloc_status": (I, [P]),
     "spec_mt_seed": (I, [P, C.c_uint32]),
     "spec_set_capture": (I, [P, P, I, P]),
+    "spec_set_split": (I, [P, I, P]),
     "spec_verify_tree": (I, [P, C.POINTER(spec_weights), C.POINTER(spec_kv), P, P, P, I, P, P,
                              C.POINTER(spec_taps)]),
     "spec_sample_accept": (I, [P, P, P, P, I, P, C.POINTER(spec_kv), P]),
@@ -247,3 +248,8 @@ def spec_gemm_q4k_noalloc(w, N, K, x, M, y, stream) -> int:
 
 def spec_gemm_q4k_noalloc_status(stream) -> int:
     return _call("spec_gemm_q4k_noalloc_status", P(stream or 0))
+
+
+def spec_set_split(ctx, layer: int, event) -> int:
+    """event: a cudaEvent_t handle (e.g. torch.cuda.Event().cuda_event), or None with layer = -1."""
+    return _call("spec_set_split", ctx, int(layer), P(event or 0))

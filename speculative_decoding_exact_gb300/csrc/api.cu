@@ -45,6 +45,9 @@ struct spec_ctx {
   int cap_n = 0;
   int cap_ids[8] = {0, 0, 0, 0, 0, 0, 0, 0};
   float* cap_rows = nullptr;
+  // split submit: an event recorded after block split_layer's output
+  int split_layer = -1;
+  cudaEvent_t split_ev = nullptr;
   int32_t* step_state = nullptr; // [2]
   int32_t* idx_buf = nullptr;    // [16]
   float* hidden_dev = nullptr;   // host-buffer entry point staging
@@ -510,6 +513,17 @@ static int enqueue_step(spec_ctx* c, const spec_weights* w, spec_kv* kv, const f
     if (tap_resid)
       SPEC_TRY(cudaMemcpyAsync(tap_resid + (size_t)(l + 1) * M * H, c->resid, rows_bytes,
                                cudaMemcpyDeviceToDevice, st));
+    // the prefix through block l is done (its output and capture rows are
+    // written): another stream that waits on this event overlaps the suffix
+    if (l == c->split_layer && c->split_ev) {
+      // inside a recorded graph the record is an external event node, which
+      // streams outside the graph can wait on
+      cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+      SPEC_TRY(cudaStreamIsCapturing(st, &cs));
+      SPEC_TRY(cudaEventRecordWithFlags(c->split_ev, st,
+                                        cs == cudaStreamCaptureStatusActive ? cudaEventRecordExternal
+                                                                            : cudaEventRecordDefault));
+    }
   }
   SPEC_TRY(gemm(c->p_head, w->w_head)); ++n;
   if (ta) {
@@ -563,6 +577,8 @@ static uint64_t step_key(const spec_ctx* c, const spec_weights* w, const spec_kv
   h = mix(h, ta ? P(ta->parent) : 0);
   h = mix(h, ta ? P(ta->path_out) : 0);
   for (int j = 0; j < c->cap_n; ++j) h = mix(h, 0x100 + (uint64_t)c->cap_ids[j]);
+  h = mix(h, 0x200 + (uint64_t)(c->split_layer + 1));
+  h = mix(h, P(c->split_ev));
   h = mix(h, P(hidden));
   h = mix(h, P(draft));
   h = mix(h, P(res));
@@ -685,6 +701,15 @@ int spec_set_capture(spec_ctx* c, const int32_t* layer_ids, int n, float* rows) 
   c->cap_n = n;
   for (int j = 0; j < n; ++j) c->cap_ids[j] = layer_ids[j];
   c->cap_rows = n > 0 ? rows : nullptr;
+  return SPEC_OK;
+}
+
+int spec_set_split(spec_ctx* c, int layer, void* cuda_event) {
+  if (!c) return SPEC_ENULL;
+  if (layer < -1 || layer >= c->cfg.n_layers) return SPEC_EINVAL;
+  if (layer >= 0 && !cuda_event) return SPEC_ENULL;
+  c->split_layer = layer;
+  c->split_ev = layer >= 0 ? static_cast<cudaEvent_t>(cuda_event) : nullptr;
   return SPEC_OK;
 }
 

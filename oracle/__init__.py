@@ -48,7 +48,8 @@ def build(force: bool = False) -> str:
 class _Cfg(C.Structure):
     _fields_ = [("hidden", C.c_int32), ("n_layers", C.c_int32), ("n_q_heads", C.c_int32),
                 ("n_kv_heads", C.c_int32), ("head_dim", C.c_int32), ("ffn", C.c_int32),
-                ("vocab", C.c_int32), ("page_size", C.c_int32), ("rms_eps", C.c_float)]
+                ("vocab", C.c_int32), ("page_size", C.c_int32), ("rms_eps", C.c_float),
+                ("swa_window", C.c_int32), ("swa_period", C.c_int32)]
 
 
 class _Weights(C.Structure):
@@ -79,6 +80,8 @@ def lib():
         _lib.orc_mt_seed.argtypes = [C.c_void_p, C.c_uint32]
         _lib.orc_uniform_f32.restype = C.c_float
         _lib.orc_uniform_f32.argtypes = [C.c_void_p]
+        _lib.orc_layer_window.restype = C.c_int
+        _lib.orc_layer_window.argtypes = [C.c_void_p, C.c_int]
         _lib.orc_sample_ordered.restype = C.c_int32
         _lib.orc_sample_ordered.argtypes = [C.c_void_p, C.c_int, C.c_void_p, C.c_void_p]
         _lib.orc_sample_accept.argtypes = [C.c_void_p, C.c_void_p, C.c_void_p, C.c_int, C.c_int,
@@ -271,10 +274,15 @@ class Config:
     vocab: int
     page_size: int = 16
     rms_eps: float = 1e-6
+    swa_window: int = 0      # sliding-window layers: every swa_period-th layer (the last of each period)
+    swa_period: int = 0
 
     def c(self) -> _Cfg:
         return _Cfg(self.hidden, self.n_layers, self.n_q_heads, self.n_kv_heads, self.head_dim,
-                    self.ffn, self.vocab, self.page_size, self.rms_eps)
+                    self.ffn, self.vocab, self.page_size, self.rms_eps, self.swa_window, self.swa_period)
+
+    def layer_window(self, layer: int) -> int:
+        return int(lib().orc_layer_window(C.byref(self.c()), int(layer)))
 
     @property
     def n_qkv(self) -> int:
@@ -429,11 +437,14 @@ def verify_step(cfg: Config, w: Weights, kv: KV, hidden: np.ndarray, draft: np.n
 ST_BAD_TREE = 0x40
 
 
+TREE_MAX = 64        # nodes of a token tree ([33] §33.7 names trees of 24 to 64 nodes)
+
+
 def tree_masks(tokens: np.ndarray, parent: np.ndarray, vocab: int):
-    """(ancestor-or-self masks uint32 [n], status) of a token tree."""
+    """(ancestor-or-self masks uint64 [n], status) of a token tree of up to 64 nodes."""
     tokens = np.ascontiguousarray(tokens, dtype=np.int32)
     parent = np.ascontiguousarray(parent, dtype=np.int32)
-    mask = np.zeros(len(parent), dtype=np.uint32)
+    mask = np.zeros(max(1, len(parent)), dtype=np.uint64)
     st = lib().orc_tree_masks(_p(tokens), _p(parent), len(parent), int(vocab), _p(mask))
     return mask, int(st)
 
@@ -444,7 +455,7 @@ def tree_accept(idx: np.ndarray, tokens: np.ndarray, parent: np.ndarray):
     tokens = np.ascontiguousarray(tokens, dtype=np.int32)
     parent = np.ascontiguousarray(parent, dtype=np.int32)
     L, nxt = C.c_int32(), C.c_int32()
-    path = np.zeros(16, dtype=np.int32)
+    path = np.zeros(TREE_MAX, dtype=np.int32)
     lib().orc_tree_accept(_p(idx), _p(tokens), _p(parent), len(parent), C.byref(L), C.byref(nxt), _p(path))
     return int(L.value), int(nxt.value), path[: L.value + 1].copy()
 
@@ -458,7 +469,7 @@ def verify_tree(cfg: Config, w: Weights, kv: KV, hidden: np.ndarray, tokens: np.
     parent = np.ascontiguousarray(parent, dtype=np.int32)
     n = len(parent)
     res = np.zeros(4, dtype=np.int32)
-    path = np.full(16, -1, dtype=np.int32)
+    path = np.full(TREE_MAX, -1, dtype=np.int32)
     idx = np.full(n, -1, dtype=np.int32)
     lg = np.empty((n, cfg.vocab), dtype=np.float32) if logits else None
     c, cw, ck = cfg.c(), w.c(), kv.c()

@@ -492,21 +492,31 @@ void orc_kv_write_row(const orc_cfg* c, orc_kv* kv, int layer, int pos,
 /* visible t (max subtracted), o = sum_t softmax_t v_t.  K and V are the      */
 /* stored bf16 values.  fp64 throughout, stored fp32.                          */
 /* ------------------------------------------------------------------------ */
+int orc_layer_window(const orc_cfg* c, int layer) {
+    if (c->swa_window > 0 && c->swa_period > 0 && layer % c->swa_period == c->swa_period - 1)
+        return c->swa_window;
+    return 0;
+}
+
 /* Row i sees the positions 0..n_past-1 and the block rows j with bit j of
  * mask[i] set (mask NULL: the causal block, j <= i).  A token tree's mask is
- * a node's ancestors and itself. */
+ * a node's ancestors and itself (up to 64 nodes).  In a sliding-window layer of window W the
+ * row at position p = n_past + i sees only the positions t > p - W of those. */
 void orc_attention_tree(const orc_cfg* c, const orc_kv* kv, int layer, const float* q,
-                        int M, int n_past, const uint32_t* mask, float* out) {
+                        int M, int n_past, const uint64_t* mask, float* out) {
     int dh = c->head_dim, group = c->n_q_heads / c->n_kv_heads;
     int max_vis = n_past + M;
+    int W = orc_layer_window(c, layer);
     double* s = (double*)malloc(sizeof(double) * (size_t)max_vis);
     int* vt = (int*)malloc(sizeof(int) * (size_t)max_vis);
     double scale = 1.0 / sqrt((double)dh);
     for (int i = 0; i < M; ++i) {
         int nv = 0;                                   /* the visible positions, in order */
-        for (int t = 0; t < n_past; ++t) vt[nv++] = t;
+        int lo = W > 0 ? n_past + i - W + 1 : 0;      /* the window's first position */
+        for (int t = 0; t < n_past; ++t)
+            if (t >= lo) vt[nv++] = t;
         for (int j = 0; j < M; ++j)
-            if (mask ? ((mask[i] >> j) & 1u) : (j <= i)) vt[nv++] = n_past + j;
+            if ((mask ? ((mask[i] >> j) & 1ull) : (j <= i)) && n_past + j >= lo) vt[nv++] = n_past + j;
         for (int h = 0; h < c->n_q_heads; ++h) {
             int g = h / group;
             const float* qh = q + ((size_t)i * c->n_q_heads + h) * dh;
@@ -553,7 +563,7 @@ void orc_attention(const orc_cfg* c, const orc_kv* kv, int layer, const float* q
 /*   xn = rmsnorm(x, ffn_norm); [g|u] = W_gu q8(xn); x += W_down q8(silu(g)u) */
 /* ------------------------------------------------------------------------ */
 static int orc_block_tree(const orc_cfg* c, const orc_weights* w, orc_kv* kv, int layer,
-                          const float* x_in, int M, int n_past, const uint32_t* mask, float* x_out) {
+                          const float* x_in, int M, int n_past, const uint64_t* mask, float* x_out) {
     int H = c->hidden, dh = c->head_dim, F = c->ffn;
     int nq = c->n_q_heads * dh, nkv = c->n_kv_heads * dh;
     int Nqkv = nq + 2 * nkv;
@@ -598,7 +608,7 @@ int orc_block(const orc_cfg* c, const orc_weights* w, orc_kv* kv, int layer,
 }
 
 static int orc_forward_tree(const orc_cfg* c, const orc_weights* w, orc_kv* kv, const float* hidden,
-                            int M, const uint32_t* mask, int32_t* idx, float* logits, float* resid) {
+                            int M, const uint64_t* mask, int32_t* idx, float* logits, float* resid) {
     int H = c->hidden, V = c->vocab;
     int n_past = *kv->seq_len;
     int st = orc_kv_reserve(kv, n_past + M);
@@ -669,20 +679,21 @@ int orc_verify_step(const orc_cfg* c, const orc_weights* w, orc_kv* kv, const fl
 
 /* ------------------------------------------------------------------------ */
 /* Token-tree verification ([33] §33.7: a tree spends the batch on covering  */
-/* near-miss branches).  Node 0 is the carried frontier; node i >= 1 holds    */
-/* the draft token tokens[i], proposed as the continuation of parent[i] <     */
-/* i.  Node i's row sees the context and its ancestors and itself.           */
+/* near-miss branches; it names trees of 24, 32, 48 and 64 nodes).  Node 0  */
+/* is the carried frontier; node i >= 1 holds the draft token tokens[i],      */
+/* proposed as the continuation of parent[i] < i.  Node i's row sees the      */
+/* context and its ancestors and itself.  Up to ORC_TREE_MAX = 64 nodes.      */
 /* ------------------------------------------------------------------------ */
 
 /* ancestor-or-self masks; ORC_ST_BAD_TREE for a parent list that is not a
  * tree in topological order, ORC_ST_TOKEN_RANGE for a token outside [0, V) */
-int orc_tree_masks(const int32_t* tokens, const int32_t* parent, int n, int vocab, uint32_t* mask) {
-    if (n < 1 || n > 16 || parent[0] != -1) return ORC_ST_BAD_TREE;
-    mask[0] = 1u;
+int orc_tree_masks(const int32_t* tokens, const int32_t* parent, int n, int vocab, uint64_t* mask) {
+    if (n < 1 || n > ORC_TREE_MAX || parent[0] != -1) return ORC_ST_BAD_TREE;
+    mask[0] = 1ull;
     for (int i = 1; i < n; ++i) {
         if (parent[i] < 0 || parent[i] >= i) return ORC_ST_BAD_TREE;
         if (tokens[i] < 0 || tokens[i] >= vocab) return ORC_ST_TOKEN_RANGE;
-        mask[i] = mask[parent[i]] | (1u << i);
+        mask[i] = mask[parent[i]] | (1ull << i);
     }
     return 0;
 }
@@ -693,7 +704,7 @@ int orc_tree_masks(const int32_t* tokens, const int32_t* parent, int n, int voca
  * L = depth(a) drafts accepted, next = idx[a].  path[0..L] = the nodes. */
 void orc_tree_accept(const int32_t* idx, const int32_t* tokens, const int32_t* parent, int n,
                      int32_t* L, int32_t* next, int32_t* path) {
-    int acc[16], depth[16];
+    int acc[ORC_TREE_MAX], depth[ORC_TREE_MAX];
     int best = 0;
     acc[0] = 1;
     depth[0] = 0;
@@ -714,7 +725,7 @@ void orc_tree_accept(const int32_t* idx, const int32_t* tokens, const int32_t* p
 /* move the K/V rows of block slots path[d] to slots d (d = 1..L), every layer */
 void orc_kv_compact(const orc_cfg* c, orc_kv* kv, int n_past, const int32_t* path, int L) {
     size_t row = (size_t)c->head_dim;
-    uint16_t* tmp = (uint16_t*)malloc(sizeof(uint16_t) * row * 16);
+    uint16_t* tmp = (uint16_t*)malloc(sizeof(uint16_t) * row * ORC_TREE_MAX);
     for (int l = 0; l < c->n_layers; ++l)
         for (int which = 0; which < 2; ++which)
             for (int g = 0; g < c->n_kv_heads; ++g) {
@@ -742,7 +753,7 @@ void orc_kv_compact(const orc_cfg* c, orc_kv* kv, int n_past, const int32_t* pat
 int orc_verify_tree(const orc_cfg* c, const orc_weights* w, orc_kv* kv, const float* hidden,
                     const int32_t* tokens, const int32_t* parent, int n, int32_t* res, int32_t* path,
                     int32_t* idx, float* logits) {
-    uint32_t mask[16];
+    uint64_t mask[ORC_TREE_MAX];
     int n_past = *kv->seq_len;
     res[0] = 0;
     res[1] = -1;

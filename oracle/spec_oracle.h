@@ -30,6 +30,10 @@
 typedef struct {
     int32_t hidden, n_layers, n_q_heads, n_kv_heads, head_dim, ffn, vocab, page_size;
     float rms_eps;
+    /* sliding-window layers ([8] §8.6 item 4 names them "SWA rings"): layer l
+     * is one when swa_window > 0, swa_period > 0 and l % swa_period ==
+     * swa_period - 1; its row at position p sees positions p-swa_window+1..p */
+    int32_t swa_window, swa_period;
 } orc_cfg;
 
 /* Host pointers to CANONICAL Q4_K matrices (see orc_q4k_* below). */
@@ -99,15 +103,19 @@ int orc_block(const orc_cfg* c, const orc_weights* w, orc_kv* kv, int layer,
               const float* x_in, int M, int n_past, float* x_out);
 /* token trees ([33] §33.7): node 0 = the carried frontier, parent[i] < i */
 #define ORC_ST_BAD_TREE 0x40
+#define ORC_TREE_MAX 64     /* nodes of a token tree ([33] §33.7 names 24 to 64) */
 void orc_attention_tree(const orc_cfg* c, const orc_kv* kv, int layer, const float* q,
-                        int M, int n_past, const uint32_t* mask, float* out);
-int  orc_tree_masks(const int32_t* tokens, const int32_t* parent, int n, int vocab, uint32_t* mask);
+                        int M, int n_past, const uint64_t* mask, float* out);
+int  orc_tree_masks(const int32_t* tokens, const int32_t* parent, int n, int vocab, uint64_t* mask);
 void orc_tree_accept(const int32_t* idx, const int32_t* tokens, const int32_t* parent, int n,
                      int32_t* L, int32_t* next, int32_t* path);
 void orc_kv_compact(const orc_cfg* c, orc_kv* kv, int n_past, const int32_t* path, int L);
 int  orc_verify_tree(const orc_cfg* c, const orc_weights* w, orc_kv* kv, const float* hidden,
                      const int32_t* tokens, const int32_t* parent, int n, int32_t* res, int32_t* path,
                      int32_t* idx, float* logits);
+
+/* the window of layer l: swa_window for a sliding-window layer, 0 otherwise */
+int orc_layer_window(const orc_cfg* c, int layer);
 
 /* stochastic exact acceptance ([33] §33.2): MT19937 state of 625 words */
 void     orc_mt_seed(uint32_t* st, uint32_t seed);

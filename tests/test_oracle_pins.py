@@ -392,6 +392,65 @@ def test_attention_matches_softmax_reference():
 
 
 # ---------------------------------------------------------------------------
+# sliding-window layers ([8] §8.6 item 4): row at position p sees p-W+1..p
+# ---------------------------------------------------------------------------
+def _swa_cfg(W, period=1):
+    return oracle.Config(hidden=512, n_layers=2, n_q_heads=4, n_kv_heads=2, head_dim=128, ffn=256,
+                         vocab=64, swa_window=W, swa_period=period)
+
+
+def test_swa_layer_selection():
+    c = _swa_cfg(32, period=2)
+    assert [c.layer_window(l) for l in range(2)] == [0, 32]
+    c = _swa_cfg(32, period=1)
+    assert [c.layer_window(l) for l in range(2)] == [32, 32]
+    assert _swa_cfg(0, period=1).layer_window(0) == 0
+
+
+def test_swa_window_covering_everything_is_plain_attention():
+    n_past, M = 37, 5
+    plain = oracle.KV(_swa_cfg(0), num_pages=8, max_seq_pages=8)
+    plain.extend(n_past + M)
+    _fill_kv(plain, 0, n_past + M, 9)
+    q = synth.normal((M, 4, 128), 9, 3)
+    ref = plain.attention(0, q, n_past)
+    for W in (n_past + M, n_past + M + 16, 4096):
+        wide = plain.copy()
+        wide.cfg = _swa_cfg(W)
+        assert np.array_equal(wide.attention(0, q, n_past).view(np.uint32), ref.view(np.uint32))
+    # a window one short of the first row's reach differs
+    short = plain.copy()
+    short.cfg = _swa_cfg(n_past)
+    assert not np.array_equal(short.attention(0, q, n_past), ref)
+
+
+def test_swa_window_one_returns_own_value_and_two_is_a_pair_softmax():
+    n_past, M = 40, 4
+    kv = oracle.KV(_swa_cfg(1), num_pages=8, max_seq_pages=8)
+    kv.extend(n_past + M)
+    rk, rv = _fill_kv(kv, 0, n_past + M, 10)
+    kb = np.vectorize(oracle.bf16_to_float)(synth.bf16_bits(rk)).reshape(-1, 2, 128)
+    vb = np.vectorize(oracle.bf16_to_float)(synth.bf16_bits(rv)).reshape(-1, 2, 128)
+    q = synth.normal((M, 4, 128), 10, 3)
+    out = kv.attention(0, q, n_past)
+    for i in range(M):
+        for h in range(4):
+            assert np.allclose(out[i, 128 * h:128 * h + 128], vb[n_past + i, h // 2], rtol=1e-6)
+    # W = 2: the row and its predecessor, weights 1 / (1 + exp(-(s_p - s_{p-1})))
+    kv.cfg = _swa_cfg(2)
+    out = kv.attention(0, q, n_past)
+    for i in range(M):
+        p = n_past + i
+        for h in range(4):
+            g = h // 2
+            s1 = float(kb[p, g] @ q[i, h].astype(np.float64)) / math.sqrt(128)
+            s0 = float(kb[p - 1, g] @ q[i, h].astype(np.float64)) / math.sqrt(128)
+            a = 1.0 / (1.0 + math.exp(s0 - s1))
+            ref = a * vb[p, g] + (1 - a) * vb[p - 1, g]
+            assert np.allclose(out[i, 128 * h:128 * h + 128], ref, rtol=1e-5, atol=1e-6)
+
+
+# ---------------------------------------------------------------------------
 # whole-step invariants on a tiny model
 # ---------------------------------------------------------------------------
 def tiny_model(seed=0, n_layers=2, vocab=512):
@@ -683,8 +742,8 @@ def _committed_equal(kv_a, kv_b):
 
 def test_tree_masks_are_ancestor_sets_and_reject_bad_trees():
     rng = np.random.default_rng(4)
-    for _ in range(50):
-        n = int(rng.integers(1, 17))
+    for _ in range(80):
+        n = int(rng.integers(1, 65))
         parent = np.array([-1] + [int(rng.integers(0, i)) for i in range(1, n)], dtype=np.int32)
         tokens = rng.integers(0, 100, n).astype(np.int32)
         mask, st = oracle.tree_masks(tokens, parent, 100)
@@ -698,6 +757,10 @@ def test_tree_masks_are_ancestor_sets_and_reject_bad_trees():
     ok_tok = np.zeros(3, dtype=np.int32)
     assert oracle.tree_masks(ok_tok, np.array([0, 0, 1], dtype=np.int32), 100)[1] == oracle.ST_BAD_TREE
     assert oracle.tree_masks(ok_tok, np.array([-1, 1, 0], dtype=np.int32), 100)[1] == oracle.ST_BAD_TREE
+    big = np.arange(-1, 64, dtype=np.int32)                  # a chain of 65 nodes: one too many
+    assert oracle.tree_masks(np.zeros(65, dtype=np.int32), big, 100)[1] == oracle.ST_BAD_TREE
+    m64, st = oracle.tree_masks(np.zeros(64, dtype=np.int32), big[:64], 100)
+    assert st == 0 and int(m64[63]) == (1 << 64) - 1
     assert oracle.tree_masks(np.array([0, 100, 1], dtype=np.int32), np.array([-1, 0, 0], dtype=np.int32),
                              100)[1] == oracle.ST_TOKEN_RANGE
 
@@ -707,8 +770,8 @@ def test_tree_accept_is_the_longest_matching_root_path():
     # chain; the longest wins, the lowest end node among equals
     rng = np.random.default_rng(6)
     V = 5                                           # small vocabulary: many matches and ties
-    for _ in range(300):
-        n = int(rng.integers(1, 17))
+    for _ in range(400):
+        n = int(rng.integers(1, 65))
         parent = np.array([-1] + [int(rng.integers(0, i)) for i in range(1, n)], dtype=np.int32)
         tokens = rng.integers(0, V, n).astype(np.int32)
         idx = rng.integers(0, V, n).astype(np.int32)
@@ -745,6 +808,43 @@ def test_chain_tree_is_the_linear_verify():
         assert list(res_t) == list(res_l) and np.array_equal(path, np.arange(L_t + 1))
         assert np.array_equal(idx_t, idx_l) and np.array_equal(lg_t.view(np.uint32), lg_l.view(np.uint32))
         _committed_equal(kv_t, kv_l)
+
+
+def test_large_tree_with_decoys_equals_serial_greedy():
+    # the same pin for the tree sizes [33] §33.7 names (24 to 64 nodes): a
+    # true branch of depth 12 with 2-3 decoys per level, 40-50 nodes
+    cfg, w = tiny_model(seed=4)
+    k = 12
+    rng = np.random.default_rng(21)
+    hidden = synth.normal((k + 1, cfg.hidden), 4, 62)
+    kv0 = oracle.KV(cfg, num_pages=16, max_seq_pages=16)
+    kv0.extend(23)
+    for layer in range(cfg.n_layers):
+        _fill_kv(kv0, layer, 23, 95 + layer)
+    kv_s = kv0.copy()
+    serial, st = oracle.serial_greedy(cfg, w, kv_s, hidden, k)
+    assert st == 0
+    for L_t in (3, k):
+        rows, tokens, parent, true_node = [hidden[0]], [0], [-1], [0]
+        for depth in range(k):
+            for _ in range(int(rng.integers(2, 4))):
+                rows.append(synth.normal((cfg.hidden,), 4, 2000 + len(rows)))
+                tokens.append((serial[depth] + 1 + int(rng.integers(0, cfg.vocab - 1))) % cfg.vocab)
+                parent.append(int(rng.choice(true_node)))
+            rows.append(hidden[depth + 1])
+            tokens.append(serial[depth] if depth < L_t else (serial[depth] + 7) % cfg.vocab)
+            parent.append(true_node[-1])
+            true_node.append(len(rows) - 1)
+        n = len(rows)
+        assert 40 <= n <= 64
+        kv_t = kv0.copy()
+        res, path, idx, _ = oracle.verify_tree(cfg, w, kv_t, np.stack(rows).astype(np.float32),
+                                               np.array(tokens, dtype=np.int32), np.array(parent, dtype=np.int32))
+        assert res[2] == 0 and res[0] == L_t and res[1] == serial[L_t], (res, L_t, serial)
+        assert np.array_equal(path, np.array(true_node[:L_t + 1]))
+        kv_r = kv_s.copy()
+        kv_r.rollback(23 + L_t + 1)
+        _committed_equal(kv_t, kv_r)
 
 
 def test_tree_with_decoys_equals_serial_greedy():

@@ -717,6 +717,49 @@ def run_sweep(args):
     ctx.close()
 
 
+def run_cudacore(args):
+    """The tensor-core GEMM against the CUDA-core (dp4a) one on one Q4_K
+    shape (--cudacore NxK), 16 rows, weights rotated over >= 2 GB of device
+    copies; one JSON line with both weight GB/s."""
+    import torch
+
+    from speculative_decoding_exact_gb300 import abi, runtime, synth
+    from speculative_decoding_exact_gb300 import build as b
+
+    b.build()
+    stream = torch.cuda.Stream()
+    torch.cuda.set_stream(stream)
+    ctx = runtime.Context(runtime.ModelConfig(**synth.FULL), max_ctx=2112, stream=stream)
+    N, K = (int(v) for v in args.cudacore.lower().split("x"))
+    wbytes = N * (K // 256) * 144
+    ncopies = max(2, -(-2 * 10**9 // wbytes))
+    W0 = runtime.upload_tiled(ctx, synth.q4k_matrix(N, K, 7, N), N, K)
+    copies = [W0] + [W0.clone() for _ in range(ncopies - 1)]
+    x = torch.from_numpy(synth.normal((16, K), 7, 16)).cuda()
+    y = torch.zeros((16, N), dtype=torch.float32, device="cuda")
+    torch.cuda.synchronize()
+    out = {}
+    for name, fn in (("tensor_core", abi.spec_gemm_q4k), ("cuda_core_dp4a", abi.spec_gemm_q4k_cudacore)):
+        it = [0]
+
+        def call():
+            W = copies[it[0] % ncopies]
+            it[0] += 1
+            abi.check(name, fn(ctx.h, W.data_ptr(), N, K, x.data_ptr(), 16, y.data_ptr()))
+
+        ms = _time_steps(torch, stream, call, max(args.warmup, 3), max(args.steps, 2 * ncopies))
+        out[name] = {"us_per_call": ms * 1e3, "weight_gbs": wbytes / (ms * 1e-3) / 1e9}
+    peak, peak_kind = measured_peaks()
+    print(json.dumps({"metric": "Q4_K GEMM weight GB/s, tensor cores vs CUDA cores (16 rows)",
+                      "value": out["tensor_core"]["weight_gbs"], "unit": "GB/s", **out,
+                      "speedup_tensor_over_cuda_core": out["cuda_core_dp4a"]["us_per_call"] /
+                      out["tensor_core"]["us_per_call"],
+                      "peak": peak, "peak_kind": peak_kind, "shape": {"N": N, "K": K, "rows": 16},
+                      "config": {"workload": f"one Q4_K projection {K}->{N}, 16 rows",
+                                 "l2": f"weights rotated over {ncopies} device copies"}}), flush=True)
+    ctx.close()
+
+
 def run_head_accept(args):
     """LM head + accept: final RMSNorm, the Q4_K head 6656 -> 131072 with its
     fused per-row argmax over 16 rows (spec_lm_head_argmax), then the accept
@@ -1073,7 +1116,7 @@ def run_tree(args):
                                        dtype=np.int32)).cuda()
     tokens = torch.from_numpy(rng.integers(0, cfg.vocab, n).astype(np.int32)).cuda()
     rows = torch.from_numpy(synth.normal((n, cfg.hidden), 0, 55)).cuda()
-    path = torch.zeros(16, dtype=torch.int32, device="cuda")
+    path = torch.zeros(max(16, n), dtype=torch.int32, device="cuda")
 
     def tree():
         abi.check("spec_verify_tree", abi.spec_verify_tree(ctx.h, mdl.ws, mdl.ks, rows.data_ptr(), tokens.data_ptr(),
@@ -1090,7 +1133,8 @@ def run_tree(args):
     r = mdl.res.cpu().numpy()
     assert r[2] == 0, f"tree step status {r[2]}"
     ms_l = _time_steps(torch, stream, linear, args.warmup, args.steps)
-    print(json.dumps({"metric": f"token-tree verify steps/s ({n} nodes)", "value": 1000.0 / ms_t,
+    print(json.dumps({"metric": f"token-tree verify steps/s ({n} nodes, {(n + 15) // 16} pass(es) of <= 16 rows)",
+                      "value": 1000.0 / ms_t,
                       "unit": "verify steps/s", "ms_per_step": ms_t, "linear_16_rows_steps_per_s": 1000.0 / ms_l,
                       "steps": args.steps, "warmup": args.warmup,
                       "config": dict(workload_config(cfg), tree="random parents, random tokens")}), flush=True)
@@ -1164,11 +1208,14 @@ def main():
     ap.add_argument("--accept-profile", action="store_true",
                     help="steps with planted drafts at mean accepted lengths 1, 4, 12, 15: accepted tokens/s")
     ap.add_argument("--tree", type=int, default=0,
-                    help="time token-tree verify steps with a random tree of this many nodes (1..16)")
+                    help="time token-tree verify steps with a random tree of this many nodes (1..64; "
+                         "more than 16 run in passes of 16 rows)")
     ap.add_argument("--attn", action="store_true",
                     help="time the verify attention alone at context --ctx instead of the verify step")
     ap.add_argument("--sweep", action="store_true",
                     help="projection sweep 6656->6656 and 6656->26624 at M = 1..16, weights rotated over 2 GB")
+    ap.add_argument("--cudacore", default=None,
+                    help="NxK: the tensor-core GEMM against the CUDA-core (dp4a) GEMM on one shape")
     ap.add_argument("--head-accept", action="store_true",
                     help="LM head 6656->131072 + argmax + accept/rollback at n_past 2055, L ~ U{0..15}")
     ap.add_argument("--ctx-sweep", action="store_true",
@@ -1192,6 +1239,9 @@ def main():
         return
     if args.head_accept:
         run_head_accept(args)
+        return
+    if args.cudacore:
+        run_cudacore(args)
         return
     if args.ctx_sweep:
         run_ctx_sweep(args)

@@ -119,6 +119,14 @@ typedef struct spec_config {
     int32_t page_size;    /* 16                                             */
     int32_t max_ctx;      /* maximum sequence length in positions           */
     float   rms_eps;      /* RMSNorm epsilon, e.g. 1e-6                     */
+    /* Optional sliding-window layers (Ch. 8 §8.6 item 4: "SWA rings"):
+     * with swa_window W > 0, layer l is a sliding-window layer when
+     * l % swa_period == swa_period - 1 (1 <= swa_period <= n_layers); its row
+     * at position p sees positions p-W+1..p, and its K/V live in a ring of W
+     * rows (spec_kv.swa_ring) instead of the paged pool.  16 <= W <= max_ctx.
+     * swa_window = 0: no such layers (swa_period is ignored). */
+    int32_t swa_window;
+    int32_t swa_period;
 } spec_config;
 
 /* Target weights.  Each `const void* const*` is a HOST array of n_layers
@@ -150,7 +158,23 @@ typedef struct spec_weights {
  *   free_stack  int32 [num_pages] LIFO of free physical page ids
  *   free_top    int32 [1]: number of ids on free_stack
  * Committed state = (seq_len, page_table[0 .. ceil(seq_len/16)), free stack).
- * Bytes of positions >= seq_len are stale and carry no meaning. */
+ * Bytes of positions >= seq_len are stale and carry no meaning.
+ *
+ * Sliding-window layers (spec_config.swa_window > 0; NULL pointers otherwise),
+ * with n_swa = n_layers / swa_period such layers, s = l / swa_period:
+ *   swa_ring   bf16 [n_swa][2 (K,V)][n_kv_heads][W][head_dim]: position t of
+ *              layer s in slot t mod W (the window's rows; the caller lays
+ *              down a prefilled context's last W positions there)
+ *   swa_ckpt   bf16 [n_swa][2][n_kv_heads][16][head_dim]: the checkpoint, the
+ *              ring rows that the last verify block overwrote
+ *   swa_state  int32 [2]: {position of the last block (-1: no checkpoint),
+ *              rows in it}; set by spec_kv_reset and the steps
+ * A step saves the ring slots its M rows overwrite into the checkpoint before
+ * writing them; every rollback (the step's own, or spec_kv_rollback) writes
+ * the checkpoint rows of the positions past the new length back.  A rollback
+ * below the last step's position, or after an extend, is refused
+ * (SPEC_ST_ROLLBACK): the ring no longer holds those rows.  The paged pool's
+ * slices of sliding-window layers are not used. */
 typedef struct spec_kv {
     void*    pool;
     int32_t  num_pages;
@@ -159,6 +183,9 @@ typedef struct spec_kv {
     int32_t* seq_len;
     int32_t* free_stack;
     int32_t* free_top;
+    void*    swa_ring;
+    void*    swa_ckpt;
+    int32_t* swa_state;
 } spec_kv;
 
 /* Step result, DEVICE memory written by the accept kernel at the end of the
@@ -291,6 +318,17 @@ SPEC_API int spec_gemm_q4k_sums(spec_ctx* ctx, const void* w_tiled, int N, int K
                        const float* x, int M, float* y,
                        int32_t* isc, int32_t* imn);
 
+/* The same y = W x on CUDA cores: 4-way byte dot products (dp4a) instead of
+ * tensor-core MMAs, for the comparison that chose the tensor cores for the
+ * 16-row tile (the integer-dot anchor of Ch. 32 §32.7 on either unit).  The
+ * integer sums and each superblock's value are the same exact quantities;
+ * the sum over superblocks is split over CTAs and added with atomics, so y
+ * agrees with spec_gemm_q4k within rounding and is not batch-height
+ * invariant.  Not used by the verify step.  Arguments as spec_gemm_q4k
+ * (K <= the largest K of the ctx's model, including 5*H). */
+SPEC_API int spec_gemm_q4k_cudacore(spec_ctx* ctx, const void* w_tiled, int N, int K,
+                                    const float* x, int M, float* y);
+
 /* The same GEMM for callers that must not allocate device memory (no ctx).
  * The pages have no counterpart; this exists for hosts where calling the CUDA
  * allocator is not allowed or not safe at the call site.  Scratch (activation
@@ -322,9 +360,9 @@ SPEC_API int spec_lm_head_argmax(spec_ctx* ctx, const void* w_head_tiled,
                         const float* final_norm, const float* x, int M,
                         int32_t* idx, float* logits);
 
-/* Verify attention of one layer: M query rows at positions
- * seq_len-M .. seq_len-1 (their K/V rows already in the cache) against all
- * positions 0..p_i of row i.  q DEVICE fp32 [M][n_q_heads][head_dim]; out
+/* Verify attention of one (paged, not sliding-window) layer: M query rows at
+ * positions seq_len-M .. seq_len-1 (their K/V rows already in the cache)
+ * against all positions 0..p_i of row i.  q DEVICE fp32 [M][n_q_heads][head_dim]; out
  * DEVICE fp32 [M][n_q_heads*head_dim].  s = q.k/sqrt(head_dim), softmax over
  * the visible positions, o = sum p v; K and V read as bf16. */
 SPEC_API int spec_attention(spec_ctx* ctx, const spec_kv* kv, int layer,
@@ -342,7 +380,8 @@ SPEC_API int spec_accept(spec_ctx* ctx, const int32_t* idx, const int32_t* draft
                 spec_kv* kv, spec_result* res);
 
 /* ---- Token-tree verification (Ch. 33 §33.7: a tree spends the verify batch
- * on covering near-miss branches), up to 16 nodes.
+ * on covering near-miss branches; the section names trees of 24, 32, 48 and
+ * 64 nodes), up to 64 nodes.
  *
  * Node 0 is the carried frontier; node i >= 1 holds the draft token
  * tokens[i], proposed as the continuation of node parent[i] < i (parent[0] =
@@ -353,11 +392,17 @@ SPEC_API int spec_accept(spec_ctx* ctx, const int32_t* idx, const int32_t* draft
  * -> a: accepted_len = depth(a), next_token = argmax of a.  The path's K/V
  * rows move to positions n_past .. n_past + depth(a), and the KV is rolled
  * back to n_past + depth(a) + 1.
- *   hidden   DEVICE fp32 [n][H]; tokens, parent DEVICE int32 [n]; 1 <= n <= 16
- *   path_out DEVICE int32 [16] or NULL: the path's nodes, then -1
- *   taps     as in spec_verify_step_ex (argmax = per node)
- * A parent list that is not a tree in topological order sets
- * SPEC_ST_BAD_TREE before any work; the KV is left as it was. */
+ *   hidden   DEVICE fp32 [n][H]; tokens, parent DEVICE int32 [n]; 1 <= n <= 64
+ *   path_out DEVICE int32 [max(16, n)] or NULL: the path's nodes, then -1
+ *   taps     as in spec_verify_step_ex (argmax and logits = per node; the
+ *            residual taps only for n <= max_rows, else SPEC_EINVAL)
+ * Up to max_rows nodes run as one batched forward; a larger tree runs in
+ * passes of max_rows rows (nodes 0..15, 16..31, ...), each a full forward of
+ * its rows that streams the weights once, with every node's row seeing its
+ * ancestors in earlier passes through the KV cache.  A parent list that is
+ * not a tree in topological order sets SPEC_ST_BAD_TREE before any work; the
+ * KV is left as it was.  A model with sliding-window layers is refused
+ * (SPEC_EINVAL): the path's K/V moves are defined for the paged cache only. */
 SPEC_API int spec_verify_tree(spec_ctx* ctx, const spec_weights* w, spec_kv* kv, const float* hidden,
                               const int32_t* tokens, const int32_t* parent, int n, spec_result* res,
                               int32_t* path_out, const spec_taps* taps);

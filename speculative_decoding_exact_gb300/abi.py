@@ -24,7 +24,8 @@ class spec_config(C.Structure):
     _fields_ = [("hidden", C.c_int32), ("n_layers", C.c_int32), ("n_q_heads", C.c_int32),
                 ("n_kv_heads", C.c_int32), ("head_dim", C.c_int32), ("ffn", C.c_int32),
                 ("vocab", C.c_int32), ("max_rows", C.c_int32), ("page_size", C.c_int32),
-                ("max_ctx", C.c_int32), ("rms_eps", C.c_float)]
+                ("max_ctx", C.c_int32), ("rms_eps", C.c_float), ("swa_window", C.c_int32),
+                ("swa_period", C.c_int32)]
 
 
 class spec_weights(C.Structure):
@@ -36,7 +37,8 @@ class spec_weights(C.Structure):
 class spec_kv(C.Structure):
     _fields_ = [("pool", C.c_void_p), ("num_pages", C.c_int32), ("max_seq_pages", C.c_int32),
                 ("page_table", C.c_void_p), ("seq_len", C.c_void_p), ("free_stack", C.c_void_p),
-                ("free_top", C.c_void_p)]
+                ("free_top", C.c_void_p), ("swa_ring", C.c_void_p), ("swa_ckpt", C.c_void_p),
+                ("swa_state", C.c_void_p)]
 
 
 class spec_result(C.Structure):
@@ -69,6 +71,7 @@ _SIGS = {
     "spec_quantize_q8": (I, [P, P, I, I, P, P, P]),
     "spec_gemm_q4k": (I, [P, P, I, I, P, I, P]),
     "spec_gemm_q4k_sums": (I, [P, P, I, I, P, I, P, P, P]),
+    "spec_gemm_q4k_cudacore": (I, [P, P, I, I, P, I, P]),
     "spec_lm_head_argmax": (I, [P, P, P, P, I, P, P]),
     "spec_attention": (I, [P, C.POINTER(spec_kv), I, P, I, P]),
     "spec_accept": (I, [P, P, P, I, C.POINTER(spec_kv), P]),
@@ -253,3 +256,7 @@ def spec_gemm_q4k_noalloc_status(stream) -> int:
 def spec_set_split(ctx, layer: int, event) -> int:
     """event: a cudaEvent_t handle (e.g. torch.cuda.Event().cuda_event), or None with layer = -1."""
     return _call("spec_set_split", ctx, int(layer), P(event or 0))
+
+
+def spec_gemm_q4k_cudacore(ctx, w, N, K, x, M, y) -> int:
+    return _call("spec_gemm_q4k_cudacore", ctx, P(w), N, K, P(x), M, P(y))

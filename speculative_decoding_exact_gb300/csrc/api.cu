@@ -30,6 +30,12 @@ struct spec_ctx {
   uint8_t* act = nullptr;
   float* pieces = nullptr;
   float* resid = nullptr;        // [16][H]
+  float* q32 = nullptr;          // [16][H] fp32 queries of a sliding-window layer
+  int8_t* q8 = nullptr;          // plain int8 codes, d_a and sub-block sums of the
+  float* da8 = nullptr;          // CUDA-core comparison GEMM
+  int32_t* a8 = nullptr;
+  int kmax = 0;
+  float* swa_part = nullptr;     // sliding-window attention partials
   uint8_t* qtile = nullptr;      // attention query tiles, 64 KB per (kv head, tile)
   float* attn_part = nullptr;
   float* head_val = nullptr;     // [nparts][16]
@@ -39,7 +45,7 @@ struct spec_ctx {
   float* logits_ws = nullptr;    // [16][V] target logits of a sampled step
   float2* sstats = nullptr;      // [16] row max and sum of exp of a sampled step
   uint8_t* sscratch = nullptr;   // decision scratch of a sampled step
-  uint32_t* tree_mask = nullptr; // [16] ancestor masks of a token-tree step
+  uint64_t* tree_mask = nullptr; // [64] ancestor masks of a token-tree step
   uint8_t* tscratch = nullptr;   // decision scratch of a token-tree step
   // hidden-state capture: block outputs of cap_ids[j] -> cap_rows[m][j*H ..]
   int cap_n = 0;
@@ -49,7 +55,7 @@ struct spec_ctx {
   int split_layer = -1;
   cudaEvent_t split_ev = nullptr;
   int32_t* step_state = nullptr; // [2]
-  int32_t* idx_buf = nullptr;    // [16]
+  int32_t* idx_buf = nullptr;    // [64] per-row (per tree node) argmax
   float* hidden_dev = nullptr;   // host-buffer entry point staging
   int32_t* draft_dev = nullptr;
   spec_result* res_dev = nullptr;
@@ -103,14 +109,31 @@ KvView view_of(const spec_ctx* c, const spec_kv* kv) {
   v.n_kv = c->cfg.n_kv_heads;
   v.head_dim = c->cfg.head_dim;
   v.page_size = c->cfg.page_size;
+  v.swa_ring = static_cast<uint16_t*>(kv->swa_ring);
+  v.swa_ckpt = static_cast<uint16_t*>(kv->swa_ckpt);
+  v.swa_state = kv->swa_state;
+  v.swa_window = c->cfg.swa_window;
+  v.swa_period = c->cfg.swa_period;
   return v;
 }
+
+bool has_swa(const spec_config& c) { return c.swa_window > 0; }
+
+// the sliding-window buffers a cache needs under this geometry
+int check_kv_swa(const spec_ctx* c, const spec_kv* kv);
 
 int check_kv(const spec_kv* kv) {
   if (!kv || !kv->pool || !kv->page_table || !kv->seq_len || !kv->free_stack || !kv->free_top)
     return SPEC_ENULL;
   if (kv->num_pages <= 0 || kv->max_seq_pages <= 0 || kv->num_pages > (1 << 30)) return SPEC_EINVAL;
   if (!aligned(kv->pool)) return SPEC_EALIGN;
+  return SPEC_OK;
+}
+
+int check_kv_swa(const spec_ctx* c, const spec_kv* kv) {
+  if (!has_swa(c->cfg)) return SPEC_OK;
+  if (!kv->swa_ring || !kv->swa_ckpt || !kv->swa_state) return SPEC_ENULL;
+  if (!aligned(kv->swa_ring) || !aligned(kv->swa_ckpt)) return SPEC_EALIGN;
   return SPEC_OK;
 }
 
@@ -126,6 +149,10 @@ int check_cfg(const spec_config* c) {
   if (c->max_rows < 1 || c->max_rows > 16) return SPEC_EINVAL;
   if (c->max_ctx < c->max_rows) return SPEC_EINVAL;
   if (!(c->rms_eps >= 0.f)) return SPEC_EINVAL;
+  if (c->swa_window < 0) return SPEC_EINVAL;
+  if (c->swa_window > 0 &&
+      (c->swa_window < 16 || c->swa_window > c->max_ctx || c->swa_period < 1 || c->swa_period > c->n_layers))
+    return SPEC_EINVAL;
   return SPEC_OK;
 }
 
@@ -197,11 +224,19 @@ int spec_verify_init(const spec_config* cfg, void* cuda_stream, spec_ctx** out) 
   int kmax = H > F ? H : F;
   if (5 * H > kmax) kmax = 5 * H;   // a draft front projection over 5 concatenated hidden rows
   c->act_bytes = (size_t)(kmax / 256) * kActSBBytes;
+  c->kmax = kmax;
   c->head_parts = head_argmax_blocks(V);
   rc = SPEC_OK;
   rc |= dalloc(&c->act, c->act_bytes);
   rc |= dalloc(&c->pieces, c->pieces_floats);
   rc |= dalloc(&c->resid, (size_t)16 * H);
+  rc |= dalloc(&c->q8, (size_t)16 * kmax);
+  rc |= dalloc(&c->da8, (size_t)16 * (kmax / 256));
+  rc |= dalloc(&c->a8, (size_t)16 * (kmax / 32));
+  if (has_swa(*cfg)) {
+    rc |= dalloc(&c->q32, (size_t)16 * H);
+    rc |= dalloc(&c->swa_part, swa_partial_floats(cfg->swa_window, cfg->n_q_heads));
+  }
   rc |= dalloc(&c->qtile, qtile_bytes(c->attn));
   rc |= dalloc(&c->attn_part, attn_partial_floats(c->attn, 16));
   rc |= dalloc(&c->head_val, (size_t)c->head_parts * 16);
@@ -210,10 +245,10 @@ int spec_verify_init(const spec_config* cfg, void* cuda_stream, spec_ctx** out) 
   rc |= dalloc(&c->logits_ws, (size_t)16 * V);
   rc |= dalloc(&c->sstats, 16);
   rc |= dalloc(&c->sscratch, sample_scratch_bytes());
-  rc |= dalloc(&c->tree_mask, 16);
+  rc |= dalloc(&c->tree_mask, kTreeMax);
   rc |= dalloc(&c->tscratch, tree_scratch_bytes());
   rc |= dalloc(&c->step_state, 4);
-  rc |= dalloc(&c->idx_buf, 16);
+  rc |= dalloc(&c->idx_buf, kTreeMax);
   rc |= dalloc(&c->hidden_dev, (size_t)16 * H);
   rc |= dalloc(&c->draft_dev, 16);
   rc |= dalloc(&c->res_dev, 1);
@@ -244,6 +279,11 @@ void spec_verify_destroy(spec_ctx* c) {
   cudaFree(c->act);
   cudaFree(c->pieces);
   cudaFree(c->resid);
+  cudaFree(c->q8);
+  cudaFree(c->da8);
+  cudaFree(c->a8);
+  cudaFree(c->q32);
+  cudaFree(c->swa_part);
   cudaFree(c->qtile);
   cudaFree(c->logits_ws);
   cudaFree(c->sstats);
@@ -357,6 +397,15 @@ int spec_gemm_q4k_sums(spec_ctx* c, const void* w, int N, int K, const float* x,
   return gemm_common(c, w, N, K, x, M, y, isc, imn);
 }
 
+int spec_gemm_q4k_cudacore(spec_ctx* c, const void* w, int N, int K, const float* x, int M, float* y) {
+  if (!c || !w || !x || !y) return SPEC_ENULL;
+  if (M < 1 || M > 16 || N <= 0 || K <= 0 || N % 16 || K % 256 || K > c->kmax) return SPEC_EINVAL;
+  if (!aligned(w) || !aligned(x) || !aligned(y)) return SPEC_EALIGN;
+  SPEC_TRY(cudaMemsetAsync(c->status, 0, 4, c->stream));
+  SPEC_TRY(launch_quantize(x, M, K, c->act, c->q8, c->da8, c->a8, c->status, c->stream, false));
+  return cuda_code(launch_gemm_dp4a(w, c->q8, c->da8, c->a8, M, N, K, y, c->num_sms, c->stream));
+}
+
 int spec_lm_head_argmax(spec_ctx* c, const void* w_head, const float* final_norm, const float* x,
                         int M, int32_t* idx, float* logits) {
   if (!c || !w_head || !x || !idx) return SPEC_ENULL;
@@ -377,6 +426,7 @@ int spec_attention(spec_ctx* c, const spec_kv* kv, int layer, const float* q, in
   int rc = check_kv(kv);
   if (rc) return rc;
   if (M < 1 || M > 16 || layer < 0 || layer >= c->cfg.n_layers) return SPEC_EINVAL;
+  if (swa_index(view_of(c, kv), layer) >= 0) return SPEC_EINVAL;   // a ring layer: see the step
   if (kv->max_seq_pages * c->cfg.page_size > c->attn.max_chunks * c->attn.chunk)
     return SPEC_ECAPACITY;   // attention workspace must cover every position the cache can hold
   if (!aligned(q) || !aligned(out)) return SPEC_EALIGN;
@@ -394,17 +444,21 @@ int spec_accept(spec_ctx* c, const int32_t* idx, const int32_t* draft, int k, sp
   if (kv) {
     int rc = check_kv(kv);
     if (rc) return rc;
+    rc = check_kv_swa(c, kv);
+    if (rc) return rc;
   }
   KvView v;
   if (kv) v = view_of(c, kv);
-  return cuda_code(launch_accept(idx, nullptr, nullptr, 0, draft, k, c->cfg.vocab, kv ? &v : nullptr,
-                                 nullptr, c->status, reinterpret_cast<int32_t*>(res), nullptr,
-                                 c->stream, false));
+  SPEC_TRY(launch_accept(idx, nullptr, nullptr, 0, draft, k, c->cfg.vocab, kv ? &v : nullptr,
+                         nullptr, c->status, reinterpret_cast<int32_t*>(res), nullptr, c->stream, false));
+  return kv ? cuda_code(launch_swa_restore(v, c->stream, false)) : SPEC_OK;
 }
 
 int spec_kv_reset(spec_ctx* c, spec_kv* kv) {
   if (!c) return SPEC_ENULL;
   int rc = check_kv(kv);
+  if (rc) return rc;
+  rc = check_kv_swa(c, kv);
   if (rc) return rc;
   return cuda_code(launch_kv_reset(view_of(c, kv), c->stream));
 }
@@ -412,6 +466,8 @@ int spec_kv_reset(spec_ctx* c, spec_kv* kv) {
 int spec_kv_extend(spec_ctx* c, spec_kv* kv, int32_t n) {
   if (!c) return SPEC_ENULL;
   int rc = check_kv(kv);
+  if (rc) return rc;
+  rc = check_kv_swa(c, kv);
   if (rc) return rc;
   if (n < 0) return SPEC_EINVAL;
   return cuda_code(launch_kv_reserve(view_of(c, kv), n, 1, nullptr, 0, 0, c->status, nullptr,
@@ -423,7 +479,10 @@ int spec_kv_rollback(spec_ctx* c, spec_kv* kv, int32_t new_len) {
   int rc = check_kv(kv);
   if (rc) return rc;
   if (new_len < 0) return SPEC_EINVAL;
-  return cuda_code(launch_kv_rollback(view_of(c, kv), new_len, c->status, c->stream));
+  rc = check_kv_swa(c, kv);
+  if (rc) return rc;
+  SPEC_TRY(launch_kv_rollback(view_of(c, kv), new_len, c->status, c->stream));
+  return cuda_code(launch_swa_restore(view_of(c, kv), c->stream, false));
 }
 
 // ---------------------------------------------------------------------------
@@ -484,55 +543,87 @@ static int enqueue_step(spec_ctx* c, const spec_weights* w, spec_kv* kv, const f
   auto attn_gamma = [&](int l) -> const float* { return w->attn_norm ? w->attn_norm[l] : nullptr; };
   auto ffn_gamma = [&](int l) -> const float* { return w->ffn_norm ? w->ffn_norm[l] : nullptr; };
   float* tap_resid = taps ? taps->resid : nullptr;
-  const size_t rows_bytes = sizeof(float) * (size_t)M * H;
 
-  const uint32_t* tmask = ta ? c->tree_mask : nullptr;
+  // A token tree of more than max_rows nodes runs in passes of up to
+  // max_rows rows, each streaming the weights once; every other step is one
+  // pass over its M rows.
+  const int P = ta ? (M < g.max_rows ? M : g.max_rows) : M;
+  const int npass = (M + P - 1) / P;
   SPEC_TRY(launch_kv_reserve(kvv, M, 0, ta ? ta->tokens + 1 : draft, k, g.vocab, c->status, c->step_state, st,
                              true, ta ? ta->parent : nullptr, ta ? c->tree_mask : nullptr)); ++n;
-  if (tap_resid) SPEC_TRY(cudaMemcpyAsync(tap_resid, hidden, rows_bytes, cudaMemcpyDeviceToDevice, st));
-  SPEC_TRY(launch_resid_norm_quant(nullptr, nullptr, hidden, c->resid, attn_gamma(0), g.rms_eps, M, H,
-                                   c->act, nullptr, c->status, st, true)); ++n;
-  for (int l = 0; l < g.n_layers; ++l) {
-    SPEC_TRY(gemm(c->p_qkv, w->w_qkv[l])); ++n;
-    SPEC_TRY(launch_qkv_post(c->p_qkv, c->pieces, M, g.n_q_heads, g.n_kv_heads, g.head_dim, kvv, l,
-                              c->qtile, c->attn.tiles, c->status, st, true, c->attn.early)); ++n;
-    SPEC_TRY(launch_attention(c->attn, kvv, l, c->qtile, M, c->attn_part, nullptr, c->act, c->status,
-                              st, true, tmask)); n += 2;
-    SPEC_TRY(gemm(c->p_o, w->w_o[l])); ++n;
-    SPEC_TRY(launch_resid_norm_quant(&c->p_o, c->pieces, c->resid, c->resid, ffn_gamma(l), g.rms_eps,
-                                     M, H, c->act, nullptr, c->status, st, true)); ++n;
-    SPEC_TRY(gemm(c->p_gu, w->w_gate_up[l])); ++n;
-    SPEC_TRY(launch_swiglu_quant(c->p_gu, c->pieces, M, F, c->act, c->status, st, true)); ++n;
-    SPEC_TRY(gemm(c->p_down, w->w_down[l])); ++n;
-    const float* next_gamma = (l + 1 < g.n_layers) ? attn_gamma(l + 1) : w->final_norm;
-    float* cap = nullptr;
-    for (int j = 0; j < c->cap_n; ++j)
-      if (c->cap_ids[j] == l) cap = c->cap_rows + (size_t)j * H;
-    SPEC_TRY(launch_resid_norm_quant(&c->p_down, c->pieces, c->resid, c->resid, next_gamma, g.rms_eps,
-                                     M, H, c->act, nullptr, c->status, st, true, cap, c->cap_n * H)); ++n;
-    if (tap_resid)
-      SPEC_TRY(cudaMemcpyAsync(tap_resid + (size_t)(l + 1) * M * H, c->resid, rows_bytes,
-                               cudaMemcpyDeviceToDevice, st));
-    // the prefix through block l is done (its output and capture rows are
-    // written): another stream that waits on this event overlaps the suffix
-    if (l == c->split_layer && c->split_ev) {
-      // inside a recorded graph the record is an external event node, which
-      // streams outside the graph can wait on
-      cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-      SPEC_TRY(cudaStreamIsCapturing(st, &cs));
-      SPEC_TRY(cudaEventRecordWithFlags(c->split_ev, st,
-                                        cs == cudaStreamCaptureStatusActive ? cudaEventRecordExternal
-                                                                            : cudaEventRecordDefault));
+  if (has_swa(g)) {
+    SPEC_TRY(launch_swa_checkpoint(kvv, M, c->step_state, c->status, st, true)); ++n;
+  }
+  for (int pass = 0; pass < npass; ++pass) {
+    const int r0 = pass * P, Mp = (M - r0 < P) ? M - r0 : P;
+    const size_t rows_bytes = sizeof(float) * (size_t)Mp * H;
+    const float* hid = hidden + (size_t)r0 * H;
+    const uint64_t* tmask = ta ? c->tree_mask + r0 : nullptr;
+    if (npass > 1) {
+      SPEC_TRY(launch_tree_pass(kvv, c->step_state, c->status, r0 + Mp, st, true)); ++n;
+    }
+    if (tap_resid) SPEC_TRY(cudaMemcpyAsync(tap_resid, hid, rows_bytes, cudaMemcpyDeviceToDevice, st));
+    SPEC_TRY(launch_resid_norm_quant(nullptr, nullptr, hid, c->resid, attn_gamma(0), g.rms_eps, Mp, H,
+                                     c->act, nullptr, c->status, st, true)); ++n;
+    for (int l = 0; l < g.n_layers; ++l) {
+      SPEC_TRY(gemm(c->p_qkv, w->w_qkv[l])); ++n;
+      if (swa_index(kvv, l) >= 0) {
+        // sliding-window layer: K/V into the ring, attention over the window
+        SPEC_TRY(launch_qkv_post(c->p_qkv, c->pieces, Mp, g.n_q_heads, g.n_kv_heads, g.head_dim, kvv, l,
+                                  c->qtile, c->attn.tiles, c->status, st, true, false, c->q32)); ++n;
+        SPEC_TRY(launch_swa_attention(kvv, l, c->q32, Mp, g.n_q_heads, c->swa_part, nullptr, c->act,
+                                      c->status, st, true)); n += 2;
+      } else {
+        SPEC_TRY(launch_qkv_post(c->p_qkv, c->pieces, Mp, g.n_q_heads, g.n_kv_heads, g.head_dim, kvv, l,
+                                  c->qtile, c->attn.tiles, c->status, st, true, c->attn.early)); ++n;
+        SPEC_TRY(launch_attention(c->attn, kvv, l, c->qtile, Mp, c->attn_part, nullptr, c->act, c->status,
+                                  st, true, tmask, ta ? c->step_state : nullptr)); n += 2;
+      }
+      SPEC_TRY(gemm(c->p_o, w->w_o[l])); ++n;
+      SPEC_TRY(launch_resid_norm_quant(&c->p_o, c->pieces, c->resid, c->resid, ffn_gamma(l), g.rms_eps,
+                                       Mp, H, c->act, nullptr, c->status, st, true)); ++n;
+      SPEC_TRY(gemm(c->p_gu, w->w_gate_up[l])); ++n;
+      SPEC_TRY(launch_swiglu_quant(c->p_gu, c->pieces, Mp, F, c->act, c->status, st, true)); ++n;
+      SPEC_TRY(gemm(c->p_down, w->w_down[l])); ++n;
+      const float* next_gamma = (l + 1 < g.n_layers) ? attn_gamma(l + 1) : w->final_norm;
+      float* cap = nullptr;
+      if (pass == 0)                           // the capture holds the first pass's rows
+        for (int j = 0; j < c->cap_n; ++j)
+          if (c->cap_ids[j] == l) cap = c->cap_rows + (size_t)j * H;
+      SPEC_TRY(launch_resid_norm_quant(&c->p_down, c->pieces, c->resid, c->resid, next_gamma, g.rms_eps,
+                                       Mp, H, c->act, nullptr, c->status, st, true, cap, c->cap_n * H)); ++n;
+      if (tap_resid)
+        SPEC_TRY(cudaMemcpyAsync(tap_resid + (size_t)(l + 1) * Mp * H, c->resid, rows_bytes,
+                                 cudaMemcpyDeviceToDevice, st));
+      // the prefix through block l is done (its output and capture rows are
+      // written): another stream that waits on this event overlaps the suffix
+      if (l == c->split_layer && c->split_ev && pass == npass - 1) {
+        // inside a recorded graph the record is an external event node, which
+        // streams outside the graph can wait on
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        SPEC_TRY(cudaStreamIsCapturing(st, &cs));
+        SPEC_TRY(cudaEventRecordWithFlags(c->split_ev, st,
+                                          cs == cudaStreamCaptureStatusActive ? cudaEventRecordExternal
+                                                                              : cudaEventRecordDefault));
+      }
+    }
+    SPEC_TRY(gemm(c->p_head, w->w_head)); ++n;
+    if (ta) {
+      // every node's argmax; the decision follows the last pass
+      SPEC_TRY(launch_head_argmax(c->p_head, c->pieces, Mp,
+                                  taps && taps->logits ? taps->logits + (size_t)r0 * g.vocab : nullptr,
+                                  c->head_val, c->head_idx, c->status, st, true)); ++n;
+      SPEC_TRY(launch_argmax_final(c->head_val, c->head_idx, c->head_parts, Mp, c->idx_buf + r0, st, true)); ++n;
     }
   }
-  SPEC_TRY(gemm(c->p_head, w->w_head)); ++n;
   if (ta) {
-    // token tree: the argmax of every node, the accepted path, its K/V moves
-    SPEC_TRY(launch_head_argmax(c->p_head, c->pieces, M, taps ? taps->logits : nullptr, c->head_val,
-                                c->head_idx, c->status, st, true)); ++n;
-    SPEC_TRY(launch_tree_accept(c->head_val, c->head_idx, c->head_parts, ta->tokens, ta->parent, M, g.vocab,
-                                kvv, c->step_state, c->tscratch, c->status, reinterpret_cast<int32_t*>(res),
-                                ta->path_out, taps ? taps->argmax : nullptr, st, true));
+    // token tree: the accepted path over all nodes, its K/V moves, the rollback
+    if (npass > 1) {
+      SPEC_TRY(launch_tree_pass(kvv, c->step_state, c->status, M, st, true)); ++n;
+    }
+    SPEC_TRY(launch_tree_accept(c->idx_buf, ta->tokens, ta->parent, M, g.vocab, kvv, c->step_state, c->tscratch,
+                                c->status, reinterpret_cast<int32_t*>(res), ta->path_out,
+                                taps ? taps->argmax : nullptr, st, true));
     n += 3;
   } else if (sa) {
     // sampled acceptance: the logits of every row, their normalizers, then
@@ -555,6 +646,10 @@ static int enqueue_step(spec_ctx* c, const spec_weights* w, spec_kv* kv, const f
     SPEC_TRY(launch_accept(nullptr, c->head_val, c->head_idx, c->head_parts, draft, k, g.vocab, &kvv,
                            c->step_state, c->status, reinterpret_cast<int32_t*>(res),
                            taps ? taps->argmax : nullptr, st, true)); ++n;
+  }
+  if (has_swa(g)) {
+    // the ring rows of the rejected positions come back from the checkpoint
+    SPEC_TRY(launch_swa_restore(kvv, st, true)); ++n;
   }
   c->last_launches = n;
   return SPEC_OK;
@@ -590,6 +685,9 @@ static uint64_t step_key(const spec_ctx* c, const spec_weights* w, const spec_kv
   h = mix(h, P(kv->free_top));
   h = mix(h, (uint64_t)kv->num_pages);
   h = mix(h, (uint64_t)kv->max_seq_pages);
+  h = mix(h, P(kv->swa_ring));
+  h = mix(h, P(kv->swa_ckpt));
+  h = mix(h, P(kv->swa_state));
   for (int l = 0; l < c->cfg.n_layers; ++l) {
     h = mix(h, P(w->w_qkv[l]));
     h = mix(h, P(w->w_o[l]));
@@ -607,11 +705,16 @@ static int run_step(spec_ctx* c, const spec_weights* w, spec_kv* kv, const float
                     const int32_t* draft, int k, spec_result* res, const spec_taps* taps,
                     const SampleArgs* sa, const TreeArgs* ta = nullptr) {
   if (!c || !hidden || !draft || !res) return SPEC_ENULL;
-  if (ta ? (k < 0 || k > 15) : (k != 3 && k != 7 && k != 15)) return SPEC_EVERIFYLEN;
+  if (ta ? (k < 0 || k > kTreeMax - 1) : (k != 3 && k != 7 && k != 15)) return SPEC_EVERIFYLEN;
   const int M = k + 1;
-  if (M > c->cfg.max_rows) return SPEC_ECAPACITY;
+  // a tree larger than max_rows runs in passes; the residual taps hold one pass
+  if (!ta && M > c->cfg.max_rows) return SPEC_ECAPACITY;
+  if (ta && M > c->cfg.max_rows && taps && taps->resid) return SPEC_EINVAL;
   int rc = check_kv(kv);
   if (rc) return rc;
+  rc = check_kv_swa(c, kv);
+  if (rc) return rc;
+  if (ta && has_swa(c->cfg)) return SPEC_EINVAL;   // K/V moves of a tree path: paged layers only
   rc = check_weights(c, w);
   if (rc) return rc;
   if (!aligned(hidden)) return SPEC_EALIGN;
@@ -674,7 +777,7 @@ int spec_verify_tree(spec_ctx* c, const spec_weights* w, spec_kv* kv, const floa
                      const int32_t* tokens, const int32_t* parent, int n, spec_result* res,
                      int32_t* path_out, const spec_taps* taps) {
   if (!tokens || !parent) return SPEC_ENULL;
-  if (n < 1 || n > 16) return SPEC_EVERIFYLEN;
+  if (n < 1 || n > kTreeMax) return SPEC_EVERIFYLEN;
   const TreeArgs ta{tokens, parent, path_out};
   return run_step(c, w, kv, hidden, tokens, n - 1, res, taps, nullptr, &ta);
 }
@@ -732,12 +835,15 @@ int spec_sample_accept(spec_ctx* c, const float* logits, const float* q, const i
   if (kv) {
     int rc = check_kv(kv);
     if (rc) return rc;
+    rc = check_kv_swa(c, kv);
+    if (rc) return rc;
   }
   KvView v;
   if (kv) v = view_of(c, kv);
-  return cuda_code(launch_sample_accept(logits, q, draft, k, c->cfg.vocab, c->sstats, c->sscratch, mt,
-                                        kv ? &v : nullptr, nullptr, c->status,
-                                        reinterpret_cast<int32_t*>(res), c->stream, false));
+  SPEC_TRY(launch_sample_accept(logits, q, draft, k, c->cfg.vocab, c->sstats, c->sscratch, mt,
+                                kv ? &v : nullptr, nullptr, c->status, reinterpret_cast<int32_t*>(res),
+                                c->stream, false));
+  return kv ? cuda_code(launch_swa_restore(v, c->stream, false)) : SPEC_OK;
 }
 
 int spec_verify_step_host(spec_ctx* c, const spec_weights* w, spec_kv* kv, const float* hidden_host,

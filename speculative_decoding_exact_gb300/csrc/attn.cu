@@ -216,8 +216,8 @@ template <bool kTree>
 __global__ void __launch_bounds__(kAttnWarps * 32, 1)
 attn_partial_kernel(const uint8_t* __restrict__ qtile, int M, int nq, int nkv, int group, int tiles,
                     int chunk_keys, KvView kv, const __grid_constant__ CUtensorMap kvmap, int layer,
-                    const uint32_t* __restrict__ tree_mask, float* __restrict__ part, int32_t* status,
-                    int early) {
+                    const uint64_t* __restrict__ tree_mask, const int32_t* __restrict__ tree_base,
+                    float* __restrict__ part, int32_t* status, int early) {
   extern __shared__ __align__(128) uint8_t dsm[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm) + 1023) & ~(uintptr_t)1023);
   uint8_t* qs = sm;                                    // Q tile: hi [0, 32K), lo [32K, 64K)
@@ -229,7 +229,7 @@ attn_partial_kernel(const uint8_t* __restrict__ qtile, int M, int nq, int nkv, i
 
   __shared__ float rowmax[2][2][128];       // [sub-chunk parity][column half][row]
   __shared__ float lpart[2][128];           // [column half][row]
-  __shared__ int proceed, len_sh;
+  __shared__ int proceed, len_sh, tb_sh;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int chunk = blockIdx.x, kvh = blockIdx.y, tile = blockIdx.z;
@@ -273,6 +273,7 @@ attn_partial_kernel(const uint8_t* __restrict__ qtile, int M, int nq, int nkv, i
     if (tid == 0) {
       proceed = !(st & kStepAbort) && key0 < len0;
       len_sh = len0;
+      tb_sh = kTree ? __ldcg(tree_base) : 0;
     }
   }
   tc_fence_before();
@@ -281,6 +282,10 @@ attn_partial_kernel(const uint8_t* __restrict__ qtile, int M, int nq, int nkv, i
   const uint32_t tmem = tmem_slot;
   const int len = len_sh;                  // block appended: n_past + M
   const int n_past = len - M;
+  // token tree: the tree's first position (node 0); a tree of more than 16
+  // nodes runs in passes of up to 16 rows, and n_past is this pass's first
+  // row, so earlier passes' nodes lie between the two
+  const int tb = kTree ? tb_sh : n_past;
   // sub-chunks with keys (0 when the CTA has nothing to do)
   const int nsub = proceed ? min(chunk_keys, len - key0 + kChunk - 1) / kChunk : 0;
   // The first sub-chunks whose keys all precede the block (rows of earlier
@@ -417,9 +422,9 @@ attn_partial_kernel(const uint8_t* __restrict__ qtile, int M, int nq, int nkv, i
     const int hl = tile * kHeadsPerTile + (r >> 4);     // head within the kv group
     const int row = r & 15;                             // block row
     const bool live = hl < group && row < M;
-    // token tree: the block rows this row sees (bit j = block row j: its
+    // token tree: the tree nodes this row sees (bit j = node j: its
     // ancestors and itself); the causal step sees rows 0..row
-    const uint32_t tm = (kTree && live) ? tree_mask[row] : 0u;
+    const uint64_t tm = (kTree && live) ? tree_mask[row] : 0ull;
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
     const float c2 = 1.4426950408889634f / sqrtf(128.0f);   // log2(e) / sqrt(d)
     float mref = -INFINITY, lsum = 0.f;
@@ -451,7 +456,7 @@ attn_partial_kernel(const uint8_t* __restrict__ qtile, int M, int nq, int nkv, i
 #pragma unroll
       for (int pp = 0; pp < 4; ++pp) pok[pp] = page_of(ks0 + 16 * pp) >= 0;
       const bool allpages = pok[0] && pok[1] && pok[2] && pok[3];
-      const bool full = ks0 + kChunk - 1 <= n_past && allpages;
+      const bool full = ks0 + kChunk - 1 <= tb && allpages;
       // scores in base-2 units, masked -> -inf
       float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
       if (full && live) {
@@ -461,16 +466,17 @@ attn_partial_kernel(const uint8_t* __restrict__ qtile, int M, int nq, int nkv, i
           mx4[c & 3] = fmaxf(mx4[c & 3], s[c]);
         }
       } else {
-        // tree: key ks0 + 32h + c is visible when it precedes the block (and
-        // the row is live), or when it is block row rel = base + c with bit
-        // rel of tm set, and its page is valid: bit c of vm
+        // tree: key ks0 + 32h + c is visible when it precedes the tree (and
+        // the row is live), or when it is node rel = base + c with bit rel of
+        // tm set, and its page is valid: bit c of vm
         const int lim = live ? n_past + row - ks0 : -1;
         uint32_t vm;
         if (kTree) {
-          const int base = ks0 + 32 * h - n_past;
+          const int base = ks0 + 32 * h - tb;
           const int nold = min(32, max(0, -base));
           const uint32_t mold = !live ? 0u : (nold >= 32 ? 0xffffffffu : (1u << nold) - 1u);
-          const uint32_t blk = base >= 0 ? (base < 32 ? tm >> base : 0u) : (-base < 32 ? tm << -base : 0u);
+          const uint32_t blk = base >= 0 ? (base < 64 ? (uint32_t)(tm >> base) : 0u)
+                                         : (-base < 32 ? (uint32_t)(tm << -base) : 0u);
           const uint32_t pm = ((h ? pok[2] : pok[0]) ? 0x0000ffffu : 0u) | ((h ? pok[3] : pok[1]) ? 0xffff0000u : 0u);
           vm = (mold | blk) & pm;
         }
@@ -675,7 +681,7 @@ attn_merge_kernel(const float* __restrict__ part, int M, int nq, int max_chunks,
 
 cudaError_t launch_attention(const AttnPlan& a, const KvView& kv, int layer, const uint8_t* qtile,
                              int M, float* part, float* out, uint8_t* act, int32_t* status,
-                             cudaStream_t st, bool pdl, const uint32_t* tree_mask) {
+                             cudaStream_t st, bool pdl, const uint64_t* tree_mask, const int32_t* tree_base) {
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -700,7 +706,7 @@ cudaError_t launch_attention(const AttnPlan& a, const KvView& kv, int layer, con
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
   cudaError_t e = cudaLaunchKernelEx(&cfg, kern, qtile, M, a.nq, a.nkv, a.group, a.tiles,
-                                     a.chunk, kv, kvmap, layer, tree_mask, part, status, (int)a.early);
+                                     a.chunk, kv, kvmap, layer, tree_mask, tree_base, part, status, (int)a.early);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg2 = {};
   cfg2.gridDim = dim3(a.nq * 128 / 256, 16);

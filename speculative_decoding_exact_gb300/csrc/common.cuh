@@ -18,6 +18,7 @@ namespace spec {
 constexpr int kSB = 144;            // bytes per Q4_K superblock
 constexpr int kActSlots = 17;       // 16 k-steps + 1 min-term slot per superblock
 constexpr int kActSBBytes = kActSlots * 512 + 64;   // + 16 fp32 d_a
+constexpr int kTreeMax = 64;        // nodes of a token tree (passes of up to 16 rows)
 
 // ---- shared-memory addresses
 SPEC_DEV uint32_t smem_u32(const void* p) {

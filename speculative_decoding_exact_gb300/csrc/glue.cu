@@ -292,7 +292,7 @@ constexpr int kQkvThreads = 256;     // columns per CTA; one more warp prefetche
 __global__ void qkv_post_kernel(const float* __restrict__ pieces, int pN, int pnb, long long pU,
                                 int pG, int M, int nq, int nkv, int dh, KvView kv, int layer,
                                 uint8_t* __restrict__ qtile, int tiles, const int32_t* status,
-                                int late_trigger) {
+                                int late_trigger, float* __restrict__ q32) {
   // With late_trigger the attention that follows reads the KV metadata before
   // its own wait: signalling it only after this wait means that every kernel
   // before this one has completed when it starts.
@@ -304,7 +304,9 @@ __global__ void qkv_post_kernel(const float* __restrict__ pieces, int pN, int pn
   // extra warp sends them to L2 now, while HBM has nothing else to do: lane l
   // of CTA c takes page c + l * (number of CTAs), spreading the copies over
   // the SMs' copy engines; its loads run alongside the other warps' loads.
+  const int swa = swa_index(kv, layer);
   if (threadIdx.x >= kQkvThreads) {
+    if (swa >= 0) return;                    // a ring layer reads no pages
     const int ncta = gridDim.x * gridDim.y;
     const int gi = blockIdx.y * gridDim.x + blockIdx.x + (threadIdx.x - kQkvThreads) * ncta;
     const int lp = gi < kv.max_seq_pages ? gi : kv.max_seq_pages - 1;
@@ -323,12 +325,13 @@ __global__ void qkv_post_kernel(const float* __restrict__ pieces, int pN, int pn
   const int qcols = nq * dh;
   if (col >= pN) return;
   if (row >= M) {
-    if (col < qcols) write_qtile(qtile, row, col / dh, col % dh, 0.f, nq / nkv, tiles);
+    if (col < qcols && swa < 0) write_qtile(qtile, row, col / dh, col % dh, 0.f, nq / nkv, tiles);
     return;
   }
   const float v = piece_sum(pieces, pN, piece_slots(pnb, (int)pU, pG, col), row, col);
   if (col < qcols) {
-    write_qtile(qtile, row, col / dh, col % dh, v, nq / nkv, tiles);
+    if (swa >= 0) q32[(size_t)row * qcols + col] = v;
+    else write_qtile(qtile, row, col / dh, col % dh, v, nq / nkv, tiles);
     return;
   }
   if (*status & kStepAbort) return;
@@ -336,6 +339,13 @@ __global__ void qkv_post_kernel(const float* __restrict__ pieces, int pN, int pn
   const int which = c / (nkv * dh);          // 0 = K, 1 = V
   const int head = (c % (nkv * dh)) / dh, d = c % dh;
   const int pos = *kv.seq_len - M + row;
+  if (swa >= 0) {
+    // the ring slot pos mod W (the checkpoint kernel saved it at the step's start)
+    if (pos >= 0)
+      kv.swa_ring[ring_row(kv, swa, which, head, pos % kv.swa_window) + d] =
+          __bfloat16_as_ushort(__float2bfloat16_rn(v));
+    return;
+  }
   const int lp = pos / kv.page_size;
   if (pos < 0 || lp >= kv.max_seq_pages) return;
   const int page = kv.page_table[lp];
@@ -348,12 +358,13 @@ __global__ void qkv_post_kernel(const float* __restrict__ pieces, int pN, int pn
 
 cudaError_t launch_qkv_post(const GemmPlan& p, const float* pieces, int M, int nq, int nkv, int dh,
                             const KvView& kv, int layer, uint8_t* qtile, int tiles,
-                            const int32_t* status, cudaStream_t st, bool pdl, bool late_trigger) {
+                            const int32_t* status, cudaStream_t st, bool pdl, bool late_trigger,
+                            float* q32) {
   cudaLaunchAttribute attrs[2];
   cudaLaunchConfig_t cfg = make_cfg(dim3((p.N + kQkvThreads - 1) / kQkvThreads, 16), dim3(kQkvThreads + 32), 0,
                                     st, pdl, attrs);
   return cudaLaunchKernelEx(&cfg, qkv_post_kernel, pieces, p.N, p.nb, p.U, p.G, M, nq, nkv, dh, kv,
-                            layer, qtile, tiles, status, (int)late_trigger);
+                            layer, qtile, tiles, status, (int)late_trigger, q32);
 }
 
 // ---------------------------------------------------------------------------
@@ -505,6 +516,10 @@ __global__ void kv_reset_kernel(KvView kv) {
   if (i == 0) {
     *kv.free_top = kv.num_pages;
     *kv.seq_len = 0;
+    if (kv.swa_state) {
+      kv.swa_state[0] = -1;                  // no checkpoint
+      kv.swa_state[1] = 0;
+    }
   }
 }
 
@@ -517,7 +532,7 @@ cudaError_t launch_kv_reset(const KvView& kv, cudaStream_t st) {
 // step_state: [0] = n_past, [1] = 1 when the block was appended
 __global__ void kv_reserve_kernel(KvView kv, int n, int commit, const int32_t* __restrict__ draft,
                                   int k, int vocab, int32_t* status, int32_t* step_state,
-                                  const int32_t* __restrict__ parent, uint32_t* tree_mask) {
+                                  const int32_t* __restrict__ parent, uint64_t* tree_mask) {
   pdl_trigger();
   pdl_wait();
   if (blockIdx.x != 0) return;
@@ -530,20 +545,16 @@ __global__ void kv_reserve_kernel(KvView kv, int n, int commit, const int32_t* _
       step_state[1] = 0;
     }
     if (parent) {
-      // a token tree of n nodes: parent[0] = -1, 0 <= parent[i] < i; the mask
-      // of node i = its ancestors and itself (Ch. 33 §33.7)
-      uint32_t m[16];
-      if (n < 1 || n > 16 || parent[0] != -1) st |= SPEC_ST_BAD_TREE;
-      m[0] = 1u;
-      for (int i = 1; i < n && !st; ++i) {
-        if (parent[i] < 0 || parent[i] >= i) {
-          st |= SPEC_ST_BAD_TREE;
-          break;
-        }
-        m[i] = m[parent[i]] | (1u << i);
+      // a token tree of n <= 64 nodes: parent[0] = -1, 0 <= parent[i] < i;
+      // the mask of node i = its ancestors and itself (Ch. 33 §33.7), built
+      // in place (a parent's mask is final before its children's)
+      if (n < 1 || n > kTreeMax || parent[0] != -1) st |= SPEC_ST_BAD_TREE;
+      for (int i = 1; i < n && !st; ++i)
+        if (parent[i] < 0 || parent[i] >= i) st |= SPEC_ST_BAD_TREE;
+      if (!st) {
+        tree_mask[0] = 1ull;
+        for (int i = 1; i < n; ++i) tree_mask[i] = tree_mask[parent[i]] | (1ull << i);
       }
-      if (!st)
-        for (int i = 0; i < n; ++i) tree_mask[i] = m[i];
     }
     if (draft) {
       for (int i = 0; i < k; ++i)
@@ -577,6 +588,9 @@ __global__ void kv_reserve_kernel(KvView kv, int n, int commit, const int32_t* _
       *kv.free_top = top - need;
       if (commit || step_state) *kv.seq_len = upto;
       if (step_state) step_state[1] = 1;
+      // rows laid down by an extend are not a speculative block: the ring
+      // checkpoint of an earlier step no longer applies
+      if (commit && !step_state && kv.swa_state) kv.swa_state[0] = -1;
     }
   }
   if (lane != 0) return;
@@ -589,7 +603,7 @@ __global__ void kv_reserve_kernel(KvView kv, int n, int commit, const int32_t* _
 
 cudaError_t launch_kv_reserve(const KvView& kv, int n, int commit, const int32_t* draft, int k,
                               int vocab, int32_t* status, int32_t* step_state, cudaStream_t st,
-                              bool pdl, const int32_t* parent, uint32_t* tree_mask) {
+                              bool pdl, const int32_t* parent, uint64_t* tree_mask) {
   cudaLaunchAttribute attrs[2];
   cudaLaunchConfig_t cfg = make_cfg(dim3(1), dim3(32), 0, st, pdl, attrs);
   return cudaLaunchKernelEx(&cfg, kv_reserve_kernel, kv, n, commit, draft, k, vocab, status,
@@ -599,7 +613,11 @@ cudaError_t launch_kv_reserve(const KvView& kv, int n, int commit, const int32_t
 __global__ void kv_rollback_kernel(KvView kv, int new_len, int32_t* status) {
   if (threadIdx.x != 0 || blockIdx.x != 0) return;
   const int len = *kv.seq_len;
-  if (new_len < 0 || new_len > len) {
+  bool bad = new_len < 0 || new_len > len;
+  // a sliding-window ring can be wound back only over the rows its checkpoint
+  // holds: to lengths at or above the last step's n_past
+  if (swa_layers(kv) > 0 && new_len < len && (kv.swa_state[0] < 0 || new_len < kv.swa_state[0])) bad = true;
+  if (bad) {
     atomicOr(status, SPEC_ST_ROLLBACK);
     return;
   }

@@ -49,6 +49,12 @@ cudaError_t launch_gemm(const GemmPlan& p, const void* w_tiled, const uint8_t* a
 cudaError_t launch_sum_pieces(const GemmPlan& p, const float* pieces, float* y, int M,
                               cudaStream_t st, bool pdl);
 
+// the CUDA-core (dp4a) GEMM of the tensor-core comparison: plain int8 codes q
+// [M][K], d_a [M][K/256], sub-block sums A [M][K/32] -> y [M][N] (zeroed
+// here, superblock ranges added with atomics)
+cudaError_t launch_gemm_dp4a(const void* w_tiled, const int8_t* q, const float* da, const int32_t* A, int M,
+                             int N, int K, float* y, int num_sms, cudaStream_t st);
+
 // act buffer: (K/256) superblocks of kActSBBytes bytes (fragment-ordered f16 codes,
 // min-term slot, d_a) produced from fp32 rows x[M][K]
 cudaError_t launch_quantize(const float* x, int M, int K, uint8_t* act, int8_t* q_dbg,
@@ -75,10 +81,48 @@ struct KvView {
   int32_t* free_stack;
   int32_t* free_top;
   int num_pages, max_seq_pages, n_layers, n_kv, head_dim, page_size;
+  // sliding-window layers (swa_window 0: none): ring [n_swa][K,V][n_kv][W][dh]
+  // and checkpoint [n_swa][K,V][n_kv][16][dh] bf16; swa_state = {checkpoint
+  // position n (-1: none), rows checkpointed}
+  uint16_t* swa_ring;
+  uint16_t* swa_ckpt;
+  int32_t* swa_state;
+  int swa_window, swa_period;
 };
+
+// layer l is a sliding-window layer when l % period == period - 1; its index
+// among those layers is l / period
+__host__ __device__ __forceinline__ int swa_index(const KvView& kv, int layer) {
+  if (kv.swa_window <= 0 || kv.swa_period <= 0 || layer % kv.swa_period != kv.swa_period - 1) return -1;
+  return layer / kv.swa_period;
+}
+__host__ __device__ __forceinline__ int swa_layers(const KvView& kv) {
+  return (kv.swa_window > 0 && kv.swa_period > 0) ? kv.n_layers / kv.swa_period : 0;
+}
+__host__ __device__ __forceinline__ size_t ring_row(const KvView& kv, int s, int which, int head, int slot) {
+  return ((((size_t)s * 2 + which) * kv.n_kv + head) * kv.swa_window + slot) * kv.head_dim;
+}
+__host__ __device__ __forceinline__ size_t ckpt_row(const KvView& kv, int s, int which, int head, int j) {
+  return ((((size_t)s * 2 + which) * kv.n_kv + head) * 16 + j) * kv.head_dim;
+}
+// In a sliding-window layer the K,V rows go to the layer's ring and Q to q32
+// (fp32 [16][nq*dh]) instead of the query tiles.
 cudaError_t launch_qkv_post(const GemmPlan& p, const float* pieces, int M, int nq, int nkv,
                             int dh, const KvView& kv, int layer, uint8_t* qtile, int tiles,
-                            const int32_t* status, cudaStream_t st, bool pdl, bool late_trigger);
+                            const int32_t* status, cudaStream_t st, bool pdl, bool late_trigger,
+                            float* q32 = nullptr);
+
+// sliding-window layers: the checkpoint of the ring slots a block of M rows
+// overwrites (after the reservation), the attention of one such layer
+// (partials + merge + quantise for the output projection), and the restore of
+// the checkpoint rows past the committed length (after every rollback)
+int swa_splits(int window);
+size_t swa_partial_floats(int window, int nq);
+cudaError_t launch_swa_checkpoint(const KvView& kv, int M, const int32_t* step_state, const int32_t* status,
+                                  cudaStream_t st, bool pdl);
+cudaError_t launch_swa_restore(const KvView& kv, cudaStream_t st, bool pdl);
+cudaError_t launch_swa_attention(const KvView& kv, int layer, const float* q32, int M, int nq, float* part,
+                                 float* out, uint8_t* act, int32_t* status, cudaStream_t st, bool pdl);
 
 // verify attention: partials then merge (+ quantise for the O projection)
 struct AttnPlan {
@@ -97,11 +141,12 @@ size_t attn_partial_floats(const AttnPlan& a, int max_rows);
 size_t qtile_bytes(const AttnPlan& a);
 cudaError_t launch_q_to_tile(const float* q, int M, const AttnPlan& a, uint8_t* qtile, cudaStream_t st,
                              bool pdl);
-// tree_mask (DEVICE uint32 [M], optional): the block rows row i sees (bit j =
-// block row j); NULL = causal
+// tree_mask (DEVICE uint64 [M], optional): the tree nodes row i sees (bit j
+// = node j at position *tree_base + j); NULL = causal
 cudaError_t launch_attention(const AttnPlan& a, const KvView& kv, int layer, const uint8_t* qtile,
                              int M, float* part, float* out, uint8_t* act, int32_t* status,
-                             cudaStream_t st, bool pdl, const uint32_t* tree_mask = nullptr);
+                             cudaStream_t st, bool pdl, const uint64_t* tree_mask = nullptr,
+                             const int32_t* tree_base = nullptr);
 
 // stochastic exact acceptance: row normalizers (stats fp32x2 [k+1]: max and
 // sum of exp) then the decisions, the final draw and the rollback; mt is the
@@ -112,15 +157,17 @@ cudaError_t launch_sample_accept(const float* logits, const float* q, const int3
                                  const int32_t* step_state, int32_t* status, int32_t* res,
                                  cudaStream_t st, bool pdl);
 
-// token-tree decision: argmax of the n rows from the head partials, the
-// accepted path, the K/V moves of the path and the rollback; path_out (DEVICE
-// int32 [16], optional) = the path's nodes, -1 after it
+// token-tree decision over n <= kTreeMax nodes from every node's argmax idx
+// [n]: the accepted path, its K/V moves and the rollback; path_out (DEVICE
+// int32 [max(16, n)], optional) = the path's nodes, -1 after it
 size_t tree_scratch_bytes();
-cudaError_t launch_tree_accept(const float* part_val, const int32_t* part_idx, int nparts,
-                               const int32_t* tokens, const int32_t* parent, int n, int vocab,
-                               const KvView& kv, const int32_t* step_state, uint8_t* scratch,
+cudaError_t launch_tree_accept(const int32_t* idx, const int32_t* tokens, const int32_t* parent, int n,
+                               int vocab, const KvView& kv, const int32_t* step_state, uint8_t* scratch,
                                int32_t* status, int32_t* res, int32_t* path_out, int32_t* idx_out,
                                cudaStream_t st, bool pdl);
+// a pass of a tree forward over the nodes [.., end): seq_len = tree start + end
+cudaError_t launch_tree_pass(const KvView& kv, const int32_t* step_state, const int32_t* status, int end,
+                             cudaStream_t st, bool pdl);
 
 // LM head argmax over the head GEMM pieces: per-(CTA,row) partial (value, index)
 int head_argmax_blocks(int V);
@@ -138,7 +185,7 @@ cudaError_t launch_kv_reset(const KvView& kv, cudaStream_t st);
 cudaError_t launch_kv_reserve(const KvView& kv, int n, int commit, const int32_t* draft, int k,
                               int vocab, int32_t* status, int32_t* step_state, cudaStream_t st,
                               bool pdl, const int32_t* parent = nullptr,
-                              uint32_t* tree_mask = nullptr);
+                              uint64_t* tree_mask = nullptr);
 cudaError_t launch_kv_rollback(const KvView& kv, int new_len, int32_t* status, cudaStream_t st);
 // accept + rollback; idx [k+1] from head_argmax final reduce (or given)
 cudaError_t launch_accept(const int32_t* idx, const float* part_val, const int32_t* part_idx,

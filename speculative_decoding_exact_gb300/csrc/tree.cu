@@ -7,10 +7,14 @@
 // The deepest accepted node a (the lowest index among equals) ends the path
 // root -> a: L = depth(a) drafts accepted, next = argmax of a.  The path's
 // K/V rows (block slots path[d]) move to slots d, then the KV is rolled back
-// to n_past + L + 1.
+// to n_past + L + 1.  Up to 64 nodes (the section names trees of 24 to 64
+// nodes): the forward runs in passes of up to 16 rows, each with the KV
+// length set to the end of its rows, and every node's argmax is reduced
+// before the decision.
 //
-// Kernels: the decision (one warp), the K/V moves (one CTA per layer, K/V and
-// KV head), the rollback and the result (one thread).
+// Kernels: the length of a pass (one thread), the decision (one thread), the
+// K/V moves (one CTA per layer, K/V and KV head), the rollback and the result
+// (one thread).
 #include "common.cuh"
 #include "internal.h"
 #include "kvmeta.cuh"
@@ -19,57 +23,57 @@ namespace spec {
 
 struct TreeScratch {
   int L, next, status, pad;
-  int path[16];
+  int path[kTreeMax];
 };
 size_t tree_scratch_bytes() { return sizeof(TreeScratch); }
 
-SPEC_DEV void better_idx(float& bv, int& bi, float v, int i) {
-  if (v > bv || (v == bv && i < bi)) {
-    bv = v;
-    bi = i;
-  }
+// before a pass over nodes [.., end): seq_len = the tree's first position +
+// end, so that the step's kernels place row r of the pass at position
+// seq_len - M + r (nothing when the step was aborted)
+__global__ void tree_pass_kernel(KvView kv, const int32_t* step_state, const int32_t* status, int end) {
+  pdl_trigger();
+  pdl_wait();
+  if (threadIdx.x == 0 && !(*status & kStepAbort) && step_state[1]) *kv.seq_len = step_state[0] + end;
 }
 
-__global__ void tree_decide_kernel(const float* __restrict__ part_val, const int32_t* __restrict__ part_idx,
-                                   int nparts, const int32_t* __restrict__ tokens,
+cudaError_t launch_tree_pass(const KvView& kv, const int32_t* step_state, const int32_t* status, int end,
+                             cudaStream_t st, bool pdl) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(32);
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, tree_pass_kernel, kv, step_state, status, end);
+}
+
+// idx [n]: every node's argmax (lowest index among equal maxima)
+__global__ void tree_decide_kernel(const int32_t* __restrict__ idx, const int32_t* __restrict__ tokens,
                                    const int32_t* __restrict__ parent, int n, int vocab,
                                    const int32_t* status, TreeScratch* sc, int32_t* idx_out) {
   pdl_trigger();
   pdl_wait();
-  __shared__ int idx_s[16];
-  const int row = threadIdx.x >> 5, lane = threadIdx.x & 31;   // one warp per node
-  if (row < n) {
-    float bv = -INFINITY;
-    int bi = 0x7fffffff;
-    for (int c = lane; c < nparts; c += 32)
-      better_idx(bv, bi, part_val[(size_t)c * 16 + row], part_idx[(size_t)c * 16 + row]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      better_idx(bv, bi, ov, oi);
-    }
-    if (lane == 0) idx_s[row] = bi;
-  }
-  __syncthreads();
   if (threadIdx.x != 0) return;
   int st = *status;
   for (int row = 0; row < n; ++row) {
-    if (idx_s[row] < 0 || idx_s[row] >= vocab) st |= SPEC_ST_NONFINITE;
-    if (idx_out) idx_out[row] = idx_s[row];
+    if (idx[row] < 0 || idx[row] >= vocab) st |= SPEC_ST_NONFINITE;
+    if (idx_out) idx_out[row] = idx[row];
   }
   int L = 0, next = -1;
   if (!st) {
-    int acc[16], depth[16], best = 0;
+    int acc[kTreeMax], depth[kTreeMax], best = 0;
     acc[0] = 1;
     depth[0] = 0;
     for (int i = 1; i < n; ++i) {
-      acc[i] = acc[parent[i]] && tokens[i] == idx_s[parent[i]];
+      acc[i] = acc[parent[i]] && tokens[i] == idx[parent[i]];
       depth[i] = depth[parent[i]] + 1;
       if (acc[i] && depth[i] > depth[best]) best = i;
     }
     L = depth[best];
-    next = idx_s[best];
+    next = idx[best];
     int a = best;
     for (int d = L; d >= 0; --d) {
       sc->path[d] = a;
@@ -90,7 +94,7 @@ __global__ void tree_compact_kernel(KvView kv, const int32_t* step_state, const 
   if (sc->status || L == 0 || step_state[1] == 0) return;
   const int layer = blockIdx.x, which = blockIdx.y, head = blockIdx.z;
   const int n_past = step_state[0];
-  const int t = threadIdx.x;                // (row d - 1, 16-byte chunk)
+  const int t = threadIdx.x;                // (row d - 1, 16-byte chunk): up to 63 rows
   const int d = 1 + (t >> 4), ch = t & 15;
   auto row_ptr = [&](int slot) -> uint4* {
     const int page = kv.page_table[slot / kv.page_size];
@@ -107,7 +111,7 @@ __global__ void tree_compact_kernel(KvView kv, const int32_t* step_state, const 
 }
 
 __global__ void tree_finish_kernel(KvView kv, const int32_t* step_state, const TreeScratch* sc,
-                                   int32_t* status, int32_t* res, int32_t* path_out) {
+                                   int32_t* status, int32_t* res, int32_t* path_out, int path_len) {
   pdl_trigger();
   pdl_wait();
   if (threadIdx.x != 0) return;
@@ -123,7 +127,7 @@ __global__ void tree_finish_kernel(KvView kv, const int32_t* step_state, const T
     kv_rollback_dev(kv, n_past + L + 1);
   }
   if (path_out)
-    for (int d = 0; d < 16; ++d) path_out[d] = (!st && d <= L) ? sc->path[d] : -1;
+    for (int d = 0; d < path_len; ++d) path_out[d] = (!st && d <= L) ? sc->path[d] : -1;
   *status = st;
   res[0] = L;
   res[1] = next;
@@ -131,12 +135,11 @@ __global__ void tree_finish_kernel(KvView kv, const int32_t* step_state, const T
   res[3] = *kv.seq_len;
 }
 
-cudaError_t launch_tree_accept(const float* part_val, const int32_t* part_idx, int nparts,
-                               const int32_t* tokens, const int32_t* parent, int n, int vocab,
-                               const KvView& kv, const int32_t* step_state, uint8_t* scratch,
+cudaError_t launch_tree_accept(const int32_t* idx, const int32_t* tokens, const int32_t* parent, int n,
+                               int vocab, const KvView& kv, const int32_t* step_state, uint8_t* scratch,
                                int32_t* status, int32_t* res, int32_t* path_out, int32_t* idx_out,
                                cudaStream_t st, bool pdl) {
-  if (kv.head_dim * 2 != 256 || n < 1 || n > 16) return cudaErrorInvalidValue;
+  if (kv.head_dim * 2 != 256 || n < 1 || n > kTreeMax) return cudaErrorInvalidValue;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -146,18 +149,18 @@ cudaError_t launch_tree_accept(const float* part_val, const int32_t* part_idx, i
   cfg.numAttrs = pdl ? 1 : 0;
   TreeScratch* sc = reinterpret_cast<TreeScratch*>(scratch);
   cfg.gridDim = dim3(1);
-  cfg.blockDim = dim3(32 * 16);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, tree_decide_kernel, part_val, part_idx, nparts, tokens, parent, n,
-                                     vocab, (const int32_t*)status, sc, idx_out);
+  cfg.blockDim = dim3(32);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, tree_decide_kernel, idx, tokens, parent, n, vocab,
+                                     (const int32_t*)status, sc, idx_out);
   if (e != cudaSuccess) return e;
   cfg.gridDim = dim3(kv.n_layers, 2, kv.n_kv);
-  cfg.blockDim = dim3(16 * 16);             // 15 rows x 16 chunks of 16 bytes
+  cfg.blockDim = dim3(16 * max(n - 1, 1));  // (n - 1) rows x 16 chunks of 16 bytes
   e = cudaLaunchKernelEx(&cfg, tree_compact_kernel, kv, step_state, (const TreeScratch*)sc);
   if (e != cudaSuccess) return e;
   cfg.gridDim = dim3(1);
   cfg.blockDim = dim3(32);
   return cudaLaunchKernelEx(&cfg, tree_finish_kernel, kv, step_state, (const TreeScratch*)sc, status, res,
-                            path_out);
+                            path_out, n > 16 ? n : 16);
 }
 
 }  // namespace spec

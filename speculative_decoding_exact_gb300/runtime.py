@@ -24,6 +24,18 @@ class ModelConfig:
     vocab: int
     page_size: int = 16
     rms_eps: float = 1e-6
+    swa_window: int = 0     # sliding-window layers: window W (0 = none) ...
+    swa_period: int = 0     # ... at layers l with l % period == period - 1
+
+    def swa_index(self, layer: int) -> int:
+        """Index of layer among the sliding-window layers, or -1."""
+        if self.swa_window <= 0 or self.swa_period <= 0 or layer % self.swa_period != self.swa_period - 1:
+            return -1
+        return layer // self.swa_period
+
+    @property
+    def n_swa(self) -> int:
+        return self.n_layers // self.swa_period if self.swa_window > 0 and self.swa_period > 0 else 0
 
     @property
     def n_qkv(self) -> int:
@@ -49,7 +61,7 @@ class Context:
         self.stream = stream or torch.cuda.current_stream()
         self.c = abi.spec_config(cfg.hidden, cfg.n_layers, cfg.n_q_heads, cfg.n_kv_heads,
                                  cfg.head_dim, cfg.ffn, cfg.vocab, max_rows, cfg.page_size,
-                                 max_ctx, cfg.rms_eps)
+                                 max_ctx, cfg.rms_eps, cfg.swa_window, cfg.swa_period)
         self.h = abi.spec_verify_init(self.c, self.stream.cuda_stream)
         self.max_ctx = max_ctx
 
@@ -116,11 +128,39 @@ class DeviceKV:
         self.free_top = torch.zeros(4, dtype=torch.int32, device="cuda")
         self.num_pages = num_pages
         self.max_seq_pages = max_seq_pages
+        # sliding-window layers: ring [n_swa][K,V][n_kv][W][dh], checkpoint of 16 rows, state
+        self.swa_ring = self.swa_ckpt = self.swa_state = None
+        if cfg.n_swa > 0:
+            self.swa_ring = torch.zeros((cfg.n_swa, 2, cfg.n_kv_heads, cfg.swa_window, cfg.head_dim),
+                                        dtype=torch.bfloat16, device="cuda")
+            self.swa_ckpt = torch.zeros((cfg.n_swa, 2, cfg.n_kv_heads, 16, cfg.head_dim),
+                                        dtype=torch.bfloat16, device="cuda")
+            self.swa_state = torch.full((4,), -1, dtype=torch.int32, device="cuda")
 
     def struct(self) -> abi.spec_kv:
         return abi.spec_kv(self.pool.data_ptr(), self.num_pages, self.max_seq_pages,
                            self.page_table.data_ptr(), self.seq_len.data_ptr(),
-                           self.free_stack.data_ptr(), self.free_top.data_ptr())
+                           self.free_stack.data_ptr(), self.free_top.data_ptr(),
+                           ptr(self.swa_ring), ptr(self.swa_ckpt), ptr(self.swa_state))
+
+    def write_ring_rows(self, layer: int, pos0: int, k_bits: np.ndarray, v_bits: np.ndarray):
+        """Write bf16 bit patterns [n][n_kv*dh] of positions pos0.. of a
+        sliding-window layer into its ring (slot = position mod W)."""
+        s = self.cfg.swa_index(layer)
+        assert s >= 0
+        n, W, nkv, dh = k_bits.shape[0], self.cfg.swa_window, self.cfg.n_kv_heads, self.cfg.head_dim
+        kb = torch.from_numpy(k_bits.astype(np.int16).reshape(n, nkv, dh)).cuda()
+        vb = torch.from_numpy(v_bits.astype(np.int16).reshape(n, nkv, dh)).cuda()
+        slots = torch.from_numpy((np.arange(pos0, pos0 + n) % W).astype(np.int64)).cuda()
+        ring16 = self.swa_ring.view(torch.int16)
+        ring16[s, 0, :, slots, :] = kb.permute(1, 0, 2)
+        ring16[s, 1, :, slots, :] = vb.permute(1, 0, 2)
+
+    def ring_rows(self, layer: int, positions) -> np.ndarray:
+        """bf16 bits [2][n_kv][len(positions)][dh] of the given positions' ring slots."""
+        s = self.cfg.swa_index(layer)
+        slots = np.asarray(positions) % self.cfg.swa_window
+        return self.swa_ring.view(torch.int16)[s][:, :, slots, :].cpu().numpy().view(np.uint16)
 
     def reset(self, ctx: Context):
         abi.check("spec_kv_reset", abi.spec_kv_reset(ctx.h, self.struct()))

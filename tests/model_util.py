@@ -9,7 +9,8 @@ from speculative_decoding_exact_gb300 import runtime, synth
 def ocfg_of(cfg: runtime.ModelConfig) -> oracle.Config:
     return oracle.Config(hidden=cfg.hidden, n_layers=cfg.n_layers, n_q_heads=cfg.n_q_heads,
                          n_kv_heads=cfg.n_kv_heads, head_dim=cfg.head_dim, ffn=cfg.ffn,
-                         vocab=cfg.vocab, rms_eps=cfg.rms_eps)
+                         vocab=cfg.vocab, rms_eps=cfg.rms_eps, swa_window=cfg.swa_window,
+                         swa_period=cfg.swa_period)
 
 
 def build_model(ctx, cfg: runtime.ModelConfig, seed: int = 0, gammas: bool = True,
@@ -53,7 +54,12 @@ def fill_context(cfg, dkv, okv, n_past: int, seed: int):
     for l in range(cfg.n_layers):
         kb = synth.bf16_bits(synth.normal((n_past, cfg.n_kv_heads * cfg.head_dim), seed, 2 * l + 100))
         vb = synth.bf16_bits(synth.normal((n_past, cfg.n_kv_heads * cfg.head_dim), seed, 2 * l + 101))
-        dkv.write_rows_bulk(l, n_past, kb, vb)
+        if cfg.swa_index(l) >= 0:
+            # a sliding-window layer keeps the last W positions in its ring
+            p0 = max(0, n_past - cfg.swa_window)
+            dkv.write_ring_rows(l, p0, kb[p0:], vb[p0:])
+        else:
+            dkv.write_rows_bulk(l, n_past, kb, vb)
         if okv is not None:
             for p in range(n_past):
                 page, slot = okv.page_table[p // 16], p % 16

@@ -199,6 +199,22 @@ def test_gemm_integer_sums_exact_at_extreme_magnitudes(ctx, K):
     assert_close(y, oy, what="y")
 
 
+@pytest.mark.parametrize("M,N,K", [(16, 1024, 6656), (5, 2048, 17920), (1, 272, 256)])
+def test_cudacore_gemm_matches_oracle_and_tensor_core_gemm(ctx, M, N, K):
+    """The dp4a comparison kernel computes the same y within rounding."""
+    W = synth.q4k_matrix(N, K, 12, N + K)
+    x = synth.normal((M, K), 12, 3 * M + K)
+    Wt = runtime.upload_tiled(ctx, W, N, K)
+    y = torch.zeros((M, N), dtype=torch.float32, device="cuda")
+    xd = dev(x)
+    abi.check("spec_gemm_q4k_cudacore", abi.spec_gemm_q4k_cudacore(ctx.h, Wt.data_ptr(), N, K, xd.data_ptr(), M,
+                                                                   y.data_ptr()))
+    sync()
+    yc = y.cpu().numpy()
+    assert_close(yc, oracle.linear(W, N, K, x), what="dp4a GEMM vs oracle")
+    assert_close(yc, run_gemm(ctx, Wt, N, K, x), what="dp4a GEMM vs tensor-core GEMM")
+
+
 @pytest.mark.parametrize("N", [6656, 26624])
 def test_gemm_full_width_sampled(ctx, N):
     """Projection sweep shapes (K=6656, M=16): all outputs on the GPU, a sample of

@@ -53,7 +53,7 @@ def gpu_tree(ctx, dw, dkv, rows, tokens, parent):
     t = torch.from_numpy(np.ascontiguousarray(tokens, dtype=np.int32)).cuda()
     p = torch.from_numpy(np.ascontiguousarray(parent, dtype=np.int32)).cuda()
     res = torch.zeros(4, dtype=torch.int32, device="cuda")
-    path = torch.zeros(16, dtype=torch.int32, device="cuda")
+    path = torch.zeros(max(16, n), dtype=torch.int32, device="cuda")
     am = torch.zeros(n, dtype=torch.int32, device="cuda")
     lg = torch.zeros((n, SMALL.vocab), dtype=torch.float32, device="cuda")
     taps = abi.spec_taps(None, am.data_ptr(), lg.data_ptr())
@@ -186,3 +186,81 @@ def test_tree_graph_replay_and_bad_tree(model):
     after = dkv.state()
     assert after[0] == before[0] and all(np.array_equal(x, y) for x, y in zip(after[1:], before[1:]))
     assert np.all(path.cpu().numpy() == -1)
+
+
+def planted_big_tree(cfg, ow, okv0, seed, depth_max, decoys):
+    """A true branch of depth depth_max following the oracle's greedy decode,
+    with decoys (wrong tokens, other rows) hanging off random true nodes."""
+    rng = np.random.default_rng(seed)
+    hidden = synth.normal((depth_max + 1, cfg.hidden), 7, 900 + seed)
+    serial, _ = oracle.serial_greedy(ocfg_of(cfg), ow, okv0.copy(), hidden, depth_max)
+    L_t = int(rng.integers(depth_max // 2, depth_max + 1))
+    rows, tokens, parent, true_node = [hidden[0]], [0], [-1], [0]
+    for depth in range(depth_max):
+        for _ in range(int(rng.integers(decoys[0], decoys[1] + 1))):
+            rows.append(synth.normal((cfg.hidden,), 7, 5000 + 97 * seed + len(rows)))
+            tokens.append((serial[depth] + 1 + int(rng.integers(0, cfg.vocab - 1))) % cfg.vocab)
+            parent.append(int(rng.choice(true_node)))
+        rows.append(hidden[depth + 1])
+        tokens.append(serial[depth] if depth < L_t else (serial[depth] + 5) % cfg.vocab)
+        parent.append(true_node[-1])
+        true_node.append(len(rows) - 1)
+    return (np.stack(rows).astype(np.float32), np.array(tokens, dtype=np.int32),
+            np.array(parent, dtype=np.int32), L_t)
+
+
+@pytest.mark.parametrize("seed,depth_max,decoys", [(1, 7, (2, 3)), (2, 10, (2, 4)), (3, 12, (3, 4))])
+def test_large_tree_step_matches_oracle(model, seed, depth_max, decoys):
+    """Trees of 24 to 64 nodes (Ch. 33 §33.7), verified in passes of 16 rows."""
+    ctx, ow, dw = model
+    cfg = SMALL
+    dkv, okv = fresh_kv(ctx)
+    rows, tokens, parent, L_t = planted_big_tree(cfg, ow, okv, seed, depth_max, decoys)
+    n = len(parent)
+    assert 17 <= n <= 64, n
+    ores, opath, oidx, olg = oracle.verify_tree(ocfg_of(cfg), ow, okv, rows, tokens, parent)
+    assert ores[2] == 0 and ores[0] == L_t
+    res, path, am, lg = gpu_tree(ctx, dw, dkv, rows, tokens, parent)
+    assert res[2] == 0
+    assert_close(lg, olg, what=f"logits of {n} nodes")
+    _, gap = oracle.argmax(olg)
+    require_clear_rows(gap, f"large tree {seed} ({n} nodes)")
+    assert np.array_equal(am, oidx)
+    assert list(res) == list(ores)
+    assert np.array_equal(path[: res[0] + 1], opath) and np.all(path[res[0] + 1:] == -1)
+    kv_rows_equal(dkv, okv, int(ores[3]))
+
+
+def test_large_chain_tree_and_64_nodes(model):
+    """A chain of 40 nodes accepts down to its first wrong token; a 64-node
+    tree (the largest) matches the oracle and its graph replay."""
+    ctx, ow, dw = model
+    cfg = SMALL
+    dkv, okv = fresh_kv(ctx)
+    rows, tokens, parent, _ = planted_big_tree(cfg, ow, okv, 9, 16, (3, 3))
+    rows, tokens, parent = rows[:64], tokens[:64], parent[:64]
+    assert len(parent) == 64
+    ores, opath, oidx, olg = oracle.verify_tree(ocfg_of(cfg), ow, okv, rows, tokens, parent)
+    _, gap = oracle.argmax(olg)
+    require_clear_rows(gap, "64-node tree")
+    res, path, am, _ = gpu_tree(ctx, dw, dkv, rows, tokens, parent)
+    assert list(res) == list(ores) and np.array_equal(am, oidx)
+    assert np.array_equal(path[: res[0] + 1], opath)
+    kv_rows_equal(dkv, okv, int(ores[3]))
+    # the same tree through the recorded graph (no taps), twice
+    h = torch.from_numpy(rows).cuda()
+    t = torch.from_numpy(tokens).cuda()
+    p = torch.from_numpy(parent).cuda()
+    r = torch.zeros(4, dtype=torch.int32, device="cuda")
+    pth = torch.zeros(64, dtype=torch.int32, device="cuda")
+    for _ in range(2):
+        dkv2, _ = fresh_kv(ctx)
+        abi.check("spec_verify_tree", abi.spec_verify_tree(ctx.h, dw.struct(), dkv2.struct(), h.data_ptr(),
+                                                           t.data_ptr(), p.data_ptr(), 64, r.data_ptr(),
+                                                           pth.data_ptr(), None))
+        torch.cuda.synchronize()
+        assert list(r.cpu().numpy()) == list(ores)
+        assert np.array_equal(pth.cpu().numpy()[: res[0] + 1], opath)
+    # 65 nodes: refused before any work
+    assert abi.spec_verify_tree(ctx.h, dw.struct(), dkv2.struct(), h.data_ptr(), t.data_ptr(), p.data_ptr(), 65,
+                                r.data_ptr(), pth.data_ptr(), None) == abi.SPEC_EVERIFYLEN

@@ -329,6 +329,15 @@ SPEC_API int spec_gemm_q4k_sums(spec_ctx* ctx, const void* w_tiled, int N, int K
 SPEC_API int spec_gemm_q4k_cudacore(spec_ctx* ctx, const void* w_tiled, int N, int K,
                                     const float* x, int M, float* y);
 
+/* Self-test of the bounded device waits (failure detection without a GPU
+ * fault): launches the GEMM kernel on w_tiled (N x K, as spec_gemm_q4k) with
+ * its copy producer held back, so that no bulk copy or MMA is ever issued
+ * and every consumer wait gives up after its limit (about 2 s).  The kernel
+ * then unwinds and frees its tensor memory; the ctx status word holds
+ * SPEC_ST_DEVICE_WAIT (spec_last_status) and the context stays usable.
+ * Writes no output. */
+SPEC_API int spec_gemm_wait_selftest(spec_ctx* ctx, const void* w_tiled, int N, int K);
+
 /* The same GEMM for callers that must not allocate device memory (no ctx).
  * The pages have no counterpart; this exists for hosts where calling the CUDA
  * allocator is not allowed or not safe at the call site.  Scratch (activation

@@ -72,6 +72,7 @@ _SIGS = {
     "spec_gemm_q4k": (I, [P, P, I, I, P, I, P]),
     "spec_gemm_q4k_sums": (I, [P, P, I, I, P, I, P, P, P]),
     "spec_gemm_q4k_cudacore": (I, [P, P, I, I, P, I, P]),
+    "spec_gemm_wait_selftest": (I, [P, P, I, I]),
     "spec_lm_head_argmax": (I, [P, P, P, P, I, P, P]),
     "spec_attention": (I, [P, C.POINTER(spec_kv), I, P, I, P]),
     "spec_accept": (I, [P, P, P, I, C.POINTER(spec_kv), P]),
@@ -260,3 +261,7 @@ def spec_set_split(ctx, layer: int, event) -> int:
 
 def spec_gemm_q4k_cudacore(ctx, w, N, K, x, M, y) -> int:
     return _call("spec_gemm_q4k_cudacore", ctx, P(w), N, K, P(x), M, P(y))
+
+
+def spec_gemm_wait_selftest(ctx, w, N, K) -> int:
+    return _call("spec_gemm_wait_selftest", ctx, P(w), N, K)

@@ -397,6 +397,16 @@ int spec_gemm_q4k_sums(spec_ctx* c, const void* w, int N, int K, const float* x,
   return gemm_common(c, w, N, K, x, M, y, isc, imn);
 }
 
+int spec_gemm_wait_selftest(spec_ctx* c, const void* w, int N, int K) {
+  if (!c || !w) return SPEC_ENULL;
+  if (N <= 0 || K <= 0 || N % 16 || K % 256 || K > c->kmax) return SPEC_EINVAL;
+  if (!aligned(w)) return SPEC_EALIGN;
+  const GemmPlan p = make_gemm_plan(N, K, c->num_sms);
+  if (pieces_need(p) > c->pieces_floats) return SPEC_ECAPACITY;
+  SPEC_TRY(cudaMemsetAsync(c->status, 0, 4, c->stream));
+  return cuda_code(launch_gemm(p, w, c->act, c->pieces, nullptr, nullptr, 0, c->status, c->stream, false, true));
+}
+
 int spec_gemm_q4k_cudacore(spec_ctx* c, const void* w, int N, int K, const float* x, int M, float* y) {
   if (!c || !w || !x || !y) return SPEC_ENULL;
   if (M < 1 || M > 16 || N <= 0 || K <= 0 || N % 16 || K % 256 || K > c->kmax) return SPEC_EINVAL;

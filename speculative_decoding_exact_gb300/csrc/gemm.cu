@@ -193,7 +193,7 @@ __global__ void __maxnreg__(kGemmMaxRegs)
 gemm_q4k_kernel(const uint8_t* __restrict__ wt, const uint8_t* __restrict__ act,
                 float* __restrict__ pieces, int N, int nb, int U, int G,
                 int32_t* __restrict__ isc_out, int32_t* __restrict__ imn_out, int m_sums,
-                int pre_stages, int32_t* status) {
+                int pre_stages, int withhold, int32_t* status) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ uint32_t tmem_slot;
   __shared__ __align__(8) uint64_t full[kGemmStages], empty[kGemmStages];
@@ -243,7 +243,10 @@ gemm_q4k_kernel(const uint8_t* __restrict__ wt, const uint8_t* __restrict__ act,
       // while the previous (latency-bound) kernel reads its inputs from L2,
       // and 152 CTAs x 6 stages of 18 KB queued in front of those reads slowed
       // them (the plan sets the depth per GEMM).
-      const int pre = min(nunits, min(max(pre_stages, 0), kGemmStages));
+      // withhold (the self-test of the bounded waits): no copy is issued, so
+      // every consumer wait gives up with nothing in flight
+      const int nissue = withhold ? 0 : nunits;
+      const int pre = min(nissue, min(max(pre_stages, 0), kGemmStages));
       {
         int gg = g, bb = b;
         for (int i = 0; i < pre; ++i) {
@@ -256,7 +259,7 @@ gemm_q4k_kernel(const uint8_t* __restrict__ wt, const uint8_t* __restrict__ act,
       }
       pdl_trigger();
       pdl_wait();
-      for (int i = 0; i < nunits; ++i) {
+      for (int i = 0; i < nissue; ++i) {
         const int s = i % kGemmStages;
         if (i >= kGemmStages && !mbar_wait_ns(&empty[s], ((i / kGemmStages) - 1) & 1, kWaitNs)) {
           ok = false;
@@ -507,7 +510,7 @@ cudaError_t gemm_init_attributes() {
 
 cudaError_t launch_gemm(const GemmPlan& p, const void* w_tiled, const uint8_t* act, float* pieces,
                         int32_t* isc, int32_t* imn, int m_sums, int32_t* status, cudaStream_t st,
-                        bool pdl) {
+                        bool pdl, bool withhold) {
   const size_t smem = gemm_smem_bytes();
   const bool sums = isc != nullptr;
   auto kern = sums ? gemm_q4k_kernel<true> : gemm_q4k_kernel<false>;
@@ -522,7 +525,7 @@ cudaError_t launch_gemm(const GemmPlan& p, const void* w_tiled, const uint8_t* a
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kern, static_cast<const uint8_t*>(w_tiled), act, pieces, p.N, p.nb,
-                            (int)p.U, p.G, isc, imn, m_sums, p.pre_stages, status);
+                            (int)p.U, p.G, isc, imn, m_sums, p.pre_stages, (int)withhold, status);
 }
 
 // y[m][n] = sum over the group's slots, in slot order

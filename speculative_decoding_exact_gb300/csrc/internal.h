@@ -42,9 +42,11 @@ int plan_slots_of_group(const GemmPlan& p, int gr);
 
 // ---- launchers (all enqueue on `st`; `pdl` = programmatic dependent launch)
 cudaError_t launch_repack(const void* src, void* dst, int N, int K, cudaStream_t st);
+// withhold: the producer issues no copy (the self-test of the bounded waits:
+// every consumer gives up after its limit with nothing in flight)
 cudaError_t launch_gemm(const GemmPlan& p, const void* w_tiled, const uint8_t* act, float* pieces,
                         int32_t* isc, int32_t* imn, int m_sums, int32_t* status, cudaStream_t st,
-                        bool pdl);
+                        bool pdl, bool withhold = false);
 // y[m][n] = sum of the pieces, m < M
 cudaError_t launch_sum_pieces(const GemmPlan& p, const float* pieces, float* y, int M,
                               cudaStream_t st, bool pdl);

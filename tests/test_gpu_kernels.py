@@ -215,6 +215,28 @@ def test_cudacore_gemm_matches_oracle_and_tensor_core_gemm(ctx, M, N, K):
     assert_close(yc, run_gemm(ctx, Wt, N, K, x), what="dp4a GEMM vs tensor-core GEMM")
 
 
+def test_bounded_waits_give_up_and_leave_the_context_usable(ctx):
+    """Failure detection without a GPU fault: with the GEMM's copy producer
+    held back, every consumer wait runs out (about 2 s), the kernel unwinds
+    with nothing in flight and reports SPEC_ST_DEVICE_WAIT; the next GEMM on
+    the same context is correct and clean."""
+    import time
+    N, K, M = 1024, 6656, 16
+    W = synth.q4k_matrix(N, K, 13, 1)
+    Wt = runtime.upload_tiled(ctx, W, N, K)
+    sync()
+    t0 = time.perf_counter()
+    abi.check("spec_gemm_wait_selftest", abi.spec_gemm_wait_selftest(ctx.h, Wt.data_ptr(), N, K))
+    st = abi.spec_last_status(ctx.h)                 # synchronises
+    dt = time.perf_counter() - t0
+    assert st == abi.ST_DEVICE_WAIT, st
+    assert 1.0 < dt < 30.0, dt                       # the waits' 2 s limit, not a hang
+    x = synth.normal((M, K), 13, 2)
+    y = run_gemm(ctx, Wt, N, K, x)
+    assert abi.spec_last_status(ctx.h) == 0
+    assert_close(y, oracle.linear(W, N, K, x), what="GEMM after the self-test")
+
+
 @pytest.mark.parametrize("N", [6656, 26624])
 def test_gemm_full_width_sampled(ctx, N):
     """Projection sweep shapes (K=6656, M=16): all outputs on the GPU, a sample of

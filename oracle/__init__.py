@@ -49,13 +49,14 @@ class _Cfg(C.Structure):
     _fields_ = [("hidden", C.c_int32), ("n_layers", C.c_int32), ("n_q_heads", C.c_int32),
                 ("n_kv_heads", C.c_int32), ("head_dim", C.c_int32), ("ffn", C.c_int32),
                 ("vocab", C.c_int32), ("page_size", C.c_int32), ("rms_eps", C.c_float),
-                ("swa_window", C.c_int32), ("swa_period", C.c_int32)]
+                ("swa_window", C.c_int32), ("swa_period", C.c_int32), ("rope_theta", C.c_float)]
 
 
 class _Weights(C.Structure):
     _fields_ = [("w_qkv", C.c_void_p), ("w_o", C.c_void_p), ("w_gate_up", C.c_void_p),
                 ("w_down", C.c_void_p), ("attn_norm", C.c_void_p), ("ffn_norm", C.c_void_p),
-                ("final_norm", C.c_void_p), ("w_head", C.c_void_p)]
+                ("final_norm", C.c_void_p), ("w_head", C.c_void_p), ("q_norm", C.c_void_p),
+                ("k_norm", C.c_void_p)]
 
 
 class _KV(C.Structure):
@@ -276,10 +277,12 @@ class Config:
     rms_eps: float = 1e-6
     swa_window: int = 0      # sliding-window layers: every swa_period-th layer (the last of each period)
     swa_period: int = 0
+    rope_theta: float = 0.0  # rotary position embedding of q and k (0 = none)
 
     def c(self) -> _Cfg:
         return _Cfg(self.hidden, self.n_layers, self.n_q_heads, self.n_kv_heads, self.head_dim,
-                    self.ffn, self.vocab, self.page_size, self.rms_eps, self.swa_window, self.swa_period)
+                    self.ffn, self.vocab, self.page_size, self.rms_eps, self.swa_window, self.swa_period,
+                    self.rope_theta)
 
     def layer_window(self, layer: int) -> int:
         return int(lib().orc_layer_window(C.byref(self.c()), int(layer)))
@@ -300,6 +303,8 @@ class Weights:
     attn_norm: list | None = None
     ffn_norm: list | None = None
     final_norm: np.ndarray | None = None
+    q_norm: list | None = None       # per-layer QK-norm gains [head_dim] (None = no QK-norm)
+    k_norm: list | None = None
     _keep: list = field(default_factory=list, repr=False)
 
     def c(self) -> _Weights:
@@ -312,7 +317,7 @@ class Weights:
         return _Weights(arr(self.w_qkv), arr(self.w_o), arr(self.w_gate_up), arr(self.w_down),
                         arr(self.attn_norm), arr(self.ffn_norm),
                         None if self.final_norm is None else self.final_norm.ctypes.data,
-                        self.w_head.ctypes.data)
+                        self.w_head.ctypes.data, arr(self.q_norm), arr(self.k_norm))
 
 
 class KV:
@@ -394,6 +399,14 @@ class KV:
         return other
 
 
+def qk_norm_rope(cfg: Config, w: Weights, layer: int, qkv: np.ndarray, n_past: int) -> np.ndarray:
+    """QK-norm (when the layer has gains) and RoPE (when rope_theta > 0) of the
+    rows of a QKV projection output [M][(nq + 2 nkv) * dh] at positions n_past.."""
+    out = np.ascontiguousarray(qkv, dtype=np.float32).copy()
+    lib().orc_qk_norm_rope(C.byref(cfg.c()), C.byref(w.c()), int(layer), _p(out), out.shape[0], int(n_past))
+    return out
+
+
 def block(cfg: Config, w: Weights, kv: KV, layer: int, x: np.ndarray, n_past: int):
     x = np.ascontiguousarray(x, dtype=np.float32)
     out = np.empty_like(x)
@@ -473,8 +486,10 @@ def verify_tree(cfg: Config, w: Weights, kv: KV, hidden: np.ndarray, tokens: np.
     idx = np.full(n, -1, dtype=np.int32)
     lg = np.empty((n, cfg.vocab), dtype=np.float32) if logits else None
     c, cw, ck = cfg.c(), w.c(), kv.c()
-    lib().orc_verify_tree(C.byref(c), C.byref(cw), C.byref(ck), _p(hidden), _p(tokens), _p(parent), n,
-                          _p(res), _p(path), _p(idx), _p(lg))
+    rc = lib().orc_verify_tree(C.byref(c), C.byref(cw), C.byref(ck), _p(hidden), _p(tokens), _p(parent), n,
+                               _p(res), _p(path), _p(idx), _p(lg))
+    if rc:
+        raise ValueError("token trees are not modelled with rotary positions")
     return res, path[: res[0] + 1].copy(), idx, lg
 
 

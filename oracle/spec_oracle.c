@@ -557,6 +557,53 @@ void orc_attention(const orc_cfg* c, const orc_kv* kv, int layer, const float* q
 }
 
 /* ------------------------------------------------------------------------ */
+/* QK-norm and rotary position embedding ([8] §8.2: the draft's attention    */
+/* has "QK-norms and RoPE like an ordinary transformer block").  Readings:    */
+/*   QK-norm: each q head and each k head x (head_dim values) becomes         */
+/*     x_d / sqrt(mean(x^2) + eps) * g_d, the layer's gain g shared by heads; */
+/*   RoPE ("rotate half"): with h = head_dim/2 and f_i = theta^(-i/h), the    */
+/*     pair (x_i, x_{i+h}) at position p rotates by the angle p * f_i:        */
+/*     x_i' = x_i cos - x_{i+h} sin,  x_{i+h}' = x_{i+h} cos + x_i sin.       */
+/* Computed in fp64 and stored fp32; v is not touched.                        */
+/* ------------------------------------------------------------------------ */
+static void orc_head_norm_rope(const orc_cfg* c, const float* gain, float* x, int pos) {
+    int dh = c->head_dim, h = dh / 2;
+    double y[256];
+    if (gain) {
+        double ss = 0.0;
+        for (int d = 0; d < dh; ++d) ss += (double)x[d] * x[d];
+        double r = 1.0 / sqrt(ss / dh + (double)c->rms_eps);
+        for (int d = 0; d < dh; ++d) y[d] = (double)x[d] * r * gain[d];
+    } else {
+        for (int d = 0; d < dh; ++d) y[d] = x[d];
+    }
+    if (c->rope_theta > 0.f) {
+        for (int i = 0; i < h; ++i) {
+            double a = (double)pos * pow((double)c->rope_theta, -(double)i / h);
+            double cs = cos(a), sn = sin(a);
+            double u = y[i], v = y[i + h];
+            y[i] = u * cs - v * sn;
+            y[i + h] = v * cs + u * sn;
+        }
+    }
+    for (int d = 0; d < dh; ++d) x[d] = (float)y[d];
+}
+
+void orc_qk_norm_rope(const orc_cfg* c, const orc_weights* w, int layer, float* qkv, int M, int n_past) {
+    int dh = c->head_dim;
+    int Nqkv = (c->n_q_heads + 2 * c->n_kv_heads) * dh;
+    const float* gq = w->q_norm ? w->q_norm[layer] : NULL;
+    const float* gk = w->k_norm ? w->k_norm[layer] : NULL;
+    if (!gq && !gk && !(c->rope_theta > 0.f)) return;
+    for (int i = 0; i < M; ++i) {
+        float* row = qkv + (size_t)i * Nqkv;
+        for (int hq = 0; hq < c->n_q_heads; ++hq) orc_head_norm_rope(c, gq, row + (size_t)hq * dh, n_past + i);
+        for (int hk = 0; hk < c->n_kv_heads; ++hk)
+            orc_head_norm_rope(c, gk, row + (size_t)(c->n_q_heads + hk) * dh, n_past + i);
+    }
+}
+
+/* ------------------------------------------------------------------------ */
 /* One transformer block over M rows at positions n_past.. :                  */
 /*   xn = rmsnorm(x, attn_norm); [Q|K|V] = W_qkv q8(xn); K,V -> bf16 cache;   */
 /*   x += W_o q8(attention(Q));                                               */
@@ -582,6 +629,7 @@ static int orc_block_tree(const orc_cfg* c, const orc_weights* w, orc_kv* kv, in
 
     orc_rmsnorm(x_in, g_attn, M, H, c->rms_eps, xn);
     st |= orc_linear(w->w_qkv[layer], Nqkv, H, xn, M, qkv);
+    orc_qk_norm_rope(c, w, layer, qkv, M, n_past);
     for (int i = 0; i < M; ++i) {
         memcpy(qv + (size_t)i * nq, qkv + (size_t)i * Nqkv, sizeof(float) * nq);
         orc_kv_write_row(c, kv, layer, n_past + i, qkv + (size_t)i * Nqkv + nq,
@@ -755,6 +803,9 @@ int orc_verify_tree(const orc_cfg* c, const orc_weights* w, orc_kv* kv, const fl
                     int32_t* idx, float* logits) {
     uint64_t mask[ORC_TREE_MAX];
     int n_past = *kv->seq_len;
+    /* the rotary angle of a tree node follows its depth, not its row: not
+     * modelled here, so a rotary configuration is refused */
+    if (c->rope_theta > 0.f) return -1;
     res[0] = 0;
     res[1] = -1;
     res[3] = n_past;

@@ -34,6 +34,9 @@ typedef struct {
      * is one when swa_window > 0, swa_period > 0 and l % swa_period ==
      * swa_period - 1; its row at position p sees positions p-swa_window+1..p */
     int32_t swa_window, swa_period;
+    /* rotary position embedding of q and k ([8] §8.2 lists RoPE for the
+     * draft's attention): 0 = none, else the base theta */
+    float rope_theta;
 } orc_cfg;
 
 /* Host pointers to CANONICAL Q4_K matrices (see orc_q4k_* below). */
@@ -46,6 +49,10 @@ typedef struct {
     const float* const* ffn_norm;
     const float* final_norm;
     const uint8_t* w_head;
+    /* per-head RMSNorm of q and of k before RoPE ([8] §8.2 "QK-norms"):
+     * per-layer gains of head_dim floats; NULL = none */
+    const float* const* q_norm;
+    const float* const* k_norm;
 } orc_weights;
 
 /* Host paged KV model; same meaning as the library's cache. */
@@ -113,6 +120,12 @@ void orc_kv_compact(const orc_cfg* c, orc_kv* kv, int n_past, const int32_t* pat
 int  orc_verify_tree(const orc_cfg* c, const orc_weights* w, orc_kv* kv, const float* hidden,
                      const int32_t* tokens, const int32_t* parent, int n, int32_t* res, int32_t* path,
                      int32_t* idx, float* logits);
+
+/* QK-norm and RoPE of the M rows of a QKV projection output qkv [M][Nqkv]
+ * (q heads, then k heads, then v heads) at positions n_past.., in place: the
+ * q and k heads each normalised over head_dim (rms, eps, gain of the layer)
+ * when the layer has gains, then rotated by RoPE when rope_theta > 0 */
+void orc_qk_norm_rope(const orc_cfg* c, const orc_weights* w, int layer, float* qkv, int M, int n_past);
 
 /* the window of layer l: swa_window for a sliding-window layer, 0 otherwise */
 int orc_layer_window(const orc_cfg* c, int layer);

@@ -451,6 +451,76 @@ def test_swa_window_one_returns_own_value_and_two_is_a_pair_softmax():
 
 
 # ---------------------------------------------------------------------------
+# QK-norm and RoPE ([8] §8.2 lists both for the draft's attention)
+# ---------------------------------------------------------------------------
+def _rope_cfg(theta):
+    return oracle.Config(hidden=512, n_layers=1, n_q_heads=4, n_kv_heads=2, head_dim=128, ffn=256,
+                         vocab=64, rope_theta=theta)
+
+
+def _empty_w(q_norm=None, k_norm=None):
+    return oracle.Weights(w_qkv=[None], w_o=[None], w_gate_up=[None], w_down=[None],
+                          w_head=np.zeros(1, dtype=np.uint8), q_norm=q_norm, k_norm=k_norm)
+
+
+def test_rope_identity_at_position_zero_and_norm_preserving():
+    cfg, w = _rope_cfg(10000.0), _empty_w()
+    qkv = synth.normal((3, 8 * 128), 30, 1)
+    out = oracle.qk_norm_rope(cfg, w, 0, qkv[:1], 0)
+    assert np.array_equal(out, qkv[:1])                         # angle 0 everywhere
+    out = oracle.qk_norm_rope(cfg, w, 0, qkv, 1000)
+    heads_in = qkv.reshape(3, 8, 128).astype(np.float64)
+    heads_out = out.reshape(3, 8, 128).astype(np.float64)
+    assert np.allclose(np.linalg.norm(heads_out[:, :6], axis=2), np.linalg.norm(heads_in[:, :6], axis=2), rtol=1e-6)
+    assert np.array_equal(heads_out[:, 6:], heads_in[:, 6:].astype(np.float32))   # v untouched
+
+
+def test_rope_closed_form_and_relative_positions():
+    theta = 10000.0
+    cfg, w = _rope_cfg(theta), _empty_w()
+    for p in (1, 7, 123):
+        x = np.zeros((1, 8 * 128), dtype=np.float32)
+        x[0, 0] = 1.0                                           # pair (0, 64), frequency 1
+        x[0, 128 + 63] = 1.0                                    # q head 1, pair (63, 127)
+        y = oracle.qk_norm_rope(cfg, w, 0, x, p)[0]
+        assert abs(y[0] - math.cos(p)) < 1e-7 and abs(y[64] - math.sin(p)) < 1e-7
+        a = p * theta ** (-63.0 / 64.0)
+        assert abs(y[128 + 63] - math.cos(a)) < 1e-7 and abs(y[128 + 127] - math.sin(a)) < 1e-7
+    # the q.k score depends only on the distance of the two positions
+    q = synth.normal((1, 8 * 128), 31, 1)
+    k = synth.normal((1, 8 * 128), 31, 2)
+
+    def score(m, n):
+        qm = oracle.qk_norm_rope(cfg, w, 0, q, m)[0, :128].astype(np.float64)
+        kn = oracle.qk_norm_rope(cfg, w, 0, k, n)[0, 512:640].astype(np.float64)
+        return float(qm @ kn)
+    for m, n, s in ((5, 2, 100), (40, 9, 1000), (0, 0, 77)):
+        assert abs(score(m, n) - score(m + s, n + s)) < 2e-5 * max(1.0, abs(score(m, n)))
+    assert abs(score(5, 2) - score(5, 3)) > 1e-3
+
+
+def test_qk_norm_rms_and_scale_invariance():
+    cfg = oracle.Config(hidden=512, n_layers=1, n_q_heads=4, n_kv_heads=2, head_dim=128, ffn=256, vocab=64)
+    gq = (1.0 + 0.5 * synth.normal((128,), 32, 1)).astype(np.float32)
+    gk = np.full(128, 2.0, dtype=np.float32)
+    w = _empty_w(q_norm=[gq], k_norm=[gk])
+    x = synth.normal((2, 8 * 128), 32, 2) * 7.0
+    y = oracle.qk_norm_rope(cfg, w, 0, x, 0).reshape(2, 8, 128).astype(np.float64)
+    # each q head divided by its gain has rms 1; each k head has rms 2
+    assert np.allclose(np.sqrt(np.mean((y[:, :4] / gq) ** 2, axis=2)), 1.0, rtol=1e-6)
+    assert np.allclose(np.sqrt(np.mean(y[:, 4:6] ** 2, axis=2)), 2.0, rtol=1e-6)
+    assert np.array_equal(y[:, 6:].astype(np.float32), x.reshape(2, 8, 128)[:, 6:])
+    # scaling a head by s changes its output by s * sqrt(ms + eps) / sqrt(s^2 ms + eps): eps sits
+    # inside the root, beside the mean square, so a tiny head is not blown up to unit rms
+    s = np.float32(0.001)
+    y2 = oracle.qk_norm_rope(cfg, w, 0, x * s, 0).reshape(2, 8, 128).astype(np.float64)
+    ms = np.mean(x.reshape(2, 8, 128).astype(np.float64) ** 2, axis=2)[:, :6, None]
+    ratio = float(s) * np.sqrt(ms + 1e-6) / np.sqrt(float(s) ** 2 * ms + 1e-6)
+    assert ratio.min() < 0.995                                  # the case actually exercises eps
+    assert np.allclose(y2[:, :6], y[:, :6] * ratio, rtol=2e-5, atol=1e-7)
+
+
+# ---------------------------------------------------------------------------
 # whole-step invariants on a tiny model
 # ---------------------------------------------------------------------------
 def tiny_model(seed=0, n_layers=2, vocab=512):

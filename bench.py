@@ -277,7 +277,7 @@ def workload_config(cfg):
 # ---------------------------------------------------------------------------
 def kernel_source_sha():
     h = hashlib.sha256()
-    for f in ("gemm.cu", "common.cuh", "internal.h"):
+    for f in ("gemm.cu", "common.cuh", "gemm_plan.h"):
         h.update(open(os.path.join(ROOT, "speculative_decoding_exact_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 
@@ -1015,12 +1015,13 @@ def run_draft(args):
     6,656 (52 query heads, FFN 17,920), attention over a context of 2,112 rows
     (the 64-row sink plus the 2,048-row window of Ch. 8 §8.3) and the 16-row
     block, then the target's own LM head and the per-row argmax (the draft
-    borrows the target's head, Ch. 8 §8.2).  The pages' draft has 8 KV heads
-    of 128; the attention kernels take a whole number of query heads per KV
-    head and 52 is not a multiple of 8, so the draft blocks here have the
-    target's 4 KV heads.  Everything runs through the library's own kernels:
-    spec_gemm_q4k for fc, then a 5-layer verify step for the blocks, head and
-    argmax.  Reports ms per draft forward, per verify step, and per cycle."""
+    borrows the target's head, Ch. 8 §8.2).  The draft's k and v project
+    6,656 -> 1,024 (8 KV heads of 128, Ch. 8 §8.2); its query head count is
+    not given and is taken as 48 (6 per KV head, an attention width of
+    6,144).  q and k are QK-normed and rotated (RoPE, theta 1e6: the base is
+    not given either).  Everything runs through the library's own kernels: spec_gemm_q4k
+    for fc, then a 5-layer verify step for the blocks, head and argmax.
+    Reports ms per draft forward, per verify step, and per cycle."""
     import torch
 
     from speculative_decoding_exact_gb300 import abi, runtime, synth
@@ -1028,7 +1029,7 @@ def run_draft(args):
     mdl = setup_model(0)
     cfg, ctx, stream = mdl.cfg, mdl.ctx, mdl.stream
     H = cfg.hidden
-    dcfg = runtime.ModelConfig(**dict(synth.FULL, n_layers=5))
+    dcfg = runtime.ModelConfig(**dict(synth.FULL, n_layers=5, n_q_heads=48, n_kv_heads=8, rope_theta=1.0e6))
     dctx_len = 64 + 2048
     dmax = dctx_len + 64
     dctx = runtime.Context(dcfg, max_ctx=dmax, stream=stream)
@@ -1037,6 +1038,11 @@ def run_draft(args):
         for j, (name, N, K) in enumerate(dcfg.matrices()):
             getattr(dw, name).append(runtime.upload_tiled(dctx, synth.q4k_matrix(N, K, 9, 5000 + 10 * l + j), N, K))
     dw.w_head = mdl.dw.w_head                     # the target's LM head
+    # QK-norm gains per layer (random around 1)
+    dw.q_norm = [torch.from_numpy((1.0 + 0.1 * synth.normal((128,), 9, 5100 + l)).astype(np.float32)).cuda()
+                 for l in range(dcfg.n_layers)]
+    dw.k_norm = [torch.from_numpy((1.0 + 0.1 * synth.normal((128,), 9, 5200 + l)).astype(np.float32)).cuda()
+                 for l in range(dcfg.n_layers)]
     fc_N, fc_K = H, 5 * H
     Wfc = runtime.upload_tiled(dctx, synth.q4k_matrix(fc_N, fc_K, 9, 5999), fc_N, fc_K)
     pages = dmax // 16
@@ -1081,11 +1087,63 @@ def run_draft(args):
                       "draft_ms": ms_d, "verify_ms": ms_v, "cycle_ms": ms_c,
                       "draft_weight_bytes": dbytes, "draft_weight_gbs": dbytes / (ms_d * 1e-3) / 1e9,
                       "steps": args.steps, "warmup": args.warmup,
-                      "config": {"workload": "draft: fc Q4_K 33280->6656, 5 blocks hidden 6656 (52 q / 4 kv heads, "
-                                             "FFN 17920), context 64 sink + 2048 window, target LM head 131072, "
+                      "config": {"workload": "draft: fc Q4_K 33280->6656, 5 blocks hidden 6656 (48 q / 8 kv heads: "
+                                             "k/v 6656->1024, FFN 17920), context 64 sink + 2048 window, "
+                                             "target LM head 131072, "
                                              "16 rows; verify: the full 52-block step at context "
                                              f"{CTX}", "draft_weights": "random Q4_K"}}), flush=True)
     dctx.close()
+    ctx.close()
+
+
+def run_swa(args):
+    """Sliding-window layers (Ch. 8 §8.6 item 4) on the full model at context
+    --ctx: every second block is a window layer of --swa positions (its K/V in
+    a ring of W + 16 rows, attended by the same tensor-core kernel over the
+    window's chunks), the others attend the whole paged context.  Timed beside
+    the plain step at the same context, sharing the weights."""
+    import torch
+
+    from speculative_decoding_exact_gb300 import abi, runtime, synth
+
+    mdl = setup_model(0)
+    cfg, ctx, stream = mdl.cfg, mdl.ctx, mdl.stream
+
+    def plain():
+        abi.check("spec_verify_step", abi.spec_verify_step(ctx.h, mdl.ws, mdl.ks, mdl.hidden.data_ptr(),
+                                                           mdl.draft.data_ptr(), K_DRAFT, mdl.res.data_ptr()))
+        abi.check("spec_kv_rollback", abi.spec_kv_rollback(ctx.h, mdl.ks, CTX))
+
+    ms_plain = _time_steps(torch, stream, plain, args.warmup, args.steps)
+    scfg = runtime.ModelConfig(**dict(synth.FULL, swa_window=args.swa, swa_period=2))
+    sctx = runtime.Context(scfg, max_ctx=CTX + 64, stream=stream)
+    pages = (CTX + 64) // 16
+    skv = runtime.DeviceKV(scfg, pages, pages)
+    skv.reset(sctx)
+    skv.extend(sctx, CTX)
+    g = torch.Generator(device="cuda").manual_seed(4321)
+    with torch.cuda.stream(stream):
+        for l in range(scfg.n_layers):
+            if scfg.swa_index(l) < 0:
+                skv.pool[:, l].copy_(torch.randn(skv.pool[:, l].shape, generator=g, device="cuda").to(torch.bfloat16))
+        skv.swa_ring.copy_(torch.randn(skv.swa_ring.shape, generator=g, device="cuda").to(torch.bfloat16))
+    torch.cuda.synchronize()
+    sks = skv.struct()
+
+    def windowed():
+        abi.check("spec_verify_step", abi.spec_verify_step(sctx.h, mdl.ws, sks, mdl.hidden.data_ptr(),
+                                                           mdl.draft.data_ptr(), K_DRAFT, mdl.res.data_ptr()))
+        abi.check("spec_kv_rollback", abi.spec_kv_rollback(sctx.h, sks, CTX))
+
+    ms_swa = _time_steps(torch, stream, windowed, args.warmup, args.steps)
+    r = mdl.res.cpu().numpy()
+    assert r[2] == 0 and abi.spec_last_status(sctx.h) == 0, "sliding-window step status"
+    print(json.dumps({"metric": "verify steps/s with sliding-window layers (every second block)",
+                      "value": 1000.0 / ms_swa, "unit": "verify steps/s", "ms_per_step": ms_swa,
+                      "plain_steps_per_s": 1000.0 / ms_plain, "window": args.swa, "context": CTX,
+                      "window_layers": scfg.n_swa, "steps": args.steps, "warmup": args.warmup,
+                      "config": dict(workload_config(cfg), swa_window=args.swa, swa_period=2)}), flush=True)
+    sctx.close()
     ctx.close()
 
 
@@ -1222,6 +1280,8 @@ def main():
                     help="verify steps at context 2k/16k/32k x mean accepted length 1/4/12, with the fc timing")
     ap.add_argument("--draft", action="store_true",
                     help="time a DFlash-shaped draft forward (fc + 5 blocks + LM head) beside the verify step")
+    ap.add_argument("--swa", type=int, default=0,
+                    help="W: every second block a sliding-window layer of W positions, at context --ctx")
     ap.add_argument("--overlap", action="store_true",
                     help="split submit: the draft front projection on a second stream overlaps the step's suffix")
     ap.add_argument("--ctx", type=int, default=2048,
@@ -1248,6 +1308,9 @@ def main():
         return
     if args.overlap:
         run_overlap(args)
+        return
+    if args.swa:
+        run_swa(args)
         return
     if args.draft:
         run_draft(args)

@@ -103,10 +103,12 @@ extern "C" {
 #define SPEC_ST_DEVICE_WAIT   0x20 /* a bounded device wait (tensor core, bulk copy) gave up */
 #define SPEC_ST_BAD_TREE      0x40 /* a token tree's parent list is not a tree in topological order */
 
-/* Model geometry and workspace sizing.  H = n_q_heads*head_dim; H and ffn are
- * multiples of 256; n_q_heads is a multiple of n_kv_heads; head_dim = 128;
- * page_size = 16; max_rows <= 16 (k_max + 1).  max_ctx bounds the attention
- * workspace (positions per sequence). */
+/* Model geometry and workspace sizing.  H and ffn are multiples of 256; the
+ * attention width Q = n_q_heads*head_dim is a multiple of 256 too (usually
+ * Q = H; a draft block may differ, e.g. 48 query heads at H = 6656);
+ * n_q_heads is a multiple of n_kv_heads, at most 13 query heads per KV head;
+ * head_dim = 128; page_size = 16; max_rows <= 16 (k_max + 1).  max_ctx
+ * bounds the attention workspace (positions per sequence). */
 typedef struct spec_config {
     int32_t hidden;       /* H, e.g. 6656                                   */
     int32_t n_layers;     /* e.g. 52                                        */
@@ -122,18 +124,31 @@ typedef struct spec_config {
     /* Optional sliding-window layers (Ch. 8 §8.6 item 4: "SWA rings"):
      * with swa_window W > 0, layer l is a sliding-window layer when
      * l % swa_period == swa_period - 1 (1 <= swa_period <= n_layers); its row
-     * at position p sees positions p-W+1..p, and its K/V live in a ring of W
-     * rows (spec_kv.swa_ring) instead of the paged pool.  16 <= W <= max_ctx.
-     * swa_window = 0: no such layers (swa_period is ignored). */
+     * at position p sees positions p-W+1..p, and its K/V live in a ring of
+     * SPEC_SWA_RING_ROWS(W) rows (spec_kv.swa_ring) instead of the paged
+     * pool.  16 <= W <= max_ctx.  swa_window = 0: no such layers
+     * (swa_period is ignored). */
     int32_t swa_window;
     int32_t swa_period;
+    /* Optional rotary position embedding of q and k (Ch. 8 §8.2 lists RoPE
+     * for the draft's attention): with rope_theta > 0, element pair
+     * (i, i + head_dim/2) of every q and k head of the row at position p is
+     * rotated by the angle p * rope_theta^(-i / (head_dim/2)), i < head_dim/2
+     * ("rotate-half" pairing), after the optional QK-norm (spec_weights.q_norm,
+     * k_norm).  The cos/sin table is computed on the host in double precision
+     * at spec_verify_init for positions < max_ctx; a step that would place a
+     * row at max_ctx or beyond is refused (SPEC_ST_CTX_FULL), whether or not
+     * RoPE is on.  0 = no rotation.  Token trees (spec_verify_tree) refuse a
+     * context with rope_theta > 0 (SPEC_EINVAL): their rows' positions are
+     * their depths, which this table-per-row layout does not model. */
+    float   rope_theta;
 } spec_config;
 
 /* Target weights.  Each `const void* const*` is a HOST array of n_layers
  * DEVICE pointers to TILED Q4_K matrices:
  *   w_qkv[l]     N = (n_q_heads + 2*n_kv_heads)*head_dim, K = H; output
  *                columns [0, nq*dh) are Q (head-major), then K, then V.
- *   w_o[l]       N = H, K = H
+ *   w_o[l]       N = H, K = n_q_heads*head_dim
  *   w_gate_up[l] N = 2F, K = H; columns [0, F) gate, [F, 2F) up.
  *   w_down[l]    N = H, K = F
  *   w_head       N = V, K = H
@@ -148,6 +163,13 @@ typedef struct spec_weights {
     const float* const* ffn_norm;   /* host array of device pointers, or NULL */
     const float* final_norm;        /* device pointer or NULL                 */
     const void* w_head;
+    /* Optional QK-norm (Ch. 8 §8.2): per-layer device fp32 gains of length
+     * head_dim.  When q_norm (k_norm) is non-NULL and its entry for layer l is
+     * non-NULL, every q (k) head of layer l's QKV output is RMS-normalised over
+     * its head_dim elements, x * g / sqrt(mean(x^2) + rms_eps), before RoPE and
+     * before the K row enters the cache.  NULL = no QK-norm for that side. */
+    const float* const* q_norm;     /* host array of device pointers, or NULL */
+    const float* const* k_norm;     /* host array of device pointers, or NULL */
 } spec_weights;
 
 /* Paged KV cache (all pointers DEVICE, caller-owned).
@@ -162,19 +184,25 @@ typedef struct spec_weights {
  *
  * Sliding-window layers (spec_config.swa_window > 0; NULL pointers otherwise),
  * with n_swa = n_layers / swa_period such layers, s = l / swa_period:
- *   swa_ring   bf16 [n_swa][2 (K,V)][n_kv_heads][W][head_dim]: position t of
- *              layer s in slot t mod W (the window's rows; the caller lays
- *              down a prefilled context's last W positions there)
- *   swa_ckpt   bf16 [n_swa][2][n_kv_heads][16][head_dim]: the checkpoint, the
- *              ring rows that the last verify block overwrote
- *   swa_state  int32 [2]: {position of the last block (-1: no checkpoint),
- *              rows in it}; set by spec_kv_reset and the steps
- * A step saves the ring slots its M rows overwrite into the checkpoint before
- * writing them; every rollback (the step's own, or spec_kv_rollback) writes
- * the checkpoint rows of the positions past the new length back.  A rollback
- * below the last step's position, or after an extend, is refused
- * (SPEC_ST_ROLLBACK): the ring no longer holds those rows.  The paged pool's
- * slices of sliding-window layers are not used. */
+ *   swa_ring   bf16 [n_swa][2 (K,V)][n_kv_heads][R][head_dim], R =
+ *              SPEC_SWA_RING_ROWS(W): position t of layer s in slot t mod R
+ *              (the caller lays down a prefilled context's last W positions
+ *              there); 16-byte aligned
+ *   swa_state  int32 [2]: {position of the last step's block (-1: none),
+ *              rows in it}; set by spec_kv_reset, spec_kv_extend and the steps
+ * The ring holds W rows rounded up to a multiple of 16, plus 16 spare rows:
+ * a block of M <= 16 rows at positions n..n+M-1 overwrites only the slots of
+ * positions n-R..n+M-1-R, which precede every window that a row at position
+ * n or later sees.  So the rows that a rejected block would have displaced
+ * are still in the ring, and every rollback to a length >= n (the step's own
+ * accept, or spec_kv_rollback) is served by the metadata alone (Ch. 8 §8.6
+ * item 4 keeps those rows in a checkpoint; here the spare slots are that
+ * checkpoint).  A rollback below the last step's block, or after an extend,
+ * is refused (SPEC_ST_ROLLBACK): the ring may no longer hold the rows a
+ * window would need.  The paged pool's slices of sliding-window layers are
+ * not used. */
+#define SPEC_SWA_RING_ROWS(W) ((((W) + 15) / 16) * 16 + 16)
+
 typedef struct spec_kv {
     void*    pool;
     int32_t  num_pages;
@@ -184,7 +212,6 @@ typedef struct spec_kv {
     int32_t* free_stack;
     int32_t* free_top;
     void*    swa_ring;
-    void*    swa_ckpt;
     int32_t* swa_state;
 } spec_kv;
 
@@ -369,11 +396,12 @@ SPEC_API int spec_lm_head_argmax(spec_ctx* ctx, const void* w_head_tiled,
                         const float* final_norm, const float* x, int M,
                         int32_t* idx, float* logits);
 
-/* Verify attention of one (paged, not sliding-window) layer: M query rows at
- * positions seq_len-M .. seq_len-1 (their K/V rows already in the cache)
- * against all positions 0..p_i of row i.  q DEVICE fp32 [M][n_q_heads][head_dim]; out
- * DEVICE fp32 [M][n_q_heads*head_dim].  s = q.k/sqrt(head_dim), softmax over
- * the visible positions, o = sum p v; K and V read as bf16. */
+/* Verify attention of one layer: M query rows at positions seq_len-M ..
+ * seq_len-1 (their K/V rows already in the cache) against all positions
+ * 0..p_i of row i (a sliding-window layer: p_i-W+1..p_i, from its ring).
+ * q DEVICE fp32 [M][n_q_heads][head_dim]; out DEVICE fp32
+ * [M][n_q_heads*head_dim].  s = q.k/sqrt(head_dim), softmax over the visible
+ * positions, o = sum p v; K and V read as bf16. */
 SPEC_API int spec_attention(spec_ctx* ctx, const spec_kv* kv, int layer,
                    const float* q, int M, float* out);
 

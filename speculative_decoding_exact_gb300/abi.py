@@ -25,20 +25,20 @@ class spec_config(C.Structure):
                 ("n_kv_heads", C.c_int32), ("head_dim", C.c_int32), ("ffn", C.c_int32),
                 ("vocab", C.c_int32), ("max_rows", C.c_int32), ("page_size", C.c_int32),
                 ("max_ctx", C.c_int32), ("rms_eps", C.c_float), ("swa_window", C.c_int32),
-                ("swa_period", C.c_int32)]
+                ("swa_period", C.c_int32), ("rope_theta", C.c_float)]
 
 
 class spec_weights(C.Structure):
     _fields_ = [("w_qkv", C.c_void_p), ("w_o", C.c_void_p), ("w_gate_up", C.c_void_p),
                 ("w_down", C.c_void_p), ("attn_norm", C.c_void_p), ("ffn_norm", C.c_void_p),
-                ("final_norm", C.c_void_p), ("w_head", C.c_void_p)]
+                ("final_norm", C.c_void_p), ("w_head", C.c_void_p), ("q_norm", C.c_void_p),
+                ("k_norm", C.c_void_p)]
 
 
 class spec_kv(C.Structure):
     _fields_ = [("pool", C.c_void_p), ("num_pages", C.c_int32), ("max_seq_pages", C.c_int32),
                 ("page_table", C.c_void_p), ("seq_len", C.c_void_p), ("free_stack", C.c_void_p),
-                ("free_top", C.c_void_p), ("swa_ring", C.c_void_p), ("swa_ckpt", C.c_void_p),
-                ("swa_state", C.c_void_p)]
+                ("free_top", C.c_void_p), ("swa_ring", C.c_void_p), ("swa_state", C.c_void_p)]
 
 
 class spec_result(C.Structure):

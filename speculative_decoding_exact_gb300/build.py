@@ -14,8 +14,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libspecverify.so")
-SOURCES = ["gemm.cu", "glue.cu", "attn.cu", "sample.cu", "tree.cu", "swa.cu", "cudacore.cu", "api.cu", "noalloc.cu"]
-HEADERS = ["common.cuh", "internal.h", "quant.cuh", "kvmeta.cuh"]
+SOURCES = ["gemm.cu", "glue.cu", "attn.cu", "sample.cu", "tree.cu", "cudacore.cu", "api.cu", "noalloc.cu"]
+HEADERS = ["common.cuh", "internal.h", "gemm_plan.h", "quant.cuh", "kvmeta.cuh"]
 ROOT = os.path.dirname(HERE)
 PUBLIC_HEADER = os.path.join(ROOT, "include", "spec_verify.h")
 

@@ -12,7 +12,9 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <cmath>
 #include <new>
+#include <vector>
 
 #include "../../include/spec_verify.h"
 #include "common.cuh"
@@ -25,17 +27,17 @@ struct spec_ctx {
   cudaStream_t stream = nullptr;
   int num_sms = 0;
   GemmPlan p_qkv, p_o, p_gu, p_down, p_head;
-  AttnPlan attn;
+  AttnPlan attn;                 // paged layers: chunks over the whole context
+  AttnPlan attn_swa;             // sliding-window layers: chunks over the window
   size_t act_bytes = 0, pieces_floats = 0;
   uint8_t* act = nullptr;
   float* pieces = nullptr;
   float* resid = nullptr;        // [16][H]
-  float* q32 = nullptr;          // [16][H] fp32 queries of a sliding-window layer
+  float2* rope_cs = nullptr;     // [max_ctx][dh/2] (cos, sin) of the rotary angles
   int8_t* q8 = nullptr;          // plain int8 codes, d_a and sub-block sums of the
   float* da8 = nullptr;          // CUDA-core comparison GEMM
   int32_t* a8 = nullptr;
   int kmax = 0;
-  float* swa_part = nullptr;     // sliding-window attention partials
   uint8_t* qtile = nullptr;      // attention query tiles, 64 KB per (kv head, tile)
   float* attn_part = nullptr;
   float* head_val = nullptr;     // [nparts][16]
@@ -110,10 +112,11 @@ KvView view_of(const spec_ctx* c, const spec_kv* kv) {
   v.head_dim = c->cfg.head_dim;
   v.page_size = c->cfg.page_size;
   v.swa_ring = static_cast<uint16_t*>(kv->swa_ring);
-  v.swa_ckpt = static_cast<uint16_t*>(kv->swa_ckpt);
   v.swa_state = kv->swa_state;
   v.swa_window = c->cfg.swa_window;
   v.swa_period = c->cfg.swa_period;
+  v.swa_rows = c->cfg.swa_window > 0 ? swa_ring_rows(c->cfg.swa_window) : 0;
+  v.max_ctx = c->cfg.max_ctx;
   return v;
 }
 
@@ -132,8 +135,8 @@ int check_kv(const spec_kv* kv) {
 
 int check_kv_swa(const spec_ctx* c, const spec_kv* kv) {
   if (!has_swa(c->cfg)) return SPEC_OK;
-  if (!kv->swa_ring || !kv->swa_ckpt || !kv->swa_state) return SPEC_ENULL;
-  if (!aligned(kv->swa_ring) || !aligned(kv->swa_ckpt)) return SPEC_EALIGN;
+  if (!kv->swa_ring || !kv->swa_state) return SPEC_ENULL;
+  if (!aligned(kv->swa_ring)) return SPEC_EALIGN;
   return SPEC_OK;
 }
 
@@ -144,7 +147,9 @@ int check_cfg(const spec_config* c) {
   if (c->head_dim != 128 || c->page_size != 16) return SPEC_EINVAL;
   if (c->n_q_heads <= 0 || c->n_kv_heads <= 0 || c->n_q_heads % c->n_kv_heads) return SPEC_EINVAL;
   if (c->n_q_heads / c->n_kv_heads > 13) return SPEC_EINVAL;
-  if (c->n_q_heads * c->head_dim != c->hidden) return SPEC_EINVAL;
+  // the attention output (n_q_heads * head_dim wide, the O projection's K)
+  // is quantised in 256-blocks; it need not equal the hidden width
+  if ((c->n_q_heads * c->head_dim) % 256 || c->n_q_heads * c->head_dim > 64 * 256) return SPEC_EINVAL;
   if (c->n_layers <= 0 || c->vocab <= 0 || c->vocab % 16) return SPEC_EINVAL;
   if (c->max_rows < 1 || c->max_rows > 16) return SPEC_EINVAL;
   if (c->max_ctx < c->max_rows) return SPEC_EINVAL;
@@ -153,6 +158,7 @@ int check_cfg(const spec_config* c) {
   if (c->swa_window > 0 &&
       (c->swa_window < 16 || c->swa_window > c->max_ctx || c->swa_period < 1 || c->swa_period > c->n_layers))
     return SPEC_EINVAL;
+  if (!(c->rope_theta >= 0.f) || !(c->rope_theta < INFINITY)) return SPEC_EINVAL;
   return SPEC_OK;
 }
 
@@ -202,7 +208,8 @@ int spec_verify_init(const spec_config* cfg, void* cuda_stream, spec_ctx** out) 
   const int H = cfg->hidden, F = cfg->ffn, V = cfg->vocab;
   const int nqkv = (cfg->n_q_heads + 2 * cfg->n_kv_heads) * cfg->head_dim;
   c->p_qkv = make_gemm_plan(nqkv, H, sms);
-  c->p_o = make_gemm_plan(H, H, sms);
+  const int QW = cfg->n_q_heads * cfg->head_dim;   // attention output width
+  c->p_o = make_gemm_plan(H, QW, sms);
   c->p_gu = make_gemm_plan(2 * F, H, sms);
   c->p_down = make_gemm_plan(H, F, sms);
   c->p_head = make_gemm_plan(V, H, sms);
@@ -217,11 +224,16 @@ int spec_verify_init(const spec_config* cfg, void* cuda_stream, spec_ctx** out) 
   c->p_down.pre_stages = kPreDown;
   c->p_head.pre_stages = kPreHead;
   c->attn = make_attn_plan(cfg->n_q_heads, cfg->n_kv_heads, cfg->head_dim, cfg->max_ctx);
+  // a window layer's block sees at most W + 15 keys, from the page of its
+  // first one: W + 32 covers them
+  if (has_swa(*cfg))
+    c->attn_swa = make_attn_plan(cfg->n_q_heads, cfg->n_kv_heads, cfg->head_dim, cfg->swa_window + 32);
   size_t pf = 0;
   for (const GemmPlan* p : {&c->p_qkv, &c->p_o, &c->p_gu, &c->p_down, &c->p_head})
     if (pieces_need(*p) > pf) pf = pieces_need(*p);
   c->pieces_floats = pf;
   int kmax = H > F ? H : F;
+  if (QW > kmax) kmax = QW;
   if (5 * H > kmax) kmax = 5 * H;   // a draft front projection over 5 concatenated hidden rows
   c->act_bytes = (size_t)(kmax / 256) * kActSBBytes;
   c->kmax = kmax;
@@ -233,12 +245,12 @@ int spec_verify_init(const spec_config* cfg, void* cuda_stream, spec_ctx** out) 
   rc |= dalloc(&c->q8, (size_t)16 * kmax);
   rc |= dalloc(&c->da8, (size_t)16 * (kmax / 256));
   rc |= dalloc(&c->a8, (size_t)16 * (kmax / 32));
-  if (has_swa(*cfg)) {
-    rc |= dalloc(&c->q32, (size_t)16 * H);
-    rc |= dalloc(&c->swa_part, swa_partial_floats(cfg->swa_window, cfg->n_q_heads));
-  }
   rc |= dalloc(&c->qtile, qtile_bytes(c->attn));
-  rc |= dalloc(&c->attn_part, attn_partial_floats(c->attn, 16));
+  {
+    size_t parts = attn_partial_floats(c->attn, 16);
+    if (has_swa(*cfg) && attn_partial_floats(c->attn_swa, 16) > parts) parts = attn_partial_floats(c->attn_swa, 16);
+    rc |= dalloc(&c->attn_part, parts);
+  }
   rc |= dalloc(&c->head_val, (size_t)c->head_parts * 16);
   rc |= dalloc(&c->head_idx, (size_t)c->head_parts * 16);
   rc |= dalloc(&c->status, 4);
@@ -252,6 +264,7 @@ int spec_verify_init(const spec_config* cfg, void* cuda_stream, spec_ctx** out) 
   rc |= dalloc(&c->hidden_dev, (size_t)16 * H);
   rc |= dalloc(&c->draft_dev, 16);
   rc |= dalloc(&c->res_dev, 1);
+  if (cfg->rope_theta > 0.f) rc |= dalloc(&c->rope_cs, (size_t)cfg->max_ctx * (cfg->head_dim / 2));
   if (rc != SPEC_OK) {
     spec_verify_destroy(c);
     return SPEC_ENOMEM;
@@ -259,6 +272,23 @@ int spec_verify_init(const spec_config* cfg, void* cuda_stream, spec_ctx** out) 
   if (gemm_init_attributes() != cudaSuccess) {
     spec_verify_destroy(c);
     return SPEC_ECUDA;
+  }
+  if (c->rope_cs) {
+    // the rotary table: angle p * theta^(-i/h) and its cosine and sine in
+    // double precision, rounded to float once
+    const int h = cfg->head_dim / 2;
+    std::vector<float2> cs((size_t)cfg->max_ctx * h);
+    for (int i = 0; i < h; ++i) {
+      const double f = std::pow((double)cfg->rope_theta, -(double)i / h);
+      for (int p = 0; p < cfg->max_ctx; ++p) {
+        const double a = (double)p * f;
+        cs[(size_t)p * h + i] = make_float2((float)std::cos(a), (float)std::sin(a));
+      }
+    }
+    if (cudaMemcpy(c->rope_cs, cs.data(), sizeof(float2) * cs.size(), cudaMemcpyHostToDevice) != cudaSuccess) {
+      spec_verify_destroy(c);
+      return SPEC_ECUDA;
+    }
   }
   if (cudaMemsetAsync(c->status, 0, 16, c->stream) != cudaSuccess ||
       cudaMemsetAsync(c->act, 0, c->act_bytes, c->stream) != cudaSuccess ||
@@ -282,8 +312,7 @@ void spec_verify_destroy(spec_ctx* c) {
   cudaFree(c->q8);
   cudaFree(c->da8);
   cudaFree(c->a8);
-  cudaFree(c->q32);
-  cudaFree(c->swa_part);
+  cudaFree(c->rope_cs);
   cudaFree(c->qtile);
   cudaFree(c->logits_ws);
   cudaFree(c->sstats);
@@ -436,13 +465,18 @@ int spec_attention(spec_ctx* c, const spec_kv* kv, int layer, const float* q, in
   int rc = check_kv(kv);
   if (rc) return rc;
   if (M < 1 || M > 16 || layer < 0 || layer >= c->cfg.n_layers) return SPEC_EINVAL;
-  if (swa_index(view_of(c, kv), layer) >= 0) return SPEC_EINVAL;   // a ring layer: see the step
-  if (kv->max_seq_pages * c->cfg.page_size > c->attn.max_chunks * c->attn.chunk)
+  const bool ring = swa_index(view_of(c, kv), layer) >= 0;
+  if (ring) {
+    rc = check_kv_swa(c, kv);
+    if (rc) return rc;
+  } else if (kv->max_seq_pages * c->cfg.page_size > c->attn.max_chunks * c->attn.chunk) {
     return SPEC_ECAPACITY;   // attention workspace must cover every position the cache can hold
+  }
   if (!aligned(q) || !aligned(out)) return SPEC_EALIGN;
+  const AttnPlan& ap = ring ? c->attn_swa : c->attn;
   SPEC_TRY(cudaMemsetAsync(c->status, 0, 4, c->stream));
-  SPEC_TRY(launch_q_to_tile(q, M, c->attn, c->qtile, c->stream, false));
-  SPEC_TRY(launch_attention(c->attn, view_of(c, kv), layer, c->qtile, M, c->attn_part, out, nullptr,
+  SPEC_TRY(launch_q_to_tile(q, M, ap, c->qtile, c->stream, false));
+  SPEC_TRY(launch_attention(ap, view_of(c, kv), layer, c->qtile, M, c->attn_part, out, nullptr,
                             c->status, c->stream, false));
   return SPEC_OK;
 }
@@ -459,9 +493,8 @@ int spec_accept(spec_ctx* c, const int32_t* idx, const int32_t* draft, int k, sp
   }
   KvView v;
   if (kv) v = view_of(c, kv);
-  SPEC_TRY(launch_accept(idx, nullptr, nullptr, 0, draft, k, c->cfg.vocab, kv ? &v : nullptr,
-                         nullptr, c->status, reinterpret_cast<int32_t*>(res), nullptr, c->stream, false));
-  return kv ? cuda_code(launch_swa_restore(v, c->stream, false)) : SPEC_OK;
+  return cuda_code(launch_accept(idx, nullptr, nullptr, 0, draft, k, c->cfg.vocab, kv ? &v : nullptr, nullptr,
+                                c->status, reinterpret_cast<int32_t*>(res), nullptr, c->stream, false));
 }
 
 int spec_kv_reset(spec_ctx* c, spec_kv* kv) {
@@ -491,8 +524,7 @@ int spec_kv_rollback(spec_ctx* c, spec_kv* kv, int32_t new_len) {
   if (new_len < 0) return SPEC_EINVAL;
   rc = check_kv_swa(c, kv);
   if (rc) return rc;
-  SPEC_TRY(launch_kv_rollback(view_of(c, kv), new_len, c->status, c->stream));
-  return cuda_code(launch_swa_restore(view_of(c, kv), c->stream, false));
+  return cuda_code(launch_kv_rollback(view_of(c, kv), new_len, c->status, c->stream));
 }
 
 // ---------------------------------------------------------------------------
@@ -507,6 +539,8 @@ static int check_weights(const spec_ctx* c, const spec_weights* w) {
       return SPEC_EALIGN;
     if (w->attn_norm && w->attn_norm[l] && !aligned(w->attn_norm[l])) return SPEC_EALIGN;
     if (w->ffn_norm && w->ffn_norm[l] && !aligned(w->ffn_norm[l])) return SPEC_EALIGN;
+    if (w->q_norm && w->q_norm[l] && !aligned(w->q_norm[l])) return SPEC_EALIGN;
+    if (w->k_norm && w->k_norm[l] && !aligned(w->k_norm[l])) return SPEC_EALIGN;
   }
   if (!aligned(w->w_head) || (w->final_norm && !aligned(w->final_norm))) return SPEC_EALIGN;
   return SPEC_OK;
@@ -552,6 +586,15 @@ static int enqueue_step(spec_ctx* c, const spec_weights* w, spec_kv* kv, const f
   };
   auto attn_gamma = [&](int l) -> const float* { return w->attn_norm ? w->attn_norm[l] : nullptr; };
   auto ffn_gamma = [&](int l) -> const float* { return w->ffn_norm ? w->ffn_norm[l] : nullptr; };
+  auto qk_of = [&](int l) {
+    QkTransform t;
+    t.gq = w->q_norm ? w->q_norm[l] : nullptr;
+    t.gk = w->k_norm ? w->k_norm[l] : nullptr;
+    t.cs = c->rope_cs;
+    t.cs_len = g.max_ctx;
+    t.eps = g.rms_eps;
+    return t;
+  };
   float* tap_resid = taps ? taps->resid : nullptr;
 
   // A token tree of more than max_rows nodes runs in passes of up to
@@ -561,9 +604,6 @@ static int enqueue_step(spec_ctx* c, const spec_weights* w, spec_kv* kv, const f
   const int npass = (M + P - 1) / P;
   SPEC_TRY(launch_kv_reserve(kvv, M, 0, ta ? ta->tokens + 1 : draft, k, g.vocab, c->status, c->step_state, st,
                              true, ta ? ta->parent : nullptr, ta ? c->tree_mask : nullptr)); ++n;
-  if (has_swa(g)) {
-    SPEC_TRY(launch_swa_checkpoint(kvv, M, c->step_state, c->status, st, true)); ++n;
-  }
   for (int pass = 0; pass < npass; ++pass) {
     const int r0 = pass * P, Mp = (M - r0 < P) ? M - r0 : P;
     const size_t rows_bytes = sizeof(float) * (size_t)Mp * H;
@@ -577,18 +617,12 @@ static int enqueue_step(spec_ctx* c, const spec_weights* w, spec_kv* kv, const f
                                      c->act, nullptr, c->status, st, true)); ++n;
     for (int l = 0; l < g.n_layers; ++l) {
       SPEC_TRY(gemm(c->p_qkv, w->w_qkv[l])); ++n;
-      if (swa_index(kvv, l) >= 0) {
-        // sliding-window layer: K/V into the ring, attention over the window
-        SPEC_TRY(launch_qkv_post(c->p_qkv, c->pieces, Mp, g.n_q_heads, g.n_kv_heads, g.head_dim, kvv, l,
-                                  c->qtile, c->attn.tiles, c->status, st, true, false, c->q32)); ++n;
-        SPEC_TRY(launch_swa_attention(kvv, l, c->q32, Mp, g.n_q_heads, c->swa_part, nullptr, c->act,
-                                      c->status, st, true)); n += 2;
-      } else {
-        SPEC_TRY(launch_qkv_post(c->p_qkv, c->pieces, Mp, g.n_q_heads, g.n_kv_heads, g.head_dim, kvv, l,
-                                  c->qtile, c->attn.tiles, c->status, st, true, c->attn.early)); ++n;
-        SPEC_TRY(launch_attention(c->attn, kvv, l, c->qtile, Mp, c->attn_part, nullptr, c->act, c->status,
-                                  st, true, tmask, ta ? c->step_state : nullptr)); n += 2;
-      }
+      // a sliding-window layer: K/V into its ring, attention over the window
+      const AttnPlan& ap = swa_index(kvv, l) >= 0 ? c->attn_swa : c->attn;
+      SPEC_TRY(launch_qkv_post(c->p_qkv, c->pieces, Mp, g.n_q_heads, g.n_kv_heads, g.head_dim, kvv, l, c->qtile,
+                                ap.tiles, c->status, st, true, ap.early, qk_of(l))); ++n;
+      SPEC_TRY(launch_attention(ap, kvv, l, c->qtile, Mp, c->attn_part, nullptr, c->act, c->status, st, true,
+                                tmask, ta ? c->step_state : nullptr)); n += 2;
       SPEC_TRY(gemm(c->p_o, w->w_o[l])); ++n;
       SPEC_TRY(launch_resid_norm_quant(&c->p_o, c->pieces, c->resid, c->resid, ffn_gamma(l), g.rms_eps,
                                        Mp, H, c->act, nullptr, c->status, st, true)); ++n;
@@ -657,10 +691,6 @@ static int enqueue_step(spec_ctx* c, const spec_weights* w, spec_kv* kv, const f
                            c->step_state, c->status, reinterpret_cast<int32_t*>(res),
                            taps ? taps->argmax : nullptr, st, true)); ++n;
   }
-  if (has_swa(g)) {
-    // the ring rows of the rejected positions come back from the checkpoint
-    SPEC_TRY(launch_swa_restore(kvv, st, true)); ++n;
-  }
   c->last_launches = n;
   return SPEC_OK;
 }
@@ -696,7 +726,6 @@ static uint64_t step_key(const spec_ctx* c, const spec_weights* w, const spec_kv
   h = mix(h, (uint64_t)kv->num_pages);
   h = mix(h, (uint64_t)kv->max_seq_pages);
   h = mix(h, P(kv->swa_ring));
-  h = mix(h, P(kv->swa_ckpt));
   h = mix(h, P(kv->swa_state));
   for (int l = 0; l < c->cfg.n_layers; ++l) {
     h = mix(h, P(w->w_qkv[l]));
@@ -705,6 +734,8 @@ static uint64_t step_key(const spec_ctx* c, const spec_weights* w, const spec_kv
     h = mix(h, P(w->w_down[l]));
     h = mix(h, w->attn_norm ? P(w->attn_norm[l]) : 1);
     h = mix(h, w->ffn_norm ? P(w->ffn_norm[l]) : 2);
+    h = mix(h, w->q_norm ? P(w->q_norm[l]) : 3);
+    h = mix(h, w->k_norm ? P(w->k_norm[l]) : 4);
   }
   h = mix(h, P(w->final_norm));
   h = mix(h, P(w->w_head));
@@ -725,6 +756,7 @@ static int run_step(spec_ctx* c, const spec_weights* w, spec_kv* kv, const float
   rc = check_kv_swa(c, kv);
   if (rc) return rc;
   if (ta && has_swa(c->cfg)) return SPEC_EINVAL;   // K/V moves of a tree path: paged layers only
+  if (ta && c->cfg.rope_theta > 0.f) return SPEC_EINVAL;   // a tree row's position is its depth
   rc = check_weights(c, w);
   if (rc) return rc;
   if (!aligned(hidden)) return SPEC_EALIGN;
@@ -850,10 +882,9 @@ int spec_sample_accept(spec_ctx* c, const float* logits, const float* q, const i
   }
   KvView v;
   if (kv) v = view_of(c, kv);
-  SPEC_TRY(launch_sample_accept(logits, q, draft, k, c->cfg.vocab, c->sstats, c->sscratch, mt,
-                                kv ? &v : nullptr, nullptr, c->status, reinterpret_cast<int32_t*>(res),
-                                c->stream, false));
-  return kv ? cuda_code(launch_swa_restore(v, c->stream, false)) : SPEC_OK;
+  return cuda_code(launch_sample_accept(logits, q, draft, k, c->cfg.vocab, c->sstats, c->sscratch, mt,
+                                       kv ? &v : nullptr, nullptr, c->status, reinterpret_cast<int32_t*>(res),
+                                       c->stream, false));
 }
 
 int spec_verify_step_host(spec_ctx* c, const spec_weights* w, spec_kv* kv, const float* hidden_host,

@@ -130,6 +130,34 @@ static cudaError_t make_kv_tmap(const KvView& kv, CUtensorMap* map) {
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// The sliding-window rings [n_swa][K, V][n_kv][R][128] bf16 as one 2-D tensor
+// of 256-byte rows (row = ((s*2 + kv)*n_kv + head)*R + slot); the same boxes.
+// R is a multiple of 16, so a 16-row box never straddles two rings.
+static cudaError_t make_ring_tmap(const KvView& kv, CUtensorMap* map) {
+  using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+  static EncodeFn encode = nullptr;
+  if (!encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess) return e;
+    if (q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
+    encode = reinterpret_cast<EncodeFn>(fn);
+  }
+  const unsigned long long rows = (unsigned long long)swa_layers(kv) * 2 * kv.n_kv * kv.swa_rows;
+  if (rows == 0 || rows >= (1ull << 31) || kv.swa_rows % 16) return cudaErrorInvalidValue;
+  const cuuint64_t dims[2] = {128, rows};
+  const cuuint64_t strides[1] = {256};
+  const cuuint32_t box[2] = {64, 16};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kv.swa_ring, dims, strides, box, estr,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 // 2^x (PTX ex2.approx: relative error about 2^-22; 2^-inf = 0)
 SPEC_DEV float exp2_approx(float x) {
   float y;
@@ -217,7 +245,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 1)
 attn_partial_kernel(const uint8_t* __restrict__ qtile, int M, int nq, int nkv, int group, int tiles,
                     int chunk_keys, KvView kv, const __grid_constant__ CUtensorMap kvmap, int layer,
                     const uint64_t* __restrict__ tree_mask, const int32_t* __restrict__ tree_base,
-                    float* __restrict__ part, int32_t* status, int early) {
+                    float* __restrict__ part, int32_t* status, int early, int ring_s) {
   extern __shared__ __align__(128) uint8_t dsm[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm) + 1023) & ~(uintptr_t)1023);
   uint8_t* qs = sm;                                    // Q tile: hi [0, 32K), lo [32K, 64K)
@@ -229,11 +257,13 @@ attn_partial_kernel(const uint8_t* __restrict__ qtile, int M, int nq, int nkv, i
 
   __shared__ float rowmax[2][2][128];       // [sub-chunk parity][column half][row]
   __shared__ float lpart[2][128];           // [column half][row]
-  __shared__ int proceed, len_sh, tb_sh;
+  __shared__ int proceed, len_sh, tb_sh, key0_sh;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int chunk = blockIdx.x, kvh = blockIdx.y, tile = blockIdx.z;
-  const int key0 = chunk * chunk_keys;
+  // a sliding-window layer (ring_s >= 0) reads ring ring_s; its chunks start
+  // at the page of the first key any block row sees
+  const bool ring = ring_s >= 0;
   // barriers and TMEM do not depend on the previous kernel
   if (warp == 0) tmem_alloc(&tmem_slot, kTmCols);
   if (tid == 0) {
@@ -266,13 +296,16 @@ attn_partial_kernel(const uint8_t* __restrict__ qtile, int M, int nq, int nkv, i
   {
     const int32_t st = __ldcg(status);
     const int len0 = __ldcg(kv.seq_len);
-    for (int i = tid; i < chunk_keys / 16; i += blockDim.x) {
-      const int lp = key0 / 16 + i;
-      pg[i] = lp < kv.max_seq_pages ? __ldcg(kv.page_table + lp) : -1;
-    }
+    const int k0 = (ring ? (max(0, len0 - M - kv.swa_window + 1) & ~15) : 0) + chunk * chunk_keys;
+    if (!ring)
+      for (int i = tid; i < chunk_keys / 16; i += blockDim.x) {
+        const int lp = k0 / 16 + i;
+        pg[i] = lp < kv.max_seq_pages ? __ldcg(kv.page_table + lp) : -1;
+      }
     if (tid == 0) {
-      proceed = !(st & kStepAbort) && key0 < len0;
+      proceed = !(st & kStepAbort) && k0 < len0;
       len_sh = len0;
+      key0_sh = k0;
       tb_sh = kTree ? __ldcg(tree_base) : 0;
     }
   }
@@ -282,6 +315,9 @@ attn_partial_kernel(const uint8_t* __restrict__ qtile, int M, int nq, int nkv, i
   const uint32_t tmem = tmem_slot;
   const int len = len_sh;                  // block appended: n_past + M
   const int n_past = len - M;
+  const int key0 = key0_sh;
+  // sliding window: row r sees keys >= wlo + r; keys below wlo no row sees
+  const int wlo = ring ? n_past - kv.swa_window + 1 : 0;
   // token tree: the tree's first position (node 0); a tree of more than 16
   // nodes runs in passes of up to 16 rows, and n_past is this pass's first
   // row, so earlier passes' nodes lie between the two
@@ -294,8 +330,10 @@ attn_partial_kernel(const uint8_t* __restrict__ qtile, int M, int nq, int nkv, i
   int npre = 0;
   while (early && npre < min(nsub, kKvBufs) && key0 + (npre + 1) * kChunk <= n_past) ++npre;
 
-  // page id of the page holding pos0 (a multiple of 16), -1 past len or out of range
+  // page id of the page holding pos0 (a multiple of 16), -1 past len or out
+  // of range; a ring's page is its 16 slots from (pos0 mod R)
   auto page_of = [&](int pos0) -> int {
+    if (ring) return pos0 < len ? (pos0 >> 4) % (kv.swa_rows >> 4) : -1;
     const int page = pos0 < len ? pg[(pos0 - key0) >> 4] : -1;
     return (page >= 0 && page < kv.num_pages) ? page : -1;
   };
@@ -314,7 +352,8 @@ attn_partial_kernel(const uint8_t* __restrict__ qtile, int M, int nq, int nkv, i
       mbar_arrive_expect_tx(&v_full[b], kops * 2048u);   // a page's K and V come together
     }
     if (go) {
-      const int y = (((page * kv.n_layers + layer) * 2 + which) * kv.n_kv + kvh) * 16;
+      const int y = ring ? ((ring_s * 2 + which) * kv.n_kv + kvh) * kv.swa_rows + 16 * page
+                         : (((page * kv.n_layers + layer) * 2 + which) * kv.n_kv + kvh) * 16;
       tma_load_2d(buf + which * 2 * kHalfBytes + half * kHalfBytes + pp * 2048, &kvmap, 64 * half, y,
                   which == 0 ? &k_full[b] : &v_full[b]);
     }
@@ -456,7 +495,7 @@ attn_partial_kernel(const uint8_t* __restrict__ qtile, int M, int nq, int nkv, i
 #pragma unroll
       for (int pp = 0; pp < 4; ++pp) pok[pp] = page_of(ks0 + 16 * pp) >= 0;
       const bool allpages = pok[0] && pok[1] && pok[2] && pok[3];
-      const bool full = ks0 + kChunk - 1 <= tb && allpages;
+      const bool full = ks0 + kChunk - 1 <= tb && allpages && (!ring || ks0 >= wlo + M - 1);
       // scores in base-2 units, masked -> -inf
       float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
       if (full && live) {
@@ -470,6 +509,7 @@ attn_partial_kernel(const uint8_t* __restrict__ qtile, int M, int nq, int nkv, i
         // the row is live), or when it is node rel = base + c with bit rel of
         // tm set, and its page is valid: bit c of vm
         const int lim = live ? n_past + row - ks0 : -1;
+        const int lim_lo = ring ? wlo + row - ks0 : -(1 << 30);   // the window's first key
         uint32_t vm;
         if (kTree) {
           const int base = ks0 + 32 * h - tb;
@@ -484,7 +524,7 @@ attn_partial_kernel(const uint8_t* __restrict__ qtile, int M, int nq, int nkv, i
         for (int c = 0; c < 32; ++c) {
           const int key = 32 * h + c;
           // causal: key ks0 + key is visible to row when key <= n_past + row - ks0
-          const bool vis = kTree ? ((vm >> c) & 1u) != 0 : (key <= lim && pok[key >> 4]);
+          const bool vis = kTree ? ((vm >> c) & 1u) != 0 : (key <= lim && key >= lim_lo && pok[key >> 4]);
           s[c] = vis ? s[c] * c2 : -INFINITY;
           mx4[c & 3] = fmaxf(mx4[c & 3], s[c]);
         }
@@ -531,9 +571,9 @@ attn_partial_kernel(const uint8_t* __restrict__ qtile, int M, int nq, int nkv, i
           }
         }
       }
-      // V rows of keys that must read as zero (past len, bad page id), once
-      // the V copies of this buffer have landed
-      if (ks0 + kChunk > len || !allpages) {
+      // V rows of keys that must read as zero (past len, bad page id, below
+      // every row's window), once the V copies of this buffer have landed
+      if (ks0 + kChunk > len || !allpages || (ring && ks0 < wlo)) {
         if (!__all_sync(0xffffffffu, mbar_wait_ns(&v_full[b], (sc / kKvBufs) & 1, kAttnWaitNs))) {
           ok = false;
           continue;                                     // carried to the next barrier
@@ -542,7 +582,7 @@ attn_partial_kernel(const uint8_t* __restrict__ qtile, int M, int nq, int nkv, i
 #pragma unroll 1
         for (int i = 128 * h + r; i < kChunk * 16; i += kRowThreads) {   // (key, d half, 16-byte chunk)
           const int c = i >> 4, half = (i >> 3) & 1, ch = i & 7;
-          if (ks0 + c < len && pok[c >> 4]) continue;
+          if (ks0 + c < len && pok[c >> 4] && (!ring || ks0 + c >= wlo)) continue;
           *reinterpret_cast<uint4*>(vb + half * kHalfBytes + c * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
         }
         fence_proxy_async();
@@ -608,7 +648,7 @@ constexpr int kMergeBatch = 24;
 
 __global__ void __launch_bounds__(256)
 attn_merge_kernel(const float* __restrict__ part, int M, int nq, int max_chunks, int chunk_keys,
-                  const int32_t* seq_len, float* __restrict__ out, uint8_t* act, int32_t* status) {
+                  const int32_t* seq_len, float* __restrict__ out, uint8_t* act, int32_t* status, int window) {
   pdl_trigger();
   pdl_wait();
   extern __shared__ float msh[];          // [2][max_chunks] weights
@@ -634,7 +674,9 @@ attn_merge_kernel(const float* __restrict__ part, int M, int nq, int max_chunks,
   }
   const bool valid = row < M && !(*status & kStepAbort);
   const int n_past = *seq_len - M;
-  const int nchunks = valid ? min((n_past + row) / chunk_keys + 1, max_chunks) : 0;
+  // a sliding-window layer's chunks start at its window's first page
+  const int kbase = window > 0 ? (max(0, n_past - window + 1) & ~15) : 0;
+  const int nchunks = valid ? min((n_past + row - kbase) / chunk_keys + 1, max_chunks) : 0;
   if (warp < 2) {
     const float* st = part + (((size_t)(2 * b + warp)) * 16 + row) * kPartStride + 128;
     auto ml_of = [&](int c, int t) -> float2 {
@@ -685,8 +727,10 @@ cudaError_t launch_attention(const AttnPlan& a, const KvView& kv, int layer, con
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  const int ring_s = swa_index(kv, layer);
+  if (ring_s >= 0 && tree_mask) return cudaErrorInvalidValue;   // trees: paged layers only
   alignas(64) CUtensorMap kvmap;
-  cudaError_t em = make_kv_tmap(kv, &kvmap);
+  cudaError_t em = ring_s >= 0 ? make_ring_tmap(kv, &kvmap) : make_kv_tmap(kv, &kvmap);
   if (em != cudaSuccess) return em;
   const size_t smem = attn_smem_bytes(a.chunk);
   // the causal kernel and the token-tree kernel (which tests every block key
@@ -706,7 +750,8 @@ cudaError_t launch_attention(const AttnPlan& a, const KvView& kv, int layer, con
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
   cudaError_t e = cudaLaunchKernelEx(&cfg, kern, qtile, M, a.nq, a.nkv, a.group, a.tiles,
-                                     a.chunk, kv, kvmap, layer, tree_mask, tree_base, part, status, (int)a.early);
+                                     a.chunk, kv, kvmap, layer, tree_mask, tree_base, part, status, (int)a.early,
+                                     ring_s);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg2 = {};
   cfg2.gridDim = dim3(a.nq * 128 / 256, 16);
@@ -716,7 +761,8 @@ cudaError_t launch_attention(const AttnPlan& a, const KvView& kv, int layer, con
   cfg2.attrs = attr;
   cfg2.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg2, attn_merge_kernel, (const float*)part, M, a.nq, a.max_chunks,
-                            a.chunk, (const int32_t*)kv.seq_len, out, act, status);
+                            a.chunk, (const int32_t*)kv.seq_len, out, act, status,
+                            ring_s >= 0 ? kv.swa_window : 0);
 }
 
 }  // namespace spec

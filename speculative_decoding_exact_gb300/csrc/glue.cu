@@ -285,14 +285,45 @@ cudaError_t launch_swiglu_quant(const GemmPlan& p, const float* pieces, int M, i
 // QKV split: Q -> bf16 hi/lo attention fragments (rows >= M zero); K, V ->
 // bf16 (round to nearest even) into the page of position n_past + row,
 // n_past = seq_len - M (the reserve kernel has already appended the block).
-// Skips the cache when the step is invalid.
+// Skips the cache when the step is invalid.  With a QkTransform, each q and
+// k head is first QK-normed and/or rotated (RoPE) at its row's position.
 // ---------------------------------------------------------------------------
 constexpr int kQkvThreads = 256;     // columns per CTA; one more warp prefetches the KV
+
+// QK-norm and RoPE of one head (Ch. 8 §8.2), computed by the 128 threads
+// that hold its elements (thread d of the group holds element d): the group's
+// sum of squares (warp shuffles, then the four warp sums in order), then
+// y = x * g / sqrt(mean + eps), then the rotation of pair (i, i + 64) by the
+// table's (cos, sin) of row pos, element i.  The groups of a CTA synchronise
+// on their own named barriers (1 and 2), so a group whose columns lie past the
+// end may leave early.
+__device__ __forceinline__ float head_norm_rope(float x, const float* g, const float2* cs, int d, float eps) {
+  __shared__ float red[2][4];
+  __shared__ float xch[2][128];
+  const int grp = threadIdx.x >> 7, w = (threadIdx.x >> 5) & 3;
+  if (g) {
+    float s = x * x;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if ((threadIdx.x & 31) == 0) red[grp][w] = s;
+    asm volatile("bar.sync %0, 128;" ::"r"(1 + grp) : "memory");
+    const float ss = ((red[grp][0] + red[grp][1]) + red[grp][2]) + red[grp][3];
+    x = x * (1.0f / sqrtf(ss / 128.0f + eps)) * g[d];
+  }
+  if (cs) {
+    xch[grp][d] = x;
+    asm volatile("bar.sync %0, 128;" ::"r"(1 + grp) : "memory");
+    const float other = xch[grp][d ^ 64];
+    const float2 t = cs[d & 63];
+    x = d < 64 ? x * t.x - other * t.y : x * t.x + other * t.y;
+  }
+  return x;
+}
 
 __global__ void qkv_post_kernel(const float* __restrict__ pieces, int pN, int pnb, long long pU,
                                 int pG, int M, int nq, int nkv, int dh, KvView kv, int layer,
                                 uint8_t* __restrict__ qtile, int tiles, const int32_t* status,
-                                int late_trigger, float* __restrict__ q32) {
+                                int late_trigger, QkTransform qk) {
   // With late_trigger the attention that follows reads the KV metadata before
   // its own wait: signalling it only after this wait means that every kernel
   // before this one has completed when it starts.
@@ -325,24 +356,31 @@ __global__ void qkv_post_kernel(const float* __restrict__ pieces, int pN, int pn
   const int qcols = nq * dh;
   if (col >= pN) return;
   if (row >= M) {
-    if (col < qcols && swa < 0) write_qtile(qtile, row, col / dh, col % dh, 0.f, nq / nkv, tiles);
+    if (col < qcols) write_qtile(qtile, row, col / dh, col % dh, 0.f, nq / nkv, tiles);
     return;
   }
-  const float v = piece_sum(pieces, pN, piece_slots(pnb, (int)pU, pG, col), row, col);
+  float v = piece_sum(pieces, pN, piece_slots(pnb, (int)pU, pG, col), row, col);
+  const int pos = *kv.seq_len - M + row;
+  if (col < qcols + nkv * dh) {
+    // a q or k head: all 128 threads of this thread's group take this branch
+    const float* g = col < qcols ? qk.gq : qk.gk;
+    const float2* cs = nullptr;
+    if (qk.cs) cs = qk.cs + (size_t)min(max(pos, 0), qk.cs_len - 1) * 64;
+    if (g || cs) v = head_norm_rope(v, g, cs, col % dh, qk.eps);
+  }
   if (col < qcols) {
-    if (swa >= 0) q32[(size_t)row * qcols + col] = v;
-    else write_qtile(qtile, row, col / dh, col % dh, v, nq / nkv, tiles);
+    write_qtile(qtile, row, col / dh, col % dh, v, nq / nkv, tiles);
     return;
   }
   if (*status & kStepAbort) return;
   const int c = col - qcols;
   const int which = c / (nkv * dh);          // 0 = K, 1 = V
   const int head = (c % (nkv * dh)) / dh, d = c % dh;
-  const int pos = *kv.seq_len - M + row;
   if (swa >= 0) {
-    // the ring slot pos mod W (the checkpoint kernel saved it at the step's start)
+    // the ring slot pos mod R: it held position pos - R, which no window of
+    // this block or a later one sees
     if (pos >= 0)
-      kv.swa_ring[ring_row(kv, swa, which, head, pos % kv.swa_window) + d] =
+      kv.swa_ring[ring_row(kv, swa, which, head, pos % kv.swa_rows) + d] =
           __bfloat16_as_ushort(__float2bfloat16_rn(v));
     return;
   }
@@ -359,12 +397,14 @@ __global__ void qkv_post_kernel(const float* __restrict__ pieces, int pN, int pn
 cudaError_t launch_qkv_post(const GemmPlan& p, const float* pieces, int M, int nq, int nkv, int dh,
                             const KvView& kv, int layer, uint8_t* qtile, int tiles,
                             const int32_t* status, cudaStream_t st, bool pdl, bool late_trigger,
-                            float* q32) {
+                            const QkTransform& qk) {
+  // the per-head transforms assume 128-element heads, two per CTA
+  if ((qk.gq || qk.gk || qk.cs) && (dh != 128 || (qk.cs && qk.cs_len < 1))) return cudaErrorInvalidValue;
   cudaLaunchAttribute attrs[2];
   cudaLaunchConfig_t cfg = make_cfg(dim3((p.N + kQkvThreads - 1) / kQkvThreads, 16), dim3(kQkvThreads + 32), 0,
                                     st, pdl, attrs);
   return cudaLaunchKernelEx(&cfg, qkv_post_kernel, pieces, p.N, p.nb, p.U, p.G, M, nq, nkv, dh, kv,
-                            layer, qtile, tiles, status, (int)late_trigger, q32);
+                            layer, qtile, tiles, status, (int)late_trigger, qk);
 }
 
 // ---------------------------------------------------------------------------
@@ -517,7 +557,7 @@ __global__ void kv_reset_kernel(KvView kv) {
     *kv.free_top = kv.num_pages;
     *kv.seq_len = 0;
     if (kv.swa_state) {
-      kv.swa_state[0] = -1;                  // no checkpoint
+      kv.swa_state[0] = -1;                  // no block to roll back into
       kv.swa_state[1] = 0;
     }
   }
@@ -564,7 +604,9 @@ __global__ void kv_reserve_kernel(KvView kv, int n, int commit, const int32_t* _
   st = __shfl_sync(0xffffffffu, st, 0);
   const int upto = len + n;
   const int pages = (upto + kv.page_size - 1) / kv.page_size;
-  if (!st && pages > kv.max_seq_pages) st |= SPEC_ST_CTX_FULL;
+  // beyond the page table, or beyond the positions the context was sized for
+  // (the attention's chunk plan and the rotary table end at max_ctx)
+  if (!st && (pages > kv.max_seq_pages || (kv.max_ctx > 0 && upto > kv.max_ctx))) st |= SPEC_ST_CTX_FULL;
   // the unmapped pages below `pages`, counted by the warp; the r-th of them in
   // page order gets free_stack[top - 1 - r] (the pops of a serial walk)
   int need = 0;
@@ -588,9 +630,13 @@ __global__ void kv_reserve_kernel(KvView kv, int n, int commit, const int32_t* _
       *kv.free_top = top - need;
       if (commit || step_state) *kv.seq_len = upto;
       if (step_state) step_state[1] = 1;
-      // rows laid down by an extend are not a speculative block: the ring
-      // checkpoint of an earlier step no longer applies
-      if (commit && !step_state && kv.swa_state) kv.swa_state[0] = -1;
+      if (kv.swa_state) {
+        // a step's block: rollbacks down to its first position are served by
+        // the rings' spare slots.  Rows laid down by an extend are not a
+        // speculative block: no rollback below the new length.
+        kv.swa_state[0] = step_state ? len : (commit ? -1 : kv.swa_state[0]);
+        if (step_state) kv.swa_state[1] = n;
+      }
     }
   }
   if (lane != 0) return;
@@ -614,8 +660,8 @@ __global__ void kv_rollback_kernel(KvView kv, int new_len, int32_t* status) {
   if (threadIdx.x != 0 || blockIdx.x != 0) return;
   const int len = *kv.seq_len;
   bool bad = new_len < 0 || new_len > len;
-  // a sliding-window ring can be wound back only over the rows its checkpoint
-  // holds: to lengths at or above the last step's n_past
+  // a sliding-window ring can be wound back only over the rows its spare
+  // slots keep: to lengths at or above the last step's n_past
   if (swa_layers(kv) > 0 && new_len < len && (kv.swa_state[0] < 0 || new_len < kv.swa_state[0])) bad = true;
   if (bad) {
     atomicOr(status, SPEC_ST_ROLLBACK);

@@ -4,41 +4,9 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "gemm_plan.h"
+
 namespace spec {
-
-// Work plan of one skinny Q4_K GEMM.  Columns are cut into 16-wide tiles and
-// the tiles into groups of kTilesPerGroup; a work unit is (group, superblock).
-// Units are numbered group-major and CTA i of G owns units
-// [floor(i*U/G), floor((i+1)*U/G)).  Every (CTA, group) run writes one fp32
-// partial "piece" of the group's 16 x (16*kTilesPerGroup) outputs into slot
-// (i - first CTA of that group); the consumer adds the slots in order.  The
-// plan depends only on (N, K, number of SMs), never on the row count M.
-struct GemmPlan {
-  int N = 0, K = 0, nb = 0, ntiles = 0, ngroups = 0, G = 0, max_slots = 0;
-  long long U = 0;
-  int pre_stages = 3;   // stages whose weights are fetched before the dependency wait (<= 6)
-};
-
-// tcgen05 GEMM: one CTA per SM owns 128 weight columns (one per TMEM lane).
-// Warp roles: 4 unpack warps and 4 combine warps (one thread per column each),
-// one warp that issues the bulk copies, and kGemmMmaWarps warps that share the
-// 17 MMAs of a superblock.
-constexpr int kGemmUnpackWarps = 4;
-constexpr int kGemmUnpackThreads = 32 * kGemmUnpackWarps;
-constexpr int kGemmCombineThreads = 128;
-constexpr int kGemmMmaWarps = 3;
-constexpr int kGemmThreads = kGemmUnpackThreads + kGemmCombineThreads + 32 + 32 * kGemmMmaWarps;
-constexpr int kTilesPerGroup = 8;          // 16-column tiles per group = 128 columns
-constexpr int kGemmCols = 16 * kTilesPerGroup;
-constexpr int kGemmStages = 6;
-constexpr int kGemmCtasPerSm = 1;
-constexpr int kMaxSlots = 8;      // pieces per group, guaranteed by make_gemm_plan
-
-GemmPlan make_gemm_plan(int N, int K, int num_sms);
-cudaError_t gemm_init_attributes();   // once per device, before any launch or capture
-size_t gemm_smem_bytes();
-// slots of group gr, and the CTA owning a unit (host mirror of the device math)
-int plan_slots_of_group(const GemmPlan& p, int gr);
 
 // ---- launchers (all enqueue on `st`; `pdl` = programmatic dependent launch)
 cudaError_t launch_repack(const void* src, void* dst, int N, int K, cudaStream_t st);
@@ -83,13 +51,13 @@ struct KvView {
   int32_t* free_stack;
   int32_t* free_top;
   int num_pages, max_seq_pages, n_layers, n_kv, head_dim, page_size;
-  // sliding-window layers (swa_window 0: none): ring [n_swa][K,V][n_kv][W][dh]
-  // and checkpoint [n_swa][K,V][n_kv][16][dh] bf16; swa_state = {checkpoint
-  // position n (-1: none), rows checkpointed}
+  // sliding-window layers (swa_window 0: none): ring [n_swa][K,V][n_kv][R][dh]
+  // bf16 with R = swa_rows = W rounded up to 16, plus 16; swa_state = {the
+  // last step's block position n (-1: none), its rows}
   uint16_t* swa_ring;
-  uint16_t* swa_ckpt;
   int32_t* swa_state;
-  int swa_window, swa_period;
+  int swa_window, swa_period, swa_rows;
+  int max_ctx;               // positions >= max_ctx are refused (SPEC_ST_CTX_FULL)
 };
 
 // layer l is a sliding-window layer when l % period == period - 1; its index
@@ -101,30 +69,26 @@ __host__ __device__ __forceinline__ int swa_index(const KvView& kv, int layer) {
 __host__ __device__ __forceinline__ int swa_layers(const KvView& kv) {
   return (kv.swa_window > 0 && kv.swa_period > 0) ? kv.n_layers / kv.swa_period : 0;
 }
+__host__ __device__ __forceinline__ int swa_ring_rows(int window) { return (window + 15) / 16 * 16 + 16; }
 __host__ __device__ __forceinline__ size_t ring_row(const KvView& kv, int s, int which, int head, int slot) {
-  return ((((size_t)s * 2 + which) * kv.n_kv + head) * kv.swa_window + slot) * kv.head_dim;
+  return ((((size_t)s * 2 + which) * kv.n_kv + head) * kv.swa_rows + slot) * kv.head_dim;
 }
-__host__ __device__ __forceinline__ size_t ckpt_row(const KvView& kv, int s, int which, int head, int j) {
-  return ((((size_t)s * 2 + which) * kv.n_kv + head) * 16 + j) * kv.head_dim;
-}
-// In a sliding-window layer the K,V rows go to the layer's ring and Q to q32
-// (fp32 [16][nq*dh]) instead of the query tiles.
+// In a sliding-window layer the K,V rows go to the layer's ring (slot
+// position mod swa_rows) instead of the paged pool.
+// Optional per-head transforms of q and k before they are stored: QK-norm
+// with gains gq / gk (nullptr: none) and RoPE from the table cs[pos][dh/2] of
+// (cos, sin) for pos < cs_len (nullptr: none).
+struct QkTransform {
+  const float* gq = nullptr;
+  const float* gk = nullptr;
+  const float2* cs = nullptr;
+  int cs_len = 0;
+  float eps = 0.f;
+};
 cudaError_t launch_qkv_post(const GemmPlan& p, const float* pieces, int M, int nq, int nkv,
                             int dh, const KvView& kv, int layer, uint8_t* qtile, int tiles,
                             const int32_t* status, cudaStream_t st, bool pdl, bool late_trigger,
-                            float* q32 = nullptr);
-
-// sliding-window layers: the checkpoint of the ring slots a block of M rows
-// overwrites (after the reservation), the attention of one such layer
-// (partials + merge + quantise for the output projection), and the restore of
-// the checkpoint rows past the committed length (after every rollback)
-int swa_splits(int window);
-size_t swa_partial_floats(int window, int nq);
-cudaError_t launch_swa_checkpoint(const KvView& kv, int M, const int32_t* step_state, const int32_t* status,
-                                  cudaStream_t st, bool pdl);
-cudaError_t launch_swa_restore(const KvView& kv, cudaStream_t st, bool pdl);
-cudaError_t launch_swa_attention(const KvView& kv, int layer, const float* q32, int M, int nq, float* part,
-                                 float* out, uint8_t* act, int32_t* status, cudaStream_t st, bool pdl);
+                            const QkTransform& qk = QkTransform{});
 
 // verify attention: partials then merge (+ quantise for the O projection)
 struct AttnPlan {
@@ -135,6 +99,8 @@ struct AttnPlan {
   // the QKV kernel before it signals only after its own wait
   bool early = false;
 };
+// max_ctx: the span of keys one block may see (the context length; for a
+// sliding-window layer the window plus 32)
 AttnPlan make_attn_plan(int nq, int nkv, int dh, int max_ctx);
 size_t attn_partial_floats(const AttnPlan& a, int max_rows);
 // Q tiles (bf16 hi/lo, 64 KB per (kv head, tile); layout at write_qtile) from
@@ -144,7 +110,10 @@ size_t qtile_bytes(const AttnPlan& a);
 cudaError_t launch_q_to_tile(const float* q, int M, const AttnPlan& a, uint8_t* qtile, cudaStream_t st,
                              bool pdl);
 // tree_mask (DEVICE uint64 [M], optional): the tree nodes row i sees (bit j
-// = node j at position *tree_base + j); NULL = causal
+// = node j at position *tree_base + j); NULL = causal.  A sliding-window
+// layer (swa_index(kv, layer) >= 0) reads its ring, keeps the keys of the
+// window, and places its chunks from the window's first page on (a plan made
+// for the window).
 cudaError_t launch_attention(const AttnPlan& a, const KvView& kv, int layer, const uint8_t* qtile,
                              int M, float* part, float* out, uint8_t* act, int32_t* status,
                              cudaStream_t st, bool pdl, const uint64_t* tree_mask = nullptr,

@@ -26,12 +26,18 @@ class ModelConfig:
     rms_eps: float = 1e-6
     swa_window: int = 0     # sliding-window layers: window W (0 = none) ...
     swa_period: int = 0     # ... at layers l with l % period == period - 1
+    rope_theta: float = 0.0  # rotary embedding base of q and k (0 = none)
 
     def swa_index(self, layer: int) -> int:
         """Index of layer among the sliding-window layers, or -1."""
         if self.swa_window <= 0 or self.swa_period <= 0 or layer % self.swa_period != self.swa_period - 1:
             return -1
         return layer // self.swa_period
+
+    @property
+    def swa_ring_rows(self) -> int:
+        """Slots of a sliding-window ring: W rounded up to 16, plus 16 spare."""
+        return (self.swa_window + 15) // 16 * 16 + 16 if self.swa_window > 0 else 0
 
     @property
     def n_swa(self) -> int:
@@ -44,7 +50,7 @@ class ModelConfig:
     def matrices(self):
         """(name, N, K) of every Q4_K matrix of one block, then the head."""
         H, F = self.hidden, self.ffn
-        return [("w_qkv", self.n_qkv, H), ("w_o", H, H), ("w_gate_up", 2 * F, H),
+        return [("w_qkv", self.n_qkv, H), ("w_o", H, self.n_q_heads * self.head_dim), ("w_gate_up", 2 * F, H),
                 ("w_down", H, F)]
 
     def weight_bytes(self) -> int:
@@ -61,7 +67,7 @@ class Context:
         self.stream = stream or torch.cuda.current_stream()
         self.c = abi.spec_config(cfg.hidden, cfg.n_layers, cfg.n_q_heads, cfg.n_kv_heads,
                                  cfg.head_dim, cfg.ffn, cfg.vocab, max_rows, cfg.page_size,
-                                 max_ctx, cfg.rms_eps, cfg.swa_window, cfg.swa_period)
+                                 max_ctx, cfg.rms_eps, cfg.swa_window, cfg.swa_period, cfg.rope_theta)
         self.h = abi.spec_verify_init(self.c, self.stream.cuda_stream)
         self.max_ctx = max_ctx
 
@@ -101,6 +107,8 @@ class DeviceWeights:
         self.ffn_norm: list | None = None
         self.final_norm: torch.Tensor | None = None
         self.w_head: torch.Tensor | None = None
+        self.q_norm: list | None = None      # per layer: fp32 [head_dim] QK-norm gains
+        self.k_norm: list | None = None
         self._keep = []
 
     def struct(self) -> abi.spec_weights:
@@ -112,7 +120,7 @@ class DeviceWeights:
             return C.cast(a, C.c_void_p)
         return abi.spec_weights(arr(self.w_qkv), arr(self.w_o), arr(self.w_gate_up),
                                 arr(self.w_down), arr(self.attn_norm), arr(self.ffn_norm),
-                                ptr(self.final_norm), ptr(self.w_head))
+                                ptr(self.final_norm), ptr(self.w_head), arr(self.q_norm), arr(self.k_norm))
 
 
 class DeviceKV:
@@ -128,12 +136,11 @@ class DeviceKV:
         self.free_top = torch.zeros(4, dtype=torch.int32, device="cuda")
         self.num_pages = num_pages
         self.max_seq_pages = max_seq_pages
-        # sliding-window layers: ring [n_swa][K,V][n_kv][W][dh], checkpoint of 16 rows, state
-        self.swa_ring = self.swa_ckpt = self.swa_state = None
+        # sliding-window layers: ring [n_swa][K,V][n_kv][R][dh] (R = W rounded up
+        # to 16, plus 16 spare slots) and the last block's state
+        self.swa_ring = self.swa_state = None
         if cfg.n_swa > 0:
-            self.swa_ring = torch.zeros((cfg.n_swa, 2, cfg.n_kv_heads, cfg.swa_window, cfg.head_dim),
-                                        dtype=torch.bfloat16, device="cuda")
-            self.swa_ckpt = torch.zeros((cfg.n_swa, 2, cfg.n_kv_heads, 16, cfg.head_dim),
+            self.swa_ring = torch.zeros((cfg.n_swa, 2, cfg.n_kv_heads, cfg.swa_ring_rows, cfg.head_dim),
                                         dtype=torch.bfloat16, device="cuda")
             self.swa_state = torch.full((4,), -1, dtype=torch.int32, device="cuda")
 
@@ -141,17 +148,17 @@ class DeviceKV:
         return abi.spec_kv(self.pool.data_ptr(), self.num_pages, self.max_seq_pages,
                            self.page_table.data_ptr(), self.seq_len.data_ptr(),
                            self.free_stack.data_ptr(), self.free_top.data_ptr(),
-                           ptr(self.swa_ring), ptr(self.swa_ckpt), ptr(self.swa_state))
+                           ptr(self.swa_ring), ptr(self.swa_state))
 
     def write_ring_rows(self, layer: int, pos0: int, k_bits: np.ndarray, v_bits: np.ndarray):
         """Write bf16 bit patterns [n][n_kv*dh] of positions pos0.. of a
-        sliding-window layer into its ring (slot = position mod W)."""
+        sliding-window layer into its ring (slot = position mod R)."""
         s = self.cfg.swa_index(layer)
         assert s >= 0
-        n, W, nkv, dh = k_bits.shape[0], self.cfg.swa_window, self.cfg.n_kv_heads, self.cfg.head_dim
+        n, R, nkv, dh = k_bits.shape[0], self.cfg.swa_ring_rows, self.cfg.n_kv_heads, self.cfg.head_dim
         kb = torch.from_numpy(k_bits.astype(np.int16).reshape(n, nkv, dh)).cuda()
         vb = torch.from_numpy(v_bits.astype(np.int16).reshape(n, nkv, dh)).cuda()
-        slots = torch.from_numpy((np.arange(pos0, pos0 + n) % W).astype(np.int64)).cuda()
+        slots = torch.from_numpy((np.arange(pos0, pos0 + n) % R).astype(np.int64)).cuda()
         ring16 = self.swa_ring.view(torch.int16)
         ring16[s, 0, :, slots, :] = kb.permute(1, 0, 2)
         ring16[s, 1, :, slots, :] = vb.permute(1, 0, 2)
@@ -159,7 +166,7 @@ class DeviceKV:
     def ring_rows(self, layer: int, positions) -> np.ndarray:
         """bf16 bits [2][n_kv][len(positions)][dh] of the given positions' ring slots."""
         s = self.cfg.swa_index(layer)
-        slots = np.asarray(positions) % self.cfg.swa_window
+        slots = np.asarray(positions) % self.cfg.swa_ring_rows
         return self.swa_ring.view(torch.int16)[s][:, :, slots, :].cpu().numpy().view(np.uint16)
 
     def reset(self, ctx: Context):

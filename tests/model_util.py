@@ -10,7 +10,7 @@ def ocfg_of(cfg: runtime.ModelConfig) -> oracle.Config:
     return oracle.Config(hidden=cfg.hidden, n_layers=cfg.n_layers, n_q_heads=cfg.n_q_heads,
                          n_kv_heads=cfg.n_kv_heads, head_dim=cfg.head_dim, ffn=cfg.ffn,
                          vocab=cfg.vocab, rms_eps=cfg.rms_eps, swa_window=cfg.swa_window,
-                         swa_period=cfg.swa_period)
+                         swa_period=cfg.swa_period, rope_theta=cfg.rope_theta)
 
 
 def build_model(ctx, cfg: runtime.ModelConfig, seed: int = 0, gammas: bool = True,
@@ -45,6 +45,19 @@ def build_model(ctx, cfg: runtime.ModelConfig, seed: int = 0, gammas: bool = Tru
         ow.final_norm = gfin
         dw.final_norm = torch.from_numpy(gfin).cuda()
     return ow, dw
+
+
+def add_qk_norm(cfg, ow, dw, seed: int):
+    """Per-layer QK-norm gains (head_dim long, around 1) on both sides."""
+    import torch
+    ow.q_norm, ow.k_norm, dw.q_norm, dw.k_norm = [], [], [], []
+    for l in range(cfg.n_layers):
+        gq = (1.0 + 0.2 * synth.normal((cfg.head_dim,), seed, 1000 * l + 900)).astype(np.float32)
+        gk = (1.0 + 0.2 * synth.normal((cfg.head_dim,), seed, 1000 * l + 901)).astype(np.float32)
+        ow.q_norm.append(gq)
+        ow.k_norm.append(gk)
+        dw.q_norm.append(torch.from_numpy(gq).cuda())
+        dw.k_norm.append(torch.from_numpy(gk).cuda())
 
 
 def fill_context(cfg, dkv, okv, n_past: int, seed: int):

@@ -25,7 +25,7 @@ def test_strerror_texts():
 def _cfg(**kw):
     base = dict(hidden=6656, n_layers=52, n_q_heads=52, n_kv_heads=4, head_dim=128, ffn=17920,
                 vocab=131072, max_rows=16, page_size=16, max_ctx=2112, rms_eps=1e-6, swa_window=0,
-                swa_period=0)
+                swa_period=0, rope_theta=0.0)
     base.update(kw)
     return abi.spec_config(*[base[f] for f, _ in abi.spec_config._fields_])
 
@@ -35,7 +35,9 @@ def _cfg(**kw):
                                  dict(max_rows=17), dict(vocab=131071), dict(page_size=32),
                                  dict(max_ctx=4), dict(n_layers=0), dict(swa_window=-1),
                                  dict(swa_window=8, swa_period=2), dict(swa_window=4096, swa_period=2),
-                                 dict(swa_window=256, swa_period=0), dict(swa_window=256, swa_period=53)])
+                                 dict(swa_window=256, swa_period=0), dict(swa_window=256, swa_period=53),
+                                 dict(rope_theta=-1.0), dict(rope_theta=float("nan")),
+                                 dict(rope_theta=float("inf"))])
 def test_init_rejects_bad_geometry_before_touching_a_device(bad):
     h = C.c_void_p()
     rc = abi.lib().spec_verify_init(C.byref(_cfg(**bad)), None, C.byref(h))

@@ -8,6 +8,8 @@ be 0 for its inputs.  Tolerance: logits and the per-layer residual stream,
 teacher-forced per layer (the oracle block runs on the GPU's own input to that
 layer).
 """
+import dataclasses
+
 import numpy as np
 import pytest
 
@@ -18,7 +20,7 @@ torch = pytest.importorskip("torch")
 import oracle  # noqa: E402
 from speculative_decoding_exact_gb300 import abi, runtime, synth  # noqa: E402
 from tests.gpu_util import assert_close, require_clear_rows  # noqa: E402
-from tests.model_util import build_model, fill_context, ocfg_of  # noqa: E402
+from tests.model_util import add_qk_norm, build_model, fill_context, ocfg_of  # noqa: E402
 
 SMALL = runtime.ModelConfig(hidden=3328, n_layers=2, n_q_heads=26, n_kv_heads=2, head_dim=128,
                             ffn=8960, vocab=4096)
@@ -244,3 +246,105 @@ def test_step_host_buffers_and_consecutive_rounds(model):
         assert [res.accepted_len, res.next_token, res.status, res.seq_len] == list(ores)
         s, oc = dkv.state(), okv.committed()
         assert s[0] == oc[0] and np.array_equal(s[1], oc[1]) and np.array_equal(s[3], oc[3])
+
+
+def test_step_with_attention_narrower_than_hidden():
+    """A block whose attention width differs from the hidden width (24 query
+    heads of 128 over 4 KV heads at H = 3328, group 6), the geometry of the
+    draft's k/v 6,656 -> 1,024 projections: the step against the oracle."""
+    import __graft_entry__
+    __graft_entry__.build()
+    cfg = runtime.ModelConfig(hidden=3328, n_layers=2, n_q_heads=24, n_kv_heads=4, head_dim=128, ffn=8960,
+                              vocab=4096)
+    ocfg = ocfg_of(cfg)
+    ctx = runtime.Context(cfg, max_ctx=PAGES * 16)
+    try:
+        ow, dw = build_model(ctx, cfg, seed=8)
+        dkv = runtime.DeviceKV(cfg, PAGES, PAGES)
+        dkv.reset(ctx)
+        dkv.extend(ctx, N_PAST)
+        okv = oracle.KV(ocfg, PAGES, PAGES)
+        okv.extend(N_PAST)
+        fill_context(cfg, dkv, okv, N_PAST, seed=12)
+        k = 15
+        hidden = synth.normal((k + 1, cfg.hidden), 8, 40)
+        oidx, olog, _, st = oracle.forward(ocfg, ow, okv.copy(), hidden, logits=True)
+        assert st == 0
+        _, gap = oracle.argmax(olog)
+        require_clear_rows(gap, "narrow-attention rows")
+        draft = synth.plant_draft(oidx, 8, cfg.vocab, 8, 41)
+        ores, oidx2, olog2, _ = oracle.verify_step(ocfg, ow, okv, hidden, draft)
+        h_d = torch.from_numpy(hidden).cuda()
+        d_d = torch.from_numpy(draft).cuda()
+        res = torch.zeros(4, dtype=torch.int32, device="cuda")
+        am = torch.zeros(k + 1, dtype=torch.int32, device="cuda")
+        lg = torch.zeros((k + 1, cfg.vocab), dtype=torch.float32, device="cuda")
+        abi.check("spec_verify_step_ex", abi.spec_verify_step_ex(ctx.h, dw.struct(), dkv.struct(), h_d.data_ptr(),
+                                                                 d_d.data_ptr(), k, res.data_ptr(),
+                                                                 abi.spec_taps(None, am.data_ptr(), lg.data_ptr())))
+        torch.cuda.synchronize()
+        assert_close(lg.cpu().numpy(), olog2, what="logits")
+        assert np.array_equal(am.cpu().numpy(), oidx2)
+        assert list(res.cpu().numpy()) == list(ores)
+        s, oc = dkv.state(), okv.committed()
+        assert s[0] == oc[0] and np.array_equal(s[1], oc[1])
+    finally:
+        ctx.close()
+
+
+@pytest.mark.parametrize("n_past", [N_PAST, 329])
+def test_step_with_qk_norm_and_rope(n_past):
+    """The draft's attention variant (Ch. 8 §8.2 lists QK-norms and RoPE):
+    every q and k head RMS-normed with its own gains, then rotated at its
+    row's position (theta 1e6), 24 query heads over 4 KV heads.  The step
+    against the oracle, at two context lengths; the same inputs without the
+    transforms give other logits (the transforms are live)."""
+    import __graft_entry__
+    __graft_entry__.build()
+    cfg = runtime.ModelConfig(hidden=3328, n_layers=2, n_q_heads=24, n_kv_heads=4, head_dim=128, ffn=8960,
+                              vocab=4096, rope_theta=1.0e6)
+    ocfg = ocfg_of(cfg)
+    ctx = runtime.Context(cfg, max_ctx=PAGES * 16)
+    try:
+        ow, dw = build_model(ctx, cfg, seed=9)
+        add_qk_norm(cfg, ow, dw, seed=9)
+        dkv = runtime.DeviceKV(cfg, PAGES, PAGES)
+        dkv.reset(ctx)
+        dkv.extend(ctx, n_past)
+        okv = oracle.KV(ocfg, PAGES, PAGES)
+        okv.extend(n_past)
+        fill_context(cfg, dkv, okv, n_past, seed=13)
+        k = 15
+        hidden = synth.normal((k + 1, cfg.hidden), 9, 40 + n_past)
+        oidx, olog, _, st = oracle.forward(ocfg, ow, okv.copy(), hidden, logits=True)
+        assert st == 0
+        _, gap = oracle.argmax(olog)
+        require_clear_rows(gap, "qk-norm/rope rows")
+        plain = dataclasses.replace(ocfg, rope_theta=0.0)
+        _, olog_plain, _, _ = oracle.forward(plain, ow, okv.copy(), hidden, logits=True)
+        assert np.max(np.abs(olog_plain - olog)) > 1e-2
+        draft = synth.plant_draft(oidx, 6, cfg.vocab, 9, 41)
+        ores, oidx2, olog2, _ = oracle.verify_step(ocfg, ow, okv, hidden, draft)
+        h_d = torch.from_numpy(hidden).cuda()
+        d_d = torch.from_numpy(draft).cuda()
+        res = torch.zeros(4, dtype=torch.int32, device="cuda")
+        am = torch.zeros(k + 1, dtype=torch.int32, device="cuda")
+        lg = torch.zeros((k + 1, cfg.vocab), dtype=torch.float32, device="cuda")
+        abi.check("spec_verify_step_ex", abi.spec_verify_step_ex(ctx.h, dw.struct(), dkv.struct(), h_d.data_ptr(),
+                                                                 d_d.data_ptr(), k, res.data_ptr(),
+                                                                 abi.spec_taps(None, am.data_ptr(), lg.data_ptr())))
+        torch.cuda.synchronize()
+        assert_close(lg.cpu().numpy(), olog2, what="logits")
+        assert np.array_equal(am.cpu().numpy(), oidx2)
+        assert list(res.cpu().numpy()) == list(ores)
+        s_, oc = dkv.state(), okv.committed()
+        assert s_[0] == oc[0] and np.array_equal(s_[1], oc[1])
+        # a token tree is refused under a rotary configuration
+        tok = torch.zeros(4, dtype=torch.int32, device="cuda")
+        par = torch.tensor([-1, 0, 0, 1], dtype=torch.int32, device="cuda")
+        path = torch.zeros(64, dtype=torch.int32, device="cuda")
+        rc = abi.spec_verify_tree(ctx.h, dw.struct(), dkv.struct(), h_d.data_ptr(), tok.data_ptr(), par.data_ptr(),
+                                  4, res.data_ptr(), path.data_ptr(), None)
+        assert rc == abi.SPEC_EINVAL
+    finally:
+        ctx.close()

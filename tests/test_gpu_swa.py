@@ -1,17 +1,20 @@
-"""Sliding-window layers and their ring checkpoint (Ch. 8 §8.6 item 4: the
-target's KV checkpoint rewinds the paged planes' metadata only, while the
-sliding-window rings keep the at most 16 rows a block may overwrite).
+"""Sliding-window layers and their rings (Ch. 8 §8.6 item 4: the target's KV
+checkpoint rewinds the paged planes' metadata only, while the sliding-window
+rings keep the at most 16 rows a block may overwrite; here the ring has 16
+spare slots, so those rows are never overwritten).
 
-A 2-layer model whose layer 1 is a sliding-window layer of W = 64 positions,
-with the block well past W (the ring has wrapped).  Against the oracle (plain
-definition: a windowed causal mask over the full history):
+A 2-layer model whose layer 1 is a sliding-window layer, with the block well
+past W (the ring has wrapped): W = 64 (a multiple of 16), W = 40 (rounded up
+in the ring) and W = 2048 at a context of 2,400 (several attention chunks).
+Against the oracle (plain definition: a windowed causal mask over the full
+history):
   * tolerance: logits and the per-layer residual stream (teacher-forced);
   * bit-exact: argmax, accepted length, next token, status, KV metadata;
   * the ring after the step holds, for the last W positions, the oracle's
     rows (context rows bit-exact, the block's own rows within one bf16 ulp);
-  * a rollback to the block's start puts back every ring row the block
-    overwrote (bit-exact against the context written before the step), and a
-    rollback below it is refused;
+  * the step leaves the ring rows of the W positions before the block
+    untouched (bit-exact), so a rollback to the block's start needs no copy;
+    a rollback below it is refused;
   * two consecutive rounds agree with the oracle run over the same rounds.
 """
 import numpy as np
@@ -43,25 +46,25 @@ def model():
     ctx.close()
 
 
-def fresh_kv(ctx, n_past=N_PAST):
-    dkv = runtime.DeviceKV(CFG, PAGES, PAGES)
+def fresh_kv(ctx, n_past=N_PAST, cfg=CFG, pages=PAGES):
+    dkv = runtime.DeviceKV(cfg, pages, pages)
     dkv.reset(ctx)
     dkv.extend(ctx, n_past)
-    okv = oracle.KV(ocfg_of(CFG), PAGES, PAGES)
+    okv = oracle.KV(ocfg_of(cfg), pages, pages)
     okv.extend(n_past)
-    fill_context(CFG, dkv, okv, n_past, seed=13)
+    fill_context(cfg, dkv, okv, n_past, seed=13)
     torch.cuda.synchronize()
     return dkv, okv
 
 
-def step(ctx, dw, dkv, hidden, draft):
+def step(ctx, dw, dkv, hidden, draft, cfg=CFG):
     k, M = len(draft), len(draft) + 1
     h = torch.from_numpy(np.ascontiguousarray(hidden)).cuda()
     d = torch.from_numpy(np.ascontiguousarray(draft, dtype=np.int32)).cuda()
     res = torch.zeros(4, dtype=torch.int32, device="cuda")
-    resid = torch.zeros((CFG.n_layers + 1, M, CFG.hidden), dtype=torch.float32, device="cuda")
+    resid = torch.zeros((cfg.n_layers + 1, M, cfg.hidden), dtype=torch.float32, device="cuda")
     am = torch.zeros(M, dtype=torch.int32, device="cuda")
-    lg = torch.zeros((M, CFG.vocab), dtype=torch.float32, device="cuda")
+    lg = torch.zeros((M, cfg.vocab), dtype=torch.float32, device="cuda")
     taps = abi.spec_taps(resid.data_ptr(), am.data_ptr(), lg.data_ptr())
     abi.check("spec_verify_step_ex", abi.spec_verify_step_ex(ctx.h, dw.struct(), dkv.struct(), h.data_ptr(),
                                                              d.data_ptr(), k, res.data_ptr(), taps))
@@ -69,10 +72,10 @@ def step(ctx, dw, dkv, hidden, draft):
     return res.cpu().numpy(), resid.cpu().numpy(), am.cpu().numpy(), lg.cpu().numpy()
 
 
-def ring_vs_oracle(dkv, okv, upto, block_from, what):
+def ring_vs_oracle(dkv, okv, upto, block_from, what, w=W):
     """Ring slots of positions [upto - W, upto) against the oracle's rows: the
     context rows bit-exact, rows the GPU computed (>= block_from) within one ulp."""
-    pos = np.arange(max(0, upto - W), upto)
+    pos = np.arange(max(0, upto - w), upto)
     ring = dkv.ring_rows(1, pos).astype(np.int32)                   # [2][nkv][n][dh]
     ref = np.stack([okv.pool[okv.page_table[p // 16], 1, :, :, p % 16] for p in pos], axis=2).astype(np.int32)
     ctx_part = pos < block_from
@@ -80,43 +83,64 @@ def ring_vs_oracle(dkv, okv, upto, block_from, what):
     assert np.max(np.abs(ring - ref)) <= 1, f"{what}: block rows differ by more than one bf16 ulp"
 
 
-def test_swa_step_matches_oracle_and_ring_checkpoint_restores(model):
-    ctx, ow, dw = model
-    ocfg, k = ocfg_of(CFG), 15
-    hidden = synth.normal((k + 1, CFG.hidden), 5, 300)
-    dkv, okv = fresh_kv(ctx)
-    ring_before = dkv.ring_rows(1, np.arange(N_PAST - W, N_PAST)).copy()
+def check_window_step(ctx, ow, dw, cfg, n_past, pages, seed):
+    w = cfg.swa_window
+    ocfg, k = ocfg_of(cfg), 15
+    hidden = synth.normal((k + 1, cfg.hidden), seed, 300)
+    dkv, okv = fresh_kv(ctx, n_past, cfg, pages)
+    ring_before = dkv.ring_rows(1, np.arange(n_past - w, n_past)).copy()
     oidx, olog, _, st = oracle.forward(ocfg, ow, okv.copy(), hidden, logits=True)
     assert st == 0
     _, gap = oracle.argmax(olog)
-    require_clear_rows(gap, "sliding-window step rows")
+    require_clear_rows(gap, f"sliding-window (W {w}) step rows")
     for L_t in (4, 15, 0):
-        dkv, okv = fresh_kv(ctx)
-        draft = synth.plant_draft(oidx, L_t, CFG.vocab, 5, 310 + L_t)
+        dkv, okv = fresh_kv(ctx, n_past, cfg, pages)
+        draft = synth.plant_draft(oidx, L_t, cfg.vocab, seed, 310 + L_t)
         ores, oidx2, olog2, _ = oracle.verify_step(ocfg, ow, okv, hidden, draft)
-        res, resid, am, lg = step(ctx, dw, dkv, hidden, draft)
+        res, resid, am, lg = step(ctx, dw, dkv, hidden, draft, cfg)
         assert_close(lg, olog2, what="logits")
         assert np.array_equal(am, oidx2)
         assert list(res) == list(ores), (list(res), list(ores))
         s, oc = dkv.state(), okv.committed()
         assert s[0] == oc[0] and np.array_equal(s[1], oc[1]) and np.array_equal(s[3], oc[3])
-        ring_vs_oracle(dkv, okv, int(res[3]), N_PAST, f"ring after accepting {L_t}")
-        # back to the block's start: the checkpoint puts every overwritten row back
-        abi.check("spec_kv_rollback", abi.spec_kv_rollback(ctx.h, dkv.struct(), N_PAST))
+        ring_vs_oracle(dkv, okv, int(res[3]), n_past, f"ring after accepting {L_t}", w)
+        # the block wrote only spare slots: the W rows before it are untouched
+        after = dkv.ring_rows(1, np.arange(n_past - w, n_past))
+        assert np.array_equal(after, ring_before), "the step overwrote a ring row of the window"
+        # back to the block's start: metadata only
+        abi.check("spec_kv_rollback", abi.spec_kv_rollback(ctx.h, dkv.struct(), n_past))
         assert abi.spec_last_status(ctx.h) == 0
-        after = dkv.ring_rows(1, np.arange(N_PAST - W, N_PAST))
-        assert np.array_equal(after, ring_before), "rollback did not restore the ring"
-        # below the checkpoint: refused, nothing changes
-        abi.check("spec_kv_rollback", abi.spec_kv_rollback(ctx.h, dkv.struct(), N_PAST - 1))
+        assert dkv.state()[0] == n_past
+        # below the block: refused, nothing changes
+        abi.check("spec_kv_rollback", abi.spec_kv_rollback(ctx.h, dkv.struct(), n_past - 1))
         assert abi.spec_last_status(ctx.h) & abi.ST_ROLLBACK
-        assert dkv.state()[0] == N_PAST
-    # teacher-forced per layer on the last step's taps (block at N_PAST)
-    okv_t = fresh_kv(ctx)[1]
-    okv_t.reserve(N_PAST + k + 1)
-    for l in range(CFG.n_layers):
-        x_out, st = oracle.block(ocfg, ow, okv_t, l, resid[l], N_PAST)
+        assert dkv.state()[0] == n_past
+    # teacher-forced per layer on the last step's taps (block at n_past)
+    okv_t = fresh_kv(ctx, n_past, cfg, pages)[1]
+    okv_t.reserve(n_past + k + 1)
+    for l in range(cfg.n_layers):
+        x_out, st = oracle.block(ocfg, ow, okv_t, l, resid[l], n_past)
         assert st == 0
-        assert_close(resid[l + 1], x_out, what=f"layer {l} output (window {CFG.swa_index(l) >= 0})")
+        assert_close(resid[l + 1], x_out, what=f"layer {l} output (window {cfg.swa_index(l) >= 0})")
+
+
+def test_swa_step_matches_oracle_and_ring_keeps_the_window(model):
+    ctx, ow, dw = model
+    check_window_step(ctx, ow, dw, CFG, N_PAST, PAGES, 5)
+
+
+@pytest.mark.parametrize("w,n_past,pages", [(40, 150, 24), (2048, 2400, 152)])
+def test_swa_other_windows(w, n_past, pages):
+    """A window that is not a multiple of 16 (the ring rounds it up), and a
+    2,048-position window at a context of 2,400 (the window spans several
+    attention chunks and starts inside a page)."""
+    cfg = runtime.ModelConfig(**{**CFG.__dict__, "swa_window": w})
+    ctx = runtime.Context(cfg, max_ctx=pages * 16)
+    try:
+        ow, dw = build_model(ctx, cfg, seed=5)
+        check_window_step(ctx, ow, dw, cfg, n_past, pages, 7)
+    finally:
+        ctx.close()
 
 
 def test_swa_consecutive_rounds_match_oracle(model):

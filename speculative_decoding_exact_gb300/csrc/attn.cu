@@ -496,9 +496,14 @@ attn_partial_kernel(const uint8_t* __restrict__ qtile, int M, int nq, int nkv, i
       for (int pp = 0; pp < 4; ++pp) pok[pp] = page_of(ks0 + 16 * pp) >= 0;
       const bool allpages = pok[0] && pok[1] && pok[2] && pok[3];
       const bool full = ks0 + kChunk - 1 <= tb && allpages && (!ring || ks0 >= wlo + M - 1);
-      // scores in base-2 units, masked -> -inf
+      // scores in base-2 units, masked -> -inf.  A row past the block or a
+      // head past the group is never stored: it takes the unmasked path too
+      // (its q is zero), so that a warp with such rows does not split between
+      // the two paths.  Measured at a 32k context: the second tile of a KV
+      // head (5 heads, rows 80-127 dead) took 50 us against 32 us for the
+      // first while its dead rows ran the masked path.
       float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-      if (full && live) {
+      if (full || !live) {
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
           s[c] *= c2;

@@ -8,12 +8,12 @@
 // Decomposition (flash-decoding): CTA (chunk c, kv head, tile) takes the keys
 // [c*C, (c+1)*C) for up to 8 query heads of that kv head.  The 8 heads x 16
 // block rows are the 128 rows of tcgen05 MMAs:
-//   S[128 x 64 keys]   = Q[128 x 128 d] . K^T      (A, B in shared memory)
-//   O[128 x 128 d]    += P[128 x 64 keys] . V      (A = P in TMEM, B = V)
-// walking the chunk in 64-key sub-chunks with a running (max, sum) per row
-// and O accumulated in TMEM (online softmax), and writes the partials.  C is
-// 64 times the sub-chunks per chunk, set from max_ctx alone so that one
-// launch is one wave of at most kCtaBudget CTAs.  A merge kernel combines the
+//   S[128 x B keys]   = Q[128 x 128 d] . K^T      (A, B in shared memory)
+//   O[128 x 128 d]   += P[128 x B keys] . V       (A = P in TMEM, B = V)
+// walking the chunk in sub-chunks of B = 64 or 128 keys with a running
+// (max, sum) per row and O accumulated in TMEM (online softmax), and writes
+// the partials.  C is B times the sub-chunks per chunk, set from max_ctx
+// alone so that one launch is one wave of at most kCtaBudget CTAs.  A merge kernel combines the
 // chunks in chunk order, normalises, and quantises the rows for the output
 // projection.  Chunk and sub-chunk boundaries are fixed by max_ctx and masked
 // keys contribute exact zeros, so row i's result is the same for every M
@@ -30,11 +30,31 @@
 
 namespace spec {
 
-constexpr int kChunk = 64;                 // keys per sub-chunk (4 pages of 16)
 constexpr int kCtaBudget = 148;            // CTAs of one partial launch at most
 constexpr int kHeadsPerTile = 8;           // 8 heads x 16 rows = 128 MMA rows
-constexpr int kKvBufs = 3;                 // K/V sub-chunk ring
 constexpr int kPartStride = 130;           // floats per partial row: o[128], max, sum
+constexpr int kQHalfBytes = 128 * 128;     // 16 KB
+constexpr int kQTileBytes = 4 * kQHalfBytes;   // 64 KB
+
+// The layout of one sub-chunk size B (64 or 128 keys): its K/V ring in shared
+// memory (K then V, each [d half][B keys][128 B]; 3 slots of 32 KB or 2 of
+// 64 KB), and TMEM columns S (two buffers of B), P hi and lo (B/2 each), O
+// (128) out of 512.  Each row thread holds B/2 score columns.
+template <int B>
+struct Sub {
+  static_assert(B == 64 || B == 128, "sub-chunk of 64 or 128 keys");
+  static constexpr int kKeys = B;
+  static constexpr int kPages = B / 16;
+  static constexpr int kCols = B / 2;
+  static constexpr int kKvBufs = B == 64 ? 3 : 2;
+  static constexpr int kHalfBytes = B * 128;
+  static constexpr int kKvBufBytes = 4 * kHalfBytes;
+  static constexpr uint32_t kTmS = 0, kTmP = 2 * B, kTmO = 3 * B;
+  static constexpr size_t kSmemFixed = 1024 + kQTileBytes + (size_t)kKvBufs * kKvBufBytes;
+  static_assert(128 * kPartStride * 4 <= kQTileBytes + kKvBufBytes, "partials staging");
+  static_assert(kTmO + 128 <= 512, "TMEM columns");
+};
+int sub_bufs(int sub) { return sub == 64 ? Sub<64>::kKvBufs : Sub<128>::kKvBufs; }
 
 AttnPlan make_attn_plan(int nq, int nkv, int dh, int max_ctx) {
   AttnPlan a;
@@ -46,43 +66,48 @@ AttnPlan make_attn_plan(int nq, int nkv, int dh, int max_ctx) {
   a.tiles = (a.group + kHeadsPerTile - 1) / kHeadsPerTile;
   const int per_chunk = nkv * (a.tiles > 0 ? a.tiles : 1);
   const int budget = kCtaBudget / per_chunk > 0 ? kCtaBudget / per_chunk : 1;
-  const int subs64 = max_ctx > 0 ? (max_ctx + kChunk - 1) / kChunk : 1;
-  const int subs = (subs64 + budget - 1) / budget;            // 64-key sub-chunks per chunk
-  a.chunk = kChunk * subs;
+  // Sub-chunks of 128 keys halve the hand-offs per key (one QK MMA of N =
+  // 128 where 64-key sub-chunks need two); measured on the verify step at a
+  // 32k context, 157.5 against 166.6 steps/s.  A chunk that would hold one
+  // such sub-chunk takes two of 64 instead, which overlap (2k: 223.2 against
+  // 222.4 steps/s).
+  auto subs_of = [&](int b) {
+    const int n = max_ctx > 0 ? (max_ctx + b - 1) / b : 1;
+    return (n + budget - 1) / budget;                          // sub-chunks per chunk
+  };
+  a.sub = subs_of(128) > 1 ? 128 : 64;
+  a.chunk = a.sub * subs_of(a.sub);
   a.max_chunks = (max_ctx + a.chunk - 1) / a.chunk;
   if (a.max_chunks < 1) a.max_chunks = 1;
   // Measured on the 52-block verify step: copying before the wait gains 0.4 %
   // at a 2k context (2 sub-chunks per chunk); at 16k (15 per chunk) the later
   // signal of the QKV kernel cost 1 % and the early copies gained nothing.
-  a.early = a.chunk <= kKvBufs * kChunk;
+  a.early = a.chunk <= sub_bufs(a.sub) * a.sub;
   return a;
 }
 
 // Shared memory of the partial kernel (1 KB aligned; the 128-byte swizzle
 // repeats every 1 KB): the Q tile (hi, lo; each [d half][128 rows][128 B]),
-// a ring of kKvBufs K/V sub-chunks (K then V, each [d half][64 keys][128 B]),
-// then the chunk's page ids.  In every [rows][128 B] block the 16-byte chunk j
-// of row r sits at j ^ (r % 8).  The partials of the tile are staged over the
-// Q tile and the first ring slot once every MMA has completed.
-constexpr int kHalfBytes = kChunk * 128;                       // 8 KB
-constexpr int kKvBufBytes = 4 * kHalfBytes;                    // 32 KB
-constexpr int kQHalfBytes = 128 * 128;                         // 16 KB
-constexpr int kQTileBytes = 4 * kQHalfBytes;                   // 64 KB
-constexpr size_t kSmemFixed = 1024 + kQTileBytes + (size_t)kKvBufs * kKvBufBytes;
-static_assert(128 * kPartStride * 4 <= kQTileBytes + kKvBufBytes, "partials staging");
-size_t attn_smem_bytes(int chunk) { return kSmemFixed + sizeof(int) * (size_t)(chunk / 16); }
-
-// TMEM columns: S (two buffers of 64), P hi (32) and lo (32), O (128)
-constexpr uint32_t kTmS = 0, kTmP = 128, kTmO = 256;
+// the K/V ring of Sub<B>, then the chunk's page ids.  In every [rows][128 B]
+// block the 16-byte chunk j of row r sits at j ^ (r % 8).  The partials of the
+// tile are staged over the Q tile and the first ring slot once every MMA has
+// completed.
+size_t attn_smem_bytes(const AttnPlan& a) {
+  return (a.sub == 64 ? Sub<64>::kSmemFixed : Sub<128>::kSmemFixed) + sizeof(int) * (size_t)(a.chunk / 16);
+}
 constexpr int kTmCols = 512;
 
 // warps: 0-7 own the tile rows, two threads per row (warp w: rows 32(w%4)..,
-// S columns 32(w/4).., O columns 64(w/4)..) for the softmax, the O rescale and
-// the partials; 8 issues the MMAs, 9 issues the copies
+// S columns (B/2)(w/4).., O columns 64(w/4)..) for the softmax, the O rescale
+// and the partials; 8 issues the QK MMAs, 9 the PV MMAs, 10 the K copies and
+// 11 the V copies.  Per-CTA timelines at a 32k context put each issuing role
+// on the critical path when another role shared its warp: the 16 QK and 8 PV
+// MMAs of a 64-key sub-chunk took about 1,500 cycles of one warp's issue, and
+// the 16 tensor copies about 1,000.
 constexpr int kRowWarps = 8;
 constexpr int kRowThreads = 32 * kRowWarps;
-constexpr int kAttnWarps = kRowWarps + 2;
-constexpr int kWarpMma = kRowWarps, kWarpCopy = kRowWarps + 1;
+constexpr int kAttnWarps = kRowWarps + 4;
+constexpr int kWarpQk = kRowWarps, kWarpPv = kRowWarps + 1, kWarpKc = kRowWarps + 2, kWarpVc = kRowWarps + 3;
 constexpr uint64_t kAttnWaitNs = 2000000000ull;
 
 size_t qtile_bytes(const AttnPlan& a) { return (size_t)a.nkv * a.tiles * kQTileBytes; }
@@ -240,19 +265,24 @@ cudaError_t launch_q_to_tile(const float* q, int M, const AttnPlan& a, uint8_t* 
 // ---------------------------------------------------------------------------
 // partials: grid (chunk, kv head, tile), kAttnWarps warps.
 // ---------------------------------------------------------------------------
-template <bool kTree>
+template <bool kTree, int kSub>
 __global__ void __launch_bounds__(kAttnWarps * 32, 1)
 attn_partial_kernel(const uint8_t* __restrict__ qtile, int M, int nq, int nkv, int group, int tiles,
                     int chunk_keys, KvView kv, const __grid_constant__ CUtensorMap kvmap, int layer,
                     const uint64_t* __restrict__ tree_mask, const int32_t* __restrict__ tree_base,
                     float* __restrict__ part, int32_t* status, int early, int ring_s) {
+  using S = Sub<kSub>;
+  constexpr int kChunk = S::kKeys, kPages = S::kPages, kCols = S::kCols, kKvBufs = S::kKvBufs;
+  constexpr int kHalfBytes = S::kHalfBytes, kKvBufBytes = S::kKvBufBytes;
+  constexpr uint32_t kTmS = S::kTmS, kTmP = S::kTmP, kTmO = S::kTmO;
+  constexpr size_t kSmemFixed = S::kSmemFixed;
   extern __shared__ __align__(128) uint8_t dsm[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm) + 1023) & ~(uintptr_t)1023);
   uint8_t* qs = sm;                                    // Q tile: hi [0, 32K), lo [32K, 64K)
   uint8_t* kvb = sm + kQTileBytes;                     // ring slot b at kvb + b * kKvBufBytes
   int* pg = reinterpret_cast<int*>(dsm + kSmemFixed);
   __shared__ uint32_t tmem_slot;
-  __shared__ __align__(8) uint64_t q_full, k_full[kKvBufs], v_full[kKvBufs], kv_free[kKvBufs], s_full[2],
+  __shared__ __align__(8) uint64_t q_full, k_full[kKvBufs], v_full[kKvBufs], k_free[kKvBufs], v_free[kKvBufs], s_full[2],
       s_free[2], p_full, pv_done;
 
   __shared__ float rowmax[2][2][128];       // [sub-chunk parity][column half][row]
@@ -271,7 +301,8 @@ attn_partial_kernel(const uint8_t* __restrict__ qtile, int M, int nq, int nkv, i
     for (int b = 0; b < kKvBufs; ++b) {
       mbar_init(&k_full[b], 1);
       mbar_init(&v_full[b], 1);
-      mbar_init(&kv_free[b], 1);
+      mbar_init(&k_free[b], 1);                  // K read by the QK MMAs
+      mbar_init(&v_free[b], 1);                  // V read by the PV MMAs
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&s_full[b], 1);
@@ -281,7 +312,7 @@ attn_partial_kernel(const uint8_t* __restrict__ qtile, int M, int nq, int nkv, i
     mbar_init(&pv_done, 1);
     fence_mbarrier_init();
   }
-  if (warp == kWarpCopy && lane == 0)
+  if ((warp == kWarpKc || warp == kWarpVc) && lane == 0)
     asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&kvmap)) : "memory");
   // Status, length and page ids were written by the reserve at the start of
   // the step.  With `early` the kernel launched before this one signals its
@@ -337,37 +368,37 @@ attn_partial_kernel(const uint8_t* __restrict__ qtile, int M, int nq, int nkv, i
     const int page = pos0 < len ? pg[(pos0 - key0) >> 4] : -1;
     return (page >= 0 && page < kv.num_pages) ? page : -1;
   };
-  // copy warp: the K and V rows of sub-chunk sc into ring slot sc % kKvBufs;
-  // lanes 0..15 take K (lanes 0-7) or V, page (lane/2)%4, d half
+  // copy warps: the K (warp kWarpKc) or V rows of sub-chunk sc into ring slot
+  // sc % kKvBufs; lane l < 2 * kPages takes page l / 2, d half l % 2
+  const int which = warp == kWarpVc ? 1 : 0;
+  uint64_t* kv_full_w = which ? v_full : k_full;
+  uint64_t* kv_free_w = which ? v_free : k_free;
   auto issue_kv = [&](int sc) {
     const int b = sc % kKvBufs;
     uint8_t* buf = kvb + (size_t)b * kKvBufBytes;
     const int ks0 = key0 + sc * kChunk;
-    const int which = (lane >> 3) & 1, pp = (lane >> 1) & 3, half = lane & 1;
+    const int pp = (lane >> 1) % kPages, half = lane & 1;
     const int page = page_of(ks0 + 16 * pp);
-    const bool go = lane < 16 && page >= 0;
-    const uint32_t kops = __popc(__ballot_sync(0xffffffffu, go && which == 0));
-    if (lane == 0) {
-      mbar_arrive_expect_tx(&k_full[b], kops * 2048u);
-      mbar_arrive_expect_tx(&v_full[b], kops * 2048u);   // a page's K and V come together
-    }
+    const bool go = lane < 2 * kPages && page >= 0;
+    const uint32_t ops = __popc(__ballot_sync(0xffffffffu, go));
+    if (lane == 0) mbar_arrive_expect_tx(&kv_full_w[b], ops * 2048u);
     if (go) {
       const int y = ring ? ((ring_s * 2 + which) * kv.n_kv + kvh) * kv.swa_rows + 16 * page
                          : (((page * kv.n_layers + layer) * 2 + which) * kv.n_kv + kvh) * 16;
       tma_load_2d(buf + which * 2 * kHalfBytes + half * kHalfBytes + pp * 2048, &kvmap, 64 * half, y,
-                  which == 0 ? &k_full[b] : &v_full[b]);
+                  &kv_full_w[b]);
     }
   };
-  if (warp == kWarpCopy)
+  if (warp == kWarpKc || warp == kWarpVc)
     for (int sc = 0; sc < npre; ++sc) issue_kv(sc);
   if (early) {
     pdl_trigger();
     pdl_wait();
   }
 
-  if (warp == kWarpCopy) {
+  if (warp == kWarpKc || warp == kWarpVc) {
     // ------------------------------------------------------------ copies
-    if (lane == 0) {
+    if (lane == 0 && which == 0) {
       mbar_arrive_expect_tx(&q_full, (uint32_t)kQTileBytes);
       bulk_g2s(qs, qtile + (size_t)(kvh * tiles + tile) * kQTileBytes, (uint32_t)kQTileBytes, &q_full);
     }
@@ -376,7 +407,7 @@ attn_partial_kernel(const uint8_t* __restrict__ qtile, int M, int nq, int nkv, i
     for (int sc = npre; sc < nsub; ++sc) {
       const int b = sc % kKvBufs;
       if (sc >= kKvBufs)
-        ok = __all_sync(0xffffffffu, mbar_wait_ns(&kv_free[b], ((sc / kKvBufs) - 1) & 1, kAttnWaitNs));
+        ok = __all_sync(0xffffffffu, mbar_wait_ns(&kv_free_w[b], ((sc / kKvBufs) - 1) & 1, kAttnWaitNs));
       if (!ok) break;
       issue_kv(sc);
       issued = sc + 1;
@@ -384,80 +415,85 @@ attn_partial_kernel(const uint8_t* __restrict__ qtile, int M, int nq, int nkv, i
     if (!ok && lane == 0) atomicOr(status, SPEC_ST_DEVICE_WAIT);
     // no copy may still be writing shared memory when the CTA exits
     if (lane == 0) {
-      mbar_wait_ns(&q_full, 0, kAttnWaitNs);
-      for (int u = max(0, issued - kKvBufs); u < issued; ++u) {
-        mbar_wait_ns(&k_full[u % kKvBufs], (u / kKvBufs) & 1, kAttnWaitNs);
-        mbar_wait_ns(&v_full[u % kKvBufs], (u / kKvBufs) & 1, kAttnWaitNs);
-      }
+      if (which == 0) mbar_wait_ns(&q_full, 0, kAttnWaitNs);
+      for (int u = max(0, issued - kKvBufs); u < issued; ++u)
+        mbar_wait_ns(&kv_full_w[u % kKvBufs], (u / kKvBufs) & 1, kAttnWaitNs);
     }
-  } else if (warp == kWarpMma) {
-    // ------------------------------------------------------------ MMA issue
-    // D f32 (bit 4), A and B bf16 (bits 7, 10), N >> 3 at 17, M >> 4 at 24;
-    // P.V reads V (the B operand) MN-major (bit 16)
-    constexpr uint32_t kIdQK = (1u << 4) | (1u << 7) | (1u << 10) | ((64u >> 3) << 17) | ((128u >> 4) << 24);
-    constexpr uint32_t kIdPV =
-        (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
+  } else if (warp == kWarpQk) {
+    // ------------------------------------------------------------ QK issue
+    // S[sc % 2] = Q . K(sc)^T: 8 d steps of 16, hi and lo parts of Q.
+    // D f32 (bit 4), A and B bf16 (bits 7, 10), N >> 3 at 17, M >> 4 at 24.
+    // The descriptors are built once; a step adds its byte offset / 16 to
+    // the start-address field (addresses stay below 256 KB: no carry).
+    constexpr uint32_t kIdQK =
+        (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kChunk >> 3) << 17) | ((128u >> 4) << 24);
     const uint32_t tm = __shfl_sync(0xffffffffu, tmem, 0);
-    const uint32_t qa = __shfl_sync(0xffffffffu, smem_u32(qs), 0);
-    const uint32_t kva = __shfl_sync(0xffffffffu, smem_u32(kvb), 0);
+    const uint64_t dq0 = desc_sw128(__shfl_sync(0xffffffffu, smem_u32(qs), 0), 16, 1024);
+    const uint64_t dk0 = desc_sw128(__shfl_sync(0xffffffffu, smem_u32(kvb), 0), 16, 1024);
     bool ok = __all_sync(0xffffffffu, mbar_wait_ns(&q_full, 0, kAttnWaitNs));
-    int last_pv = -1, last_qk = -1;
-    // S[sc % 2] = Q . K(sc)^T: 8 d steps of 16, hi and lo parts of Q
-    auto issue_qk = [&](int sc) -> bool {
+    int last = -1;
+    for (int sc = 0; ok && sc < nsub; ++sc) {
       const int b = sc % kKvBufs, sb = sc & 1;
       bool w = mbar_wait_ns(&k_full[b], (sc / kKvBufs) & 1, kAttnWaitNs);
       if (sc >= 2) w = w && mbar_wait_ns(&s_free[sb], ((sc >> 1) - 1) & 1, kAttnWaitNs);
-      if (!__all_sync(0xffffffffu, w)) return false;
-      tc_fence_after();
-      if (elect_one()) {
-        const uint32_t kaddr = kva + (uint32_t)(b * kKvBufBytes);
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks)
-#pragma unroll
-          for (int part = 0; part < 2; ++part) {
-            const uint64_t da = desc_sw128(qa + part * 2 * kQHalfBytes + (ks >> 2) * kQHalfBytes + (ks & 3) * 32, 16, 1024);
-            const uint64_t db = desc_sw128(kaddr + (ks >> 2) * kHalfBytes + (ks & 3) * 32, 16, 1024);
-            mma_f16_ss(tm + kTmS + 64u * sb, da, db, kIdQK, (ks | part) != 0);
-          }
-        mma_commit(&s_full[sb]);
-      }
-      __syncwarp();
-      last_qk = sc;
-      return true;
-    };
-    if (ok && nsub > 0) ok = issue_qk(0);
-    for (int sc = 0; ok && sc < nsub; ++sc) {
-      if (sc + 1 < nsub && !(ok = issue_qk(sc + 1))) break;
-      // O (+)= P . V(sc): 4 key steps of 16, hi and lo parts of P
-      ok = __all_sync(0xffffffffu, mbar_wait_ns(&p_full, sc & 1, kAttnWaitNs) &&
-                                       mbar_wait_ns(&v_full[sc % kKvBufs], (sc / kKvBufs) & 1, kAttnWaitNs));
+      ok = __all_sync(0xffffffffu, w);
       if (!ok) break;
       tc_fence_after();
       if (elect_one()) {
-        const uint32_t vaddr = kva + (uint32_t)((sc % kKvBufs) * kKvBufBytes + 2 * kHalfBytes);
+        const uint64_t dk = dk0 + (uint64_t)((b * kKvBufBytes) >> 4);
+        const uint32_t d = tm + kTmS + (uint32_t)kChunk * sb;
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
+        for (int ks = 0; ks < 8; ++ks)
 #pragma unroll
-          for (int part = 0; part < 2; ++part) {
-            // V is MN-major: lbo = 8 KB between d halves, sbo = 1 KB between 8-key groups
-            const uint64_t db = desc_sw128(vaddr + kk * 2048, kHalfBytes, 1024);
-            mma_f16_ts(tm + kTmO, tm + kTmP + 32u * part + 8u * kk, db, kIdPV,
-                       (sc | kk | part) != 0);
-          }
-        mma_commit(&pv_done);
-        mma_commit(&kv_free[sc % kKvBufs]);
+          for (int part = 0; part < 2; ++part)
+            mma_f16_ss(d, dq0 + (uint64_t)((part * 2 * kQHalfBytes + (ks >> 2) * kQHalfBytes + (ks & 3) * 32) >> 4),
+                       dk + (uint64_t)(((ks >> 2) * kHalfBytes + (ks & 3) * 32) >> 4), kIdQK, (ks | part) != 0);
+        mma_commit(&s_full[sb]);
+        mma_commit(&k_free[b]);
       }
       __syncwarp();
-      last_pv = sc;
+      last = sc;
     }
     if (!ok && lane == 0) atomicOr(status, SPEC_ST_DEVICE_WAIT);
-    // TMEM is released at the end: every MMA issued here must have finished
-    if (last_pv >= 0) mbar_wait_ns(&pv_done, last_pv & 1, kAttnWaitNs);
-    if (last_qk > last_pv) mbar_wait_ns(&s_full[last_qk & 1], (last_qk >> 1) & 1, kAttnWaitNs);
+    // TMEM is released at the end: this warp's MMAs must have finished
+    if (last >= 0) mbar_wait_ns(&s_full[last & 1], (last >> 1) & 1, kAttnWaitNs);
+  } else if (warp == kWarpPv) {
+    // ------------------------------------------------------------ PV issue
+    // O (+)= P . V(sc): key steps of 16, hi and lo parts of P; V (the B
+    // operand) MN-major (bit 16): lbo = the d-half stride, sbo = 1 KB between
+    // 8-key groups
+    constexpr uint32_t kIdPV =
+        (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
+    const uint32_t tm = __shfl_sync(0xffffffffu, tmem, 0);
+    const uint64_t dv0 = desc_sw128(__shfl_sync(0xffffffffu, smem_u32(kvb), 0) + 2 * kHalfBytes, kHalfBytes, 1024);
+    bool ok = true;
+    int last = -1;
+    for (int sc = 0; ok && sc < nsub; ++sc) {
+      const int b = sc % kKvBufs;
+      ok = __all_sync(0xffffffffu, mbar_wait_ns(&p_full, sc & 1, kAttnWaitNs) &&
+                                       mbar_wait_ns(&v_full[b], (sc / kKvBufs) & 1, kAttnWaitNs));
+      if (!ok) break;
+      tc_fence_after();
+      if (elect_one()) {
+        const uint64_t dv = dv0 + (uint64_t)((b * kKvBufBytes) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < kChunk / 16; ++kk)
+#pragma unroll
+          for (int part = 0; part < 2; ++part)
+            mma_f16_ts(tm + kTmO, tm + kTmP + (uint32_t)(kChunk / 2) * part + 8u * kk,
+                       dv + (uint64_t)((kk * 2048) >> 4), kIdPV, (sc | kk | part) != 0);
+        mma_commit(&pv_done);
+        mma_commit(&v_free[b]);
+      }
+      __syncwarp();
+      last = sc;
+    }
+    if (!ok && lane == 0) atomicOr(status, SPEC_ST_DEVICE_WAIT);
+    if (last >= 0) mbar_wait_ns(&pv_done, last & 1, kAttnWaitNs);
   } else {
     // ------------------------------------------------------------ tile rows
     const int r = 32 * (warp & 3) + lane;               // tile row = TMEM lane
-    const int h = warp >> 2;                            // S columns 32h.., O columns 64h..
+    const int h = warp >> 2;                            // S columns kCols*h.., O columns 64h..
     const int hl = tile * kHeadsPerTile + (r >> 4);     // head within the kv group
     const int row = r & 15;                             // block row
     const bool live = hl < group && row < M;
@@ -475,26 +511,32 @@ attn_partial_kernel(const uint8_t* __restrict__ qtile, int M, int nq, int nkv, i
       const int sb = sc & 1, b = sc % kKvBufs;
       const int ks0 = key0 + sc * kChunk;
       const bool got = ok && __all_sync(0xffffffffu, mbar_wait_ns(&s_full[sb], (sc >> 1) & 1, kAttnWaitNs));
-      float s[32];
+      float s[kCols];
       if (got) {
         tc_fence_after();
-        uint32_t u[32];
-        tmem_ld32(tmem + lane_base + kTmS + 64u * sb + 32u * h, u);
-        tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < 32; ++c) s[c] = __uint_as_float(u[c]);
+        for (int q = 0; q < kCols / 32; ++q) {
+          uint32_t u[32];
+          tmem_ld32(tmem + lane_base + kTmS + (uint32_t)kChunk * sb + (uint32_t)kCols * h + 32u * q, u);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < 32; ++c) s[32 * q + c] = __uint_as_float(u[c]);
+        }
         tc_fence_before();
         mbar_arrive(&s_free[sb]);
       } else {
 #pragma unroll
-        for (int c = 0; c < 32; ++c) s[c] = 0.f;
+        for (int c = 0; c < kCols; ++c) s[c] = 0.f;
       }
       // pages of this sub-chunk: a key of a page past len or with an
       // out-of-range id is masked (and its V row zeroed below)
-      bool pok[4];
+      bool pok[kPages];
+      bool allpages = true;
 #pragma unroll
-      for (int pp = 0; pp < 4; ++pp) pok[pp] = page_of(ks0 + 16 * pp) >= 0;
-      const bool allpages = pok[0] && pok[1] && pok[2] && pok[3];
+      for (int pp = 0; pp < kPages; ++pp) {
+        pok[pp] = page_of(ks0 + 16 * pp) >= 0;
+        allpages = allpages && pok[pp];
+      }
       const bool full = ks0 + kChunk - 1 <= tb && allpages && (!ring || ks0 >= wlo + M - 1);
       // scores in base-2 units, masked -> -inf.  A row past the block or a
       // head past the group is never stored: it takes the unmasked path too
@@ -505,31 +547,33 @@ attn_partial_kernel(const uint8_t* __restrict__ qtile, int M, int nq, int nkv, i
       float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
       if (full || !live) {
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
+        for (int c = 0; c < kCols; ++c) {
           s[c] *= c2;
           mx4[c & 3] = fmaxf(mx4[c & 3], s[c]);
         }
       } else {
-        // tree: key ks0 + 32h + c is visible when it precedes the tree (and
-        // the row is live), or when it is node rel = base + c with bit rel of
-        // tm set, and its page is valid: bit c of vm
+        // tree: key ks0 + kCols*h + c is visible when it precedes the tree
+        // (and the row is live), or when it is node rel = base + c with bit
+        // rel of tm set, and its page is valid: bit c of vm
         const int lim = live ? n_past + row - ks0 : -1;
         const int lim_lo = ring ? wlo + row - ks0 : -(1 << 30);   // the window's first key
-        uint32_t vm;
+        uint64_t vm = 0ull;
         if (kTree) {
-          const int base = ks0 + 32 * h - tb;
-          const int nold = min(32, max(0, -base));
-          const uint32_t mold = !live ? 0u : (nold >= 32 ? 0xffffffffu : (1u << nold) - 1u);
-          const uint32_t blk = base >= 0 ? (base < 64 ? (uint32_t)(tm >> base) : 0u)
-                                         : (-base < 32 ? (uint32_t)(tm << -base) : 0u);
-          const uint32_t pm = ((h ? pok[2] : pok[0]) ? 0x0000ffffu : 0u) | ((h ? pok[3] : pok[1]) ? 0xffff0000u : 0u);
+          const int base = ks0 + kCols * h - tb;
+          const int nold = min(kCols, max(0, -base));
+          const uint64_t mold = !live ? 0ull : (nold >= 64 ? ~0ull : (1ull << nold) - 1ull);
+          const uint64_t blk = base >= 0 ? (base < 64 ? tm >> base : 0ull) : (-base < 64 ? tm << -base : 0ull);
+          uint64_t pm = 0ull;
+#pragma unroll
+          for (int pp = 0; pp < kPages / 2; ++pp)
+            if (pok[(kPages / 2) * h + pp]) pm |= 0xffffull << (16 * pp);
           vm = (mold | blk) & pm;
         }
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const int key = 32 * h + c;
+        for (int c = 0; c < kCols; ++c) {
+          const int key = kCols * h + c;
           // causal: key ks0 + key is visible to row when key <= n_past + row - ks0
-          const bool vis = kTree ? ((vm >> c) & 1u) != 0 : (key <= lim && key >= lim_lo && pok[key >> 4]);
+          const bool vis = kTree ? ((vm >> c) & 1ull) != 0 : (key <= lim && key >= lim_lo && pok[key >> 4]);
           s[c] = vis ? s[c] * c2 : -INFINITY;
           mx4[c & 3] = fmaxf(mx4[c & 3], s[c]);
         }
@@ -549,13 +593,12 @@ attn_partial_kernel(const uint8_t* __restrict__ qtile, int M, int nq, int nkv, i
         lsum *= alpha;
       }
       const float base = mref == -INFINITY ? 0.f : mref;
-      uint32_t ph[16], pl[16];
       float ps4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const float p0 = exp2_approx(s[2 * c] - base), p1 = exp2_approx(s[2 * c + 1] - base);
-        ps4[c & 3] += p0 + p1;
-        split2(p0, p1, ph[c], pl[c]);
+      for (int c = 0; c < kCols; c += 2) {
+        s[c] = exp2_approx(s[c] - base);                // p, in place
+        s[c + 1] = exp2_approx(s[c + 1] - base);
+        ps4[(c >> 1) & 3] += s[c] + s[c + 1];
       }
       lsum += (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
       // P(sc) may be written, and O rescaled, once P.V(sc-1) has finished
@@ -592,8 +635,16 @@ attn_partial_kernel(const uint8_t* __restrict__ qtile, int M, int nq, int nkv, i
         }
         fence_proxy_async();
       }
-      tmem_st16(tmem + lane_base + kTmP + 16u * h, ph);
-      tmem_st16(tmem + lane_base + kTmP + 32u + 16u * h, pl);
+      // P hi / lo as bf16 pairs: the keys kCols*h + 32q .. at columns
+      // (kCols/2)*h + 16q .. of each half
+#pragma unroll
+      for (int q = 0; q < kCols / 32; ++q) {
+        uint32_t ph[16], pl[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) split2(s[32 * q + 2 * c], s[32 * q + 2 * c + 1], ph[c], pl[c]);
+        tmem_st16(tmem + lane_base + kTmP + (uint32_t)(kCols / 2) * h + 16u * q, ph);
+        tmem_st16(tmem + lane_base + kTmP + (uint32_t)(kChunk / 2) + (uint32_t)(kCols / 2) * h + 16u * q, pl);
+      }
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&p_full);
@@ -737,15 +788,18 @@ cudaError_t launch_attention(const AttnPlan& a, const KvView& kv, int layer, con
   alignas(64) CUtensorMap kvmap;
   cudaError_t em = ring_s >= 0 ? make_ring_tmap(kv, &kvmap) : make_kv_tmap(kv, &kvmap);
   if (em != cudaSuccess) return em;
-  const size_t smem = attn_smem_bytes(a.chunk);
+  const size_t smem = attn_smem_bytes(a);
   // the causal kernel and the token-tree kernel (which tests every block key
-  // against the row's ancestor mask)
-  auto kern = tree_mask ? attn_partial_kernel<true> : attn_partial_kernel<false>;
-  static size_t smem_attr[2] = {0, 0};
-  if (smem_attr[tree_mask != nullptr] < smem) {
+  // against the row's ancestor mask), each for sub-chunks of 64 and 128 keys
+  const int inst = (tree_mask != nullptr) * 2 + (a.sub == 128);
+  auto kern = inst == 0 ? attn_partial_kernel<false, 64>
+                        : inst == 1 ? attn_partial_kernel<false, 128>
+                                    : inst == 2 ? attn_partial_kernel<true, 64> : attn_partial_kernel<true, 128>;
+  static size_t smem_attr[4] = {0, 0, 0, 0};
+  if (smem_attr[inst] < smem) {
     cudaError_t ea = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (ea != cudaSuccess) return ea;
-    smem_attr[tree_mask != nullptr] = smem;
+    smem_attr[inst] = smem;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.max_chunks, a.nkv, a.tiles);

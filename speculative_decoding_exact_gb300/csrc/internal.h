@@ -93,6 +93,7 @@ cudaError_t launch_qkv_post(const GemmPlan& p, const float* pieces, int M, int n
 // verify attention: partials then merge (+ quantise for the O projection)
 struct AttnPlan {
   int nq = 0, nkv = 0, dh = 0, max_ctx = 0, chunk = 0, max_chunks = 0;
+  int sub = 64;                 // keys per sub-chunk: 64 or 128
   int group = 0, tiles = 0;     // query heads per kv head; 128-row MMA tiles per kv head
   // the chunk fits the K/V ring: the partial kernel reads the KV metadata and
   // copies the chunk's rows of earlier steps before its dependency wait, and

@@ -119,9 +119,9 @@ def test_step_matches_oracle_and_is_teacher_forced_per_layer(model):
 
 def test_step_long_context_plan_matches_oracle(model):
     """The same step under a long-context work plan (max_ctx 8192: chunks of
-    256 keys, more than the K/V ring holds, so the attention reads the KV
-    metadata after its dependency wait) matches the oracle as the short plan
-    does."""
+    512 keys in sub-chunks of 128, more than the K/V ring holds, so the
+    attention reads the KV metadata after its dependency wait) matches the
+    oracle as the short plan (sub-chunks of 64) does."""
     _, ow, dw = model
     cfg, ocfg = SMALL, ocfg_of(SMALL)
     k = 15

@@ -129,6 +129,31 @@ def planted_tree(cfg, ow, okv0, seed, n_max):
             np.array(parent, dtype=np.int32))
 
 
+def test_tree_step_long_plan_matches_oracle(model):
+    """A tree step under a long-context work plan (max_ctx 8192: the
+    attention's tree instance with 128-key sub-chunks, 64 score columns per
+    row thread and 64-bit visibility masks) against the oracle."""
+    _, ow, dw = model
+    cfg = SMALL
+    ctx_long = runtime.Context(SMALL, max_ctx=8192)
+    try:
+        for seed in (7, 8):
+            dkv, okv = fresh_kv(ctx_long)
+            rows, tokens, parent = planted_tree(cfg, ow, okv, seed, 16)
+            ores, opath, oidx, olg = oracle.verify_tree(ocfg_of(cfg), ow, okv, rows, tokens, parent)
+            assert ores[2] == 0
+            res, path, am, lg = gpu_tree(ctx_long, dw, dkv, rows, tokens, parent)
+            assert_close(lg, olg, what="logits (long plan)")
+            _, gap = oracle.argmax(olg)
+            require_clear_rows(gap, f"long-plan tree {seed} nodes")
+            assert np.array_equal(am, oidx)
+            assert list(res) == list(ores)
+            assert np.array_equal(path[: res[0] + 1], opath)
+            kv_rows_equal(dkv, okv, int(ores[3]))
+    finally:
+        ctx_long.close()
+
+
 @pytest.mark.parametrize("seed", [1, 2, 3, 4, 5, 6])
 def test_tree_step_matches_oracle(model, seed):
     ctx, ow, dw = model

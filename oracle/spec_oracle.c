@@ -557,8 +557,8 @@ void orc_attention(const orc_cfg* c, const orc_kv* kv, int layer, const float* q
 }
 
 /* ------------------------------------------------------------------------ */
-/* QK-norm and rotary position embedding ([8] §8.2: the draft's attention    */
-/* has "QK-norms and RoPE like an ordinary transformer block").  Readings:    */
+/* QK-norm and rotary position embedding (The DFlash draft, Ch. 8 §8.2,     */
+/* lists both for the draft's attention, without formulas).  Readings:       */
 /*   QK-norm: each q head and each k head x (head_dim values) becomes         */
 /*     x_d / sqrt(mean(x^2) + eps) * g_d, the layer's gain g shared by heads; */
 /*   RoPE ("rotate half"): with h = head_dim/2 and f_i = theta^(-i/h), the    */

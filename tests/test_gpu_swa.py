@@ -169,3 +169,29 @@ def test_swa_model_refuses_token_trees(model):
     res = torch.zeros(4, dtype=torch.int32, device="cuda")
     assert abi.spec_verify_tree(ctx.h, dw.struct(), dkv.struct(), h.data_ptr(), t.data_ptr(), p.data_ptr(), 4,
                                 res.data_ptr(), None, None) == abi.SPEC_EINVAL
+
+
+@pytest.mark.parametrize("n_past,M", [(10, 4), (60, 16), (150, 16), (300, 8)])
+def test_window_attention_alone_matches_oracle(model, n_past, M):
+    """spec_attention on the window layer (its ring, the window mask and the
+    window's chunk plan) against the oracle's windowed attention: a block
+    inside the first window, one at the window's edge, one past a wrapped
+    ring, one far past it."""
+    ctx, _, _ = model
+    n = n_past + M
+    dkv, okv = fresh_kv(ctx, n)
+    # the block's first row looks back W - 1 positions past the last W: lay
+    # down the last R positions (the whole ring) from the oracle's rows
+    p0 = max(0, n - CFG.swa_ring_rows)
+    pos = np.arange(p0, n)
+    kb = np.stack([okv.pool[okv.page_table[p // 16], 1, 0, :, p % 16].reshape(-1) for p in pos])
+    vb = np.stack([okv.pool[okv.page_table[p // 16], 1, 1, :, p % 16].reshape(-1) for p in pos])
+    dkv.write_ring_rows(1, p0, kb, vb)
+    torch.cuda.synchronize()
+    q = synth.normal((M, CFG.n_q_heads, CFG.head_dim), 9, n_past) * 4.0
+    qd = torch.from_numpy(np.ascontiguousarray(q.reshape(M, -1))).cuda()
+    out = torch.zeros((M, CFG.n_q_heads * CFG.head_dim), dtype=torch.float32, device="cuda")
+    abi.check("spec_attention", abi.spec_attention(ctx.h, dkv.struct(), 1, qd.data_ptr(), M, out.data_ptr()))
+    torch.cuda.synchronize()
+    ref = okv.attention(1, q.reshape(M, -1), n_past)
+    assert_close(out.cpu().numpy(), ref, what=f"window attention at n_past {n_past}, M {M}")

@@ -121,7 +121,7 @@ typedef struct spec_config {
     int32_t page_size;    /* 16                                             */
     int32_t max_ctx;      /* maximum sequence length in positions           */
     float   rms_eps;      /* RMSNorm epsilon, e.g. 1e-6                     */
-    /* Optional sliding-window layers (Ch. 8 §8.6 item 4: "SWA rings"):
+    /* Optional sliding-window layers (Ch. 8 §8.6 item 4, the window rings):
      * with swa_window W > 0, layer l is a sliding-window layer when
      * l % swa_period == swa_period - 1 (1 <= swa_period <= n_layers); its row
      * at position p sees positions p-W+1..p, and its K/V live in a ring of

@@ -7,7 +7,8 @@
  * Every function is the plain definition, scalar, in serial order.  Precision:
  *   - integer sums are exact (int32/int64);
  *   - the per-superblock combination is fp32 with each operation rounded
- *     (the "fixed fp32 order" reading of the integer-dot anchor, [32] §32.7);
+ *     (our reading of the integer-dot anchor's fixed combination order,
+ *     [32] §32.7);
  *   - sums of many fp32 terms (GEMM outputs over superblocks) accumulate in
  *     fp64 and are rounded to fp32 once;
  *   - RMSNorm, attention and SwiGLU are computed in fp64 and stored as fp32;
@@ -331,7 +332,7 @@ void orc_softmax_row(const float* l, int V, float* p) {
 /* The draw of [33] §33.2 (sample_distribution_mt_ordered is named there, not
  * printed): one uniform u, then the tokens of the row's order with a running
  * fp32 sum c of their probabilities w; the first token with u < c.  The order
- * is index order (the reading of "a precomputed token order"), restricted to
+ * is index order (our reading of the precomputed order the rule walks), restricted to
  * the tokens with w > 0 as the listing filters it; a token of weight 0 adds
  * nothing to c and can never be the first with u < c, so the walk below skips
  * nothing explicitly.  If rounding leaves c <= u after the last token, the

@@ -129,11 +129,12 @@ def test_swa_step_matches_oracle_and_ring_keeps_the_window(model):
     check_window_step(ctx, ow, dw, CFG, N_PAST, PAGES, 5)
 
 
-@pytest.mark.parametrize("w,n_past,pages", [(40, 150, 24), (2048, 2400, 152)])
+@pytest.mark.parametrize("w,n_past,pages", [(40, 150, 24), (2048, 2400, 152), (8192, 8400, 530)])
 def test_swa_other_windows(w, n_past, pages):
-    """A window that is not a multiple of 16 (the ring rounds it up), and a
+    """A window that is not a multiple of 16 (the ring rounds it up), a
     2,048-position window at a context of 2,400 (the window spans several
-    attention chunks and starts inside a page)."""
+    attention chunks and starts inside a page), and an 8,192-position window
+    at 8,400 (the window's plan takes 128-key sub-chunks)."""
     cfg = runtime.ModelConfig(**{**CFG.__dict__, "swa_window": w})
     ctx = runtime.Context(cfg, max_ctx=pages * 16)
     try:

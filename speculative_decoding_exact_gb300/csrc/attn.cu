@@ -13,9 +13,9 @@
 // walking the chunk in sub-chunks of B = 64 or 128 keys with a running
 // (max, sum) per row and O accumulated in TMEM (online softmax), and writes
 // the partials.  C is B times the sub-chunks per chunk, set from max_ctx
-// alone so that one launch is one wave of at most kCtaBudget CTAs.  A merge kernel combines the
-// chunks in chunk order, normalises, and quantises the rows for the output
-// projection.  Chunk and sub-chunk boundaries are fixed by max_ctx and masked
+// alone so that one launch is one wave of at most kCtaBudget CTAs.  A merge
+// kernel combines the chunks in chunk order, normalises, and quantises the
+// rows for the output projection.  Chunk and sub-chunk boundaries are fixed by max_ctx and masked
 // keys contribute exact zeros, so row i's result is the same for every M
 // (batch-height invariance: "The Two-Fifteen That Wasn't").
 //
@@ -282,7 +282,8 @@ attn_partial_kernel(const uint8_t* __restrict__ qtile, int M, int nq, int nkv, i
   uint8_t* kvb = sm + kQTileBytes;                     // ring slot b at kvb + b * kKvBufBytes
   int* pg = reinterpret_cast<int*>(dsm + kSmemFixed);
   __shared__ uint32_t tmem_slot;
-  __shared__ __align__(8) uint64_t q_full, k_full[kKvBufs], v_full[kKvBufs], k_free[kKvBufs], v_free[kKvBufs], s_full[2],
+  __shared__ __align__(8) uint64_t q_full, k_full[kKvBufs], v_full[kKvBufs], k_free[kKvBufs], v_free[kKvBufs],
+      s_full[2],
       s_free[2], p_full, pv_done;
 
   __shared__ float rowmax[2][2][128];       // [sub-chunk parity][column half][row]

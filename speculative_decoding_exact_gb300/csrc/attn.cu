@@ -283,8 +283,7 @@ attn_partial_kernel(const uint8_t* __restrict__ qtile, int M, int nq, int nkv, i
   int* pg = reinterpret_cast<int*>(dsm + kSmemFixed);
   __shared__ uint32_t tmem_slot;
   __shared__ __align__(8) uint64_t q_full, k_full[kKvBufs], v_full[kKvBufs], k_free[kKvBufs], v_free[kKvBufs],
-      s_full[2],
-      s_free[2], p_full, pv_done;
+      s_full[2], s_free[2], p_full, pv_done;
 
   __shared__ float rowmax[2][2][128];       // [sub-chunk parity][column half][row]
   __shared__ float lpart[2][128];           // [column half][row]

@@ -297,6 +297,14 @@ constexpr int kQkvThreads = 256;     // columns per CTA; one more warp prefetche
 // table's (cos, sin) of row pos, element i.  The groups of a CTA synchronise
 // on their own named barriers (1 and 2), so a group whose columns lie past the
 // end may leave early.
+// named barrier of one 128-thread group (ids 1 and 2: immediates, so the
+// kernel reserves two hardware barriers, not all sixteen)
+__device__ __forceinline__ void group_bar(int grp) {
+  if (grp == 0)
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+  else
+    asm volatile("bar.sync 2, 128;" ::: "memory");
+}
 __device__ __forceinline__ float head_norm_rope(float x, const float* g, const float2* cs, int d, float eps) {
   __shared__ float red[2][4];
   __shared__ float xch[2][128];
@@ -306,13 +314,13 @@ __device__ __forceinline__ float head_norm_rope(float x, const float* g, const f
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
     if ((threadIdx.x & 31) == 0) red[grp][w] = s;
-    asm volatile("bar.sync %0, 128;" ::"r"(1 + grp) : "memory");
+    group_bar(grp);
     const float ss = ((red[grp][0] + red[grp][1]) + red[grp][2]) + red[grp][3];
     x = x * (1.0f / sqrtf(ss / 128.0f + eps)) * g[d];
   }
   if (cs) {
     xch[grp][d] = x;
-    asm volatile("bar.sync %0, 128;" ::"r"(1 + grp) : "memory");
+    group_bar(grp);
     const float other = xch[grp][d ^ 64];
     const float2 t = cs[d & 63];
     x = d < 64 ? x * t.x - other * t.y : x * t.x + other * t.y;

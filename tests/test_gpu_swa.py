@@ -27,7 +27,7 @@ torch = pytest.importorskip("torch")
 import oracle  # noqa: E402
 from speculative_decoding_exact_gb300 import abi, runtime, synth  # noqa: E402
 from tests.gpu_util import assert_close, require_clear_rows  # noqa: E402
-from tests.model_util import build_model, fill_context, ocfg_of  # noqa: E402
+from tests.model_util import add_qk_norm, build_model, fill_context, ocfg_of  # noqa: E402
 
 W = 64
 CFG = runtime.ModelConfig(hidden=3328, n_layers=2, n_q_heads=26, n_kv_heads=2, head_dim=128, ffn=8960,
@@ -196,3 +196,30 @@ def test_window_attention_alone_matches_oracle(model, n_past, M):
     torch.cuda.synchronize()
     ref = okv.attention(1, q.reshape(M, -1), n_past)
     assert_close(out.cpu().numpy(), ref, what=f"window attention at n_past {n_past}, M {M}")
+
+
+def test_window_layers_with_qk_norm_and_rope():
+    """Window layers together with QK-norm and RoPE (the transforms run before
+    the K row enters the ring): one step against the oracle, and the ring
+    rows of the block against the oracle's (within one bf16 ulp)."""
+    cfg = runtime.ModelConfig(**{**CFG.__dict__, "rope_theta": 10000.0})
+    ctx = runtime.Context(cfg, max_ctx=PAGES * 16)
+    try:
+        ow, dw = build_model(ctx, cfg, seed=6)
+        add_qk_norm(cfg, ow, dw, seed=6)
+        ocfg = ocfg_of(cfg)
+        hidden = synth.normal((16, cfg.hidden), 6, 700)
+        dkv, okv = fresh_kv(ctx, N_PAST, cfg, PAGES)
+        oidx, olog, _, st = oracle.forward(ocfg, ow, okv.copy(), hidden, logits=True)
+        assert st == 0
+        _, gap = oracle.argmax(olog)
+        require_clear_rows(gap, "window + rope rows")
+        draft = synth.plant_draft(oidx, 9, cfg.vocab, 6, 701)
+        ores, oidx2, olog2, _ = oracle.verify_step(ocfg, ow, okv, hidden, draft)
+        res, _, am, lg = step(ctx, dw, dkv, hidden, draft, cfg)
+        assert_close(lg, olog2, what="logits (window + rope)")
+        assert np.array_equal(am, oidx2)
+        assert list(res) == list(ores)
+        ring_vs_oracle(dkv, okv, int(res[3]), N_PAST, "ring (window + rope)")
+    finally:
+        ctx.close()

@@ -795,11 +795,17 @@ cudaError_t launch_attention(const AttnPlan& a, const KvView& kv, int layer, con
   auto kern = inst == 0 ? attn_partial_kernel<false, 64>
                         : inst == 1 ? attn_partial_kernel<false, 128>
                                     : inst == 2 ? attn_partial_kernel<true, 64> : attn_partial_kernel<true, 128>;
-  static size_t smem_attr[4] = {0, 0, 0, 0};
-  if (smem_attr[inst] < smem) {
+  // the shared-memory limit is a per-device attribute of each instance
+  constexpr int kMaxDevices = 64;
+  static size_t smem_attr[kMaxDevices][4] = {};
+  int dev = 0;
+  cudaError_t ed = cudaGetDevice(&dev);
+  if (ed != cudaSuccess) return ed;
+  size_t* have = (dev >= 0 && dev < kMaxDevices) ? &smem_attr[dev][inst] : nullptr;
+  if (!have || *have < smem) {
     cudaError_t ea = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (ea != cudaSuccess) return ea;
-    smem_attr[inst] = smem;
+    if (have) *have = smem;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.max_chunks, a.nkv, a.tiles);

@@ -99,7 +99,7 @@ extern "C" {
 #define SPEC_ST_NONFINITE     0x2  /* NaN/Inf in an activation or a logit       */
 #define SPEC_ST_POOL_EMPTY    0x4  /* not enough free KV pages for the block     */
 #define SPEC_ST_ROLLBACK      0x8  /* rollback length < 0 or > seq_len           */
-#define SPEC_ST_CTX_FULL      0x10 /* seq_len + rows exceeds the page table      */
+#define SPEC_ST_CTX_FULL      0x10 /* seq_len + rows exceeds the page table or max_ctx */
 #define SPEC_ST_DEVICE_WAIT   0x20 /* a bounded device wait (tensor core, bulk copy) gave up */
 #define SPEC_ST_BAD_TREE      0x40 /* a token tree's parent list is not a tree in topological order */
 

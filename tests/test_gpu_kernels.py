@@ -422,6 +422,25 @@ def test_kv_metadata_sequences_match_oracle(ctx):
         assert np.array_equal(s[3], m.stack)
 
 
+def test_positions_past_max_ctx_are_refused():
+    """A context sized for max_ctx positions refuses a reservation past it
+    (SPEC_ST_CTX_FULL) even when the page table has room, and commits
+    nothing; one that ends exactly at max_ctx is served."""
+    c = runtime.Context(SMALL, max_ctx=64)
+    try:
+        kv = make_kv(SMALL, num_pages=24, max_seq_pages=24)
+        kv.reset(c)
+        kv.extend(c, 60)
+        assert abi.spec_last_status(c.h) == 0 and kv.state()[0] == 60
+        kv.extend(c, 5)
+        assert abi.spec_last_status(c.h) & abi.ST_CTX_FULL
+        assert kv.state()[0] == 60
+        kv.extend(c, 4)
+        assert kv.state()[0] == 64
+    finally:
+        c.close()
+
+
 def test_accept_token_range_restores_kv(ctx):
     kv = make_kv(FULL, num_pages=140, max_seq_pages=140)
     kv.reset(ctx)

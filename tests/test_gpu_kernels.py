@@ -509,11 +509,13 @@ def long_ctx():
     c.close()
 
 
-def test_attention_parity_long_context(long_ctx):
+@pytest.mark.parametrize("M", [16, 4])
+def test_attention_parity_long_context(long_ctx, M):
     # long-context verify (16k keys, the block straddling a page boundary):
-    # 257 64-key chunks per row, merged in chunk order
+    # the long plan's 128-key sub-chunks, chunks merged in chunk order; with
+    # M = 4 rows 4..15 of every tile are dead rows
     cfg = SMALL
-    n_past, M = 16384 + 7, 16
+    n_past = 16384 + 7
     pages = (n_past + M + 15) // 16 + 1
     kv = make_kv(cfg, num_pages=pages, max_seq_pages=pages)
     kv.reset(long_ctx)
@@ -529,6 +531,34 @@ def test_attention_parity_long_context(long_ctx):
     sync()
     ref = okv.attention(1, q, n_past)
     assert_close(out.cpu().numpy(), ref, what="attention at 16k context")
+
+
+def test_attention_batch_height_invariance_long_plan(long_ctx):
+    """Under the long plan (128-key sub-chunks) as under the short one: row i
+    of a 16-row block equals the same row computed alone, bit for bit."""
+    cfg = SMALL
+    n_past, M = 1000, 16
+    pages = 66
+    kv = make_kv(cfg, num_pages=pages, max_seq_pages=pages)
+    kv.reset(long_ctx)
+    kv.extend(long_ctx, n_past + M)
+    okv = oracle.KV(_ocfg(cfg), pages, pages)
+    okv.extend(n_past + M)
+    fill_kv_both(long_ctx, cfg, kv, okv, 0, n_past + M, 19)
+    q = synth.normal((M, cfg.n_q_heads, 128), 43, 1) * 4.0
+    out16 = torch.zeros((M, cfg.hidden), dtype=torch.float32, device="cuda")
+    abi.check("spec_attention", abi.spec_attention(long_ctx.h, kv.struct(), 0, dev(q).data_ptr(), M,
+                                                   out16.data_ptr()))
+    sync()
+    o16 = out16.cpu().numpy()
+    for i in (0, 5, 15):
+        kv.rollback(long_ctx, n_past + i + 1)
+        out1 = torch.zeros((1, cfg.hidden), dtype=torch.float32, device="cuda")
+        abi.check("spec_attention", abi.spec_attention(long_ctx.h, kv.struct(), 0, dev(q[i:i + 1]).data_ptr(), 1,
+                                                       out1.data_ptr()))
+        sync()
+        assert np.array_equal(out1.cpu().numpy().view(np.uint32), o16[i:i + 1].view(np.uint32)), i
+        kv.extend(long_ctx, M - i - 1)
 
 
 def test_attention_batch_height_invariance(small_ctx):

@@ -158,6 +158,20 @@ def gemm_q4k(W: np.ndarray, N: int, K: int, q, d_a, A, sums: bool = False):
     return (y, isc, imn, vb) if sums else y
 
 
+def split_ranges(N: int, K: int, processors: int) -> int:
+    """G of the fixed summation order for a GPU of `processors` SMs."""
+    return int(lib().orc_split_ranges(N, K, processors))
+
+
+def sum_split(vb: np.ndarray, G: int) -> np.ndarray:
+    """y[m][n] = sum over superblocks of vb[m][n][b] in the fixed order of G ranges."""
+    vb = np.ascontiguousarray(vb, dtype=np.float32)
+    M, N, nb = vb.shape
+    y = np.empty((M, N), dtype=np.float32)
+    lib().orc_sum_split(_p(vb), M, N, nb, int(G), _p(y))
+    return y
+
+
 def linear(W: np.ndarray, N: int, K: int, x: np.ndarray) -> np.ndarray:
     q, d_a, A, _ = quantize_q8(x)
     return gemm_q4k(W, N, K, q, d_a, A)

@@ -189,6 +189,69 @@ void orc_gemm_q4k(const uint8_t* W, int N, int K, const int8_t* q, const float* 
     free(acc);
 }
 
+/* ------------------------------------------------------------------------ */
+/* The fixed fp32 order of the sum over superblocks (reading c6 of the       */
+/* integer-dot contract, "a canonical order both sides implement"):          */
+/*   units u = (group g of 128 output columns, superblock b), numbered       */
+/*   g-major, U = ceil(N/128) * nb of them, are cut into G contiguous ranges */
+/*   [floor(iU/G), floor((i+1)U/G)), i = 0..G-1;                             */
+/*   inside a range, one group's values v_b are added in b order to a         */
+/*   partial that starts at +0.0f;                                            */
+/*   a group's partials are then added in range order, the first partial     */
+/*   being the start value.                                                  */
+/* G comes from the number of processors P: the largest G <= min(P, U,        */
+/* floor(6U/nb)), at least 1, for which no group meets more than 8 ranges.    */
+/* With G = 1 the result is the plain left-to-right fp32 sum over b.         */
+/* ------------------------------------------------------------------------ */
+static int orc_range_of_unit(long long x, long long U, int G) {
+    return (int)(((x + 1) * (long long)G - 1) / U);   /* largest i: floor(iU/G) <= x */
+}
+
+int orc_split_ranges(int N, int K, int processors) {
+    int nb = K / 256, ngroups = (N + 127) / 128;
+    long long U = (long long)ngroups * nb;
+    long long G = processors;
+    if (G > U) G = U;
+    if (nb > 0 && G > (6 * U) / nb) G = (6 * U) / nb;
+    if (G < 1) G = 1;
+    for (;;) {
+        int worst = 1;
+        for (int g = 0; g < ngroups; ++g) {
+            long long first = (long long)g * nb, last = first + nb - 1;
+            int n = orc_range_of_unit(last, U, (int)G) - orc_range_of_unit(first, U, (int)G) + 1;
+            if (n > worst) worst = n;
+        }
+        if (worst <= 8 || G == 1) break;
+        --G;
+    }
+    return (int)G;
+}
+
+void orc_sum_split(const float* vb, int M, int N, int nb, int G, float* y) {
+    int ngroups = (N + 127) / 128;
+    long long U = (long long)ngroups * nb;
+    for (int m = 0; m < M; ++m)
+        for (int n = 0; n < N; ++n) {
+            int g = n / 128;
+            const float* v = vb + ((size_t)m * N + n) * nb;
+            float total = 0.0f;
+            int have = 0;
+            /* the ranges that meet group g, in order */
+            int r0 = orc_range_of_unit((long long)g * nb, U, G);
+            int r1 = orc_range_of_unit((long long)g * nb + nb - 1, U, G);
+            for (int r = r0; r <= r1; ++r) {
+                long long lo = (long long)r * U / G, hi = (long long)(r + 1) * U / G;
+                long long b0 = lo > (long long)g * nb ? lo - (long long)g * nb : 0;
+                long long b1 = hi < (long long)(g + 1) * nb ? hi - (long long)g * nb : nb;
+                float part = 0.0f;
+                for (long long b = b0; b < b1; ++b) part = part + v[b];
+                total = have ? total + part : part;
+                have = 1;
+            }
+            y[(size_t)m * N + n] = total;
+        }
+}
+
 int orc_linear(const uint8_t* W, int N, int K, const float* x, int M, float* y) {
     int8_t* q = (int8_t*)malloc((size_t)M * K);
     float* d_a = (float*)malloc(sizeof(float) * (size_t)M * (K / 256));

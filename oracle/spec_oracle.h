@@ -86,6 +86,9 @@ void orc_gemm_q4k(const uint8_t* W, int N, int K, const int8_t* q, const float* 
                   const int32_t* A, int M, float* y, int32_t* isc, int32_t* imn, float* vb);
 /* quantise + GEMM; returns the quantiser status */
 int orc_linear(const uint8_t* W, int N, int K, const float* x, int M, float* y);
+/* the fixed fp32 summation order over superblocks (see spec_oracle.c) */
+int  orc_split_ranges(int N, int K, int processors);
+void orc_sum_split(const float* vb, int M, int N, int nb, int G, float* y);
 /* dense fp64 reference: y = dequant(W) x, x given in fp64 */
 void orc_dense_f64(const uint8_t* W, int N, int K, const double* x, int M, double* y);
 

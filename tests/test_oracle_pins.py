@@ -451,6 +451,58 @@ def test_swa_window_one_returns_own_value_and_two_is_a_pair_softmax():
 
 
 # ---------------------------------------------------------------------------
+# the fixed summation order over superblocks (reading c6 of the contract)
+# ---------------------------------------------------------------------------
+def _seq_f32(v):
+    acc = np.float32(0.0)
+    for t in v:
+        acc = np.float32(acc + np.float32(t))
+    return acc
+
+
+def test_split_sum_one_range_is_the_left_to_right_sum():
+    rng = np.random.default_rng(3)
+    vb = (rng.standard_normal((2, 256, 7)) * 10.0 ** rng.integers(-3, 6, (2, 256, 7))).astype(np.float32)
+    for G in (1, 2 * 7):          # one range, or one unit per range: both are left to right
+        y = oracle.sum_split(vb, G)
+        ref = np.array([[_seq_f32(vb[m, n]) for n in range(256)] for m in range(2)], dtype=np.float32)
+        assert np.array_equal(y.view(np.uint32), ref.view(np.uint32)), G
+
+
+def test_split_sum_groups_partials_by_range():
+    # one group of 128 columns, 4 superblocks, 2 ranges: (v0 + v1) + (v2 + v3);
+    # 1e8 + 1 loses the 1 in fp32, so the grouping decides the result
+    vb = np.zeros((1, 128, 4), dtype=np.float32)
+    vb[0, 0] = [1e8, 1.0, -1e8, 1.0]
+    y = oracle.sum_split(vb, 2)
+    assert y[0, 0] == np.float32(0.0)                    # (1e8 + 1) + (-1e8 + 1) = 1e8 - 1e8
+    assert _seq_f32(vb[0, 0]) == np.float32(1.0)         # left to right keeps the last 1
+    # two groups, 3 superblocks each, U = 6, G = 4: ranges [0,1) [1,3) [3,4) [4,6)
+    vb = np.zeros((1, 256, 3), dtype=np.float32)
+    vb[0, 0] = [1.0, 1e8, -1e8]          # group 0: v0 + (v1 + v2) = 1 + 0 = 1
+    vb[0, 128] = [1e8, -1e8, 1.0]        # group 1: v0 + (v1 + v2) = 1e8 + (-1e8) = 0
+    y = oracle.sum_split(vb, 4)
+    assert y[0, 0] == np.float32(1.0) and y[0, 128] == np.float32(0.0)
+    assert _seq_f32(vb[0, 0]) == np.float32(0.0) and _seq_f32(vb[0, 128]) == np.float32(1.0)
+
+
+def test_split_ranges_rule():
+    # G = min(processors, units), capped at 6U/nb, and no group meets more than 8 ranges
+    assert oracle.split_ranges(6656, 6656, 152) == 152
+    assert oracle.split_ranges(512, 512, 152) == 8                 # U = 4 groups x 2 superblocks
+    assert oracle.split_ranges(128, 25600, 152) == 6               # one group of 100: cap 6U/nb
+    for N, K in ((7680, 6656), (35840, 6656), (6656, 17920), (131072, 6656), (6656, 33280), (4112, 512)):
+        G = oracle.split_ranges(N, K, 152)
+        nb, ng = K // 256, (N + 127) // 128
+        U = ng * nb
+        assert 1 <= G <= min(152, U)
+        starts = [i * U // G for i in range(G + 1)]
+        for g in range(ng):
+            meet = sum(1 for i in range(G) if starts[i] < (g + 1) * nb and starts[i + 1] > g * nb)
+            assert meet <= 8, (N, K, g, meet)
+
+
+# ---------------------------------------------------------------------------
 # QK-norm and RoPE ([8] §8.2 lists both for the draft's attention)
 # ---------------------------------------------------------------------------
 def _rope_cfg(theta):

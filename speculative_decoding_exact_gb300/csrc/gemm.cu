@@ -21,9 +21,13 @@
 //     (exact), so d*ISc rounds exactly as in the plain formula;
 //   * the min term IMn = sum_j m_j A_j is one more MMA per superblock
 //     (kind::f16) with the activation sums split as A_j = 64*hi_j + lo_j.
-// The per-superblock combination d_a*(d*ISc - dmin*IMn) uses packed f32x2
-// operations, each rounded on its own (no contraction), and the superblock
-// values accumulate in f32 in superblock order.
+// The per-superblock combination d_a*(d*ISc - dmin*IMn) rounds each
+// operation on its own, and the superblock values accumulate in f32 in
+// superblock order.  Packed f32x2 multiplies feeding an add or sub get fused
+// into one fma by the compiler (d*ISc - dmin*IMn then rounds once), so every
+// product is an fma whose addend is -0, passed in as a kernel argument the
+// compiler cannot fold: RN(a*b + -0) = RN(a*b) for all a, b (a zero product
+// keeps its sign), and an fma is never fused into its consumer.
 //
 // Work split: one CTA per SM owns 128 weight columns at a time.  Four
 // unpack warps (one thread per column) turn a column's 144-byte superblock
@@ -195,7 +199,7 @@ __global__ void __maxnreg__(kGemmMaxRegs)
 gemm_q4k_kernel(const uint8_t* __restrict__ wt, const uint8_t* __restrict__ act,
                 float* __restrict__ pieces, int N, int nb, int U, int G,
                 int32_t* __restrict__ isc_out, int32_t* __restrict__ imn_out, int m_sums,
-                int pre_stages, int withhold, int32_t* status) {
+                int pre_stages, int withhold, int32_t* status, float neg_zero) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ uint32_t tmem_slot;
   __shared__ __align__(8) uint64_t full[kGemmStages], empty[kGemmStages];
@@ -429,7 +433,7 @@ gemm_q4k_kernel(const uint8_t* __restrict__ wt, const uint8_t* __restrict__ act,
       // d * 2^9 (exact): the D values are 2^-9 * integer sums
       const float d = __half2float(__ushort_as_half((unsigned short)(hdr.x & 0xffff))) * 512.f;
       const float dm = __half2float(__ushort_as_half((unsigned short)(hdr.x >> 16)));
-      const unsigned long long D2 = f2pack(d, d), M2 = f2pack(dm, dm);
+      const unsigned long long D2 = f2pack(d, d), M2 = f2pack(dm, dm), NZ = f2pack(neg_zero, neg_zero);
 #pragma unroll
       for (int rb = 0; rb < 2; ++rb) {             // rows 8rb .. 8rb+7
         if (rb == 1) {
@@ -453,12 +457,11 @@ gemm_q4k_kernel(const uint8_t* __restrict__ wt, const uint8_t* __restrict__ act,
             else hi = j == 4 ? f2mul(sc2, sj) : f2fma(sc2, sj, hi);
           }
           const int r = 8 * rb + n;
-          const unsigned long long isc = f2add(lo, hi);
+          const unsigned long long isc = f2add(lo, hi);   // exact: ISc * 2^-9
           const unsigned long long imn = f2pack(__uint_as_float(rm[n]), __uint_as_float(rm[n + 1]));
-          const unsigned long long v =
-              f2mul(f2pack(da[r], da[r + 1]), f2sub(f2mul(D2, isc), f2mul(M2, imn)));
-          const unsigned long long yy = f2add(f2pack(y[r], y[r + 1]), v);
-          f2unpack(yy, y[r], y[r + 1]);
+          const unsigned long long t = f2sub(f2fma(D2, isc, NZ), f2fma(M2, imn, NZ));
+          const unsigned long long v = f2fma(f2pack(da[r], da[r + 1]), t, NZ);
+          f2unpack(f2add(f2pack(y[r], y[r + 1]), v), y[r], y[r + 1]);
           if (SUMS && valid) {
             float l0, l1, h0, h1;
             f2unpack(lo, l0, l1);
@@ -527,7 +530,7 @@ cudaError_t launch_gemm(const GemmPlan& p, const void* w_tiled, const uint8_t* a
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kern, static_cast<const uint8_t*>(w_tiled), act, pieces, p.N, p.nb,
-                            (int)p.U, p.G, isc, imn, m_sums, p.pre_stages, (int)withhold, status);
+                            (int)p.U, p.G, isc, imn, m_sums, p.pre_stages, (int)withhold, status, -0.0f);
 }
 
 // y[m][n] = sum over the group's slots, in slot order

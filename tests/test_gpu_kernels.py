@@ -139,6 +139,26 @@ def test_gemm_integer_sums_bit_exact(ctx, M, N, K):
     assert_close(y, oy, what="y")
 
 
+@pytest.mark.parametrize("M,N,K", [(16, 6656, 6656), (16, 7680, 6656), (4, 2048, 512), (16, 272, 768),
+                                   (1, 4096, 17920), (16, 35840, 6656)])
+def test_gemm_output_bit_exact_in_the_fixed_order(ctx, M, N, K):
+    """y itself, not only the integer sums, is bit for bit the oracle's: the
+    per-superblock values agree exactly, and the oracle adds them in the
+    order of the GEMM's work split for this GPU's SM count (G ranges of
+    (group, superblock) units; partials in range order)."""
+    W = synth.q4k_matrix(N, K, 5, N + K)
+    x = synth.normal((M, K), 5, 3 * M + K)
+    Wt = runtime.upload_tiled(ctx, W, N, K)
+    y = run_gemm(ctx, Wt, N, K, x)
+    q, da, A, _ = oracle.quantize_q8(x)
+    _, _, _, vb = oracle.gemm_q4k(W, N, K, q, da, A, sums=True)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    G = oracle.split_ranges(N, K, sms)
+    oy = oracle.sum_split(vb, G)
+    assert np.array_equal(y.view(np.uint32), oy.view(np.uint32)), \
+        f"{int(np.sum(y.view(np.uint32) != oy.view(np.uint32)))} of {y.size} outputs differ (G {G})"
+
+
 def _extreme_superblocks(rng, n):
     """n canonical superblocks drawn from three extreme patterns: every code 15
     with sc = m = 63 (the largest sums), codes alternating 0/15 with sc

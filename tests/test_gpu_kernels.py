@@ -140,7 +140,8 @@ def test_gemm_integer_sums_bit_exact(ctx, M, N, K):
 
 
 @pytest.mark.parametrize("M,N,K", [(16, 6656, 6656), (16, 7680, 6656), (4, 2048, 512), (16, 272, 768),
-                                   (1, 4096, 17920), (16, 35840, 6656)])
+                                   (7, 400, 256), (1, 4096, 17920), (16, 35840, 6656),
+                                   (16, 131072, 6656)])
 def test_gemm_output_bit_exact_in_the_fixed_order(ctx, M, N, K):
     """y itself, not only the integer sums, is bit for bit the oracle's: the
     per-superblock values agree exactly, and the oracle adds them in the

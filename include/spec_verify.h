@@ -64,8 +64,14 @@
  *   ISc = sum_j sc_j * S_j,  IMn = sum_j m_j * A_j            (exact, int32)
  * Per-superblock value, fp32, each operation rounded to nearest, no fusion:
  *   v_b = d_a * ((float)d * (float)ISc - (float)dmin * (float)IMn)
- * Output y[m][n] = sum_b v_b (fp32 accumulation; the summation order is the
- * kernel's own fixed order and depends on K and N only, never on M).
+ * Output y[m][n] = sum_b v_b in fp32, in a fixed order that depends on N, K
+ * and the SM count P only, never on M: the U = ceil(N/128) * (K/256) units
+ * (128-column group, superblock), numbered group-major, are cut into G
+ * contiguous ranges [floor(i*U/G), floor((i+1)*U/G)), where G is the largest
+ * value <= min(P, U, 6*U/(K/256)) (at least 1) for which no group meets more
+ * than 8 ranges.  Within a range the v_b of a column are added from +0 in
+ * superblock order; the partials of the ranges that meet the column's group
+ * are added in range order, starting from the first.
  */
 #ifndef SPEC_VERIFY_H
 #define SPEC_VERIFY_H

@@ -345,6 +345,13 @@ SPEC_API int spec_quantize_q8(spec_ctx* ctx, const float* x, int M, int K,
 SPEC_API int spec_gemm_q4k(spec_ctx* ctx, const void* w_tiled, int N, int K,
                   const float* x, int M, float* y);
 
+/* The number G of contiguous unit ranges in the GEMM's fixed summation order
+ * (stated at the top of this file) for an N x K matrix on a GPU of num_sms
+ * SMs: the value every GEMM entry point here uses on such a GPU.  Host only:
+ * touches no device and needs no ctx.  Returns G >= 1, or SPEC_EINVAL unless
+ * N > 0, N % 16 == 0, K > 0, K % 256 == 0 and num_sms > 0. */
+SPEC_API int spec_gemm_ranges(int N, int K, int num_sms);
+
 /* Same GEMM, also writing the exact integer sums ISc and IMn (DEVICE int32
  * [M][N][K/256] each) of every (row, column, superblock). */
 SPEC_API int spec_gemm_q4k_sums(spec_ctx* ctx, const void* w_tiled, int N, int K,

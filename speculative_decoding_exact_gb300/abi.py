@@ -70,6 +70,7 @@ _SIGS = {
     "spec_weights_repack": (I, [P, P, P, I, I]),
     "spec_quantize_q8": (I, [P, P, I, I, P, P, P]),
     "spec_gemm_q4k": (I, [P, P, I, I, P, I, P]),
+    "spec_gemm_ranges": (I, [I, I, I]),
     "spec_gemm_q4k_sums": (I, [P, P, I, I, P, I, P, P, P]),
     "spec_gemm_q4k_cudacore": (I, [P, P, I, I, P, I, P]),
     "spec_gemm_wait_selftest": (I, [P, P, I, I]),
@@ -194,6 +195,10 @@ def spec_quantize_q8(ctx, x, M, K, q, d_a, A) -> int:
 
 def spec_gemm_q4k(ctx, w, N, K, x, M, y) -> int:
     return _call("spec_gemm_q4k", ctx, P(w), N, K, P(x), M, P(y))
+
+
+def spec_gemm_ranges(N: int, K: int, num_sms: int) -> int:
+    return _call("spec_gemm_ranges", N, K, num_sms)
 
 
 def spec_gemm_q4k_sums(ctx, w, N, K, x, M, y, isc, imn) -> int:

@@ -858,6 +858,11 @@ int spec_set_split(spec_ctx* c, int layer, void* cuda_event) {
   return SPEC_OK;
 }
 
+int spec_gemm_ranges(int N, int K, int num_sms) {
+  if (N <= 0 || N % 16 != 0 || K <= 0 || K % 256 != 0 || num_sms <= 0) return SPEC_EINVAL;
+  return make_gemm_plan(N, K, num_sms).G;
+}
+
 // MT19937 seeding (Matsumoto & Nishimura 1998): word 0 = seed, word i =
 // 1812433253 * (w[i-1] ^ (w[i-1] >> 30)) + i; word 624 = 624 (regenerate first)
 int spec_mt_seed(uint32_t* state_host, uint32_t seed) {

@@ -51,3 +51,22 @@ def test_null_arguments_are_rejected():
     assert L.spec_kv_rollback(None, None, 0) == abi.SPEC_ENULL
     assert L.spec_gemm_q4k(None, None, 16, 256, None, 1, None) == abi.SPEC_ENULL
     L.spec_verify_destroy(None)
+
+
+@pytest.mark.parametrize("sms", [1, 2, 3, 7, 64, 132, 148, 152, 160, 1000])
+def test_gemm_summation_ranges_match_the_oracle(sms):
+    """The GEMM's fixed fp32 order is fixed by its number of unit ranges G:
+    the library's plan (host code, no device) takes the value the oracle's
+    restatement of the rule gives, for the model's matrices and ragged or
+    single-superblock shapes, on GPUs of any SM count."""
+    import oracle
+    shapes = [(7680, 6656), (6656, 6656), (35840, 6656), (6656, 17920), (131072, 6656),
+              (6656, 33280), (16, 256), (272, 768), (400, 256), (2048, 512), (4096, 17920),
+              (1040, 2560), (12800, 25600)]
+    for N, K in shapes:
+        assert abi.spec_gemm_ranges(N, K, sms) == oracle.split_ranges(N, K, sms), (N, K, sms)
+
+
+def test_gemm_ranges_rejects_bad_shapes():
+    for N, K, sms in [(0, 256, 152), (8, 256, 152), (16, 0, 152), (16, 200, 152), (16, 256, 0)]:
+        assert abi.spec_gemm_ranges(N, K, sms) == abi.SPEC_EINVAL

@@ -20,6 +20,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -400,6 +401,11 @@ def run_gpu(args, rank, world):
     ms_per_step = ms / args.steps
     steps_per_s = job_steps_per_s(ms, args.steps, world)
 
+    # per-step distribution: a separate pass of the same steps with an event
+    # after each one (kept out of the timed region above, whose consecutive
+    # steps overlap through programmatic dependent launch)
+    step_ms = step_time_stats(torch, stream, step, args.steps)
+
     # GEMM kernel timing: CUDA events around every GEMM launch of the same steps
     gemm_ms, gemm_launches = profile_gemms(ctx, abi, torch, stream, ws, ks, hidden, draft, res,
                                            args.steps)
@@ -454,11 +460,28 @@ def run_gpu(args, rank, world):
                 "d2h_bytes_per_step": 16},
         "gpu_launches": launches * args.steps,
         "clocks": clk,
+        "step_ms": step_ms,
         "setup_s": setup_s,
         "accepted_len_last": int(r[0]),
     }
     print(json.dumps(line), flush=True)
     ctx.close()
+
+
+def step_time_stats(torch, stream, step, steps):
+    """Median and 95th percentile of single-step times: `steps` more steps,
+    a CUDA event on the step's stream after each one."""
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    torch.cuda.synchronize()
+    ev[0].record(stream)
+    for i in range(steps):
+        step()
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize()
+    t = sorted(ev[i].elapsed_time(ev[i + 1]) for i in range(steps))
+    p95 = t[min(len(t) - 1, int(math.ceil(0.95 * len(t))) - 1)]
+    return {"median": statistics.median(t), "p95": p95, "min": t[0], "max": t[-1], "steps": steps,
+            "pass": "separate, an event after every step"}
 
 
 def profile_gemms(ctx, abi, torch, stream, ws, ks, hidden, draft, res, steps):

@@ -226,6 +226,26 @@ class OracleSample:
                 f"LM-head columns; extrapolated x52 layers, x{self.COLF} columns, x{self.HEADF} head")
 
 
+def host_cpu():
+    """The host the oracle runs on: architecture, logical CPUs, and the CPU
+    model from /proc/cpuinfo (x86: "model name"; Arm: implementer and part
+    codes, e.g. 0x41 / 0xd4f for a Neoverse V2)."""
+    import platform
+    info = {"machine": platform.machine(), "nproc": os.cpu_count()}
+    try:
+        fields = {}
+        for line in open("/proc/cpuinfo"):
+            k, _, v = line.partition(":")
+            fields.setdefault(k.strip(), v.strip())
+        if "model name" in fields:
+            info["model"] = fields["model name"]
+        elif "CPU part" in fields:
+            info["model"] = f"implementer {fields.get('CPU implementer', '?')} part {fields['CPU part']}"
+    except OSError:
+        pass
+    return info
+
+
 def cpu_baseline(cfg, min_seconds=10.0):
     s = OracleSample(cfg)
     times, spent = [], 0.0
@@ -234,7 +254,7 @@ def cpu_baseline(cfg, min_seconds=10.0):
         times.append(step_s)
         spent += wall
     return {"value": 1.0 / statistics.median(times), "unit": "verify steps/s", "cores": 1,
-            "kind": "oracle", "sample": s.describe() + f"; {len(times)} samples"}
+            "kind": "oracle", "sample": s.describe() + f"; {len(times)} samples", "host": host_cpu()}
 
 
 def run_reference(args, rank, world):
@@ -256,7 +276,7 @@ def run_reference(args, rank, world):
             "vs_baseline": None, "dtype": "int8xint4 dot, f32 combine", "data": "synthetic",
             "config": workload_config(cfg),
             "cpu_baseline": {"value": v, "unit": "verify steps/s", "cores": 1, "kind": "oracle",
-                             "sample": s.describe()},
+                             "sample": s.describe(), "host": host_cpu()},
             "e2e": {"value": v, "unit": "verify steps/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0},
             "sample_wall_s": wall}
